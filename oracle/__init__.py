@@ -1,0 +1,165 @@
+"""fp64 CPU oracle for the pluggable-map attention forward.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product path
+(``softmax_free_attention_gb300``) never imports it, and this package imports
+nothing from the product path.
+
+The arithmetic lives in ``cattn_oracle.c`` (plain C, double precision, one
+query row at a time); this module only compiles it with ``gcc`` when needed
+and marshals numpy arrays through ``ctypes``.  The definitions it follows are
+cited in the C file's header:
+
+* softmax and Yat branches -- "Softmax-Free Attention in JAX/Flax NNX",
+  section "One module, two compatibility functions";
+* the Yat kernel and its row mass -- "The Kernel Between the Roles";
+* shapes, key-axis softmax, masks -- "NNX Scaled Dot-Product Attention";
+* s^tau -- "s^tau: a focal-length knob for attention" (forum.trae.cn), core
+  formula a_i = phi(s_i)^tau / sum_j phi(s_j)^tau, phi = softplus(s) + eps.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+SOFTMAX, YAT, STAU = 0, 1, 2
+VARIANTS = {"softmax": SOFTMAX, "yat": YAT, "stau": STAU}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "cattn_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libcattn_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class _Problem(ctypes.Structure):
+    _fields_ = [
+        ("variant", ctypes.c_int),
+        ("B", ctypes.c_int), ("h", ctypes.c_int), ("hkv", ctypes.c_int),
+        ("Tq", ctypes.c_int), ("Tk", ctypes.c_int), ("dk", ctypes.c_int), ("dv", ctypes.c_int),
+        ("causal", ctypes.c_int),
+        ("scale", ctypes.c_double),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+        ("b", ctypes.c_void_p), ("eps", ctypes.c_void_p), ("tau", ctypes.c_void_p),
+        ("rows", ctypes.c_void_p), ("nrows", ctypes.c_int64),
+        ("out", ctypes.c_void_p), ("row_mass", ctypes.c_void_p), ("row_max", ctypes.c_void_p),
+        ("weights", ctypes.c_void_p),
+    ]
+
+
+def build(force: bool = False) -> str:
+    """Compile cattn_oracle.c into libcattn_oracle.so next to it (gcc, -O2)."""
+    with _lock:
+        stale = (not os.path.exists(_LIB_PATH)
+                 or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+        if force or stale:
+            tmp = _LIB_PATH + f".tmp{os.getpid()}"
+            cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-pthread",
+                   "-o", tmp, _SRC, "-lm"]
+            subprocess.run(cmd, check=True)
+            os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        lib.oracle_forward.argtypes = [ctypes.POINTER(_Problem), ctypes.c_int]
+        lib.oracle_forward.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _as_f64(x, name):
+    if x is None:
+        return None
+    if hasattr(x, "detach"):  # torch tensor: widen exactly on the host
+        import torch
+        x = x.detach().to(device="cpu", dtype=torch.float64).numpy()
+    arr = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    return arr
+
+
+def _per_head(x, h, name):
+    if x is None:
+        return None
+    arr = _as_f64(x, name).reshape(-1)
+    if arr.size == 1:
+        arr = np.full(h, arr[0], dtype=np.float64)
+    if arr.size != h:
+        raise ValueError(f"{name} must have one value per query head ({h}), got {arr.size}")
+    return arr
+
+
+def forward(variant, q, k, v, *, b=None, eps=None, tau=None, causal=False, scale=None,
+            rows=None, nthreads=None, return_weights=False):
+    """Attention forward in fp64.
+
+    q: [B, h, Tq, dk]; k: [B, hkv, Tk, dk]; v: [B, hkv, Tk, dv] (numpy arrays or
+    torch tensors of any float dtype; widened exactly to fp64).  b / eps / tau:
+    one value per query head (or a scalar).  ``scale`` multiplies q.k for
+    softmax and s^tau (default 1/sqrt(dk)); Yat uses the raw q.k.
+
+    rows: optional flat indices into [B, h, Tq]; only those rows are computed
+    and the outputs are returned in that order with a leading ``len(rows)``
+    axis.  Without ``rows`` the outputs have the full [B, h, Tq(, dv)] shape.
+
+    Returns (out, row_mass, row_max) and, with ``return_weights``, the weight
+    matrix [.., Tk] as a fourth element.
+    """
+    variant = VARIANTS.get(variant, variant)
+    q = _as_f64(q, "q")
+    k = _as_f64(k, "k")
+    v = _as_f64(v, "v")
+    if q.ndim != 4 or k.ndim != 4 or v.ndim != 4:
+        raise ValueError("q, k, v must be 4-D [B, heads, T, d]")
+    B, h, Tq, dk = q.shape
+    Bk, hkv, Tk, dk2 = k.shape
+    Bv, hkv2, Tk2, dv = v.shape
+    if (Bk, dk2) != (B, dk) or (Bv, hkv2, Tk2) != (B, hkv, Tk):
+        raise ValueError("inconsistent q/k/v shapes")
+    if scale is None:
+        scale = 1.0 / np.sqrt(dk)
+    b = _per_head(b, h, "b")
+    eps = _per_head(eps, h, "eps")
+    tau = _per_head(tau, h, "tau")
+
+    if rows is None:
+        rows_arr = None
+        nrows = B * h * Tq
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+        nrows = rows_arr.size
+    out = np.zeros((nrows, dv), dtype=np.float64)
+    row_mass = np.zeros(nrows, dtype=np.float64)
+    row_max = np.zeros(nrows, dtype=np.float64)
+    weights = np.zeros((nrows, Tk), dtype=np.float64) if return_weights else None
+
+    def ptr(a):
+        return None if a is None else a.ctypes.data
+
+    prob = _Problem(variant, B, h, hkv, Tq, Tk, dk, dv, int(bool(causal)), float(scale),
+                    ptr(q), ptr(k), ptr(v), ptr(b), ptr(eps), ptr(tau),
+                    ptr(rows_arr), nrows, ptr(out), ptr(row_mass), ptr(row_max), ptr(weights))
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    rc = _load().oracle_forward(ctypes.byref(prob), int(nthreads))
+    if rc == -2:
+        raise FloatingPointError("oracle: phi^tau is not finite in fp64 for this input")
+    if rc != 0:
+        raise ValueError(f"oracle_forward failed with code {rc}")
+    if rows_arr is None:
+        out = out.reshape(B, h, Tq, dv)
+        row_mass = row_mass.reshape(B, h, Tq)
+        row_max = row_max.reshape(B, h, Tq)
+        if weights is not None:
+            weights = weights.reshape(B, h, Tq, Tk)
+    if return_weights:
+        return out, row_mass, row_max, weights
+    return out, row_mass, row_max
