@@ -1,0 +1,151 @@
+/*
+ * cattn.h -- C ABI of the pluggable-map attention forward for GB300 (sm_103a).
+ *
+ * One call computes, for every batch b, query head i and query row t,
+ *
+ *     out[b,i,t,:] = sum_j w_tj * v[b,g,j,:],    g = i / (h / hkv)
+ *
+ * where the weights w_tj come from one of three score-to-weight maps:
+ *
+ *   CATTN_SOFTMAX  scaled dot-product softmax: s_j = scale * q.k_j, masked
+ *                  keys excluded, w = exp(s - max) / sum exp(s - max).
+ *                  ("Softmax-Free Attention in JAX/Flax NNX", section "One
+ *                  module, two compatibility functions", softmax branch;
+ *                  "NNX Scaled Dot-Product Attention", "Shapes and the three
+ *                  steps").
+ *   CATTN_YAT      the Yat compatibility kernel
+ *                  kappa_j = (q.k_j + b_i)^2 / (max(|q - k_j|^2, 0) + eps_i)
+ *                  on the raw (unscaled) dot product, masked keys get
+ *                  kappa = 0, w = kappa / (sum kappa + 1e-9): no exponential
+ *                  and no max subtraction.  (Same page, kernel branch; "The
+ *                  Kernel Between the Roles", "What the exponential was hired
+ *                  to do".)
+ *   CATTN_STAU     the s^tau power-law map: s_j = scale * q.k_j,
+ *                  phi = softplus(s) + eps_i, w = phi^tau_i / sum phi^tau_i,
+ *                  masked keys excluded.  ("s^tau: a focal-length knob for
+ *                  attention", core formula.)
+ *
+ * Telemetry (optional outputs, fp32, [B, h, Tq]):
+ *   row_mass       Yat: sum_j kappa_j (the row mass kept as its own channel,
+ *                  "What each normalizer forgets").  softmax: log-sum-exp of
+ *                  the scaled scores.  s^tau: log sum_j phi_j^tau.
+ *   row_max_score  Yat: max_j kappa_j.  softmax and s^tau: max_j s_j (scaled).
+ *
+ * Memory layout.  All tensors are dense row-major, innermost index last:
+ *   q   [B, h,   Tq, dk]      k [B, hkv, Tk, dk]      v [B, hkv, Tk, dv]
+ *   out [B, h,   Tq, dv]      (same element type as q, k, v)
+ *   b, eps, tau: fp32 [h], one value per query head.
+ * All data pointers are DEVICE pointers on the current CUDA device and must
+ * be 16-byte aligned.  The caller owns every buffer; the library never
+ * allocates, frees or keeps a reference to them after the call returns.
+ *
+ * Execution.  Every call is asynchronous on `stream` (NULL = legacy default
+ * stream) and never synchronises, except cattn_check_status.  Argument
+ * errors are reported before anything is enqueued.
+ *
+ * Errors.  Every entry point returns an int status: CATTN_OK or one of the
+ * CATTN_ERR_* codes below; cattn_error_string() names them.
+ */
+#ifndef CATTN_H
+#define CATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st *cattn_stream_t;
+
+/* Score-to-weight maps. */
+enum { CATTN_SOFTMAX = 0, CATTN_YAT = 1, CATTN_STAU = 2 };
+
+/* Element type of q, k, v and out.  bf16 runs on the tensor cores (tcgen05,
+ * fp32 accumulation); fp32 runs on the CUDA cores in full fp32. */
+enum { CATTN_F32 = 0, CATTN_BF16 = 1 };
+
+/* cattn_problem_t.flags */
+enum {
+  /* Yat only: the workspace already holds the squared row norms of these q
+   * and k, written by cattn_row_norms for the same problem; skip them. */
+  CATTN_FLAG_NORMS_READY = 1
+};
+
+/* Status codes. */
+enum {
+  CATTN_OK = 0,
+  CATTN_ERR_INVALID_ARG = 1, /* NULL required pointer, unknown enum, negative size, bad scale */
+  CATTN_ERR_SHAPE = 2,       /* h % hkv != 0, causal with Tq != Tk, Tk < 1, workspace too small */
+  CATTN_ERR_UNSUPPORTED = 3, /* head width not in the supported set, pointer not 16-byte
+                                aligned, device is not sm_103 */
+  CATTN_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
+  CATTN_ERR_TIMEOUT = 5      /* a kernel gave up on a bounded wait (reported by
+                                cattn_check_status) */
+};
+
+typedef struct {
+  int B;      /* batch size (>= 0; 0 is a no-op) */
+  int h;      /* query heads (>= 0; 0 is a no-op) */
+  int hkv;    /* key/value heads, h % hkv == 0; query head i reads kv head i / (h/hkv) */
+  int Tq;     /* query rows per head (>= 0; 0 is a no-op) */
+  int Tk;     /* key rows per head (>= 1) */
+  int dk;     /* query/key width and        bf16: (dk, dv) in {(64,64), (128,128), (128,64)} */
+  int dv;     /* value width; supported:    fp32: (dk, dv) in {(32,32), (64,64), (128,128), (128,64)} */
+  int dtype;  /* CATTN_F32 or CATTN_BF16 */
+  int causal; /* nonzero: key j is allowed for query row t only when j <= t; needs Tq == Tk */
+  float scale; /* softmax and s^tau multiply q.k by this (> 0, e.g. 1/sqrt(dk)); Yat ignores it */
+  int flags;  /* CATTN_FLAG_* */
+} cattn_problem_t;
+
+/* Library version, 100*major + minor. */
+int cattn_version(void);
+
+/* Static name of a status code. Never NULL. */
+const char *cattn_error_string(int status);
+
+/* Bytes of device workspace cattn_forward / cattn_row_norms need for this
+ * problem and variant (0 if none).  Only the bf16 Yat path uses workspace:
+ * fp32 squared norms of every query row and of every key row, the key part
+ * padded to a multiple of 128 rows per head.  Returns 0 for an invalid
+ * problem as well; cattn_validate says why. */
+size_t cattn_workspace_bytes(int variant, const cattn_problem_t *p);
+
+/* Host-side argument checks only: never touches the GPU, never dereferences
+ * a pointer.  Returns the status cattn_forward would return before launching
+ * anything (CATTN_OK if the arguments are acceptable). */
+int cattn_validate(int variant, const cattn_problem_t *p, const void *q, const void *k,
+                   const void *v, const float *b, const float *eps, const float *tau,
+                   const void *out, const void *workspace, size_t workspace_bytes);
+
+/* Squared L2 norms of the q rows and the k rows, fp32, computed from the
+ * stored bf16 values, written into the workspace (the norm prologue of the
+ * Yat map: |q - k|^2 = |q|^2 + |k|^2 - 2 q.k is assembled from the same dot
+ * products the scores need, "Softmax-Free Attention in JAX/Flax NNX", section
+ * "One module, two compatibility functions").  bf16 problems only.
+ * cattn_forward(CATTN_YAT, ...) runs this itself unless
+ * CATTN_FLAG_NORMS_READY is set. */
+int cattn_row_norms(const cattn_problem_t *p, const void *q, const void *k, void *workspace,
+                    size_t workspace_bytes, cattn_stream_t stream);
+
+/* The attention forward.  b and eps are required for CATTN_YAT (b >= 0,
+ * eps > 0), eps and tau for CATTN_STAU (eps > 0, tau > 0); unused ones may be
+ * NULL.  These device values are not read on the host, so their ranges are
+ * preconditions, not checked.  row_mass and row_max_score may be NULL.
+ * workspace may be NULL when cattn_workspace_bytes() is 0. */
+int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const void *k,
+                  const void *v, const float *b, const float *eps, const float *tau, void *out,
+                  float *row_mass, float *row_max_score, void *workspace,
+                  size_t workspace_bytes, cattn_stream_t stream);
+
+/* Synchronises `stream`, then reports (and clears) the device-side status
+ * word the kernels set when a bounded wait gives up: CATTN_ERR_TIMEOUT if
+ * any kernel since the last check did so, CATTN_ERR_CUDA if the stream
+ * reports an error, else CATTN_OK. */
+int cattn_check_status(cattn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CATTN_H */

@@ -1,0 +1,148 @@
+"""Python entry points over the C ABI (torch tensors in, torch tensors out).
+
+PyTorch supplies device memory and the current stream; the library's CUDA
+kernels do every step of the forward.  Host (CPU) tensors are accepted too:
+they are copied to the GPU, the forward runs there, and the results are copied
+back; this is the end-to-end form of the same call.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import native
+
+_VARIANTS = {"softmax": native.SOFTMAX, "yat": native.YAT, "stau": native.STAU,
+             native.SOFTMAX: native.SOFTMAX, native.YAT: native.YAT, native.STAU: native.STAU}
+_DTYPES = {torch.float32: native.F32, torch.bfloat16: native.BF16}
+
+
+def variant_id(variant) -> int:
+    try:
+        return _VARIANTS[variant]
+    except KeyError:
+        raise ValueError(f"unknown variant {variant!r}; use 'yat', 'softmax' or 'stau'") from None
+
+
+def make_problem(q, k, v, *, causal=False, scale=None, norms_ready=False) -> native.Problem:
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D: [B, h, Tq, dk], [B, hkv, Tk, dk], [B, hkv, Tk, dv]")
+    B, h, Tq, dk = q.shape
+    Bk, hkv, Tk, dk2 = k.shape
+    Bv, hkv2, Tk2, dv = v.shape
+    if (Bk, dk2) != (B, dk) or (Bv, hkv2, Tk2) != (B, hkv, Tk):
+        raise ValueError(f"inconsistent shapes q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in _DTYPES:
+        raise ValueError("q, k, v must share one dtype: torch.bfloat16 or torch.float32")
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    return native.Problem(B, h, hkv, Tq, Tk, dk, dv, _DTYPES[q.dtype], int(bool(causal)),
+                          float(scale), native.FLAG_NORMS_READY if norms_ready else 0)
+
+
+def workspace_bytes(variant, problem: native.Problem) -> int:
+    return int(native.load().cattn_workspace_bytes(variant_id(variant), ctypes.byref(problem)))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _per_head(x, h, device, name):
+    if x is None:
+        return None
+    t = torch.as_tensor(x, dtype=torch.float32)
+    if t.numel() == 1:
+        t = t.reshape(1).expand(h)
+    t = t.reshape(-1).contiguous()
+    if t.numel() != h:
+        raise ValueError(f"{name} needs one value per query head ({h}), got {t.numel()}")
+    return t.to(device)
+
+
+def _stream_handle(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def row_norms(q, k, v, workspace, *, causal=False, scale=None):
+    """Fill a Yat workspace with the squared q/k row norms (bf16 inputs).
+
+    A later ``forward('yat', ..., workspace=workspace, norms_ready=True)`` on the
+    same q, k, v skips the norm prologue.
+    """
+    prob = make_problem(q, k, v, causal=causal, scale=scale)
+    lib = native.load()
+    native.check(lib.cattn_row_norms(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(),
+                                     _stream_handle(q.device)), "cattn_row_norms")
+
+
+def forward(variant, q, k, v, *, b=None, eps=None, tau=None, causal=False, scale=None,
+            out=None, row_mass=None, row_max=None, telemetry=True, workspace=None,
+            norms_ready=False):
+    """Attention forward with a pluggable score-to-weight map.
+
+    variant: 'yat' | 'softmax' | 'stau'.  q [B,h,Tq,dk], k [B,hkv,Tk,dk],
+    v [B,hkv,Tk,dv], all torch.bfloat16 or all torch.float32, contiguous.
+    b, eps (Yat) and eps, tau (s^tau): one value per query head (or a scalar).
+    scale: softmax / s^tau score scale (default 1/sqrt(dk)); Yat ignores it.
+
+    Returns (out [B,h,Tq,dv], row_mass [B,h,Tq] or None, row_max [B,h,Tq] or None).
+    CUDA tensors: runs asynchronously on the current stream.  CPU tensors: copied
+    to the current CUDA device, computed there, and copied back (synchronous).
+    """
+    vid = variant_id(variant)
+    if q.device.type == "cpu":
+        return _forward_from_host(vid, q, k, v, b=b, eps=eps, tau=tau, causal=causal,
+                                  scale=scale, telemetry=telemetry)
+    if q.device.type != "cuda":
+        raise ValueError("tensors must live on a CUDA device or on the host")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+        if t.device != q.device:
+            raise ValueError("q, k, v must be on one device")
+    prob = make_problem(q, k, v, causal=causal, scale=scale, norms_ready=norms_ready)
+    dev = q.device
+    B, h, Tq, _ = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((B, h, Tq, dv), dtype=q.dtype, device=dev)
+    if telemetry:
+        if row_mass is None:
+            row_mass = torch.empty((B, h, Tq), dtype=torch.float32, device=dev)
+        if row_max is None:
+            row_max = torch.empty((B, h, Tq), dtype=torch.float32, device=dev)
+    bt = _per_head(b, h, dev, "b") if vid == native.YAT else None
+    et = _per_head(eps, h, dev, "eps") if vid in (native.YAT, native.STAU) else None
+    tt = _per_head(tau, h, dev, "tau") if vid == native.STAU else None
+    lib = native.load()
+    need = int(lib.cattn_workspace_bytes(vid, ctypes.byref(prob)))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    status = lib.cattn_forward(vid, ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(bt),
+                               _ptr(et), _ptr(tt), _ptr(out), _ptr(row_mass), _ptr(row_max),
+                               _ptr(workspace), ws_bytes, _stream_handle(dev))
+    native.check(status, "cattn_forward")
+    return out, row_mass, row_max
+
+
+def _forward_from_host(vid, q, k, v, *, b, eps, tau, causal, scale, telemetry):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    qd = q.to(dev, non_blocking=True)
+    kd = k.to(dev, non_blocking=True)
+    vd = v.to(dev, non_blocking=True)
+    o, m, x = forward(vid, qd, kd, vd, b=b, eps=eps, tau=tau, causal=causal, scale=scale,
+                      telemetry=telemetry)
+    res = (o.to("cpu"), None if m is None else m.to("cpu"), None if x is None else x.to("cpu"))
+    return res
+
+
+def check_status(stream=None) -> int:
+    """Synchronise `stream` (default: current) and return the kernels' wait status."""
+    handle = ctypes.c_void_p(stream.cuda_stream if stream is not None
+                             else torch.cuda.current_stream().cuda_stream)
+    return int(native.load().cattn_check_status(handle))

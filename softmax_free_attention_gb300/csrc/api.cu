@@ -1,0 +1,226 @@
+// api.cu -- the C ABI declared in include/cattn.h: argument validation,
+// workspace layout, TMA descriptor encoding and kernel dispatch.  Nothing here
+// allocates device memory or synchronises (cattn_check_status excepted).
+#include <cudaTypedefs.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "cattn.h"
+#include "kernels.h"
+
+namespace {
+
+using namespace cattn;
+
+constexpr int kTile = 128;  // key rows per tile; the key-norm vector is padded to it
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int tk_pad(const cattn_problem_t *p) { return (p->Tk + kTile - 1) / kTile * kTile; }
+
+bool is_empty(const cattn_problem_t *p) { return p->B == 0 || p->h == 0 || p->Tq == 0; }
+
+// Workspace layout (bf16 Yat only): nq [B*h, Tq] then nk [B*hkv, Tk_pad], fp32.
+size_t ws_nq_bytes(const cattn_problem_t *p) {
+  return align256((size_t)p->B * p->h * p->Tq * sizeof(float));
+}
+size_t ws_nk_bytes(const cattn_problem_t *p) {
+  return align256((size_t)p->B * p->hkv * tk_pad(p) * sizeof(float));
+}
+bool needs_workspace(int variant, const cattn_problem_t *p) {
+  return variant == CATTN_YAT && p->dtype == CATTN_BF16;
+}
+
+int check_problem(int variant, const cattn_problem_t *p) {
+  if (!p) return CATTN_ERR_INVALID_ARG;
+  if (variant != CATTN_SOFTMAX && variant != CATTN_YAT && variant != CATTN_STAU)
+    return CATTN_ERR_INVALID_ARG;
+  if (p->dtype != CATTN_F32 && p->dtype != CATTN_BF16) return CATTN_ERR_INVALID_ARG;
+  if (p->B < 0 || p->h < 0 || p->hkv < 1 || p->Tq < 0 || p->dk < 1 || p->dv < 1)
+    return CATTN_ERR_INVALID_ARG;
+  if (p->Tk < 1) return CATTN_ERR_SHAPE;
+  if (p->h % p->hkv != 0) return CATTN_ERR_SHAPE;
+  if (p->causal && p->Tq != p->Tk) return CATTN_ERR_SHAPE;
+  if (variant != CATTN_YAT && !(p->scale > 0.f && p->scale < 3.0e38f)) return CATTN_ERR_INVALID_ARG;
+  if (p->flags & ~CATTN_FLAG_NORMS_READY) return CATTN_ERR_INVALID_ARG;
+  const bool shape_ok = p->dtype == CATTN_BF16 ? fwd_tc_supported(p->dk, p->dv)
+                                               : fwd_simt_supported(p->dk, p->dv);
+  if (!shape_ok) return CATTN_ERR_UNSUPPORTED;
+  // every index the kernels form stays inside int32 per head and size_t overall
+  if ((long long)p->Tq * p->dk > (1ll << 31) || (long long)p->Tk * p->dk > (1ll << 31) ||
+      (long long)p->Tk * p->dv > (1ll << 31))
+    return CATTN_ERR_UNSUPPORTED;
+  if ((long long)p->B * p->h > (1ll << 24)) return CATTN_ERR_UNSUPPORTED;
+  return CATTN_OK;
+}
+
+int map_cuda(cudaError_t e) { return e == cudaSuccess ? CATTN_OK : CATTN_ERR_CUDA; }
+
+// The library is built for sm_103a only.
+int check_device() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CATTN_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+    return CATTN_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return CATTN_ERR_CUDA;
+  if (major != 10 || minor != 3) return CATTN_ERR_UNSUPPORTED;
+  return CATTN_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// bf16 [BH, T, d] as a 3-D tensor map with 64 x 128 x 1 boxes and 128-byte
+// swizzle (the shared-memory layout the tcgen05 descriptors describe).  Rows
+// past T read as zeros.
+int encode_bf16_3d(CUtensorMap *map, const void *base, int d, int T, int BH) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return CATTN_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CATTN_OK : CATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cattn_version(void) { return 100; }
+
+const char *cattn_error_string(int status) {
+  switch (status) {
+    case CATTN_OK: return "ok";
+    case CATTN_ERR_INVALID_ARG: return "invalid argument";
+    case CATTN_ERR_SHAPE: return "inconsistent shape";
+    case CATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case CATTN_ERR_CUDA: return "CUDA error";
+    case CATTN_ERR_TIMEOUT: return "kernel wait timed out";
+    default: return "unknown status";
+  }
+}
+
+size_t cattn_workspace_bytes(int variant, const cattn_problem_t *p) {
+  if (check_problem(variant, p) != CATTN_OK) return 0;
+  if (!needs_workspace(variant, p)) return 0;
+  return ws_nq_bytes(p) + ws_nk_bytes(p);
+}
+
+int cattn_validate(int variant, const cattn_problem_t *p, const void *q, const void *k,
+                   const void *v, const float *b, const float *eps, const float *tau,
+                   const void *out, const void *workspace, size_t workspace_bytes) {
+  int rc = check_problem(variant, p);
+  if (rc != CATTN_OK) return rc;
+  if (is_empty(p)) return CATTN_OK;
+  if (!q || !k || !v || !out) return CATTN_ERR_INVALID_ARG;
+  if (variant == CATTN_YAT && (!b || !eps)) return CATTN_ERR_INVALID_ARG;
+  if (variant == CATTN_STAU && (!eps || !tau)) return CATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return CATTN_ERR_UNSUPPORTED;
+  if (needs_workspace(variant, p)) {
+    if (!workspace) return CATTN_ERR_INVALID_ARG;
+    if (workspace_bytes < ws_nq_bytes(p) + ws_nk_bytes(p)) return CATTN_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CATTN_ERR_UNSUPPORTED;
+  }
+  return CATTN_OK;
+}
+
+int cattn_row_norms(const cattn_problem_t *p, const void *q, const void *k, void *workspace,
+                    size_t workspace_bytes, cattn_stream_t stream) {
+  int rc = check_problem(CATTN_YAT, p);
+  if (rc != CATTN_OK) return rc;
+  if (p->dtype != CATTN_BF16) return CATTN_ERR_UNSUPPORTED;
+  if (is_empty(p)) return CATTN_OK;
+  if (!q || !k || !workspace) return CATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return CATTN_ERR_UNSUPPORTED;
+  if (workspace_bytes < ws_nq_bytes(p) + ws_nk_bytes(p)) return CATTN_ERR_SHAPE;
+  rc = check_device();
+  if (rc != CATTN_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float *nq = static_cast<float *>(workspace);
+  float *nk = reinterpret_cast<float *>(static_cast<char *>(workspace) + ws_nq_bytes(p));
+  rc = map_cuda(launch_row_sqnorm_bf16(q, nq, p->B * p->h, p->Tq, p->Tq, p->dk, s));
+  if (rc != CATTN_OK) return rc;
+  return map_cuda(launch_row_sqnorm_bf16(k, nk, p->B * p->hkv, p->Tk, tk_pad(p), p->dk, s));
+}
+
+int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const void *k,
+                  const void *v, const float *b, const float *eps, const float *tau, void *out,
+                  float *row_mass, float *row_max_score, void *workspace,
+                  size_t workspace_bytes, cattn_stream_t stream) {
+  int rc = cattn_validate(variant, p, q, k, v, b, eps, tau, out, workspace, workspace_bytes);
+  if (rc != CATTN_OK) return rc;
+  if (is_empty(p)) return CATTN_OK;
+  rc = check_device();
+  if (rc != CATTN_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  FwdParams fp;
+  memset(&fp, 0, sizeof(fp));
+  fp.q = q;
+  fp.k = k;
+  fp.v = v;
+  fp.out = out;
+  fp.row_mass = row_mass;
+  fp.row_max = row_max_score;
+  fp.b = b;
+  fp.eps = eps;
+  fp.tau = tau;
+  fp.B = p->B;
+  fp.h = p->h;
+  fp.hkv = p->hkv;
+  fp.Tq = p->Tq;
+  fp.Tk = p->Tk;
+  fp.Tk_pad = tk_pad(p);
+  fp.causal = p->causal ? 1 : 0;
+  fp.scale = p->scale;
+  fp.n_pairs = (p->Tq + 2 * kTile - 1) / (2 * kTile);
+  fp.n_kv_tiles = (p->Tk + kTile - 1) / kTile;
+
+  if (p->dtype == CATTN_F32) return map_cuda(launch_fwd_simt(variant, p->dk, p->dv, fp, s));
+
+  if (variant == CATTN_YAT) {
+    fp.nq = static_cast<const float *>(workspace);
+    fp.nk = reinterpret_cast<const float *>(static_cast<const char *>(workspace) + ws_nq_bytes(p));
+    if (!(p->flags & CATTN_FLAG_NORMS_READY)) {
+      rc = cattn_row_norms(p, q, k, workspace, workspace_bytes, stream);
+      if (rc != CATTN_OK) return rc;
+    }
+  }
+  CUtensorMap tq, tk, tv;
+  if ((rc = encode_bf16_3d(&tq, q, p->dk, p->Tq, p->B * p->h)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&tk, k, p->dk, p->Tk, p->B * p->hkv)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&tv, v, p->dv, p->Tk, p->B * p->hkv)) != CATTN_OK) return rc;
+  return map_cuda(launch_fwd_tc(variant, p->dk, p->dv, fp, tq, tk, tv, s));
+}
+
+int cattn_check_status(cattn_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return CATTN_ERR_CUDA;
+  unsigned int status = 0;
+  if (read_and_clear_status(&status) != cudaSuccess) return CATTN_ERR_CUDA;
+  return status ? CATTN_ERR_TIMEOUT : CATTN_OK;
+}
+
+}  // extern "C"

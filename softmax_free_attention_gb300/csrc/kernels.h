@@ -1,0 +1,45 @@
+// kernels.h -- host-side launch interface between the C ABI (api.cu) and the
+// kernel translation units.  Internal to the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cattn {
+
+enum Variant { kSoftmax = 0, kYat = 1, kStau = 2 };
+
+// Everything a forward kernel reads besides the tensor maps.
+struct FwdParams {
+  const void *q, *k, *v;        // element pointers (the tensor-core path reads through TMA)
+  void *out;                    // [B, h, Tq, dv]
+  float *row_mass, *row_max;    // [B, h, Tq] or NULL
+  const float *b, *eps, *tau;   // [h]
+  const float *nq;              // [B*h, Tq]        squared q row norms (Yat, bf16)
+  const float *nk;              // [B*hkv, Tk_pad]  squared k row norms, zero padded
+  int B, h, hkv, Tq, Tk, Tk_pad;
+  int causal;
+  float scale;
+  int n_pairs;     // query-tile pairs per head: ceil(Tq / 256)
+  int n_kv_tiles;  // ceil(Tk / 128)
+};
+
+// Tensor-core (tcgen05) forward for bf16 inputs.  Returns a cudaError_t.
+cudaError_t launch_fwd_tc(int variant, int dk, int dv, const FwdParams &p, const CUtensorMap &tq,
+                          const CUtensorMap &tk, const CUtensorMap &tv, cudaStream_t s);
+bool fwd_tc_supported(int dk, int dv);
+
+// CUDA-core fp32 forward.
+cudaError_t launch_fwd_simt(int variant, int dk, int dv, const FwdParams &p, cudaStream_t s);
+bool fwd_simt_supported(int dk, int dv);
+
+// Squared row norms of a bf16 [BH, T, d] tensor into out[BH, T_pad] (zeros
+// for padded rows).
+cudaError_t launch_row_sqnorm_bf16(const void *x, float *out, int BH, int T, int T_pad, int d,
+                                   cudaStream_t s);
+
+// Device status word set by kernels whose bounded waits gave up.
+cudaError_t read_and_clear_status(unsigned int *value);
+
+}  // namespace cattn

@@ -1,0 +1,214 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs, element by element.
+
+Small problems are compared on every output; the full-size workloads are run
+in the same launch sequence the benchmark times and compared on sampled rows
+the oracle computes one by one.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import parity_utils as pu
+from softmax_free_attention_gb300 import attention, workloads
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = ["yat", "softmax", "stau"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from softmax_free_attention_gb300 import build
+    build.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _wl(name, B, h, hkv, Tq, Tk, dk, dv, dtype="bf16", causal=True, qk=1.0, seed=0):
+    return workloads.Workload(name, B=B, h=h, hkv=hkv, Tq=Tq, Tk=Tk, dk=dk, dv=dv, dtype=dtype,
+                              causal=causal, qk_factor=qk, yat_param="softplus_uniform", seed=seed)
+
+
+# ---------------------------------------------------------------- worked example
+
+def test_sdpa_worked_example_on_gpu(golden_dir):
+    """The SDPA page's example, zero-padded to a supported head width (which
+    leaves every dot product and every output column unchanged)."""
+    with open(os.path.join(golden_dir, "sdpa_worked_example.json")) as f:
+        g = json.load(f)
+    q = torch.zeros(1, 1, 2, 32)
+    k = torch.zeros(1, 1, 2, 32)
+    v = torch.zeros(1, 1, 2, 32)
+    q[0, 0, :, :1] = torch.tensor(g["q"])
+    k[0, 0, :, :1] = torch.tensor(g["k"])
+    v[0, 0, :, :2] = torch.tensor(g["v"])
+    out, lse, mx = attention.forward("softmax", q.cuda(), k.cuda(), v.cuda(), scale=1.0)
+    torch.cuda.synchronize()
+    np.testing.assert_allclose(out[0, 0, :, :2].cpu().numpy(), g["out"], atol=1e-6)
+    assert out[0, 0, :, 2:].abs().max().item() == 0.0
+    np.testing.assert_allclose(lse[0, 0].cpu().numpy(), [math.log(3), math.log(2)], atol=1e-6)
+    # the tensor-core path on the same example (bf16 rounds ln 2 to 0.69140625)
+    qb, kb, vb = (t.new_zeros(1, 1, 2, 64) for t in (q, k, v))
+    qb[..., :32], kb[..., :32], vb[..., :32] = q, k, v
+    ob, _, _ = attention.forward("softmax", qb.bfloat16().cuda(), kb.bfloat16().cuda(),
+                                 vb.bfloat16().cuda(), scale=1.0)
+    torch.cuda.synchronize()
+    assert np.abs(ob[0, 0, :, :2].float().cpu().numpy() - np.array(g["out"])).max() <= 2e-2 * 6
+
+
+# ---------------------------------------------------------------- ragged / edge shapes
+
+SHAPES = [
+    # B, h, hkv, Tq, Tk, dk, dv, causal
+    (1, 2, 2, 1, 1, 64, 64, True),
+    (1, 2, 2, 2, 2, 64, 64, True),
+    (2, 2, 1, 127, 127, 64, 64, True),
+    (1, 2, 2, 128, 128, 128, 128, True),
+    (1, 2, 2, 129, 129, 128, 128, True),
+    (1, 2, 2, 255, 255, 128, 64, True),
+    (1, 2, 2, 300, 300, 128, 128, False),
+    (1, 4, 2, 200, 700, 128, 64, False),
+    (2, 2, 2, 640, 640, 64, 64, True),
+    (1, 1, 1, 1, 129, 64, 64, False),
+    (1, 2, 1, 384, 384, 128, 128, True),
+]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_tensor_core_ragged(variant, shape):
+    B, h, hkv, Tq, Tk, dk, dv, causal = shape
+    w = _wl("ragged", B, h, hkv, Tq, Tk, dk, dv, causal=causal, seed=Tq * 7 + Tk)
+    inp = workloads.generate(w)
+    pu.full_parity(variant, inp, causal=causal, scale=w.scale, where=f"{variant} {shape}")
+
+
+F32_SHAPES = [
+    (1, 2, 2, 1, 1, 32, 32, True),
+    (1, 2, 1, 77, 77, 64, 64, True),
+    (2, 2, 2, 100, 150, 128, 64, False),
+    (1, 1, 1, 65, 65, 128, 128, True),
+]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("shape", F32_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_fp32_ragged(variant, shape):
+    B, h, hkv, Tq, Tk, dk, dv, causal = shape
+    w = _wl("ragged32", B, h, hkv, Tq, Tk, dk, dv, dtype="f32", causal=causal, seed=Tq + 3)
+    inp = workloads.generate(w)
+    pu.full_parity(variant, inp, causal=causal, scale=w.scale, where=f"f32 {variant} {shape}")
+
+
+# ---------------------------------------------------------------- the small workloads
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_cfg1_fp32(variant):
+    w = workloads.WORKLOADS["cfg1_f32"]
+    pu.full_parity(variant, workloads.generate(w), causal=w.causal, scale=w.scale,
+                   where=f"cfg1 {variant}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("name", ["cfg2_s1", "cfg2_s4", "cfg2_s16"])
+def test_cfg2_char_gpt(variant, name):
+    w = workloads.WORKLOADS[name]
+    pu.full_parity(variant, workloads.generate(w), causal=w.causal, scale=w.scale,
+                   two_step=True, where=f"{name} {variant}")
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+def _rows(T, seed):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 127, 128, 129, 255, 256, T // 2, T - 2, T - 1]
+    return sorted(set([r for r in fixed if 0 <= r < T] + rng.integers(0, T, 12).tolist()))
+
+
+@pytest.fixture(scope="module")
+def cfg3_inputs():
+    return workloads.generate(workloads.WORKLOADS["cfg3"])
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_cfg3_full_size_sampled(variant, cfg3_inputs):
+    w = workloads.WORKLOADS["cfg3"]
+    pairs = [(0, 0), (15, 15), (7, 3)]
+    pu.sampled_parity(variant, cfg3_inputs, causal=True, scale=w.scale, pairs=pairs,
+                      rows_per_pair=lambda b, hh: _rows(w.Tq, b * 31 + hh), two_step=True,
+                      where=f"cfg3 {variant}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_cfg4_gqa_full_size_sampled(variant):
+    w = workloads.WORKLOADS["cfg4_gqa"]
+    inp = workloads.generate(w)
+    pairs = [(0, 0), (0, 1), (3, 14), (2, 7)]  # heads 0 and 1 share kv head 0
+    pu.sampled_parity(variant, inp, causal=True, scale=w.scale, pairs=pairs,
+                      rows_per_pair=lambda b, hh: _rows(w.Tq, b * 17 + hh), two_step=True,
+                      where=f"cfg4 {variant}")
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_cfg5_cross_full_size_sampled(variant):
+    w = workloads.WORKLOADS["cfg5_cross"]
+    inp = workloads.generate(w)
+    pairs = [(0, 0), (0, 31)]
+    pu.sampled_parity(variant, inp, causal=False, scale=w.scale, pairs=pairs,
+                      rows_per_pair=lambda b, hh: _rows(w.Tq, hh)[:10], two_step=True,
+                      where=f"cfg5 {variant}")
+
+
+# ---------------------------------------------------------------- properties and API paths
+
+def test_deterministic_and_telemetry_optional():
+    w = _wl("det", 2, 4, 2, 333, 333, 128, 128, causal=True, seed=5)
+    inp = workloads.generate(w, device="cuda")
+    kw = dict(b=inp["yat_b"], eps=inp["yat_eps"], causal=True)
+    a = attention.forward("yat", inp["q"], inp["k"], inp["v"], **kw)
+    b = attention.forward("yat", inp["q"], inp["k"], inp["v"], **kw)
+    c = attention.forward("yat", inp["q"], inp["k"], inp["v"], telemetry=False, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    assert c[1] is None and c[2] is None and torch.equal(a[0], c[0])
+
+
+def test_host_tensors_round_trip():
+    w = _wl("host", 1, 2, 2, 256, 256, 64, 64, causal=True, seed=9)
+    inp = workloads.generate(w)
+    pinned = {n: inp[n].pin_memory() for n in ("q", "k", "v")}
+    host = attention.forward("softmax", pinned["q"], pinned["k"], pinned["v"], causal=True)
+    dev = attention.forward("softmax", inp["q"].cuda(), inp["k"].cuda(), inp["v"].cuda(),
+                            causal=True)
+    torch.cuda.synchronize()
+    assert host[0].device.type == "cpu"
+    assert torch.equal(host[0], dev[0].cpu()) and torch.equal(host[1], dev[1].cpu())
+
+
+def test_empty_problems():
+    q = torch.zeros(0, 2, 16, 64, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(0, 2, 16, 64, dtype=torch.bfloat16, device="cuda")
+    out, m, x = attention.forward("softmax", q, k, k, causal=True)
+    assert out.shape == (0, 2, 16, 64)
+    q = torch.zeros(1, 2, 0, 64, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 2, 5, 64, dtype=torch.bfloat16, device="cuda")
+    out, m, x = attention.forward("yat", q, k, k, b=1.0, eps=1.0)
+    torch.cuda.synchronize()
+    assert out.shape == (1, 2, 0, 64)
+
+
+def test_constant_values_give_constant_output():
+    # weights sum to one (Yat: mass / (mass + 1e-9)) so a constant v comes back
+    w = _wl("const", 1, 2, 2, 300, 300, 128, 128, causal=True, seed=4)
+    inp = workloads.generate(w, device="cuda")
+    v = torch.full_like(inp["v"], 0.75)
+    for variant in VARIANTS:
+        kw = pu.params_for(variant, inp)
+        out, _, _ = attention.forward(variant, inp["q"], inp["k"], v, causal=True, **kw)
+        torch.cuda.synchronize()
+        assert (out.float() - 0.75).abs().max().item() <= 2e-2 * 0.75, variant

@@ -1,0 +1,150 @@
+"""The C-ABI library without a GPU: it loads, exports what include/cattn.h
+declares, and rejects bad arguments on the host before touching CUDA.
+
+Every call here fails validation on purpose (or never reaches CUDA), so the
+same tests are safe on a machine with a GPU: no kernel is ever launched with
+the placeholder pointers used below.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from softmax_free_attention_gb300 import native, workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from softmax_free_attention_gb300 import build
+    build.build()
+    return native.load()
+
+
+def _declared_symbols():
+    with open(os.path.join(ROOT, "include", "cattn.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"\b(cattn_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_symbols()
+    assert set(declared) == set(native.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert lib.cattn_version() == 100
+
+
+def test_error_strings(lib):
+    for code in range(6):
+        assert lib.cattn_error_string(code)
+    assert lib.cattn_error_string(99) == b"unknown status"
+
+
+FAKE = ctypes.c_void_p(1 << 20)          # 16-byte aligned, never dereferenced
+MISALIGNED = ctypes.c_void_p((1 << 20) + 8)
+
+
+def prob(**kw):
+    base = dict(B=1, h=4, hkv=4, Tq=256, Tk=256, dk=128, dv=128, dtype=native.BF16, causal=1,
+                scale=0.088, flags=0)
+    base.update(kw)
+    return native.Problem(**base)
+
+
+def validate(lib, variant, p, q=FAKE, k=FAKE, v=FAKE, b=FAKE, eps=FAKE, tau=FAKE, out=FAKE,
+             ws=None, ws_bytes=0):
+    return lib.cattn_validate(variant, ctypes.byref(p), q, k, v, b, eps, tau, out, ws, ws_bytes)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(h=3, hkv=2), native.ERR_SHAPE),               # h % hkv != 0
+    (dict(Tq=256, Tk=128), native.ERR_SHAPE),           # causal needs Tq == Tk
+    (dict(Tk=0, causal=0), native.ERR_SHAPE),
+    (dict(B=-1), native.ERR_INVALID_ARG),
+    (dict(hkv=0), native.ERR_INVALID_ARG),
+    (dict(dtype=7), native.ERR_INVALID_ARG),
+    (dict(scale=0.0), native.ERR_INVALID_ARG),
+    (dict(scale=-1.0), native.ERR_INVALID_ARG),
+    (dict(flags=2), native.ERR_INVALID_ARG),
+    (dict(dk=96, dv=96), native.ERR_UNSUPPORTED),
+    (dict(dk=64, dv=128), native.ERR_UNSUPPORTED),
+    (dict(dk=32, dv=32), native.ERR_UNSUPPORTED),       # bf16 needs 64 or 128
+])
+def test_problem_rejections(lib, kw, code):
+    assert validate(lib, native.SOFTMAX, prob(**kw)) == code
+    assert lib.cattn_workspace_bytes(native.SOFTMAX, ctypes.byref(prob(**kw))) == 0
+
+
+def test_pointer_rejections(lib):
+    p = prob()
+    assert validate(lib, 9, p) == native.ERR_INVALID_ARG                       # unknown variant
+    assert validate(lib, native.SOFTMAX, p, q=None) == native.ERR_INVALID_ARG
+    assert validate(lib, native.SOFTMAX, p, out=None) == native.ERR_INVALID_ARG
+    assert validate(lib, native.SOFTMAX, p, k=MISALIGNED) == native.ERR_UNSUPPORTED
+    assert validate(lib, native.STAU, p, tau=None) == native.ERR_INVALID_ARG
+    assert validate(lib, native.YAT, p, b=None) == native.ERR_INVALID_ARG
+    # Yat bf16 needs a workspace of the advertised size, 256-byte aligned
+    need = lib.cattn_workspace_bytes(native.YAT, ctypes.byref(p))
+    assert need > 0
+    assert validate(lib, native.YAT, p) == native.ERR_INVALID_ARG
+    assert validate(lib, native.YAT, p, ws=FAKE, ws_bytes=need - 1) == native.ERR_SHAPE
+    assert validate(lib, native.YAT, p, ws=ctypes.c_void_p((1 << 20) + 16),
+                    ws_bytes=need) == native.ERR_UNSUPPORTED
+    assert validate(lib, native.YAT, p, ws=FAKE, ws_bytes=need) == native.OK
+    assert validate(lib, native.SOFTMAX, p) == native.OK
+    # the forward itself returns the same codes without touching the GPU
+    assert lib.cattn_forward(native.SOFTMAX, ctypes.byref(prob(h=3, hkv=2)), FAKE, FAKE, FAKE,
+                             None, None, None, FAKE, None, None, None, 0, None) == native.ERR_SHAPE
+    assert lib.cattn_forward(native.YAT, ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                             FAKE, None, None, FAKE, need - 1, None) == native.ERR_SHAPE
+
+
+def test_workspace_layout(lib):
+    # nq [B*h, Tq] then nk [B*hkv, ceil(Tk/128)*128], fp32, each rounded to 256 B
+    p = prob(B=2, h=4, hkv=2, Tq=300, Tk=300, dk=64, dv=64)
+    nq = (2 * 4 * 300 * 4 + 255) // 256 * 256
+    nk = (2 * 2 * 384 * 4 + 255) // 256 * 256
+    assert lib.cattn_workspace_bytes(native.YAT, ctypes.byref(p)) == nq + nk
+    assert lib.cattn_workspace_bytes(native.SOFTMAX, ctypes.byref(p)) == 0
+    assert lib.cattn_workspace_bytes(native.STAU, ctypes.byref(p)) == 0
+    p32 = prob(dtype=native.F32, dk=32, dv=32)
+    assert lib.cattn_workspace_bytes(native.YAT, ctypes.byref(p32)) == 0
+
+
+def test_empty_problem_is_a_noop_on_the_host(lib):
+    # B = 0: nothing to compute, accepted without pointers and without CUDA
+    p = prob(B=0)
+    assert validate(lib, native.SOFTMAX, p, q=None, k=None, v=None, out=None) == native.OK
+    assert lib.cattn_forward(native.SOFTMAX, ctypes.byref(p), None, None, None, None, None, None,
+                             None, None, None, None, 0, None) == native.OK
+
+
+def test_python_problem_marshalling():
+    import torch
+    from softmax_free_attention_gb300 import attention
+    q = torch.zeros(2, 4, 10, 64, dtype=torch.bfloat16)
+    k = torch.zeros(2, 2, 12, 64, dtype=torch.bfloat16)
+    v = torch.zeros(2, 2, 12, 64, dtype=torch.bfloat16)
+    p = attention.make_problem(q, k, v, causal=False)
+    assert (p.B, p.h, p.hkv, p.Tq, p.Tk, p.dk, p.dv, p.dtype) == (2, 4, 2, 10, 12, 64, 64, 1)
+    assert p.scale == pytest.approx(1 / 8)
+    with pytest.raises(ValueError):
+        attention.make_problem(q, k, v[:, :, :5])
+    with pytest.raises(ValueError):
+        attention.make_problem(q, k.float(), v)
+    with pytest.raises(ValueError):
+        attention.variant_id("relu")
+
+
+def test_workload_table_matches_stated_shapes():
+    w = workloads.WORKLOADS
+    assert (w["cfg3"].B, w["cfg3"].h, w["cfg3"].Tq, w["cfg3"].dk) == (16, 16, 4096, 128)
+    assert w["cfg3"].flops() == pytest.approx(2 ** 40)
+    assert (w["cfg4_gqa"].h, w["cfg4_gqa"].hkv, w["cfg4_gqa"].Tq) == (16, 8, 8192)
+    assert (w["cfg5_cross"].Tq, w["cfg5_cross"].Tk, w["cfg5_cross"].dv) == (2048, 32768, 64)
+    assert not w["cfg5_cross"].causal
+    rows = workloads.sample_rows(w["cfg2_s1"])
+    assert rows.min() >= 0 and rows.max() < 32 * 4 * 256
