@@ -1,0 +1,387 @@
+"""Benchmark: attention forward TFLOP/s and fraction of the GB300 bf16 tensor
+peak, per score-to-weight map, on one GPU (or N independent replicas).
+
+Workload: B=16, h=16, T=4096, dk=dv=128, bf16, causal (the mid-size causal
+layer on which the Yat target is set), seeded synthetic inputs.  One step is
+one Yat forward through the C ABI: the norm prologue (cattn_row_norms) and
+the fused forward (cattn_forward with the norms marked ready).  softmax and
+s^tau are timed on the same inputs in the same run.  FLOPs per forward:
+2*B*h*Tq*Tk*(dk+dv), halved for causal.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 oracle on
+the host cores on bounded samples of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s and % of GB300 bf16 tensor peak per variant, 1 GPU"
+WORKLOAD = "cfg3"
+FALLBACK_TFLOPS = 1900.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def workload():
+    from softmax_free_attention_gb300 import workloads
+    return workloads.WORKLOADS[WORKLOAD]
+
+
+def config_block(w, extra=None):
+    cfg = {"workload": f"{w.name}: B={w.B} h={w.h} hkv={w.hkv} Tq={w.Tq} Tk={w.Tk} "
+                       f"dk={w.dk} dv={w.dv} {w.dtype} {'causal' if w.causal else 'non-causal'}",
+           "B": w.B, "h": w.h, "hkv": w.hkv, "Tq": w.Tq, "Tk": w.Tk, "dk": w.dk, "dv": w.dv,
+           "causal": w.causal, "step": "Yat forward (norm prologue + fused tcgen05 kernel)",
+           "l2": "inputs larger than L2 (q,k,v = 768 MiB bf16 vs 129 MB L2); no flush needed",
+           "flops_per_step": w.flops()}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0.0)), "measured"
+    except Exception:
+        return FALLBACK_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("fwd_tc.cu", "ptx.cuh", "kernels.h"):
+        with open(os.path.join(ROOT, "softmax_free_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        rec = d.get(kernel_key)
+        if rec and rec.get("source_hash") == kernel_source_hash():
+            return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        busy = [s for s in sm if mx and s > 0.3 * mx] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_sample(w, inputs, target_seconds, seed=0, cap_rows=None):
+    """Time the fp64 oracle on a bounded random sample of query rows.
+
+    Rows are drawn uniformly over (batch, head, t); each (batch, head) pair is
+    widened to fp64 separately.  Returns (TFLOP/s, seconds, rows, threads).
+    """
+    import torch
+
+    import oracle
+
+    threads = os.cpu_count() or 1
+    rng = np.random.default_rng(seed)
+    pairs = [(int(b), int(hh)) for b, hh in zip(rng.integers(0, w.B, 8), rng.integers(0, w.h, 8))]
+    kw_all = {"yat": dict(b=inputs["yat_b"], eps=inputs["yat_eps"])}
+    prepared = []
+    for (b, hh) in pairs:
+        g = hh // (w.h // w.hkv)
+        prepared.append((b, hh, inputs["q"][b:b + 1, hh:hh + 1].to(torch.float64).numpy(),
+                         inputs["k"][b:b + 1, g:g + 1].to(torch.float64).numpy(),
+                         inputs["v"][b:b + 1, g:g + 1].to(torch.float64).numpy()))
+
+    def run(rows_per_pair):
+        flops, t0 = 0.0, time.perf_counter()
+        for (b, hh, q, k, v) in prepared:
+            rows = rng.integers(0, w.Tq, rows_per_pair)
+            keys = (rows + 1) if w.causal else np.full_like(rows, w.Tk)
+            flops += float(np.sum(2.0 * keys * (w.dk + w.dv)))
+            oracle.forward("yat", q, k, v, b=kw_all["yat"]["b"][hh:hh + 1],
+                           eps=kw_all["yat"]["eps"][hh:hh + 1], causal=w.causal,
+                           scale=w.scale, rows=rows, nthreads=threads)
+        return flops, time.perf_counter() - t0
+
+    f, t = run(max(1, threads // 2))  # calibration
+    per_row = t / (8 * max(1, threads // 2))
+    rows_per_pair = max(1, int(target_seconds / per_row / 8))
+    if cap_rows:
+        rows_per_pair = min(rows_per_pair, cap_rows)
+    f, t = run(rows_per_pair)
+    return f / t / 1e12, t, rows_per_pair * 8, threads
+
+
+def reference_arm(args):
+    """The fp64 oracle on the host cores, as the reference arm."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from softmax_free_attention_gb300 import workloads
+    w = workload()
+    inputs = workloads.generate(w)
+    per_step = max(1.0, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, inputs, per_step / 4)
+    vals, secs, rows_total, threads = [], 0.0, 0, 1
+    for s in range(args.steps):
+        v, t, rows, threads = cpu_oracle_sample(w, inputs, per_step, seed=100 + s)
+        vals.append(v)
+        secs += t
+        rows_total += rows
+    value = statistics.mean(vals)
+    sample = (f"{rows_total} query rows drawn uniformly from 8 (batch, head) pairs of {w.name}, "
+              f"Yat map, fp64, over {args.steps} steps")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * secs / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_block(w, {"step": "fp64 oracle on a bounded row sample"}),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    import torch.distributed as dist
+
+    from softmax_free_attention_gb300 import attention, build, native, workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        build.build()
+    if world > 1:
+        dist.barrier()
+    native.load()
+
+    w = workload()
+    inputs_host = workloads.generate(w)
+    q, k, v = (inputs_host[n].to(dev) for n in ("q", "k", "v"))
+    yb = torch.as_tensor(inputs_host["yat_b"], device=dev)
+    ye = torch.as_tensor(inputs_host["yat_eps"], device=dev)
+    se = torch.as_tensor(inputs_host["stau_eps"], device=dev)
+    tau = torch.as_tensor(inputs_host["tau"], device=dev)
+    prob = attention.make_problem(q, k, v, causal=w.causal, scale=w.scale)
+    ws = torch.empty(attention.workspace_bytes("yat", prob), dtype=torch.uint8, device=dev)
+    out = torch.empty((w.B, w.h, w.Tq, w.dv), dtype=q.dtype, device=dev)
+    mass = torch.empty((w.B, w.h, w.Tq), dtype=torch.float32, device=dev)
+    mx = torch.empty_like(mass)
+
+    def yat_step(ev=None):
+        if ev is not None:
+            ev[0].record()
+        attention.row_norms(q, k, v, ws, causal=w.causal, scale=w.scale)
+        if ev is not None:
+            ev[1].record()
+        attention.forward("yat", q, k, v, b=yb, eps=ye, causal=w.causal, scale=w.scale,
+                          out=out, row_mass=mass, row_max=mx, workspace=ws, norms_ready=True)
+        if ev is not None:
+            ev[2].record()
+
+    def variant_step(variant):
+        kw = {"softmax": {}, "stau": dict(eps=se, tau=tau)}[variant]
+        attention.forward(variant, q, k, v, causal=w.causal, scale=w.scale, out=out,
+                          row_mass=mass, row_max=mx, **kw)
+
+    # ---- headline: K Yat steps
+    for _ in range(max(3, args.warmup)):
+        yat_step()
+    torch.cuda.synchronize()
+    assert attention.check_status() == 0
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record()
+        for s in range(args.steps):
+            yat_step(evs[s])
+        stop.record()
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    norms_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    fwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    assert attention.check_status() == 0
+    ms_per_step = elapsed_ms / args.steps
+    flops = w.flops()
+    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    peak_burst, peak_sust, peak_kind = measured_peaks()
+
+    # ---- per-variant forward timing on the same inputs
+    per_variant = {}
+    fwd_tflops = flops / (fwd_ms * 1e-3) / 1e12
+    per_variant["yat"] = {"tflops": flops / (ms_per_step * 1e-3) / 1e12,
+                          "kernel_tflops": fwd_tflops, "kernel_ms": fwd_ms,
+                          "norm_prologue_ms": norms_ms,
+                          "frac_of_peak": fwd_tflops / peak_burst}
+    for variant in ("softmax", "stau"):
+        for _ in range(3):
+            variant_step(variant)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            variant_step(variant)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / args.steps
+        tf = flops / (ms * 1e-3) / 1e12
+        per_variant[variant] = {"tflops": tf, "kernel_ms": ms, "frac_of_peak": tf / peak_burst}
+    assert attention.check_status() == 0
+    per_variant["yat_over_softmax"] = per_variant["yat"]["tflops"] / per_variant["softmax"]["tflops"]
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pinned = {n: inputs_host[n].pin_memory() for n in ("q", "k", "v")}
+        h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+        d2h = w.B * w.h * w.Tq * (w.dv * 2 + 8)
+        res = attention.forward("yat", pinned["q"], pinned["k"], pinned["v"], b=yb.cpu(),
+                                eps=ye.cpu(), causal=w.causal, scale=w.scale)  # warm-up
+        del res
+        torch.cuda.synchronize()
+        n_e2e = max(2, min(args.steps, 5))
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            res = attention.forward("yat", pinned["q"], pinned["k"], pinned["v"], b=yb.cpu(),
+                                    eps=ye.cpu(), causal=w.causal, scale=w.scale)
+        torch.cuda.synchronize()
+        e2e_s = (time.perf_counter() - t0) / n_e2e
+        e2e = {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e}
+
+    # ---- CPU baseline: the oracle on the host cores, bounded sample
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        val, secs, rows, threads = cpu_oracle_sample(w, inputs_host, 12.0)
+        cpu = {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{rows} random query rows from 8 (batch, head) pairs of {w.name}, "
+                         f"Yat map, fp64 ({secs:.1f} s)"}
+
+    achieved = fwd_tflops
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
+                "frac": achieved / peak_burst, "traffic": recorded_traffic("fwd_kernel_yat_cfg3"),
+                "peak_kind": f"{peak_kind} bf16 burst (cuBLAS)",
+                "kernel": "cattn::tc::fwd_kernel<Yat,128,128>"}
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": config_block(w), "per_variant": per_variant,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clocks.summary(), "gpu_launches": 2 * args.steps,
+            "peak_sustained_tflops": peak_sust}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

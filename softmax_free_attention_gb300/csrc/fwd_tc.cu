@@ -444,6 +444,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const float mn = fmaxf(m_used, m_new);
             const float corr = ex2_approx(m_used - mn);
             acc_a *= corr;
+            acc_b *= corr;
             if (j > 0) scale_o_tmem<DV>(t_o, corr);
             m_used = mn;
           }
