@@ -44,12 +44,15 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override B (small cases for profiler captures; not a bench line)")
     return ap.parse_args()
 
 
-def workload():
+def workload(batch=None):
     from softmax_free_attention_gb300 import workloads
-    return workloads.WORKLOADS[WORKLOAD]
+    w = workloads.WORKLOADS[WORKLOAD]
+    return w.scaled(B=batch) if batch else w
 
 
 def config_block(w, extra=None):
@@ -187,9 +190,15 @@ def cpu_oracle_sample(w, inputs, target_seconds, seed=0, cap_rows=None):
                            scale=w.scale, rows=rows, nthreads=threads)
         return flops, time.perf_counter() - t0
 
-    f, t = run(max(1, threads // 2))  # calibration
-    per_row = t / (8 * max(1, threads // 2))
-    rows_per_pair = max(1, int(target_seconds / per_row / 8))
+    rows_per_pair = max(1, threads // 2)
+    f, t = run(rows_per_pair)  # calibration: grow the sample until it takes a measurable time
+    while t < 0.25 * target_seconds:
+        rows_per_pair = max(rows_per_pair + 1, int(rows_per_pair * min(8.0, target_seconds / max(t, 1e-3))))
+        if cap_rows and rows_per_pair >= cap_rows:
+            rows_per_pair = cap_rows
+            break
+        f, t = run(rows_per_pair)
+    rows_per_pair = max(1, int(rows_per_pair * target_seconds / max(t, 1e-3)))
     if cap_rows:
         rows_per_pair = min(rows_per_pair, cap_rows)
     f, t = run(rows_per_pair)
@@ -202,7 +211,7 @@ def reference_arm(args):
     if rank != 0:
         return 0
     from softmax_free_attention_gb300 import workloads
-    w = workload()
+    w = workload(args.batch)
     inputs = workloads.generate(w)
     per_step = max(1.0, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
@@ -252,7 +261,7 @@ def main():
         dist.barrier()
     native.load()
 
-    w = workload()
+    w = workload(args.batch)
     inputs_host = workloads.generate(w)
     q, k, v = (inputs_host[n].to(dev) for n in ("q", "k", "v"))
     yb = torch.as_tensor(inputs_host["yat_b"], device=dev)

@@ -14,7 +14,7 @@ namespace {
 
 using namespace cattn;
 
-constexpr int kTile = 128;  // key rows per tile; the key-norm vector is padded to it
+constexpr int kTile = 128;  // the key-norm vector is padded to a multiple of this
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -86,15 +86,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 [BH, T, d] as a 3-D tensor map with 64 x 128 x 1 boxes and 128-byte
+// bf16 [BH, T, d] as a 3-D tensor map with 64 x box_rows x 1 boxes and 128-byte
 // swizzle (the shared-memory layout the tcgen05 descriptors describe).  Rows
 // past T read as zeros.
-int encode_bf16_3d(CUtensorMap *map, const void *base, int d, int T, int BH) {
+int encode_bf16_3d(CUtensorMap *map, const void *base, int d, int T, int BH, int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return CATTN_ERR_CUDA;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -195,8 +195,8 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
   fp.Tk_pad = tk_pad(p);
   fp.causal = p->causal ? 1 : 0;
   fp.scale = p->scale;
-  fp.n_pairs = (p->Tq + 2 * kTile - 1) / (2 * kTile);
-  fp.n_kv_tiles = (p->Tk + kTile - 1) / kTile;
+  fp.n_qtiles = (p->Tq + kTcQueryTile - 1) / kTcQueryTile;
+  fp.n_kv_tiles = (p->Tk + kTcKeyTile - 1) / kTcKeyTile;
 
   if (p->dtype == CATTN_F32) return map_cuda(launch_fwd_simt(variant, p->dk, p->dv, fp, s));
 
@@ -209,9 +209,9 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
     }
   }
   CUtensorMap tq, tk, tv;
-  if ((rc = encode_bf16_3d(&tq, q, p->dk, p->Tq, p->B * p->h)) != CATTN_OK) return rc;
-  if ((rc = encode_bf16_3d(&tk, k, p->dk, p->Tk, p->B * p->hkv)) != CATTN_OK) return rc;
-  if ((rc = encode_bf16_3d(&tv, v, p->dv, p->Tk, p->B * p->hkv)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&tq, q, p->dk, p->Tq, p->B * p->h, kTcQueryTile)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&tk, k, p->dk, p->Tk, p->B * p->hkv, kTcKeyTile)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&tv, v, p->dv, p->Tk, p->B * p->hkv, kTcKeyTile)) != CATTN_OK) return rc;
   return map_cuda(launch_fwd_tc(variant, p->dk, p->dv, fp, tq, tk, tv, s));
 }
 

@@ -1,12 +1,12 @@
 // fwd_tc.cu -- fused attention forward on the sm_103a tensor cores.
 //
-// One CTA owns two 128-row query tiles (Q0, Q1) of one (batch, head) and
-// streams 128-key K/V tiles through shared memory.  Per KV tile j:
+// One CTA owns one 128-row query tile of one (batch, head) and streams
+// 128-key K/V tiles through shared memory.  Per KV tile j:
 //
-//   S_x = Q_x K_j^T          tcgen05.mma (A, B from smem)  -> TMEM, fp32
-//   P_x = map(S_x)           epilogue warpgroup x: tcgen05.ld S, apply the
-//                            score-to-weight map, tcgen05.st P (bf16) over S
-//   O_x += P_x V_j           tcgen05.mma (A = P from TMEM, B = V from smem)
+//   S(j) = Q K_j^T      tcgen05.mma, A and B from shared memory -> TMEM fp32
+//   P(j) = map(S(j))    the eight epilogue warps: tcgen05.ld S, apply the
+//                       score-to-weight map, tcgen05.st P (bf16) to TMEM
+//   O += P(j) V_j       tcgen05.mma, A = P from TMEM, B = V from shared memory
 //
 // The maps ("Softmax-Free Attention in JAX/Flax NNX", section "One module,
 // two compatibility functions"; "s^tau: a focal-length knob for attention",
@@ -21,15 +21,18 @@
 //            running max of tau log2 phi, taken from the max raw score since
 //            phi is increasing.
 //
-// Warp roles (320 threads): warps 0-3 epilogue for Q0, warps 4-7 epilogue
-// for Q1 (one query row per thread = one TMEM lane), warp 8 TMA producer,
-// warp 9 TMEM allocation + MMA issue (lane 0).  K and V tiles share one ring
-// of shared-memory slots guarded by full/empty mbarriers; the squared key
-// norms of the Yat map ride in a small ring of their own.
+// TMEM (512 columns): S buffers [0,128) [128,256) | P buffers [256,320)
+// [320,384) | O [384,512).  S and P are both double buffered and P has its own
+// columns, so the MMA warp issues S(j+2) as soon as the epilogue has loaded
+// S(j), two tiles ahead of PV(j): the tensor cores always have S work queued
+// while the map of tile j runs, and the period per tile is the larger of the
+// tensor time and the map time.
 //
-// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+dv) O1 [384,384+dv).
-// P_x is written over the first 64 columns of S_x; the MMA pipe executes a
-// CTA's MMAs in issue order, so PV_x(j) reads P_x before S_x(j+1) lands.
+// Warp roles (320 threads): warps 0-7 map (warp w: TMEM lanes 32*(w%4)..+31 =
+// those query rows, key columns [64h, 64h+64) with h = w/4), warp 8 issues TMA
+// loads, warp 9 allocates TMEM and issues the MMAs (lane 0).  K and V tiles
+// share one ring of shared-memory slots guarded by full/empty mbarriers; the
+// squared key norms of the Yat map ride in a small ring of their own.
 //
 // Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the kernel
 // records a site code in g_status, raises a CTA-wide abort flag, and all roles
@@ -43,10 +46,26 @@ namespace cattn {
 
 __device__ unsigned int g_status;
 
+#ifdef CATTN_TRACE
+// Optional per-tile clock64 trace of the first CTAs (compiled out by default).
+__device__ unsigned long long g_trace[8][12][160];
+extern "C" int cattn_trace_read(void *host, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(host, g_trace, bytes);
+}
+#define CATTN_TR(ev, j)                                          \
+  do {                                                           \
+    if (tr_slot >= 0 && (j) < 160) g_trace[tr_slot][ev][(j)] = clock64(); \
+  } while (0)
+#else
+#define CATTN_TR(ev, j) \
+  do {                  \
+  } while (0)
+#endif
+
 namespace tc {
 
-constexpr int BM = 128;  // query rows per tile
-constexpr int BN = 128;  // keys per tile
+constexpr int BM = kTcQueryTile;  // 128 query rows per tile
+constexpr int BN = kTcKeyTile;    // 128 keys per tile
 constexpr int NUM_THREADS = 320;
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;
@@ -57,12 +76,17 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 
+// TMEM column map
+constexpr uint32_t TM_S = 0;    // S buffer b at TM_S + 128 b
+constexpr uint32_t TM_P = 256;  // P buffer b at TM_P + 64 b (keys [64h,64h+64) at +32 h)
+constexpr uint32_t TM_O = 384;  // O
+
 // wait-site codes recorded in g_status
 enum : unsigned {
   SITE_PRODUCER = 0x100,
   SITE_MMA = 0x200,
   SITE_EPI = 0x300,
-  SITE_FINAL = 0x400,
+  SITE_ALIGN = 0x400,
 };
 
 template <int DK, int DV>
@@ -70,19 +94,30 @@ struct Layout {
   static constexpr int Q_TILE = BM * DK * 2;
   static constexpr int K_TILE = BN * DK * 2;
   static constexpr int V_TILE = BN * DV * 2;
-  static constexpr int SLOT = K_TILE > V_TILE ? K_TILE : V_TILE;
-  static constexpr int NS = (DK == 64 && DV == 64) ? 6 : 4;
+  // K and V have rings of their own: K(j+2) is loaded while V(j) is still
+  // waiting for its PV, so neither blocks the other.
+  static constexpr int NSK = DK == 64 ? 5 : 3;
+  static constexpr int NSV = (DK == 64 || DV == 64) ? 5 : 3;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_RING = OFF_Q + 2 * Q_TILE;
-  static constexpr int OFF_NK = OFF_RING + NS * SLOT;
-  static constexpr int OFF_BAR = OFF_NK + NKS * BN * 4;
-  // q_full, kv_full[NS], kv_empty[NS], nk_full[NKS], nk_empty[NKS],
-  // s_full[2], p_full[2], o_full[2], drain
-  static constexpr int NBAR = 1 + 2 * NS + 2 * NKS + 7;
+  static constexpr int OFF_K = OFF_Q + Q_TILE;
+  static constexpr int OFF_V = OFF_K + NSK * K_TILE;
+  // aux: the Yat key-norm ring, or the softmax / s^tau row-max exchange
+  // [2 uses][2 halves][BM]; after the last tile both serve the final exchange
+  // of the two halves' partial sums
+  static constexpr int OFF_AUX = OFF_V + NSV * V_TILE;
+  static constexpr int AUX_BYTES = 4 * BM * 4;
+  static constexpr int OFF_BAR = OFF_AUX + AUX_BYTES;
+  // q_full, kf[NSK], ke[NSK], vf[NSV], ve[NSV], nk_full[NKS], nk_empty[NKS],
+  // s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, drain
+  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 2 * NKS + 8 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
-  static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024 B
+  // the dynamic shared memory base is checked to be 1024-byte aligned at run time
+  static constexpr int ALLOC = BYTES;
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
+  static_assert(NKS * BN * 4 <= AUX_BYTES, "key-norm ring fits the aux region");
+  static_assert(K_TILE % 1024 == 0 && V_TILE % 1024 == 0 && Q_TILE % 1024 == 0,
+                "swizzle atoms stay 1024-B aligned");
 };
 
 // Warp-collective bounded wait.  Every lane polls (so every lane acquires the
@@ -93,54 +128,158 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
-    if ((it & 63u) == 0) {
-      const int bad =
-          (honor_abort && *abort != 0) || (globaltimer_ns() - t0 > WAIT_LIMIT_NS);
-      if (__any_sync(FULL, bad)) {
-        if ((threadIdx.x & 31) == 0) {
-          atomicCAS(&g_status, 0u, site | 1u);
-          *abort = 1;
-        }
-        return false;
+    const int bad = (honor_abort && *abort != 0) || (globaltimer_ns() - t0 > WAIT_LIMIT_NS);
+    if (__any_sync(FULL, bad)) {
+      if ((threadIdx.x & 31) == 0) {
+        atomicCAS(&g_status, 0u, site | 1u);
+        *abort = 1;
       }
+      return false;
     }
   }
 }
 
+// S = Q K^T for one 128 x 128 tile: 16-element k steps, 64-column boxes.
 template <int DK>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
   constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, false);
 #pragma unroll
   for (int kk = 0; kk < DK / 16; ++kk) {
-    // 64-column boxes of 128 rows x 128 B; 16-element k steps are 32 B apart
-    const uint32_t off = (uint32_t)(kk >> 2) * (BM * 128) + (uint32_t)(kk & 3) * 32;
-    mma_ss(d_tmem, smem_desc_sw128(q_smem + off, 16, 1024), smem_desc_sw128(k_smem + off, 16, 1024),
-           IDESC, kk > 0 ? 1u : 0u);
+    const uint32_t qa = q_smem + (uint32_t)(kk >> 2) * (BM * 128) + (uint32_t)(kk & 3) * 32;
+    const uint32_t ka = k_smem + (uint32_t)(kk >> 2) * (BN * 128) + (uint32_t)(kk & 3) * 32;
+    mma_ss(d_tmem, smem_desc_sw128(qa, 16, 1024), smem_desc_sw128(ka, 16, 1024), IDESC,
+           kk > 0 ? 1u : 0u);
   }
 }
 
+// O += P V for one 128-key tile; P (bf16 pairs) in 64 TMEM columns (keys
+// [64h, 64h+64) at columns [32h, 32h+32)), V N-major with its 64-wide dv boxes
+// BN*128 bytes apart.
 template <int DV>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
                                          bool accumulate) {
   constexpr uint32_t IDESC = idesc_bf16_f32(BM, DV, true);
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk) {
-    // V is N-major: 16 keys = 16 rows of 128 B; 64-wide dv boxes are BN*128 B apart
-    mma_ts(d_tmem, p_tmem + (uint32_t)kk * 8, smem_desc_sw128(v_smem + (uint32_t)kk * 2048, BN * 128, 1024),
-           IDESC, (accumulate || kk > 0) ? 1u : 0u);
+    mma_ts(d_tmem, p_tmem + (uint32_t)kk * 8,
+           smem_desc_sw128(v_smem + (uint32_t)kk * 2048, BN * 128, 1024), IDESC,
+           (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
+// Multiply dv/2 columns of this thread's row of O by f in place.
 template <int DV>
-__device__ __forceinline__ void scale_o_tmem(uint32_t t_o, float f) {
+__device__ __forceinline__ void scale_o_half(uint32_t t_o, float f) {
 #pragma unroll
-  for (int c = 0; c < DV / 32; ++c) {
+  for (int c = 0; c < DV / 64; ++c) {
     uint32_t r[32];
     tmem_ld32(t_o + c * 32, r);
     tmem_wait_ld();
+    tmem_ld_fence(r);
 #pragma unroll
     for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
     tmem_st32(t_o + c * 32, r);
+  }
+}
+
+__device__ __forceinline__ float2 f2(uint32_t a, uint32_t b) {
+  return make_float2(__uint_as_float(a), __uint_as_float(b));
+}
+
+// Yat map over one 32-key chunk (columns 32c .. 32c+31 of the tile) of one row.  sr: raw
+// dots; nk2: squared key norms of the tile (pairs); qe = |q|^2 + eps.
+// kappa = (dot + b)^2 / max(|q|^2 + |k|^2 - 2 dot + eps, eps); masked keys
+// (col >= limit) get kappa = 0.
+template <bool PARTIAL>
+__device__ __forceinline__ void yat_chunk(const uint32_t (&sr)[32], int c, const float2 *nk2,
+                                          float yb, float qe, float yeps, int limit,
+                                          float2 (&mass)[2], float (&top)[2],
+                                          uint32_t (&pk)[16]) {
+  const float2 b2 = make_float2(yb, yb), qe2 = make_float2(qe, qe);
+  const float2 m2 = make_float2(-2.f, -2.f);
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const int col = c * 32 + i;
+    const int chain = (i >> 1) & 1;
+    const float2 d = f2(sr[i], sr[i + 1]);
+    const float2 t = __fadd2_rn(d, b2);
+    const float2 num = __fmul2_rn(t, t);
+    const float2 den = __ffma2_rn(m2, d, __fadd2_rn(qe2, nk2[col >> 1]));
+    const float2 r = make_float2(rcp_approx(fmaxf(den.x, yeps)), rcp_approx(fmaxf(den.y, yeps)));
+    float2 k = __fmul2_rn(num, r);
+    if (PARTIAL) {
+      k.x = col < limit ? k.x : 0.f;
+      k.y = col + 1 < limit ? k.y : 0.f;
+    }
+    mass[chain] = __fadd2_rn(mass[chain], k);
+    top[chain] = max3(top[chain], k.x, k.y);
+    pk[i >> 1] = pack_bf16x2(k.x, k.y);
+  }
+}
+
+// Max of the raw dot over the allowed keys of one 32-key chunk (masked -> -inf).
+template <bool PARTIAL>
+__device__ __forceinline__ float chunk_max(const uint32_t (&sr)[32], int c, int limit) {
+  float m[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const int col = c * 32 + i;
+    float x0 = __uint_as_float(sr[i]), x1 = __uint_as_float(sr[i + 1]);
+    if (PARTIAL) {
+      x0 = col < limit ? x0 : -INFINITY;
+      x1 = col + 1 < limit ? x1 : -INFINITY;
+    }
+    m[(i >> 1) & 1] = max3(m[(i >> 1) & 1], x0, x1);
+  }
+  return fmaxf(m[0], m[1]);
+}
+
+// softmax over one 32-key chunk: p = 2^(dot * c2 - m), c2 = scale * log2(e).
+template <bool PARTIAL>
+__device__ __forceinline__ void softmax_chunk(const uint32_t (&sr)[32], int c, float c2,
+                                              float neg_m, int limit, float2 (&l)[2],
+                                              uint32_t (&pk)[16]) {
+  const float2 c22 = make_float2(c2, c2), nm2 = make_float2(neg_m, neg_m);
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const int col = c * 32 + i;
+    const float2 x = __ffma2_rn(f2(sr[i], sr[i + 1]), c22, nm2);
+    float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    if (PARTIAL) {
+      pr.x = col < limit ? pr.x : 0.f;
+      pr.y = col + 1 < limit ? pr.y : 0.f;
+    }
+    l[(i >> 1) & 1] = __fadd2_rn(l[(i >> 1) & 1], pr);
+    pk[i >> 1] = pack_bf16x2(pr.x, pr.y);
+  }
+}
+
+// log2(softplus(s) + eps), softplus(s) = max(s, 0) + ln(1 + 2^(-|s| log2 e)).
+__device__ __forceinline__ float log2_phi(float s, float abs_s_log2e, float eps) {
+  constexpr float LN2 = 0.6931471805599453f;
+  const float e = ex2_approx(-abs_s_log2e);
+  const float l1p = e < 0x1p-12f ? e : lg2_approx(1.f + e) * LN2;
+  return lg2_approx(fmaxf(s, 0.f) + l1p + eps);
+}
+
+// s^tau over one 32-key chunk: p = 2^(tau log2 phi(s) - m).
+template <bool PARTIAL>
+__device__ __forceinline__ void stau_chunk(const uint32_t (&sr)[32], int c, float scale, float c2,
+                                           float tau, float eps, float neg_m, int limit,
+                                           float2 (&l)[2], uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const int col = c * 32 + i;
+    const float d0 = __uint_as_float(sr[i]), d1 = __uint_as_float(sr[i + 1]);
+    const float g0 = log2_phi(d0 * scale, fabsf(d0) * c2, eps);
+    const float g1 = log2_phi(d1 * scale, fabsf(d1) * c2, eps);
+    float2 pr = make_float2(ex2_approx(fmaf(tau, g0, neg_m)), ex2_approx(fmaf(tau, g1, neg_m)));
+    if (PARTIAL) {
+      pr.x = col < limit ? pr.x : 0.f;
+      pr.y = col + 1 < limit ? pr.y : 0.f;
+    }
+    l[(i >> 1) & 1] = __fadd2_rn(l[(i >> 1) & 1], pr);
+    pk[i >> 1] = pack_bf16x2(pr.x, pr.y);
   }
 }
 
@@ -149,65 +288,82 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using L = Layout<DK, DV>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_s = smem_u32(smem_raw);
-  uint8_t *smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sb = smem_u32(smem);
+  if (sb & 1023u) {  // the 128-byte swizzle needs 1024-byte aligned tiles
+    if (threadIdx.x == 0) atomicCAS(&g_status, 0u, SITE_ALIGN);
+    return;
+  }
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   const uint32_t bar0 = sb + L::OFF_BAR;
   const uint32_t bar_q = bar0;
-  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (1 + L::NS + s); };
-  auto nk_full = [&](int s) { return bar0 + 8u * (1 + 2 * L::NS + s); };
-  auto nk_empty = [&](int s) { return bar0 + 8u * (1 + 2 * L::NS + NKS + s); };
-  auto s_full = [&](int x) { return bar0 + 8u * (1 + 2 * L::NS + 2 * NKS + x); };
-  auto p_full = [&](int x) { return bar0 + 8u * (3 + 2 * L::NS + 2 * NKS + x); };
-  auto o_full = [&](int x) { return bar0 + 8u * (5 + 2 * L::NS + 2 * NKS + x); };
-  const uint32_t bar_drain = bar0 + 8u * (7 + 2 * L::NS + 2 * NKS);
-  auto q_smem = [&](int x) { return sb + L::OFF_Q + (uint32_t)x * L::Q_TILE; };
-  auto slot_smem = [&](int s) { return sb + L::OFF_RING + (uint32_t)s * L::SLOT; };
-  const float *nk_ring = reinterpret_cast<const float *>(smem + L::OFF_NK);
+  auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto k_empty = [&](int s) { return bar0 + 8u * (1 + L::NSK + s); };
+  auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * L::NSK + s); };
+  auto v_empty = [&](int s) { return bar0 + 8u * (1 + 2 * L::NSK + L::NSV + s); };
+  constexpr int B1 = 1 + 2 * L::NSK + 2 * L::NSV;
+  auto nk_full = [&](int s) { return bar0 + 8u * (B1 + s); };
+  auto nk_empty = [&](int s) { return bar0 + 8u * (B1 + NKS + s); };
+  constexpr int B2 = B1 + 2 * NKS;
+  auto s_full = [&](int b) { return bar0 + 8u * (B2 + b); };
+  auto s_empty = [&](int b) { return bar0 + 8u * (B2 + 2 + b); };
+  auto p_full = [&](int b) { return bar0 + 8u * (B2 + 4 + b); };
+  auto p_empty = [&](int b) { return bar0 + 8u * (B2 + 6 + b); };
+  const uint32_t bar_o = bar0 + 8u * (B2 + 8);
+  const uint32_t bar_drain = bar0 + 8u * (B2 + 9);
+  const uint32_t q_smem = sb + L::OFF_Q;
+  auto k_smem = [&](int s) { return sb + L::OFF_K + (uint32_t)s * L::K_TILE; };
+  auto v_smem = [&](int s) { return sb + L::OFF_V + (uint32_t)s * L::V_TILE; };
+  const float *nk_ring = reinterpret_cast<const float *>(smem + L::OFF_AUX);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
 
-  // ---- work unit: (query-tile pair, batch, head); causal pairs heaviest first
-  const int BH = p.B * p.h;
-  int pair = blockIdx.x / BH;
-  const int bh = blockIdx.x - pair * BH;
-  if (p.causal) pair = p.n_pairs - 1 - pair;
+  // ---- work unit: (batch, head, query tile).  The tiles of one head are
+  // consecutive, so its K/V stays in L2 while they run; causal tiles go
+  // heaviest first.
+  const int bh = blockIdx.x / p.n_qtiles;
+  int qt = blockIdx.x - bh * p.n_qtiles;
+  if (p.causal) qt = p.n_qtiles - 1 - qt;
   const int head = bh % p.h;
   const int batch = bh / p.h;
   const int bh_kv = batch * p.hkv + head / (p.h / p.hkv);
-  const int q0 = pair * 2 * BM;
-  const bool q1_valid = (q0 + BM) < p.Tq;
-  int nkv0, nkv1;
-  if (p.causal) {
-    nkv0 = min(2 * pair + 1, p.n_kv_tiles);
-    nkv1 = q1_valid ? min(2 * pair + 2, p.n_kv_tiles) : 0;
-  } else {
-    nkv0 = p.n_kv_tiles;
-    nkv1 = q1_valid ? p.n_kv_tiles : 0;
-  }
-  const int nkv = max(nkv0, nkv1);
+  const int q0 = qt * BM;
+  // causal: keys 0 .. last row of the tile
+  const int nkv = p.causal ? min(qt + 1, p.n_kv_tiles) : p.n_kv_tiles;
+  // The query tiles of one head run side by side; each walks its key tiles
+  // from its own starting point (then wraps), so they do not all request the
+  // same K/V tile at the same moment.  Every map is order independent.
+  const int rot = (qt * 7) % nkv;
+  auto kv_tile = [&](int j) { return j + rot < nkv ? j + rot : j + rot - nkv; };
+#ifdef CATTN_TRACE
+  const int tr_slot =
+      (blockIdx.x % p.n_qtiles == 0 && (int)(blockIdx.x / p.n_qtiles) < 8) ? (int)(blockIdx.x / p.n_qtiles) : -1;
+#endif
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int s = 0; s < L::NS; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+    for (int s = 0; s < L::NSK; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+    }
+    for (int s = 0; s < L::NSV; ++s) {
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
     }
     for (int s = 0; s < NKS; ++s) {
       mbar_init(nk_full(s), 1);
       mbar_init(nk_empty(s), 1);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(s_full(x), 1);
-      mbar_init(p_full(x), BM);
-      mbar_init(o_full(x), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(s_empty(b), 8 * 32);  // every epilogue thread has loaded its part of S
+      mbar_init(p_full(b), 8 * 32);   // every epilogue thread has stored its part of P
+      mbar_init(p_empty(b), 1);
     }
+    mbar_init(bar_o, 1);
     mbar_init(bar_drain, 1);
     *abort = 0;
     fence_mbar_init();
@@ -228,112 +384,94 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
+    // load order K0 K1 | K(j+2) V(j) for j = 0.. : the order the MMAs consume
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar_q, (q1_valid ? 2u : 1u) * (uint32_t)L::Q_TILE);
+      mbar_arrive_expect_tx(bar_q, (uint32_t)L::Q_TILE);
 #pragma unroll
-      for (int c = 0; c < DK / 64; ++c) {
-        tma_load_3d(q_smem(0) + c * BM * 128, &tm_q, c * 64, q0, bh, bar_q);
-        if (q1_valid) tma_load_3d(q_smem(1) + c * BM * 128, &tm_q, c * 64, q0 + BM, bh, bar_q);
-      }
+      for (int c = 0; c < DK / 64; ++c) tma_load_3d(q_smem + c * BM * 128, &tm_q, c * 64, q0, bh, bar_q);
     }
     __syncwarp();
-    for (int j = 0; j < nkv; ++j) {
-      {  // K_j
-        const int idx = 2 * j, s = idx % L::NS;
-        const uint32_t use = (uint32_t)(idx / L::NS);
-        if (!warp_wait(kv_empty(s), (use & 1u) ^ 1u, abort, SITE_PRODUCER | 0x10)) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(kv_full(s), L::K_TILE);
+    auto load_k = [&](int t) -> bool {
+      const int s = t % L::NSK;
+      const uint32_t use = (uint32_t)(t / L::NSK);
+      if (!warp_wait(k_empty(s), (use & 1u) ^ 1u, abort, SITE_PRODUCER | 0x10)) return false;
+      if (lane == 0) CATTN_TR(9, t);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(k_full(s), L::K_TILE);
 #pragma unroll
-          for (int c = 0; c < DK / 64; ++c)
-            tma_load_3d(slot_smem(s) + c * BN * 128, &tm_k, c * 64, j * BN, bh_kv, kv_full(s));
+        for (int c = 0; c < DK / 64; ++c)
+          tma_load_3d(k_smem(s) + c * BN * 128, &tm_k, c * 64, kv_tile(t) * BN, bh_kv, k_full(s));
+      }
+      __syncwarp();
+      if (VARIANT == kYat) {  // squared key norms of tile t
+        const int ns = t % NKS;
+        const uint32_t nuse = (uint32_t)(t / NKS);
+        if (!warp_wait(nk_empty(ns), (nuse & 1u) ^ 1u, abort, SITE_PRODUCER | 0x20)) return false;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(nk_full(ns), BN * 4);
+          bulk_load(sb + L::OFF_AUX + (uint32_t)ns * BN * 4,
+                    p.nk + (size_t)bh_kv * p.Tk_pad + (size_t)kv_tile(t) * BN, BN * 4, nk_full(ns));
         }
         __syncwarp();
       }
-      if (VARIANT == kYat) {  // squared key norms of tile j
-        const int s = j % NKS;
-        const uint32_t use = (uint32_t)(j / NKS);
-        if (!warp_wait(nk_empty(s), (use & 1u) ^ 1u, abort, SITE_PRODUCER | 0x20)) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(nk_full(s), BN * 4);
-          bulk_load(sb + L::OFF_NK + (uint32_t)s * BN * 4,
-                    p.nk + (size_t)bh_kv * p.Tk_pad + (size_t)j * BN, BN * 4, nk_full(s));
-        }
-        __syncwarp();
-      }
-      {  // V_j
-        const int idx = 2 * j + 1, s = idx % L::NS;
-        const uint32_t use = (uint32_t)(idx / L::NS);
-        if (!warp_wait(kv_empty(s), (use & 1u) ^ 1u, abort, SITE_PRODUCER | 0x30)) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(kv_full(s), L::V_TILE);
+      return true;
+    };
+    bool ok = true;
+    if (nkv > 0) ok = load_k(0);
+    if (ok && nkv > 1) ok = load_k(1);
+    for (int j = 0; ok && j < nkv; ++j) {
+      if (j + 2 < nkv && !(ok = load_k(j + 2))) break;
+      const int s = j % L::NSV;
+      const uint32_t use = (uint32_t)(j / L::NSV);
+      if (!(ok = warp_wait(v_empty(s), (use & 1u) ^ 1u, abort, SITE_PRODUCER | 0x30))) break;
+      if (lane == 0) CATTN_TR(10, j);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(v_full(s), L::V_TILE);
 #pragma unroll
-          for (int c = 0; c < DV / 64; ++c)
-            tma_load_3d(slot_smem(s) + c * BN * 128, &tm_v, c * 64, j * BN, bh_kv, kv_full(s));
-        }
-        __syncwarp();
+        for (int c = 0; c < DV / 64; ++c)
+          tma_load_3d(v_smem(s) + c * BN * 128, &tm_v, c * 64, kv_tile(j) * BN, bh_kv, v_full(s));
       }
+      __syncwarp();
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issue
+    // S(0), S(1) up front; then step j issues S(j+2) (once the epilogue has
+    // loaded S(j) out of its buffer) followed by PV(j).
     bool ok = warp_wait(bar_q, 0, abort, SITE_MMA | 0x10);
     tc_fence_after();
-    uint32_t pph0 = 0, pph1 = 0;
-    const int release_limit = 2 * nkv - L::NS;  // later slots are never reloaded
-    for (int j = 0; ok && j <= nkv; ++j) {
-      const int vidx = 2 * (j - 1) + 1;
-      const int vs = j >= 1 ? vidx % L::NS : 0;
-      if (j >= 1) {
-        if (!(ok = warp_wait(kv_full(vs), (uint32_t)(vidx / L::NS) & 1u, abort, SITE_MMA | 0x20)))
-          break;
-        tc_fence_after();
-      }
-      if (j >= 1 && j - 1 < nkv0) {  // O0 += P0(j-1) V(j-1)
-        if (!(ok = warp_wait(p_full(0), pph0, abort, SITE_MMA | 0x30))) break;
-        pph0 ^= 1u;
-        tc_fence_after();
-        if (lane == 0) {
-          issue_pv<DV>(tmem + 256, tmem + 0, slot_smem(vs), j - 1 > 0);
-          if (j - 1 == nkv0 - 1) mma_commit(o_full(0));
-        }
-        __syncwarp();
-      }
-      const int kidx = 2 * j;
-      const int ks = kidx % L::NS;
-      if (j < nkv) {
-        if (!(ok = warp_wait(kv_full(ks), (uint32_t)(kidx / L::NS) & 1u, abort, SITE_MMA | 0x40)))
-          break;
-        tc_fence_after();
-      }
-      if (j < nkv0) {  // S0 = Q0 K(j)^T
-        if (lane == 0) {
-          issue_qk<DK>(tmem + 0, q_smem(0), slot_smem(ks));
-          mma_commit(s_full(0));
-        }
-        __syncwarp();
-      }
-      if (j >= 1 && j - 1 < nkv1) {  // O1 += P1(j-1) V(j-1)
-        if (!(ok = warp_wait(p_full(1), pph1, abort, SITE_MMA | 0x50))) break;
-        pph1 ^= 1u;
-        tc_fence_after();
-        if (lane == 0) {
-          issue_pv<DV>(tmem + 384, tmem + 128, slot_smem(vs), j - 1 > 0);
-          if (j - 1 == nkv1 - 1) mma_commit(o_full(1));
-        }
-        __syncwarp();
-      }
-      if (j < nkv1) {  // S1 = Q1 K(j)^T
-        if (lane == 0) {
-          issue_qk<DK>(tmem + 128, q_smem(1), slot_smem(ks));
-          mma_commit(s_full(1));
-        }
-        __syncwarp();
-      }
+    auto issue_s = [&](int t) -> bool {
+      const int ks = t % L::NSK, b = t & 1;
+      if (!warp_wait(k_full(ks), (uint32_t)(t / L::NSK) & 1u, abort, SITE_MMA | 0x20)) return false;
+      CATTN_TR(7, t);
+      if (t >= 2 && !warp_wait(s_empty(b), (uint32_t)((t >> 1) - 1) & 1u, abort, SITE_MMA | 0x30))
+        return false;
+      tc_fence_after();
+      CATTN_TR(8, t);
       if (lane == 0) {
-        if (j < nkv && kidx < release_limit) mma_commit(kv_empty(ks));
-        if (j >= 1 && vidx < release_limit) mma_commit(kv_empty(vs));
-        // both epilogues delivered P for tile j-1, so they are done with its key norms
-        if (VARIANT == kYat && j >= 1) mbar_arrive(nk_empty((j - 1) % NKS));
+        issue_qk<DK>(tmem + TM_S + 128u * b, q_smem, k_smem(ks));
+        mma_commit(s_full(b));
+        if (t + L::NSK < nkv) mma_commit(k_empty(ks));  // only slots that are reloaded
+      }
+      __syncwarp();
+      return true;
+    };
+    if (ok && nkv > 0) ok = issue_s(0);
+    if (ok && nkv > 1) ok = issue_s(1);
+    for (int j = 0; ok && j < nkv; ++j) {
+      if (j + 2 < nkv && !(ok = issue_s(j + 2))) break;
+      const int vs = j % L::NSV, b = j & 1;
+      if (!(ok = warp_wait(v_full(vs), (uint32_t)(j / L::NSV) & 1u, abort, SITE_MMA | 0x40))) break;
+      CATTN_TR(11, j);
+      if (!(ok = warp_wait(p_full(b), (uint32_t)(j >> 1) & 1u, abort, SITE_MMA | 0x50))) break;
+      CATTN_TR(6, j);
+      tc_fence_after();
+      if (lane == 0) {
+        issue_pv<DV>(tmem + TM_O, tmem + TM_P + 64u * b, v_smem(vs), j > 0);
+        mma_commit(p_empty(b));
+        if (j == nkv - 1) mma_commit(bar_o);
+        if (j + L::NSV < nkv) mma_commit(v_empty(vs));
+        // every epilogue thread delivered P(j), so all are done with its key norms
+        if (VARIANT == kYat) mbar_arrive(nk_empty(j % NKS));
       }
       __syncwarp();
     }
@@ -342,164 +480,175 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) mma_commit(bar_drain);
     __syncwarp();
     warp_wait(bar_drain, 0, abort, SITE_MMA | 0x60, false);
-  } else {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ epilogue
-    const int x = warp >> 2;  // query tile of this warpgroup
     const int quarter = warp & 3;
+    const int half = warp >> 2;
     const int r = quarter * 32 + lane;  // row in tile == TMEM lane
-    const int nkv_x = x ? nkv1 : nkv0;
-    if (nkv_x > 0) {
-      const int qrow0 = q0 + x * BM;
-      const int row = qrow0 + r;
-      const int qt = qrow0 / BM;
-      const bool row_ok = row < p.Tq;
-      const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-      const uint32_t t_s = tmem + lane_off + (uint32_t)x * 128;
-      const uint32_t t_o = tmem + lane_off + 256u + (uint32_t)x * 128;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t t_o = tmem + lane_off + TM_O + (uint32_t)half * (DV / 2);
+    const uint32_t named_bar = 1u + (uint32_t)quarter;  // pairs warps w and w^4
+    float *xchg = reinterpret_cast<float *>(smem + L::OFF_AUX);
+    const int row = q0 + r;
+    const bool row_ok = row < p.Tq;
 
-      // per-row state
-      float acc_a = 0.f, acc_b = 0.f;  // Yat: row mass (two partial sums); else l
-      float row_top = -INFINITY;       // Yat: max kappa; else max scaled score
-      float m_used = -INFINITY;        // softmax / s^tau: running max, log2 units
-      float yb = 0.f, yeps = 0.f, qe = 0.f, tau = 1.f, seps = 0.f;
+    float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // Yat: mass; else l
+    float top[2] = {-INFINITY, -INFINITY};  // Yat: max kappa; else max raw dot
+    float m_used = -INFINITY;               // softmax / s^tau: running max, log2 units
+    float yb = 0.f, yeps = 0.f, qe = 0.f, tau = 1.f, seps = 0.f;
+    if (VARIANT == kYat) {
+      yb = p.b[head];
+      yeps = p.eps[head];
+      qe = (row_ok ? p.nq[(size_t)bh * p.Tq + row] : 0.f) + yeps;
+    } else if (VARIANT == kStau) {
+      tau = p.tau[head];
+      seps = p.eps[head];
+    }
+    const float c2 = p.scale * LOG2E;  // scaled score in log2 units per raw dot
+    uint32_t xpar = 0;
+
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      const int b = j & 1;
+      const uint32_t t_s = tmem + lane_off + TM_S + 128u * b + 64u * half;
+      if (!(ok = warp_wait(s_full(b), (uint32_t)(j >> 1) & 1u, abort, SITE_EPI | 0x10))) break;
+      if (threadIdx.x == 0) CATTN_TR(0, j);
+      tc_fence_after();
+      uint32_t sr[2][32];
+      tmem_ld32(t_s, sr[0]);
+      tmem_ld32(t_s + 32, sr[1]);
+      const float2 *nk2 = nullptr;
       if (VARIANT == kYat) {
-        yb = p.b[head];
-        yeps = p.eps[head];
-        const float nq = row_ok ? p.nq[(size_t)bh * p.Tq + row] : 0.f;
-        qe = nq + yeps;
-      } else if (VARIANT == kStau) {
-        tau = p.tau[head];
-        seps = p.eps[head];
+        const int ns = j % NKS;
+        if (!(ok = warp_wait(nk_full(ns), (uint32_t)(j / NKS) & 1u, abort, SITE_EPI | 0x20))) break;
+        nk2 = reinterpret_cast<const float2 *>(nk_ring + ns * BN);
       }
-      const float c2 = p.scale * LOG2E;  // scaled score in log2 units per raw dot
+      tmem_wait_ld();
+      tmem_ld_fence(sr[0]);
+      tmem_ld_fence(sr[1]);
+      // S(j) is in registers: the tensor cores may overwrite its buffer
+      tc_fence_before();
+      mbar_arrive(s_empty(b));
+      if (threadIdx.x == 0) CATTN_TR(1, j);
 
-      uint32_t sph = 0;
-      bool ok = true;
-      for (int j = 0; j < nkv_x; ++j) {
-        if (!(ok = warp_wait(s_full(x), sph, abort, SITE_EPI | 0x10))) break;
-        sph ^= 1u;
-        tc_fence_after();
-        uint32_t sr[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(t_s + c * 32, sr[c]);
-        tmem_wait_ld();
+      // keys j*BN + col allowed for col < limit (col counts the whole tile)
+      int limit = BN;
+      const int jt = kv_tile(j);
+      if (jt == p.n_kv_tiles - 1) limit = min(limit, p.Tk - jt * BN);
+      if (p.causal) limit = min(limit, row + 1 - jt * BN);
+      const bool partial = __any_sync(FULL, limit < BN);  // warp-uniform path choice
 
-        int limit = BN;
-        if (j == p.n_kv_tiles - 1) limit = min(limit, p.Tk - j * BN);
-        if (p.causal && j == qt) limit = min(limit, r + 1);
-        const bool partial = limit < BN;
-
-        uint32_t pk[2][32];  // P as bf16 pairs: columns [0,32) and [32,64)
-        if (VARIANT == kYat) {
-          const int ns = j % NKS;
-          if (!(ok = warp_wait(nk_full(ns), (uint32_t)(j / NKS) & 1u, abort, SITE_EPI | 0x20)))
-            break;
-          const float2 *nk2 = reinterpret_cast<const float2 *>(nk_ring + ns * BN);
-          float top = row_top;
+      uint32_t pk[32];  // P as bf16 pairs, this warp's 32 TMEM columns
+      if (VARIANT == kYat) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
+          uint32_t hk[16];
+          if (partial)
+            yat_chunk<true>(sr[c], half * 2 + c, nk2, yb, qe, yeps, limit, acc, top, hk);
+          else
+            yat_chunk<false>(sr[c], half * 2 + c, nk2, yb, qe, yeps, limit, acc, top, hk);
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const int col = c * 32 + i;
-              const float2 nkv = nk2[col >> 1];
-              const float d0 = __uint_as_float(sr[c][i]);
-              const float d1 = __uint_as_float(sr[c][i + 1]);
-              const float t0 = d0 + yb, t1 = d1 + yb;
-              const float den0 = fmaxf(fmaf(-2.f, d0, qe + nkv.x), yeps);
-              const float den1 = fmaxf(fmaf(-2.f, d1, qe + nkv.y), yeps);
-              float k0 = t0 * t0 * rcp_approx(den0);
-              float k1 = t1 * t1 * rcp_approx(den1);
-              if (partial) {
-                k0 = col < limit ? k0 : 0.f;
-                k1 = col + 1 < limit ? k1 : 0.f;
-              }
-              acc_a += k0;
-              acc_b += k1;
-              top = fmaxf(top, fmaxf(k0, k1));
-              pk[c >> 1][(c & 1) * 16 + (i >> 1)] = pack_bf16x2(k0, k1);
-            }
-          }
-          row_top = top;
-        } else {
-          // max of the raw dot over allowed keys (scale > 0 keeps the order)
-          float mt = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float d = __uint_as_float(sr[c][i]);
-              if (!partial || c * 32 + i < limit) mt = fmaxf(mt, d);
-            }
-          const float s_top = mt * p.scale;
-          row_top = fmaxf(row_top, s_top);
-          float m_new;
-          if (VARIANT == kSoftmax) {
+          for (int i = 0; i < 16; ++i) pk[c * 16 + i] = hk[i];
+        }
+      } else {
+        float mt = partial ? fmaxf(chunk_max<true>(sr[0], half * 2, limit),
+                                   chunk_max<true>(sr[1], half * 2 + 1, limit))
+                           : fmaxf(chunk_max<false>(sr[0], half * 2, limit),
+                                   chunk_max<false>(sr[1], half * 2 + 1, limit));
+        // the row max over the whole tile: swap halves with the partner warp
+        float *xb = xchg + xpar * 2 * BM;
+        xb[half * BM + r] = mt;
+        named_barrier_sync(named_bar, 64);
+        mt = fmaxf(mt, xb[(half ^ 1) * BM + r]);
+        xpar ^= 1u;
+        top[0] = fmaxf(top[0], mt);
+        float m_new = -INFINITY;
+        if (mt > -INFINITY) {
+          if (VARIANT == kSoftmax)
             m_new = mt * c2;
-          } else {
-            const float e = ex2_approx(-fabsf(s_top) * LOG2E);
-            const float l1p = e < 0x1p-12f ? e : lg2_approx(1.f + e) * LN2;
-            m_new = tau * lg2_approx(fmaxf(s_top, 0.f) + l1p + seps);
-          }
-          if (__any_sync(FULL, m_new > m_used + RESCALE_THRESHOLD)) {
-            const float mn = fmaxf(m_used, m_new);
-            const float corr = ex2_approx(m_used - mn);
-            acc_a *= corr;
-            acc_b *= corr;
-            if (j > 0) scale_o_tmem<DV>(t_o, corr);
-            m_used = mn;
-          }
-          const float neg_m = -m_used;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const int col = c * 32 + i;
-              const float d0 = __uint_as_float(sr[c][i]);
-              const float d1 = __uint_as_float(sr[c][i + 1]);
-              float p0, p1;
-              if (VARIANT == kSoftmax) {
-                p0 = ex2_approx(fmaf(d0, c2, neg_m));
-                p1 = ex2_approx(fmaf(d1, c2, neg_m));
-              } else {
-                const float s0 = d0 * p.scale, s1 = d1 * p.scale;
-                const float e0 = ex2_approx(-fabsf(d0) * c2);
-                const float e1 = ex2_approx(-fabsf(d1) * c2);
-                const float l0 = e0 < 0x1p-12f ? e0 : lg2_approx(1.f + e0) * LN2;
-                const float l1 = e1 < 0x1p-12f ? e1 : lg2_approx(1.f + e1) * LN2;
-                const float g0 = lg2_approx(fmaxf(s0, 0.f) + l0 + seps);
-                const float g1 = lg2_approx(fmaxf(s1, 0.f) + l1 + seps);
-                p0 = ex2_approx(fmaf(tau, g0, neg_m));
-                p1 = ex2_approx(fmaf(tau, g1, neg_m));
-              }
-              if (partial) {
-                p0 = col < limit ? p0 : 0.f;
-                p1 = col + 1 < limit ? p1 : 0.f;
-              }
-              acc_a += p0;
-              acc_b += p1;
-              pk[c >> 1][(c & 1) * 16 + (i >> 1)] = pack_bf16x2(p0, p1);
-            }
+          else
+            m_new = tau * log2_phi(mt * p.scale, fabsf(mt) * c2, seps);
+        }
+        if (__any_sync(FULL, m_new > m_used + RESCALE_THRESHOLD)) {
+          const float mn = fmaxf(m_used, m_new);
+          const float corr = ex2_approx(m_used - mn);
+          acc[0].x *= corr;
+          acc[0].y *= corr;
+          acc[1].x *= corr;
+          acc[1].y *= corr;
+          m_used = mn;
+          if (j > 0) {
+            // O must hold every tile before j: wait for PV(j-1), then rescale
+            if (!(ok = warp_wait(p_empty((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, abort,
+                                 SITE_EPI | 0x40)))
+              break;
+            tc_fence_after();
+            scale_o_half<DV>(t_o, corr);
           }
         }
-        // P (bf16 pairs) over the first 64 columns of S_x
-        tmem_st32(t_s + 0, pk[0]);
-        tmem_st32(t_s + 32, pk[1]);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(p_full(x));
-      }
-
-      if (ok && warp_wait(o_full(x), 0, abort, SITE_EPI | 0x30)) {
-        tc_fence_after();
-        const float total = acc_a + acc_b;
-        const float inv = VARIANT == kYat ? 1.f / (total + 1e-9f) : 1.f / total;
-        __nv_bfloat16 *orow =
-            reinterpret_cast<__nv_bfloat16 *>(p.out) + ((size_t)bh * p.Tq + row) * DV;
 #pragma unroll
-        for (int c = 0; c < DV / 32; ++c) {
+        for (int c = 0; c < 2; ++c) {
+          uint32_t hk[16];
+          if (VARIANT == kSoftmax) {
+            if (partial)
+              softmax_chunk<true>(sr[c], half * 2 + c, c2, -m_used, limit, acc, hk);
+            else
+              softmax_chunk<false>(sr[c], half * 2 + c, c2, -m_used, limit, acc, hk);
+          } else {
+            if (partial)
+              stau_chunk<true>(sr[c], half * 2 + c, p.scale, c2, tau, seps, -m_used, limit, acc, hk);
+            else
+              stau_chunk<false>(sr[c], half * 2 + c, p.scale, c2, tau, seps, -m_used, limit, acc, hk);
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[c * 16 + i] = hk[i];
+        }
+      }
+      // P buffer b is free once PV(j-2) has completed
+      if (!(ok = warp_wait(p_empty(b), ((uint32_t)(j >> 1) & 1u) ^ 1u, abort, SITE_EPI | 0x50)))
+        break;
+      tc_fence_after();
+      tmem_st32(tmem + lane_off + TM_P + 64u * b + 32u * half, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full(b));
+      if (threadIdx.x == 0) CATTN_TR(2, j);
+    }
+
+    // ---- finalise: combine the two halves of the row, normalise, store
+    if (ok) {
+      const float part = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+      float total, all_top;
+      float *fb = xchg;
+      if (VARIANT == kYat) {
+        // the aux region held the key norms: wait until all eight epilogue warps
+        // are past their last read of it
+        named_barrier_sync(5, 8 * 32);
+        fb[(0 * 2 + half) * BM + r] = part;
+        fb[(1 * 2 + half) * BM + r] = fmaxf(top[0], top[1]);
+        named_barrier_sync(named_bar, 64);
+        total = part + fb[(0 * 2 + (half ^ 1)) * BM + r];
+        all_top = fmaxf(fmaxf(top[0], top[1]), fb[(1 * 2 + (half ^ 1)) * BM + r]);
+      } else {
+        // the row max was already shared tile by tile; swap the partial sums in
+        // the exchange buffer the last tile did not use
+        fb = xchg + xpar * 2 * BM;
+        fb[half * BM + r] = part;
+        named_barrier_sync(named_bar, 64);
+        total = part + fb[(half ^ 1) * BM + r];
+        all_top = top[0];
+      }
+      if (warp_wait(bar_o, 0, abort, SITE_EPI | 0x30)) {
+        tc_fence_after();
+        const float inv = VARIANT == kYat ? 1.f / (total + 1e-9f) : 1.f / total;
+        __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
+                              ((size_t)bh * p.Tq + row) * DV + half * (DV / 2);
+#pragma unroll
+        for (int c = 0; c < DV / 64; ++c) {
           uint32_t o[32];
           tmem_ld32(t_o + c * 32, o);
           tmem_wait_ld();
+          tmem_ld_fence(o);
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -513,11 +662,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                   packed[4 * i + 3]);
           }
         }
-        if (row_ok) {
+        if (row_ok && half == 0) {
           const size_t ti = (size_t)bh * p.Tq + row;
           if (p.row_mass)
             p.row_mass[ti] = VARIANT == kYat ? total : (m_used + log2f(total)) * LN2;
-          if (p.row_max) p.row_max[ti] = row_top;
+          if (p.row_max) p.row_max[ti] = VARIANT == kYat ? all_top : all_top * p.scale;
         }
       }
     }
@@ -545,7 +694,7 @@ cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap 
     if (e != cudaSuccess) return e;
     configured_for = dev;
   }
-  const long long units = (long long)p.B * p.h * p.n_pairs;
+  const long long units = (long long)p.B * p.h * p.n_qtiles;
   if (units <= 0) return cudaSuccess;
   kern<<<(unsigned)units, NUM_THREADS, L::ALLOC, s>>>(p, tq, tk, tv);
   return cudaGetLastError();

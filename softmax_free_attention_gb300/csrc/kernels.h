@@ -10,6 +10,10 @@ namespace cattn {
 
 enum Variant { kSoftmax = 0, kYat = 1, kStau = 2 };
 
+// Tile shape of the tensor-core forward: query rows per tile, keys per tile.
+constexpr int kTcQueryTile = 128;
+constexpr int kTcKeyTile = 128;
+
 // Everything a forward kernel reads besides the tensor maps.
 struct FwdParams {
   const void *q, *k, *v;        // element pointers (the tensor-core path reads through TMA)
@@ -21,8 +25,8 @@ struct FwdParams {
   int B, h, hkv, Tq, Tk, Tk_pad;
   int causal;
   float scale;
-  int n_pairs;     // query-tile pairs per head: ceil(Tq / 256)
-  int n_kv_tiles;  // ceil(Tk / 128)
+  int n_qtiles;    // query tiles per head: ceil(Tq / kTcQueryTile)
+  int n_kv_tiles;  // ceil(Tk / kTcKeyTile)
 };
 
 // Tensor-core (tcgen05) forward for bf16 inputs.  Returns a cudaError_t.
