@@ -196,6 +196,7 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
   fp.causal = p->causal ? 1 : 0;
   fp.scale = p->scale;
   fp.n_qtiles = (p->Tq + kTcQueryTile - 1) / kTcQueryTile;
+  fp.n_pairs = (fp.n_qtiles + 1) / 2;  // two query tiles per CTA
   fp.n_kv_tiles = (p->Tk + kTcKeyTile - 1) / kTcKeyTile;
 
   if (p->dtype == CATTN_F32) return map_cuda(launch_fwd_simt(variant, p->dk, p->dv, fp, s));

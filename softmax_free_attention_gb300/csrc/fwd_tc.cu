@@ -1,12 +1,13 @@
 // fwd_tc.cu -- fused attention forward on the sm_103a tensor cores.
 //
-// One CTA owns one 128-row query tile of one (batch, head) and streams
-// 128-key K/V tiles through shared memory.  Per KV tile j:
+// One CTA owns two 128-row query tiles (Q0, Q1) of one (batch, head) and
+// streams 128-key K/V tiles through shared memory, so every K/V tile that
+// reaches the SM serves 256 query rows.  Per KV tile j and query tile x:
 //
-//   S(j) = Q K_j^T      tcgen05.mma, A and B from shared memory -> TMEM fp32
-//   P(j) = map(S(j))    the eight epilogue warps: tcgen05.ld S, apply the
-//                       score-to-weight map, tcgen05.st P (bf16) to TMEM
-//   O += P(j) V_j       tcgen05.mma, A = P from TMEM, B = V from shared memory
+//   S_x = Q_x K_j^T     tcgen05.mma, A and B from shared memory -> TMEM fp32
+//   P_x = map(S_x)      eight map warps of tile x: tcgen05.ld S, apply the
+//                       score-to-weight map, tcgen05.st P (bf16) over S_x
+//   O_x += P_x V_j      tcgen05.mma, A = P from TMEM, B = V from shared memory
 //
 // The maps ("Softmax-Free Attention in JAX/Flax NNX", section "One module,
 // two compatibility functions"; "s^tau: a focal-length knob for attention",
@@ -21,18 +22,18 @@
 //            running max of tau log2 phi, taken from the max raw score since
 //            phi is increasing.
 //
-// TMEM (512 columns): S buffers [0,128) [128,256) | P buffers [256,320)
-// [320,384) | O [384,512).  S and P are both double buffered and P has its own
-// columns, so the MMA warp issues S(j+2) as soon as the epilogue has loaded
-// S(j), two tiles ahead of PV(j): the tensor cores always have S work queued
-// while the map of tile j runs, and the period per tile is the larger of the
-// tensor time and the map time.
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).  P_x
+// is written over S_x; the MMA pipe executes a CTA's MMAs in issue order, so
+// PV_x(j) reads P_x before S_x(j+1) lands, and the commit that signals S_x(j)
+// also covers PV_x(j-1).  The MMA order PV0(j-1) S0(j) PV1(j-1) S1(j) lets
+// one query tile's MMAs run while the other tile is being mapped.
 //
-// Warp roles (320 threads): warps 0-7 map (warp w: TMEM lanes 32*(w%4)..+31 =
-// those query rows, key columns [64h, 64h+64) with h = w/4), warp 8 issues TMA
-// loads, warp 9 allocates TMEM and issues the MMAs (lane 0).  K and V tiles
-// share one ring of shared-memory slots guarded by full/empty mbarriers; the
-// squared key norms of the Yat map ride in a small ring of their own.
+// Warp roles (576 threads): warps 0-15 map (warp w: query tile x = w/8, TMEM
+// lanes 32*(w%4)..+31 = those query rows, key columns [64h, 64h+64) with
+// h = (w/4)%2, so each tile has two warps per SM sub-partition), warp 16 issues
+// TMA loads, warp 17 allocates TMEM and issues the MMAs (lane 0).  K and V
+// tiles share one ring of shared-memory slots guarded by full/empty mbarriers;
+// the squared key norms of the Yat map ride in a small ring of their own.
 //
 // Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the kernel
 // records a site code in g_status, raises a CTA-wide abort flag, and all roles
@@ -66,9 +67,10 @@ namespace tc {
 
 constexpr int BM = kTcQueryTile;  // 128 query rows per tile
 constexpr int BN = kTcKeyTile;    // 128 keys per tile
-constexpr int NUM_THREADS = 320;
-constexpr int PRODUCER_WARP = 8;
-constexpr int MMA_WARP = 9;
+constexpr int NUM_THREADS = 576;
+constexpr int MAP_WARPS = 16;
+constexpr int PRODUCER_WARP = 16;
+constexpr int MMA_WARP = 17;
 constexpr int NKS = 4;  // stages of the key-norm ring
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr unsigned FULL = 0xffffffffu;
@@ -76,17 +78,16 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 
-// TMEM column map
-constexpr uint32_t TM_S = 0;    // S buffer b at TM_S + 128 b
-constexpr uint32_t TM_P = 256;  // P buffer b at TM_P + 64 b (keys [64h,64h+64) at +32 h)
-constexpr uint32_t TM_O = 384;  // O
+// TMEM column map: S_x (and P_x over it) at 128 x, O_x at 256 + 128 x.  Keys
+// [64h, 64h+64) of P_x sit at columns [64h, 64h+32) of S_x.
+constexpr uint32_t TM_S = 0;
+constexpr uint32_t TM_O = 256;
 
 // wait-site codes recorded in g_status
 enum : unsigned {
   SITE_PRODUCER = 0x100,
   SITE_MMA = 0x200,
   SITE_EPI = 0x300,
-  SITE_ALIGN = 0x400,
 };
 
 template <int DK, int DV>
@@ -94,30 +95,24 @@ struct Layout {
   static constexpr int Q_TILE = BM * DK * 2;
   static constexpr int K_TILE = BN * DK * 2;
   static constexpr int V_TILE = BN * DV * 2;
-  // K and V have rings of their own: K(j+2) is loaded while V(j) is still
-  // waiting for its PV, so neither blocks the other.
-  static constexpr int NSK = DK == 64 ? 5 : 3;
-  static constexpr int NSV = (DK == 64 || DV == 64) ? 5 : 3;
+  static constexpr int SLOT = K_TILE > V_TILE ? K_TILE : V_TILE;
+  static constexpr int NS = DK == 64 ? 8 : 4;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_TILE;
-  static constexpr int OFF_V = OFF_K + NSK * K_TILE;
-  // aux: the Yat key-norm ring, or the softmax / s^tau row-max exchange
-  // [2 uses][2 halves][BM]; after the last tile both serve the final exchange
-  // of the two halves' partial sums
-  static constexpr int OFF_AUX = OFF_V + NSV * V_TILE;
-  static constexpr int AUX_BYTES = 4 * BM * 4;
-  static constexpr int OFF_BAR = OFF_AUX + AUX_BYTES;
-  // q_full, kf[NSK], ke[NSK], vf[NSV], ve[NSV], nk_full[NKS], nk_empty[NKS],
-  // s_full[2], s_empty[2], p_full[2], p_empty[2], o_full, drain
-  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 2 * NKS + 8 + 2;
+  static constexpr int OFF_RING = OFF_Q + 2 * Q_TILE;
+  static constexpr int OFF_NK = OFF_RING + NS * SLOT;
+  // row-max exchange of the two column halves: per tile [2 uses][2 tiles][2 halves][BM],
+  // final [2 tiles][2 values][2 halves][BM]
+  static constexpr int OFF_XCHG = OFF_NK + NKS * BN * 4;
+  static constexpr int XCHG_FLOATS = 16 * BM;
+  static constexpr int OFF_BAR = OFF_XCHG + XCHG_FLOATS * 4;
+  // q_full, kv_full[NS], kv_empty[NS], nk_full[NKS], nk_empty[NKS],
+  // s_full[2], p_full[2], o_full[2], drain
+  static constexpr int NBAR = 1 + 2 * NS + 2 * NKS + 7;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
-  // the dynamic shared memory base is checked to be 1024-byte aligned at run time
-  static constexpr int ALLOC = BYTES;
+  static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024 B
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
-  static_assert(NKS * BN * 4 <= AUX_BYTES, "key-norm ring fits the aux region");
-  static_assert(K_TILE % 1024 == 0 && V_TILE % 1024 == 0 && Q_TILE % 1024 == 0,
-                "swizzle atoms stay 1024-B aligned");
+  static_assert(SLOT % 1024 == 0 && Q_TILE % 1024 == 0, "swizzle atoms stay 1024-B aligned");
 };
 
 // Warp-collective bounded wait.  Every lane polls (so every lane acquires the
@@ -152,16 +147,16 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
   }
 }
 
-// O += P V for one 128-key tile; P (bf16 pairs) in 64 TMEM columns (keys
-// [64h, 64h+64) at columns [32h, 32h+32)), V N-major with its 64-wide dv boxes
-// BN*128 bytes apart.
+// O += P V for one 128-key tile; P (bf16 pairs) over S (keys [64h, 64h+64)
+// at columns [64h, 64h+32)), V N-major with its 64-wide dv boxes BN*128 bytes
+// apart.
 template <int DV>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
                                          bool accumulate) {
   constexpr uint32_t IDESC = idesc_bf16_f32(BM, DV, true);
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk) {
-    mma_ts(d_tmem, p_tmem + (uint32_t)kk * 8,
+    mma_ts(d_tmem, p_tmem + (uint32_t)(kk >> 2) * 64 + (uint32_t)(kk & 3) * 8,
            smem_desc_sw128(v_smem + (uint32_t)kk * 2048, BN * 128, 1024), IDESC,
            (accumulate || kk > 0) ? 1u : 0u);
   }
@@ -288,82 +283,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using L = Layout<DK, DV>;
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(smem);
-  if (sb & 1023u) {  // the 128-byte swizzle needs 1024-byte aligned tiles
-    if (threadIdx.x == 0) atomicCAS(&g_status, 0u, SITE_ALIGN);
-    return;
-  }
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   const uint32_t bar0 = sb + L::OFF_BAR;
   const uint32_t bar_q = bar0;
-  auto k_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto k_empty = [&](int s) { return bar0 + 8u * (1 + L::NSK + s); };
-  auto v_full = [&](int s) { return bar0 + 8u * (1 + 2 * L::NSK + s); };
-  auto v_empty = [&](int s) { return bar0 + 8u * (1 + 2 * L::NSK + L::NSV + s); };
-  constexpr int B1 = 1 + 2 * L::NSK + 2 * L::NSV;
-  auto nk_full = [&](int s) { return bar0 + 8u * (B1 + s); };
-  auto nk_empty = [&](int s) { return bar0 + 8u * (B1 + NKS + s); };
-  constexpr int B2 = B1 + 2 * NKS;
-  auto s_full = [&](int b) { return bar0 + 8u * (B2 + b); };
-  auto s_empty = [&](int b) { return bar0 + 8u * (B2 + 2 + b); };
-  auto p_full = [&](int b) { return bar0 + 8u * (B2 + 4 + b); };
-  auto p_empty = [&](int b) { return bar0 + 8u * (B2 + 6 + b); };
-  const uint32_t bar_o = bar0 + 8u * (B2 + 8);
-  const uint32_t bar_drain = bar0 + 8u * (B2 + 9);
-  const uint32_t q_smem = sb + L::OFF_Q;
-  auto k_smem = [&](int s) { return sb + L::OFF_K + (uint32_t)s * L::K_TILE; };
-  auto v_smem = [&](int s) { return sb + L::OFF_V + (uint32_t)s * L::V_TILE; };
-  const float *nk_ring = reinterpret_cast<const float *>(smem + L::OFF_AUX);
+  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (1 + L::NS + s); };
+  auto nk_full = [&](int s) { return bar0 + 8u * (1 + 2 * L::NS + s); };
+  auto nk_empty = [&](int s) { return bar0 + 8u * (1 + 2 * L::NS + NKS + s); };
+  constexpr int B2 = 1 + 2 * L::NS + 2 * NKS;
+  auto s_full = [&](int x) { return bar0 + 8u * (B2 + x); };
+  auto p_full = [&](int x) { return bar0 + 8u * (B2 + 2 + x); };
+  auto o_full = [&](int x) { return bar0 + 8u * (B2 + 4 + x); };
+  const uint32_t bar_drain = bar0 + 8u * (B2 + 6);
+  auto q_smem = [&](int x) { return sb + L::OFF_Q + (uint32_t)x * L::Q_TILE; };
+  auto slot_smem = [&](int s) { return sb + L::OFF_RING + (uint32_t)s * L::SLOT; };
+  const float *nk_ring = reinterpret_cast<const float *>(smem + L::OFF_NK);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
 
-  // ---- work unit: (batch, head, query tile).  The tiles of one head are
-  // consecutive, so its K/V stays in L2 while they run; causal tiles go
+  // ---- work unit: (batch, head, query-tile pair).  The pairs of one head are
+  // consecutive, so its K/V stays in L2 while they run; causal pairs go
   // heaviest first.
-  const int bh = blockIdx.x / p.n_qtiles;
-  int qt = blockIdx.x - bh * p.n_qtiles;
-  if (p.causal) qt = p.n_qtiles - 1 - qt;
+  const int bh = blockIdx.x / p.n_pairs;
+  int pair = blockIdx.x - bh * p.n_pairs;
+  if (p.causal) pair = p.n_pairs - 1 - pair;
   const int head = bh % p.h;
   const int batch = bh / p.h;
   const int bh_kv = batch * p.hkv + head / (p.h / p.hkv);
-  const int q0 = qt * BM;
-  // causal: keys 0 .. last row of the tile
-  const int nkv = p.causal ? min(qt + 1, p.n_kv_tiles) : p.n_kv_tiles;
-  // The query tiles of one head run side by side; each walks its key tiles
-  // from its own starting point (then wraps), so they do not all request the
-  // same K/V tile at the same moment.  Every map is order independent.
-  const int rot = (qt * 7) % nkv;
-  auto kv_tile = [&](int j) { return j + rot < nkv ? j + rot : j + rot - nkv; };
+  const int q0 = pair * 2 * BM;
+  const bool q1_valid = (q0 + BM) < p.Tq;
+  int nkv_x[2];
+  if (p.causal) {  // keys 0 .. last row of the query tile
+    nkv_x[0] = min(2 * pair + 1, p.n_kv_tiles);
+    nkv_x[1] = q1_valid ? min(2 * pair + 2, p.n_kv_tiles) : 0;
+  } else {
+    nkv_x[0] = p.n_kv_tiles;
+    nkv_x[1] = q1_valid ? p.n_kv_tiles : 0;
+  }
+  const int nkv = max(nkv_x[0], nkv_x[1]);
 #ifdef CATTN_TRACE
-  const int tr_slot =
-      (blockIdx.x % p.n_qtiles == 0 && (int)(blockIdx.x / p.n_qtiles) < 8) ? (int)(blockIdx.x / p.n_qtiles) : -1;
+  const int tr_slot = (pair == p.n_pairs - 1 && bh < 8) ? bh : -1;
 #endif
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int s = 0; s < L::NSK; ++s) {
-      mbar_init(k_full(s), 1);
-      mbar_init(k_empty(s), 1);
-    }
-    for (int s = 0; s < L::NSV; ++s) {
-      mbar_init(v_full(s), 1);
-      mbar_init(v_empty(s), 1);
+    for (int s = 0; s < L::NS; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
     }
     for (int s = 0; s < NKS; ++s) {
       mbar_init(nk_full(s), 1);
       mbar_init(nk_empty(s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(s_full(b), 1);
-      mbar_init(s_empty(b), 8 * 32);  // every epilogue thread has loaded its part of S
-      mbar_init(p_full(b), 8 * 32);   // every epilogue thread has stored its part of P
-      mbar_init(p_empty(b), 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(s_full(x), 1);
+      mbar_init(p_full(x), 8 * 32);  // the eight map warps of query tile x
+      mbar_init(o_full(x), 1);
     }
-    mbar_init(bar_o, 1);
     mbar_init(bar_drain, 1);
     *abort = 0;
     fence_mbar_init();
@@ -384,94 +367,105 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
-    // load order K0 K1 | K(j+2) V(j) for j = 0.. : the order the MMAs consume
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar_q, (uint32_t)L::Q_TILE);
+      mbar_arrive_expect_tx(bar_q, (q1_valid ? 2u : 1u) * (uint32_t)L::Q_TILE);
 #pragma unroll
-      for (int c = 0; c < DK / 64; ++c) tma_load_3d(q_smem + c * BM * 128, &tm_q, c * 64, q0, bh, bar_q);
+      for (int c = 0; c < DK / 64; ++c) {
+        tma_load_3d(q_smem(0) + c * BM * 128, &tm_q, c * 64, q0, bh, bar_q);
+        if (q1_valid) tma_load_3d(q_smem(1) + c * BM * 128, &tm_q, c * 64, q0 + BM, bh, bar_q);
+      }
     }
     __syncwarp();
-    auto load_k = [&](int t) -> bool {
-      const int s = t % L::NSK;
-      const uint32_t use = (uint32_t)(t / L::NSK);
-      if (!warp_wait(k_empty(s), (use & 1u) ^ 1u, abort, SITE_PRODUCER | 0x10)) return false;
-      if (lane == 0) CATTN_TR(9, t);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(k_full(s), L::K_TILE);
-#pragma unroll
-        for (int c = 0; c < DK / 64; ++c)
-          tma_load_3d(k_smem(s) + c * BN * 128, &tm_k, c * 64, kv_tile(t) * BN, bh_kv, k_full(s));
-      }
-      __syncwarp();
-      if (VARIANT == kYat) {  // squared key norms of tile t
-        const int ns = t % NKS;
-        const uint32_t nuse = (uint32_t)(t / NKS);
-        if (!warp_wait(nk_empty(ns), (nuse & 1u) ^ 1u, abort, SITE_PRODUCER | 0x20)) return false;
+    for (int j = 0; j < nkv; ++j) {
+      {  // K_j
+        const int idx = 2 * j, s = idx % L::NS;
+        const uint32_t use = (uint32_t)(idx / L::NS);
+        if (!warp_wait(kv_empty(s), (use & 1u) ^ 1u, abort, SITE_PRODUCER | 0x10)) break;
+        if (lane == 0) CATTN_TR(9, j);
         if (lane == 0) {
-          mbar_arrive_expect_tx(nk_full(ns), BN * 4);
-          bulk_load(sb + L::OFF_AUX + (uint32_t)ns * BN * 4,
-                    p.nk + (size_t)bh_kv * p.Tk_pad + (size_t)kv_tile(t) * BN, BN * 4, nk_full(ns));
+          mbar_arrive_expect_tx(kv_full(s), L::K_TILE);
+#pragma unroll
+          for (int c = 0; c < DK / 64; ++c)
+            tma_load_3d(slot_smem(s) + c * BN * 128, &tm_k, c * 64, j * BN, bh_kv, kv_full(s));
         }
         __syncwarp();
       }
-      return true;
-    };
-    bool ok = true;
-    if (nkv > 0) ok = load_k(0);
-    if (ok && nkv > 1) ok = load_k(1);
-    for (int j = 0; ok && j < nkv; ++j) {
-      if (j + 2 < nkv && !(ok = load_k(j + 2))) break;
-      const int s = j % L::NSV;
-      const uint32_t use = (uint32_t)(j / L::NSV);
-      if (!(ok = warp_wait(v_empty(s), (use & 1u) ^ 1u, abort, SITE_PRODUCER | 0x30))) break;
-      if (lane == 0) CATTN_TR(10, j);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(v_full(s), L::V_TILE);
-#pragma unroll
-        for (int c = 0; c < DV / 64; ++c)
-          tma_load_3d(v_smem(s) + c * BN * 128, &tm_v, c * 64, kv_tile(j) * BN, bh_kv, v_full(s));
+      if (VARIANT == kYat) {  // squared key norms of tile j
+        const int s = j % NKS;
+        const uint32_t use = (uint32_t)(j / NKS);
+        if (!warp_wait(nk_empty(s), (use & 1u) ^ 1u, abort, SITE_PRODUCER | 0x20)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(nk_full(s), BN * 4);
+          bulk_load(sb + L::OFF_NK + (uint32_t)s * BN * 4,
+                    p.nk + (size_t)bh_kv * p.Tk_pad + (size_t)j * BN, BN * 4, nk_full(s));
+        }
+        __syncwarp();
       }
-      __syncwarp();
+      {  // V_j
+        const int idx = 2 * j + 1, s = idx % L::NS;
+        const uint32_t use = (uint32_t)(idx / L::NS);
+        if (!warp_wait(kv_empty(s), (use & 1u) ^ 1u, abort, SITE_PRODUCER | 0x30)) break;
+        if (lane == 0) CATTN_TR(10, j);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(kv_full(s), L::V_TILE);
+#pragma unroll
+          for (int c = 0; c < DV / 64; ++c)
+            tma_load_3d(slot_smem(s) + c * BN * 128, &tm_v, c * 64, j * BN, bh_kv, kv_full(s));
+        }
+        __syncwarp();
+      }
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issue
-    // S(0), S(1) up front; then step j issues S(j+2) (once the epilogue has
-    // loaded S(j) out of its buffer) followed by PV(j).
+    // iteration j: PV0(j-1) S0(j) PV1(j-1) S1(j)
     bool ok = warp_wait(bar_q, 0, abort, SITE_MMA | 0x10);
     tc_fence_after();
-    auto issue_s = [&](int t) -> bool {
-      const int ks = t % L::NSK, b = t & 1;
-      if (!warp_wait(k_full(ks), (uint32_t)(t / L::NSK) & 1u, abort, SITE_MMA | 0x20)) return false;
-      CATTN_TR(7, t);
-      if (t >= 2 && !warp_wait(s_empty(b), (uint32_t)((t >> 1) - 1) & 1u, abort, SITE_MMA | 0x30))
-        return false;
-      tc_fence_after();
-      CATTN_TR(8, t);
-      if (lane == 0) {
-        issue_qk<DK>(tmem + TM_S + 128u * b, q_smem, k_smem(ks));
-        mma_commit(s_full(b));
-        if (t + L::NSK < nkv) mma_commit(k_empty(ks));  // only slots that are reloaded
+    uint32_t pph[2] = {0u, 0u};
+    const int release_limit = 2 * nkv - L::NS;  // later slots are never reloaded
+    for (int j = 0; ok && j <= nkv; ++j) {
+      const int vidx = 2 * (j - 1) + 1;
+      const int vs = j >= 1 ? vidx % L::NS : 0;
+      if (j >= 1) {
+        if (!(ok = warp_wait(kv_full(vs), (uint32_t)(vidx / L::NS) & 1u, abort, SITE_MMA | 0x20)))
+          break;
+        CATTN_TR(11, j - 1);
+        tc_fence_after();
       }
-      __syncwarp();
-      return true;
-    };
-    if (ok && nkv > 0) ok = issue_s(0);
-    if (ok && nkv > 1) ok = issue_s(1);
-    for (int j = 0; ok && j < nkv; ++j) {
-      if (j + 2 < nkv && !(ok = issue_s(j + 2))) break;
-      const int vs = j % L::NSV, b = j & 1;
-      if (!(ok = warp_wait(v_full(vs), (uint32_t)(j / L::NSV) & 1u, abort, SITE_MMA | 0x40))) break;
-      CATTN_TR(11, j);
-      if (!(ok = warp_wait(p_full(b), (uint32_t)(j >> 1) & 1u, abort, SITE_MMA | 0x50))) break;
-      CATTN_TR(6, j);
-      tc_fence_after();
+      const int kidx = 2 * j;
+      const int ks = kidx % L::NS;
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        if (j >= 1 && j - 1 < nkv_x[x]) {  // O_x += P_x(j-1) V(j-1)
+          if (!(ok = warp_wait(p_full(x), pph[x], abort, SITE_MMA | 0x30))) break;
+          pph[x] ^= 1u;
+          if (x == 0) CATTN_TR(6, j - 1);
+          tc_fence_after();
+          if (lane == 0) {
+            issue_pv<DV>(tmem + TM_O + 128u * x, tmem + TM_S + 128u * x, slot_smem(vs), j - 1 > 0);
+            if (j - 1 == nkv_x[x] - 1) mma_commit(o_full(x));
+          }
+          __syncwarp();
+        }
+        if (x == 0 && j < nkv) {
+          if (!(ok = warp_wait(kv_full(ks), (uint32_t)(kidx / L::NS) & 1u, abort, SITE_MMA | 0x40)))
+            break;
+          CATTN_TR(7, j);
+          tc_fence_after();
+        }
+        if (j < nkv_x[x]) {  // S_x = Q_x K(j)^T
+          if (lane == 0) {
+            issue_qk<DK>(tmem + TM_S + 128u * x, q_smem(x), slot_smem(ks));
+            mma_commit(s_full(x));
+          }
+          __syncwarp();
+        }
+      }
+      if (!ok) break;
       if (lane == 0) {
-        issue_pv<DV>(tmem + TM_O, tmem + TM_P + 64u * b, v_smem(vs), j > 0);
-        mma_commit(p_empty(b));
-        if (j == nkv - 1) mma_commit(bar_o);
-        if (j + L::NSV < nkv) mma_commit(v_empty(vs));
-        // every epilogue thread delivered P(j), so all are done with its key norms
-        if (VARIANT == kYat) mbar_arrive(nk_empty(j % NKS));
+        if (j < nkv && kidx < release_limit) mma_commit(kv_empty(ks));
+        if (j >= 1 && vidx < release_limit) mma_commit(kv_empty(vs));
+        // every map warp delivered P for tile j-1, so all are done with its key norms
+        if (VARIANT == kYat && j >= 1) mbar_arrive(nk_empty((j - 1) % NKS));
       }
       __syncwarp();
     }
@@ -480,16 +474,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) mma_commit(bar_drain);
     __syncwarp();
     warp_wait(bar_drain, 0, abort, SITE_MMA | 0x60, false);
-  } else if (warp < 8) {
-    // ------------------------------------------------------------ epilogue
+  } else if (warp < MAP_WARPS) {
+    // ------------------------------------------------------------ map warps
+    const int x = warp >> 3;          // query tile
+    const int half = (warp >> 2) & 1;  // key columns [64 half, 64 half + 64)
     const int quarter = warp & 3;
-    const int half = warp >> 2;
     const int r = quarter * 32 + lane;  // row in tile == TMEM lane
+    const int nk_tiles = nkv_x[x];
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t t_o = tmem + lane_off + TM_O + (uint32_t)half * (DV / 2);
-    const uint32_t named_bar = 1u + (uint32_t)quarter;  // pairs warps w and w^4
-    float *xchg = reinterpret_cast<float *>(smem + L::OFF_AUX);
-    const int row = q0 + r;
+    const uint32_t t_s = tmem + lane_off + TM_S + 128u * x + 64u * half;
+    const uint32_t t_o = tmem + lane_off + TM_O + 128u * x + (uint32_t)half * (DV / 2);
+    const uint32_t named_bar = 1u + (uint32_t)(x * 4 + quarter);  // warps w and w^4
+    float *xchg = reinterpret_cast<float *>(smem + L::OFF_XCHG);
+    const int row = q0 + x * BM + r;
     const bool row_ok = row < p.Tq;
 
     float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // Yat: mass; else l
@@ -508,55 +505,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t xpar = 0;
 
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int b = j & 1;
-      const uint32_t t_s = tmem + lane_off + TM_S + 128u * b + 64u * half;
-      if (!(ok = warp_wait(s_full(b), (uint32_t)(j >> 1) & 1u, abort, SITE_EPI | 0x10))) break;
+    for (int j = 0; j < nk_tiles; ++j) {
+      if (!(ok = warp_wait(s_full(x), (uint32_t)j & 1u, abort, SITE_EPI | 0x10))) break;
       if (threadIdx.x == 0) CATTN_TR(0, j);
       tc_fence_after();
-      uint32_t sr[2][32];
-      tmem_ld32(t_s, sr[0]);
-      tmem_ld32(t_s + 32, sr[1]);
-      const float2 *nk2 = nullptr;
-      if (VARIANT == kYat) {
-        const int ns = j % NKS;
-        if (!(ok = warp_wait(nk_full(ns), (uint32_t)(j / NKS) & 1u, abort, SITE_EPI | 0x20))) break;
-        nk2 = reinterpret_cast<const float2 *>(nk_ring + ns * BN);
-      }
-      tmem_wait_ld();
-      tmem_ld_fence(sr[0]);
-      tmem_ld_fence(sr[1]);
-      // S(j) is in registers: the tensor cores may overwrite its buffer
-      tc_fence_before();
-      mbar_arrive(s_empty(b));
-      if (threadIdx.x == 0) CATTN_TR(1, j);
 
       // keys j*BN + col allowed for col < limit (col counts the whole tile)
       int limit = BN;
-      const int jt = kv_tile(j);
-      if (jt == p.n_kv_tiles - 1) limit = min(limit, p.Tk - jt * BN);
-      if (p.causal) limit = min(limit, row + 1 - jt * BN);
+      if (j == p.n_kv_tiles - 1) limit = min(limit, p.Tk - j * BN);
+      if (p.causal) limit = min(limit, row + 1 - j * BN);
       const bool partial = __any_sync(FULL, limit < BN);  // warp-uniform path choice
 
-      uint32_t pk[32];  // P as bf16 pairs, this warp's 32 TMEM columns
+      bool rescale = false;
+      float corr = 1.f;
       if (VARIANT == kYat) {
+        const int ns = j % NKS;
+        if (!(ok = warp_wait(nk_full(ns), (uint32_t)(j / NKS) & 1u, abort, SITE_EPI | 0x20))) break;
+        const float2 *nk2 = reinterpret_cast<const float2 *>(nk_ring + ns * BN);
+        // chunk by chunk: P chunk c lands on S columns this warp has read
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
+          uint32_t sr[32];
+          tmem_ld32(t_s + 32 * c, sr);
+          tmem_wait_ld();
+          tmem_ld_fence(sr);
           uint32_t hk[16];
           if (partial)
-            yat_chunk<true>(sr[c], half * 2 + c, nk2, yb, qe, yeps, limit, acc, top, hk);
+            yat_chunk<true>(sr, half * 2 + c, nk2, yb, qe, yeps, limit, acc, top, hk);
           else
-            yat_chunk<false>(sr[c], half * 2 + c, nk2, yb, qe, yeps, limit, acc, top, hk);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pk[c * 16 + i] = hk[i];
+            yat_chunk<false>(sr, half * 2 + c, nk2, yb, qe, yeps, limit, acc, top, hk);
+          tmem_st16(t_s + 16 * c, hk);
         }
       } else {
+        uint32_t sr[2][32];
+        tmem_ld32(t_s, sr[0]);
+        tmem_ld32(t_s + 32, sr[1]);
+        tmem_wait_ld();
+        tmem_ld_fence(sr[0]);
+        tmem_ld_fence(sr[1]);
         float mt = partial ? fmaxf(chunk_max<true>(sr[0], half * 2, limit),
                                    chunk_max<true>(sr[1], half * 2 + 1, limit))
                            : fmaxf(chunk_max<false>(sr[0], half * 2, limit),
                                    chunk_max<false>(sr[1], half * 2 + 1, limit));
         // the row max over the whole tile: swap halves with the partner warp
-        float *xb = xchg + xpar * 2 * BM;
+        float *xb = xchg + ((xpar * 2 + (uint32_t)x) * 2) * BM;
         xb[half * BM + r] = mt;
         named_barrier_sync(named_bar, 64);
         mt = fmaxf(mt, xb[(half ^ 1) * BM + r]);
@@ -571,20 +563,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (__any_sync(FULL, m_new > m_used + RESCALE_THRESHOLD)) {
           const float mn = fmaxf(m_used, m_new);
-          const float corr = ex2_approx(m_used - mn);
+          corr = ex2_approx(m_used - mn);
           acc[0].x *= corr;
           acc[0].y *= corr;
           acc[1].x *= corr;
           acc[1].y *= corr;
           m_used = mn;
-          if (j > 0) {
-            // O must hold every tile before j: wait for PV(j-1), then rescale
-            if (!(ok = warp_wait(p_empty((j - 1) & 1), (uint32_t)((j - 1) >> 1) & 1u, abort,
-                                 SITE_EPI | 0x40)))
-              break;
-            tc_fence_after();
-            scale_o_half<DV>(t_o, corr);
-          }
+          rescale = j > 0;
         }
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -600,45 +585,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             else
               stau_chunk<false>(sr[c], half * 2 + c, p.scale, c2, tau, seps, -m_used, limit, acc, hk);
           }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pk[c * 16 + i] = hk[i];
+          tmem_st16(t_s + 16 * c, hk);
         }
       }
-      // P buffer b is free once PV(j-2) has completed
-      if (!(ok = warp_wait(p_empty(b), ((uint32_t)(j >> 1) & 1u) ^ 1u, abort, SITE_EPI | 0x50)))
-        break;
-      tc_fence_after();
-      tmem_st32(tmem + lane_off + TM_P + 64u * b + 32u * half, pk);
+      // O_x holds every tile before j (S_x(j) landed after PV_x(j-1)): bring
+      // this warp's dv/2 columns onto the new max
+      if (rescale) scale_o_half<DV>(t_o, corr);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_full(b));
+      mbar_arrive(p_full(x));
       if (threadIdx.x == 0) CATTN_TR(2, j);
     }
 
     // ---- finalise: combine the two halves of the row, normalise, store
-    if (ok) {
+    if (ok && nk_tiles > 0) {
       const float part = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
-      float total, all_top;
-      float *fb = xchg;
-      if (VARIANT == kYat) {
-        // the aux region held the key norms: wait until all eight epilogue warps
-        // are past their last read of it
-        named_barrier_sync(5, 8 * 32);
-        fb[(0 * 2 + half) * BM + r] = part;
-        fb[(1 * 2 + half) * BM + r] = fmaxf(top[0], top[1]);
-        named_barrier_sync(named_bar, 64);
-        total = part + fb[(0 * 2 + (half ^ 1)) * BM + r];
-        all_top = fmaxf(fmaxf(top[0], top[1]), fb[(1 * 2 + (half ^ 1)) * BM + r]);
-      } else {
-        // the row max was already shared tile by tile; swap the partial sums in
-        // the exchange buffer the last tile did not use
-        fb = xchg + xpar * 2 * BM;
-        fb[half * BM + r] = part;
-        named_barrier_sync(named_bar, 64);
-        total = part + fb[(half ^ 1) * BM + r];
-        all_top = top[0];
-      }
-      if (warp_wait(bar_o, 0, abort, SITE_EPI | 0x30)) {
+      const float ptop = fmaxf(top[0], top[1]);
+      float *fb = xchg + (8 + (uint32_t)x * 4) * BM;  // [2 values][2 halves][BM]
+      fb[(0 * 2 + half) * BM + r] = part;
+      fb[(1 * 2 + half) * BM + r] = ptop;
+      named_barrier_sync(named_bar, 64);
+      const float total = part + fb[(0 * 2 + (half ^ 1)) * BM + r];
+      const float all_top = fmaxf(ptop, fb[(1 * 2 + (half ^ 1)) * BM + r]);
+      if (warp_wait(o_full(x), 0, abort, SITE_EPI | 0x30)) {
         tc_fence_after();
         const float inv = VARIANT == kYat ? 1.f / (total + 1e-9f) : 1.f / total;
         __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
@@ -694,7 +663,7 @@ cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap 
     if (e != cudaSuccess) return e;
     configured_for = dev;
   }
-  const long long units = (long long)p.B * p.h * p.n_qtiles;
+  const long long units = (long long)p.B * p.h * p.n_pairs;
   if (units <= 0) return cudaSuccess;
   kern<<<(unsigned)units, NUM_THREADS, L::ALLOC, s>>>(p, tq, tk, tv);
   return cudaGetLastError();

@@ -26,6 +26,7 @@ struct FwdParams {
   int causal;
   float scale;
   int n_qtiles;    // query tiles per head: ceil(Tq / kTcQueryTile)
+  int n_pairs;     // CTAs per head: ceil(n_qtiles / 2)
   int n_kv_tiles;  // ceil(Tk / kTcKeyTile)
 };
 
