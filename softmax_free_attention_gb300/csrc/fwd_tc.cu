@@ -41,6 +41,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "maps.cuh"
 #include "ptx.cuh"
 
 namespace cattn {
@@ -52,6 +53,10 @@ __device__ unsigned int g_status;
 __device__ unsigned long long g_trace[8][12][160];
 extern "C" int cattn_trace_read(void *host, size_t bytes) {
   return (int)cudaMemcpyFromSymbol(host, g_trace, bytes);
+}
+__device__ unsigned long long g_cta_trace[16384][4];
+extern "C" int cattn_cta_trace_read(void *host, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(host, g_cta_trace, bytes);
 }
 #define CATTN_TR(ev, j)                                          \
   do {                                                           \
@@ -177,107 +182,6 @@ __device__ __forceinline__ void scale_o_half(uint32_t t_o, float f) {
   }
 }
 
-__device__ __forceinline__ float2 f2(uint32_t a, uint32_t b) {
-  return make_float2(__uint_as_float(a), __uint_as_float(b));
-}
-
-// Yat map over one 32-key chunk (columns 32c .. 32c+31 of the tile) of one row.  sr: raw
-// dots; nk2: squared key norms of the tile (pairs); qe = |q|^2 + eps.
-// kappa = (dot + b)^2 / max(|q|^2 + |k|^2 - 2 dot + eps, eps); masked keys
-// (col >= limit) get kappa = 0.
-template <bool PARTIAL>
-__device__ __forceinline__ void yat_chunk(const uint32_t (&sr)[32], int c, const float2 *nk2,
-                                          float yb, float qe, float yeps, int limit,
-                                          float2 (&mass)[2], float (&top)[2],
-                                          uint32_t (&pk)[16]) {
-  const float2 b2 = make_float2(yb, yb), qe2 = make_float2(qe, qe);
-  const float2 m2 = make_float2(-2.f, -2.f);
-#pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    const int col = c * 32 + i;
-    const int chain = (i >> 1) & 1;
-    const float2 d = f2(sr[i], sr[i + 1]);
-    const float2 t = __fadd2_rn(d, b2);
-    const float2 num = __fmul2_rn(t, t);
-    const float2 den = __ffma2_rn(m2, d, __fadd2_rn(qe2, nk2[col >> 1]));
-    const float2 r = make_float2(rcp_approx(fmaxf(den.x, yeps)), rcp_approx(fmaxf(den.y, yeps)));
-    float2 k = __fmul2_rn(num, r);
-    if (PARTIAL) {
-      k.x = col < limit ? k.x : 0.f;
-      k.y = col + 1 < limit ? k.y : 0.f;
-    }
-    mass[chain] = __fadd2_rn(mass[chain], k);
-    top[chain] = max3(top[chain], k.x, k.y);
-    pk[i >> 1] = pack_bf16x2(k.x, k.y);
-  }
-}
-
-// Max of the raw dot over the allowed keys of one 32-key chunk (masked -> -inf).
-template <bool PARTIAL>
-__device__ __forceinline__ float chunk_max(const uint32_t (&sr)[32], int c, int limit) {
-  float m[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    const int col = c * 32 + i;
-    float x0 = __uint_as_float(sr[i]), x1 = __uint_as_float(sr[i + 1]);
-    if (PARTIAL) {
-      x0 = col < limit ? x0 : -INFINITY;
-      x1 = col + 1 < limit ? x1 : -INFINITY;
-    }
-    m[(i >> 1) & 1] = max3(m[(i >> 1) & 1], x0, x1);
-  }
-  return fmaxf(m[0], m[1]);
-}
-
-// softmax over one 32-key chunk: p = 2^(dot * c2 - m), c2 = scale * log2(e).
-template <bool PARTIAL>
-__device__ __forceinline__ void softmax_chunk(const uint32_t (&sr)[32], int c, float c2,
-                                              float neg_m, int limit, float2 (&l)[2],
-                                              uint32_t (&pk)[16]) {
-  const float2 c22 = make_float2(c2, c2), nm2 = make_float2(neg_m, neg_m);
-#pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    const int col = c * 32 + i;
-    const float2 x = __ffma2_rn(f2(sr[i], sr[i + 1]), c22, nm2);
-    float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-    if (PARTIAL) {
-      pr.x = col < limit ? pr.x : 0.f;
-      pr.y = col + 1 < limit ? pr.y : 0.f;
-    }
-    l[(i >> 1) & 1] = __fadd2_rn(l[(i >> 1) & 1], pr);
-    pk[i >> 1] = pack_bf16x2(pr.x, pr.y);
-  }
-}
-
-// log2(softplus(s) + eps), softplus(s) = max(s, 0) + ln(1 + 2^(-|s| log2 e)).
-__device__ __forceinline__ float log2_phi(float s, float abs_s_log2e, float eps) {
-  constexpr float LN2 = 0.6931471805599453f;
-  const float e = ex2_approx(-abs_s_log2e);
-  const float l1p = e < 0x1p-12f ? e : lg2_approx(1.f + e) * LN2;
-  return lg2_approx(fmaxf(s, 0.f) + l1p + eps);
-}
-
-// s^tau over one 32-key chunk: p = 2^(tau log2 phi(s) - m).
-template <bool PARTIAL>
-__device__ __forceinline__ void stau_chunk(const uint32_t (&sr)[32], int c, float scale, float c2,
-                                           float tau, float eps, float neg_m, int limit,
-                                           float2 (&l)[2], uint32_t (&pk)[16]) {
-#pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    const int col = c * 32 + i;
-    const float d0 = __uint_as_float(sr[i]), d1 = __uint_as_float(sr[i + 1]);
-    const float g0 = log2_phi(d0 * scale, fabsf(d0) * c2, eps);
-    const float g1 = log2_phi(d1 * scale, fabsf(d1) * c2, eps);
-    float2 pr = make_float2(ex2_approx(fmaf(tau, g0, neg_m)), ex2_approx(fmaf(tau, g1, neg_m)));
-    if (PARTIAL) {
-      pr.x = col < limit ? pr.x : 0.f;
-      pr.y = col + 1 < limit ? pr.y : 0.f;
-    }
-    l[(i >> 1) & 1] = __fadd2_rn(l[(i >> 1) & 1], pr);
-    pk[i >> 1] = pack_bf16x2(pr.x, pr.y);
-  }
-}
-
 template <int VARIANT, int DK, int DV>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
@@ -330,6 +234,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int nkv = max(nkv_x[0], nkv_x[1]);
 #ifdef CATTN_TRACE
   const int tr_slot = (pair == p.n_pairs - 1 && bh < 8) ? bh : -1;
+  if (threadIdx.x == 0 && blockIdx.x < 16384) {
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    g_cta_trace[blockIdx.x][0] = globaltimer_ns();
+    g_cta_trace[blockIdx.x][2] = smid;
+    g_cta_trace[blockIdx.x][3] = pair;
+  }
 #endif
 
   if (threadIdx.x == 0) {
@@ -647,6 +558,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+#ifdef CATTN_TRACE
+  if (threadIdx.x == 0 && blockIdx.x < 16384) g_cta_trace[blockIdx.x][1] = globaltimer_ns();
+#endif
 }
 
 template <int VARIANT, int DK, int DV>

@@ -1,0 +1,124 @@
+// maps.cuh -- the three score-to-weight maps over one 32-key chunk of one
+// query row (one thread = one row, the chunk's raw dot products in registers),
+// as the tensor-core forward applies them between the two MMAs.
+//
+//   Yat      kappa = (q.k + b)^2 / max(|q|^2 + |k|^2 - 2 q.k + eps, eps)
+//            ("Softmax-Free Attention in JAX/Flax NNX", section "One module,
+//            two compatibility functions": (dots + b)^2 / (max(d2, 0) + eps),
+//            with d2 assembled from the norms and the same dot products)
+//   softmax  2^(scale log2(e) q.k - m)
+//   s^tau    2^(tau log2(softplus(scale q.k) + eps) - m)  ("s^tau: a focal-length
+//            knob for attention": phi^tau with phi = softplus(s) + eps, taken in
+//            the log domain so that phi^tau cannot overflow)
+#pragma once
+
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace cattn {
+namespace tc {
+
+__device__ __forceinline__ float2 f2(uint32_t a, uint32_t b) {
+  return make_float2(__uint_as_float(a), __uint_as_float(b));
+}
+
+// Yat map over one 32-key chunk (columns 32c .. 32c+31 of the tile) of one row.  sr: raw
+// dots; nk2: squared key norms of the tile (pairs); qe = |q|^2 + eps.
+// kappa = (dot + b)^2 / max(|q|^2 + |k|^2 - 2 dot + eps, eps); masked keys
+// (col >= limit) get kappa = 0.
+template <bool PARTIAL>
+__device__ __forceinline__ void yat_chunk(const uint32_t (&sr)[32], int c, const float2 *nk2,
+                                          float yb, float qe, float yeps, int limit,
+                                          float2 (&mass)[2], float (&top)[2],
+                                          uint32_t (&pk)[16]) {
+  const float2 b2 = make_float2(yb, yb), qe2 = make_float2(qe, qe);
+  const float2 m2 = make_float2(-2.f, -2.f);
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const int col = c * 32 + i;
+    const int chain = (i >> 1) & 1;
+    const float2 d = f2(sr[i], sr[i + 1]);
+    const float2 t = __fadd2_rn(d, b2);
+    const float2 num = __fmul2_rn(t, t);
+    const float2 den = __ffma2_rn(m2, d, __fadd2_rn(qe2, nk2[col >> 1]));
+    const float2 r = make_float2(rcp_approx(fmaxf(den.x, yeps)), rcp_approx(fmaxf(den.y, yeps)));
+    float2 k = __fmul2_rn(num, r);
+    if (PARTIAL) {
+      k.x = col < limit ? k.x : 0.f;
+      k.y = col + 1 < limit ? k.y : 0.f;
+    }
+    mass[chain] = __fadd2_rn(mass[chain], k);
+    top[chain] = max3(top[chain], k.x, k.y);
+    pk[i >> 1] = pack_bf16x2(k.x, k.y);
+  }
+}
+
+// Max of the raw dot over the allowed keys of one 32-key chunk (masked -> -inf).
+template <bool PARTIAL>
+__device__ __forceinline__ float chunk_max(const uint32_t (&sr)[32], int c, int limit) {
+  float m[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const int col = c * 32 + i;
+    float x0 = __uint_as_float(sr[i]), x1 = __uint_as_float(sr[i + 1]);
+    if (PARTIAL) {
+      x0 = col < limit ? x0 : -INFINITY;
+      x1 = col + 1 < limit ? x1 : -INFINITY;
+    }
+    m[(i >> 1) & 1] = max3(m[(i >> 1) & 1], x0, x1);
+  }
+  return fmaxf(m[0], m[1]);
+}
+
+// softmax over one 32-key chunk: p = 2^(dot * c2 - m), c2 = scale * log2(e).
+template <bool PARTIAL>
+__device__ __forceinline__ void softmax_chunk(const uint32_t (&sr)[32], int c, float c2,
+                                              float neg_m, int limit, float2 (&l)[2],
+                                              uint32_t (&pk)[16]) {
+  const float2 c22 = make_float2(c2, c2), nm2 = make_float2(neg_m, neg_m);
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const int col = c * 32 + i;
+    const float2 x = __ffma2_rn(f2(sr[i], sr[i + 1]), c22, nm2);
+    float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    if (PARTIAL) {
+      pr.x = col < limit ? pr.x : 0.f;
+      pr.y = col + 1 < limit ? pr.y : 0.f;
+    }
+    l[(i >> 1) & 1] = __fadd2_rn(l[(i >> 1) & 1], pr);
+    pk[i >> 1] = pack_bf16x2(pr.x, pr.y);
+  }
+}
+
+// log2(softplus(s) + eps), softplus(s) = max(s, 0) + ln(1 + 2^(-|s| log2 e)).
+__device__ __forceinline__ float log2_phi(float s, float abs_s_log2e, float eps) {
+  constexpr float LN2 = 0.6931471805599453f;
+  const float e = ex2_approx(-abs_s_log2e);
+  const float l1p = e < 0x1p-12f ? e : lg2_approx(1.f + e) * LN2;
+  return lg2_approx(fmaxf(s, 0.f) + l1p + eps);
+}
+
+// s^tau over one 32-key chunk: p = 2^(tau log2 phi(s) - m).
+template <bool PARTIAL>
+__device__ __forceinline__ void stau_chunk(const uint32_t (&sr)[32], int c, float scale, float c2,
+                                           float tau, float eps, float neg_m, int limit,
+                                           float2 (&l)[2], uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const int col = c * 32 + i;
+    const float d0 = __uint_as_float(sr[i]), d1 = __uint_as_float(sr[i + 1]);
+    const float g0 = log2_phi(d0 * scale, fabsf(d0) * c2, eps);
+    const float g1 = log2_phi(d1 * scale, fabsf(d1) * c2, eps);
+    float2 pr = make_float2(ex2_approx(fmaf(tau, g0, neg_m)), ex2_approx(fmaf(tau, g1, neg_m)));
+    if (PARTIAL) {
+      pr.x = col < limit ? pr.x : 0.f;
+      pr.y = col + 1 < limit ? pr.y : 0.f;
+    }
+    l[(i >> 1) & 1] = __fadd2_rn(l[(i >> 1) & 1], pr);
+    pk[i >> 1] = pack_bf16x2(pr.x, pr.y);
+  }
+}
+
+}  // namespace tc
+}  // namespace cattn
