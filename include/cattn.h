@@ -80,8 +80,10 @@ enum {
   CATTN_ERR_UNSUPPORTED = 3, /* head width not in the supported set, pointer not 16-byte
                                 aligned, device is not sm_103 */
   CATTN_ERR_CUDA = 4,        /* a CUDA runtime or driver call failed */
-  CATTN_ERR_TIMEOUT = 5      /* a kernel gave up on a bounded wait (reported by
+  CATTN_ERR_TIMEOUT = 5,     /* a kernel gave up on a bounded wait (reported by
                                 cattn_check_status) */
+  CATTN_ERR_SCRATCH_LIMIT = 6 /* the problem needs more scratch than cattn_forward_noalloc's
+                                 fixed array holds */
 };
 
 typedef struct {
@@ -137,6 +139,31 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
                   const void *v, const float *b, const float *eps, const float *tau, void *out,
                   float *row_mass, float *row_max_score, void *workspace,
                   size_t workspace_bytes, cattn_stream_t stream);
+
+/* The same forward for callers that cannot allocate device memory (a plug-in
+ * whose host engine plans all device memory at start-up and forbids later
+ * allocations, or a latency-critical loop that cannot afford cudaMalloc's
+ * implicit synchronisation).  The source pages have no counterpart: this is a
+ * library convenience, not part of the method.
+ *
+ * Arguments as cattn_forward, minus the workspace: the scratch comes from a
+ * fixed 16 MiB array of device memory inside the library, which every GPU that
+ * loads the library holds until the process exits.  Problems whose
+ * cattn_workspace_bytes() exceeds 16 MiB (bf16 Yat with B*h*Tq + B*hkv*Tk_pad
+ * above about 4.19 million rows) are rejected with CATTN_ERR_SCRATCH_LIMIT
+ * before anything is enqueued; CATTN_FLAG_NORMS_READY is rejected with
+ * CATTN_ERR_INVALID_ARG.  Nothing is allocated or freed.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array and each rewrites what it reads, so
+ * calls in sequence are independent, but calls that can overlap on the GPU
+ * (different streams, or several threads) race on it and must be serialised by
+ * the caller. */
+int cattn_forward_noalloc(int variant, const cattn_problem_t *p, const void *q, const void *k,
+                          const void *v, const float *b, const float *eps, const float *tau,
+                          void *out, float *row_mass, float *row_max_score,
+                          cattn_stream_t stream);
 
 /* Synchronises `stream`, then reports (and clears) the device-side status
  * word the kernels set when a bounded wait gives up: CATTN_ERR_TIMEOUT if

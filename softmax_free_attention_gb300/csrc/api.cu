@@ -116,6 +116,7 @@ const char *cattn_error_string(int status) {
     case CATTN_ERR_UNSUPPORTED: return "unsupported configuration";
     case CATTN_ERR_CUDA: return "CUDA error";
     case CATTN_ERR_TIMEOUT: return "kernel wait timed out";
+    case CATTN_ERR_SCRATCH_LIMIT: return "problem exceeds the fixed scratch of cattn_forward_noalloc";
     default: return "unknown status";
   }
 }

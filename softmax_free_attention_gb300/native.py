@@ -22,10 +22,11 @@ ERR_SHAPE = 2
 ERR_UNSUPPORTED = 3
 ERR_CUDA = 4
 ERR_TIMEOUT = 5
+ERR_SCRATCH_LIMIT = 6
 
 # every symbol include/cattn.h declares
 EXPORTS = ("cattn_version", "cattn_error_string", "cattn_workspace_bytes", "cattn_validate",
-           "cattn_row_norms", "cattn_forward", "cattn_check_status")
+           "cattn_row_norms", "cattn_forward", "cattn_forward_noalloc", "cattn_check_status")
 
 
 class Problem(ctypes.Structure):
@@ -71,6 +72,8 @@ def load():
     lib.cattn_row_norms.restype = i
     lib.cattn_forward.argtypes = [i, pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.cattn_forward.restype = i
+    lib.cattn_forward_noalloc.argtypes = [i, pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.cattn_forward_noalloc.restype = i
     lib.cattn_check_status.argtypes = [vp]
     lib.cattn_check_status.restype = i
     _lib = lib

@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_error_strings(lib):
-    for code in range(6):
+    for code in range(7):
         assert lib.cattn_error_string(code)
     assert lib.cattn_error_string(99) == b"unknown status"
 
