@@ -107,10 +107,15 @@ int cattn_version(void);
 const char *cattn_error_string(int status);
 
 /* Bytes of device workspace cattn_forward / cattn_row_norms need for this
- * problem and variant (0 if none).  Only the bf16 Yat path uses workspace:
- * fp32 squared norms of every query row and of every key row, the key part
- * padded to a multiple of 128 rows per head.  Returns 0 for an invalid
- * problem as well; cattn_validate says why. */
+ * problem and variant (0 if none), 256-byte aligned.  The fp32 path needs
+ * none.  The bf16 path needs 256 bytes for its work-unit ticket, plus, for
+ * CATTN_YAT, the fp32 squared norms of every query row and of every key row
+ * (the key part padded to a multiple of 128 rows per head), plus, for
+ * non-causal problems with few (batch, head, 256-row) units, the fp32 partial
+ * outputs and per-row statistics of a fixed split of the keys (at most 64
+ * splits, chosen from the shape alone).  The contents need not be
+ * initialised.  Returns 0 for an invalid problem as well; cattn_validate says
+ * why. */
 size_t cattn_workspace_bytes(int variant, const cattn_problem_t *p);
 
 /* Host-side argument checks only: never touches the GPU, never dereferences
@@ -149,10 +154,12 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
  * Arguments as cattn_forward, minus the workspace: the scratch comes from a
  * fixed 16 MiB array of device memory inside the library, which every GPU that
  * loads the library holds until the process exits.  Problems whose
- * cattn_workspace_bytes() exceeds 16 MiB (bf16 Yat with B*h*Tq + B*hkv*Tk_pad
- * above about 4.19 million rows) are rejected with CATTN_ERR_SCRATCH_LIMIT
- * before anything is enqueued; CATTN_FLAG_NORMS_READY is rejected with
- * CATTN_ERR_INVALID_ARG.  Nothing is allocated or freed.
+ * cattn_workspace_bytes() exceeds 16 MiB (for causal bf16 Yat: B*h*Tq +
+ * B*hkv*Tk_pad above about 4.19 million rows; non-causal problems whose keys
+ * are split need room for the partial outputs as well) are rejected with
+ * CATTN_ERR_SCRATCH_LIMIT before anything is enqueued;
+ * CATTN_FLAG_NORMS_READY is rejected with CATTN_ERR_INVALID_ARG.  Nothing is
+ * allocated or freed.
  *
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream

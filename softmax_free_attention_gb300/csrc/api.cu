@@ -24,15 +24,49 @@ int tk_pad(const cattn_problem_t *p) { return (p->Tk + kTile - 1) / kTile * kTil
 
 bool is_empty(const cattn_problem_t *p) { return p->B == 0 || p->h == 0 || p->Tq == 0; }
 
-// Workspace layout (bf16 Yat only): nq [B*h, Tq] then nk [B*hkv, Tk_pad], fp32.
+// Workspace layout of the bf16 (tensor-core) path, each part 256-byte aligned:
+//   ctrl       256 B: the persistent schedule's unit ticket (zeroed per call)
+//   nq, nk     Yat only: squared q row norms [B*h, Tq], squared k row norms
+//              [B*hkv, Tk_pad], fp32
+//   part_o     key splits only: unnormalised partial outputs
+//              [n_splits, B*h, Tq, dv] fp32
+//   part_stat  key splits only: per-row [n_splits, B*h, Tq, 4] fp32
+// The fp32 (CUDA-core) path needs none.
 size_t ws_nq_bytes(const cattn_problem_t *p) {
   return align256((size_t)p->B * p->h * p->Tq * sizeof(float));
 }
 size_t ws_nk_bytes(const cattn_problem_t *p) {
   return align256((size_t)p->B * p->hkv * tk_pad(p) * sizeof(float));
 }
-bool needs_workspace(int variant, const cattn_problem_t *p) {
-  return variant == CATTN_YAT && p->dtype == CATTN_BF16;
+
+struct WsLayout {
+  size_t ctrl, nq, nk, part_o, part_stat, total;
+  TcSchedule sched;
+};
+
+WsLayout ws_layout(int variant, const cattn_problem_t *p) {
+  WsLayout w;
+  memset(&w, 0, sizeof(w));
+  if (p->dtype != CATTN_BF16) return w;
+  w.sched = tc_schedule(p->B, p->h, p->Tq, p->Tk, p->causal);
+  size_t off = 0;
+  w.ctrl = off;
+  off += 256;
+  if (variant == CATTN_YAT) {
+    w.nq = off;
+    off += ws_nq_bytes(p);
+    w.nk = off;
+    off += ws_nk_bytes(p);
+  }
+  if (w.sched.n_splits > 1) {
+    const size_t rows = (size_t)w.sched.n_splits * p->B * p->h * p->Tq;
+    w.part_o = off;
+    off += align256(rows * p->dv * sizeof(float));
+    w.part_stat = off;
+    off += align256(rows * 4 * sizeof(float));
+  }
+  w.total = off;
+  return w;
 }
 
 int check_problem(int variant, const cattn_problem_t *p) {
@@ -55,6 +89,9 @@ int check_problem(int variant, const cattn_problem_t *p) {
       (long long)p->Tk * p->dv > (1ll << 31))
     return CATTN_ERR_UNSUPPORTED;
   if ((long long)p->B * p->h > (1ll << 24)) return CATTN_ERR_UNSUPPORTED;
+  // the persistent schedule numbers its units with 32-bit ints
+  if (p->dtype == CATTN_BF16 && tc_schedule(p->B, p->h, p->Tq, p->Tk, p->causal).n_units > (1ll << 30))
+    return CATTN_ERR_UNSUPPORTED;
   return CATTN_OK;
 }
 
@@ -123,8 +160,7 @@ const char *cattn_error_string(int status) {
 
 size_t cattn_workspace_bytes(int variant, const cattn_problem_t *p) {
   if (check_problem(variant, p) != CATTN_OK) return 0;
-  if (!needs_workspace(variant, p)) return 0;
-  return ws_nq_bytes(p) + ws_nk_bytes(p);
+  return ws_layout(variant, p).total;
 }
 
 int cattn_validate(int variant, const cattn_problem_t *p, const void *q, const void *k,
@@ -138,9 +174,10 @@ int cattn_validate(int variant, const cattn_problem_t *p, const void *q, const v
   if (variant == CATTN_STAU && (!eps || !tau)) return CATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return CATTN_ERR_UNSUPPORTED;
-  if (needs_workspace(variant, p)) {
+  const size_t need = ws_layout(variant, p).total;
+  if (need > 0) {
     if (!workspace) return CATTN_ERR_INVALID_ARG;
-    if (workspace_bytes < ws_nq_bytes(p) + ws_nk_bytes(p)) return CATTN_ERR_SHAPE;
+    if (workspace_bytes < need) return CATTN_ERR_SHAPE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CATTN_ERR_UNSUPPORTED;
   }
   return CATTN_OK;
@@ -155,12 +192,13 @@ int cattn_row_norms(const cattn_problem_t *p, const void *q, const void *k, void
   if (!q || !k || !workspace) return CATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return CATTN_ERR_UNSUPPORTED;
-  if (workspace_bytes < ws_nq_bytes(p) + ws_nk_bytes(p)) return CATTN_ERR_SHAPE;
+  const WsLayout w = ws_layout(CATTN_YAT, p);
+  if (workspace_bytes < w.total) return CATTN_ERR_SHAPE;
   rc = check_device();
   if (rc != CATTN_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  float *nq = static_cast<float *>(workspace);
-  float *nk = reinterpret_cast<float *>(static_cast<char *>(workspace) + ws_nq_bytes(p));
+  float *nq = reinterpret_cast<float *>(static_cast<char *>(workspace) + w.nq);
+  float *nk = reinterpret_cast<float *>(static_cast<char *>(workspace) + w.nk);
   rc = map_cuda(launch_row_sqnorm_bf16(q, nq, p->B * p->h, p->Tq, p->Tq, p->dk, s));
   if (rc != CATTN_OK) return rc;
   return map_cuda(launch_row_sqnorm_bf16(k, nk, p->B * p->hkv, p->Tk, tk_pad(p), p->dk, s));
@@ -197,14 +235,25 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
   fp.causal = p->causal ? 1 : 0;
   fp.scale = p->scale;
   fp.n_qtiles = (p->Tq + kTcQueryTile - 1) / kTcQueryTile;
-  fp.n_pairs = (fp.n_qtiles + 1) / 2;  // two query tiles per CTA
+  fp.n_pairs = (fp.n_qtiles + 1) / 2;  // two query tiles per work unit
   fp.n_kv_tiles = (p->Tk + kTcKeyTile - 1) / kTcKeyTile;
 
   if (p->dtype == CATTN_F32) return map_cuda(launch_fwd_simt(variant, p->dk, p->dv, fp, s));
 
+  const WsLayout w = ws_layout(variant, p);
+  char *ws = static_cast<char *>(workspace);
+  fp.n_splits = w.sched.n_splits;
+  fp.kv_per_split = w.sched.kv_per_split;
+  fp.head_group = w.sched.head_group;
+  fp.n_units = (int)w.sched.n_units;
+  fp.tile_counter = reinterpret_cast<unsigned int *>(ws + w.ctrl);
+  if (w.sched.n_splits > 1) {
+    fp.part_o = reinterpret_cast<float *>(ws + w.part_o);
+    fp.part_stat = reinterpret_cast<float *>(ws + w.part_stat);
+  }
   if (variant == CATTN_YAT) {
-    fp.nq = static_cast<const float *>(workspace);
-    fp.nk = reinterpret_cast<const float *>(static_cast<const char *>(workspace) + ws_nq_bytes(p));
+    fp.nq = reinterpret_cast<const float *>(ws + w.nq);
+    fp.nk = reinterpret_cast<const float *>(ws + w.nk);
     if (!(p->flags & CATTN_FLAG_NORMS_READY)) {
       rc = cattn_row_norms(p, q, k, workspace, workspace_bytes, stream);
       if (rc != CATTN_OK) return rc;
@@ -214,6 +263,8 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
   if ((rc = encode_bf16_3d(&tq, q, p->dk, p->Tq, p->B * p->h, kTcQueryTile)) != CATTN_OK) return rc;
   if ((rc = encode_bf16_3d(&tk, k, p->dk, p->Tk, p->B * p->hkv, kTcKeyTile)) != CATTN_OK) return rc;
   if ((rc = encode_bf16_3d(&tv, v, p->dv, p->Tk, p->B * p->hkv, kTcKeyTile)) != CATTN_OK) return rc;
+  if ((rc = map_cuda(cudaMemsetAsync(fp.tile_counter, 0, sizeof(unsigned int), s))) != CATTN_OK)
+    return rc;
   return map_cuda(launch_fwd_tc(variant, p->dk, p->dv, fp, tq, tk, tv, s));
 }
 

@@ -1,8 +1,10 @@
 // fwd_tc.cu -- fused attention forward on the sm_103a tensor cores.
 //
-// One CTA owns two 128-row query tiles (Q0, Q1) of one (batch, head) and
-// streams 128-key K/V tiles through shared memory, so every K/V tile that
-// reaches the SM serves 256 query rows.  Per KV tile j and query tile x:
+// A persistent kernel: one CTA per SM works through a list of units, each
+// unit two 128-row query tiles (Q0, Q1) of one (batch, head) -- and, for
+// non-causal problems with few units, one split of the keys.  K/V tiles of
+// 128 keys stream through shared memory, so every tile that reaches the SM
+// serves 256 query rows.  Per key tile j and query tile x:
 //
 //   S_x = Q_x K_j^T     tcgen05.mma, A and B from shared memory -> TMEM fp32
 //   P_x = map(S_x)      eight map warps of tile x: tcgen05.ld S, apply the
@@ -22,11 +24,23 @@
 //            running max of tau log2 phi, taken from the max raw score since
 //            phi is increasing.
 //
+// Schedule.  The producer warp hands out units: its CTA's first unit is
+// blockIdx.x, every later one comes from an atomic ticket in the workspace,
+// so CTAs that drew light units take more of them.  Units are ordered so that
+// the units of a group of (batch, head) pairs run together (their K/V stays in
+// L2) and, for causal problems, heaviest first.  A two-entry unit ring in
+// shared memory passes each unit number to the MMA warp and the map warps.
+// Key splits leave unnormalised partial outputs and per-row statistics in the
+// workspace; a small combine kernel merges them (Yat: plain sums of O and of
+// the mass; softmax and s^tau: onto the largest running max first).
+//
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512).  P_x
 // is written over S_x; the MMA pipe executes a CTA's MMAs in issue order, so
 // PV_x(j) reads P_x before S_x(j+1) lands, and the commit that signals S_x(j)
 // also covers PV_x(j-1).  The MMA order PV0(j-1) S0(j) PV1(j-1) S1(j) lets
-// one query tile's MMAs run while the other tile is being mapped.
+// one query tile's MMAs run while the other tile is being mapped.  Between
+// units the next unit's S MMAs follow the last PVs at once; its first PV_x
+// waits (o_empty) until the map warps have read O_x out.
 //
 // Warp roles (576 threads): warps 0-15 map (warp w: query tile x = w/8, TMEM
 // lanes 32*(w%4)..+31 = those query rows, key columns [64h, 64h+64) with
@@ -48,25 +62,6 @@ namespace cattn {
 
 __device__ unsigned int g_status;
 
-#ifdef CATTN_TRACE
-// Optional per-tile clock64 trace of the first CTAs (compiled out by default).
-__device__ unsigned long long g_trace[8][12][160];
-extern "C" int cattn_trace_read(void *host, size_t bytes) {
-  return (int)cudaMemcpyFromSymbol(host, g_trace, bytes);
-}
-__device__ unsigned long long g_cta_trace[16384][4];
-extern "C" int cattn_cta_trace_read(void *host, size_t bytes) {
-  return (int)cudaMemcpyFromSymbol(host, g_cta_trace, bytes);
-}
-#define CATTN_TR(ev, j)                                          \
-  do {                                                           \
-    if (tr_slot >= 0 && (j) < 160) g_trace[tr_slot][ev][(j)] = clock64(); \
-  } while (0)
-#else
-#define CATTN_TR(ev, j) \
-  do {                  \
-  } while (0)
-#endif
 
 namespace tc {
 
@@ -110,10 +105,11 @@ struct Layout {
   static constexpr int OFF_XCHG = OFF_NK + NKS * BN * 4;
   static constexpr int XCHG_FLOATS = 16 * BM;
   static constexpr int OFF_BAR = OFF_XCHG + XCHG_FLOATS * 4;
-  // q_full, kv_full[NS], kv_empty[NS], nk_full[NKS], nk_empty[NKS],
-  // s_full[2], p_full[2], o_full[2], drain
-  static constexpr int NBAR = 1 + 2 * NS + 2 * NKS + 7;
+  // q_full, q_empty, kv_full[NS], kv_empty[NS], nk_full[NKS], nk_empty[NKS],
+  // s_full[2], p_full[2], o_full[2], o_empty[2], unit_full[2], unit_empty[2], drain
+  static constexpr int NBAR = 2 + 2 * NS + 2 * NKS + 13;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  // TMEM base address, abort flag, unit ring[2]
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int ALLOC = BYTES + 1024;  // room to align the base to 1024 B
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
@@ -182,6 +178,51 @@ __device__ __forceinline__ void scale_o_half(uint32_t t_o, float f) {
   }
 }
 
+// One work unit: (batch*head, query-tile pair, key split), decoded the same
+// way by every role.
+struct Unit {
+  int bh, batch, head, bh_kv;
+  int q0;          // first query row of the pair
+  int split;       // key split (0 without splits)
+  int kv_begin;    // first key tile
+  int n[2];        // key tiles of query tile 0 and 1 (0: the tile does not exist)
+  int nkv;         // key tiles loaded for the pair: max(n[0], n[1])
+};
+
+// Units are ordered group by group of p.head_group (batch, head) pairs; inside
+// a group by pair (causal: heaviest first), then split, then (batch, head).  A
+// group's K/V stays in L2 while its units run, and the light units come last.
+__device__ __forceinline__ Unit decode_unit(const FwdParams &p, int u) {
+  Unit t;
+  const int BH = p.B * p.h;
+  const int per_bh = p.n_pairs * p.n_splits;
+  const int g = u / (p.head_group * per_bh);
+  const int base = g * p.head_group;
+  const int gs = min(p.head_group, BH - base);
+  int rem = u - g * p.head_group * per_bh;
+  const int pp = rem / (p.n_splits * gs);
+  rem -= pp * p.n_splits * gs;
+  t.split = rem / gs;
+  t.bh = base + (rem - t.split * gs);
+  const int pair = p.causal ? p.n_pairs - 1 - pp : pp;
+  t.head = t.bh % p.h;
+  t.batch = t.bh / p.h;
+  t.bh_kv = t.batch * p.hkv + t.head / (p.h / p.hkv);
+  t.q0 = pair * 2 * BM;
+  const bool q1_valid = (t.q0 + BM) < p.Tq;
+  if (p.causal) {  // keys 0 .. last row of the query tile
+    t.kv_begin = 0;
+    t.n[0] = min(2 * pair + 1, p.n_kv_tiles);
+    t.n[1] = q1_valid ? min(2 * pair + 2, p.n_kv_tiles) : 0;
+  } else {
+    t.kv_begin = t.split * p.kv_per_split;
+    t.n[0] = min(p.n_kv_tiles - t.kv_begin, p.kv_per_split);
+    t.n[1] = q1_valid ? t.n[0] : 0;
+  }
+  t.nkv = max(t.n[0], t.n[1]);
+  return t;
+}
+
 template <int VARIANT, int DK, int DV>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
@@ -196,55 +237,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int lane = threadIdx.x & 31;
 
   const uint32_t bar0 = sb + L::OFF_BAR;
-  const uint32_t bar_q = bar0;
-  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (1 + L::NS + s); };
-  auto nk_full = [&](int s) { return bar0 + 8u * (1 + 2 * L::NS + s); };
-  auto nk_empty = [&](int s) { return bar0 + 8u * (1 + 2 * L::NS + NKS + s); };
-  constexpr int B2 = 1 + 2 * L::NS + 2 * NKS;
+  const uint32_t bar_q_full = bar0;
+  const uint32_t bar_q_empty = bar0 + 8u;
+  auto kv_full = [&](uint32_t s) { return bar0 + 8u * (2 + s); };
+  auto kv_empty = [&](uint32_t s) { return bar0 + 8u * (2 + L::NS + s); };
+  auto nk_full = [&](uint32_t s) { return bar0 + 8u * (2 + 2 * L::NS + s); };
+  auto nk_empty = [&](uint32_t s) { return bar0 + 8u * (2 + 2 * L::NS + NKS + s); };
+  constexpr int B2 = 2 + 2 * L::NS + 2 * NKS;
   auto s_full = [&](int x) { return bar0 + 8u * (B2 + x); };
   auto p_full = [&](int x) { return bar0 + 8u * (B2 + 2 + x); };
   auto o_full = [&](int x) { return bar0 + 8u * (B2 + 4 + x); };
-  const uint32_t bar_drain = bar0 + 8u * (B2 + 6);
+  auto o_empty = [&](int x) { return bar0 + 8u * (B2 + 6 + x); };
+  auto unit_full = [&](uint32_t s) { return bar0 + 8u * (B2 + 8 + s); };
+  auto unit_empty = [&](uint32_t s) { return bar0 + 8u * (B2 + 10 + s); };
+  const uint32_t bar_drain = bar0 + 8u * (B2 + 12);
   auto q_smem = [&](int x) { return sb + L::OFF_Q + (uint32_t)x * L::Q_TILE; };
-  auto slot_smem = [&](int s) { return sb + L::OFF_RING + (uint32_t)s * L::SLOT; };
+  auto slot_smem = [&](uint32_t s) { return sb + L::OFF_RING + s * L::SLOT; };
   const float *nk_ring = reinterpret_cast<const float *>(smem + L::OFF_NK);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
-
-  // ---- work unit: (batch, head, query-tile pair).  The pairs of one head are
-  // consecutive, so its K/V stays in L2 while they run; causal pairs go
-  // heaviest first.
-  const int bh = blockIdx.x / p.n_pairs;
-  int pair = blockIdx.x - bh * p.n_pairs;
-  if (p.causal) pair = p.n_pairs - 1 - pair;
-  const int head = bh % p.h;
-  const int batch = bh / p.h;
-  const int bh_kv = batch * p.hkv + head / (p.h / p.hkv);
-  const int q0 = pair * 2 * BM;
-  const bool q1_valid = (q0 + BM) < p.Tq;
-  int nkv_x[2];
-  if (p.causal) {  // keys 0 .. last row of the query tile
-    nkv_x[0] = min(2 * pair + 1, p.n_kv_tiles);
-    nkv_x[1] = q1_valid ? min(2 * pair + 2, p.n_kv_tiles) : 0;
-  } else {
-    nkv_x[0] = p.n_kv_tiles;
-    nkv_x[1] = q1_valid ? p.n_kv_tiles : 0;
-  }
-  const int nkv = max(nkv_x[0], nkv_x[1]);
-#ifdef CATTN_TRACE
-  const int tr_slot = (pair == p.n_pairs - 1 && bh < 8) ? bh : -1;
-  if (threadIdx.x == 0 && blockIdx.x < 16384) {
-    unsigned smid;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-    g_cta_trace[blockIdx.x][0] = globaltimer_ns();
-    g_cta_trace[blockIdx.x][2] = smid;
-    g_cta_trace[blockIdx.x][3] = pair;
-  }
-#endif
+  volatile int *unit_ring = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 8);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
+    mbar_init(bar_q_full, 1);
+    mbar_init(bar_q_empty, 1);
     for (int s = 0; s < L::NS; ++s) {
       mbar_init(kv_full(s), 1);
       mbar_init(kv_empty(s), 1);
@@ -255,8 +271,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(s_full(x), 1);
-      mbar_init(p_full(x), 8 * 32);  // the eight map warps of query tile x
+      mbar_init(p_full(x), 8 * 32);  // every thread of the eight map warps of tile x
       mbar_init(o_full(x), 1);
+      mbar_init(o_empty(x), 8);      // lane 0 of each of those warps
+      mbar_init(unit_full(x), 1);
+      mbar_init(unit_empty(x), 1 + MAP_WARPS);  // the MMA warp and every map warp
     }
     mbar_init(bar_drain, 1);
     *abort = 0;
@@ -276,109 +295,153 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
+  // Every consumer role reads unit number uc from the two-entry unit ring
+  // (-1 at the end of the schedule, or on abort) and releases the entry when
+  // it has finished the unit, so the entry stays readable meanwhile.
+  auto peek_unit = [&](uint32_t uc, unsigned site) -> int {
+    if (!warp_wait(unit_full(uc & 1u), (uc >> 1) & 1u, abort, site)) return -1;
+    return unit_ring[uc & 1u];
+  };
+  auto release_unit = [&](uint32_t uc) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(unit_empty(uc & 1u));
+  };
+
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bar_q, (q1_valid ? 2u : 1u) * (uint32_t)L::Q_TILE);
-#pragma unroll
-      for (int c = 0; c < DK / 64; ++c) {
-        tma_load_3d(q_smem(0) + c * BM * 128, &tm_q, c * 64, q0, bh, bar_q);
-        if (q1_valid) tma_load_3d(q_smem(1) + c * BM * 128, &tm_q, c * 64, q0 + BM, bh, bar_q);
+    // Hands out units (the first one is blockIdx.x, later ones come from the
+    // global ticket) and loads each unit's Q pair, then its K/V tiles (and key
+    // norms) through the rings.  Ring positions run on across units.
+    int u = blockIdx.x;
+    uint32_t kv_pos = 0, nk_pos = 0;
+    for (uint32_t uc = 0;; ++uc) {
+      const uint32_t us = uc & 1u;
+      if (!warp_wait(unit_empty(us), ((uc >> 1) & 1u) ^ 1u, abort, SITE_PRODUCER | 0x40)) break;
+      if (lane == 0) {
+        unit_ring[us] = u < p.n_units ? u : -1;
+        mbar_arrive(unit_full(us));
       }
-    }
-    __syncwarp();
-    for (int j = 0; j < nkv; ++j) {
-      {  // K_j
-        const int idx = 2 * j, s = idx % L::NS;
-        const uint32_t use = (uint32_t)(idx / L::NS);
-        if (!warp_wait(kv_empty(s), (use & 1u) ^ 1u, abort, SITE_PRODUCER | 0x10)) break;
-        if (lane == 0) CATTN_TR(9, j);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(kv_full(s), L::K_TILE);
+      __syncwarp();
+      if (u >= p.n_units) break;
+      const Unit t = decode_unit(p, u);
+      // the previous unit's last S MMAs have read both Q tiles
+      if (!warp_wait(bar_q_empty, (uc & 1u) ^ 1u, abort, SITE_PRODUCER | 0x50)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_q_full, (t.n[1] > 0 ? 2u : 1u) * (uint32_t)L::Q_TILE);
 #pragma unroll
-          for (int c = 0; c < DK / 64; ++c)
-            tma_load_3d(slot_smem(s) + c * BN * 128, &tm_k, c * 64, j * BN, bh_kv, kv_full(s));
+        for (int c = 0; c < DK / 64; ++c) {
+          tma_load_3d(q_smem(0) + c * BM * 128, &tm_q, c * 64, t.q0, t.bh, bar_q_full);
+          if (t.n[1] > 0)
+            tma_load_3d(q_smem(1) + c * BM * 128, &tm_q, c * 64, t.q0 + BM, t.bh, bar_q_full);
         }
-        __syncwarp();
       }
-      if (VARIANT == kYat) {  // squared key norms of tile j
-        const int s = j % NKS;
-        const uint32_t use = (uint32_t)(j / NKS);
-        if (!warp_wait(nk_empty(s), (use & 1u) ^ 1u, abort, SITE_PRODUCER | 0x20)) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(nk_full(s), BN * 4);
-          bulk_load(sb + L::OFF_NK + (uint32_t)s * BN * 4,
-                    p.nk + (size_t)bh_kv * p.Tk_pad + (size_t)j * BN, BN * 4, nk_full(s));
-        }
-        __syncwarp();
-      }
-      {  // V_j
-        const int idx = 2 * j + 1, s = idx % L::NS;
-        const uint32_t use = (uint32_t)(idx / L::NS);
-        if (!warp_wait(kv_empty(s), (use & 1u) ^ 1u, abort, SITE_PRODUCER | 0x30)) break;
-        if (lane == 0) CATTN_TR(10, j);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(kv_full(s), L::V_TILE);
-#pragma unroll
-          for (int c = 0; c < DV / 64; ++c)
-            tma_load_3d(slot_smem(s) + c * BN * 128, &tm_v, c * 64, j * BN, bh_kv, kv_full(s));
-        }
-        __syncwarp();
-      }
-    }
-  } else if (warp == MMA_WARP) {
-    // ------------------------------------------------------------ MMA issue
-    // iteration j: PV0(j-1) S0(j) PV1(j-1) S1(j)
-    bool ok = warp_wait(bar_q, 0, abort, SITE_MMA | 0x10);
-    tc_fence_after();
-    uint32_t pph[2] = {0u, 0u};
-    const int release_limit = 2 * nkv - L::NS;  // later slots are never reloaded
-    for (int j = 0; ok && j <= nkv; ++j) {
-      const int vidx = 2 * (j - 1) + 1;
-      const int vs = j >= 1 ? vidx % L::NS : 0;
-      if (j >= 1) {
-        if (!(ok = warp_wait(kv_full(vs), (uint32_t)(vidx / L::NS) & 1u, abort, SITE_MMA | 0x20)))
-          break;
-        CATTN_TR(11, j - 1);
-        tc_fence_after();
-      }
-      const int kidx = 2 * j;
-      const int ks = kidx % L::NS;
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        if (j >= 1 && j - 1 < nkv_x[x]) {  // O_x += P_x(j-1) V(j-1)
-          if (!(ok = warp_wait(p_full(x), pph[x], abort, SITE_MMA | 0x30))) break;
-          pph[x] ^= 1u;
-          if (x == 0) CATTN_TR(6, j - 1);
-          tc_fence_after();
+      __syncwarp();
+      bool ok = true;
+      for (int j = 0; j < t.nkv; ++j) {
+        const int jt = t.kv_begin + j;  // key tile
+        {  // K
+          const uint32_t pos = kv_pos + 2u * j, s = pos % L::NS;
+          if (!(ok = warp_wait(kv_empty(s), ((pos / L::NS) & 1u) ^ 1u, abort, SITE_PRODUCER | 0x10)))
+            break;
           if (lane == 0) {
-            issue_pv<DV>(tmem + TM_O + 128u * x, tmem + TM_S + 128u * x, slot_smem(vs), j - 1 > 0);
-            if (j - 1 == nkv_x[x] - 1) mma_commit(o_full(x));
+            mbar_arrive_expect_tx(kv_full(s), L::K_TILE);
+#pragma unroll
+            for (int c = 0; c < DK / 64; ++c)
+              tma_load_3d(slot_smem(s) + c * BN * 128, &tm_k, c * 64, jt * BN, t.bh_kv, kv_full(s));
           }
           __syncwarp();
         }
-        if (x == 0 && j < nkv) {
-          if (!(ok = warp_wait(kv_full(ks), (uint32_t)(kidx / L::NS) & 1u, abort, SITE_MMA | 0x40)))
+        if (VARIANT == kYat) {  // squared key norms of the tile
+          const uint32_t pos = nk_pos + j, s = pos % NKS;
+          if (!(ok = warp_wait(nk_empty(s), ((pos / NKS) & 1u) ^ 1u, abort, SITE_PRODUCER | 0x20)))
             break;
-          CATTN_TR(7, j);
-          tc_fence_after();
-        }
-        if (j < nkv_x[x]) {  // S_x = Q_x K(j)^T
           if (lane == 0) {
-            issue_qk<DK>(tmem + TM_S + 128u * x, q_smem(x), slot_smem(ks));
-            mma_commit(s_full(x));
+            mbar_arrive_expect_tx(nk_full(s), BN * 4);
+            bulk_load(sb + L::OFF_NK + s * BN * 4,
+                      p.nk + (size_t)t.bh_kv * p.Tk_pad + (size_t)jt * BN, BN * 4, nk_full(s));
+          }
+          __syncwarp();
+        }
+        {  // V
+          const uint32_t pos = kv_pos + 2u * j + 1u, s = pos % L::NS;
+          if (!(ok = warp_wait(kv_empty(s), ((pos / L::NS) & 1u) ^ 1u, abort, SITE_PRODUCER | 0x30)))
+            break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(kv_full(s), L::V_TILE);
+#pragma unroll
+            for (int c = 0; c < DV / 64; ++c)
+              tma_load_3d(slot_smem(s) + c * BN * 128, &tm_v, c * 64, jt * BN, t.bh_kv, kv_full(s));
           }
           __syncwarp();
         }
       }
       if (!ok) break;
-      if (lane == 0) {
-        if (j < nkv && kidx < release_limit) mma_commit(kv_empty(ks));
-        if (j >= 1 && vidx < release_limit) mma_commit(kv_empty(vs));
-        // every map warp delivered P for tile j-1, so all are done with its key norms
-        if (VARIANT == kYat && j >= 1) mbar_arrive(nk_empty((j - 1) % NKS));
+      kv_pos += 2u * t.nkv;
+      nk_pos += t.nkv;
+      if (lane == 0) u = (int)atomicAdd(p.tile_counter, 1u) + (int)gridDim.x;
+      u = __shfl_sync(FULL, u, 0);
+    }
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issue
+    // Per unit, iteration j: PV0(j-1) S0(j) PV1(j-1) S1(j).  The next unit's
+    // S MMAs follow the last PVs of this one directly; its first PV_x waits
+    // until the map warps have read O_x out.
+    uint32_t kv_pos = 0, nk_pos = 0, pph[2] = {0u, 0u}, ou[2] = {0u, 0u};
+    bool ok = true;
+    for (uint32_t uc = 0; ok; ++uc) {
+      const int u = peek_unit(uc, SITE_MMA | 0x70);
+      if (u < 0) break;
+      const Unit t = decode_unit(p, u);
+      if (!(ok = warp_wait(bar_q_full, uc & 1u, abort, SITE_MMA | 0x10))) break;
+      tc_fence_after();
+      for (int j = 0; ok && j <= t.nkv; ++j) {
+        const uint32_t vpos = kv_pos + 2u * j - 1u, vs = vpos % L::NS;
+        const uint32_t kpos = kv_pos + 2u * j, ks = kpos % L::NS;
+        if (j >= 1) {
+          if (!(ok = warp_wait(kv_full(vs), (vpos / L::NS) & 1u, abort, SITE_MMA | 0x20))) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (j >= 1 && j - 1 < t.n[x]) {  // O_x += P_x(j-1) V(j-1)
+            if (!(ok = warp_wait(p_full(x), pph[x], abort, SITE_MMA | 0x30))) break;
+            pph[x] ^= 1u;
+            if (j == 1 && !(ok = warp_wait(o_empty(x), (ou[x] & 1u) ^ 1u, abort, SITE_MMA | 0x50)))
+              break;
+            tc_fence_after();
+            if (lane == 0) {
+              issue_pv<DV>(tmem + TM_O + 128u * x, tmem + TM_S + 128u * x, slot_smem(vs), j > 1);
+              if (j == t.n[x]) mma_commit(o_full(x));
+            }
+            __syncwarp();
+          }
+          if (x == 0 && j < t.nkv) {
+            if (!(ok = warp_wait(kv_full(ks), (kpos / L::NS) & 1u, abort, SITE_MMA | 0x40))) break;
+            tc_fence_after();
+          }
+          if (j < t.n[x]) {  // S_x = Q_x K(j)^T
+            if (lane == 0) {
+              issue_qk<DK>(tmem + TM_S + 128u * x, q_smem(x), slot_smem(ks));
+              mma_commit(s_full(x));
+            }
+            __syncwarp();
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          if (j == t.nkv - 1) mma_commit(bar_q_empty);  // the unit's last S MMAs
+          if (j < t.nkv) mma_commit(kv_empty(ks));
+          if (j >= 1) mma_commit(kv_empty(vs));
+          // every map warp delivered P for tile j-1, so all are done with its key norms
+          if (VARIANT == kYat && j >= 1) mbar_arrive(nk_empty((nk_pos + j - 1) % NKS));
+        }
+        __syncwarp();
       }
-      __syncwarp();
+      kv_pos += 2u * t.nkv;
+      nk_pos += t.nkv;
+      ou[0] += t.n[0] > 0 ? 1u : 0u;
+      ou[1] += t.n[1] > 0 ? 1u : 0u;
+      release_unit(uc);
     }
     // all MMAs issued by this thread have completed once `drain` flips; this
     // wait ignores the abort flag so TMEM is never released under a live MMA
@@ -391,164 +454,205 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int half = (warp >> 2) & 1;  // key columns [64 half, 64 half + 64)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // row in tile == TMEM lane
-    const int nk_tiles = nkv_x[x];
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t t_s = tmem + lane_off + TM_S + 128u * x + 64u * half;
     const uint32_t t_o = tmem + lane_off + TM_O + 128u * x + (uint32_t)half * (DV / 2);
     const uint32_t named_bar = 1u + (uint32_t)(x * 4 + quarter);  // warps w and w^4
     float *xchg = reinterpret_cast<float *>(smem + L::OFF_XCHG);
-    const int row = q0 + x * BM + r;
-    const bool row_ok = row < p.Tq;
-
-    float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // Yat: mass; else l
-    float top[2] = {-INFINITY, -INFINITY};  // Yat: max kappa; else max raw dot
-    float m_used = -INFINITY;               // softmax / s^tau: running max, log2 units
-    float yb = 0.f, yeps = 0.f, qe = 0.f, tau = 1.f, seps = 0.f;
-    if (VARIANT == kYat) {
-      yb = p.b[head];
-      yeps = p.eps[head];
-      qe = (row_ok ? p.nq[(size_t)bh * p.Tq + row] : 0.f) + yeps;
-    } else if (VARIANT == kStau) {
-      tau = p.tau[head];
-      seps = p.eps[head];
-    }
     const float c2 = p.scale * LOG2E;  // scaled score in log2 units per raw dot
-    uint32_t xpar = 0;
-
+    uint32_t xpar = 0, cs = 0, ou = 0, nk_pos = 0;
     bool ok = true;
-    for (int j = 0; j < nk_tiles; ++j) {
-      if (!(ok = warp_wait(s_full(x), (uint32_t)j & 1u, abort, SITE_EPI | 0x10))) break;
-      if (threadIdx.x == 0) CATTN_TR(0, j);
-      tc_fence_after();
 
-      // keys j*BN + col allowed for col < limit (col counts the whole tile)
-      int limit = BN;
-      if (j == p.n_kv_tiles - 1) limit = min(limit, p.Tk - j * BN);
-      if (p.causal) limit = min(limit, row + 1 - j * BN);
-      const bool partial = __any_sync(FULL, limit < BN);  // warp-uniform path choice
-
-      bool rescale = false;
-      float corr = 1.f;
-      if (VARIANT == kYat) {
-        const int ns = j % NKS;
-        if (!(ok = warp_wait(nk_full(ns), (uint32_t)(j / NKS) & 1u, abort, SITE_EPI | 0x20))) break;
-        const float2 *nk2 = reinterpret_cast<const float2 *>(nk_ring + ns * BN);
-        // chunk by chunk: P chunk c lands on S columns this warp has read
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t sr[32];
-          tmem_ld32(t_s + 32 * c, sr);
-          tmem_wait_ld();
-          tmem_ld_fence(sr);
-          uint32_t hk[16];
-          if (partial)
-            yat_chunk<true>(sr, half * 2 + c, nk2, yb, qe, yeps, limit, acc, top, hk);
-          else
-            yat_chunk<false>(sr, half * 2 + c, nk2, yb, qe, yeps, limit, acc, top, hk);
-          tmem_st16(t_s + 16 * c, hk);
-        }
-      } else {
-        uint32_t sr[2][32];
-        tmem_ld32(t_s, sr[0]);
-        tmem_ld32(t_s + 32, sr[1]);
-        tmem_wait_ld();
-        tmem_ld_fence(sr[0]);
-        tmem_ld_fence(sr[1]);
-        float mt = partial ? fmaxf(chunk_max<true>(sr[0], half * 2, limit),
-                                   chunk_max<true>(sr[1], half * 2 + 1, limit))
-                           : fmaxf(chunk_max<false>(sr[0], half * 2, limit),
-                                   chunk_max<false>(sr[1], half * 2 + 1, limit));
-        // the row max over the whole tile: swap halves with the partner warp
-        float *xb = xchg + ((xpar * 2 + (uint32_t)x) * 2) * BM;
-        xb[half * BM + r] = mt;
-        named_barrier_sync(named_bar, 64);
-        mt = fmaxf(mt, xb[(half ^ 1) * BM + r]);
-        xpar ^= 1u;
-        top[0] = fmaxf(top[0], mt);
-        float m_new = -INFINITY;
-        if (mt > -INFINITY) {
-          if (VARIANT == kSoftmax)
-            m_new = mt * c2;
-          else
-            m_new = tau * log2_phi(mt * p.scale, fabsf(mt) * c2, seps);
-        }
-        if (__any_sync(FULL, m_new > m_used + RESCALE_THRESHOLD)) {
-          const float mn = fmaxf(m_used, m_new);
-          corr = ex2_approx(m_used - mn);
-          acc[0].x *= corr;
-          acc[0].y *= corr;
-          acc[1].x *= corr;
-          acc[1].y *= corr;
-          m_used = mn;
-          rescale = j > 0;
-        }
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t hk[16];
-          if (VARIANT == kSoftmax) {
-            if (partial)
-              softmax_chunk<true>(sr[c], half * 2 + c, c2, -m_used, limit, acc, hk);
-            else
-              softmax_chunk<false>(sr[c], half * 2 + c, c2, -m_used, limit, acc, hk);
-          } else {
-            if (partial)
-              stau_chunk<true>(sr[c], half * 2 + c, p.scale, c2, tau, seps, -m_used, limit, acc, hk);
-            else
-              stau_chunk<false>(sr[c], half * 2 + c, p.scale, c2, tau, seps, -m_used, limit, acc, hk);
-          }
-          tmem_st16(t_s + 16 * c, hk);
+    for (uint32_t uc = 0; ok; ++uc) {
+      const int u = peek_unit(uc, SITE_EPI | 0x70);
+      if (u < 0) break;
+      // per unit: key tiles of this query tile, and the allowed-key bound of
+      // this row relative to the unit's first key tile
+      int nk_tiles, lim_base, nkv;
+      float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // Yat: mass; else l
+      float top[2] = {-INFINITY, -INFINITY};  // Yat: max kappa; else max raw dot
+      float m_used = -INFINITY;               // softmax / s^tau: running max, log2 units
+      float yb = 0.f, yeps = 0.f, qe = 0.f, tau = 1.f, seps = 0.f;
+      {
+        const Unit t = decode_unit(p, u);
+        nk_tiles = x ? t.n[1] : t.n[0];
+        nkv = t.nkv;
+        const int row = t.q0 + x * BM + r;
+        lim_base = (p.causal ? min(row + 1, p.Tk) : p.Tk) - t.kv_begin * BN;
+        if (VARIANT == kYat) {
+          yb = p.b[t.head];
+          yeps = p.eps[t.head];
+          qe = (row < p.Tq ? p.nq[(size_t)t.bh * p.Tq + row] : 0.f) + yeps;
+        } else if (VARIANT == kStau) {
+          tau = p.tau[t.head];
+          seps = p.eps[t.head];
         }
       }
-      // O_x holds every tile before j (S_x(j) landed after PV_x(j-1)): bring
-      // this warp's dv/2 columns onto the new max
-      if (rescale) scale_o_half<DV>(t_o, corr);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(p_full(x));
-      if (threadIdx.x == 0) CATTN_TR(2, j);
-    }
 
-    // ---- finalise: combine the two halves of the row, normalise, store
-    if (ok && nk_tiles > 0) {
-      const float part = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
-      const float ptop = fmaxf(top[0], top[1]);
-      float *fb = xchg + (8 + (uint32_t)x * 4) * BM;  // [2 values][2 halves][BM]
-      fb[(0 * 2 + half) * BM + r] = part;
-      fb[(1 * 2 + half) * BM + r] = ptop;
-      named_barrier_sync(named_bar, 64);
-      const float total = part + fb[(0 * 2 + (half ^ 1)) * BM + r];
-      const float all_top = fmaxf(ptop, fb[(1 * 2 + (half ^ 1)) * BM + r]);
-      if (warp_wait(o_full(x), 0, abort, SITE_EPI | 0x30)) {
+      for (int j = 0; j < nk_tiles; ++j, ++cs) {
+        if (!(ok = warp_wait(s_full(x), cs & 1u, abort, SITE_EPI | 0x10))) break;
         tc_fence_after();
-        const float inv = VARIANT == kYat ? 1.f / (total + 1e-9f) : 1.f / total;
-        __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
-                              ((size_t)bh * p.Tq + row) * DV + half * (DV / 2);
+
+        // keys of tile j allowed for col < limit (col counts the whole tile)
+        const int limit = min(BN, lim_base - j * BN);
+        const bool partial = __any_sync(FULL, limit < BN);  // warp-uniform path choice
+
+        bool rescale = false;
+        float corr = 1.f;
+        if (VARIANT == kYat) {
+          const uint32_t npos = nk_pos + j, ns = npos % NKS;
+          if (!(ok = warp_wait(nk_full(ns), (npos / NKS) & 1u, abort, SITE_EPI | 0x20))) break;
+          const float2 *nk2 = reinterpret_cast<const float2 *>(nk_ring + ns * BN);
+          // chunk by chunk: P chunk c lands on S columns this warp has read
 #pragma unroll
-        for (int c = 0; c < DV / 64; ++c) {
-          uint32_t o[32];
-          tmem_ld32(t_o + c * 32, o);
+          for (int c = 0; c < 2; ++c) {
+            uint32_t sr[32];
+            tmem_ld32(t_s + 32 * c, sr);
+            tmem_wait_ld();
+            tmem_ld_fence(sr);
+            uint32_t hk[16];
+            if (partial)
+              yat_chunk<true>(sr, half * 2 + c, nk2, yb, qe, yeps, limit, acc, top, hk);
+            else
+              yat_chunk<false>(sr, half * 2 + c, nk2, yb, qe, yeps, limit, acc, top, hk);
+            tmem_st16(t_s + 16 * c, hk);
+          }
+        } else {
+          uint32_t sr[2][32];
+          tmem_ld32(t_s, sr[0]);
+          tmem_ld32(t_s + 32, sr[1]);
           tmem_wait_ld();
-          tmem_ld_fence(o);
-          uint32_t packed[16];
+          tmem_ld_fence(sr[0]);
+          tmem_ld_fence(sr[1]);
+          float mt = partial ? fmaxf(chunk_max<true>(sr[0], half * 2, limit),
+                                     chunk_max<true>(sr[1], half * 2 + 1, limit))
+                             : fmaxf(chunk_max<false>(sr[0], half * 2, limit),
+                                     chunk_max<false>(sr[1], half * 2 + 1, limit));
+          // the row max over the whole tile: swap halves with the partner warp
+          float *xb = xchg + ((xpar * 2 + (uint32_t)x) * 2) * BM;
+          xb[half * BM + r] = mt;
+          named_barrier_sync(named_bar, 64);
+          mt = fmaxf(mt, xb[(half ^ 1) * BM + r]);
+          xpar ^= 1u;
+          top[0] = fmaxf(top[0], mt);
+          float m_new = -INFINITY;
+          if (mt > -INFINITY) {
+            if (VARIANT == kSoftmax)
+              m_new = mt * c2;
+            else
+              m_new = tau * log2_phi(mt * p.scale, fabsf(mt) * c2, seps);
+          }
+          if (__any_sync(FULL, m_new > m_used + RESCALE_THRESHOLD)) {
+            const float mn = fmaxf(m_used, m_new);
+            corr = ex2_approx(m_used - mn);
+            acc[0].x *= corr;
+            acc[0].y *= corr;
+            acc[1].x *= corr;
+            acc[1].y *= corr;
+            m_used = mn;
+            rescale = j > 0;
+          }
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            packed[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv,
-                                    __uint_as_float(o[2 * i + 1]) * inv);
-          if (row_ok) {
-            uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                  packed[4 * i + 3]);
+          for (int c = 0; c < 2; ++c) {
+            uint32_t hk[16];
+            if (VARIANT == kSoftmax) {
+              if (partial)
+                softmax_chunk<true>(sr[c], half * 2 + c, c2, -m_used, limit, acc, hk);
+              else
+                softmax_chunk<false>(sr[c], half * 2 + c, c2, -m_used, limit, acc, hk);
+            } else {
+              if (partial)
+                stau_chunk<true>(sr[c], half * 2 + c, p.scale, c2, tau, seps, -m_used, limit, acc,
+                                 hk);
+              else
+                stau_chunk<false>(sr[c], half * 2 + c, p.scale, c2, tau, seps, -m_used, limit, acc,
+                                  hk);
+            }
+            tmem_st16(t_s + 16 * c, hk);
           }
         }
-        if (row_ok && half == 0) {
-          const size_t ti = (size_t)bh * p.Tq + row;
-          if (p.row_mass)
-            p.row_mass[ti] = VARIANT == kYat ? total : (m_used + log2f(total)) * LN2;
-          if (p.row_max) p.row_max[ti] = VARIANT == kYat ? all_top : all_top * p.scale;
-        }
+        // O_x holds every tile before j (S_x(j) landed after PV_x(j-1)): bring
+        // this warp's dv/2 columns onto the new max
+        if (rescale) scale_o_half<DV>(t_o, corr);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full(x));
       }
+
+      // ---- finalise: combine the two halves of the row, then normalise and
+      // store (or, with key splits, store the unnormalised partial)
+      if (ok && nk_tiles > 0) {
+        const float part = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+        const float ptop = fmaxf(top[0], top[1]);
+        float *fb = xchg + (8 + (uint32_t)x * 4) * BM;  // [2 values][2 halves][BM]
+        fb[(0 * 2 + half) * BM + r] = part;
+        fb[(1 * 2 + half) * BM + r] = ptop;
+        named_barrier_sync(named_bar, 64);
+        const float total = part + fb[(0 * 2 + (half ^ 1)) * BM + r];
+        const float all_top = fmaxf(ptop, fb[(1 * 2 + (half ^ 1)) * BM + r]);
+        // the partner reads fb before either warp writes it for the next unit
+        named_barrier_sync(named_bar, 64);
+        if (!(ok = warp_wait(o_full(x), ou & 1u, abort, SITE_EPI | 0x30))) break;
+        tc_fence_after();
+        const Unit t = decode_unit(p, unit_ring[uc & 1u]);
+        const int row = t.q0 + x * BM + r;
+        const bool row_ok = row < p.Tq;
+        if (p.n_splits == 1) {
+          const float inv = VARIANT == kYat ? 1.f / (total + 1e-9f) : 1.f / total;
+          __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
+                                ((size_t)t.bh * p.Tq + row) * DV + half * (DV / 2);
+#pragma unroll
+          for (int c = 0; c < DV / 64; ++c) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c * 32, o);
+            tmem_wait_ld();
+            tmem_ld_fence(o);
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              packed[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv,
+                                      __uint_as_float(o[2 * i + 1]) * inv);
+            if (row_ok) {
+              uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                    packed[4 * i + 3]);
+            }
+          }
+          if (row_ok && half == 0) {
+            const size_t ti = (size_t)t.bh * p.Tq + row;
+            if (p.row_mass)
+              p.row_mass[ti] = VARIANT == kYat ? total : (m_used + log2f(total)) * LN2;
+            if (p.row_max) p.row_max[ti] = VARIANT == kYat ? all_top : all_top * p.scale;
+          }
+        } else {
+          const size_t ti = ((size_t)t.split * p.B * p.h + t.bh) * p.Tq + row;
+          float *prow = p.part_o + ti * DV + half * (DV / 2);
+#pragma unroll
+          for (int c = 0; c < DV / 64; ++c) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c * 32, o);
+            tmem_wait_ld();
+            tmem_ld_fence(o);
+            if (row_ok) {
+              uint4 *dst = reinterpret_cast<uint4 *>(prow + c * 32);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            }
+          }
+          if (row_ok && half == 0)
+            reinterpret_cast<float4 *>(p.part_stat)[ti] = make_float4(total, m_used, all_top, 0.f);
+        }
+        // O_x has been read: the next unit's first PV_x may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_empty(x));
+        ++ou;
+      }
+      nk_pos += nkv;
+      release_unit(uc);
     }
   }
 
@@ -558,9 +662,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-#ifdef CATTN_TRACE
-  if (threadIdx.x == 0 && blockIdx.x < 16384) g_cta_trace[blockIdx.x][1] = globaltimer_ns();
-#endif
+}
+
+// Key-split combine: one warp per query row merges the n_splits partials.
+// Yat adds masses and outputs (the mass is a plain sum); softmax and s^tau
+// bring each partial onto the largest running max first.
+template <int VARIANT, int DV>
+__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ FwdParams p) {
+  const long long rows = (long long)p.B * p.h * p.Tq;
+  const long long rrow = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (rrow >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const float4 *stat = reinterpret_cast<const float4 *>(p.part_stat);
+  float m_all = -INFINITY, top = -INFINITY;
+  for (int s = 0; s < p.n_splits; ++s) {
+    const float4 st = stat[(long long)s * rows + rrow];
+    m_all = fmaxf(m_all, st.y);
+    top = fmaxf(top, st.z);
+  }
+  float total = 0.f;
+  constexpr int PER_LANE = DV / 32;  // 2 or 4 columns per lane
+  float o[PER_LANE];
+#pragma unroll
+  for (int i = 0; i < PER_LANE; ++i) o[i] = 0.f;
+  for (int s = 0; s < p.n_splits; ++s) {
+    const float4 st = stat[(long long)s * rows + rrow];
+    const float w = VARIANT == kYat ? 1.f : (st.y == -INFINITY ? 0.f : exp2f(st.y - m_all));
+    total += w * st.x;
+    const float *src = p.part_o + ((long long)s * rows + rrow) * DV + lane * PER_LANE;
+#pragma unroll
+    for (int i = 0; i < PER_LANE; ++i) o[i] += w * src[i];
+  }
+  const float inv = VARIANT == kYat ? 1.f / (total + 1e-9f) : 1.f / total;
+  __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + rrow * DV + lane * PER_LANE;
+#pragma unroll
+  for (int i = 0; i < PER_LANE; i += 2) {
+    const uint32_t v = pack_bf16x2(o[i] * inv, o[i + 1] * inv);
+    *reinterpret_cast<uint32_t *>(dst + i) = v;
+  }
+  if (lane == 0) {
+    if (p.row_mass) p.row_mass[rrow] = VARIANT == kYat ? total : (m_all + log2f(total)) * LN2;
+    if (p.row_max) p.row_max[rrow] = VARIANT == kYat ? top : top * p.scale;
+  }
 }
 
 template <int VARIANT, int DK, int DV>
@@ -569,21 +712,47 @@ cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap 
   using L = Layout<DK, DV>;
   auto kern = fwd_kernel<VARIANT, DK, DV>;
   static int configured_for = -1;
+  static int sm_count = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_for != dev) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
     if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
     configured_for = dev;
   }
-  const long long units = (long long)p.B * p.h * p.n_pairs;
-  if (units <= 0) return cudaSuccess;
-  kern<<<(unsigned)units, NUM_THREADS, L::ALLOC, s>>>(p, tq, tk, tv);
+  if (p.n_units <= 0) return cudaSuccess;
+  const int grid = p.n_units < sm_count ? p.n_units : sm_count;  // one CTA per SM
+  kern<<<grid, NUM_THREADS, L::ALLOC, s>>>(p, tq, tk, tv);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.n_splits == 1) return e;
+  const long long rows = (long long)p.B * p.h * p.Tq;
+  combine_kernel<VARIANT, DV><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace tc
+
+TcSchedule tc_schedule(int B, int h, int Tq, int Tk, int causal) {
+  TcSchedule s;
+  const int n_qtiles = (Tq + kTcQueryTile - 1) / kTcQueryTile;
+  s.n_pairs = (n_qtiles + 1) / 2;
+  s.n_kv_tiles = (Tk + kTcKeyTile - 1) / kTcKeyTile;
+  s.head_group = 16;
+  const long long pairs = (long long)B * h * s.n_pairs;
+  // Without a causal mask every unit costs the same, so a problem with few
+  // units would leave SMs idle in its last wave: split the keys until there
+  // are about seven units per SM (at most 64 splits, at least 8 key tiles each).
+  int splits = 1;
+  if (!causal)
+    while (pairs * splits < 1024 && splits < 64 && s.n_kv_tiles >= 16 * splits) splits *= 2;
+  s.kv_per_split = (s.n_kv_tiles + splits - 1) / splits;
+  s.n_splits = s.n_kv_tiles > 0 ? (s.n_kv_tiles + s.kv_per_split - 1) / s.kv_per_split : 1;
+  s.n_units = pairs * s.n_splits;
+  return s;
+}
 
 bool fwd_tc_supported(int dk, int dv) {
   return (dk == 64 && dv == 64) || (dk == 128 && dv == 128) || (dk == 128 && dv == 64);

@@ -26,11 +26,30 @@ struct FwdParams {
   int causal;
   float scale;
   int n_qtiles;    // query tiles per head: ceil(Tq / kTcQueryTile)
-  int n_pairs;     // CTAs per head: ceil(n_qtiles / 2)
+  int n_pairs;     // query-tile pairs per head: ceil(n_qtiles / 2)
   int n_kv_tiles;  // ceil(Tk / kTcKeyTile)
+  // persistent schedule of the tensor-core forward: one work unit is
+  // (batch*head, query-tile pair, key split)
+  int n_splits;      // key splits per pair (non-causal only; 1 = no split)
+  int kv_per_split;  // key tiles per split
+  int head_group;    // (batch, head) pairs whose units are scheduled together
+  int n_units;       // B * h * n_pairs * n_splits
+  unsigned int *tile_counter;  // next unit to hand out (zeroed before launch)
+  float *part_o;     // [n_splits, B*h, Tq, dv] unnormalised partial outputs (n_splits > 1)
+  float *part_stat;  // [n_splits, B*h, Tq, 4]: mass or l, running max (log2), top score
 };
 
+// Split count and grouping of the persistent tensor-core schedule; a pure
+// function of the problem so that the workspace size is known on the host.
+struct TcSchedule {
+  int n_pairs, n_kv_tiles, n_splits, kv_per_split, head_group;
+  long long n_units;
+};
+TcSchedule tc_schedule(int B, int h, int Tq, int Tk, int causal);
+
 // Tensor-core (tcgen05) forward for bf16 inputs.  Returns a cudaError_t.
+// Launches the persistent kernel (and, with key splits, the combine kernel);
+// p.tile_counter must already be zero on stream s.
 cudaError_t launch_fwd_tc(int variant, int dk, int dv, const FwdParams &p, const CUtensorMap &tq,
                           const CUtensorMap &tk, const CUtensorMap &tv, cudaStream_t s);
 bool fwd_tc_supported(int dk, int dv);

@@ -5,8 +5,9 @@
 // inside a host engine that plans all device memory up front and forbids
 // allocations after start-up, or a latency-critical loop where the implicit
 // synchronisation of cudaMalloc is unacceptable.  cattn_forward asks them for
-// a workspace (the fp32 squared row norms of the bf16 Yat map); this entry
-// point supplies it from a fixed array in device memory instead.
+// a workspace (the work-unit ticket, the fp32 squared row norms of the bf16
+// Yat map, the partials of a key split); this entry point supplies it from a
+// fixed array in device memory instead.
 //
 // The array is a file-scope __device__ variable, so every GPU on which the
 // library's module is loaded holds its kScratchBytes until the process exits.
@@ -65,8 +66,9 @@ int cattn_forward_noalloc(int variant, const cattn_problem_t *p, const void *q, 
   void *scratch = nullptr;
   const int rc = scratch_address(&scratch);
   if (rc != CATTN_OK) return rc;
-  // cattn_forward rewrites every norm it reads (padding included), so stale
-  // contents from an earlier call never leak into this one
+  // cattn_forward zeroes the ticket and rewrites every norm and partial it
+  // reads (padding included), so stale contents from an earlier call never
+  // leak into this one
   return cattn_forward(variant, p, q, k, v, b, eps, tau, out, row_mass, row_max_score, scratch,
                        kScratchBytes, stream);
 }

@@ -76,6 +76,12 @@ SHAPES = [
     (2, 2, 2, 640, 640, 64, 64, True),
     (1, 1, 1, 1, 129, 64, 64, False),
     (1, 2, 1, 384, 384, 128, 128, True),
+    # more units than SMs: later units come from the work ticket; odd tile count
+    (8, 8, 4, 1100, 1100, 64, 64, True),
+    # non-causal with few units: the keys are split and the partials combined
+    (1, 2, 2, 200, 2100, 128, 128, False),   # 2 splits of 9 and 8 key tiles
+    (1, 1, 1, 130, 4100, 128, 64, False),    # 4 splits, the last one ragged
+    (2, 2, 1, 64, 2048, 64, 64, False),      # 2 splits, GQA
 ]
 
 

@@ -94,7 +94,10 @@ def test_pointer_rejections(lib):
     assert validate(lib, native.YAT, p, ws=ctypes.c_void_p((1 << 20) + 16),
                     ws_bytes=need) == native.ERR_UNSUPPORTED
     assert validate(lib, native.YAT, p, ws=FAKE, ws_bytes=need) == native.OK
-    assert validate(lib, native.SOFTMAX, p) == native.OK
+    # every bf16 map needs at least the 256-byte work-unit ticket
+    assert validate(lib, native.SOFTMAX, p) == native.ERR_INVALID_ARG
+    assert validate(lib, native.SOFTMAX, p, ws=FAKE, ws_bytes=255) == native.ERR_SHAPE
+    assert validate(lib, native.SOFTMAX, p, ws=FAKE, ws_bytes=256) == native.OK
     # the forward itself returns the same codes without touching the GPU
     assert lib.cattn_forward(native.SOFTMAX, ctypes.byref(prob(h=3, hkv=2)), FAKE, FAKE, FAKE,
                              None, None, None, FAKE, None, None, None, 0, None) == native.ERR_SHAPE
@@ -103,15 +106,24 @@ def test_pointer_rejections(lib):
 
 
 def test_workspace_layout(lib):
-    # nq [B*h, Tq] then nk [B*hkv, ceil(Tk/128)*128], fp32, each rounded to 256 B
+    # 256-byte ticket, then (Yat) nq [B*h, Tq] and nk [B*hkv, ceil(Tk/128)*128],
+    # fp32, each rounded to 256 B
     p = prob(B=2, h=4, hkv=2, Tq=300, Tk=300, dk=64, dv=64)
     nq = (2 * 4 * 300 * 4 + 255) // 256 * 256
     nk = (2 * 2 * 384 * 4 + 255) // 256 * 256
-    assert lib.cattn_workspace_bytes(native.YAT, ctypes.byref(p)) == nq + nk
-    assert lib.cattn_workspace_bytes(native.SOFTMAX, ctypes.byref(p)) == 0
-    assert lib.cattn_workspace_bytes(native.STAU, ctypes.byref(p)) == 0
+    assert lib.cattn_workspace_bytes(native.YAT, ctypes.byref(p)) == 256 + nq + nk
+    assert lib.cattn_workspace_bytes(native.SOFTMAX, ctypes.byref(p)) == 256
+    assert lib.cattn_workspace_bytes(native.STAU, ctypes.byref(p)) == 256
     p32 = prob(dtype=native.F32, dk=32, dv=32)
     assert lib.cattn_workspace_bytes(native.YAT, ctypes.byref(p32)) == 0
+    # non-causal with two 256-row units and 17 key tiles: two key splits of 9
+    # and 8 tiles, each leaving fp32 partials [2, B*h, Tq, dv] and [2, B*h, Tq, 4]
+    ps = prob(B=1, h=2, hkv=2, Tq=200, Tk=2100, causal=0)
+    part = 2 * 2 * 200 * 128 * 4 + 2 * 2 * 200 * 16
+    assert lib.cattn_workspace_bytes(native.SOFTMAX, ctypes.byref(ps)) == 256 + part
+    # causal problems are never split
+    pc = prob(B=1, h=2, hkv=2, Tq=2100, Tk=2100)
+    assert lib.cattn_workspace_bytes(native.SOFTMAX, ctypes.byref(pc)) == 256
 
 
 def test_empty_problem_is_a_noop_on_the_host(lib):
