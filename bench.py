@@ -3,7 +3,7 @@ peak, per score-to-weight map, on one GPU (or N independent replicas).
 
 Workload: B=16, h=16, T=4096, dk=dv=128, bf16, causal (the mid-size causal
 layer on which the Yat target is set), seeded synthetic inputs.  One step is
-one Yat forward through the C ABI: the norm prologue (cattn_row_norms) and
+one Yat forward through the C ABI: the norm prologue (cattn_key_norms) and
 the fused forward (cattn_forward with the norms marked ready).  softmax and
 s^tau are timed on the same inputs in the same run.  FLOPs per forward:
 2*B*h*Tq*Tk*(dk+dv), halved for causal.
@@ -277,7 +277,7 @@ def main():
     def yat_step(ev=None):
         if ev is not None:
             ev[0].record()
-        attention.row_norms(q, k, v, ws, causal=w.causal, scale=w.scale)
+        attention.key_norms(q, k, v, ws, causal=w.causal, scale=w.scale)
         if ev is not None:
             ev[1].record()
         attention.forward("yat", q, k, v, b=yb, eps=ye, causal=w.causal, scale=w.scale,

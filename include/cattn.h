@@ -67,8 +67,8 @@ enum { CATTN_F32 = 0, CATTN_BF16 = 1 };
 
 /* cattn_problem_t.flags */
 enum {
-  /* Yat only: the workspace already holds the squared row norms of these q
-   * and k, written by cattn_row_norms for the same problem; skip them. */
+  /* Yat only: the workspace already holds the squared row norms of this k,
+   * written by cattn_key_norms for the same problem; skip them. */
   CATTN_FLAG_NORMS_READY = 1
 };
 
@@ -106,11 +106,11 @@ int cattn_version(void);
 /* Static name of a status code. Never NULL. */
 const char *cattn_error_string(int status);
 
-/* Bytes of device workspace cattn_forward / cattn_row_norms need for this
+/* Bytes of device workspace cattn_forward / cattn_key_norms need for this
  * problem and variant (0 if none), 256-byte aligned.  The fp32 path needs
  * none.  The bf16 path needs 256 bytes for its work-unit ticket, plus, for
- * CATTN_YAT, the fp32 squared norms of every query row and of every key row
- * (the key part padded to a multiple of 128 rows per head), plus, for
+ * CATTN_YAT, the fp32 squared norms of every key row (padded to a multiple of
+ * 128 rows per head), plus, for
  * non-causal problems with few (batch, head, 256-row) units, the fp32 partial
  * outputs and per-row statistics of a fixed split of the keys (at most 64
  * splits, chosen from the shape alone).  The contents need not be
@@ -125,14 +125,15 @@ int cattn_validate(int variant, const cattn_problem_t *p, const void *q, const v
                    const void *v, const float *b, const float *eps, const float *tau,
                    const void *out, const void *workspace, size_t workspace_bytes);
 
-/* Squared L2 norms of the q rows and the k rows, fp32, computed from the
- * stored bf16 values, written into the workspace (the norm prologue of the
- * Yat map: |q - k|^2 = |q|^2 + |k|^2 - 2 q.k is assembled from the same dot
- * products the scores need, "Softmax-Free Attention in JAX/Flax NNX", section
- * "One module, two compatibility functions").  bf16 problems only.
- * cattn_forward(CATTN_YAT, ...) runs this itself unless
- * CATTN_FLAG_NORMS_READY is set. */
-int cattn_row_norms(const cattn_problem_t *p, const void *q, const void *k, void *workspace,
+/* Squared L2 norms of the k rows, fp32, computed from the stored bf16 values
+ * and written into the workspace: the key half of the Yat map's norm
+ * prologue.  |q - k|^2 = |q|^2 + |k|^2 - 2 q.k is assembled from the same dot
+ * products the scores need ("Softmax-Free Attention in JAX/Flax NNX", section
+ * "One module, two compatibility functions"); the forward kernel takes |q|^2
+ * itself from the query tiles it holds, |k|^2 from here because every key
+ * tile serves many query tiles.  bf16 problems only.  cattn_forward(CATTN_YAT,
+ * ...) runs this itself unless CATTN_FLAG_NORMS_READY is set. */
+int cattn_key_norms(const cattn_problem_t *p, const void *k, void *workspace,
                     size_t workspace_bytes, cattn_stream_t stream);
 
 /* The attention forward.  b and eps are required for CATTN_YAT (b >= 0,
@@ -154,9 +155,9 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
  * Arguments as cattn_forward, minus the workspace: the scratch comes from a
  * fixed 16 MiB array of device memory inside the library, which every GPU that
  * loads the library holds until the process exits.  Problems whose
- * cattn_workspace_bytes() exceeds 16 MiB (for causal bf16 Yat: B*h*Tq +
- * B*hkv*Tk_pad above about 4.19 million rows; non-causal problems whose keys
- * are split need room for the partial outputs as well) are rejected with
+ * cattn_workspace_bytes() exceeds 16 MiB (for causal bf16 Yat: B*hkv*Tk_pad
+ * above about 4.19 million key rows; non-causal problems whose keys are split
+ * need room for the partial outputs as well) are rejected with
  * CATTN_ERR_SCRATCH_LIMIT before anything is enqueued;
  * CATTN_FLAG_NORMS_READY is rejected with CATTN_ERR_INVALID_ARG.  Nothing is
  * allocated or freed.

@@ -66,17 +66,17 @@ def _stream_handle(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
 
-def row_norms(q, k, v, workspace, *, causal=False, scale=None):
-    """Fill a Yat workspace with the squared q/k row norms (bf16 inputs).
+def key_norms(q, k, v, workspace, *, causal=False, scale=None):
+    """Fill a Yat workspace with the squared k row norms (bf16 inputs).
 
     A later ``forward('yat', ..., workspace=workspace, norms_ready=True)`` on the
-    same q, k, v skips the norm prologue.
+    same q, k, v skips this prologue.
     """
     prob = make_problem(q, k, v, causal=causal, scale=scale)
     lib = native.load()
-    native.check(lib.cattn_row_norms(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(workspace),
+    native.check(lib.cattn_key_norms(ctypes.byref(prob), _ptr(k), _ptr(workspace),
                                      workspace.numel() * workspace.element_size(),
-                                     _stream_handle(q.device)), "cattn_row_norms")
+                                     _stream_handle(q.device)), "cattn_key_norms")
 
 
 def forward(variant, q, k, v, *, b=None, eps=None, tau=None, causal=False, scale=None,

@@ -26,21 +26,18 @@ bool is_empty(const cattn_problem_t *p) { return p->B == 0 || p->h == 0 || p->Tq
 
 // Workspace layout of the bf16 (tensor-core) path, each part 256-byte aligned:
 //   ctrl       256 B: the persistent schedule's unit ticket (zeroed per call)
-//   nq, nk     Yat only: squared q row norms [B*h, Tq], squared k row norms
-//              [B*hkv, Tk_pad], fp32
+//   nk         Yat only: squared k row norms [B*hkv, Tk_pad], fp32 (the
+//              query norms are taken in-kernel from the Q tiles)
 //   part_o     key splits only: unnormalised partial outputs
 //              [n_splits, B*h, Tq, dv] fp32
 //   part_stat  key splits only: per-row [n_splits, B*h, Tq, 4] fp32
 // The fp32 (CUDA-core) path needs none.
-size_t ws_nq_bytes(const cattn_problem_t *p) {
-  return align256((size_t)p->B * p->h * p->Tq * sizeof(float));
-}
 size_t ws_nk_bytes(const cattn_problem_t *p) {
   return align256((size_t)p->B * p->hkv * tk_pad(p) * sizeof(float));
 }
 
 struct WsLayout {
-  size_t ctrl, nq, nk, part_o, part_stat, total;
+  size_t ctrl, nk, part_o, part_stat, total;
   TcSchedule sched;
 };
 
@@ -53,8 +50,6 @@ WsLayout ws_layout(int variant, const cattn_problem_t *p) {
   w.ctrl = off;
   off += 256;
   if (variant == CATTN_YAT) {
-    w.nq = off;
-    off += ws_nq_bytes(p);
     w.nk = off;
     off += ws_nk_bytes(p);
   }
@@ -183,24 +178,21 @@ int cattn_validate(int variant, const cattn_problem_t *p, const void *q, const v
   return CATTN_OK;
 }
 
-int cattn_row_norms(const cattn_problem_t *p, const void *q, const void *k, void *workspace,
+int cattn_key_norms(const cattn_problem_t *p, const void *k, void *workspace,
                     size_t workspace_bytes, cattn_stream_t stream) {
   int rc = check_problem(CATTN_YAT, p);
   if (rc != CATTN_OK) return rc;
   if (p->dtype != CATTN_BF16) return CATTN_ERR_UNSUPPORTED;
   if (is_empty(p)) return CATTN_OK;
-  if (!q || !k || !workspace) return CATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+  if (!k || !workspace) return CATTN_ERR_INVALID_ARG;
+  if (!aligned16(k) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return CATTN_ERR_UNSUPPORTED;
   const WsLayout w = ws_layout(CATTN_YAT, p);
   if (workspace_bytes < w.total) return CATTN_ERR_SHAPE;
   rc = check_device();
   if (rc != CATTN_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  float *nq = reinterpret_cast<float *>(static_cast<char *>(workspace) + w.nq);
   float *nk = reinterpret_cast<float *>(static_cast<char *>(workspace) + w.nk);
-  rc = map_cuda(launch_row_sqnorm_bf16(q, nq, p->B * p->h, p->Tq, p->Tq, p->dk, s));
-  if (rc != CATTN_OK) return rc;
   return map_cuda(launch_row_sqnorm_bf16(k, nk, p->B * p->hkv, p->Tk, tk_pad(p), p->dk, s));
 }
 
@@ -252,10 +244,9 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
     fp.part_stat = reinterpret_cast<float *>(ws + w.part_stat);
   }
   if (variant == CATTN_YAT) {
-    fp.nq = reinterpret_cast<const float *>(ws + w.nq);
     fp.nk = reinterpret_cast<const float *>(ws + w.nk);
     if (!(p->flags & CATTN_FLAG_NORMS_READY)) {
-      rc = cattn_row_norms(p, q, k, workspace, workspace_bytes, stream);
+      rc = cattn_key_norms(p, k, workspace, workspace_bytes, stream);
       if (rc != CATTN_OK) return rc;
     }
   }

@@ -260,7 +260,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q_full, 1);
-    mbar_init(bar_q_empty, 1);
+    // the last S MMAs of a unit, plus (Yat) every map warp once it has read
+    // its row's |q|^2 out of the Q tile
+    mbar_init(bar_q_empty, VARIANT == kYat ? 1 + MAP_WARPS : 1);
     for (int s = 0; s < L::NS; ++s) {
       mbar_init(kv_full(s), 1);
       mbar_init(kv_empty(s), 1);
@@ -460,7 +462,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t named_bar = 1u + (uint32_t)(x * 4 + quarter);  // warps w and w^4
     float *xchg = reinterpret_cast<float *>(smem + L::OFF_XCHG);
     const float c2 = p.scale * LOG2E;  // scaled score in log2 units per raw dot
-    uint32_t xpar = 0, cs = 0, ou = 0, nk_pos = 0;
+    // phase bits: 1 = s_full parity, 2 = o_full parity, 4 = row-max exchange buffer
+    uint32_t ph = 0, nk_pos = 0;
     bool ok = true;
 
     for (uint32_t uc = 0; ok; ++uc) {
@@ -482,15 +485,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (VARIANT == kYat) {
           yb = p.b[t.head];
           yeps = p.eps[t.head];
-          qe = (row < p.Tq ? p.nq[(size_t)t.bh * p.Tq + row] : 0.f) + yeps;
         } else if (VARIANT == kStau) {
           tau = p.tau[t.head];
           seps = p.eps[t.head];
         }
       }
+      if (VARIANT == kYat) {
+        // |q|^2 of this thread's row, in fp32 from the bf16 Q tile in shared
+        // memory (rows past Tq were loaded as zeros).  The order of a row's
+        // 16-byte units is rotated by lane so that a warp's loads fall in
+        // distinct banks; the sum does not depend on where a unit sits in the
+        // swizzled row.  The Q tiles are released once every map warp has
+        // read them.
+        if (!(ok = warp_wait(bar_q_full, uc & 1u, abort, SITE_EPI | 0x40))) break;
+        if (nk_tiles > 0) {
+          const uint32_t qrow = q_smem(x) + (uint32_t)r * 128u;
+          float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < DK / 64; ++c) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint4 v = lds128(qrow + (uint32_t)c * (BM * 128) + ((uint32_t)((k + lane) & 7) << 4));
+              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 f = make_float2(__uint_as_float(w[i] << 16),
+                                             __uint_as_float(w[i] & 0xffff0000u));
+                s2 = __ffma2_rn(f, f, s2);
+              }
+            }
+          }
+          qe = (s2.x + s2.y) + yeps;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_q_empty);
+      }
 
-      for (int j = 0; j < nk_tiles; ++j, ++cs) {
-        if (!(ok = warp_wait(s_full(x), cs & 1u, abort, SITE_EPI | 0x10))) break;
+      for (int j = 0; j < nk_tiles; ++j, ph ^= 1u) {
+        if (!(ok = warp_wait(s_full(x), ph & 1u, abort, SITE_EPI | 0x10))) break;
         tc_fence_after();
 
         // keys of tile j allowed for col < limit (col counts the whole tile)
@@ -529,11 +561,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                              : fmaxf(chunk_max<false>(sr[0], half * 2, limit),
                                      chunk_max<false>(sr[1], half * 2 + 1, limit));
           // the row max over the whole tile: swap halves with the partner warp
-          float *xb = xchg + ((xpar * 2 + (uint32_t)x) * 2) * BM;
+          float *xb = xchg + ((((ph >> 2) & 1u) * 2 + (uint32_t)x) * 2) * BM;
           xb[half * BM + r] = mt;
           named_barrier_sync(named_bar, 64);
           mt = fmaxf(mt, xb[(half ^ 1) * BM + r]);
-          xpar ^= 1u;
+          ph ^= 4u;
           top[0] = fmaxf(top[0], mt);
           float m_new = -INFINITY;
           if (mt > -INFINITY) {
@@ -554,6 +586,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
+            if (VARIANT == kStau && c == 1) {
+              // s^tau holds more temporaries: read the second chunk again
+              // rather than keep it live through the first one's map
+              tmem_ld32(t_s + 32, sr[1]);
+              tmem_wait_ld();
+              tmem_ld_fence(sr[1]);
+            }
             uint32_t hk[16];
             if (VARIANT == kSoftmax) {
               if (partial)
@@ -592,7 +631,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float all_top = fmaxf(ptop, fb[(1 * 2 + (half ^ 1)) * BM + r]);
         // the partner reads fb before either warp writes it for the next unit
         named_barrier_sync(named_bar, 64);
-        if (!(ok = warp_wait(o_full(x), ou & 1u, abort, SITE_EPI | 0x30))) break;
+        if (!(ok = warp_wait(o_full(x), (ph >> 1) & 1u, abort, SITE_EPI | 0x30))) break;
         tc_fence_after();
         const Unit t = decode_unit(p, unit_ring[uc & 1u]);
         const int row = t.q0 + x * BM + r;
@@ -649,7 +688,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(o_empty(x));
-        ++ou;
+        ph ^= 2u;
       }
       nk_pos += nkv;
       release_unit(uc);

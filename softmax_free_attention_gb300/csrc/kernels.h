@@ -20,8 +20,7 @@ struct FwdParams {
   void *out;                    // [B, h, Tq, dv]
   float *row_mass, *row_max;    // [B, h, Tq] or NULL
   const float *b, *eps, *tau;   // [h]
-  const float *nq;              // [B*h, Tq]        squared q row norms (Yat, bf16)
-  const float *nk;              // [B*hkv, Tk_pad]  squared k row norms, zero padded
+  const float *nk;              // [B*hkv, Tk_pad]  squared k row norms (Yat, bf16), zero padded
   int B, h, hkv, Tq, Tk, Tk_pad;
   int causal;
   float scale;

@@ -3,9 +3,11 @@
 // The Yat map needs |q - k|^2 for every score; it is assembled as
 // |q|^2 + |k|^2 - 2 q.k from the dot products the scores already need
 // ("Softmax-Free Attention in JAX/Flax NNX", section "One module, two
-// compatibility functions").  This kernel supplies the two norm vectors, in
-// fp32 from the stored bf16 values.  It is bandwidth bound: d/8 threads share
-// a row, each reading one 16-byte vector, then a shuffle reduction.
+// compatibility functions").  This kernel supplies the key norms, in fp32
+// from the stored bf16 values.  It is bandwidth bound: d/8 threads share a
+// row, each reading one 16-byte vector of it; every thread keeps ROWS such
+// loads in flight before the shuffle reductions, and the grid strides over
+// the rows with a few CTAs per SM.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -13,31 +15,46 @@
 namespace cattn {
 namespace {
 
+constexpr int kThreads = 256;
+constexpr int kRows = 4;  // row groups per thread per pass
+
 template <int G>  // threads per row = d / 8
-__global__ void __launch_bounds__(256) row_sqnorm_kernel(const uint4 *__restrict__ x,
-                                                         float *__restrict__ out, int T, int T_pad,
-                                                         long long n_out) {
-  const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const long long slot = gtid / G;
-  const int part = (int)(gtid % G);
-  float acc = 0.f;
-  if (slot < n_out) {
-    const long long bh = slot / T_pad;
-    const int t = (int)(slot - bh * T_pad);
-    if (t < T) {
-      const uint4 raw = __ldg(x + (bh * T + t) * G + part);
-      const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+__global__ void __launch_bounds__(kThreads) row_sqnorm_kernel(const uint4 *__restrict__ x,
+                                                              float *__restrict__ out, int T,
+                                                              int T_pad, long long n_out) {
+  // One pass of a block covers SPAN consecutive output slots; T_pad is a
+  // multiple of 128 >= SPAN, so a span never crosses from one head to the next.
+  constexpr int RPB = kThreads / G;
+  constexpr int SPAN = RPB * kRows;
+  static_assert(128 % SPAN == 0, "a span stays inside one head");
+  const int part = threadIdx.x % G;
+  const int sub = threadIdx.x / G;
+  for (long long base = (long long)blockIdx.x * SPAN; base < n_out;
+       base += (long long)gridDim.x * SPAN) {
+    const long long bh = base / T_pad;
+    const int t0 = (int)(base - bh * T_pad);
+    const uint4 *xh = x + bh * T * G;
+    uint4 raw[kRows];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h2[i]);
+    for (int i = 0; i < kRows; ++i) {
+      const int t = t0 + i * RPB + sub;
+      raw[i] = t < T ? __ldg(xh + (long long)t * G + part) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) {
+      const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&raw[i]);
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h2[e]);
         acc = fmaf(f.x, f.x, acc);
         acc = fmaf(f.y, f.y, acc);
       }
+#pragma unroll
+      for (int o = G / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (part == 0) out[base + i * RPB + sub] = acc;  // padded rows get zero
     }
   }
-#pragma unroll
-  for (int o = G / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (part == 0 && slot < n_out) out[slot] = acc;
 }
 
 }  // namespace
@@ -47,15 +64,20 @@ cudaError_t launch_row_sqnorm_bf16(const void *x, float *out, int BH, int T, int
   const long long n_out = (long long)BH * T_pad;
   if (n_out == 0) return cudaSuccess;
   const int G = d / 8;
-  const long long threads = n_out * G;
-  const unsigned blocks = (unsigned)((threads + 255) / 256);
+  if (G != 16 && G != 8) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long per_block = (long long)(kThreads / G) * kRows;
+  long long blocks = (n_out + per_block - 1) / per_block;
+  if (blocks > 8LL * sms) blocks = 8LL * sms;
   const uint4 *xv = reinterpret_cast<const uint4 *>(x);
   if (G == 16)
-    row_sqnorm_kernel<16><<<blocks, 256, 0, s>>>(xv, out, T, T_pad, n_out);
-  else if (G == 8)
-    row_sqnorm_kernel<8><<<blocks, 256, 0, s>>>(xv, out, T, T_pad, n_out);
+    row_sqnorm_kernel<16><<<(unsigned)blocks, kThreads, 0, s>>>(xv, out, T, T_pad, n_out);
   else
-    return cudaErrorInvalidValue;
+    row_sqnorm_kernel<8><<<(unsigned)blocks, kThreads, 0, s>>>(xv, out, T, T_pad, n_out);
   return cudaGetLastError();
 }
 

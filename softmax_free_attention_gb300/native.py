@@ -26,7 +26,7 @@ ERR_SCRATCH_LIMIT = 6
 
 # every symbol include/cattn.h declares
 EXPORTS = ("cattn_version", "cattn_error_string", "cattn_workspace_bytes", "cattn_validate",
-           "cattn_row_norms", "cattn_forward", "cattn_forward_noalloc", "cattn_check_status")
+           "cattn_key_norms", "cattn_forward", "cattn_forward_noalloc", "cattn_check_status")
 
 
 class Problem(ctypes.Structure):
@@ -68,8 +68,8 @@ def load():
     lib.cattn_workspace_bytes.restype = sz
     lib.cattn_validate.argtypes = [i, pp, vp, vp, vp, vp, vp, vp, vp, vp, sz]
     lib.cattn_validate.restype = i
-    lib.cattn_row_norms.argtypes = [pp, vp, vp, vp, sz, vp]
-    lib.cattn_row_norms.restype = i
+    lib.cattn_key_norms.argtypes = [pp, vp, vp, sz, vp]
+    lib.cattn_key_norms.restype = i
     lib.cattn_forward.argtypes = [i, pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.cattn_forward.restype = i
     lib.cattn_forward_noalloc.argtypes = [i, pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]

@@ -34,7 +34,7 @@ def run_gpu(variant, inputs, *, causal, scale, two_step=False):
         # forward told that the norms are ready
         prob = attention.make_problem(q, k, v, causal=causal, scale=scale)
         ws = torch.empty(attention.workspace_bytes("yat", prob), dtype=torch.uint8, device="cuda")
-        attention.row_norms(q, k, v, ws, causal=causal, scale=scale)
+        attention.key_norms(q, k, v, ws, causal=causal, scale=scale)
         res = attention.forward(variant, q, k, v, causal=causal, scale=scale, workspace=ws,
                                 norms_ready=True, **kw)
     else:

@@ -106,12 +106,11 @@ def test_pointer_rejections(lib):
 
 
 def test_workspace_layout(lib):
-    # 256-byte ticket, then (Yat) nq [B*h, Tq] and nk [B*hkv, ceil(Tk/128)*128],
-    # fp32, each rounded to 256 B
+    # 256-byte ticket, then (Yat) nk [B*hkv, ceil(Tk/128)*128] fp32, rounded
+    # to 256 B
     p = prob(B=2, h=4, hkv=2, Tq=300, Tk=300, dk=64, dv=64)
-    nq = (2 * 4 * 300 * 4 + 255) // 256 * 256
     nk = (2 * 2 * 384 * 4 + 255) // 256 * 256
-    assert lib.cattn_workspace_bytes(native.YAT, ctypes.byref(p)) == 256 + nq + nk
+    assert lib.cattn_workspace_bytes(native.YAT, ctypes.byref(p)) == 256 + nk
     assert lib.cattn_workspace_bytes(native.SOFTMAX, ctypes.byref(p)) == 256
     assert lib.cattn_workspace_bytes(native.STAU, ctypes.byref(p)) == 256
     p32 = prob(dtype=native.F32, dk=32, dv=32)
