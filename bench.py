@@ -20,6 +20,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -77,27 +78,34 @@ def measured_peaks():
         return FALLBACK_TFLOPS, 1700.0, "fallback"
 
 
+KERNEL_SOURCES = ("fwd_tc.cu", "maps.cuh", "ptx.cuh", "kernels.h")
+TRAFFIC_SUMMARY = os.path.join(ROOT, "profiles", "fwd_kernel_yat_b4_full.md")
+
+
 def kernel_source_hash():
+    """Hash of the sources the fused kernel is compiled from."""
     h = hashlib.sha256()
-    for name in ("fwd_tc.cu", "ptx.cuh", "kernels.h"):
+    for name in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "softmax_free_attention_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel_key):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source; otherwise None."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+def recorded_traffic():
+    """DRAM bytes per full-size launch of the fused Yat kernel, from the
+    committed ncu summary, if it was captured on the current kernel sources;
+    otherwise None.  The summary holds `source_hash:`, the per-launch DRAM
+    bytes of the captured (smaller) case and the factor that scales it to the
+    benchmark workload."""
     try:
-        with open(path) as f:
-            d = json.load(f)
-        rec = d.get(kernel_key)
-        if rec and rec.get("source_hash") == kernel_source_hash():
-            return float(rec["dram_bytes_per_launch"])
+        with open(TRAFFIC_SUMMARY) as f:
+            text = f.read()
+        fields = dict(re.findall(r"^- (\w+): `([^`]+)`", text, flags=re.M))
+        if fields.get("source_hash") != kernel_source_hash():
+            return None
+        return float(fields["dram_bytes_per_launch"]) * float(fields["scale_to_workload"])
     except Exception:
-        pass
-    return None
+        return None
 
 
 class ClockSampler:
@@ -375,7 +383,7 @@ def main():
 
     achieved = fwd_tflops
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
-                "frac": achieved / peak_burst, "traffic": recorded_traffic("fwd_kernel_yat_cfg3"),
+                "frac": achieved / peak_burst, "traffic": recorded_traffic(),
                 "peak_kind": f"{peak_kind} bf16 burst (cuBLAS)",
                 "kernel": "cattn::tc::fwd_kernel<Yat,128,128>"}
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,

@@ -62,6 +62,23 @@ namespace cattn {
 
 __device__ unsigned int g_status;
 
+#ifdef CATTN_TRACE
+// Optional clock64 timeline of the first CTAs' steps (compiled out by
+// default): [CTA][event][running step].
+__device__ unsigned long long g_trace[4][16][512];
+extern "C" int cattn_trace_read(void *host, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(host, g_trace, bytes);
+}
+#define CATTN_TR(ev, idx)                                                     \
+  do {                                                                        \
+    if (blockIdx.x < 4 && (idx) < 512) g_trace[blockIdx.x][ev][(idx)] = clock64(); \
+  } while (0)
+#else
+#define CATTN_TR(ev, idx) \
+  do {                    \
+  } while (0)
+#endif
+
 
 namespace tc {
 
@@ -390,6 +407,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // until the map warps have read O_x out.
     uint32_t kv_pos = 0, nk_pos = 0, pph[2] = {0u, 0u}, ou[2] = {0u, 0u};
     bool ok = true;
+#ifdef CATTN_TRACE
+    int ms = 0;  // running MMA iteration
+#endif
     for (uint32_t uc = 0; ok; ++uc) {
       const int u = peek_unit(uc, SITE_MMA | 0x70);
       if (u < 0) break;
@@ -411,6 +431,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (j == 1 && !(ok = warp_wait(o_empty(x), (ou[x] & 1u) ^ 1u, abort, SITE_MMA | 0x50)))
               break;
             tc_fence_after();
+#ifdef CATTN_TRACE
+            if (lane == 0) CATTN_TR(4 + 2 * x, ms);
+#endif
             if (lane == 0) {
               issue_pv<DV>(tmem + TM_O + 128u * x, tmem + TM_S + 128u * x, slot_smem(vs), j > 1);
               if (j == t.n[x]) mma_commit(o_full(x));
@@ -422,6 +445,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after();
           }
           if (j < t.n[x]) {  // S_x = Q_x K(j)^T
+#ifdef CATTN_TRACE
+            if (lane == 0) CATTN_TR(5 + 2 * x, ms);
+#endif
             if (lane == 0) {
               issue_qk<DK>(tmem + TM_S + 128u * x, q_smem(x), slot_smem(ks));
               mma_commit(s_full(x));
@@ -438,6 +464,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (VARIANT == kYat && j >= 1) mbar_arrive(nk_empty((nk_pos + j - 1) % NKS));
         }
         __syncwarp();
+#ifdef CATTN_TRACE
+        ++ms;
+#endif
       }
       kv_pos += 2u * t.nkv;
       nk_pos += t.nkv;
@@ -465,6 +494,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // phase bits: 1 = s_full parity, 2 = o_full parity, 4 = row-max exchange buffer
     uint32_t ph = 0, nk_pos = 0;
     bool ok = true;
+#ifdef CATTN_TRACE
+    int tr_step = 0;
+    const bool tr_warp = (warp & 7) == 0 && lane == 0;  // warps 0 and 8
+#endif
 
     for (uint32_t uc = 0; ok; ++uc) {
       const int u = peek_unit(uc, SITE_EPI | 0x70);
@@ -524,6 +557,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int j = 0; j < nk_tiles; ++j, ph ^= 1u) {
         if (!(ok = warp_wait(s_full(x), ph & 1u, abort, SITE_EPI | 0x10))) break;
         tc_fence_after();
+#ifdef CATTN_TRACE
+        if (tr_warp) CATTN_TR(2 * x, tr_step);
+#endif
 
         // keys of tile j allowed for col < limit (col counts the whole tile)
         const int limit = min(BN, lim_base - j * BN);
@@ -615,6 +651,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (rescale) scale_o_half<DV>(t_o, corr);
         tmem_wait_st();
         tc_fence_before();
+#ifdef CATTN_TRACE
+        if (tr_warp) CATTN_TR(2 * x + 1, tr_step);
+        ++tr_step;
+#endif
         mbar_arrive(p_full(x));
       }
 
