@@ -108,6 +108,22 @@ def recorded_traffic():
         return None
 
 
+def max_over_ranks(x, world, device):
+    """Max of a per-rank float over all ranks (the slowest rank's time)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step, steps, seconds, world):
+    """Whole-job throughput: every rank runs the same workload (weak scaling)."""
+    return world * flops_per_step * steps / seconds / 1e12
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
@@ -319,14 +335,11 @@ def main():
     elapsed_ms = start.elapsed_time(stop)
     norms_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     fwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
     assert attention.check_status() == 0
     ms_per_step = elapsed_ms / args.steps
     flops = w.flops()
-    value = world * flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    value = job_tflops(flops, args.steps, elapsed_ms * 1e-3, world)
 
     peak_burst, peak_sust, peak_kind = measured_peaks()
 
@@ -363,14 +376,16 @@ def main():
                                 eps=ye.cpu(), causal=w.causal, scale=w.scale)  # warm-up
         del res
         torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
         n_e2e = max(2, min(args.steps, 5))
         t0 = time.perf_counter()
         for _ in range(n_e2e):
             res = attention.forward("yat", pinned["q"], pinned["k"], pinned["v"], b=yb.cpu(),
                                     eps=ye.cpu(), causal=w.causal, scale=w.scale)
         torch.cuda.synchronize()
-        e2e_s = (time.perf_counter() - t0) / n_e2e
-        e2e = {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
+        e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, world, dev)
+        e2e = {"value": job_tflops(flops, 1, e2e_s, world), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e}
 
     # ---- CPU baseline: the oracle on the host cores, bounded sample

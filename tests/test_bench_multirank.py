@@ -1,0 +1,58 @@
+"""The benchmark's multi-rank host logic on CPU: two gloo ranks agree on the
+slowest rank's time, and the whole-job figure counts every rank's work.  The
+reference arm does its work on rank 0 only."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        mx = bench.max_over_ranks(10.0 + 5.0 * rank, world, "cpu")
+        out.put((rank, mx))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_with_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    results = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert results == {0: 15.0, 1: 15.0}
+
+
+def test_job_tflops_counts_every_rank():
+    one = bench.job_tflops(2.0 ** 40, 10, 0.012, 1)
+    assert one == pytest.approx(2.0 ** 40 * 10 / 0.012 / 1e12)
+    assert bench.job_tflops(2.0 ** 40, 10, 0.012, 4) == pytest.approx(4 * one)
+    assert bench.max_over_ranks(3.5, 1, "cpu") == 3.5
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+
+    class Args:
+        batch, steps, warmup, gpus = None, 1, 1, 2
+
+    assert bench.reference_arm(Args()) == 0
