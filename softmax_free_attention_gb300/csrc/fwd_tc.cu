@@ -152,6 +152,47 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Single-thread bounded wait (the MMA issuer runs on one lane).  Returns
+// false on timeout or abort.
+__device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                            unsigned site, bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((honor_abort && *abort != 0) || (globaltimer_ns() - t0 > WAIT_LIMIT_NS)) {
+      atomicCAS(&g_status, 0u, site | 1u);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+// S = Q K^T for one 128 x 128 tile from prebuilt descriptors of the Q tile
+// and the K slot: 16-element k steps, 64-column boxes.
+template <int DK>
+__device__ __forceinline__ void issue_qk_d(uint32_t d_tmem, uint64_t qdesc, uint64_t kdesc) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, false);
+#pragma unroll
+  for (int kk = 0; kk < DK / 16; ++kk) {
+    const uint64_t qo = (uint64_t)(((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4);
+    const uint64_t ko = (uint64_t)(((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4);
+    mma_ss(d_tmem, qdesc + qo, kdesc + ko, IDESC, kk > 0 ? 1u : 0u);
+  }
+}
+
+// O += P V from a prebuilt descriptor of the V slot.
+template <int DV>
+__device__ __forceinline__ void issue_pv_d(uint32_t d_tmem, uint32_t p_tmem, uint64_t vdesc,
+                                           bool accumulate) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(BM, DV, true);
+#pragma unroll
+  for (int kk = 0; kk < BN / 16; ++kk) {
+    mma_ts(d_tmem, p_tmem + (uint32_t)(kk >> 2) * 64 + (uint32_t)(kk & 3) * 8,
+           vdesc + (uint64_t)((kk * 2048) >> 4), IDESC, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
 // S = Q K^T for one 128 x 128 tile: 16-element k steps, 64-column boxes.
 template <int DK>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
@@ -294,7 +335,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(o_full(x), 1);
       mbar_init(o_empty(x), 8);      // lane 0 of each of those warps
       mbar_init(unit_full(x), 1);
-      mbar_init(unit_empty(x), 1 + MAP_WARPS);  // the MMA warp and every map warp
+      mbar_init(unit_empty(x), 1 + MAP_WARPS);  // the MMA lane and every map warp
     }
     mbar_init(bar_drain, 1);
     *abort = 0;
@@ -328,24 +369,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == PRODUCER_WARP) {
     // ------------------------------------------------------------ producer
-    // Hands out units (the first one is blockIdx.x, later ones come from the
-    // global ticket) and loads each unit's Q pair, then its K/V tiles (and key
-    // norms) through the rings.  Ring positions run on across units.
-    int u = blockIdx.x;
-    uint32_t kv_pos = 0, nk_pos = 0;
-    for (uint32_t uc = 0;; ++uc) {
-      const uint32_t us = uc & 1u;
-      if (!warp_wait(unit_empty(us), ((uc >> 1) & 1u) ^ 1u, abort, SITE_PRODUCER | 0x40)) break;
-      if (lane == 0) {
+    // One lane hands out units (its CTA's first unit is blockIdx.x, later
+    // ones come from the global ticket, fetched one unit ahead so that the
+    // atomic's latency hides behind the current unit's loads) and loads each
+    // unit's Q pair, then its K/V tiles (and key norms) through the rings.
+    // Ring positions run on across units.
+    if (lane == 0) {
+      int u = blockIdx.x;
+      uint32_t kv_pos = 0, nk_pos = 0;
+      for (uint32_t uc = 0;; ++uc) {
+        const uint32_t us = uc & 1u;
+        if (!thread_wait(unit_empty(us), ((uc >> 1) & 1u) ^ 1u, abort, SITE_PRODUCER | 0x40)) break;
         unit_ring[us] = u < p.n_units ? u : -1;
         mbar_arrive(unit_full(us));
-      }
-      __syncwarp();
-      if (u >= p.n_units) break;
-      const Unit t = decode_unit(p, u);
-      // the previous unit's last S MMAs have read both Q tiles
-      if (!warp_wait(bar_q_empty, (uc & 1u) ^ 1u, abort, SITE_PRODUCER | 0x50)) break;
-      if (lane == 0) {
+        if (u >= p.n_units) break;
+        const Unit t = decode_unit(p, u);
+        // the previous unit's last S MMAs have read both Q tiles
+        if (!thread_wait(bar_q_empty, (uc & 1u) ^ 1u, abort, SITE_PRODUCER | 0x50)) break;
         mbar_arrive_expect_tx(bar_q_full, (t.n[1] > 0 ? 2u : 1u) * (uint32_t)L::Q_TILE);
 #pragma unroll
         for (int c = 0; c < DK / 64; ++c) {
@@ -353,132 +393,122 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (t.n[1] > 0)
             tma_load_3d(q_smem(1) + c * BM * 128, &tm_q, c * 64, t.q0 + BM, t.bh, bar_q_full);
         }
-      }
-      __syncwarp();
-      bool ok = true;
-      for (int j = 0; j < t.nkv; ++j) {
-        const int jt = t.kv_begin + j;  // key tile
-        {  // K
-          const uint32_t pos = kv_pos + 2u * j, s = pos % L::NS;
-          if (!(ok = warp_wait(kv_empty(s), ((pos / L::NS) & 1u) ^ 1u, abort, SITE_PRODUCER | 0x10)))
-            break;
-          if (lane == 0) {
+        bool ok = true;
+        for (int j = 0; j < t.nkv; ++j) {
+          const int jt = t.kv_begin + j;  // key tile
+          {  // K
+            const uint32_t pos = kv_pos + 2u * j, s = pos % L::NS;
+            if (!(ok = thread_wait(kv_empty(s), ((pos / L::NS) & 1u) ^ 1u, abort,
+                                   SITE_PRODUCER | 0x10)))
+              break;
             mbar_arrive_expect_tx(kv_full(s), L::K_TILE);
 #pragma unroll
             for (int c = 0; c < DK / 64; ++c)
               tma_load_3d(slot_smem(s) + c * BN * 128, &tm_k, c * 64, jt * BN, t.bh_kv, kv_full(s));
           }
-          __syncwarp();
-        }
-        if (VARIANT == kYat) {  // squared key norms of the tile
-          const uint32_t pos = nk_pos + j, s = pos % NKS;
-          if (!(ok = warp_wait(nk_empty(s), ((pos / NKS) & 1u) ^ 1u, abort, SITE_PRODUCER | 0x20)))
-            break;
-          if (lane == 0) {
+          if (VARIANT == kYat) {  // squared key norms of the tile
+            const uint32_t pos = nk_pos + j, s = pos % NKS;
+            if (!(ok = thread_wait(nk_empty(s), ((pos / NKS) & 1u) ^ 1u, abort,
+                                   SITE_PRODUCER | 0x20)))
+              break;
             mbar_arrive_expect_tx(nk_full(s), BN * 4);
             bulk_load(sb + L::OFF_NK + s * BN * 4,
                       p.nk + (size_t)t.bh_kv * p.Tk_pad + (size_t)jt * BN, BN * 4, nk_full(s));
           }
-          __syncwarp();
-        }
-        {  // V
-          const uint32_t pos = kv_pos + 2u * j + 1u, s = pos % L::NS;
-          if (!(ok = warp_wait(kv_empty(s), ((pos / L::NS) & 1u) ^ 1u, abort, SITE_PRODUCER | 0x30)))
-            break;
-          if (lane == 0) {
+          {  // V
+            const uint32_t pos = kv_pos + 2u * j + 1u, s = pos % L::NS;
+            if (!(ok = thread_wait(kv_empty(s), ((pos / L::NS) & 1u) ^ 1u, abort,
+                                   SITE_PRODUCER | 0x30)))
+              break;
             mbar_arrive_expect_tx(kv_full(s), L::V_TILE);
 #pragma unroll
             for (int c = 0; c < DV / 64; ++c)
               tma_load_3d(slot_smem(s) + c * BN * 128, &tm_v, c * 64, jt * BN, t.bh_kv, kv_full(s));
           }
-          __syncwarp();
         }
+        if (!ok) break;
+        kv_pos += 2u * t.nkv;
+        nk_pos += t.nkv;
+        u = (int)atomicAdd(p.tile_counter, 1u) + (int)gridDim.x;
       }
-      if (!ok) break;
-      kv_pos += 2u * t.nkv;
-      nk_pos += t.nkv;
-      if (lane == 0) u = (int)atomicAdd(p.tile_counter, 1u) + (int)gridDim.x;
-      u = __shfl_sync(FULL, u, 0);
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issue
-    // Per unit, iteration j: PV0(j-1) S0(j) PV1(j-1) S1(j).  The next unit's
-    // S MMAs follow the last PVs of this one directly; its first PV_x waits
-    // until the map warps have read O_x out.
-    uint32_t kv_pos = 0, nk_pos = 0, pph[2] = {0u, 0u}, ou[2] = {0u, 0u};
-    bool ok = true;
+    // One lane issues.  Per unit, iteration j: PV0(j-1) S0(j) PV1(j-1) S1(j).
+    // The next unit's S MMAs follow the last PVs of this one directly; its
+    // first PV_x waits until the map warps have read O_x out.  Shared-memory
+    // descriptors are built once; a slot's descriptor is the base plus the
+    // slot offset in 16-byte units.
+    if (lane == 0) {
+      const uint64_t dq0 = smem_desc_sw128(q_smem(0), 16, 1024);
+      const uint64_t dq1 = smem_desc_sw128(q_smem(1), 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(slot_smem(0), 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(slot_smem(0), BN * 128, 1024);
+      constexpr uint32_t SLOT16 = L::SLOT >> 4;
+      uint32_t kv_pos = 0, nk_pos = 0, pph = 0u, ou = 0u;  // bit x: tile x
+      bool ok = true;
 #ifdef CATTN_TRACE
-    int ms = 0;  // running MMA iteration
+      int ms = 0;  // running MMA iteration
 #endif
-    for (uint32_t uc = 0; ok; ++uc) {
-      const int u = peek_unit(uc, SITE_MMA | 0x70);
-      if (u < 0) break;
-      const Unit t = decode_unit(p, u);
-      if (!(ok = warp_wait(bar_q_full, uc & 1u, abort, SITE_MMA | 0x10))) break;
-      tc_fence_after();
-      for (int j = 0; ok && j <= t.nkv; ++j) {
-        const uint32_t vpos = kv_pos + 2u * j - 1u, vs = vpos % L::NS;
-        const uint32_t kpos = kv_pos + 2u * j, ks = kpos % L::NS;
-        if (j >= 1) {
-          if (!(ok = warp_wait(kv_full(vs), (vpos / L::NS) & 1u, abort, SITE_MMA | 0x20))) break;
-          tc_fence_after();
-        }
+      for (uint32_t uc = 0; ok; ++uc) {
+        if (!thread_wait(unit_full(uc & 1u), (uc >> 1) & 1u, abort, SITE_MMA | 0x70)) break;
+        const int u = unit_ring[uc & 1u];
+        if (u < 0) break;
+        const Unit t = decode_unit(p, u);
+        mbar_arrive(unit_empty(uc & 1u));  // the unit is decoded
+        if (!(ok = thread_wait(bar_q_full, uc & 1u, abort, SITE_MMA | 0x10))) break;
+        for (int j = 0; ok && j <= t.nkv; ++j) {
+          const uint32_t vpos = kv_pos + 2u * j - 1u, vs = vpos % L::NS;
+          const uint32_t kpos = kv_pos + 2u * j, ks = kpos % L::NS;
+          if (j >= 1 && !(ok = thread_wait(kv_full(vs), (vpos / L::NS) & 1u, abort, SITE_MMA | 0x20)))
+            break;
 #pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          if (j >= 1 && j - 1 < t.n[x]) {  // O_x += P_x(j-1) V(j-1)
-            if (!(ok = warp_wait(p_full(x), pph[x], abort, SITE_MMA | 0x30))) break;
-            pph[x] ^= 1u;
-            if (j == 1 && !(ok = warp_wait(o_empty(x), (ou[x] & 1u) ^ 1u, abort, SITE_MMA | 0x50)))
-              break;
-            tc_fence_after();
+          for (int x = 0; x < 2; ++x) {
+            if (j >= 1 && j - 1 < t.n[x]) {  // O_x += P_x(j-1) V(j-1)
+              if (!(ok = thread_wait(p_full(x), (pph >> x) & 1u, abort, SITE_MMA | 0x30))) break;
+              pph ^= 1u << x;
+              if (j == 1 &&
+                  !(ok = thread_wait(o_empty(x), ((ou >> x) & 1u) ^ 1u, abort, SITE_MMA | 0x50)))
+                break;
+              tc_fence_after();
 #ifdef CATTN_TRACE
-            if (lane == 0) CATTN_TR(4 + 2 * x, ms);
+              CATTN_TR(4 + 2 * x, ms);
 #endif
-            if (lane == 0) {
-              issue_pv<DV>(tmem + TM_O + 128u * x, tmem + TM_S + 128u * x, slot_smem(vs), j > 1);
+              issue_pv_d<DV>(tmem + TM_O + 128u * x, tmem + TM_S + 128u * x, dv0 + vs * SLOT16,
+                             j > 1);
               if (j == t.n[x]) mma_commit(o_full(x));
             }
-            __syncwarp();
-          }
-          if (x == 0 && j < t.nkv) {
-            if (!(ok = warp_wait(kv_full(ks), (kpos / L::NS) & 1u, abort, SITE_MMA | 0x40))) break;
-            tc_fence_after();
-          }
-          if (j < t.n[x]) {  // S_x = Q_x K(j)^T
+            if (x == 0 && j < t.nkv &&
+                !(ok = thread_wait(kv_full(ks), (kpos / L::NS) & 1u, abort, SITE_MMA | 0x40)))
+              break;
+            if (j < t.n[x]) {  // S_x = Q_x K(j)^T
+              tc_fence_after();
 #ifdef CATTN_TRACE
-            if (lane == 0) CATTN_TR(5 + 2 * x, ms);
+              CATTN_TR(5 + 2 * x, ms);
 #endif
-            if (lane == 0) {
-              issue_qk<DK>(tmem + TM_S + 128u * x, q_smem(x), slot_smem(ks));
+              issue_qk_d<DK>(tmem + TM_S + 128u * x, x ? dq1 : dq0, dk0 + ks * SLOT16);
               mma_commit(s_full(x));
             }
-            __syncwarp();
           }
-        }
-        if (!ok) break;
-        if (lane == 0) {
+          if (!ok) break;
           if (j == t.nkv - 1) mma_commit(bar_q_empty);  // the unit's last S MMAs
           if (j < t.nkv) mma_commit(kv_empty(ks));
           if (j >= 1) mma_commit(kv_empty(vs));
           // every map warp delivered P for tile j-1, so all are done with its key norms
           if (VARIANT == kYat && j >= 1) mbar_arrive(nk_empty((nk_pos + j - 1) % NKS));
-        }
-        __syncwarp();
 #ifdef CATTN_TRACE
-        ++ms;
+          ++ms;
 #endif
+        }
+        kv_pos += 2u * t.nkv;
+        nk_pos += t.nkv;
+        ou ^= (t.n[0] > 0 ? 1u : 0u) | (t.n[1] > 0 ? 2u : 0u);
       }
-      kv_pos += 2u * t.nkv;
-      nk_pos += t.nkv;
-      ou[0] += t.n[0] > 0 ? 1u : 0u;
-      ou[1] += t.n[1] > 0 ? 1u : 0u;
-      release_unit(uc);
+      // all MMAs issued by this thread have completed once `drain` flips; this
+      // wait ignores the abort flag so TMEM is never released under a live MMA
+      mma_commit(bar_drain);
+      thread_wait(bar_drain, 0, abort, SITE_MMA | 0x60, false);
     }
-    // all MMAs issued by this thread have completed once `drain` flips; this
-    // wait ignores the abort flag so TMEM is never released under a live MMA
-    if (lane == 0) mma_commit(bar_drain);
-    __syncwarp();
-    warp_wait(bar_drain, 0, abort, SITE_MMA | 0x60, false);
   } else if (warp < MAP_WARPS) {
     // ------------------------------------------------------------ map warps
     const int x = warp >> 3;          // query tile
