@@ -25,7 +25,9 @@ int tk_pad(const cattn_problem_t *p) { return (p->Tk + kTile - 1) / kTile * kTil
 bool is_empty(const cattn_problem_t *p) { return p->B == 0 || p->h == 0 || p->Tq == 0; }
 
 // Workspace layout of the bf16 (tensor-core) path, each part 256-byte aligned:
-//   ctrl       256 B: the persistent schedule's unit ticket (zeroed per call)
+//   ctrl       256 B: the persistent schedule's unit ticket (zeroed by each
+//              forward), then (Yat) the largest key norm as fp32 bits
+//              (zeroed and written by the key-norm prologue)
 //   nk         Yat only: squared k row norms [B*hkv, Tk_pad], fp32 (the
 //              query norms are taken in-kernel from the Q tiles)
 //   part_o     key splits only: unnormalised partial outputs
@@ -193,7 +195,10 @@ int cattn_key_norms(const cattn_problem_t *p, const void *k, void *workspace,
   if (rc != CATTN_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float *nk = reinterpret_cast<float *>(static_cast<char *>(workspace) + w.nk);
-  return map_cuda(launch_row_sqnorm_bf16(k, nk, p->B * p->hkv, p->Tk, tk_pad(p), p->dk, s));
+  unsigned int *nk_max = reinterpret_cast<unsigned int *>(static_cast<char *>(workspace) + w.ctrl) + 1;
+  if ((rc = map_cuda(cudaMemsetAsync(nk_max, 0, sizeof(unsigned int), s))) != CATTN_OK) return rc;
+  return map_cuda(
+      launch_row_sqnorm_bf16(k, nk, p->B * p->hkv, p->Tk, tk_pad(p), p->dk, nk_max, s));
 }
 
 int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const void *k,
@@ -245,6 +250,7 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
   }
   if (variant == CATTN_YAT) {
     fp.nk = reinterpret_cast<const float *>(ws + w.nk);
+    fp.nk_max = reinterpret_cast<const unsigned int *>(ws + w.ctrl) + 1;
     if (!(p->flags & CATTN_FLAG_NORMS_READY)) {
       rc = cattn_key_norms(p, k, workspace, workspace_bytes, stream);
       if (rc != CATTN_OK) return rc;

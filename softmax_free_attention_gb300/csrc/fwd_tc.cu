@@ -539,6 +539,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float top[2] = {-INFINITY, -INFINITY};  // Yat: max kappa; else max raw dot
       float m_used = -INFINITY;               // softmax / s^tau: running max, log2 units
       float yb = 0.f, yeps = 0.f, qe = 0.f, tau = 1.f, seps = 0.f;
+      bool fast = false;  // Yat: the fast map path is exact up to rounding for this unit
       {
         const Unit t = decode_unit(p, u);
         nk_tiles = x ? t.n[1] : t.n[0];
@@ -579,6 +580,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           qe = (s2.x + s2.y) + yeps;
+          // the bounds under which the map's fast path is exact up to rounding
+          const float span = qe + __uint_as_float(*p.nk_max);
+          fast = yeps >= 0x1p-60f && __all_sync(FULL, span <= 0x1p61f && span * 0x1p-16f <= yeps);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_q_empty);
@@ -600,7 +604,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (VARIANT == kYat) {
           const uint32_t npos = nk_pos + j, ns = npos % NKS;
           if (!(ok = warp_wait(nk_full(ns), (npos / NKS) & 1u, abort, SITE_EPI | 0x20))) break;
-          const float2 *nk2 = reinterpret_cast<const float2 *>(nk_ring + ns * BN);
+          const float4 *nk4 = reinterpret_cast<const float4 *>(nk_ring + ns * BN);
           // chunk by chunk: P chunk c lands on S columns this warp has read
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
@@ -609,10 +613,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_wait_ld();
             tmem_ld_fence(sr);
             uint32_t hk[16];
-            if (partial)
-              yat_chunk<true>(sr, half * 2 + c, nk2, yb, qe, yeps, limit, acc, top, hk);
-            else
-              yat_chunk<false>(sr, half * 2 + c, nk2, yb, qe, yeps, limit, acc, top, hk);
+            if (fast) {
+              if (partial)
+                yat_chunk<true, true>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+              else
+                yat_chunk<false, true>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+            } else {
+              if (partial)
+                yat_chunk<true, false>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+              else
+                yat_chunk<false, false>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+            }
             tmem_st16(t_s + 16 * c, hk);
           }
         } else {

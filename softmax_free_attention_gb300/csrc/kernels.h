@@ -21,6 +21,7 @@ struct FwdParams {
   float *row_mass, *row_max;    // [B, h, Tq] or NULL
   const float *b, *eps, *tau;   // [h]
   const float *nk;              // [B*hkv, Tk_pad]  squared k row norms (Yat, bf16), zero padded
+  const unsigned int *nk_max;   // the largest of them, fp32 bits (Yat, bf16)
   int B, h, hkv, Tq, Tk, Tk_pad;
   int causal;
   float scale;
@@ -58,9 +59,10 @@ cudaError_t launch_fwd_simt(int variant, int dk, int dv, const FwdParams &p, cud
 bool fwd_simt_supported(int dk, int dv);
 
 // Squared row norms of a bf16 [BH, T, d] tensor into out[BH, T_pad] (zeros
-// for padded rows).
+// for padded rows); their maximum is folded into *max_bits (fp32 bits, which
+// must hold 0 or an earlier maximum) with atomicMax.
 cudaError_t launch_row_sqnorm_bf16(const void *x, float *out, int BH, int T, int T_pad, int d,
-                                   cudaStream_t s);
+                                   unsigned int *max_bits, cudaStream_t s);
 
 // Device status word set by kernels whose bounded waits gave up.
 cudaError_t read_and_clear_status(unsigned int *value);

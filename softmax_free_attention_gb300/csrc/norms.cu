@@ -4,10 +4,11 @@
 // |q|^2 + |k|^2 - 2 q.k from the dot products the scores already need
 // ("Softmax-Free Attention in JAX/Flax NNX", section "One module, two
 // compatibility functions").  This kernel supplies the key norms, in fp32
-// from the stored bf16 values.  It is bandwidth bound: d/8 threads share a
-// row, each reading one 16-byte vector of it; every thread keeps ROWS such
-// loads in flight before the shuffle reductions, and the grid strides over
-// the rows with a few CTAs per SM.
+// from the stored bf16 values, and the largest of them (the forward uses it
+// to check that products of two distances stay in the fp32 range).  It is
+// bandwidth bound: d/8 threads share a row, each reading one 16-byte vector
+// of it; every thread keeps ROWS such loads in flight before the shuffle
+// reductions, and the grid strides over the rows with a few CTAs per SM.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -21,7 +22,8 @@ constexpr int kRows = 4;  // row groups per thread per pass
 template <int G>  // threads per row = d / 8
 __global__ void __launch_bounds__(kThreads) row_sqnorm_kernel(const uint4 *__restrict__ x,
                                                               float *__restrict__ out, int T,
-                                                              int T_pad, long long n_out) {
+                                                              int T_pad, long long n_out,
+                                                              unsigned int *__restrict__ max_bits) {
   // One pass of a block covers SPAN consecutive output slots; T_pad is a
   // multiple of 128 >= SPAN, so a span never crosses from one head to the next.
   constexpr int RPB = kThreads / G;
@@ -29,6 +31,7 @@ __global__ void __launch_bounds__(kThreads) row_sqnorm_kernel(const uint4 *__res
   static_assert(128 % SPAN == 0, "a span stays inside one head");
   const int part = threadIdx.x % G;
   const int sub = threadIdx.x / G;
+  float running_max = 0.f;
   for (long long base = (long long)blockIdx.x * SPAN; base < n_out;
        base += (long long)gridDim.x * SPAN) {
     const long long bh = base / T_pad;
@@ -53,14 +56,28 @@ __global__ void __launch_bounds__(kThreads) row_sqnorm_kernel(const uint4 *__res
 #pragma unroll
       for (int o = G / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
       if (part == 0) out[base + i * RPB + sub] = acc;  // padded rows get zero
+      running_max = fmaxf(running_max, acc);
     }
+  }
+  // one atomic per CTA; non-negative floats order like their bit patterns
+  __shared__ float warp_max[kThreads / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    running_max = fmaxf(running_max, __shfl_xor_sync(0xffffffffu, running_max, o));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = running_max;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float m = warp_max[0];
+#pragma unroll
+    for (int w = 1; w < kThreads / 32; ++w) m = fmaxf(m, warp_max[w]);
+    atomicMax(max_bits, __float_as_uint(m));
   }
 }
 
 }  // namespace
 
 cudaError_t launch_row_sqnorm_bf16(const void *x, float *out, int BH, int T, int T_pad, int d,
-                                   cudaStream_t s) {
+                                   unsigned int *max_bits, cudaStream_t s) {
   const long long n_out = (long long)BH * T_pad;
   if (n_out == 0) return cudaSuccess;
   const int G = d / 8;
@@ -75,9 +92,9 @@ cudaError_t launch_row_sqnorm_bf16(const void *x, float *out, int BH, int T, int
   if (blocks > 8LL * sms) blocks = 8LL * sms;
   const uint4 *xv = reinterpret_cast<const uint4 *>(x);
   if (G == 16)
-    row_sqnorm_kernel<16><<<(unsigned)blocks, kThreads, 0, s>>>(xv, out, T, T_pad, n_out);
+    row_sqnorm_kernel<16><<<(unsigned)blocks, kThreads, 0, s>>>(xv, out, T, T_pad, n_out, max_bits);
   else
-    row_sqnorm_kernel<8><<<(unsigned)blocks, kThreads, 0, s>>>(xv, out, T, T_pad, n_out);
+    row_sqnorm_kernel<8><<<(unsigned)blocks, kThreads, 0, s>>>(xv, out, T, T_pad, n_out, max_bits);
   return cudaGetLastError();
 }
 
