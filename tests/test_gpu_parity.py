@@ -218,3 +218,21 @@ def test_constant_values_give_constant_output():
         out, _, _ = attention.forward(variant, inp["q"], inp["k"], v, causal=True, **kw)
         torch.cuda.synchronize()
         assert (out.float() - 0.75).abs().max().item() <= 2e-2 * 0.75, variant
+
+
+# ---------------------------------------------------------------- both Yat map paths
+
+@pytest.mark.parametrize("eps,qk,where", [
+    (0.5, 1.0, "fast path: eps well above the rounding of |q|^2 + |k|^2"),
+    (1e-3, 4.0, "exact path: eps below (|q|^2 + max |k|^2) 2^-16"),
+    (1e-20, 1.0, "exact path: eps below 2^-60"),
+])
+def test_yat_fast_and_exact_map_paths(eps, qk, where):
+    """The Yat map has a fast path (one reciprocal per key pair, no clamp)
+    taken only when the norms bound its rounding, and the plain path
+    otherwise; both must match the oracle."""
+    w = _wl("paths", 1, 2, 2, 300, 300, 128, 128, causal=True, qk=qk, seed=77)
+    inp = workloads.generate(w)
+    inp["yat_b"] = np.full(2, 0.5, dtype=np.float32)
+    inp["yat_eps"] = np.full(2, eps, dtype=np.float32)
+    pu.full_parity("yat", inp, causal=True, scale=w.scale, where=where)
