@@ -23,51 +23,57 @@ __device__ __forceinline__ float2 f2(uint32_t a, uint32_t b) {
   return make_float2(__uint_as_float(a), __uint_as_float(b));
 }
 
-// Yat map over one 32-key chunk (columns 32c .. 32c+31 of the tile) of one row.  sr: raw
-// dots; nk4: squared key norms of the tile (groups of four); qe = |q|^2 + eps.
-// kappa = (dot + b)^2 / max(|q|^2 + |k|^2 - 2 dot + eps, eps); masked keys
-// (col >= limit) get kappa = 0.
-// FAST: one reciprocal per pair of keys, 1/den0 = den1 / (den0 den1), which
-// halves the SFU work, and no clamp.  The caller takes it only when it is
-// exact up to rounding: the assembled |q-k|^2 can fall below zero only by the
-// rounding of |q|^2 + |k|^2 - 2 q.k, which is far below eps when
+// Yat kernel of one pair of keys: kappa = (dot + b)^2 / max(|q|^2 + |k|^2 -
+// 2 dot + eps, eps) with qe = |q|^2 + eps.
+// FAST: one reciprocal per pair, 1/den0 = den1 / (den0 den1), which halves
+// the SFU work, and no clamp.  The caller takes it only when it is exact up
+// to rounding: the assembled |q-k|^2 can fall below zero only by the rounding
+// of |q|^2 + |k|^2 - 2 q.k, which is far below eps when
 // (|q|^2 + max |k|^2) 2^-16 <= eps, and then every den0 den1 is a normal fp32
 // number if also eps >= 2^-60 and |q|^2 + max |k|^2 <= 2^61.
+template <bool FAST>
+__device__ __forceinline__ float2 yat_pair(float2 d, float2 nk, float2 b2, float2 qe2, float yeps) {
+  const float2 t = __fadd2_rn(d, b2);
+  const float2 num = __fmul2_rn(t, t);
+  const float2 den = __ffma2_rn(make_float2(-2.f, -2.f), d, __fadd2_rn(qe2, nk));
+  if (FAST) {
+    const float r = rcp_approx(den.x * den.y);
+    return __fmul2_rn(__fmul2_rn(num, make_float2(den.y, den.x)), make_float2(r, r));
+  }
+  return __fmul2_rn(num, make_float2(rcp_approx(fmaxf(den.x, yeps)), rcp_approx(fmaxf(den.y, yeps))));
+}
+
+// Masks, accumulates and packs one pair: masked keys (col >= limit) get
+// kappa = 0; mass (two chains) and top take kappa; returns P = bf16(kappa).
+template <bool PARTIAL>
+__device__ __forceinline__ uint32_t yat_fold(float2 k, int col, int limit, float2 &mass, float &top) {
+  if (PARTIAL) {
+    k.x = col < limit ? k.x : 0.f;
+    k.y = col + 1 < limit ? k.y : 0.f;
+  }
+  mass = __fadd2_rn(mass, k);
+  top = max3(top, k.x, k.y);
+  return pack_bf16x2(k.x, k.y);
+}
+
+// Yat map over one 32-key chunk (columns 32c .. 32c+31 of the tile) of one row.  sr: raw
+// dots; nk4: squared key norms of the tile (groups of four).
 template <bool PARTIAL, bool FAST>
 __device__ __forceinline__ void yat_chunk(const uint32_t (&sr)[32], int c, const float4 *nk4,
                                           float yb, float qe, float yeps, int limit,
                                           float2 (&mass)[2], float (&top)[2],
                                           uint32_t (&pk)[16]) {
   const float2 b2 = make_float2(yb, yb), qe2 = make_float2(qe, qe);
-  const float2 m2 = make_float2(-2.f, -2.f);
 #pragma unroll
   for (int i = 0; i < 32; i += 4) {
     const float4 n4 = nk4[(c * 32 + i) >> 2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int ii = i + 2 * h;
-      const int col = c * 32 + ii;
-      const int chain = h;
-      const float2 d = f2(sr[ii], sr[ii + 1]);
-      const float2 t = __fadd2_rn(d, b2);
-      const float2 num = __fmul2_rn(t, t);
-      const float2 den =
-          __ffma2_rn(m2, d, __fadd2_rn(qe2, h ? make_float2(n4.z, n4.w) : make_float2(n4.x, n4.y)));
-      float2 k;
-      if (FAST) {
-        const float r = rcp_approx(den.x * den.y);
-        k = __fmul2_rn(__fmul2_rn(num, make_float2(den.y, den.x)), make_float2(r, r));
-      } else {
-        k = __fmul2_rn(num, make_float2(rcp_approx(fmaxf(den.x, yeps)),
-                                        rcp_approx(fmaxf(den.y, yeps))));
-      }
-      if (PARTIAL) {
-        k.x = col < limit ? k.x : 0.f;
-        k.y = col + 1 < limit ? k.y : 0.f;
-      }
-      mass[chain] = __fadd2_rn(mass[chain], k);
-      top[chain] = max3(top[chain], k.x, k.y);
-      pk[ii >> 1] = pack_bf16x2(k.x, k.y);
+      const float2 k = yat_pair<FAST>(f2(sr[ii], sr[ii + 1]),
+                                      h ? make_float2(n4.z, n4.w) : make_float2(n4.x, n4.y), b2, qe2,
+                                      yeps);
+      pk[ii >> 1] = yat_fold<PARTIAL>(k, c * 32 + ii, limit, mass[h], top[h]);
     }
   }
 }
