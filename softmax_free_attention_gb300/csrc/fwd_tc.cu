@@ -598,6 +598,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // keys of tile j allowed for col < limit (col counts the whole tile)
         const int limit = min(BN, lim_base - j * BN);
         const bool partial = __any_sync(FULL, limit < BN);  // warp-uniform path choice
+        // Yat takes one path per 32-key chunk: every key allowed for all the
+        // warp's rows, none allowed (P = 0, nothing to compute), or per key
+        auto chunk_kind = [&](int c) -> int {  // 0 all allowed, 1 none, 2 mixed
+          const int c0 = 32 * (half * 2 + c);
+          if (!partial || __all_sync(FULL, c0 + 32 <= limit)) return 0;
+          if (__all_sync(FULL, c0 >= limit)) return 1;
+          return 2;
+        };
 
         bool rescale = false;
         float corr = 1.f;
@@ -608,21 +616,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // chunk by chunk: P chunk c lands on S columns this warp has read
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            uint32_t sr[32];
-            tmem_ld32(t_s + 32 * c, sr);
-            tmem_wait_ld();
-            tmem_ld_fence(sr);
+            const int kind = chunk_kind(c);
             uint32_t hk[16];
-            if (fast) {
-              if (partial)
-                yat_chunk<true, true>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
-              else
-                yat_chunk<false, true>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+            if (kind == 1) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) hk[i] = 0u;
             } else {
-              if (partial)
-                yat_chunk<true, false>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
-              else
-                yat_chunk<false, false>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+              uint32_t sr[32];
+              tmem_ld32(t_s + 32 * c, sr);
+              tmem_wait_ld();
+              tmem_ld_fence(sr);
+              if (fast) {
+                if (kind == 2)
+                  yat_chunk<true, true>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+                else
+                  yat_chunk<false, true>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+              } else {
+                if (kind == 2)
+                  yat_chunk<true, false>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+                else
+                  yat_chunk<false, false>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+              }
             }
             tmem_st16(t_s + 16 * c, hk);
           }
