@@ -218,6 +218,7 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
   fp.k = k;
   fp.v = v;
   fp.out = out;
+  fp.out_align32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
   fp.row_mass = row_mass;
   fp.row_max = row_max_score;
   fp.b = b;

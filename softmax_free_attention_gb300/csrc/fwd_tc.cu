@@ -747,11 +747,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               packed[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv,
                                       __uint_as_float(o[2 * i + 1]) * inv);
             if (row_ok) {
-              uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+              // each thread writes its own row: whole 32-byte sectors when the
+              // output allows it
+              if (p.out_align32) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                    packed[4 * i + 3]);
+                for (int i = 0; i < 2; ++i)
+                  stg256(orow + c * 32 + 16 * i, packed[8 * i], packed[8 * i + 1], packed[8 * i + 2],
+                         packed[8 * i + 3], packed[8 * i + 4], packed[8 * i + 5], packed[8 * i + 6],
+                         packed[8 * i + 7]);
+              } else {
+                uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                      packed[4 * i + 3]);
+              }
             }
           }
           if (row_ok && half == 0) {
@@ -769,11 +779,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_ld32(t_o + c * 32, o);
             tmem_wait_ld();
             tmem_ld_fence(o);
-            if (row_ok) {
-              uint4 *dst = reinterpret_cast<uint4 *>(prow + c * 32);
+            if (row_ok) {  // the workspace is 256-byte aligned
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+              for (int i = 0; i < 4; ++i)
+                stg256(prow + c * 32 + 8 * i, o[8 * i], o[8 * i + 1], o[8 * i + 2], o[8 * i + 3],
+                       o[8 * i + 4], o[8 * i + 5], o[8 * i + 6], o[8 * i + 7]);
             }
           }
           if (row_ok && half == 0)

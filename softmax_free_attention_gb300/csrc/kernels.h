@@ -18,6 +18,7 @@ constexpr int kTcKeyTile = 128;
 struct FwdParams {
   const void *q, *k, *v;        // element pointers (the tensor-core path reads through TMA)
   void *out;                    // [B, h, Tq, dv]
+  int out_align32;              // out is 32-byte aligned (whole-sector stores)
   float *row_mass, *row_max;    // [B, h, Tq] or NULL
   const float *b, *eps, *tau;   // [h]
   const float *nk;              // [B*hkv, Tk_pad]  squared k row norms (Yat, bf16), zero padded

@@ -276,6 +276,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// 32-byte global store (the address must be 32-byte aligned).
+__device__ __forceinline__ void stg256(void *ptr, uint32_t a0, uint32_t a1, uint32_t a2,
+                                       uint32_t a3, uint32_t a4, uint32_t a5, uint32_t a6,
+                                       uint32_t a7) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ptr), "r"(a0), "r"(a1),
+               "r"(a2), "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+               : "memory");
+}
+
 // 16-byte shared-memory load.
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
