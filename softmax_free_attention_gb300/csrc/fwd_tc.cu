@@ -726,13 +726,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float all_top = fmaxf(ptop, fb[(1 * 2 + (half ^ 1)) * BM + r]);
         // the partner reads fb before either warp writes it for the next unit
         named_barrier_sync(named_bar, 64);
-        if (!(ok = warp_wait(o_full(x), (ph >> 1) & 1u, abort, SITE_EPI | 0x30))) break;
-        tc_fence_after();
+        // everything that does not need O before the wait, while the last PV runs
         const Unit t = decode_unit(p, unit_ring[uc & 1u]);
         const int row = t.q0 + x * BM + r;
         const bool row_ok = row < p.Tq;
+        const float inv = VARIANT == kYat ? 1.f / (total + 1e-9f) : 1.f / total;
+        if (!(ok = warp_wait(o_full(x), (ph >> 1) & 1u, abort, SITE_EPI | 0x30))) break;
+        tc_fence_after();
         if (p.n_splits == 1) {
-          const float inv = VARIANT == kYat ? 1.f / (total + 1e-9f) : 1.f / total;
           __nv_bfloat16 *orow = reinterpret_cast<__nv_bfloat16 *>(p.out) +
                                 ((size_t)t.bh * p.Tq + row) * DV + half * (DV / 2);
 #pragma unroll
