@@ -38,9 +38,15 @@
 // is written over S_x; the MMA pipe executes a CTA's MMAs in issue order, so
 // PV_x(j) reads P_x before S_x(j+1) lands, and the commit that signals S_x(j)
 // also covers PV_x(j-1).  The MMA order PV0(j-1) S0(j) PV1(j-1) S1(j) lets
-// one query tile's MMAs run while the other tile is being mapped.  Between
-// units the next unit's S MMAs follow the last PVs at once; its first PV_x
-// waits (o_empty) until the map warps have read O_x out.
+// one query tile's MMAs run while the other tile is being mapped.  For Yat
+// and s^tau each PV is issued in two halves: the map warps signal once the
+// first 32-key chunk of their P is written, so half of PV_x runs while they
+// map the second chunk and only the other half stands between the map and
+// S_x(j+1).  (PV reads P from TMEM, and that form of the MMA runs markedly
+// slower than one with both operands in shared memory, so its latency is
+// worth hiding.)  Between units the next unit's S MMAs follow the last PVs
+// at once; its first PV_x waits (o_empty) until the map warps have read O_x
+// out.
 //
 // Warp roles (576 threads): warps 0-15 map (warp w: query tile x = w/8, TMEM
 // lanes 32*(w%4)..+31 = those query rows, key columns [64h, 64h+64) with
@@ -123,8 +129,9 @@ struct Layout {
   static constexpr int XCHG_FLOATS = 16 * BM;
   static constexpr int OFF_BAR = OFF_XCHG + XCHG_FLOATS * 4;
   // q_full, q_empty, kv_full[NS], kv_empty[NS], nk_full[NKS], nk_empty[NKS],
-  // s_full[2], p_full[2], o_full[2], o_empty[2], unit_full[2], unit_empty[2], drain
-  static constexpr int NBAR = 2 + 2 * NS + 2 * NKS + 13;
+  // s_full[2], p_full[2], o_full[2], o_empty[2], unit_full[2], unit_empty[2], drain,
+  // p_half[2]
+  static constexpr int NBAR = 2 + 2 * NS + 2 * NKS + 15;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // TMEM base address, abort flag, unit ring[2]
   static constexpr int BYTES = OFF_MISC + 16;
@@ -181,6 +188,21 @@ __device__ __forceinline__ void issue_qk_d(uint32_t d_tmem, uint64_t qdesc, uint
   }
 }
 
+// Half of O += P V: PART 0 takes keys [0, 32) and [64, 96) (the first
+// 32-key chunk of each column half, which the map warps finish first), PART 1
+// the other two chunks.
+template <int DV, int PART>
+__device__ __forceinline__ void issue_pv_part(uint32_t d_tmem, uint32_t p_tmem, uint64_t vdesc,
+                                              bool accumulate) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(BM, DV, true);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int kk = (i >> 1) * 4 + PART * 2 + (i & 1);
+    mma_ts(d_tmem, p_tmem + (uint32_t)(kk >> 2) * 64 + (uint32_t)(kk & 3) * 8,
+           vdesc + (uint64_t)((kk * 2048) >> 4), IDESC, (accumulate || PART == 1 || i > 0) ? 1u : 0u);
+  }
+}
+
 // O += P V from a prebuilt descriptor of the V slot.
 template <int DV>
 __device__ __forceinline__ void issue_pv_d(uint32_t d_tmem, uint32_t p_tmem, uint64_t vdesc,
@@ -218,6 +240,23 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
     mma_ts(d_tmem, p_tmem + (uint32_t)(kk >> 2) * 64 + (uint32_t)(kk & 3) * 8,
            smem_desc_sw128(v_smem + (uint32_t)kk * 2048, BN * 128, 1024), IDESC,
            (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+// Multiply dv/2 columns of this thread's row of O by f in place, 16 columns
+// at a time (for callers that still hold other registers).
+template <int DV>
+__device__ __forceinline__ void scale_o_half16(uint32_t t_o, float f) {
+#pragma unroll
+  for (int c = 0; c < DV / 32; ++c) {
+    uint32_t r[16];
+    tmem_ld16(t_o + c * 16, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(r[i])::"memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * f);
+    tmem_st16(t_o + c * 16, r);
   }
 }
 
@@ -286,6 +325,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using L = Layout<DK, DV>;
+  // Yat and s^tau split each PV in two: half of it runs while the map warps
+  // work on the second half of P (softmax, whose map is the shortest, keeps
+  // one PV and its rescale after the map)
+  constexpr bool SPLIT_PV = VARIANT != kSoftmax;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -309,6 +352,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto unit_full = [&](uint32_t s) { return bar0 + 8u * (B2 + 8 + s); };
   auto unit_empty = [&](uint32_t s) { return bar0 + 8u * (B2 + 10 + s); };
   const uint32_t bar_drain = bar0 + 8u * (B2 + 12);
+  auto p_half = [&](int x) { return bar0 + 8u * (B2 + 13 + x); };
   auto q_smem = [&](int x) { return sb + L::OFF_Q + (uint32_t)x * L::Q_TILE; };
   auto slot_smem = [&](uint32_t s) { return sb + L::OFF_RING + s * L::SLOT; };
   const float *nk_ring = reinterpret_cast<const float *>(smem + L::OFF_NK);
@@ -332,6 +376,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int x = 0; x < 2; ++x) {
       mbar_init(s_full(x), 1);
       mbar_init(p_full(x), 8 * 32);  // every thread of the eight map warps of tile x
+      mbar_init(p_half(x), 8 * 32);  // the same, once the first chunk of P is written (Yat, s^tau)
       mbar_init(o_full(x), 1);
       mbar_init(o_empty(x), 8);      // lane 0 of each of those warps
       mbar_init(unit_full(x), 1);
@@ -464,7 +509,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
-            if (j >= 1 && j - 1 < t.n[x]) {  // O_x += P_x(j-1) V(j-1)
+            if (j >= 1 && j - 1 < t.n[x] && SPLIT_PV) {  // O_x += P_x(j-1) V(j-1), in two halves
+              if (!(ok = thread_wait(p_half(x), (pph >> x) & 1u, abort, SITE_MMA | 0x34))) break;
+              if (j == 1 &&
+                  !(ok = thread_wait(o_empty(x), ((ou >> x) & 1u) ^ 1u, abort, SITE_MMA | 0x50)))
+                break;
+              tc_fence_after();
+#ifdef CATTN_TRACE
+              CATTN_TR(4 + 2 * x, ms);
+#endif
+              issue_pv_part<DV, 0>(tmem + TM_O + 128u * x, tmem + TM_S + 128u * x,
+                                   dv0 + vs * SLOT16, j > 1);
+              if (!(ok = thread_wait(p_full(x), (pph >> x) & 1u, abort, SITE_MMA | 0x30))) break;
+              pph ^= 1u << x;
+              tc_fence_after();
+              issue_pv_part<DV, 1>(tmem + TM_O + 128u * x, tmem + TM_S + 128u * x,
+                                   dv0 + vs * SLOT16, true);
+              if (j == t.n[x]) mma_commit(o_full(x));
+            } else if (j >= 1 && j - 1 < t.n[x]) {  // O_x += P_x(j-1) V(j-1)
               if (!(ok = thread_wait(p_full(x), (pph >> x) & 1u, abort, SITE_MMA | 0x30))) break;
               pph ^= 1u << x;
               if (j == 1 &&
@@ -639,6 +701,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
             }
             tmem_st16(t_s + 16 * c, hk);
+            if (c == 0) {  // the first chunk of P: half of PV may start
+              tmem_wait_st();
+              tc_fence_before();
+              mbar_arrive(p_half(x));
+            }
           }
         } else {
           uint32_t sr[2][32];
@@ -679,7 +746,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int c = 0; c < 2; ++c) {
             if (VARIANT == kStau && c == 1) {
               // s^tau holds more temporaries: read the second chunk again
-              // rather than keep it live through the first one's map
+              // rather than keep it live through the first one's map and the
+              // rescale of O
               tmem_ld32(t_s + 32, sr[1]);
               tmem_wait_ld();
               tmem_ld_fence(sr[1]);
@@ -698,12 +766,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 stau_chunk<false>(sr[c], half * 2 + c, p.scale, c2, tau, seps, -m_used, limit, acc,
                                   hk);
             }
-            tmem_st16(t_s + 16 * c, hk);
+            if (SPLIT_PV && c == 0) {
+              // O holds every tile before j (S_x(j) landed after PV_x(j-1)):
+              // bring this warp's dv/2 columns onto the new max before the
+              // first half of PV(j) adds to it
+              if (rescale) scale_o_half16<DV>(t_o, corr);
+              tmem_st16(t_s, hk);
+              tmem_wait_st();
+              tc_fence_before();
+              mbar_arrive(p_half(x));  // the first chunk of P: half of PV may start
+            } else {
+              tmem_st16(t_s + 16 * c, hk);
+            }
           }
+          // softmax: O_x holds every tile before j (S_x(j) landed after
+          // PV_x(j-1)): bring this warp's dv/2 columns onto the new max
+          if (!SPLIT_PV && rescale) scale_o_half<DV>(t_o, corr);
         }
-        // O_x holds every tile before j (S_x(j) landed after PV_x(j-1)): bring
-        // this warp's dv/2 columns onto the new max
-        if (rescale) scale_o_half<DV>(t_o, corr);
         tmem_wait_st();
         tc_fence_before();
 #ifdef CATTN_TRACE
