@@ -72,6 +72,10 @@ def _load():
         lib = ctypes.CDLL(_LIB_PATH)
         lib.oracle_forward.argtypes = [ctypes.POINTER(_Problem), ctypes.c_int]
         lib.oracle_forward.restype = ctypes.c_int
+        lib.oracle_tau_star_scores.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_double]
+        lib.oracle_tau_star_scores.restype = ctypes.c_double
+        lib.oracle_tau_star.argtypes = [ctypes.POINTER(_Problem), ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_tau_star.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -163,3 +167,40 @@ def forward(variant, q, k, v, *, b=None, eps=None, tau=None, causal=False, scale
     if return_weights:
         return out, row_mass, row_max, weights
     return out, row_mass, row_max
+
+
+def tau_star_scores(s, eps):
+    """tau* = Cov(s, ln phi(s)) / Var(ln phi(s)) over a vector of scores, phi =
+    softplus + eps ("s^tau: a focal-length knob for attention", the closed-form
+    paragraph).  fp64; NaN for fewer than two scores."""
+    arr = np.ascontiguousarray(np.asarray(s, dtype=np.float64).reshape(-1))
+    return float(_load().oracle_tau_star_scores(arr.ctypes.data, arr.size, float(eps)))
+
+
+def tau_star(q, k, eps, *, causal=False, scale=None):
+    """tau* of every query head from the softmax scores s = scale * q.k of all
+    allowed (row, key) pairs of that head, pooled over the batch.
+
+    q: [B, h, Tq, dk]; k: [B, hkv, Tk, dk]; eps: one value per query head.
+    Returns (tau [h], n [h]) in fp64, n = the number of allowed pairs.
+    """
+    q = _as_f64(q, "q")
+    k = _as_f64(k, "k")
+    if q.ndim != 4 or k.ndim != 4:
+        raise ValueError("q, k must be 4-D [B, heads, T, d]")
+    B, h, Tq, dk = q.shape
+    Bk, hkv, Tk, dk2 = k.shape
+    if (Bk, dk2) != (B, dk):
+        raise ValueError("inconsistent q/k shapes")
+    if scale is None:
+        scale = 1.0 / np.sqrt(dk)
+    eps = _per_head(eps, h, "eps")
+    tau = np.zeros(h, dtype=np.float64)
+    n = np.zeros(h, dtype=np.float64)
+    prob = _Problem(STAU, B, h, hkv, Tq, Tk, dk, 1, int(bool(causal)), float(scale),
+                    q.ctypes.data, k.ctypes.data, None, None, eps.ctypes.data, None,
+                    None, 0, None, None, None, None)
+    rc = _load().oracle_tau_star(ctypes.byref(prob), tau.ctypes.data, n.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle_tau_star failed with code {rc}")
+    return tau, n

@@ -46,6 +46,15 @@
  *     row_max = max kappa; softmax row_mass = log-sum-exp of the scaled
  *     scores, row_max = max scaled score; s^tau row_mass = log sum phi^tau,
  *     row_max = max scaled score.
+ *
+ * tau* (same s^tau page, the closed-form paragraph: tau* = Cov(s, log phi(s))
+ * / Var(log phi(s)), taken from the score distribution of one forward pass,
+ * one value per attention head).  Readings: the scores are the softmax
+ * scores s = scale * q.k of every allowed (query row, key) pair of the query
+ * head, pooled over the batch; log is the natural log (the slope that makes
+ * tau * ln phi(s) + C fit s, which is what the page's equivalence
+ * s^tau <-> softmax needs); phi uses the head's s^tau eps.  Covariance and
+ * variance are computed in two passes (means first), in fp64.
  */
 #include <math.h>
 #include <pthread.h>
@@ -258,4 +267,57 @@ int oracle_forward(const oracle_problem *p, int nthreads) {
   free(jobs);
   free(tids);
   return rc;
+}
+
+/* tau* over n scores: the least-squares slope Cov(s, ln phi(s)) / Var(ln phi(s))
+ * with phi = softplus + eps.  Two passes: the means, then the centred sums.
+ * Returns NaN when there are fewer than two scores or ln phi is constant. */
+double oracle_tau_star_scores(const double *s, int64_t n, double eps) {
+  if (!s || n < 2) return NAN;
+  double ms = 0.0, mg = 0.0;
+  for (int64_t i = 0; i < n; ++i) {
+    ms += s[i];
+    mg += log(softplus(s[i]) + eps);
+  }
+  ms /= (double)n;
+  mg /= (double)n;
+  double cov = 0.0, var = 0.0;
+  for (int64_t i = 0; i < n; ++i) {
+    const double ds = s[i] - ms, dg = log(softplus(s[i]) + eps) - mg;
+    cov += ds * dg;
+    var += dg * dg;
+  }
+  if (!(var > 0.0)) return NAN;
+  return cov / var;
+}
+
+/* tau* of every query head: gathers the allowed scores s = scale * q.k of
+ * the head over all batches and rows (causal: key j <= row t), then applies
+ * oracle_tau_star_scores with the head's eps.  tau_out: [h].  n_out
+ * (optional): [h] counts of allowed pairs. */
+int oracle_tau_star(const oracle_problem *p, double *tau_out, double *n_out) {
+  if (!p || !p->q || !p->k || !p->eps || !tau_out) return ORACLE_EBADARG;
+  if (p->B <= 0 || p->h <= 0 || p->hkv <= 0 || p->Tq <= 0 || p->Tk <= 0 || p->dk <= 0)
+    return ORACLE_EBADARG;
+  if (p->h % p->hkv != 0) return ORACLE_EBADARG;
+  if (p->causal && p->Tq != p->Tk) return ORACLE_EBADARG;
+  const int group = p->h / p->hkv;
+  double *sc = (double *)malloc(sizeof(double) * (size_t)p->B * p->Tq * p->Tk);
+  if (!sc) return ORACLE_ENOMEM;
+  for (int i = 0; i < p->h; ++i) {
+    int64_t n = 0;
+    for (int b = 0; b < p->B; ++b)
+      for (int t = 0; t < p->Tq; ++t) {
+        const double *qr = p->q + (((int64_t)b * p->h + i) * p->Tq + t) * p->dk;
+        for (int j = 0; j < p->Tk; ++j) {
+          if (p->causal && j > t) continue;
+          const double *kr = p->k + (((int64_t)b * p->hkv + i / group) * p->Tk + j) * p->dk;
+          sc[n++] = p->scale * dot(qr, kr, p->dk);
+        }
+      }
+    tau_out[i] = oracle_tau_star_scores(sc, n, p->eps[i]);
+    if (n_out) n_out[i] = (double)n;
+  }
+  free(sc);
+  return ORACLE_OK;
 }

@@ -327,3 +327,54 @@ def test_generator_parametrisations():
     for key in ("q", "k", "v"):
         assert (g1[key] == g2[key]).all()  # seeded
     assert np.all(g1["yat_b"] == np.float32(math.log(2.0)))
+
+
+# --------------------------------------------------------------------------
+# tau* ("s^tau: a focal-length knob for attention", closed-form paragraph:
+# tau* = Cov(s, log phi(s)) / Var(log phi(s)), per head, from the scores of
+# one forward pass)
+# --------------------------------------------------------------------------
+
+def _ln_phi(s, eps):
+    # softplus by its definition log(1 + e^s), in exact-enough fp64 for |s| < 30
+    return math.log(math.log1p(math.exp(s)) + eps)
+
+
+@pytest.mark.parametrize("s1,s2,eps", [(0.3, -1.2, 0.1), (2.5, 0.0, 1e-6), (-3.0, -2.0, 0.7)])
+def test_tau_star_two_scores_closed_form(s1, s2, eps):
+    # with two scores the least-squares slope is the secant slope: a wrong
+    # log base, eps inside the softplus or a variance in the numerator fail it
+    want = (s1 - s2) / (_ln_phi(s1, eps) - _ln_phi(s2, eps))
+    assert oracle.tau_star_scores([s1, s2], eps) == pytest.approx(want, rel=1e-12)
+
+
+def test_tau_star_matches_polyfit_and_invariances():
+    rng = np.random.default_rng(5)
+    s = rng.standard_normal(3001) * 1.7 + 0.4
+    eps = 1e-6
+    g = np.log(np.logaddexp(0.0, s) + eps)
+    slope = np.polyfit(g, s, 1)[0]  # least squares s ~ tau g + C, a library routine
+    t = oracle.tau_star_scores(s, eps)
+    assert t == pytest.approx(slope, rel=1e-9)
+    assert oracle.tau_star_scores(s[::-1], eps) == pytest.approx(t, rel=1e-12)
+    assert oracle.tau_star_scores(np.concatenate([s, s]), eps) == pytest.approx(t, rel=1e-12)
+    assert math.isnan(oracle.tau_star_scores([1.0], eps))
+
+
+def test_tau_star_heads_gather_allowed_scores():
+    # brute force on a tiny GQA problem: enumerate the allowed (row, key) scores
+    # of each query head over the batch, then the score-level estimator
+    rng = np.random.default_rng(6)
+    B, h, hkv, T, d = 2, 4, 2, 7, 5
+    q = rng.standard_normal((B, h, T, d))
+    k = rng.standard_normal((B, hkv, T, d))
+    eps = np.array([1e-6, 0.3, 1e-3, 2.0])
+    scale = 0.45
+    for causal in (True, False):
+        tau, n = oracle.tau_star(q, k, eps, causal=causal, scale=scale)
+        for i in range(h):
+            sc = [scale * float(np.dot(q[b, i, t], k[b, i // (h // hkv), j]))
+                  for b in range(B) for t in range(T) for j in range(T)
+                  if not (causal and j > t)]
+            assert n[i] == len(sc) == (B * T * (T + 1) // 2 if causal else B * T * T)
+            assert tau[i] == pytest.approx(oracle.tau_star_scores(sc, eps[i]), rel=1e-12)
