@@ -173,6 +173,28 @@ int cattn_forward_noalloc(int variant, const cattn_problem_t *p, const void *q, 
                           void *out, float *row_mass, float *row_max_score,
                           cattn_stream_t stream);
 
+/* tau* of the s^tau map, per query head, from one pass over the softmax
+ * scores ("s^tau: a focal-length knob for attention", the closed-form
+ * paragraph): tau*_i = Cov(s, ln phi(s)) / Var(ln phi(s)) over the scores
+ * s = scale * q.k of every allowed (query row, key) pair of query head i,
+ * pooled over the batch, with phi(s) = softplus(s) + eps_i.  It is the
+ * least-squares slope that makes tau * ln phi(s) + C fit s, i.e. the tau for
+ * which the s^tau map tracks the softmax map on these scores.
+ *
+ * The scores come from the same tensor-core S = Q K^T as the forward (bf16
+ * only; dk in {64, 128}; p->dv and v are not used).  Causal masking as in the
+ * forward.  eps: device fp32 [h] (> 0, not checked).  tau_star: device fp32
+ * [h] output (NaN for a head with fewer than two scores).  moments: optional
+ * device fp64 [h][6] output: n, sum s, sum g, sum s g, sum g^2 with
+ * g = ln phi(s) - g0, and g0 = ln(ln 2 + eps_i) (the sums are taken from fp32
+ * partial sums of each thread's scores in a work unit, added in fp64).
+ * workspace: cattn_tau_star_workspace_bytes(p) bytes, 256-byte aligned,
+ * contents need not be initialised.  Asynchronous on `stream`. */
+size_t cattn_tau_star_workspace_bytes(const cattn_problem_t *p);
+int cattn_tau_star(const cattn_problem_t *p, const void *q, const void *k, const float *eps,
+                   float *tau_star, double *moments, void *workspace, size_t workspace_bytes,
+                   cattn_stream_t stream);
+
 /* Synchronises `stream`, then reports (and clears) the device-side status
  * word the kernels set when a bounded wait gives up: CATTN_ERR_TIMEOUT if
  * any kernel since the last check did so, CATTN_ERR_CUDA if the stream

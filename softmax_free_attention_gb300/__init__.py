@@ -4,5 +4,6 @@ The compute path is the C-ABI library libcattn.so (hand-written sm_103a CUDA,
 see include/cattn.h); this package holds its build script, the ctypes binding
 and the seeded workload generators.
 """
-from .attention import check_status, forward, make_problem, key_norms, workspace_bytes  # noqa: F401
+from .attention import (check_status, forward, key_norms, make_problem, tau_star,  # noqa: F401
+                        workspace_bytes)
 from .native import CattnError  # noqa: F401

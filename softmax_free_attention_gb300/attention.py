@@ -141,6 +141,44 @@ def _forward_from_host(vid, q, k, v, *, b, eps, tau, causal, scale, telemetry):
     return res
 
 
+def tau_star(q, k, eps, *, causal=False, scale=None, return_moments=False, workspace=None):
+    """tau* of the s^tau map per query head from one pass over the softmax
+    scores ("s^tau: a focal-length knob for attention", closed form):
+    Cov(s, ln phi(s)) / Var(ln phi(s)) over the allowed scores s = scale q.k of
+    each head, pooled over the batch, phi = softplus + eps.
+
+    q [B,h,Tq,dk], k [B,hkv,Tk,dk]: torch.bfloat16 CUDA tensors, dk 64 or 128.
+    eps: one value per query head.  scale defaults to 1/sqrt(dk).
+    Returns tau [h] (float32) and, with ``return_moments``, the per-head
+    moments [h, 6] (float64: n, sum s, sum g, sum s g, sum g^2, g0).
+    """
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q, k must be 4-D: [B, h, Tq, dk], [B, hkv, Tk, dk]")
+    if q.device.type != "cuda" or k.device != q.device:
+        raise ValueError("q and k must be CUDA tensors on one device")
+    if not (q.is_contiguous() and k.is_contiguous()):
+        raise ValueError("q and k must be contiguous")
+    B, h, Tq, dk = q.shape
+    # v is not read: a view of k stands in for its shape
+    prob = make_problem(q, k, k, causal=causal, scale=scale)
+    dev = q.device
+    et = _per_head(eps, h, dev, "eps")
+    lib = native.load()
+    need = int(lib.cattn_tau_star_workspace_bytes(ctypes.byref(prob)))
+    if need == 0:
+        raise ValueError("unsupported problem for tau* (bf16, dk 64 or 128)")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    tau = torch.empty(h, dtype=torch.float32, device=dev)
+    mom = torch.empty((h, 6), dtype=torch.float64, device=dev) if return_moments else None
+    status = lib.cattn_tau_star(ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(et), _ptr(tau),
+                                _ptr(mom), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(),
+                                _stream_handle(dev))
+    native.check(status, "cattn_tau_star")
+    return (tau, mom) if return_moments else tau
+
+
 def check_status(stream=None) -> int:
     """Synchronise `stream` (default: current) and return the kernels' wait status."""
     handle = ctypes.c_void_p(stream.cuda_stream if stream is not None

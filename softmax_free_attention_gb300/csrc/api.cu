@@ -266,6 +266,79 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
   return map_cuda(launch_fwd_tc(variant, p->dk, p->dv, fp, tq, tk, tv, s));
 }
 
+// The tau* pass reads no V: its problem is checked as an s^tau problem whose
+// value width equals the key width.
+cattn_problem_t tau_problem(const cattn_problem_t *p) {
+  cattn_problem_t q = *p;
+  q.dv = q.dk;
+  return q;
+}
+
+size_t tau_ws_bytes(const cattn_problem_t *p) {
+  return 256 + align256((size_t)p->h * 6 * sizeof(double));
+}
+
+size_t cattn_tau_star_workspace_bytes(const cattn_problem_t *p) {
+  if (!p) return 0;
+  const cattn_problem_t tp = tau_problem(p);
+  if (check_problem(CATTN_STAU, &tp) != CATTN_OK || tp.dtype != CATTN_BF16) return 0;
+  return tau_ws_bytes(&tp);
+}
+
+int cattn_tau_star(const cattn_problem_t *p, const void *q, const void *k, const float *eps,
+                   float *tau_star, double *moments, void *workspace, size_t workspace_bytes,
+                   cattn_stream_t stream) {
+  if (!p) return CATTN_ERR_INVALID_ARG;
+  const cattn_problem_t tp = tau_problem(p);
+  int rc = check_problem(CATTN_STAU, &tp);
+  if (rc != CATTN_OK) return rc;
+  if (tp.dtype != CATTN_BF16) return CATTN_ERR_UNSUPPORTED;
+  if (tp.h == 0) return CATTN_OK;
+  if (!eps || !tau_star || !workspace) return CATTN_ERR_INVALID_ARG;
+  if (!is_empty(&tp) && (!q || !k)) return CATTN_ERR_INVALID_ARG;
+  if (!is_empty(&tp) && (!aligned16(q) || !aligned16(k))) return CATTN_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CATTN_ERR_UNSUPPORTED;
+  if (workspace_bytes < tau_ws_bytes(&tp)) return CATTN_ERR_SHAPE;
+  rc = check_device();
+  if (rc != CATTN_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  double *acc = reinterpret_cast<double *>(ws + 256);
+  // the ticket and the moments start at zero
+  if ((rc = map_cuda(cudaMemsetAsync(ws, 0, tau_ws_bytes(&tp), s))) != CATTN_OK) return rc;
+  if (!is_empty(&tp)) {
+    const TcSchedule sched = tc_schedule(tp.B, tp.h, tp.Tq, tp.Tk, tp.causal);
+    FwdParams fp;
+    memset(&fp, 0, sizeof(fp));
+    fp.q = q;
+    fp.k = k;
+    fp.eps = eps;
+    fp.B = tp.B;
+    fp.h = tp.h;
+    fp.hkv = tp.hkv;
+    fp.Tq = tp.Tq;
+    fp.Tk = tp.Tk;
+    fp.Tk_pad = tk_pad(&tp);
+    fp.causal = tp.causal ? 1 : 0;
+    fp.scale = tp.scale;
+    fp.n_qtiles = (tp.Tq + kTcQueryTile - 1) / kTcQueryTile;
+    fp.n_pairs = (fp.n_qtiles + 1) / 2;
+    fp.n_kv_tiles = (tp.Tk + kTcKeyTile - 1) / kTcKeyTile;
+    fp.n_splits = sched.n_splits;
+    fp.kv_per_split = sched.kv_per_split;
+    fp.head_group = sched.head_group;
+    fp.n_units = (int)sched.n_units;
+    fp.tile_counter = reinterpret_cast<unsigned int *>(ws);
+    fp.moments = acc;
+    CUtensorMap tq, tk;
+    if ((rc = encode_bf16_3d(&tq, q, tp.dk, tp.Tq, tp.B * tp.h, kTcQueryTile)) != CATTN_OK) return rc;
+    if ((rc = encode_bf16_3d(&tk, k, tp.dk, tp.Tk, tp.B * tp.hkv, kTcKeyTile)) != CATTN_OK) return rc;
+    // the pass reads no V; the K map stands in for the unused V map
+    if ((rc = map_cuda(launch_fwd_tc(kTau, tp.dk, tp.dk, fp, tq, tk, tk, s))) != CATTN_OK) return rc;
+  }
+  return map_cuda(launch_tau_finalize(acc, eps, tp.h, tau_star, moments, s));
+}
+
 int cattn_check_status(cattn_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return CATTN_ERR_CUDA;

@@ -328,7 +328,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // Yat and s^tau split each PV in two: half of it runs while the map warps
   // work on the second half of P (softmax, whose map is the shortest, keeps
   // one PV and its rescale after the map)
-  constexpr bool SPLIT_PV = VARIANT != kSoftmax;
+  constexpr bool SPLIT_PV = VARIANT == kYat || VARIANT == kStau;
+  // the tau* pass (kTau) reads no V and issues no PV: one ring slot per key tile
+  constexpr bool HAS_V = VARIANT != kTau;
+  constexpr uint32_t STEP = HAS_V ? 2u : 1u;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
@@ -442,7 +445,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int j = 0; j < t.nkv; ++j) {
           const int jt = t.kv_begin + j;  // key tile
           {  // K
-            const uint32_t pos = kv_pos + 2u * j, s = pos % L::NS;
+            const uint32_t pos = kv_pos + STEP * j, s = pos % L::NS;
             if (!(ok = thread_wait(kv_empty(s), ((pos / L::NS) & 1u) ^ 1u, abort,
                                    SITE_PRODUCER | 0x10)))
               break;
@@ -460,7 +463,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bulk_load(sb + L::OFF_NK + s * BN * 4,
                       p.nk + (size_t)t.bh_kv * p.Tk_pad + (size_t)jt * BN, BN * 4, nk_full(s));
           }
-          {  // V
+          if (HAS_V) {  // V
             const uint32_t pos = kv_pos + 2u * j + 1u, s = pos % L::NS;
             if (!(ok = thread_wait(kv_empty(s), ((pos / L::NS) & 1u) ^ 1u, abort,
                                    SITE_PRODUCER | 0x30)))
@@ -472,7 +475,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         if (!ok) break;
-        kv_pos += 2u * t.nkv;
+        kv_pos += STEP * t.nkv;
         nk_pos += t.nkv;
         u = (int)atomicAdd(p.tile_counter, 1u) + (int)gridDim.x;
       }
@@ -504,12 +507,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!(ok = thread_wait(bar_q_full, uc & 1u, abort, SITE_MMA | 0x10))) break;
         for (int j = 0; ok && j <= t.nkv; ++j) {
           const uint32_t vpos = kv_pos + 2u * j - 1u, vs = vpos % L::NS;
-          const uint32_t kpos = kv_pos + 2u * j, ks = kpos % L::NS;
-          if (j >= 1 && !(ok = thread_wait(kv_full(vs), (vpos / L::NS) & 1u, abort, SITE_MMA | 0x20)))
+          const uint32_t kpos = kv_pos + STEP * j, ks = kpos % L::NS;
+          if (HAS_V && j >= 1 &&
+              !(ok = thread_wait(kv_full(vs), (vpos / L::NS) & 1u, abort, SITE_MMA | 0x20)))
             break;
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
-            if (j >= 1 && j - 1 < t.n[x] && SPLIT_PV) {  // O_x += P_x(j-1) V(j-1), in two halves
+            if (!HAS_V) {  // tau*: S_x(j) may land once the map warps have read S_x(j-1)
+              if (j >= 1 && j - 1 < t.n[x]) {
+                if (!(ok = thread_wait(p_full(x), (pph >> x) & 1u, abort, SITE_MMA | 0x30))) break;
+                pph ^= 1u << x;
+              }
+            } else if (j >= 1 && j - 1 < t.n[x] && SPLIT_PV) {  // O_x += P_x(j-1) V(j-1), in two halves
               if (!(ok = thread_wait(p_half(x), (pph >> x) & 1u, abort, SITE_MMA | 0x34))) break;
               if (j == 1 &&
                   !(ok = thread_wait(o_empty(x), ((ou >> x) & 1u) ^ 1u, abort, SITE_MMA | 0x50)))
@@ -555,14 +564,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!ok) break;
           if (j == t.nkv - 1) mma_commit(bar_q_empty);  // the unit's last S MMAs
           if (j < t.nkv) mma_commit(kv_empty(ks));
-          if (j >= 1) mma_commit(kv_empty(vs));
+          if (HAS_V && j >= 1) mma_commit(kv_empty(vs));
           // every map warp delivered P for tile j-1, so all are done with its key norms
           if (VARIANT == kYat && j >= 1) mbar_arrive(nk_empty((nk_pos + j - 1) % NKS));
 #ifdef CATTN_TRACE
           ++ms;
 #endif
         }
-        kv_pos += 2u * t.nkv;
+        kv_pos += STEP * t.nkv;
         nk_pos += t.nkv;
         ou ^= (t.n[0] > 0 ? 1u : 0u) | (t.n[1] > 0 ? 2u : 0u);
       }
@@ -608,14 +617,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         nkv = t.nkv;
         const int row = t.q0 + x * BM + r;
         lim_base = (p.causal ? min(row + 1, p.Tk) : p.Tk) - t.kv_begin * BN;
+        // tau* counts scores of real rows only (the forward just drops the
+        // outputs of rows past Tq)
+        if (VARIANT == kTau && row >= p.Tq) lim_base = 0;
         if (VARIANT == kYat) {
           yb = p.b[t.head];
           yeps = p.eps[t.head];
         } else if (VARIANT == kStau) {
           tau = p.tau[t.head];
           seps = p.eps[t.head];
+        } else if (VARIANT == kTau) {
+          seps = p.eps[t.head];
         }
       }
+      // tau*: this thread's partial sums of 1, s, g, s g, g^2 over the unit
+      float st[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+      const float g0 = VARIANT == kTau ? logf(0.6931472f + seps) : 0.f;
       if (VARIANT == kYat) {
         // |q|^2 of this thread's row, in fp32 from the bf16 Q tile in shared
         // memory (rows past Tq were loaded as zeros).  The order of a row's
@@ -669,6 +686,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           return 2;
         };
 
+        if constexpr (VARIANT == kTau) {
+          // read S out, free the buffer for S(j+1), then take the statistics
+          uint32_t sr[2][32];
+          tmem_ld32(t_s, sr[0]);
+          tmem_ld32(t_s + 32, sr[1]);
+          tmem_wait_ld();
+          tmem_ld_fence(sr[0]);
+          tmem_ld_fence(sr[1]);
+          tc_fence_before();
+          mbar_arrive(p_full(x));
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            if (partial)
+              tau_chunk<true>(sr[c], half * 2 + c, p.scale, c2, seps, g0, limit, st);
+            else
+              tau_chunk<false>(sr[c], half * 2 + c, p.scale, c2, seps, g0, limit, st);
+          }
+          continue;
+        }
         bool rescale = false;
         float corr = 1.f;
         if (VARIANT == kYat) {
@@ -792,9 +828,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_arrive(p_full(x));
       }
 
+      if (VARIANT == kTau && ok && nk_tiles > 0) {
+        // tau*: the warp's sums, then one fp64 atomic per moment and warp
+#pragma unroll
+        for (int i = 0; i < 5; ++i) {
+          float v = st[i];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
+          st[i] = v;
+        }
+        if (lane == 0) {
+          const Unit t = decode_unit(p, unit_ring[uc & 1u]);
+          double *m = p.moments + (size_t)t.head * 6;
+#pragma unroll
+          for (int i = 0; i < 5; ++i) atomicAdd(m + i, (double)st[i]);
+        }
+      }
       // ---- finalise: combine the two halves of the row, then normalise and
       // store (or, with key splits, store the unnormalised partial)
-      if (ok && nk_tiles > 0) {
+      if (VARIANT != kTau && ok && nk_tiles > 0) {
         const float part = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
         const float ptop = fmaxf(top[0], top[1]);
         float *fb = xchg + (8 + (uint32_t)x * 4) * BM;  // [2 values][2 halves][BM]
@@ -930,6 +982,22 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Fw
   }
 }
 
+// tau* = (sum s g - sum s sum g / n) / (sum g^2 - (sum g)^2 / n), one thread
+// per head, in fp64 (the shift g0 cancels).
+__global__ void tau_finalize_kernel(const double *moments, const float *eps, int h, float *tau,
+                                    double *moments_out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= h) return;
+  const double *m = moments + (size_t)i * 6;
+  const double n = m[0], ss = m[1], sg = m[2], ssg = m[3], sgg = m[4];
+  const double cov = ssg - ss * sg / n, var = sgg - sg * sg / n;
+  tau[i] = (n >= 2.0 && var > 0.0) ? (float)(cov / var) : __int_as_float(0x7fc00000);
+  if (moments_out) {
+    for (int j = 0; j < 5; ++j) moments_out[(size_t)i * 6 + j] = m[j];
+    moments_out[(size_t)i * 6 + 5] = (double)logf(0.6931472f + eps[i]);
+  }
+}
+
 template <int VARIANT, int DK, int DV>
 cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                    const CUtensorMap &tv, cudaStream_t s) {
@@ -951,10 +1019,14 @@ cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap 
   const int grid = p.n_units < sm_count ? p.n_units : sm_count;  // one CTA per SM
   kern<<<grid, NUM_THREADS, L::ALLOC, s>>>(p, tq, tk, tv);
   e = cudaGetLastError();
-  if (e != cudaSuccess || p.n_splits == 1) return e;
-  const long long rows = (long long)p.B * p.h * p.Tq;
-  combine_kernel<VARIANT, DV><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p);
-  return cudaGetLastError();
+  if constexpr (VARIANT == kTau) {
+    return e;
+  } else {
+    if (e != cudaSuccess || p.n_splits == 1) return e;
+    const long long rows = (long long)p.B * p.h * p.Tq;
+    combine_kernel<VARIANT, DV><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p);
+    return cudaGetLastError();
+  }
 }
 
 }  // namespace tc
@@ -995,8 +1067,17 @@ cudaError_t launch_fwd_tc(int variant, int dk, int dv, const FwdParams &p, const
   CATTN_TC_CASE(kStau, 64, 64)
   CATTN_TC_CASE(kStau, 128, 128)
   CATTN_TC_CASE(kStau, 128, 64)
+  CATTN_TC_CASE(kTau, 64, 64)
+  CATTN_TC_CASE(kTau, 128, 128)
 #undef CATTN_TC_CASE
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_tau_finalize(const double *moments, const float *eps, int h, float *tau,
+                                double *moments_out, cudaStream_t s) {
+  if (h <= 0) return cudaSuccess;
+  tc::tau_finalize_kernel<<<(h + 127) / 128, 128, 0, s>>>(moments, eps, h, tau, moments_out);
+  return cudaGetLastError();
 }
 
 cudaError_t read_and_clear_status(unsigned int *value) {

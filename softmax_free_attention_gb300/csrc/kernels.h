@@ -8,7 +8,8 @@
 
 namespace cattn {
 
-enum Variant { kSoftmax = 0, kYat = 1, kStau = 2 };
+// kTau is not a map: the tau* statistics pass over the softmax scores.
+enum Variant { kSoftmax = 0, kYat = 1, kStau = 2, kTau = 3 };
 
 // Tile shape of the tensor-core forward: query rows per tile, keys per tile.
 constexpr int kTcQueryTile = 128;
@@ -38,6 +39,7 @@ struct FwdParams {
   unsigned int *tile_counter;  // next unit to hand out (zeroed before launch)
   float *part_o;     // [n_splits, B*h, Tq, dv] unnormalised partial outputs (n_splits > 1)
   float *part_stat;  // [n_splits, B*h, Tq, 4]: mass or l, running max (log2), top score
+  double *moments;   // kTau: [h][6] sums n, s, g, s g, g^2 (g = ln phi(s) - g0), zeroed
 };
 
 // Split count and grouping of the persistent tensor-core schedule; a pure
@@ -54,6 +56,12 @@ TcSchedule tc_schedule(int B, int h, int Tq, int Tk, int causal);
 cudaError_t launch_fwd_tc(int variant, int dk, int dv, const FwdParams &p, const CUtensorMap &tq,
                           const CUtensorMap &tk, const CUtensorMap &tv, cudaStream_t s);
 bool fwd_tc_supported(int dk, int dv);
+
+// tau* per head from the moments the kTau pass accumulated: writes tau[h]
+// and, if moments_out is not NULL, the moments with g0 = ln(ln 2 + eps) in
+// the sixth slot.
+cudaError_t launch_tau_finalize(const double *moments, const float *eps, int h, float *tau,
+                                double *moments_out, cudaStream_t s);
 
 // CUDA-core fp32 forward.
 cudaError_t launch_fwd_simt(int variant, int dk, int dv, const FwdParams &p, cudaStream_t s);

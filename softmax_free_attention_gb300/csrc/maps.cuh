@@ -144,5 +144,33 @@ __device__ __forceinline__ void stau_chunk(const uint32_t (&sr)[32], int c, floa
   }
 }
 
+// tau* statistics of one 32-key chunk ("s^tau: a focal-length knob for
+// attention", tau* = Cov(s, ln phi(s)) / Var(ln phi(s))): for every allowed
+// key, s = scale dot and g = ln phi(s) - g0 (the shift g0 = ln(ln 2 + eps),
+// the value at s = 0, keeps the second moments well conditioned); adds 1, s,
+// g, s g and g^2 to st.
+template <bool PARTIAL>
+__device__ __forceinline__ void tau_chunk(const uint32_t (&sr)[32], int c, float scale, float c2,
+                                          float eps, float g0, int limit, float (&st)[5]) {
+  constexpr float LN2 = 0.6931471805599453f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float d = __uint_as_float(sr[i]);
+    float s = d * scale;
+    float g = fmaf(log2_phi(s, fabsf(d) * c2, eps), LN2, -g0);
+    float w = 1.f;
+    if (PARTIAL && c * 32 + i >= limit) {
+      s = 0.f;
+      g = 0.f;
+      w = 0.f;
+    }
+    st[0] += w;
+    st[1] += s;
+    st[2] += g;
+    st[3] = fmaf(s, g, st[3]);
+    st[4] = fmaf(g, g, st[4]);
+  }
+}
+
 }  // namespace tc
 }  // namespace cattn

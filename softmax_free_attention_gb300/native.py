@@ -26,7 +26,8 @@ ERR_SCRATCH_LIMIT = 6
 
 # every symbol include/cattn.h declares
 EXPORTS = ("cattn_version", "cattn_error_string", "cattn_workspace_bytes", "cattn_validate",
-           "cattn_key_norms", "cattn_forward", "cattn_forward_noalloc", "cattn_check_status")
+           "cattn_key_norms", "cattn_forward", "cattn_forward_noalloc",
+           "cattn_tau_star_workspace_bytes", "cattn_tau_star", "cattn_check_status")
 
 
 class Problem(ctypes.Structure):
@@ -74,6 +75,10 @@ def load():
     lib.cattn_forward.restype = i
     lib.cattn_forward_noalloc.argtypes = [i, pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.cattn_forward_noalloc.restype = i
+    lib.cattn_tau_star_workspace_bytes.argtypes = [pp]
+    lib.cattn_tau_star_workspace_bytes.restype = sz
+    lib.cattn_tau_star.argtypes = [pp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.cattn_tau_star.restype = i
     lib.cattn_check_status.argtypes = [vp]
     lib.cattn_check_status.restype = i
     _lib = lib

@@ -236,3 +236,63 @@ def test_yat_fast_and_exact_map_paths(eps, qk, where):
     inp["yat_b"] = np.full(2, 0.5, dtype=np.float32)
     inp["yat_eps"] = np.full(2, eps, dtype=np.float32)
     pu.full_parity("yat", inp, causal=True, scale=w.scale, where=where)
+
+
+# ---------------------------------------------------------------- tau*
+
+TAU_SHAPES = [  # B, h, hkv, T_q, T_k, d, causal
+    (2, 4, 2, 300, 300, 128, True),    # several query tiles, ragged tail, GQA
+    (1, 2, 1, 130, 130, 64, True),     # one pair, dk 64
+    (1, 2, 2, 200, 2100, 64, False),   # non-causal with key splits
+    (3, 1, 1, 129, 129, 128, False),   # a query tile of one row
+]
+
+
+@pytest.mark.parametrize("shape", TAU_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_tau_star_matches_oracle(shape):
+    """tau* per head against the fp64 oracle on the same bf16 inputs.
+
+    Tolerance 2e-3 relative: the kernel's scores are fp32 sums of exact bf16
+    products (relative error ~1e-7), ln phi goes through the SFU's log2 and
+    exp2 (~1e-6), and each thread's sums over a unit (at most a few thousand
+    scores) are fp32 before they are added in fp64 (relative error below
+    ~3e-4 for these sizes); the ratio of two such centred sums stays within
+    a few 1e-4 unless the variance nearly cancels, which these inputs avoid.
+    """
+    import oracle
+    B, h, hkv, Tq, Tk, d, causal = shape
+    g = torch.Generator().manual_seed(11)
+    q = (torch.randn(B, h, Tq, d, generator=g) * 1.5).to(torch.bfloat16)
+    k = torch.randn(B, hkv, Tk, d, generator=g).to(torch.bfloat16)
+    eps = torch.tensor([1e-6, 0.5, 1e-3, 2.0][:h], dtype=torch.float32)
+    scale = 1.0 / math.sqrt(d)
+    tau, mom = attention.tau_star(q.cuda(), k.cuda(), eps.cuda(), causal=causal, scale=scale,
+                                  return_moments=True)
+    torch.cuda.synchronize()
+    assert attention.check_status() == 0
+    want, n = oracle.tau_star(q, k, eps, causal=causal, scale=scale)
+    got = tau.cpu().double().numpy()
+    mom = mom.cpu().numpy()
+    np.testing.assert_array_equal(mom[:, 0], n)  # every allowed pair counted once
+    np.testing.assert_allclose(mom[:, 5], np.log(np.log(2.0) + eps.double().numpy()), rtol=1e-6)
+    np.testing.assert_allclose(got, want, rtol=2e-3)
+
+
+def test_tau_star_cfg4_gqa():
+    """The GQA s^tau workload (B=4, 16 query heads on 8 KV heads, T=8192):
+    tau* of every head on the GPU; the oracle checks the same data cut to its
+    first 2048 rows and keys, one batch, heads 0 and 1 (sharing KV head 0),
+    since tau* pools each head's whole score set."""
+    import oracle
+    w = workloads.WORKLOADS["cfg4_gqa"]
+    inp = workloads.generate(w, device="cuda")
+    eps = torch.from_numpy(inp["stau_eps"])
+    tau = attention.tau_star(inp["q"], inp["k"], eps, causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    assert attention.check_status() == 0
+    assert torch.isfinite(tau).all()
+    q1 = inp["q"][:1, :2, :2048].contiguous()
+    k1 = inp["k"][:1, :1, :2048].contiguous()
+    got = attention.tau_star(q1, k1, eps[:2], causal=True, scale=w.scale).cpu().double().numpy()
+    want, _ = oracle.tau_star(q1.cpu(), k1.cpu(), eps[:2], causal=True, scale=w.scale)
+    np.testing.assert_allclose(got, want, rtol=2e-3)

@@ -125,6 +125,27 @@ def test_workspace_layout(lib):
     assert lib.cattn_workspace_bytes(native.SOFTMAX, ctypes.byref(pc)) == 256
 
 
+def test_tau_star_workspace_and_argument_checks(lib):
+    # 256-byte ticket, then the per-head moments [h][6] fp64 rounded to 256 B
+    p = prob(B=2, h=5, hkv=5, Tq=300, Tk=300, dk=128, dv=64)
+    assert lib.cattn_tau_star_workspace_bytes(ctypes.byref(p)) == 256 + 256
+    assert lib.cattn_tau_star_workspace_bytes(ctypes.byref(prob(h=40, hkv=40))) == 256 + 2048
+    # bf16 only, key widths the tensor-core path has
+    assert lib.cattn_tau_star_workspace_bytes(ctypes.byref(prob(dtype=native.F32))) == 0
+    assert lib.cattn_tau_star_workspace_bytes(ctypes.byref(prob(dk=32, dv=32))) == 0
+    need = lib.cattn_tau_star_workspace_bytes(ctypes.byref(p))
+    f = lib.cattn_tau_star
+    # argument errors come back before any CUDA call
+    assert f(None, FAKE, FAKE, FAKE, FAKE, None, FAKE, need, None) == native.ERR_INVALID_ARG
+    assert f(ctypes.byref(p), FAKE, FAKE, None, FAKE, None, FAKE, need, None) == native.ERR_INVALID_ARG
+    assert f(ctypes.byref(p), FAKE, FAKE, FAKE, None, None, FAKE, need, None) == native.ERR_INVALID_ARG
+    assert f(ctypes.byref(p), FAKE, FAKE, FAKE, FAKE, None, FAKE, need - 1, None) == native.ERR_SHAPE
+    assert f(ctypes.byref(prob(dtype=native.F32, dk=32, dv=32)), FAKE, FAKE, FAKE, FAKE, None,
+             FAKE, need, None) == native.ERR_UNSUPPORTED
+    assert f(ctypes.byref(prob(h=3, hkv=2)), FAKE, FAKE, FAKE, FAKE, None, FAKE, need,
+             None) == native.ERR_SHAPE
+
+
 def test_empty_problem_is_a_noop_on_the_host(lib):
     # B = 0: nothing to compute, accepted without pointers and without CUDA
     p = prob(B=0)
