@@ -16,6 +16,7 @@ the host cores on bounded samples of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -365,6 +366,26 @@ def main():
         per_variant[variant] = {"tflops": tf, "kernel_ms": ms, "frac_of_peak": tf / peak_burst}
     assert attention.check_status() == 0
     per_variant["yat_over_softmax"] = per_variant["yat"]["tflops"] / per_variant["softmax"]["tflops"]
+
+    # ---- tau* of the s^tau map from the same scores: one S = QK^T pass plus
+    # per-score ln phi statistics (SFU-bound), not part of the step above
+    tau_prob = attention.make_problem(q, k, k, causal=w.causal, scale=w.scale)
+    tau_ws = torch.empty(int(native.load().cattn_tau_star_workspace_bytes(ctypes.byref(tau_prob))),
+                         dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        attention.tau_star(q, k, se, causal=w.causal, scale=w.scale, workspace=tau_ws)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        attention.tau_star(q, k, se, causal=w.causal, scale=w.scale, workspace=tau_ws)
+    b.record()
+    torch.cuda.synchronize()
+    assert attention.check_status() == 0
+    tau_ms = a.elapsed_time(b) / args.steps
+    qk_flops = flops * w.dk / (w.dk + w.dv)
+    per_variant["tau_star"] = {"kernel_ms": tau_ms, "qk_tflops": qk_flops / (tau_ms * 1e-3) / 1e12,
+                               "scores_per_s": qk_flops / (2 * w.dk) / (tau_ms * 1e-3)}
 
     # ---- end to end through the public API with host buffers
     e2e = None
