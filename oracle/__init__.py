@@ -48,6 +48,7 @@ class _Problem(ctypes.Structure):
         ("rows", ctypes.c_void_p), ("nrows", ctypes.c_int64),
         ("out", ctypes.c_void_p), ("row_mass", ctypes.c_void_p), ("row_max", ctypes.c_void_p),
         ("weights", ctypes.c_void_p),
+        ("yat_m", ctypes.c_int),
     ]
 
 
@@ -102,7 +103,7 @@ def _per_head(x, h, name):
 
 
 def forward(variant, q, k, v, *, b=None, eps=None, tau=None, causal=False, scale=None,
-            rows=None, nthreads=None, return_weights=False):
+            rows=None, nthreads=None, return_weights=False, yat_m=1):
     """Attention forward in fp64.
 
     q: [B, h, Tq, dk]; k: [B, hkv, Tk, dk]; v: [B, hkv, Tk, dv] (numpy arrays or
@@ -114,9 +115,13 @@ def forward(variant, q, k, v, *, b=None, eps=None, tau=None, causal=False, scale
     and the outputs are returned in that order with a leading ``len(rows)``
     axis.  Without ``rows`` the outputs have the full [B, h, Tq(, dv)] shape.
 
+    yat_m: the Yat numerator exponent is 2 * yat_m (an integer >= 1).
+
     Returns (out, row_mass, row_max) and, with ``return_weights``, the weight
     matrix [.., Tk] as a fourth element.
     """
+    if int(yat_m) != yat_m or yat_m < 1:
+        raise ValueError("yat_m must be an integer >= 1")
     variant = VARIANTS.get(variant, variant)
     q = _as_f64(q, "q")
     k = _as_f64(k, "k")
@@ -150,7 +155,8 @@ def forward(variant, q, k, v, *, b=None, eps=None, tau=None, causal=False, scale
 
     prob = _Problem(variant, B, h, hkv, Tq, Tk, dk, dv, int(bool(causal)), float(scale),
                     ptr(q), ptr(k), ptr(v), ptr(b), ptr(eps), ptr(tau),
-                    ptr(rows_arr), nrows, ptr(out), ptr(row_mass), ptr(row_max), ptr(weights))
+                    ptr(rows_arr), nrows, ptr(out), ptr(row_mass), ptr(row_max), ptr(weights),
+                    int(yat_m))
     if nthreads is None:
         nthreads = os.cpu_count() or 1
     rc = _load().oracle_forward(ctypes.byref(prob), int(nthreads))
@@ -199,7 +205,7 @@ def tau_star(q, k, eps, *, causal=False, scale=None):
     n = np.zeros(h, dtype=np.float64)
     prob = _Problem(STAU, B, h, hkv, Tq, Tk, dk, 1, int(bool(causal)), float(scale),
                     q.ctypes.data, k.ctypes.data, None, None, eps.ctypes.data, None,
-                    None, 0, None, None, None, None)
+                    None, 0, None, None, None, None, 1)
     rc = _load().oracle_tau_star(ctypes.byref(prob), tau.ctypes.data, n.ctypes.data)
     if rc != 0:
         raise ValueError(f"oracle_tau_star failed with code {rc}")

@@ -47,6 +47,12 @@
  *     scores, row_max = max scaled score; s^tau row_mass = log sum phi^tau,
  *     row_max = max scaled score.
  *
+ * Yat numerator power ("The Kernel Between the Roles", section "The run":
+ * raising the numerator's power, (q.k)^{2m}, sharpens the kernel's peak):
+ * kappa = (q.k + b)^{2m} / (max(|q-k|^2, 0) + eps) with an integer m >= 1
+ * (m = 1 is the kernel above; b = 0 gives the page's ablation).  Reading:
+ * the bias stays inside the power, as in the m = 1 kernel.
+ *
  * tau* (same s^tau page, the closed-form paragraph: tau* = Cov(s, log phi(s))
  * / Var(log phi(s)), taken from the score distribution of one forward pass,
  * one value per attention head).  Readings: the scores are the softmax
@@ -88,6 +94,7 @@ typedef struct {
   double *row_mass; /* [nrows] */
   double *row_max;  /* [nrows] */
   double *weights;  /* optional [nrows, Tk]; NULL = not wanted */
+  int yat_m;         /* Yat numerator exponent 2m; 0 is read as m = 1 */
 } oracle_problem;
 
 /* softplus(s) = log(1 + exp(s)), in the textbook overflow-free form. */
@@ -144,14 +151,15 @@ static int oracle_row(const oracle_problem *p, int64_t flat, int64_t slot, doubl
     row_mass = m + log(l);
     row_max = m;
   } else if (p->variant == ORACLE_YAT) {
-    /* kappa = (q.k + b)^2 / (max(|q-k|^2, 0) + eps); w = kappa / (mass + 1e-9). */
+    /* kappa = (q.k + b)^{2m} / (max(|q-k|^2, 0) + eps); w = kappa / (mass + 1e-9). */
     const double bh_ = p->b[head], eh = p->eps[head];
+    const int m = p->yat_m > 1 ? p->yat_m : 1;
     double mass = 0.0, kmax = -INFINITY;
     for (int j = 0; j < nallowed; ++j) {
       const double *krow = kbase + (int64_t)j * p->dk;
       double num = dot(qrow, krow, p->dk) + bh_;
       double d2 = sqdist(qrow, krow, p->dk);
-      double kappa = (num * num) / (fmax(d2, 0.0) + eh);
+      double kappa = pow(num, 2.0 * m) / (fmax(d2, 0.0) + eh);
       w[j] = kappa;
       mass += kappa;
       if (kappa > kmax) kmax = kappa;

@@ -144,6 +144,42 @@ def test_yat_self_similarity_closed_form_and_symmetry():
     assert evals.min() >= -1e-10 * np.trace(kap)
 
 
+@pytest.mark.parametrize("m", [2, 3])
+def test_yat_numerator_power_exact(m):
+    # kappa_m = (q.k + b)^{2m} / (max(|q-k|^2, 0) + eps) ("The Kernel Between the
+    # Roles", section "The run"), checked on small integers in exact rationals:
+    # q = (1, 2); keys (3, 0), (1, 1), (-2, 1); b = 1/2, eps = 1/4
+    q = np.array([[[[1.0, 2.0]]]])
+    keys = [(3, 0), (1, 1), (-2, 1)]
+    k = np.array([[[list(map(float, kk)) for kk in keys]]])
+    v = np.array([[[[1.0], [10.0], [100.0]]]])
+    b, eps = Fraction(1, 2), Fraction(1, 4)
+    kap = []
+    for kx, ky in keys:
+        dotp = 1 * kx + 2 * ky
+        d2 = (1 - kx) ** 2 + (2 - ky) ** 2
+        kap.append((dotp + b) ** (2 * m) / (d2 + eps))
+    mass_x = sum(kap)
+    out, mass, mx = oracle.forward("yat", q, k, v, b=[float(b)], eps=[float(eps)], yat_m=m)
+    assert mass[0, 0, 0] == pytest.approx(float(mass_x), rel=1e-14)
+    assert mx[0, 0, 0] == pytest.approx(float(max(kap)), rel=1e-14)
+    want = sum(kk * vv for kk, vv in zip(kap, (1, 10, 100))) / mass_x
+    assert out[0, 0, 0, 0] == pytest.approx(float(want), rel=1e-9)
+    # m = 1 is the base kernel, and the diagonal is (|q|^2 + b)^{2m} / eps
+    base = oracle.forward("yat", q, k, v, b=[0.5], eps=[0.25])
+    np.testing.assert_array_equal(oracle.forward("yat", q, k, v, b=[0.5], eps=[0.25],
+                                                 yat_m=1)[1], base[1])
+    x = np.random.default_rng(8).standard_normal((5, 4))
+    _, mq, _, wq = oracle.forward("yat", x[None, None], x[None, None], np.zeros((1, 1, 5, 1)),
+                                  b=[0.5], eps=[0.25], yat_m=m, return_weights=True)
+    kq = wq[0, 0] * (mq[0, 0][:, None] + 1e-9)
+    np.testing.assert_allclose(np.diag(kq), (np.sum(x * x, axis=1) + 0.5) ** (2 * m) / 0.25,
+                               rtol=1e-12)
+    np.testing.assert_allclose(kq, kq.T, rtol=1e-12)
+    with pytest.raises(ValueError):
+        oracle.forward("yat", q, k, v, b=[0.5], eps=[0.25], yat_m=0)
+
+
 def test_yat_b0_orthogonal_scores_zero():
     # b = 0 and q orthogonal to k gives kappa = 0 whatever the distance
     q = np.array([[[[1.0, 0.0]]]])
