@@ -98,6 +98,8 @@ typedef struct {
   int causal; /* nonzero: key j is allowed for query row t only when j <= t; needs Tq == Tk */
   float scale; /* softmax and s^tau multiply q.k by this (> 0, e.g. 1/sqrt(dk)); Yat ignores it */
   int flags;  /* CATTN_FLAG_* */
+  int yat_m;  /* Yat only: numerator (q.k + b)^{2m}, m in {1, 2, 3}; 0 means 1 ("The Kernel
+                 Between the Roles", section "The run"); ignored by the other maps */
 } cattn_problem_t;
 
 /* Library version, 100*major + minor. */

@@ -26,7 +26,8 @@ def variant_id(variant) -> int:
         raise ValueError(f"unknown variant {variant!r}; use 'yat', 'softmax' or 'stau'") from None
 
 
-def make_problem(q, k, v, *, causal=False, scale=None, norms_ready=False) -> native.Problem:
+def make_problem(q, k, v, *, causal=False, scale=None, norms_ready=False,
+                 yat_m=1) -> native.Problem:
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be 4-D: [B, h, Tq, dk], [B, hkv, Tk, dk], [B, hkv, Tk, dv]")
     B, h, Tq, dk = q.shape
@@ -38,8 +39,11 @@ def make_problem(q, k, v, *, causal=False, scale=None, norms_ready=False) -> nat
         raise ValueError("q, k, v must share one dtype: torch.bfloat16 or torch.float32")
     if scale is None:
         scale = 1.0 / math.sqrt(dk)
+    if int(yat_m) != yat_m or not 1 <= yat_m <= 3:
+        raise ValueError("yat_m must be 1, 2 or 3")
     return native.Problem(B, h, hkv, Tq, Tk, dk, dv, _DTYPES[q.dtype], int(bool(causal)),
-                          float(scale), native.FLAG_NORMS_READY if norms_ready else 0)
+                          float(scale), native.FLAG_NORMS_READY if norms_ready else 0,
+                          int(yat_m))
 
 
 def workspace_bytes(variant, problem: native.Problem) -> int:
@@ -81,13 +85,14 @@ def key_norms(q, k, v, workspace, *, causal=False, scale=None):
 
 def forward(variant, q, k, v, *, b=None, eps=None, tau=None, causal=False, scale=None,
             out=None, row_mass=None, row_max=None, telemetry=True, workspace=None,
-            norms_ready=False):
+            norms_ready=False, yat_m=1):
     """Attention forward with a pluggable score-to-weight map.
 
     variant: 'yat' | 'softmax' | 'stau'.  q [B,h,Tq,dk], k [B,hkv,Tk,dk],
     v [B,hkv,Tk,dv], all torch.bfloat16 or all torch.float32, contiguous.
     b, eps (Yat) and eps, tau (s^tau): one value per query head (or a scalar).
     scale: softmax / s^tau score scale (default 1/sqrt(dk)); Yat ignores it.
+    yat_m: Yat numerator (q.k + b)^{2 yat_m}, yat_m in {1, 2, 3}.
 
     Returns (out [B,h,Tq,dv], row_mass [B,h,Tq] or None, row_max [B,h,Tq] or None).
     CUDA tensors: runs asynchronously on the current stream.  CPU tensors: copied
@@ -96,7 +101,7 @@ def forward(variant, q, k, v, *, b=None, eps=None, tau=None, causal=False, scale
     vid = variant_id(variant)
     if q.device.type == "cpu":
         return _forward_from_host(vid, q, k, v, b=b, eps=eps, tau=tau, causal=causal,
-                                  scale=scale, telemetry=telemetry)
+                                  scale=scale, telemetry=telemetry, yat_m=yat_m)
     if q.device.type != "cuda":
         raise ValueError("tensors must live on a CUDA device or on the host")
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -104,7 +109,8 @@ def forward(variant, q, k, v, *, b=None, eps=None, tau=None, causal=False, scale
             raise ValueError(f"{n} must be contiguous")
         if t.device != q.device:
             raise ValueError("q, k, v must be on one device")
-    prob = make_problem(q, k, v, causal=causal, scale=scale, norms_ready=norms_ready)
+    prob = make_problem(q, k, v, causal=causal, scale=scale, norms_ready=norms_ready,
+                        yat_m=yat_m)
     dev = q.device
     B, h, Tq, _ = q.shape
     dv = v.shape[-1]
@@ -130,13 +136,13 @@ def forward(variant, q, k, v, *, b=None, eps=None, tau=None, causal=False, scale
     return out, row_mass, row_max
 
 
-def _forward_from_host(vid, q, k, v, *, b, eps, tau, causal, scale, telemetry):
+def _forward_from_host(vid, q, k, v, *, b, eps, tau, causal, scale, telemetry, yat_m):
     dev = torch.device("cuda", torch.cuda.current_device())
     qd = q.to(dev, non_blocking=True)
     kd = k.to(dev, non_blocking=True)
     vd = v.to(dev, non_blocking=True)
     o, m, x = forward(vid, qd, kd, vd, b=b, eps=eps, tau=tau, causal=causal, scale=scale,
-                      telemetry=telemetry)
+                      telemetry=telemetry, yat_m=yat_m)
     res = (o.to("cpu"), None if m is None else m.to("cpu"), None if x is None else x.to("cpu"))
     return res
 

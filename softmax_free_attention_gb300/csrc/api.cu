@@ -78,6 +78,7 @@ int check_problem(int variant, const cattn_problem_t *p) {
   if (p->causal && p->Tq != p->Tk) return CATTN_ERR_SHAPE;
   if (variant != CATTN_YAT && !(p->scale > 0.f && p->scale < 3.0e38f)) return CATTN_ERR_INVALID_ARG;
   if (p->flags & ~CATTN_FLAG_NORMS_READY) return CATTN_ERR_INVALID_ARG;
+  if (p->yat_m < 0 || p->yat_m > 3) return CATTN_ERR_INVALID_ARG;
   const bool shape_ok = p->dtype == CATTN_BF16 ? fwd_tc_supported(p->dk, p->dv)
                                                : fwd_simt_supported(p->dk, p->dv);
   if (!shape_ok) return CATTN_ERR_UNSUPPORTED;
@@ -224,6 +225,7 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
   fp.b = b;
   fp.eps = eps;
   fp.tau = tau;
+  fp.yat_m = p->yat_m > 1 ? p->yat_m : 1;
   fp.B = p->B;
   fp.h = p->h;
   fp.hkv = p->hkv;

@@ -122,7 +122,10 @@ __global__ void __launch_bounds__(THREADS) fwd_kernel(const FwdParams p) {
       float w;  // this lane's key weight before normalisation
       if (VARIANT == kYat) {
         const float t = dot + b;
-        w = allowed ? (t * t) / (fmaxf(d2, 0.f) + eps) : 0.f;
+        float num = t * t;  // (dot + b)^{2m}
+        const float t2 = num;
+        for (int i = 1; i < p.yat_m; ++i) num *= t2;
+        w = allowed ? num / (fmaxf(d2, 0.f) + eps) : 0.f;
         l[rr] += warp_sum(w);
         top[rr] = fmaxf(top[rr], warp_max(allowed ? w : -INFINITY));
       } else {

@@ -320,7 +320,8 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams &p, int u) {
   return t;
 }
 
-template <int VARIANT, int DK, int DV>
+// YM: Yat numerator exponent 2 YM (1 for the other maps)
+template <int VARIANT, int DK, int DV, int YM = 1>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -726,14 +727,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tmem_ld_fence(sr);
               if (fast) {
                 if (kind == 2)
-                  yat_chunk<true, true>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+                  yat_chunk<true, true, YM>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
                 else
-                  yat_chunk<false, true>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+                  yat_chunk<false, true, YM>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
               } else {
                 if (kind == 2)
-                  yat_chunk<true, false>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+                  yat_chunk<true, false, YM>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
                 else
-                  yat_chunk<false, false>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+                  yat_chunk<false, false, YM>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
               }
             }
             tmem_st16(t_s + 16 * c, hk);
@@ -998,11 +999,11 @@ __global__ void tau_finalize_kernel(const double *moments, const float *eps, int
   }
 }
 
-template <int VARIANT, int DK, int DV>
+template <int VARIANT, int DK, int DV, int YM = 1>
 cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                    const CUtensorMap &tv, cudaStream_t s) {
   using L = Layout<DK, DV>;
-  auto kern = fwd_kernel<VARIANT, DK, DV>;
+  auto kern = fwd_kernel<VARIANT, DK, DV, YM>;
   static int configured_for = -1;
   static int sm_count = 0;
   int dev = 0;
@@ -1058,6 +1059,16 @@ cudaError_t launch_fwd_tc(int variant, int dk, int dv, const FwdParams &p, const
                           const CUtensorMap &tk, const CUtensorMap &tv, cudaStream_t s) {
 #define CATTN_TC_CASE(V, DK_, DV_) \
   if (variant == V && dk == DK_ && dv == DV_) return tc::launch<V, DK_, DV_>(p, tq, tk, tv, s);
+#define CATTN_TC_YAT_M(DK_, DV_, M_)                            \
+  if (variant == kYat && p.yat_m == M_ && dk == DK_ && dv == DV_) \
+    return tc::launch<kYat, DK_, DV_, M_>(p, tq, tk, tv, s);
+  CATTN_TC_YAT_M(64, 64, 2)
+  CATTN_TC_YAT_M(128, 128, 2)
+  CATTN_TC_YAT_M(128, 64, 2)
+  CATTN_TC_YAT_M(64, 64, 3)
+  CATTN_TC_YAT_M(128, 128, 3)
+  CATTN_TC_YAT_M(128, 64, 3)
+#undef CATTN_TC_YAT_M
   CATTN_TC_CASE(kSoftmax, 64, 64)
   CATTN_TC_CASE(kSoftmax, 128, 128)
   CATTN_TC_CASE(kSoftmax, 128, 64)

@@ -22,6 +22,7 @@ struct FwdParams {
   int out_align32;              // out is 32-byte aligned (whole-sector stores)
   float *row_mass, *row_max;    // [B, h, Tq] or NULL
   const float *b, *eps, *tau;   // [h]
+  int yat_m;                    // Yat numerator exponent 2 yat_m (1, 2 or 3)
   const float *nk;              // [B*hkv, Tk_pad]  squared k row norms (Yat, bf16), zero padded
   const unsigned int *nk_max;   // the largest of them, fp32 bits (Yat, bf16)
   int B, h, hkv, Tq, Tk, Tk_pad;

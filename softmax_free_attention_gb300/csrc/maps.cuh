@@ -31,10 +31,14 @@ __device__ __forceinline__ float2 f2(uint32_t a, uint32_t b) {
 // of |q|^2 + |k|^2 - 2 q.k, which is far below eps when
 // (|q|^2 + max |k|^2) 2^-16 <= eps, and then every den0 den1 is a normal fp32
 // number if also eps >= 2^-60 and |q|^2 + max |k|^2 <= 2^61.
-template <bool FAST>
+// M: the numerator is (dot + b)^{2M} ("The Kernel Between the Roles", section
+// "The run": raising the numerator's power sharpens the kernel's peak).
+template <bool FAST, int M = 1>
 __device__ __forceinline__ float2 yat_pair(float2 d, float2 nk, float2 b2, float2 qe2, float yeps) {
   const float2 t = __fadd2_rn(d, b2);
-  const float2 num = __fmul2_rn(t, t);
+  float2 num = __fmul2_rn(t, t);
+  if constexpr (M == 2) num = __fmul2_rn(num, num);
+  if constexpr (M == 3) num = __fmul2_rn(__fmul2_rn(num, num), num);
   const float2 den = __ffma2_rn(make_float2(-2.f, -2.f), d, __fadd2_rn(qe2, nk));
   if (FAST) {
     const float r = rcp_approx(den.x * den.y);
@@ -58,7 +62,7 @@ __device__ __forceinline__ uint32_t yat_fold(float2 k, int col, int limit, float
 
 // Yat map over one 32-key chunk (columns 32c .. 32c+31 of the tile) of one row.  sr: raw
 // dots; nk4: squared key norms of the tile (groups of four).
-template <bool PARTIAL, bool FAST>
+template <bool PARTIAL, bool FAST, int M = 1>
 __device__ __forceinline__ void yat_chunk(const uint32_t (&sr)[32], int c, const float4 *nk4,
                                           float yb, float qe, float yeps, int limit,
                                           float2 (&mass)[2], float (&top)[2],
@@ -70,7 +74,7 @@ __device__ __forceinline__ void yat_chunk(const uint32_t (&sr)[32], int c, const
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int ii = i + 2 * h;
-      const float2 k = yat_pair<FAST>(f2(sr[ii], sr[ii + 1]),
+      const float2 k = yat_pair<FAST, M>(f2(sr[ii], sr[ii + 1]),
                                       h ? make_float2(n4.z, n4.w) : make_float2(n4.x, n4.y), b2, qe2,
                                       yeps);
       pk[ii >> 1] = yat_fold<PARTIAL>(k, c * 32 + ii, limit, mass[h], top[h]);

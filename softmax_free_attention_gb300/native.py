@@ -35,7 +35,7 @@ class Problem(ctypes.Structure):
         ("B", ctypes.c_int), ("h", ctypes.c_int), ("hkv", ctypes.c_int),
         ("Tq", ctypes.c_int), ("Tk", ctypes.c_int), ("dk", ctypes.c_int), ("dv", ctypes.c_int),
         ("dtype", ctypes.c_int), ("causal", ctypes.c_int), ("scale", ctypes.c_float),
-        ("flags", ctypes.c_int),
+        ("flags", ctypes.c_int), ("yat_m", ctypes.c_int),
     ]
 
 

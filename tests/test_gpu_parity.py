@@ -296,3 +296,37 @@ def test_tau_star_cfg4_gqa():
     got = attention.tau_star(q1, k1, eps[:2], causal=True, scale=w.scale).cpu().double().numpy()
     want, _ = oracle.tau_star(q1.cpu(), k1.cpu(), eps[:2], causal=True, scale=w.scale)
     np.testing.assert_allclose(got, want, rtol=2e-3)
+
+
+# ---------------------------------------------------------------- Yat numerator power
+
+YAT_M_SHAPES = [  # B, h, hkv, Tq, Tk, dk, dv, causal, dtype
+    (2, 4, 2, 300, 300, 128, 128, True, "bf16"),
+    (1, 2, 1, 130, 130, 64, 64, True, "bf16"),
+    (1, 2, 2, 200, 2100, 128, 64, False, "bf16"),   # key splits
+    (1, 2, 1, 77, 77, 64, 64, True, "f32"),
+]
+
+
+@pytest.mark.parametrize("m", [2, 3])
+@pytest.mark.parametrize("shape", YAT_M_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_yat_numerator_power(m, shape):
+    """kappa = (q.k + b)^{2m} / (max(|q-k|^2, 0) + eps) against the oracle, with
+    the same tolerances as the m = 1 map (the power only sharpens the rows)."""
+    B, h, hkv, Tq, Tk, dk, dv, causal, dtype = shape
+    w = _wl("yat_m", B, h, hkv, Tq, Tk, dk, dv, dtype=dtype, causal=causal, seed=Tq + 31 * m)
+    inp = workloads.generate(w)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    res = attention.forward("yat", q, k, v, b=inp["yat_b"], eps=inp["yat_eps"], causal=causal,
+                            yat_m=m)
+    torch.cuda.synchronize()
+    assert attention.check_status() == 0
+    ora = oracle_forward_m(inp, causal, m)
+    pu.compare("yat", tuple(pu.to_np(t) for t in res), ora, float(inp["v"].abs().max()),
+               inp["q"].dtype, where=f"yat m={m} {shape}")
+
+
+def oracle_forward_m(inp, causal, m):
+    import oracle
+    return oracle.forward("yat", inp["q"], inp["k"], inp["v"], b=inp["yat_b"], eps=inp["yat_eps"],
+                          causal=causal, yat_m=m)

@@ -125,6 +125,14 @@ def test_workspace_layout(lib):
     assert lib.cattn_workspace_bytes(native.SOFTMAX, ctypes.byref(pc)) == 256
 
 
+def test_yat_power_range(lib):
+    for m, code in ((0, native.OK), (1, native.OK), (3, native.OK), (4, native.ERR_INVALID_ARG),
+                    (-1, native.ERR_INVALID_ARG)):
+        p = prob(yat_m=m)
+        need = lib.cattn_workspace_bytes(native.YAT, ctypes.byref(p))
+        assert validate(lib, native.YAT, p, ws=FAKE, ws_bytes=need) == code
+
+
 def test_tau_star_workspace_and_argument_checks(lib):
     # 256-byte ticket, then the per-head moments [h][6] fp64 rounded to 256 B
     p = prob(B=2, h=5, hkv=5, Tq=300, Tk=300, dk=128, dv=64)
