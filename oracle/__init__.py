@@ -210,3 +210,39 @@ def tau_star(q, k, eps, *, causal=False, scale=None):
     if rc != 0:
         raise ValueError(f"oracle_tau_star failed with code {rc}")
     return tau, n
+
+
+def row_stats(variant, q, k, v, *, b=None, eps=None, tau=None, causal=False, scale=None,
+              yat_m=1, rows=None):
+    """Per-row statistics of the attention map, from the oracle's own weights:
+
+    * normalised entropy  -sum_j w_j ln w_j / ln n  over the n allowed keys
+      (0 for a row on one key, 1 for a row spread evenly; 0 when n = 1) --
+      "The Kernel Between the Roles", section "The run";
+    * the fraction of allowed keys whose weight is below 1e-6 (the s^tau page's
+      attention sparsity);
+    * the top-10 mass: the sum of the row's ten largest weights (the s^tau
+      page's top-10 concentration).
+
+    Returns three arrays shaped like row_mass ([B, h, Tq], or [len(rows)]).
+    """
+    out, _, _, w = forward(variant, q, k, v, b=b, eps=eps, tau=tau, causal=causal, scale=scale,
+                           rows=rows, return_weights=True, yat_m=yat_m)
+    B, h, Tq, _ = np.shape(q)
+    Tk = np.shape(k)[2]
+    w = w.reshape(-1, Tk)
+    flat = np.arange(B * h * Tq) if rows is None else np.asarray(rows, dtype=np.int64).reshape(-1)
+    t = flat % Tq
+    n = np.minimum(t + 1, Tk) if causal else np.full(flat.shape, Tk)
+    ent = np.zeros(len(flat))
+    small = np.zeros(len(flat))
+    top = np.zeros(len(flat))
+    for r in range(len(flat)):
+        wr = w[r, :n[r]]
+        pos = wr[wr > 0]
+        hsum = -np.sum(pos * np.log(pos))
+        ent[r] = hsum / np.log(n[r]) if n[r] > 1 else 0.0
+        small[r] = np.count_nonzero(wr < 1e-6) / n[r]
+        top[r] = np.sum(np.sort(wr)[::-1][:10])
+    shape = (B, h, Tq) if rows is None else (len(flat),)
+    return ent.reshape(shape), small.reshape(shape), top.reshape(shape)

@@ -414,3 +414,58 @@ def test_tau_star_heads_gather_allowed_scores():
                   if not (causal and j > t)]
             assert n[i] == len(sc) == (B * T * (T + 1) // 2 if causal else B * T * T)
             assert tau[i] == pytest.approx(oracle.tau_star_scores(sc, eps[i]), rel=1e-12)
+
+
+# --------------------------------------------------------------------------
+# row statistics of the map (normalised entropy: "The Kernel Between the
+# Roles", section "The run"; sparsity below 1e-6 and top-10 concentration:
+# the s^tau page's fine-tuning comparison)
+# --------------------------------------------------------------------------
+
+def test_row_stats_uniform_onehot_and_two_keys():
+    # equal scores give equal weights: entropy 1, top-10 mass 10/n, nothing small
+    n = 16
+    q = np.zeros((1, 1, 1, 4))
+    k = np.zeros((1, 1, n, 4))
+    v = np.zeros((1, 1, n, 1))
+    ent, small, top = oracle.row_stats("softmax", q, k, v, scale=1.0)
+    assert ent[0, 0, 0] == pytest.approx(1.0, rel=1e-12)
+    assert small[0, 0, 0] == 0.0
+    assert top[0, 0, 0] == pytest.approx(10 / n, rel=1e-12)
+    # one key 60 logits ahead: one weight ~1, the rest e^-60 < 1e-6
+    k2 = k.copy()
+    k2[0, 0, 3, 0] = 60.0
+    q2 = np.zeros((1, 1, 1, 4))
+    q2[..., 0] = 1.0
+    ent, small, top = oracle.row_stats("softmax", q2, k2, v, scale=1.0)
+    assert ent[0, 0, 0] == pytest.approx(0.0, abs=1e-20)
+    assert small[0, 0, 0] == pytest.approx((n - 1) / n, rel=1e-15)
+    assert top[0, 0, 0] == pytest.approx(1.0, rel=1e-12)
+    # two keys with weights p, 1-p: entropy -(p ln p + (1-p) ln(1-p)) / ln 2
+    k3 = np.zeros((1, 1, 2, 4))
+    k3[0, 0, 0, 0] = 1.0
+    ent, small, top = oracle.row_stats("softmax", q2, k3, np.zeros((1, 1, 2, 1)), scale=1.0)
+    p = math.e / (math.e + 1.0)
+    assert ent[0, 0, 0] == pytest.approx(-(p * math.log(p) + (1 - p) * math.log(1 - p))
+                                         / math.log(2), rel=1e-12)
+    assert top[0, 0, 0] == pytest.approx(1.0, rel=1e-15)
+
+
+def test_row_stats_causal_counts_allowed_keys_only():
+    # causal row t has t + 1 keys; row 0 (one key) has entropy 0 and top-10 mass 1
+    rng = np.random.default_rng(9)
+    q = rng.standard_normal((1, 2, 12, 8))
+    k = rng.standard_normal((1, 2, 12, 8))
+    v = rng.standard_normal((1, 2, 12, 3))
+    ent, small, top = oracle.row_stats("yat", q, k, v, b=[0.5, 1.0], eps=[0.3, 1e-3], causal=True)
+    _, mass, _, w = oracle.forward("yat", q, k, v, b=[0.5, 1.0], eps=[0.3, 1e-3], causal=True,
+                                   return_weights=True)
+    wsum = mass / (mass + 1e-9)  # a Yat row's weights sum to M / (M + 1e-9)
+    assert (ent[:, :, 0] == 0.0).all()
+    # rows with at most ten keys put all their weight in the top ten
+    np.testing.assert_allclose(top[:, :, :10], wsum[:, :, :10], rtol=1e-12)
+    assert (ent >= 0).all() and (ent <= 1 + 1e-12).all()
+    # a brute-force recount of one row from the weights
+    wr = w[0, 1, 11]
+    assert small[0, 1, 11] == np.count_nonzero(wr < 1e-6) / 12
+    assert top[0, 1, 11] == pytest.approx(sum(sorted(wr, reverse=True)[:10]), rel=1e-12)
