@@ -197,6 +197,28 @@ int cattn_tau_star(const cattn_problem_t *p, const void *q, const void *k, const
                    float *tau_star, double *moments, void *workspace, size_t workspace_bytes,
                    cattn_stream_t stream);
 
+/* Per-row statistics of the attention map, by a second pass over the scores
+ * that takes the row normaliser from the forward: for every (b, i, t) the
+ * normalised entropy -sum_j w_j ln w_j / ln n over the n allowed keys (0 when
+ * n = 1; "The Kernel Between the Roles", section "The run"), the fraction of
+ * allowed keys with w_j < 1e-6, and the sum of the ten largest w_j (the
+ * sparsity and top-10 concentration of "s^tau: a focal-length knob for
+ * attention").  The weights are the forward's: Yat kappa / (M + 1e-9),
+ * softmax exp(s - lse), s^tau phi^tau / sum phi^tau.
+ *
+ * Arguments as cattn_forward, minus v and out: row_mass is the row_mass
+ * output of cattn_forward for the same problem and inputs (device fp32
+ * [B, h, Tq]); entropy, frac_small, top10 are device fp32 [B, h, Tq]
+ * outputs, any of which may be NULL.  bf16 only, dk in {64, 128} (p->dv is
+ * not used), Yat with yat_m <= 1.  workspace: cattn_row_stats_workspace_bytes
+ * bytes (the Yat key norms are recomputed into it), 256-byte aligned.
+ * Asynchronous on `stream`. */
+size_t cattn_row_stats_workspace_bytes(int variant, const cattn_problem_t *p);
+int cattn_row_stats(int variant, const cattn_problem_t *p, const void *q, const void *k,
+                    const float *b, const float *eps, const float *tau, const float *row_mass,
+                    float *entropy, float *frac_small, float *top10, void *workspace,
+                    size_t workspace_bytes, cattn_stream_t stream);
+
 /* Synchronises `stream`, then reports (and clears) the device-side status
  * word the kernels set when a bounded wait gives up: CATTN_ERR_TIMEOUT if
  * any kernel since the last check did so, CATTN_ERR_CUDA if the stream

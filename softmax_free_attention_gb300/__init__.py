@@ -4,6 +4,6 @@ The compute path is the C-ABI library libcattn.so (hand-written sm_103a CUDA,
 see include/cattn.h); this package holds its build script, the ctypes binding
 and the seeded workload generators.
 """
-from .attention import (check_status, forward, key_norms, make_problem, tau_star,  # noqa: F401
-                        workspace_bytes)
+from .attention import (check_status, forward, key_norms, make_problem, row_stats,  # noqa: F401
+                        tau_star, workspace_bytes)
 from .native import CattnError  # noqa: F401

@@ -185,6 +185,36 @@ def tau_star(q, k, eps, *, causal=False, scale=None, return_moments=False, works
     return (tau, mom) if return_moments else tau
 
 
+def row_stats(variant, q, k, row_mass, *, b=None, eps=None, tau=None, causal=False, scale=None):
+    """Per-row statistics of the attention map (a second pass over the scores):
+    normalised entropy, fraction of allowed keys with weight below 1e-6, and
+    the sum of the ten largest weights; each [B, h, Tq] float32.
+
+    row_mass: the ``row_mass`` the forward returned for the same inputs and map.
+    bf16 CUDA tensors, dk 64 or 128.
+    """
+    vid = variant_id(variant)
+    if q.dim() != 4 or k.dim() != 4 or q.device.type != "cuda":
+        raise ValueError("q, k must be 4-D CUDA tensors")
+    prob = make_problem(q, k, k, causal=causal, scale=scale)
+    dev = q.device
+    B, h, Tq, _ = q.shape
+    bt = _per_head(b, h, dev, "b") if vid == native.YAT else None
+    et = _per_head(eps, h, dev, "eps") if vid in (native.YAT, native.STAU) else None
+    tt = _per_head(tau, h, dev, "tau") if vid == native.STAU else None
+    lib = native.load()
+    need = int(lib.cattn_row_stats_workspace_bytes(vid, ctypes.byref(prob)))
+    if need == 0:
+        raise ValueError("unsupported problem for row statistics (bf16, dk 64 or 128)")
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    ent, small, top = (torch.empty((B, h, Tq), dtype=torch.float32, device=dev) for _ in range(3))
+    status = lib.cattn_row_stats(vid, ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(bt), _ptr(et),
+                                 _ptr(tt), _ptr(row_mass.contiguous()), _ptr(ent), _ptr(small),
+                                 _ptr(top), _ptr(ws), need, _stream_handle(dev))
+    native.check(status, "cattn_row_stats")
+    return ent, small, top
+
+
 def check_status(stream=None) -> int:
     """Synchronise `stream` (default: current) and return the kernels' wait status."""
     handle = ctypes.c_void_p(stream.cuda_stream if stream is not None

@@ -341,6 +341,86 @@ int cattn_tau_star(const cattn_problem_t *p, const void *q, const void *k, const
   return map_cuda(launch_tau_finalize(acc, eps, tp.h, tau_star, moments, s));
 }
 
+// The row statistics pass has no key splits (its per-row results need every
+// key of the row in one unit): the workspace is the ticket plus, for Yat, the
+// key norms.
+size_t stats_ws_bytes(int variant, const cattn_problem_t *p) {
+  return 256 + (variant == CATTN_YAT ? ws_nk_bytes(p) : 0);
+}
+
+size_t cattn_row_stats_workspace_bytes(int variant, const cattn_problem_t *p) {
+  if (!p) return 0;
+  const cattn_problem_t tp = tau_problem(p);
+  if (check_problem(variant, &tp) != CATTN_OK || tp.dtype != CATTN_BF16 || tp.yat_m > 1) return 0;
+  return stats_ws_bytes(variant, &tp);
+}
+
+int cattn_row_stats(int variant, const cattn_problem_t *p, const void *q, const void *k,
+                    const float *b, const float *eps, const float *tau, const float *row_mass,
+                    float *entropy, float *frac_small, float *top10, void *workspace,
+                    size_t workspace_bytes, cattn_stream_t stream) {
+  if (!p) return CATTN_ERR_INVALID_ARG;
+  const cattn_problem_t tp = tau_problem(p);
+  int rc = check_problem(variant, &tp);
+  if (rc != CATTN_OK) return rc;
+  if (tp.dtype != CATTN_BF16 || tp.yat_m > 1) return CATTN_ERR_UNSUPPORTED;
+  if (is_empty(&tp)) return CATTN_OK;
+  if (!q || !k || !row_mass || !workspace) return CATTN_ERR_INVALID_ARG;
+  if (variant == CATTN_YAT && (!b || !eps)) return CATTN_ERR_INVALID_ARG;
+  if (variant == CATTN_STAU && (!eps || !tau)) return CATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return CATTN_ERR_UNSUPPORTED;
+  if (workspace_bytes < stats_ws_bytes(variant, &tp)) return CATTN_ERR_SHAPE;
+  rc = check_device();
+  if (rc != CATTN_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char *ws = static_cast<char *>(workspace);
+  FwdParams fp;
+  memset(&fp, 0, sizeof(fp));
+  fp.q = q;
+  fp.k = k;
+  fp.b = b;
+  fp.eps = eps;
+  fp.tau = tau;
+  fp.yat_m = 1;
+  fp.B = tp.B;
+  fp.h = tp.h;
+  fp.hkv = tp.hkv;
+  fp.Tq = tp.Tq;
+  fp.Tk = tp.Tk;
+  fp.Tk_pad = tk_pad(&tp);
+  fp.causal = tp.causal ? 1 : 0;
+  fp.scale = tp.scale;
+  fp.n_qtiles = (tp.Tq + kTcQueryTile - 1) / kTcQueryTile;
+  fp.n_pairs = (fp.n_qtiles + 1) / 2;
+  fp.n_kv_tiles = (tp.Tk + kTcKeyTile - 1) / kTcKeyTile;
+  fp.n_splits = 1;
+  fp.kv_per_split = fp.n_kv_tiles;
+  fp.head_group = 16;
+  fp.n_units = tp.B * tp.h * fp.n_pairs;
+  fp.tile_counter = reinterpret_cast<unsigned int *>(ws);
+  fp.norm_in = row_mass;
+  fp.st_entropy = entropy;
+  fp.st_small = frac_small;
+  fp.st_top10 = top10;
+  if (variant == CATTN_YAT) {
+    fp.nk = reinterpret_cast<const float *>(ws + 256);
+    fp.nk_max = reinterpret_cast<const unsigned int *>(ws) + 1;
+    // the key norms and their maximum into this workspace
+    unsigned int *nk_max = reinterpret_cast<unsigned int *>(ws) + 1;
+    if ((rc = map_cuda(cudaMemsetAsync(nk_max, 0, sizeof(unsigned int), s))) != CATTN_OK) return rc;
+    if ((rc = map_cuda(launch_row_sqnorm_bf16(k, reinterpret_cast<float *>(ws + 256), tp.B * tp.hkv,
+                                              tp.Tk, tk_pad(&tp), tp.dk, nk_max, s))) != CATTN_OK)
+      return rc;
+  }
+  CUtensorMap tq, tk;
+  if ((rc = encode_bf16_3d(&tq, q, tp.dk, tp.Tq, tp.B * tp.h, kTcQueryTile)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&tk, k, tp.dk, tp.Tk, tp.B * tp.hkv, kTcKeyTile)) != CATTN_OK) return rc;
+  if ((rc = map_cuda(cudaMemsetAsync(fp.tile_counter, 0, sizeof(unsigned int), s))) != CATTN_OK)
+    return rc;
+  return map_cuda(launch_row_stats_tc(variant, tp.dk, fp, tq, tk, s));
+}
+
 int cattn_check_status(cattn_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return CATTN_ERR_CUDA;

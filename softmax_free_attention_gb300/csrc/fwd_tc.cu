@@ -126,7 +126,8 @@ struct Layout {
   // row-max exchange of the two column halves: per tile [2 uses][2 tiles][2 halves][BM],
   // final [2 tiles][2 values][2 halves][BM]
   static constexpr int OFF_XCHG = OFF_NK + NKS * BN * 4;
-  static constexpr int XCHG_FLOATS = 16 * BM;
+  // (the row statistics pass uses [13 values][2 tiles][BM] of it)
+  static constexpr int XCHG_FLOATS = 26 * BM;
   static constexpr int OFF_BAR = OFF_XCHG + XCHG_FLOATS * 4;
   // q_full, q_empty, kv_full[NS], kv_empty[NS], nk_full[NKS], nk_empty[NKS],
   // s_full[2], p_full[2], o_full[2], o_empty[2], unit_full[2], unit_empty[2], drain,
@@ -320,8 +321,9 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams &p, int u) {
   return t;
 }
 
-// YM: Yat numerator exponent 2 YM (1 for the other maps)
-template <int VARIANT, int DK, int DV, int YM = 1>
+// YM: Yat numerator exponent 2 YM (1 for the other maps).  STATS: the row
+// statistics pass (no V, no PV, no O; the weights' statistics per row).
+template <int VARIANT, int DK, int DV, int YM = 1, bool STATS = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -330,8 +332,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // work on the second half of P (softmax, whose map is the shortest, keeps
   // one PV and its rescale after the map)
   constexpr bool SPLIT_PV = VARIANT == kYat || VARIANT == kStau;
-  // the tau* pass (kTau) reads no V and issues no PV: one ring slot per key tile
-  constexpr bool HAS_V = VARIANT != kTau;
+  // the tau* pass (kTau) and the row statistics pass read no V and issue no
+  // PV: one ring slot per key tile
+  constexpr bool HAS_V = VARIANT != kTau && !STATS;
   constexpr uint32_t STEP = HAS_V ? 2u : 1u;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_u32(smem_raw);
@@ -633,6 +636,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       // tau*: this thread's partial sums of 1, s, g, s g, g^2 over the unit
       float st[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+      // row statistics: this thread's share of the row, and the row's
+      // normaliser from the forward (Yat: 1 / (M + 1e-9) and ln(M + 1e-9);
+      // softmax / s^tau: the log-sum-exp in log2 units)
+      RowStats rs;
+      float nz_scale = 0.f, nz_log = 0.f;
+      if constexpr (STATS) {
+        rs.n = rs.hsum = rs.small = 0.f;
+#pragma unroll
+        for (int i = 0; i < 10; ++i) rs.top[i] = 0.f;
+        const Unit t = decode_unit(p, u);
+        const int row = t.q0 + x * BM + r;
+        const float z = row < p.Tq ? p.norm_in[(size_t)t.bh * p.Tq + row] : 0.f;
+        if (VARIANT == kYat) {
+          nz_scale = 1.f / (z + 1e-9f);
+          nz_log = logf(z + 1e-9f);
+        } else {
+          nz_log = z * LOG2E;
+        }
+        if (row >= p.Tq) lim_base = 0;  // rows past Tq have no keys
+      }
       const float g0 = VARIANT == kTau ? logf(0.6931472f + seps) : 0.f;
       if (VARIANT == kYat) {
         // |q|^2 of this thread's row, in fp32 from the bf16 Q tile in shared
@@ -704,6 +727,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             else
               tau_chunk<false>(sr[c], half * 2 + c, p.scale, c2, seps, g0, limit, st);
           }
+          continue;
+        }
+        if constexpr (STATS) {
+          // the row statistics: the map's weights w of the allowed keys, one
+          // 32-key chunk at a time
+          const float4 *nk4 = nullptr;
+          if (VARIANT == kYat) {
+            const uint32_t npos = nk_pos + j, ns = npos % NKS;
+            if (!(ok = warp_wait(nk_full(ns), (npos / NKS) & 1u, abort, SITE_EPI | 0x20))) break;
+            nk4 = reinterpret_cast<const float4 *>(nk_ring + ns * BN);
+          }
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int cc = half * 2 + c;
+            uint32_t sr1[32];
+            tmem_ld32(t_s + 32 * c, sr1);
+            tmem_wait_ld();
+            tmem_ld_fence(sr1);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const int col = cc * 32 + i;
+              float w0, w1, l0, l1;
+              if (VARIANT == kYat) {
+                const float4 n4 = nk4[(cc * 32 + i) >> 2];
+                const float2 kk = fast ? yat_pair<true, YM>(f2(sr1[i], sr1[i + 1]),
+                                                            (i & 2) ? make_float2(n4.z, n4.w)
+                                                                    : make_float2(n4.x, n4.y),
+                                                            make_float2(yb, yb), make_float2(qe, qe),
+                                                            yeps)
+                                       : yat_pair<false, YM>(f2(sr1[i], sr1[i + 1]),
+                                                             (i & 2) ? make_float2(n4.z, n4.w)
+                                                                     : make_float2(n4.x, n4.y),
+                                                             make_float2(yb, yb), make_float2(qe, qe),
+                                                             yeps);
+                w0 = kk.x * nz_scale;
+                w1 = kk.y * nz_scale;
+                l0 = lg2_approx(kk.x) * LN2 - nz_log;
+                l1 = lg2_approx(kk.y) * LN2 - nz_log;
+              } else {
+                const float d0 = __uint_as_float(sr1[i]), d1 = __uint_as_float(sr1[i + 1]);
+                float x0, x1;  // log2 of the weights
+                if (VARIANT == kSoftmax) {
+                  x0 = fmaf(d0, c2, -nz_log);
+                  x1 = fmaf(d1, c2, -nz_log);
+                } else {
+                  x0 = fmaf(tau, log2_phi(d0 * p.scale, fabsf(d0) * c2, seps), -nz_log);
+                  x1 = fmaf(tau, log2_phi(d1 * p.scale, fabsf(d1) * c2, seps), -nz_log);
+                }
+                w0 = ex2_approx(x0);
+                w1 = ex2_approx(x1);
+                l0 = x0 * LN2;
+                l1 = x1 * LN2;
+              }
+              stats_add(rs, w0, l0, col < limit);
+              stats_add(rs, w1, l1, col + 1 < limit);
+            }
+          }
+          // S (and, for Yat, the tile's key norms) read: S(j+1) may land
+          tc_fence_before();
+          mbar_arrive(p_full(x));
           continue;
         }
         bool rescale = false;
@@ -829,6 +912,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_arrive(p_full(x));
       }
 
+      if (STATS && ok && nk_tiles > 0) {
+        // merge the two column halves of each row: half 1 hands its share to
+        // half 0 through shared memory, half 0 writes the row's statistics
+        float *sx = xchg + (uint32_t)x * BM;  // [13 values][2 tiles][BM]
+        if (half == 1) {
+          sx[(0 * 2) * BM + r] = rs.n;
+          sx[(1 * 2) * BM + r] = rs.hsum;
+          sx[(2 * 2) * BM + r] = rs.small;
+#pragma unroll
+          for (int i = 0; i < 10; ++i) sx[((3 + i) * 2) * BM + r] = rs.top[i];
+        }
+        named_barrier_sync(named_bar, 64);
+        if (half == 0) {
+          rs.n += sx[(0 * 2) * BM + r];
+          rs.hsum += sx[(1 * 2) * BM + r];
+          rs.small += sx[(2 * 2) * BM + r];
+#pragma unroll
+          for (int i = 0; i < 10; ++i) {
+            float v = sx[((3 + i) * 2) * BM + r];
+#pragma unroll
+            for (int k2 = 0; k2 < 10; ++k2) {
+              const float hi = fmaxf(rs.top[k2], v);
+              v = fminf(rs.top[k2], v);
+              rs.top[k2] = hi;
+            }
+          }
+          const Unit t = decode_unit(p, unit_ring[uc & 1u]);
+          const int row = t.q0 + x * BM + r;
+          if (row < p.Tq) {
+            const size_t ti = (size_t)t.bh * p.Tq + row;
+            float top10 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 10; ++i) top10 += rs.top[i];
+            if (p.st_entropy) p.st_entropy[ti] = rs.n > 1.f ? -rs.hsum / logf(rs.n) : 0.f;
+            if (p.st_small) p.st_small[ti] = rs.small / rs.n;
+            if (p.st_top10) p.st_top10[ti] = top10;
+          }
+        }
+        // half 0 has read the buffer before half 1 writes it for the next unit
+        named_barrier_sync(named_bar, 64);
+      }
       if (VARIANT == kTau && ok && nk_tiles > 0) {
         // tau*: the warp's sums, then one fp64 atomic per moment and warp
 #pragma unroll
@@ -847,7 +971,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       // ---- finalise: combine the two halves of the row, then normalise and
       // store (or, with key splits, store the unnormalised partial)
-      if (VARIANT != kTau && ok && nk_tiles > 0) {
+      if (VARIANT != kTau && !STATS && ok && nk_tiles > 0) {
         const float part = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
         const float ptop = fmaxf(top[0], top[1]);
         float *fb = xchg + (8 + (uint32_t)x * 4) * BM;  // [2 values][2 halves][BM]
@@ -999,11 +1123,11 @@ __global__ void tau_finalize_kernel(const double *moments, const float *eps, int
   }
 }
 
-template <int VARIANT, int DK, int DV, int YM = 1>
+template <int VARIANT, int DK, int DV, int YM = 1, bool STATS = false>
 cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                    const CUtensorMap &tv, cudaStream_t s) {
   using L = Layout<DK, DV>;
-  auto kern = fwd_kernel<VARIANT, DK, DV, YM>;
+  auto kern = fwd_kernel<VARIANT, DK, DV, YM, STATS>;
   static int configured_for = -1;
   static int sm_count = 0;
   int dev = 0;
@@ -1020,7 +1144,7 @@ cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap 
   const int grid = p.n_units < sm_count ? p.n_units : sm_count;  // one CTA per SM
   kern<<<grid, NUM_THREADS, L::ALLOC, s>>>(p, tq, tk, tv);
   e = cudaGetLastError();
-  if constexpr (VARIANT == kTau) {
+  if constexpr (VARIANT == kTau || STATS) {
     return e;
   } else {
     if (e != cudaSuccess || p.n_splits == 1) return e;
@@ -1081,6 +1205,20 @@ cudaError_t launch_fwd_tc(int variant, int dk, int dv, const FwdParams &p, const
   CATTN_TC_CASE(kTau, 64, 64)
   CATTN_TC_CASE(kTau, 128, 128)
 #undef CATTN_TC_CASE
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_row_stats_tc(int variant, int dk, const FwdParams &p, const CUtensorMap &tq,
+                                const CUtensorMap &tk, cudaStream_t s) {
+#define CATTN_TC_STATS(V, DK_) \
+  if (variant == V && dk == DK_) return tc::launch<V, DK_, DK_, 1, true>(p, tq, tk, tk, s);
+  CATTN_TC_STATS(kSoftmax, 64)
+  CATTN_TC_STATS(kSoftmax, 128)
+  CATTN_TC_STATS(kYat, 64)
+  CATTN_TC_STATS(kYat, 128)
+  CATTN_TC_STATS(kStau, 64)
+  CATTN_TC_STATS(kStau, 128)
+#undef CATTN_TC_STATS
   return cudaErrorInvalidValue;
 }
 

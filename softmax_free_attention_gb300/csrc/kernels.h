@@ -41,6 +41,10 @@ struct FwdParams {
   float *part_o;     // [n_splits, B*h, Tq, dv] unnormalised partial outputs (n_splits > 1)
   float *part_stat;  // [n_splits, B*h, Tq, 4]: mass or l, running max (log2), top score
   double *moments;   // kTau: [h][6] sums n, s, g, s g, g^2 (g = ln phi(s) - g0), zeroed
+  // row statistics pass: the forward's row_mass as input, three [B, h, Tq]
+  // outputs (any may be NULL)
+  const float *norm_in;
+  float *st_entropy, *st_small, *st_top10;
 };
 
 // Split count and grouping of the persistent tensor-core schedule; a pure
@@ -57,6 +61,11 @@ TcSchedule tc_schedule(int B, int h, int Tq, int Tk, int causal);
 cudaError_t launch_fwd_tc(int variant, int dk, int dv, const FwdParams &p, const CUtensorMap &tq,
                           const CUtensorMap &tk, const CUtensorMap &tv, cudaStream_t s);
 bool fwd_tc_supported(int dk, int dv);
+
+// The row statistics pass: the map's S and weights again (no V), per-row
+// normalised entropy, fraction below 1e-6 and top-10 mass.  dk 64 or 128.
+cudaError_t launch_row_stats_tc(int variant, int dk, const FwdParams &p, const CUtensorMap &tq,
+                                const CUtensorMap &tk, cudaStream_t s);
 
 // tau* per head from the moments the kTau pass accumulated: writes tau[h]
 // and, if moments_out is not NULL, the moments with g0 = ln(ln 2 + eps) in

@@ -176,5 +176,35 @@ __device__ __forceinline__ void tau_chunk(const uint32_t (&sr)[32], int c, float
   }
 }
 
+// Row statistics of the map over one thread's keys (normalised entropy: "The
+// Kernel Between the Roles", section "The run"; sparsity below 1e-6 and top-10
+// concentration: the s^tau page's fine-tuning comparison): the number of
+// allowed keys, sum w ln w, the count of weights below 1e-6, and the ten
+// largest weights in descending order.
+struct RowStats {
+  float n, hsum, small;
+  float top[10];
+};
+
+// Adds one key's weight w (ln w = lnw) if it is allowed.  The top-10 insert is
+// a bubble through the sorted list, taken only when some lane of the warp has
+// a weight above its tenth largest.
+__device__ __forceinline__ void stats_add(RowStats &st, float w, float lnw, bool allowed) {
+  if (allowed) {
+    st.n += 1.f;
+    st.hsum += w > 0.f ? w * lnw : 0.f;
+    st.small += w < 1e-6f ? 1.f : 0.f;
+  }
+  float v = allowed ? w : 0.f;
+  if (__any_sync(0xffffffffu, v > st.top[9])) {
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+      const float hi = fmaxf(st.top[i], v);
+      v = fminf(st.top[i], v);
+      st.top[i] = hi;
+    }
+  }
+}
+
 }  // namespace tc
 }  // namespace cattn

@@ -330,3 +330,39 @@ def oracle_forward_m(inp, causal, m):
     import oracle
     return oracle.forward("yat", inp["q"], inp["k"], inp["v"], b=inp["yat_b"], eps=inp["yat_eps"],
                           causal=causal, yat_m=m)
+
+
+# ---------------------------------------------------------------- row statistics
+
+STATS_SHAPES = [  # B, h, hkv, T_q, T_k, d, causal
+    (2, 4, 2, 300, 300, 128, True),
+    (1, 2, 1, 130, 130, 64, True),
+    (1, 2, 2, 200, 1100, 128, False),
+]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("shape", STATS_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_row_stats_match_oracle(variant, shape):
+    """Per-row entropy, fraction below 1e-6 and top-10 mass against the oracle.
+
+    Tolerances: entropy 2e-3 absolute and top-10 mass 2e-3 relative (the
+    weights come from fp32 scores of bf16 inputs and an fp32 normaliser);
+    the fraction below 1e-6 may differ by keys whose weight sits within
+    rounding of the threshold: at most two keys per row."""
+    import oracle
+    B, h, hkv, Tq, Tk, d, causal = shape
+    w = _wl("stats", B, h, hkv, Tq, Tk, d, d, causal=causal, qk=2.0, seed=Tq + 5)
+    inp = workloads.generate(w)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    kw = pu.params_for(variant, inp)
+    _, mass, _ = attention.forward(variant, q, k, v, causal=causal, scale=w.scale, **kw)
+    ent, small, top = attention.row_stats(variant, q, k, mass, causal=causal, scale=w.scale, **kw)
+    torch.cuda.synchronize()
+    assert attention.check_status() == 0
+    e_o, s_o, t_o = oracle.row_stats(variant, inp["q"], inp["k"], inp["v"], causal=causal,
+                                     scale=w.scale, **kw)
+    n = np.minimum(np.arange(Tq) + 1, Tk) if causal else np.full(Tq, Tk)
+    np.testing.assert_allclose(pu.to_np(ent), e_o, atol=2e-3)
+    np.testing.assert_allclose(pu.to_np(top), t_o, rtol=2e-3, atol=1e-6)
+    assert (np.abs(pu.to_np(small) - s_o) * n <= 2.0 + 1e-9).all()
