@@ -912,46 +912,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_arrive(p_full(x));
       }
 
-      if (STATS && ok && nk_tiles > 0) {
-        // merge the two column halves of each row: half 1 hands its share to
-        // half 0 through shared memory, half 0 writes the row's statistics
-        float *sx = xchg + (uint32_t)x * BM;  // [13 values][2 tiles][BM]
-        if (half == 1) {
-          sx[(0 * 2) * BM + r] = rs.n;
-          sx[(1 * 2) * BM + r] = rs.hsum;
-          sx[(2 * 2) * BM + r] = rs.small;
+      if constexpr (STATS) {
+        if (ok && nk_tiles > 0) {
+          // merge the two column halves of each row: half 1 hands its share to
+          // half 0 through shared memory, half 0 writes the row's statistics
+          float *sx = xchg + (uint32_t)x * BM;  // [13 values][2 tiles][BM]
+          if (half == 1) {
+            sx[(0 * 2) * BM + r] = rs.n;
+            sx[(1 * 2) * BM + r] = rs.hsum;
+            sx[(2 * 2) * BM + r] = rs.small;
 #pragma unroll
-          for (int i = 0; i < 10; ++i) sx[((3 + i) * 2) * BM + r] = rs.top[i];
-        }
-        named_barrier_sync(named_bar, 64);
-        if (half == 0) {
-          rs.n += sx[(0 * 2) * BM + r];
-          rs.hsum += sx[(1 * 2) * BM + r];
-          rs.small += sx[(2 * 2) * BM + r];
+            for (int i = 0; i < 10; ++i) sx[((3 + i) * 2) * BM + r] = rs.top[i];
+          }
+          named_barrier_sync(named_bar, 64);
+          if (half == 0) {
+            rs.n += sx[(0 * 2) * BM + r];
+            rs.hsum += sx[(1 * 2) * BM + r];
+            rs.small += sx[(2 * 2) * BM + r];
 #pragma unroll
-          for (int i = 0; i < 10; ++i) {
-            float v = sx[((3 + i) * 2) * BM + r];
+            for (int i = 0; i < 10; ++i) {
+              float v = sx[((3 + i) * 2) * BM + r];
 #pragma unroll
-            for (int k2 = 0; k2 < 10; ++k2) {
-              const float hi = fmaxf(rs.top[k2], v);
-              v = fminf(rs.top[k2], v);
-              rs.top[k2] = hi;
+              for (int k2 = 0; k2 < 10; ++k2) {
+                const float hi = fmaxf(rs.top[k2], v);
+                v = fminf(rs.top[k2], v);
+                rs.top[k2] = hi;
+              }
+            }
+            const Unit t = decode_unit(p, unit_ring[uc & 1u]);
+            const int row = t.q0 + x * BM + r;
+            if (row < p.Tq) {
+              const size_t ti = (size_t)t.bh * p.Tq + row;
+              float top10 = 0.f;
+#pragma unroll
+              for (int i = 0; i < 10; ++i) top10 += rs.top[i];
+              if (p.st_entropy) p.st_entropy[ti] = rs.n > 1.f ? -rs.hsum / logf(rs.n) : 0.f;
+              if (p.st_small) p.st_small[ti] = rs.small / rs.n;
+              if (p.st_top10) p.st_top10[ti] = top10;
             }
           }
-          const Unit t = decode_unit(p, unit_ring[uc & 1u]);
-          const int row = t.q0 + x * BM + r;
-          if (row < p.Tq) {
-            const size_t ti = (size_t)t.bh * p.Tq + row;
-            float top10 = 0.f;
-#pragma unroll
-            for (int i = 0; i < 10; ++i) top10 += rs.top[i];
-            if (p.st_entropy) p.st_entropy[ti] = rs.n > 1.f ? -rs.hsum / logf(rs.n) : 0.f;
-            if (p.st_small) p.st_small[ti] = rs.small / rs.n;
-            if (p.st_top10) p.st_top10[ti] = top10;
-          }
+          // half 0 has read the buffer before half 1 writes it for the next unit
+          named_barrier_sync(named_bar, 64);
         }
-        // half 0 has read the buffer before half 1 writes it for the next unit
-        named_barrier_sync(named_bar, 64);
       }
       if (VARIANT == kTau && ok && nk_tiles > 0) {
         // tau*: the warp's sums, then one fp64 atomic per moment and warp
