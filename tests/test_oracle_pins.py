@@ -469,3 +469,103 @@ def test_row_stats_causal_counts_allowed_keys_only():
     wr = w[0, 1, 11]
     assert small[0, 1, 11] == np.count_nonzero(wr < 1e-6) / 12
     assert top[0, 1, 11] == pytest.approx(sum(sorted(wr, reverse=True)[:10]), rel=1e-12)
+
+
+# --------------------------------------------------------------------------
+# backward: gradients of sum(dout * out) against central differences of the
+# (pinned) oracle forward, and softmax against torch autograd of the
+# library's scaled_dot_product_attention
+# --------------------------------------------------------------------------
+
+def _fd_grads(variant, q, k, v, do, names, kw, h=1e-6):
+    def loss(**over):
+        a = dict(q=q, k=k, v=v)
+        kk = dict(kw)
+        for n_, x in over.items():
+            (a if n_ in a else kk)[n_] = x
+        out, _, _ = oracle.forward(variant, a["q"], a["k"], a["v"], **kk)
+        return float(np.sum(out * do))
+
+    grads = {}
+    for n_ in names:
+        base = dict(q=q, k=k, v=v, **kw)[n_]
+        base = np.asarray(base, dtype=np.float64)
+        g = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            x = base.copy()
+            x[idx] += h
+            lp = loss(**{n_: x})
+            x[idx] -= 2 * h
+            lm = loss(**{n_: x})
+            g[idx] = (lp - lm) / (2 * h)
+        grads[n_] = g
+    return grads
+
+
+@pytest.mark.parametrize("variant,kw", [
+    ("softmax", dict(scale=0.7)),
+    ("stau", dict(scale=0.7, eps=np.array([0.3, 0.1]), tau=np.array([1.7, 2.5]))),
+    ("yat", dict(b=np.array([0.4, 0.9]), eps=np.array([0.5, 0.2]))),
+    ("yat", dict(b=np.array([0.4, -0.6]), eps=np.array([0.5, 0.2]), yat_m=2)),
+])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_central_differences(variant, kw, causal):
+    # GQA (two query heads on one key/value head), dk != dv, and for the
+    # non-causal case Tq != Tk, so a transposed operand or a wrong head map fails
+    rng = np.random.default_rng(11)
+    Tq, Tk = (5, 5) if causal else (4, 6)
+    q = rng.standard_normal((1, 2, Tq, 3))
+    k = rng.standard_normal((1, 1, Tk, 3))
+    v = rng.standard_normal((1, 1, Tk, 2))
+    do = rng.standard_normal((1, 2, Tq, 2))
+    kw = dict(kw, causal=causal)
+    dq, dk, dv, dpar = oracle.backward(variant, q, k, v, do, **kw)
+    names = ["q", "k", "v"] + sorted(dpar)
+    fd = _fd_grads(variant, q, k, v, do, names, kw)
+    got = dict(q=dq, k=dk, v=dv, **dpar)
+    for n_ in names:
+        np.testing.assert_allclose(got[n_], fd[n_], rtol=1e-6, atol=1e-7, err_msg=n_)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_softmax_matches_torch_autograd(causal):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(12)
+    q = rng.standard_normal((2, 4, 9, 8))
+    k = rng.standard_normal((2, 2, 9, 8))
+    v = rng.standard_normal((2, 2, 9, 5))
+    do = rng.standard_normal((2, 4, 9, 5))
+    dq, dk, dv, dpar = oracle.backward("softmax", q, k, v, do, causal=causal)
+    assert dpar == {}
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    rep = lambda x: x.repeat_interleave(2, dim=1)
+    out = torch.nn.functional.scaled_dot_product_attention(tq, rep(tk), rep(tv), is_causal=causal)
+    out.backward(torch.tensor(do))
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_backward_invariants():
+    # every row's weights sum to one (softmax, s^tau) or to M / (M + 1e-9)
+    # (Yat), so the dv rows of one head sum to the weighted dout rows; softmax
+    # is unchanged by adding one vector to every key, so its dk rows sum to 0
+    rng = np.random.default_rng(13)
+    q = rng.standard_normal((1, 1, 7, 4))
+    k = rng.standard_normal((1, 1, 7, 4))
+    v = rng.standard_normal((1, 1, 7, 3))
+    do = rng.standard_normal((1, 1, 7, 3))
+    for variant, kw in [("softmax", {}), ("stau", dict(eps=0.2, tau=3.0))]:
+        dq, dk, dv, _ = oracle.backward(variant, q, k, v, do, causal=True, **kw)
+        np.testing.assert_allclose(dv.sum(axis=2), do.sum(axis=2), atol=1e-12)
+    _, dk, _, _ = oracle.backward("softmax", q, k, v, do, causal=True)
+    np.testing.assert_allclose(dk.sum(axis=2), 0.0, atol=1e-12)
+    _, mass, _ = oracle.forward("yat", q, k, v, b=0.3, eps=0.1, causal=True)
+    _, _, dv, _ = oracle.backward("yat", q, k, v, do, b=0.3, eps=0.1, causal=True)
+    ratio = mass / (mass + 1e-9)
+    np.testing.assert_allclose(dv.sum(axis=2), (do * ratio[..., None]).sum(axis=2), atol=1e-12)
+    # dout = 0 gives zero gradients; a one-key row gives w = 1 (softmax) and no dq
+    z = oracle.backward("yat", q, k, v, np.zeros_like(do), b=0.3, eps=0.1)
+    assert all(np.all(x == 0) for x in z[:3])
+    dq, _, _, _ = oracle.backward("softmax", q[:, :, :1], k[:, :, :1], v[:, :, :1], do[:, :, :1])
+    np.testing.assert_array_equal(dq, 0.0)
