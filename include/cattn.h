@@ -219,6 +219,45 @@ int cattn_row_stats(int variant, const cattn_problem_t *p, const void *q, const 
                     float *entropy, float *frac_small, float *top10, void *workspace,
                     size_t workspace_bytes, cattn_stream_t stream);
 
+/* Backward of cattn_forward: the gradients of L = sum(dout * out) with
+ * respect to q, k, v and the per-head map parameters, for the forward of the
+ * same problem whose out and row_mass are passed in.
+ *
+ * Per query row t the forward's weights are w_tj = f_tj / Z_t; they are
+ * recomputed from the scores and row_mass (softmax, s^tau: log Z; Yat: Z
+ * before its + 1e-9).  With D_t = dout_t . out_t and dW_tj = dout_t . v_j:
+ *   dv_j = sum_t w_tj dout_t
+ *   softmax  dS_tj = w_tj (dW_tj - D_t); dq = scale dS k, dk = scale dS^T q
+ *   s^tau    dS_tj = w_tj (dW_tj - D_t) tau sigma(s_tj) / phi(s_tj), same
+ *            products; dtau = sum w (dW - D) ln phi, deps = sum w (dW - D) tau / phi
+ *   Yat      g = (dW - D) / Z, a = 2m g (q.k + b)^{2m-1} / den,
+ *            e = -g kappa / den, den = max(|q - k|^2, 0) + eps;
+ *            dq_t = sum_j (a - 2 e [|q-k|^2 > 0]) k_j + 2 q_t sum_j e [..],
+ *            dk_j symmetrically; db = sum a, deps = sum e
+ * (the chain rule through the maps of "Softmax-Free Attention in JAX/Flax
+ * NNX", section "One module, two compatibility functions", and "s^tau: a
+ * focal-length knob for attention", core formula).  The sums over query
+ * heads sharing a kv head (h > hkv) are taken inside the library.
+ *
+ *   q, k, v, out  the forward's inputs and output (bf16, layouts as above)
+ *   dout          [B, h, Tq, dv] bf16: dL/d out
+ *   row_mass      [B, h, Tq] fp32: the forward's row_mass output
+ *   dq, dk, dv    bf16, shaped like q, k, v; written, never read
+ *   db, deps, dtau  fp32 [h] or NULL: the parameter gradients the map has
+ *                 (Yat: db, deps; s^tau: deps, dtau; the others untouched)
+ * bf16 only, dk == dv in {64, 128}, yat_m in {0, 1, 2, 3}; anything else is
+ * CATTN_ERR_UNSUPPORTED.  A problem with no query rows writes zeros.  The
+ * kernels' accumulation order is fixed: repeated calls give identical bits
+ * for dq, dk and dv (the fp64 parameter sums use atomics).
+ * cattn_backward_workspace_bytes: bytes needed (0 if the problem is
+ * unsupported), 256-byte aligned; the workspace must be 256-byte aligned. */
+size_t cattn_backward_workspace_bytes(int variant, const cattn_problem_t *p);
+int cattn_backward(int variant, const cattn_problem_t *p, const void *q, const void *k,
+                   const void *v, const void *out, const void *dout, const float *b,
+                   const float *eps, const float *tau, const float *row_mass, void *dq, void *dk,
+                   void *dv, float *db, float *deps, float *dtau, void *workspace,
+                   size_t workspace_bytes, cattn_stream_t stream);
+
 /* Synchronises `stream`, then reports (and clears) the device-side status
  * word the kernels set when a bounded wait gives up: CATTN_ERR_TIMEOUT if
  * any kernel since the last check did so, CATTN_ERR_CUDA if the stream

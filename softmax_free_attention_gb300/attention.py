@@ -215,6 +215,49 @@ def row_stats(variant, q, k, row_mass, *, b=None, eps=None, tau=None, causal=Fal
     return ent, small, top
 
 
+def backward(variant, q, k, v, out, dout, row_mass, *, b=None, eps=None, tau=None,
+             causal=False, scale=None, yat_m=1, workspace=None):
+    """Gradients of sum(dout * out) for the forward that produced ``out`` and
+    ``row_mass`` from the same inputs and map.
+
+    bf16 CUDA tensors, dk == dv in {64, 128}.  Returns (dq, dk, dv, dparams):
+    dq, dk, dv bf16 shaped like q, k, v (GQA: dk, dv summed over the query
+    heads sharing a kv head); dparams a dict of fp32 [h] tensors -- Yat:
+    'b', 'eps'; s^tau: 'eps', 'tau'; softmax: empty.  Runs asynchronously on
+    the current stream.
+    """
+    vid = variant_id(variant)
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"), (dout, "dout")):
+        if t.device.type != "cuda" or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous CUDA tensor")
+    prob = make_problem(q, k, v, causal=causal, scale=scale, yat_m=yat_m)
+    if tuple(out.shape) != (q.shape[0], q.shape[1], q.shape[2], v.shape[3]) or \
+            dout.shape != out.shape or out.dtype != q.dtype or dout.dtype != q.dtype:
+        raise ValueError("out and dout must be [B, h, Tq, dv] in the dtype of q")
+    dev = q.device
+    h = q.shape[1]
+    lib = native.load()
+    need = int(lib.cattn_backward_workspace_bytes(vid, ctypes.byref(prob)))
+    if need == 0:
+        raise ValueError("unsupported problem for the backward (bf16, dk == dv in {64, 128})")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    bt = _per_head(b, h, dev, "b") if vid == native.YAT else None
+    et = _per_head(eps, h, dev, "eps") if vid in (native.YAT, native.STAU) else None
+    tt = _per_head(tau, h, dev, "tau") if vid == native.STAU else None
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    names = {native.YAT: ("b", "eps"), native.STAU: ("eps", "tau")}.get(vid, ())
+    grads = {n: torch.empty(h, dtype=torch.float32, device=dev) for n in names}
+    status = lib.cattn_backward(vid, ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                _ptr(dout), _ptr(bt), _ptr(et), _ptr(tt),
+                                _ptr(row_mass.contiguous()), _ptr(dq), _ptr(dk), _ptr(dv),
+                                _ptr(grads.get("b")), _ptr(grads.get("eps")),
+                                _ptr(grads.get("tau")), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream_handle(dev))
+    native.check(status, "cattn_backward")
+    return dq, dk, dv, grads
+
+
 def check_status(stream=None) -> int:
     """Synchronise `stream` (default: current) and return the kernels' wait status."""
     handle = ctypes.c_void_p(stream.cuda_stream if stream is not None

@@ -421,12 +421,149 @@ int cattn_row_stats(int variant, const cattn_problem_t *p, const void *q, const 
   return map_cuda(launch_row_stats_tc(variant, tp.dk, fp, tq, tk, s));
 }
 
+}  // extern "C"
+
+namespace {
+
+// Backward workspace, each part 256-byte aligned:
+//   dpar   [h][2] fp64 per-head parameter gradient sums, then (Yat) the largest
+//          key norm as fp32 bits (both zeroed by each call)
+//   aux    [B*h, Tq_pad] float4: D, normaliser, |q|^2 per query row
+//   nk     Yat only: squared k row norms [B*hkv, Tk_pad]
+struct BwdWs {
+  size_t dpar, nkmax, aux, nk, total;
+};
+
+int tq_pad(const cattn_problem_t *p) { return (p->Tq + kTile - 1) / kTile * kTile; }
+
+BwdWs bwd_ws(int variant, const cattn_problem_t *p) {
+  BwdWs w;
+  memset(&w, 0, sizeof(w));
+  w.dpar = 0;
+  w.nkmax = (size_t)p->h * 2 * sizeof(double);
+  size_t off = align256(w.nkmax + sizeof(unsigned int));
+  w.aux = off;
+  off += align256((size_t)p->B * p->h * tq_pad(p) * 16);
+  if (variant == CATTN_YAT) {
+    w.nk = off;
+    off += ws_nk_bytes(p);
+  }
+  w.total = off;
+  return w;
+}
+
+int check_bwd_problem(int variant, const cattn_problem_t *p) {
+  int rc = check_problem(variant, p);
+  if (rc != CATTN_OK) return rc;
+  if (p->dtype != CATTN_BF16 || !bwd_tc_supported(p->dk, p->dv)) return CATTN_ERR_UNSUPPORTED;
+  return CATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t cattn_backward_workspace_bytes(int variant, const cattn_problem_t *p) {
+  if (check_bwd_problem(variant, p) != CATTN_OK) return 0;
+  return bwd_ws(variant, p).total;
+}
+
+int cattn_backward(int variant, const cattn_problem_t *p, const void *q, const void *k,
+                   const void *v, const void *out, const void *dout, const float *b,
+                   const float *eps, const float *tau, const float *row_mass, void *dq, void *dk,
+                   void *dv, float *db, float *deps, float *dtau, void *workspace,
+                   size_t workspace_bytes, cattn_stream_t stream) {
+  int rc = check_bwd_problem(variant, p);
+  if (rc != CATTN_OK) return rc;
+  const bool empty = is_empty(p);
+  // dk and dv are written even without query rows (as zeros); dq has no
+  // elements then
+  const bool kv_empty = p->B == 0 || p->hkv == 0;
+  if ((!kv_empty && (!dk || !dv)) || (!empty && !dq)) return CATTN_ERR_INVALID_ARG;
+  if (!aligned16(dq) || !aligned16(dk) || !aligned16(dv)) return CATTN_ERR_UNSUPPORTED;
+  if (!empty) {
+    if (!q || !k || !v || !out || !dout || !row_mass || !workspace) return CATTN_ERR_INVALID_ARG;
+    if (variant == CATTN_YAT && (!b || !eps)) return CATTN_ERR_INVALID_ARG;
+    if (variant == CATTN_STAU && (!eps || !tau)) return CATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+      return CATTN_ERR_UNSUPPORTED;
+    if (workspace_bytes < bwd_ws(variant, p).total) return CATTN_ERR_SHAPE;
+  }
+  rc = check_device();
+  if (rc != CATTN_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (empty) {
+    // no query rows: every gradient is zero
+    const size_t kbytes = (size_t)p->B * p->hkv * p->Tk * p->dk * 2;
+    const size_t vbytes = (size_t)p->B * p->hkv * p->Tk * p->dv * 2;
+    if (!kv_empty && (rc = map_cuda(cudaMemsetAsync(dk, 0, kbytes, s))) != CATTN_OK) return rc;
+    if (!kv_empty && (rc = map_cuda(cudaMemsetAsync(dv, 0, vbytes, s))) != CATTN_OK) return rc;
+    for (float *g : {db, deps, dtau})
+      if (g && (rc = map_cuda(cudaMemsetAsync(g, 0, (size_t)p->h * sizeof(float), s))) != CATTN_OK)
+        return rc;
+    return CATTN_OK;
+  }
+  const BwdWs w = bwd_ws(variant, p);
+  char *ws = static_cast<char *>(workspace);
+  BwdParams bp;
+  memset(&bp, 0, sizeof(bp));
+  bp.aux = reinterpret_cast<const float4 *>(ws + w.aux);
+  bp.aux_w = reinterpret_cast<float *>(ws + w.aux);
+  bp.b = b;
+  bp.eps = eps;
+  bp.tau = tau;
+  bp.dq = dq;
+  bp.dk = dk;
+  bp.dv = dv;
+  bp.dpar = reinterpret_cast<double *>(ws + w.dpar);
+  bp.B = p->B;
+  bp.h = p->h;
+  bp.hkv = p->hkv;
+  bp.Tq = p->Tq;
+  bp.Tk = p->Tk;
+  bp.Tq_pad = tq_pad(p);
+  bp.Tk_pad = tk_pad(p);
+  bp.causal = p->causal ? 1 : 0;
+  bp.scale = p->scale;
+  bp.n_q64 = (p->Tq + 63) / 64;
+  bp.n_q128 = (p->Tq + 127) / 128;
+  bp.n_k64 = (p->Tk + 63) / 64;
+  bp.n_k128 = (p->Tk + 127) / 128;
+  // the parameter sums and the key-norm maximum start at zero
+  if ((rc = map_cuda(cudaMemsetAsync(ws, 0, w.aux, s))) != CATTN_OK) return rc;
+  if (variant == CATTN_YAT) {
+    bp.nk = reinterpret_cast<const float *>(ws + w.nk);
+    unsigned int *nk_max = reinterpret_cast<unsigned int *>(ws + w.nkmax);
+    if ((rc = map_cuda(launch_row_sqnorm_bf16(k, reinterpret_cast<float *>(ws + w.nk),
+                                              p->B * p->hkv, p->Tk, tk_pad(p), p->dk, nk_max, s))) !=
+        CATTN_OK)
+      return rc;
+  }
+  if ((rc = map_cuda(launch_bwd_prep(variant, p->dk, bp, q, out, dout, row_mass, s))) != CATTN_OK)
+    return rc;
+  BwdMaps m;
+  const int BH = p->B * p->h, BHK = p->B * p->hkv, d = p->dk;
+  if ((rc = encode_bf16_3d(&m.q128, q, d, p->Tq, BH, 128)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&m.do128, dout, d, p->Tq, BH, 128)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&m.k128, k, d, p->Tk, BHK, 128)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&m.v128, v, d, p->Tk, BHK, 128)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&m.q64, q, d, p->Tq, BH, 64)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&m.do64, dout, d, p->Tq, BH, 64)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&m.k64, k, d, p->Tk, BHK, 64)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&m.v64, v, d, p->Tk, BHK, 64)) != CATTN_OK) return rc;
+  if ((rc = map_cuda(launch_bwd_tc(variant, d, p->yat_m > 1 ? p->yat_m : 1, bp, m, s))) != CATTN_OK)
+    return rc;
+  return map_cuda(launch_bwd_param_finalize(variant, bp.dpar, p->h, db, deps, dtau, s));
+}
+
 int cattn_check_status(cattn_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return CATTN_ERR_CUDA;
-  unsigned int status = 0;
+  unsigned int status = 0, bstatus = 0;
   if (read_and_clear_status(&status) != cudaSuccess) return CATTN_ERR_CUDA;
-  return status ? CATTN_ERR_TIMEOUT : CATTN_OK;
+  if (read_and_clear_bwd_status(&bstatus) != cudaSuccess) return CATTN_ERR_CUDA;
+  return (status | bstatus) ? CATTN_ERR_TIMEOUT : CATTN_OK;
 }
 
 }  // extern "C"

@@ -1,0 +1,799 @@
+// bwd_tc.cu -- attention backward on the sm_103a tensor cores.
+//
+// Gradients of L = sum(dout * out) through the forward of the three maps.
+// Per query row t the forward's weights are w_tj = f_tj / Z_t, recomputed here
+// from the scores and the forward's own row_mass (softmax and s^tau: the log
+// of Z; Yat: the mass itself).  With dW_tj = dout_t . v_j and D_t = dout_t .
+// out_t, the chain rule through the normalisation gives dL/df_tj =
+// (dW_tj - D_t) / Z_t, and then per map
+//
+//   softmax  C = scale w (dW - D)
+//   s^tau    C = scale w (dW - D) tau sigma(s) / phi(s),       s = scale q.k
+//            dtau += w (dW - D) ln phi,  deps += w (dW - D) tau / phi
+//   Yat      g = (dW - D) / Z,  a = 2m g (q.k + b)^{2m-1} / den,
+//            e = -g kappa / den (the gradient on den = max(d2, 0) + eps),
+//            C = a - 2 e [d2 > 0],  db += a,  deps += e
+//
+// and the three products
+//
+//   dq_t = sum_j C_tj k_j (+ 2 q_t sum_j e_tj [d2 > 0] for Yat)
+//   dk_j = sum_t C_tj q_t (+ 2 k_j sum_t e_tj [d2 > 0] for Yat)
+//   dv_j = sum_t w_tj dout_t
+//
+// (the Yat distance term: d|q - k|^2 / dq = 2 (q - k), whose k part joins C).
+// The maps themselves: "Softmax-Free Attention in JAX/Flax NNX", section "One
+// module, two compatibility functions"; "s^tau: a focal-length knob for
+// attention", core formula.
+//
+// Two passes of one kernel template, each a dense tile loop:
+//
+//   SIDE_KV  one CTA per 128-key tile of one (batch, kv head).  K and V stay
+//            in shared memory; 64-row tiles of Q and dout, of every query
+//            head that shares the kv head, stream through a two-stage ring
+//            with the per-row D, normaliser and |q|^2.  Per tile:
+//              S^T = K Q^T and dP^T = V dout^T     tcgen05, into TMEM
+//              W^T and C^T                          eight warps, into shared memory
+//              dV += W^T dout and dK += C^T Q       tcgen05, accumulators in TMEM
+//   SIDE_Q   one CTA per 128-query tile of one (batch, head): Q and dout stay,
+//            64-key tiles of K and V (and the squared key norms) stream.
+//              S = Q K^T and dP = dout V^T, then C, then dQ += C K.
+//
+// The dQ pass computes S, dP and C again rather than exchanging partial dQ
+// through global atomics: both passes write each output element once, in a
+// fixed order, so the backward is deterministic.  S and dP have two TMEM
+// buffers each, so the MMAs of tile n+1 run while the warps map tile n, and
+// the accumulating MMAs of tile n run while they map tile n+1.
+//
+// TMEM (512 columns): S[2] at 0 and 64, dP[2] at 128 and 192, the first
+// accumulator (dV, or dQ) at 256, the second (dK) at 256 + D.
+//
+// Warp roles (320 threads): warps 0-7 map (warp w: TMEM lanes 32 (w % 4)..+31
+// = rows of the resident tile, tile columns [32 (w / 4), +32)), warp 8 issues
+// the TMA loads, warp 9 allocates TMEM and issues the MMAs from one lane.
+// Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the kernel
+// records a site code, raises a CTA-wide abort flag and every role leaves its
+// loop, waits for its own copies and MMAs in flight, and TMEM is released.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "maps.cuh"
+#include "ptx.cuh"
+
+namespace cattn {
+
+__device__ unsigned int g_bwd_status;
+
+namespace bwd {
+
+constexpr int RT = 128;  // rows of the resident tile (TMEM lanes)
+constexpr int CT = 64;   // rows of a streamed tile = columns of S
+constexpr int NUM_THREADS = 320;
+constexpr int MAP_WARPS = 8;
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr unsigned FULL = 0xffffffffu;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+constexpr int SIDE_KV = 0;
+constexpr int SIDE_Q = 1;
+
+constexpr uint32_t TM_S = 0;     // + 64 b
+constexpr uint32_t TM_DP = 128;  // + 64 b
+constexpr uint32_t TM_A1 = 256;
+
+enum : unsigned { SITE_PRODUCER = 0x1100, SITE_MMA = 0x1200, SITE_MAP = 0x1300 };
+
+template <int D, int SIDE>
+struct Layout {
+  static constexpr int R_TILE = RT * D * 2;
+  static constexpr int X_TILE = CT * D * 2;
+  static constexpr int AUX = 1024;  // 64 float4 (SIDE_KV) or 64 floats (SIDE_Q)
+  static constexpr int STAGE = 2 * X_TILE + AUX;
+  static constexpr int W_TILE = RT * CT * 2;  // one 128-byte swizzle box per row
+  static constexpr int OFF_R = 0;
+  static constexpr int OFF_RP = R_TILE;
+  static constexpr int OFF_ST = 2 * R_TILE;
+  static constexpr int OFF_W = OFF_ST + 2 * STAGE;
+  static constexpr int OFF_C = OFF_W + (SIDE == SIDE_KV ? 2 * W_TILE : 0);
+  static constexpr int OFF_XCH = OFF_C + 2 * W_TILE;  // [2 halves][128] floats
+  static constexpr int OFF_BAR = OFF_XCH + 2 * RT * 4;
+  // r_full, x_full[2], x_empty[2], s_full[2], s_empty[2], wc_full[2], wc_empty[2],
+  // acc_full, drain
+  static constexpr int NBAR = 15;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_MISC + 16;
+  // at least 120 KB, so that a second CTA (which would wait for this one's
+  // 512 TMEM columns) never shares the SM
+  static constexpr int ALLOC = BYTES + 1024 > 120 * 1024 ? BYTES + 1024 : 120 * 1024;
+  static_assert(ALLOC <= 227 * 1024, "shared memory budget");
+  static_assert(STAGE % 1024 == 0 && R_TILE % 1024 == 0 && X_TILE % 1024 == 0,
+                "swizzle atoms stay 1024-B aligned");
+};
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          unsigned site) {
+  if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
+    const int bad = *abort != 0 || (globaltimer_ns() - t0 > WAIT_LIMIT_NS);
+    if (__any_sync(FULL, bad)) {
+      if ((threadIdx.x & 31) == 0) {
+        atomicCAS(&g_bwd_status, 0u, site | 1u);
+        *abort = 1;
+      }
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                            unsigned site, bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((honor_abort && *abort != 0) || (globaltimer_ns() - t0 > WAIT_LIMIT_NS)) {
+      atomicCAS(&g_bwd_status, 0u, site | 1u);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                       uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+__device__ __forceinline__ void stg128(void *ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+
+// S[128 x 64] = A[128 x D] B[64 x D]^T: A a resident tile (64-column boxes
+// RT*128 bytes apart), B a streamed tile (boxes CT*128 bytes apart).
+template <int D>
+__device__ __forceinline__ void issue_scores(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(RT, CT, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t a = a_smem + (uint32_t)(kk >> 2) * (RT * 128) + (uint32_t)(kk & 3) * 32;
+    const uint32_t b = b_smem + (uint32_t)(kk >> 2) * (CT * 128) + (uint32_t)(kk & 3) * 32;
+    mma_ss(d_tmem, smem_desc_sw128(a, 16, 1024), smem_desc_sw128(b, 16, 1024), IDESC,
+           kk > 0 ? 1u : 0u);
+  }
+}
+
+// Acc[128 x D] (+)= A[128 x 64] B[64 x D]: A the map warps' tile (one 128-byte
+// box per row, K-major), B a streamed tile read N-major (64-column boxes
+// CT*128 bytes apart).
+template <int D>
+__device__ __forceinline__ void issue_acc(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
+                                          bool accumulate) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(RT, D, true);
+#pragma unroll
+  for (int kk = 0; kk < CT / 16; ++kk) {
+    mma_ss(d_tmem, smem_desc_sw128(a_smem + (uint32_t)kk * 32, 16, 1024),
+           smem_desc_sw128(b_smem + (uint32_t)kk * 2048, CT * 128, 1024), IDESC,
+           (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+struct HeadP {
+  float b, eps, tau;
+};
+
+// One (row, column) pair: w (the forward's weight) and C (the score
+// gradient), plus the Yat distance gradient e and the per-head parameter
+// gradients.  Dt, Lt: the query row's D and normaliser (log2 Z for softmax
+// and s^tau, 1 / Z for Yat); qn, nk: squared norms of q and k (Yat).
+template <int VARIANT, int YM>
+__device__ __forceinline__ void pair_grad(float s, float dp, float Dt, float Lt, float qn,
+                                          float nk, const HeadP &hp, float scale, float c2,
+                                          bool allowed, float &w, float &c, float &esum,
+                                          float &g1, float &g2) {
+  if constexpr (VARIANT == kSoftmax) {
+    const float x = ex2_approx(fmaf(s, c2, -Lt));
+    w = allowed ? x : 0.f;
+    c = scale * w * (dp - Dt);
+  } else if constexpr (VARIANT == kStau) {
+    const float sc = s * scale;
+    const float e = ex2_approx(-fabsf(s) * c2);
+    const float l1p = e < 0x1p-12f ? e : lg2_approx(1.f + e) * LN2;
+    const float phi = fmaxf(sc, 0.f) + l1p + hp.eps;
+    const float lp = lg2_approx(phi);
+    const float x = ex2_approx(fmaf(hp.tau, lp, -Lt));
+    w = allowed ? x : 0.f;
+    const float r1 = rcp_approx(1.f + e);
+    const float sig = sc >= 0.f ? r1 : e * r1;
+    const float rphi = rcp_approx(phi);
+    const float base = w * (dp - Dt);
+    const float bt = base * hp.tau * rphi;
+    c = scale * bt * sig;
+    g1 += bt;                // eps
+    g2 += base * lp * LN2;   // tau
+  } else {  // Yat
+    const float num = s + hp.b;
+    const float num2 = num * num;
+    float nodd = num, neven = num2;  // num^{2m-1}, num^{2m}
+    if constexpr (YM == 2) {
+      nodd = num * num2;
+      neven = num2 * num2;
+    }
+    if constexpr (YM == 3) {
+      nodd = num * num2 * num2;
+      neven = num2 * num2 * num2;
+    }
+    const float den_raw = fmaf(-2.f, s, qn + nk + hp.eps);  // |q - k|^2 + eps
+    const bool act = den_raw > hp.eps;
+    const float rd = rcp_approx(act ? den_raw : hp.eps);
+    const float kap = neven * rd;
+    const float g = allowed ? (dp - Dt) * Lt : 0.f;
+    w = allowed ? kap * Lt : 0.f;
+    const float a = (float)(2 * YM) * g * nodd * rd;
+    const float e = -g * kap * rd;
+    const float bd = act ? e : 0.f;
+    c = fmaf(-2.f, bd, a);
+    esum += bd;
+    g1 += a;  // b
+    g2 += e;  // eps
+  }
+}
+
+// DP: the row-sum pass (SIDE_Q only): D_t = sum_j w_tj dW_tj from the
+// backward's own weights, written over the aux array's D; no C, no dQ.
+template <int VARIANT, int D, int SIDE, int YM = 1, bool DP = false>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    bwd_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tm_r,
+               const __grid_constant__ CUtensorMap tm_rp, const __grid_constant__ CUtensorMap tm_x,
+               const __grid_constant__ CUtensorMap tm_xp) {
+  using L = Layout<D, SIDE>;
+  constexpr bool KV = SIDE == SIDE_KV;
+  static_assert(!DP || SIDE == SIDE_Q, "the row-sum pass runs on the query side");
+  constexpr bool HAS_PAR = KV && VARIANT != kSoftmax;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024u - (raw_s & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const uint32_t bar0 = sb + L::OFF_BAR;
+  const uint32_t bar_r_full = bar0;
+  auto x_full = [&](int b) { return bar0 + 8u * (1 + b); };
+  auto x_empty = [&](int b) { return bar0 + 8u * (3 + b); };
+  auto s_full = [&](int b) { return bar0 + 8u * (5 + b); };
+  auto s_empty = [&](int b) { return bar0 + 8u * (7 + b); };
+  auto wc_full = [&](int b) { return bar0 + 8u * (9 + b); };
+  auto wc_empty = [&](int b) { return bar0 + 8u * (11 + b); };
+  const uint32_t bar_acc = bar0 + 8u * 13;
+  const uint32_t bar_drain = bar0 + 8u * 14;
+  const uint32_t r_smem = sb + L::OFF_R, rp_smem = sb + L::OFF_RP;
+  auto x_smem = [&](int b) { return sb + L::OFF_ST + (uint32_t)b * L::STAGE; };
+  auto xp_smem = [&](int b) { return x_smem(b) + L::X_TILE; };
+  auto aux_smem = [&](int b) { return x_smem(b) + 2 * L::X_TILE; };
+  auto w_smem = [&](int b) { return sb + L::OFF_W + (uint32_t)b * L::W_TILE; };
+  auto c_smem = [&](int b) { return sb + L::OFF_C + (uint32_t)b * L::W_TILE; };
+  float *xch = reinterpret_cast<float *>(smem + L::OFF_XCH);
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+  volatile int *abort = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
+
+  // ---- this CTA's tile and its list of streamed tiles
+  int rt, bh_r, n_tiles, first = 0, per_head = 0, group = 1, b_idx;
+  if constexpr (KV) {
+    const int nb = p.B * p.hkv;
+    rt = blockIdx.x / nb;  // key tile; heavy (low) tiles first under a causal mask
+    bh_r = blockIdx.x % nb;
+    b_idx = bh_r / p.hkv;
+    group = p.h / p.hkv;
+    first = p.causal ? 2 * rt : 0;
+    per_head = p.n_q64 - first;
+    n_tiles = group * per_head;
+  } else {
+    const int nb = p.B * p.h;
+    rt = p.n_q128 - 1 - (int)(blockIdx.x / nb);  // query tile, heavy (high) tiles first
+    bh_r = blockIdx.x % nb;
+    b_idx = bh_r / p.h;
+    n_tiles = p.causal ? min(2 * rt + 2, p.n_k64) : p.n_k64;
+  }
+  // head and row of streamed tile n (SIDE_KV: (query head, query tile); SIDE_Q: key tile)
+  auto stream_tile = [&](int n, int &bh_x, int &row0, int &head) {
+    if constexpr (KV) {
+      const int g = bh_r % p.hkv;
+      head = g * group + n / per_head;
+      bh_x = b_idx * p.h + head;
+      row0 = (first + n % per_head) * CT;
+    } else {
+      head = bh_r % p.h;
+      bh_x = b_idx * p.hkv + head / (p.h / p.hkv);
+      row0 = n * CT;
+    }
+  };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_r_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(x_full(b), 1);
+      // DP: released by the map warps (lane 0 of each) once they have read the
+      // stage's key norms; else by the commit after the tile's last MMA
+      mbar_init(x_empty(b), DP ? MAP_WARPS : 1);
+      mbar_init(s_full(b), 1);
+      mbar_init(s_empty(b), MAP_WARPS * 32);
+      mbar_init(wc_full(b), MAP_WARPS * 32);
+      mbar_init(wc_empty(b), 1);
+    }
+    mbar_init(bar_acc, 1);
+    mbar_init(bar_drain, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  if (warp == PRODUCER_WARP && lane == 0) {
+    tma_prefetch_desc(&tm_r);
+    tma_prefetch_desc(&tm_rp);
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_xp);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == PRODUCER_WARP) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar_r_full, 2u * L::R_TILE);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(r_smem + c * RT * 128, &tm_r, c * 64, rt * RT, bh_r, bar_r_full);
+        tma_load_3d(rp_smem + c * RT * 128, &tm_rp, c * 64, rt * RT, bh_r, bar_r_full);
+      }
+      constexpr uint32_t AUXB = KV ? CT * 16 : (VARIANT == kYat ? CT * 4 : 0);
+      int issued = 0;
+      for (int n = 0; n < n_tiles; ++n) {
+        const int b = n & 1;
+        if (n >= 2 && !thread_wait(x_empty(b), ((n >> 1) & 1) ^ 1, abort, SITE_PRODUCER | 0x10))
+          break;
+        int bh_x, row0, head;
+        stream_tile(n, bh_x, row0, head);
+        mbar_arrive_expect_tx(x_full(b), 2u * L::X_TILE + AUXB);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(x_smem(b) + c * CT * 128, &tm_x, c * 64, row0, bh_x, x_full(b));
+          tma_load_3d(xp_smem(b) + c * CT * 128, &tm_xp, c * 64, row0, bh_x, x_full(b));
+        }
+        if constexpr (KV) {
+          bulk_load(aux_smem(b), p.aux + (size_t)bh_x * p.Tq_pad + row0, AUXB, x_full(b));
+        } else if constexpr (VARIANT == kYat) {
+          bulk_load(aux_smem(b), p.nk + (size_t)bh_x * p.Tk_pad + row0, AUXB, x_full(b));
+        }
+        issued = n + 1;
+      }
+      // copies still in flight land before the CTA can exit
+      thread_wait(bar_r_full, 0, abort, SITE_PRODUCER | 0x20, false);
+      for (int m = issued >= 2 ? issued - 2 : 0; m < issued; ++m)
+        thread_wait(x_full(m & 1), (m >> 1) & 1, abort, SITE_PRODUCER | 0x30, false);
+    }
+  } else if (warp == MMA_WARP) {
+    if (lane == 0) {
+      bool ok = thread_wait(bar_r_full, 0, abort, SITE_MMA | 0x10);
+      auto do_acc = [&](int m) -> bool {
+        const int b = m & 1;
+        if (!thread_wait(wc_full(b), (m >> 1) & 1, abort, SITE_MMA | 0x20)) return false;
+        tc_fence_after();
+        if constexpr (KV) {
+          issue_acc<D>(tmem + TM_A1, w_smem(b), xp_smem(b), m > 0);      // dV += W^T dout
+          issue_acc<D>(tmem + TM_A1 + D, c_smem(b), x_smem(b), m > 0);  // dK += C^T Q
+        } else {
+          issue_acc<D>(tmem + TM_A1, c_smem(b), x_smem(b), m > 0);  // dQ += C K
+        }
+        mma_commit(x_empty(b));
+        mma_commit(wc_empty(b));
+        return true;
+      };
+      for (int n = 0; ok && n < n_tiles; ++n) {
+        const int b = n & 1;
+        if (!(ok = thread_wait(x_full(b), (n >> 1) & 1, abort, SITE_MMA | 0x30))) break;
+        if (n >= 2 && !(ok = thread_wait(s_empty(b), ((n >> 1) & 1) ^ 1, abort, SITE_MMA | 0x40)))
+          break;
+        tc_fence_after();
+        issue_scores<D>(tmem + TM_S + 64u * b, r_smem, x_smem(b));
+        issue_scores<D>(tmem + TM_DP + 64u * b, rp_smem, xp_smem(b));
+        mma_commit(s_full(b));
+        if (!DP && n >= 1) ok = do_acc(n - 1);
+      }
+      if (!DP && ok && n_tiles > 0) ok = do_acc(n_tiles - 1);
+      if (!DP && ok) mma_commit(bar_acc);
+      // every MMA this thread issued has completed once `drain` flips
+      mma_commit(bar_drain);
+      thread_wait(bar_drain, 0, abort, SITE_MMA | 0x50, false);
+    }
+  } else {
+    // ---- map warps
+    const int qd = warp & 3, hf = warp >> 2;
+    const int r = 32 * qd + lane;  // row of the resident tile
+    const uint32_t t_lane = tmem + ((uint32_t)(32 * qd) << 16);
+    const float scale = p.scale, c2 = p.scale * LOG2E;
+    const int grow = rt * RT + r;  // key j (SIDE_KV) or query t (SIDE_Q)
+    // row scalars
+    float row_nk = 0.f;
+    float4 row_aux = make_float4(0.f, 0.f, 0.f, 0.f);
+    HeadP hp{0.f, 1.f, 1.f};
+    if constexpr (KV) {
+      if (VARIANT == kYat) row_nk = p.nk[(size_t)bh_r * p.Tk_pad + grow];
+    } else {
+      row_aux = reinterpret_cast<const float4 *>(p.aux)[(size_t)bh_r * p.Tq_pad + grow];
+      const int head = bh_r % p.h;
+      if (VARIANT == kYat) hp.b = p.b[head];
+      if (VARIANT != kSoftmax) hp.eps = p.eps[head];
+      if (VARIANT == kStau) hp.tau = p.tau[head];
+    }
+    float esum = 0.f, g1 = 0.f, g2 = 0.f, dsum = 0.f;
+    bool ok = true;
+    for (int n = 0; n < n_tiles; ++n) {
+      const int b = n & 1;
+      int bh_x, row0, head;
+      stream_tile(n, bh_x, row0, head);
+      if constexpr (KV) {
+        if (n % per_head == 0) {
+          if (VARIANT == kYat) hp.b = p.b[head];
+          if (VARIANT != kSoftmax) hp.eps = p.eps[head];
+          if (VARIANT == kStau) hp.tau = p.tau[head];
+        }
+      }
+      if (!(ok = warp_wait(s_full(b), (n >> 1) & 1, abort, SITE_MAP | 0x10))) break;
+      tc_fence_after();
+      uint32_t sr[32], dr[32];
+      tmem_ld32(t_lane + TM_S + 64u * b + 32u * hf, sr);
+      tmem_ld32(t_lane + TM_DP + 64u * b + 32u * hf, dr);
+      tmem_wait_ld();
+      tmem_ld_fence(sr);
+      tmem_ld_fence(dr);
+      tc_fence_before();
+      mbar_arrive(s_empty(b));
+
+      const int col0 = row0 + 32 * hf;  // global index of this thread's first column
+      uint32_t wpk[16], cpk[16];
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        float Dt[4], Lt[4], qn[4], nk[4];
+        bool al[4];
+        if constexpr (KV) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint4 a = lds128(aux_smem(b) + 16u * (32 * hf + i + u));
+            Dt[u] = __uint_as_float(a.x);
+            Lt[u] = __uint_as_float(a.y);
+            qn[u] = __uint_as_float(a.z);
+            nk[u] = row_nk;
+            const int t = col0 + i + u;
+            al[u] = t < p.Tq && grow < p.Tk && (!p.causal || grow <= t);
+          }
+        } else {
+          uint4 a = make_uint4(0u, 0u, 0u, 0u);
+          if (VARIANT == kYat) a = lds128(aux_smem(b) + 4u * (32 * hf + i));
+          const float n4[4] = {__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z),
+                               __uint_as_float(a.w)};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            Dt[u] = row_aux.x;
+            Lt[u] = row_aux.y;
+            qn[u] = row_aux.z;
+            nk[u] = n4[u];
+            const int j = col0 + i + u;
+            al[u] = j < p.Tk && grow < p.Tq && (!p.causal || j <= grow);
+          }
+        }
+        float w[4], c[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          pair_grad<VARIANT, YM>(__uint_as_float(sr[i + u]), __uint_as_float(dr[i + u]), Dt[u],
+                                 Lt[u], qn[u], nk[u], hp, scale, c2, al[u], w[u], c[u], esum, g1,
+                                 g2);
+        if constexpr (DP) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) dsum = fmaf(w[u], __uint_as_float(dr[i + u]), dsum);
+        }
+        wpk[i >> 1] = pack_bf16x2(w[0], w[1]);
+        wpk[(i >> 1) + 1] = pack_bf16x2(w[2], w[3]);
+        cpk[i >> 1] = pack_bf16x2(c[0], c[1]);
+        cpk[(i >> 1) + 1] = pack_bf16x2(c[2], c[3]);
+      }
+      if constexpr (DP) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(x_empty(b));
+        continue;
+      }
+      if (n >= 2 && !(ok = warp_wait(wc_empty(b), ((n >> 1) & 1) ^ 1, abort, SITE_MAP | 0x20)))
+        break;
+      // row r of the 128-byte-swizzled box: logical 16-byte chunk 4 hf + q at
+      // physical chunk (4 hf + q) ^ (r % 8)
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const uint32_t off = (uint32_t)r * 128u + (uint32_t)(((4 * hf + q4) ^ (r & 7)) * 16);
+        if constexpr (KV)
+          sts128(w_smem(b) + off, wpk[4 * q4], wpk[4 * q4 + 1], wpk[4 * q4 + 2], wpk[4 * q4 + 3]);
+        sts128(c_smem(b) + off, cpk[4 * q4], cpk[4 * q4 + 1], cpk[4 * q4 + 2], cpk[4 * q4 + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(wc_full(b));
+      if constexpr (HAS_PAR) {
+        if (n % per_head == per_head - 1) {  // last tile of this query head
+          float a = g1, e = g2;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            a += __shfl_xor_sync(FULL, a, o);
+            e += __shfl_xor_sync(FULL, e, o);
+          }
+          if (lane == 0) {
+            atomicAdd(p.dpar + 2 * head, (double)a);
+            atomicAdd(p.dpar + 2 * head + 1, (double)e);
+          }
+          g1 = 0.f;
+          g2 = 0.f;
+        }
+      }
+    }
+    if constexpr (DP) {
+      // the two column halves' partial sums, then D_t over the aux array's D
+      xch[hf * RT + r] = dsum;
+      named_barrier_sync(1, MAP_WARPS * 32);
+      if (ok && hf == 0 && grow < p.Tq)
+        p.aux_w[((size_t)bh_r * p.Tq_pad + grow) * 4] = xch[r] + xch[RT + r];
+    } else {
+    // ---- epilogue: accumulators out of TMEM, Yat's rank-one term, bf16 stores
+    if (ok) ok = warp_wait(bar_acc, 0, abort, SITE_MAP | 0x30);
+    if (VARIANT == kYat) {
+      xch[hf * RT + r] = esum;
+      named_barrier_sync(1, MAP_WARPS * 32);
+      esum = xch[r] + xch[RT + r];
+    }
+    if (ok) {
+      tc_fence_after();
+      const bool row_ok = KV ? grow < p.Tk : grow < p.Tq;
+      constexpr int NACC = KV ? 2 : 1;
+#pragma unroll
+      for (int acc = 0; acc < NACC; ++acc) {
+        // SIDE_KV: acc 0 = dV (no rank-one term), acc 1 = dK; SIDE_Q: dQ
+        const bool rank1 = VARIANT == kYat && (KV ? acc == 1 : true);
+        __nv_bfloat16 *dst =
+            KV ? reinterpret_cast<__nv_bfloat16 *>(acc == 0 ? p.dv : p.dk) +
+                     ((size_t)bh_r * p.Tk + grow) * D
+               : reinterpret_cast<__nv_bfloat16 *>(p.dq) + ((size_t)bh_r * p.Tq + grow) * D;
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) {
+          const int col = hf * (D / 2) + 32 * cc;  // this thread's 32 accumulator columns
+          uint32_t ar[32];
+          tmem_ld32(t_lane + TM_A1 + (uint32_t)(acc * D + col), ar);
+          tmem_wait_ld();
+          tmem_ld_fence(ar);
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(ar[i]);
+          if (rank1) {
+            // + 2 esum x_row, x_row = this row of the resident tile (k_j or q_t)
+            const float f = 2.f * esum;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const int chunk = ((col & 63) >> 3) + q4;
+              const uint4 x = lds128(r_smem + (uint32_t)(col >> 6) * (RT * 128) +
+                                     (uint32_t)r * 128u + (uint32_t)((chunk ^ (r & 7)) * 16));
+              const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float lo = __uint_as_float(xs[u] << 16);
+                const float hi = __uint_as_float(xs[u] & 0xffff0000u);
+                v[8 * q4 + 2 * u] = fmaf(f, lo, v[8 * q4 + 2 * u]);
+                v[8 * q4 + 2 * u + 1] = fmaf(f, hi, v[8 * q4 + 2 * u + 1]);
+              }
+            }
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              stg128(dst + col + 8 * q4, pack_bf16x2(v[8 * q4], v[8 * q4 + 1]),
+                     pack_bf16x2(v[8 * q4 + 2], v[8 * q4 + 3]),
+                     pack_bf16x2(v[8 * q4 + 4], v[8 * q4 + 5]),
+                     pack_bf16x2(v[8 * q4 + 6], v[8 * q4 + 7]));
+          }
+        }
+      }
+    }
+    }  // !DP
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Per query row: D = dout . out (softmax; the other maps take D from the
+// row-sum pass), the normaliser (softmax, s^tau: row_mass
+// log2 e, the log2 of Z; Yat: 1 / (row_mass + 1e-9)) and |q|^2 (Yat); zeros
+// for the padding rows up to Tq_pad.  Eight lanes per row.
+template <int VARIANT, int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__restrict__ q,
+                                                       const __nv_bfloat16 *__restrict__ out,
+                                                       const __nv_bfloat16 *__restrict__ dout,
+                                                       const float *__restrict__ row_mass,
+                                                       float4 *__restrict__ aux, int BH, int Tq,
+                                                       int Tq_pad) {
+  const long long row = ((long long)blockIdx.x * 256 + threadIdx.x) >> 3;
+  const int sub = threadIdx.x & 7;
+  const bool live = row < (long long)BH * Tq_pad;
+  const int bh = live ? (int)(row / Tq_pad) : 0;
+  const int t = live ? (int)(row % Tq_pad) : 0;
+  const bool valid = live && t < Tq;
+  float dsum = 0.f, qsum = 0.f;
+  if (valid) {
+    const size_t base = ((size_t)bh * Tq + t) * D;
+#pragma unroll
+    for (int c = sub * 8; c < D; c += 64) {
+      const uint4 o4 = *reinterpret_cast<const uint4 *>(out + base + c);
+      const uint4 d4 = *reinterpret_cast<const uint4 *>(dout + base + c);
+      const uint32_t os[4] = {o4.x, o4.y, o4.z, o4.w}, ds[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        dsum = fmaf(__uint_as_float(os[u] << 16), __uint_as_float(ds[u] << 16), dsum);
+        dsum = fmaf(__uint_as_float(os[u] & 0xffff0000u), __uint_as_float(ds[u] & 0xffff0000u),
+                    dsum);
+      }
+      if constexpr (VARIANT == kYat) {
+        const uint4 q4 = *reinterpret_cast<const uint4 *>(q + base + c);
+        const uint32_t qs[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float lo = __uint_as_float(qs[u] << 16), hi = __uint_as_float(qs[u] & 0xffff0000u);
+          qsum = fmaf(lo, lo, qsum);
+          qsum = fmaf(hi, hi, qsum);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) {
+    dsum += __shfl_xor_sync(FULL, dsum, o);
+    qsum += __shfl_xor_sync(FULL, qsum, o);
+  }
+  if (live && sub == 0) {
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (valid) {
+      const float m = row_mass[(size_t)bh * Tq + t];
+      a.x = dsum;
+      a.y = VARIANT == kYat ? 1.f / (m + 1e-9f) : m * LOG2E;
+      a.z = qsum;
+    }
+    aux[row] = a;
+  }
+}
+
+__global__ void bwd_param_finalize(const double *dpar, int h, int variant, float *db, float *deps,
+                                   float *dtau) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= h) return;
+  const double a = dpar[2 * i], e = dpar[2 * i + 1];
+  if (variant == kYat) {
+    if (db) db[i] = (float)a;
+    if (deps) deps[i] = (float)e;
+  } else if (variant == kStau) {
+    if (deps) deps[i] = (float)a;
+    if (dtau) dtau[i] = (float)e;
+  }
+}
+
+template <int VARIANT, int D, int SIDE, int YM, bool DP = false>
+cudaError_t launch_side(const BwdParams &p, const CUtensorMap &r, const CUtensorMap &rp,
+                        const CUtensorMap &x, const CUtensorMap &xp, cudaStream_t s) {
+  using L = Layout<D, SIDE>;
+  auto kern = bwd_kernel<VARIANT, D, SIDE, YM, DP>;
+  static int configured_for = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_for != dev) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+    if (e != cudaSuccess) return e;
+    configured_for = dev;
+  }
+  const long long grid = SIDE == SIDE_KV ? (long long)p.B * p.hkv * p.n_k128
+                                         : (long long)p.B * p.h * p.n_q128;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<(unsigned)grid, NUM_THREADS, L::ALLOC, s>>>(p, r, rp, x, xp);
+  return cudaGetLastError();
+}
+
+// Yat and s^tau first replace the D of dout . out (from the bf16 forward
+// output, whose weights were rounded to bf16 before the PV product) with the
+// row sum of the backward's own weights times dW, so that sum_j w_j (dW_j - D)
+// is zero for the weights actually used.  Yat's score gradient carries the
+// factor 2 / (q.k + b) and s^tau's parameter gradients the factors 1 / phi
+// and ln phi: on rows whose mass sits on keys where those are large (a causal
+// row's first keys; strongly negative scores) a 2^-9 error in D would be
+// amplified far beyond the bf16 tolerance.  Softmax's gradient is bounded by
+// w <= 1 and keeps dout . out.
+template <int VARIANT, int D, int YM>
+cudaError_t launch_all(const BwdParams &p, const BwdMaps &m, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  if constexpr (VARIANT != kSoftmax) {
+    e = launch_side<VARIANT, D, SIDE_Q, YM, true>(p, m.q128, m.do128, m.k64, m.v64, s);
+    if (e != cudaSuccess) return e;
+  }
+  e = launch_side<VARIANT, D, SIDE_KV, YM>(p, m.k128, m.v128, m.q64, m.do64, s);
+  if (e != cudaSuccess) return e;
+  return launch_side<VARIANT, D, SIDE_Q, YM>(p, m.q128, m.do128, m.k64, m.v64, s);
+}
+
+template <int VARIANT, int D>
+cudaError_t launch_prep(const BwdParams &p, const void *q, const void *out, const void *dout,
+                        const float *row_mass, cudaStream_t s) {
+  const long long rows = (long long)p.B * p.h * p.Tq_pad;
+  const unsigned blocks = (unsigned)((rows * 8 + 255) / 256);
+  bwd_prep_kernel<VARIANT, D><<<blocks, 256, 0, s>>>(
+      static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(out),
+      static_cast<const __nv_bfloat16 *>(dout), row_mass, const_cast<float4 *>(p.aux),
+      p.B * p.h, p.Tq, p.Tq_pad);
+  return cudaGetLastError();
+}
+
+}  // namespace bwd
+
+bool bwd_tc_supported(int dk, int dv) { return dk == dv && (dk == 64 || dk == 128); }
+
+cudaError_t launch_bwd_prep(int variant, int d, const BwdParams &p, const void *q, const void *out,
+                            const void *dout, const float *row_mass, cudaStream_t s) {
+  using namespace bwd;
+  if (d == 64) {
+    if (variant == kSoftmax) return launch_prep<kSoftmax, 64>(p, q, out, dout, row_mass, s);
+    if (variant == kYat) return launch_prep<kYat, 64>(p, q, out, dout, row_mass, s);
+    return launch_prep<kStau, 64>(p, q, out, dout, row_mass, s);
+  }
+  if (variant == kSoftmax) return launch_prep<kSoftmax, 128>(p, q, out, dout, row_mass, s);
+  if (variant == kYat) return launch_prep<kYat, 128>(p, q, out, dout, row_mass, s);
+  return launch_prep<kStau, 128>(p, q, out, dout, row_mass, s);
+}
+
+cudaError_t launch_bwd_tc(int variant, int d, int yat_m, const BwdParams &p, const BwdMaps &m,
+                          cudaStream_t s) {
+  using namespace bwd;
+  if (d == 64) {
+    if (variant == kSoftmax) return launch_all<kSoftmax, 64, 1>(p, m, s);
+    if (variant == kStau) return launch_all<kStau, 64, 1>(p, m, s);
+    if (yat_m == 2) return launch_all<kYat, 64, 2>(p, m, s);
+    if (yat_m == 3) return launch_all<kYat, 64, 3>(p, m, s);
+    return launch_all<kYat, 64, 1>(p, m, s);
+  }
+  if (variant == kSoftmax) return launch_all<kSoftmax, 128, 1>(p, m, s);
+  if (variant == kStau) return launch_all<kStau, 128, 1>(p, m, s);
+  if (yat_m == 2) return launch_all<kYat, 128, 2>(p, m, s);
+  if (yat_m == 3) return launch_all<kYat, 128, 3>(p, m, s);
+  return launch_all<kYat, 128, 1>(p, m, s);
+}
+
+cudaError_t launch_bwd_param_finalize(int variant, const double *dpar, int h, float *db,
+                                      float *deps, float *dtau, cudaStream_t s) {
+  if (variant == kSoftmax || h <= 0) return cudaSuccess;
+  bwd::bwd_param_finalize<<<(h + 127) / 128, 128, 0, s>>>(dpar, h, variant, db, deps, dtau);
+  return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_bwd_status(unsigned int *value) {
+  unsigned int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_bwd_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_bwd_status, &zero, sizeof(unsigned int));
+}
+
+}  // namespace cattn

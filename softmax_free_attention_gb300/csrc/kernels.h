@@ -83,7 +83,38 @@ bool fwd_simt_supported(int dk, int dv);
 cudaError_t launch_row_sqnorm_bf16(const void *x, float *out, int BH, int T, int T_pad, int d,
                                    unsigned int *max_bits, cudaStream_t s);
 
-// Device status word set by kernels whose bounded waits gave up.
+// Everything the backward kernels read besides the tensor maps.
+struct BwdParams {
+  const float4 *aux;           // [B*h, Tq_pad]: D = dout . out, normaliser, |q|^2, 0
+  float *aux_w;                // the same array as floats (the Yat row-sum pass writes D)
+  const float *nk;             // [B*hkv, Tk_pad] squared k row norms (Yat), zero padded
+  const float *b, *eps, *tau;  // [h]
+  void *dq, *dk, *dv;          // bf16, shaped like q, k, v
+  double *dpar;                // [h][2]: Yat (b, eps), s^tau (eps, tau); zeroed
+  int B, h, hkv, Tq, Tk, Tq_pad, Tk_pad, causal;
+  float scale;
+  int n_q64, n_q128, n_k64, n_k128;  // tiles of 64 and 128 rows
+};
+// Tensor maps of the backward: q, dout, k, v with 128-row and 64-row boxes.
+struct BwdMaps {
+  CUtensorMap q128, do128, k128, v128, q64, do64, k64, v64;
+};
+bool bwd_tc_supported(int dk, int dv);
+// The per-row D, normaliser and |q|^2 (into p.aux) from q, out, dout and
+// the forward's row_mass.
+cudaError_t launch_bwd_prep(int variant, int d, const BwdParams &p, const void *q,
+                            const void *out, const void *dout, const float *row_mass,
+                            cudaStream_t s);
+// The dK/dV pass, then the dQ pass.
+cudaError_t launch_bwd_tc(int variant, int d, int yat_m, const BwdParams &p, const BwdMaps &m,
+                          cudaStream_t s);
+// The fp64 per-head parameter sums into the fp32 outputs (any may be NULL).
+cudaError_t launch_bwd_param_finalize(int variant, const double *dpar, int h, float *db,
+                                      float *deps, float *dtau, cudaStream_t s);
+
+// Device status words set by kernels whose bounded waits gave up (forward
+// and backward kernels).
 cudaError_t read_and_clear_status(unsigned int *value);
+cudaError_t read_and_clear_bwd_status(unsigned int *value);
 
 }  // namespace cattn

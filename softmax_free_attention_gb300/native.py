@@ -28,7 +28,8 @@ ERR_SCRATCH_LIMIT = 6
 EXPORTS = ("cattn_version", "cattn_error_string", "cattn_workspace_bytes", "cattn_validate",
            "cattn_key_norms", "cattn_forward", "cattn_forward_noalloc",
            "cattn_tau_star_workspace_bytes", "cattn_tau_star", "cattn_row_stats_workspace_bytes",
-           "cattn_row_stats", "cattn_check_status")
+           "cattn_row_stats", "cattn_backward_workspace_bytes", "cattn_backward",
+           "cattn_check_status")
 
 
 class Problem(ctypes.Structure):
@@ -84,6 +85,10 @@ def load():
     lib.cattn_row_stats_workspace_bytes.restype = sz
     lib.cattn_row_stats.argtypes = [i, pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.cattn_row_stats.restype = i
+    lib.cattn_backward_workspace_bytes.argtypes = [i, pp]
+    lib.cattn_backward_workspace_bytes.restype = sz
+    lib.cattn_backward.argtypes = [i, pp] + [vp] * 16 + [sz, vp]
+    lib.cattn_backward.restype = i
     lib.cattn_check_status.argtypes = [vp]
     lib.cattn_check_status.restype = i
     _lib = lib

@@ -153,6 +153,18 @@ def generate(w: Workload, device=None):
     return out
 
 
+def grad_output(w: Workload, device=None):
+    """dL/d out for the backward: standard normal [B, h, Tq, dv] in the
+    workload's dtype, from a generator of its own (seed + 7919) so that the
+    forward inputs stay those of ``generate``."""
+    import torch
+
+    rng = np.random.default_rng(w.seed + 7919)
+    d = rng.standard_normal((w.B, w.h, w.Tq, w.dv), dtype=np.float32)
+    t = torch.from_numpy(d).to(torch.bfloat16 if w.dtype == "bf16" else torch.float32)
+    return t if device is None else t.to(device)
+
+
 def sample_rows(w: Workload, n_random: int = 64, seed: int = 1):
     """Deterministic subset of flat query-row indices into [B, h, Tq].
 
