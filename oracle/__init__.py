@@ -252,18 +252,23 @@ def backward(variant, q, k, v, dout, *, b=None, eps=None, tau=None, causal=False
              yat_m=1):
     """Gradients of L = sum(dout * out) through the attention forward, in fp64.
 
-    With w_j = f_j / Z per row (f the map's unnormalised weight: softmax
-    exp(s_j), s^tau phi(s_j)^tau, Yat kappa_j; Z = sum_j f_j, plus the forward's
-    1e-9 for Yat), dW_j = dout . v_j and D = sum_j w_j dW_j = dout . out, the
-    chain rule gives dL/df_j = (dW_j - D) / Z, then
-      softmax  dL/ds_j = w_j (dW_j - D)
-      s^tau    dL/ds_j = w_j (dW_j - D) tau sigma(s_j) / phi(s_j),  d tau += sum_j w_j (dW_j - D) ln phi(s_j)
-      Yat      dL/d(q.k_j) = g_j 2m (q.k_j + b)^{2m-1} / den_j,  dL/d d2_j = -g_j kappa_j / den_j
-               (zero where the clamp max(d2, 0) is active), g_j = (dW_j - D) / Z,
-               d2 = |q|^2 + |k|^2 - 2 q.k, so dL/dq += dL/dd2 * 2 (q - k_j);
-               d b += sum_j g_j 2m (q.k_j + b)^{2m-1} / den_j, d eps += sum_j dL/dd2_j
-    and ds/dq = scale * k for softmax and s^tau.  Straight loops over rows and
-    keys; GQA gradients of K and V are summed over the query heads sharing them.
+    Per (batch, query head) with the full score matrix: f_tj the map's
+    unnormalised weight (softmax exp(s), s^tau phi(s)^tau, Yat kappa), Z_t =
+    sum_j f_tj (plus the forward's 1e-9 for Yat), w = f / Z, dW = dout V^T and
+    D_t = dout_t . out_t.  The chain rule through the normalisation gives
+    dL/df_tj = (dW_tj - D_t) / Z_t, then
+      softmax  dS = w (dW - D),                       ds/dq = scale k
+      s^tau    dS = w (dW - D) tau sigma(s) / phi,    ds/dq = scale k,
+               d tau = sum w (dW - D) ln phi,  d eps = sum w (dW - D) tau / phi
+      Yat      g = (dW - D) / Z,  A = g 2m (q.k + b)^{2m-1} / den,
+               E = -g kappa / den  (the gradient on den = max(d2, 0) + eps),
+               d2 = |q|^2 + |k|^2 - 2 q.k with d d2/dq = 2 (q - k), zero where
+               the clamp is active (d2 <= 0):
+               dq_t = sum_j A_tj k_j + 2 sum_j E'_tj (q_t - k_j)
+               dk_j = sum_t A_tj q_t + 2 sum_t E'_tj (k_j - q_t),  E' = E [d2 > 0]
+               d b = sum A,  d eps = sum E
+    and dv = w^T dout.  Masked pairs have f = 0 and no gradient.  GQA: the
+    gradients of a kv head are summed over the query heads that share it.
 
     Returns (dq, dk, dv, dparams) with dparams a dict of per-head arrays
     ('b', 'eps' for Yat; 'eps', 'tau' for s^tau; empty for softmax).
@@ -275,13 +280,13 @@ def backward(variant, q, k, v, dout, *, b=None, eps=None, tau=None, causal=False
     do = _as_f64(dout, "dout")
     B, h, Tq, dk = q.shape
     _, hkv, Tk, _ = k.shape
-    dv_ = v.shape[-1]
     if scale is None:
         scale = 1.0 / np.sqrt(dk)
     group = h // hkv
     bb = _per_head(b, h, "b")
     ee = _per_head(eps, h, "eps")
     tt = _per_head(tau, h, "tau")
+    m = int(yat_m)
     dq = np.zeros_like(q)
     dkk = np.zeros_like(k)
     dvv = np.zeros_like(v)
@@ -290,55 +295,54 @@ def backward(variant, q, k, v, dout, *, b=None, eps=None, tau=None, causal=False
         dpar = {"b": np.zeros(h), "eps": np.zeros(h)}
     elif variant == STAU:
         dpar = {"eps": np.zeros(h), "tau": np.zeros(h)}
-    m = int(yat_m)
+    allowed = np.ones((Tq, Tk), dtype=bool)
+    if causal:
+        allowed = np.arange(Tk)[None, :] <= np.arange(Tq)[:, None]
     for bi in range(B):
         for i in range(h):
             g_ = i // group
-            K = k[bi, g_]
-            V = v[bi, g_]
-            for t in range(Tq):
-                n = min(t + 1, Tk) if causal else Tk
-                qr = q[bi, i, t]
-                dots = K[:n] @ qr
-                if variant == SOFTMAX:
-                    s_ = scale * dots
-                    f = np.exp(s_ - s_.max())
-                    Z = f.sum()
-                elif variant == STAU:
-                    s_ = scale * dots
-                    phi = np.logaddexp(0.0, s_) + ee[i]
-                    lf = tt[i] * np.log(phi)
-                    f = np.exp(lf - lf.max())
-                    Z = f.sum()
-                else:
-                    num = dots + bb[i]
-                    d2 = np.sum((qr[None, :] - K[:n]) ** 2, axis=1)
-                    den = np.maximum(d2, 0.0) + ee[i]
-                    f = num ** (2 * m) / den
-                    Z = f.sum() + 1e-9
-                w = f / Z
-                out = w @ V[:n]
-                dW = V[:n] @ do[bi, i, t]
-                D = float(do[bi, i, t] @ out)
-                dvv[bi, g_, :n] += np.outer(w, do[bi, i, t])
-                if variant == SOFTMAX:
-                    ds = w * (dW - D)
-                    dq[bi, i, t] += scale * (ds @ K[:n])
-                    dkk[bi, g_, :n] += scale * np.outer(ds, qr)
-                elif variant == STAU:
-                    sig = 1.0 / (1.0 + np.exp(-s_))
-                    base = w * (dW - D)
-                    ds = base * tt[i] * sig / phi
-                    dq[bi, i, t] += scale * (ds @ K[:n])
-                    dkk[bi, g_, :n] += scale * np.outer(ds, qr)
-                    dpar["tau"][i] += float(np.sum(base * np.log(phi)))
-                    dpar["eps"][i] += float(np.sum(base * tt[i] / phi))
-                else:
-                    gj = (dW - D) / Z
-                    a = gj * 2 * m * num ** (2 * m - 1) / den
-                    bd = np.where(d2 > 0.0, -gj * f / den, 0.0)
-                    dq[bi, i, t] += a @ K[:n] + 2.0 * (bd @ (qr[None, :] - K[:n]))
-                    dkk[bi, g_, :n] += np.outer(a, qr) + 2.0 * bd[:, None] * (K[:n] - qr[None, :])
-                    dpar["b"][i] += float(np.sum(a))
-                    dpar["eps"][i] += float(np.sum(-gj * f / den))
+            Q, K, V, dO = q[bi, i], k[bi, g_], v[bi, g_], do[bi, i]
+            dots = Q @ K.T
+            if variant == SOFTMAX:
+                s_ = np.where(allowed, scale * dots, -np.inf)
+                f = np.exp(s_ - s_.max(axis=1, keepdims=True))
+                Z = f.sum(axis=1, keepdims=True)
+            elif variant == STAU:
+                s_ = scale * dots
+                phi = np.logaddexp(0.0, s_) + ee[i]
+                lf = np.where(allowed, tt[i] * np.log(phi), -np.inf)
+                f = np.exp(lf - lf.max(axis=1, keepdims=True))
+                Z = f.sum(axis=1, keepdims=True)
+            else:
+                num = dots + bb[i]
+                d2 = (Q * Q).sum(axis=1)[:, None] + (K * K).sum(axis=1)[None, :] - 2.0 * dots
+                den = np.maximum(d2, 0.0) + ee[i]
+                f = np.where(allowed, num ** (2 * m) / den, 0.0)
+                Z = f.sum(axis=1, keepdims=True) + 1e-9
+            w = f / Z
+            out = w @ V
+            dW = dO @ V.T
+            D = (dO * out).sum(axis=1, keepdims=True)
+            dvv[bi, g_] += w.T @ dO
+            if variant == SOFTMAX:
+                dS = w * (dW - D)
+                dq[bi, i] += scale * (dS @ K)
+                dkk[bi, g_] += scale * (dS.T @ Q)
+            elif variant == STAU:
+                base = w * (dW - D)
+                sig = 1.0 / (1.0 + np.exp(-s_))
+                dS = base * tt[i] * sig / phi
+                dq[bi, i] += scale * (dS @ K)
+                dkk[bi, g_] += scale * (dS.T @ Q)
+                dpar["tau"][i] += float(np.sum(base * np.log(phi)))
+                dpar["eps"][i] += float(np.sum(base * tt[i] / phi))
+            else:
+                G = np.where(allowed, (dW - D) / Z, 0.0)
+                A = G * 2 * m * num ** (2 * m - 1) / den
+                E = -G * f / den
+                Ea = np.where(d2 > 0.0, E, 0.0)
+                dq[bi, i] += A @ K + 2.0 * (Ea.sum(axis=1)[:, None] * Q - Ea @ K)
+                dkk[bi, g_] += A.T @ Q + 2.0 * (Ea.sum(axis=0)[:, None] * K - Ea.T @ Q)
+                dpar["b"][i] += float(np.sum(A))
+                dpar["eps"][i] += float(np.sum(E))
     return dq, dkk, dvv, dpar
