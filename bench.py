@@ -387,6 +387,38 @@ def main():
     per_variant["tau_star"] = {"kernel_ms": tau_ms, "qk_tflops": qk_flops / (tau_ms * 1e-3) / 1e12,
                                "scores_per_s": qk_flops / (2 * w.dk) / (tau_ms * 1e-3)}
 
+    # ---- backward of each map on the same inputs (not part of the step above):
+    # the row-sum pass (Yat, s^tau), the dK/dV pass and the dQ pass; FLOPs
+    # counted as 2.5 forward passes (the five products S, dP, dV, dK, dQ)
+    dout = workloads.grad_output(w, device=dev)
+    bwd_ws = None
+    for variant in ("yat", "softmax", "stau"):
+        kw = {"yat": dict(b=yb, eps=ye), "softmax": {}, "stau": dict(eps=se, tau=tau)}[variant]
+        o_b, m_b, _ = attention.forward(variant, q, k, v, causal=w.causal, scale=w.scale, **kw)
+        bprob = attention.make_problem(q, k, v, causal=w.causal, scale=w.scale)
+        need = int(native.load().cattn_backward_workspace_bytes(attention.variant_id(variant),
+                                                                 ctypes.byref(bprob)))
+        if bwd_ws is None or bwd_ws.numel() < need:
+            bwd_ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            attention.backward(variant, q, k, v, o_b, dout, m_b, causal=w.causal, scale=w.scale,
+                               workspace=bwd_ws, **kw)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            attention.backward(variant, q, k, v, o_b, dout, m_b, causal=w.causal, scale=w.scale,
+                               workspace=bwd_ws, **kw)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / args.steps
+        tf = 2.5 * flops / (ms * 1e-3) / 1e12
+        per_variant[variant]["backward"] = {"kernel_ms": ms, "tflops": tf,
+                                            "frac_of_peak": tf / peak_burst}
+        del o_b, m_b
+    assert attention.check_status() == 0
+    del dout, bwd_ws
+
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:

@@ -47,13 +47,16 @@
 // TMEM (512 columns): S[2] at 0 and 64, dP[2] at 128 and 192, the first
 // accumulator (dV, or dQ) at 256, the second (dK) at 256 + D.
 //
-// Warp roles (320 threads): warps 0-7 map (warp w: TMEM lanes 32 (w % 4)..+31
-// = rows of the resident tile, tile columns [32 (w / 4), +32)), warp 8 issues
-// the TMA loads, warp 9 allocates TMEM and issues the MMAs from one lane.
+// Warp roles (576 threads): warps 0-15 map (warp w: TMEM lanes 32 (w % 4)..+31
+// = rows of the resident tile, tile columns [16 (w / 4), +16); four warps per
+// SM sub-partition hide each other's TMEM and SFU latencies), warp 16 issues
+// the TMA loads, warp 17 allocates TMEM and issues the MMAs from one lane.
 // Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the kernel
 // records a site code, raises a CTA-wide abort flag and every role leaves its
 // loop, waits for its own copies and MMAs in flight, and TMEM is released.
 #include <cuda_bf16.h>
+
+#include <type_traits>
 
 #include "kernels.h"
 #include "maps.cuh"
@@ -67,10 +70,12 @@ namespace bwd {
 
 constexpr int RT = 128;  // rows of the resident tile (TMEM lanes)
 constexpr int CT = 64;   // rows of a streamed tile = columns of S
-constexpr int NUM_THREADS = 320;
-constexpr int MAP_WARPS = 8;
-constexpr int PRODUCER_WARP = 8;
-constexpr int MMA_WARP = 9;
+constexpr int NUM_THREADS = 576;
+constexpr int MAP_WARPS = 16;
+constexpr int PRODUCER_WARP = 16;
+constexpr int MMA_WARP = 17;
+constexpr int NQ = MAP_WARPS / 4;  // column slices of a tile: four map warps per TMEM lane quadrant
+constexpr int CW = CT / NQ;        // columns per map warp (16)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr unsigned FULL = 0xffffffffu;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -92,16 +97,21 @@ struct Layout {
   static constexpr int AUX = 1024;  // 64 float4 (SIDE_KV) or 64 floats (SIDE_Q)
   static constexpr int STAGE = 2 * X_TILE + AUX;
   static constexpr int W_TILE = RT * CT * 2;  // one 128-byte swizzle box per row
+  // Stages of the streamed-tile ring: a stage is held from the tile's S MMAs
+  // to its accumulating MMAs, so the ring runs two tiles ahead of the map
+  // warps.  One W / C buffer: the map warps of tile n+1 finish long after the
+  // accumulating MMAs of tile n have read it.
+  static constexpr int NS = SIDE == SIDE_KV ? 3 : 4;
   static constexpr int OFF_R = 0;
   static constexpr int OFF_RP = R_TILE;
   static constexpr int OFF_ST = 2 * R_TILE;
-  static constexpr int OFF_W = OFF_ST + 2 * STAGE;
-  static constexpr int OFF_C = OFF_W + (SIDE == SIDE_KV ? 2 * W_TILE : 0);
-  static constexpr int OFF_XCH = OFF_C + 2 * W_TILE;  // [2 halves][128] floats
-  static constexpr int OFF_BAR = OFF_XCH + 2 * RT * 4;
-  // r_full, x_full[2], x_empty[2], s_full[2], s_empty[2], wc_full[2], wc_empty[2],
+  static constexpr int OFF_W = OFF_ST + NS * STAGE;
+  static constexpr int OFF_C = OFF_W + (SIDE == SIDE_KV ? W_TILE : 0);
+  static constexpr int OFF_XCH = OFF_C + W_TILE;  // [NQ slices][128] floats
+  static constexpr int OFF_BAR = OFF_XCH + NQ * RT * 4;
+  // r_full, x_full[NS], x_empty[NS], s_full[2], s_empty[2], wc_full, wc_empty,
   // acc_full, drain
-  static constexpr int NBAR = 15;
+  static constexpr int NBAR = 1 + 2 * NS + 4 + 2 + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   // at least 120 KB, so that a second CTA (which would wait for this one's
@@ -152,6 +162,15 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
                "r"(d)
                : "memory");
 }
+__device__ __forceinline__ void tmem_ld_fence16(uint32_t (&r)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(r[i])::"memory");
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ void stg128(void *ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c),
                "r"(d)
@@ -191,60 +210,90 @@ struct HeadP {
   float b, eps, tau;
 };
 
-// One (row, column) pair: w (the forward's weight) and C (the score
-// gradient), plus the Yat distance gradient e and the per-head parameter
-// gradients.  Dt, Lt: the query row's D and normaliser (log2 Z for softmax
-// and s^tau, 1 / Z for Yat); qn, nk: squared norms of q and k (Yat).
-template <int VARIANT, int YM>
-__device__ __forceinline__ void pair_grad(float s, float dp, float Dt, float Lt, float qn,
-                                          float nk, const HeadP &hp, float scale, float c2,
-                                          bool allowed, float &w, float &c, float &esum,
-                                          float &g1, float &g2) {
+// Two (row, column) pairs of one row, as f32x2 lanes: the weights w (the
+// forward's, recomputed) and the score gradients c, plus the accumulators.
+// X, Y, Z: the query row's scalars as the prep and row-sum passes leave them
+//   softmax  X = -D scale,   Y = -log2 Z
+//   s^tau    X = -D,         Y = -log2 Z
+//   Yat      X = -D / Z,     Y = 1 / Z,     Z = |q|^2 + eps + |k|^2
+// Accumulators: Yat acc0 = -sum e [d2 > 0] (the rank-one term), acc1 = db,
+// acc2 = -deps; s^tau acc1 = deps, acc2 = dtau / ln 2.  FULL: every pair is
+// allowed (no mask).  WONLY: the weights only (the row-sum pass).
+template <int VARIANT, int YM, bool FULL, bool WONLY>
+__device__ __forceinline__ void pair2(float2 s, float2 dp, float2 X, float2 Y, float2 Z,
+                                      const HeadP &hp, float scale, float c2, bool al0, bool al1,
+                                      float2 &w, float2 &c, float2 &acc0, float2 &acc1,
+                                      float2 &acc2) {
   if constexpr (VARIANT == kSoftmax) {
-    const float x = ex2_approx(fmaf(s, c2, -Lt));
-    w = allowed ? x : 0.f;
-    c = scale * w * (dp - Dt);
+    const float2 x = __ffma2_rn(s, make_float2(c2, c2), Y);
+    w = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    if (!FULL) {
+      w.x = al0 ? w.x : 0.f;
+      w.y = al1 ? w.y : 0.f;
+    }
+    if constexpr (!WONLY) c = __fmul2_rn(w, __ffma2_rn(dp, make_float2(scale, scale), X));
   } else if constexpr (VARIANT == kStau) {
-    const float sc = s * scale;
-    const float e = ex2_approx(-fabsf(s) * c2);
-    const float l1p = e < 0x1p-12f ? e : lg2_approx(1.f + e) * LN2;
-    const float phi = fmaxf(sc, 0.f) + l1p + hp.eps;
-    const float lp = lg2_approx(phi);
-    const float x = ex2_approx(fmaf(hp.tau, lp, -Lt));
-    w = allowed ? x : 0.f;
-    const float r1 = rcp_approx(1.f + e);
-    const float sig = sc >= 0.f ? r1 : e * r1;
-    const float rphi = rcp_approx(phi);
-    const float base = w * (dp - Dt);
-    const float bt = base * hp.tau * rphi;
-    c = scale * bt * sig;
-    g1 += bt;                // eps
-    g2 += base * lp * LN2;   // tau
+    const float2 sc = __fmul2_rn(s, make_float2(scale, scale));
+    const float e0 = ex2_approx(-fabsf(s.x) * c2), e1 = ex2_approx(-fabsf(s.y) * c2);
+    const float l0 = e0 < 0x1p-12f ? e0 : lg2_approx(1.f + e0) * LN2;
+    const float l1 = e1 < 0x1p-12f ? e1 : lg2_approx(1.f + e1) * LN2;
+    const float2 phi = make_float2(fmaxf(sc.x, 0.f) + l0 + hp.eps, fmaxf(sc.y, 0.f) + l1 + hp.eps);
+    const float2 lp = make_float2(lg2_approx(phi.x), lg2_approx(phi.y));
+    const float2 x = __ffma2_rn(make_float2(hp.tau, hp.tau), lp, Y);
+    w = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+    if (!FULL) {
+      w.x = al0 ? w.x : 0.f;
+      w.y = al1 ? w.y : 0.f;
+    }
+    if constexpr (!WONLY) {
+      const float r0 = rcp_approx(1.f + e0), r1 = rcp_approx(1.f + e1);
+      const float2 sig = make_float2(sc.x >= 0.f ? r0 : e0 * r0, sc.y >= 0.f ? r1 : e1 * r1);
+      const float2 trphi =
+          __fmul2_rn(make_float2(hp.tau, hp.tau), make_float2(rcp_approx(phi.x), rcp_approx(phi.y)));
+      const float2 base = __fmul2_rn(w, __fadd2_rn(dp, X));  // w (dW - D)
+      const float2 bt = __fmul2_rn(base, trphi);
+      c = __fmul2_rn(__fmul2_rn(bt, sig), make_float2(scale, scale));
+      acc1 = __fadd2_rn(acc1, bt);
+      acc2 = __ffma2_rn(base, lp, acc2);
+    }
   } else {  // Yat
-    const float num = s + hp.b;
-    const float num2 = num * num;
-    float nodd = num, neven = num2;  // num^{2m-1}, num^{2m}
+    const float2 num = __fadd2_rn(s, make_float2(hp.b, hp.b));
+    const float2 num2 = __fmul2_rn(num, num);
+    float2 nodd = num, neven = num2;  // num^{2m-1}, num^{2m}
     if constexpr (YM == 2) {
-      nodd = num * num2;
-      neven = num2 * num2;
+      nodd = __fmul2_rn(num, num2);
+      neven = __fmul2_rn(num2, num2);
     }
     if constexpr (YM == 3) {
-      nodd = num * num2 * num2;
-      neven = num2 * num2 * num2;
+      const float2 num4 = __fmul2_rn(num2, num2);
+      nodd = __fmul2_rn(num, num4);
+      neven = __fmul2_rn(num2, num4);
     }
-    const float den_raw = fmaf(-2.f, s, qn + nk + hp.eps);  // |q - k|^2 + eps
-    const bool act = den_raw > hp.eps;
-    const float rd = rcp_approx(act ? den_raw : hp.eps);
-    const float kap = neven * rd;
-    const float g = allowed ? (dp - Dt) * Lt : 0.f;
-    w = allowed ? kap * Lt : 0.f;
-    const float a = (float)(2 * YM) * g * nodd * rd;
-    const float e = -g * kap * rd;
-    const float bd = act ? e : 0.f;
-    c = fmaf(-2.f, bd, a);
-    esum += bd;
-    g1 += a;  // b
-    g2 += e;  // eps
+    const float2 den = __ffma2_rn(make_float2(-2.f, -2.f), s, Z);  // |q - k|^2 + eps
+    const bool a0 = den.x > hp.eps, a1 = den.y > hp.eps;
+    const float2 rd =
+        make_float2(rcp_approx(a0 ? den.x : hp.eps), rcp_approx(a1 ? den.y : hp.eps));
+    const float2 kap = __fmul2_rn(neven, rd);
+    w = __fmul2_rn(kap, Y);
+    if (!FULL) {
+      w.x = al0 ? w.x : 0.f;
+      w.y = al1 ? w.y : 0.f;
+    }
+    if constexpr (!WONLY) {
+      float2 g = __ffma2_rn(dp, Y, X);  // (dW - D) / Z
+      if (!FULL) {
+        g.x = al0 ? g.x : 0.f;
+        g.y = al1 ? g.y : 0.f;
+      }
+      const float2 gr = __fmul2_rn(g, rd);
+      const float2 a = __fmul2_rn(gr, __fmul2_rn(nodd, make_float2(2.f * YM, 2.f * YM)));
+      const float2 ne = __fmul2_rn(gr, kap);  // -e
+      const float2 nea = make_float2(a0 ? ne.x : 0.f, a1 ? ne.y : 0.f);
+      c = __ffma2_rn(nea, make_float2(2.f, 2.f), a);
+      acc0 = __fadd2_rn(acc0, nea);
+      acc1 = __fadd2_rn(acc1, a);
+      acc2 = __fadd2_rn(acc2, ne);
+    }
   }
 }
 
@@ -267,21 +316,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int lane = threadIdx.x & 31;
 
   const uint32_t bar0 = sb + L::OFF_BAR;
+  constexpr int NS = L::NS;
   const uint32_t bar_r_full = bar0;
-  auto x_full = [&](int b) { return bar0 + 8u * (1 + b); };
-  auto x_empty = [&](int b) { return bar0 + 8u * (3 + b); };
-  auto s_full = [&](int b) { return bar0 + 8u * (5 + b); };
-  auto s_empty = [&](int b) { return bar0 + 8u * (7 + b); };
-  auto wc_full = [&](int b) { return bar0 + 8u * (9 + b); };
-  auto wc_empty = [&](int b) { return bar0 + 8u * (11 + b); };
-  const uint32_t bar_acc = bar0 + 8u * 13;
-  const uint32_t bar_drain = bar0 + 8u * 14;
+  auto x_full = [&](int st) { return bar0 + 8u * (1 + st); };
+  auto x_empty = [&](int st) { return bar0 + 8u * (1 + NS + st); };
+  auto s_full = [&](int b) { return bar0 + 8u * (1 + 2 * NS + b); };
+  auto s_empty = [&](int b) { return bar0 + 8u * (3 + 2 * NS + b); };
+  const uint32_t bar_wc_full = bar0 + 8u * (5 + 2 * NS);
+  const uint32_t bar_wc_empty = bar0 + 8u * (6 + 2 * NS);
+  const uint32_t bar_acc = bar0 + 8u * (7 + 2 * NS);
+  const uint32_t bar_drain = bar0 + 8u * (8 + 2 * NS);
   const uint32_t r_smem = sb + L::OFF_R, rp_smem = sb + L::OFF_RP;
-  auto x_smem = [&](int b) { return sb + L::OFF_ST + (uint32_t)b * L::STAGE; };
-  auto xp_smem = [&](int b) { return x_smem(b) + L::X_TILE; };
-  auto aux_smem = [&](int b) { return x_smem(b) + 2 * L::X_TILE; };
-  auto w_smem = [&](int b) { return sb + L::OFF_W + (uint32_t)b * L::W_TILE; };
-  auto c_smem = [&](int b) { return sb + L::OFF_C + (uint32_t)b * L::W_TILE; };
+  auto x_smem = [&](int st) { return sb + L::OFF_ST + (uint32_t)st * L::STAGE; };
+  auto xp_smem = [&](int st) { return x_smem(st) + L::X_TILE; };
+  auto aux_smem = [&](int st) { return x_smem(st) + 2 * L::X_TILE; };
+  const uint32_t w_smem = sb + L::OFF_W, c_smem = sb + L::OFF_C;
   float *xch = reinterpret_cast<float *>(smem + L::OFF_XCH);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
@@ -320,16 +369,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_r_full, 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(x_full(b), 1);
+    for (int st = 0; st < NS; ++st) {
+      mbar_init(x_full(st), 1);
       // DP: released by the map warps (lane 0 of each) once they have read the
       // stage's key norms; else by the commit after the tile's last MMA
-      mbar_init(x_empty(b), DP ? MAP_WARPS : 1);
+      mbar_init(x_empty(st), DP ? MAP_WARPS : 1);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
       mbar_init(s_empty(b), MAP_WARPS * 32);
-      mbar_init(wc_full(b), MAP_WARPS * 32);
-      mbar_init(wc_empty(b), 1);
     }
+    mbar_init(bar_wc_full, MAP_WARPS * 32);
+    mbar_init(bar_wc_empty, 1);
     mbar_init(bar_acc, 1);
     mbar_init(bar_drain, 1);
     *abort = 0;
@@ -361,54 +412,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr uint32_t AUXB = KV ? CT * 16 : (VARIANT == kYat ? CT * 4 : 0);
       int issued = 0;
       for (int n = 0; n < n_tiles; ++n) {
-        const int b = n & 1;
-        if (n >= 2 && !thread_wait(x_empty(b), ((n >> 1) & 1) ^ 1, abort, SITE_PRODUCER | 0x10))
+        const int st = n % NS;
+        if (n >= NS &&
+            !thread_wait(x_empty(st), ((n / NS) & 1) ^ 1, abort, SITE_PRODUCER | 0x10))
           break;
         int bh_x, row0, head;
         stream_tile(n, bh_x, row0, head);
-        mbar_arrive_expect_tx(x_full(b), 2u * L::X_TILE + AUXB);
+        mbar_arrive_expect_tx(x_full(st), 2u * L::X_TILE + AUXB);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(x_smem(b) + c * CT * 128, &tm_x, c * 64, row0, bh_x, x_full(b));
-          tma_load_3d(xp_smem(b) + c * CT * 128, &tm_xp, c * 64, row0, bh_x, x_full(b));
+          tma_load_3d(x_smem(st) + c * CT * 128, &tm_x, c * 64, row0, bh_x, x_full(st));
+          tma_load_3d(xp_smem(st) + c * CT * 128, &tm_xp, c * 64, row0, bh_x, x_full(st));
         }
         if constexpr (KV) {
-          bulk_load(aux_smem(b), p.aux + (size_t)bh_x * p.Tq_pad + row0, AUXB, x_full(b));
+          bulk_load(aux_smem(st), p.aux + (size_t)bh_x * p.Tq_pad + row0, AUXB, x_full(st));
         } else if constexpr (VARIANT == kYat) {
-          bulk_load(aux_smem(b), p.nk + (size_t)bh_x * p.Tk_pad + row0, AUXB, x_full(b));
+          bulk_load(aux_smem(st), p.nk + (size_t)bh_x * p.Tk_pad + row0, AUXB, x_full(st));
         }
         issued = n + 1;
       }
       // copies still in flight land before the CTA can exit
       thread_wait(bar_r_full, 0, abort, SITE_PRODUCER | 0x20, false);
-      for (int m = issued >= 2 ? issued - 2 : 0; m < issued; ++m)
-        thread_wait(x_full(m & 1), (m >> 1) & 1, abort, SITE_PRODUCER | 0x30, false);
+      for (int m = issued >= NS ? issued - NS : 0; m < issued; ++m)
+        thread_wait(x_full(m % NS), (m / NS) & 1, abort, SITE_PRODUCER | 0x30, false);
     }
   } else if (warp == MMA_WARP) {
     if (lane == 0) {
       bool ok = thread_wait(bar_r_full, 0, abort, SITE_MMA | 0x10);
       auto do_acc = [&](int m) -> bool {
-        const int b = m & 1;
-        if (!thread_wait(wc_full(b), (m >> 1) & 1, abort, SITE_MMA | 0x20)) return false;
+        const int st = m % NS;
+        if (!thread_wait(bar_wc_full, m & 1, abort, SITE_MMA | 0x20)) return false;
         tc_fence_after();
         if constexpr (KV) {
-          issue_acc<D>(tmem + TM_A1, w_smem(b), xp_smem(b), m > 0);      // dV += W^T dout
-          issue_acc<D>(tmem + TM_A1 + D, c_smem(b), x_smem(b), m > 0);  // dK += C^T Q
+          issue_acc<D>(tmem + TM_A1, w_smem, xp_smem(st), m > 0);      // dV += W^T dout
+          issue_acc<D>(tmem + TM_A1 + D, c_smem, x_smem(st), m > 0);  // dK += C^T Q
         } else {
-          issue_acc<D>(tmem + TM_A1, c_smem(b), x_smem(b), m > 0);  // dQ += C K
+          issue_acc<D>(tmem + TM_A1, c_smem, x_smem(st), m > 0);  // dQ += C K
         }
-        mma_commit(x_empty(b));
-        mma_commit(wc_empty(b));
+        mma_commit(x_empty(st));
+        mma_commit(bar_wc_empty);
         return true;
       };
       for (int n = 0; ok && n < n_tiles; ++n) {
-        const int b = n & 1;
-        if (!(ok = thread_wait(x_full(b), (n >> 1) & 1, abort, SITE_MMA | 0x30))) break;
+        const int b = n & 1, st = n % NS;
+        if (!(ok = thread_wait(x_full(st), (n / NS) & 1, abort, SITE_MMA | 0x30))) break;
         if (n >= 2 && !(ok = thread_wait(s_empty(b), ((n >> 1) & 1) ^ 1, abort, SITE_MMA | 0x40)))
           break;
         tc_fence_after();
-        issue_scores<D>(tmem + TM_S + 64u * b, r_smem, x_smem(b));
-        issue_scores<D>(tmem + TM_DP + 64u * b, rp_smem, xp_smem(b));
+        issue_scores<D>(tmem + TM_S + 64u * b, r_smem, x_smem(st));
+        issue_scores<D>(tmem + TM_DP + 64u * b, rp_smem, xp_smem(st));
         mma_commit(s_full(b));
         if (!DP && n >= 1) ok = do_acc(n - 1);
       }
@@ -420,7 +472,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // ---- map warps
-    const int qd = warp & 3, hf = warp >> 2;
+    const int qd = warp & 3, hf = warp >> 2;  // lane quadrant, column slice
     const int r = 32 * qd + lane;  // row of the resident tile
     const uint32_t t_lane = tmem + ((uint32_t)(32 * qd) << 16);
     const float scale = p.scale, c2 = p.scale * LOG2E;
@@ -438,10 +490,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (VARIANT != kSoftmax) hp.eps = p.eps[head];
       if (VARIANT == kStau) hp.tau = p.tau[head];
     }
-    float esum = 0.f, g1 = 0.f, g2 = 0.f, dsum = 0.f;
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, dsum = acc0;
     bool ok = true;
     for (int n = 0; n < n_tiles; ++n) {
-      const int b = n & 1;
+      const int b = n & 1, st = n % NS;
       int bh_x, row0, head;
       stream_tile(n, bh_x, row0, head);
       if constexpr (KV) {
@@ -453,83 +505,95 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (!(ok = warp_wait(s_full(b), (n >> 1) & 1, abort, SITE_MAP | 0x10))) break;
       tc_fence_after();
-      uint32_t sr[32], dr[32];
-      tmem_ld32(t_lane + TM_S + 64u * b + 32u * hf, sr);
-      tmem_ld32(t_lane + TM_DP + 64u * b + 32u * hf, dr);
+      uint32_t sr[CW], dr[CW];
+      tmem_ld16(t_lane + TM_S + 64u * b + (uint32_t)(CW * hf), sr);
+      tmem_ld16(t_lane + TM_DP + 64u * b + (uint32_t)(CW * hf), dr);
       tmem_wait_ld();
-      tmem_ld_fence(sr);
-      tmem_ld_fence(dr);
+      tmem_ld_fence16(sr);
+      tmem_ld_fence16(dr);
       tc_fence_before();
       mbar_arrive(s_empty(b));
 
-      const int col0 = row0 + 32 * hf;  // global index of this thread's first column
-      uint32_t wpk[16], cpk[16];
-#pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        float Dt[4], Lt[4], qn[4], nk[4];
-        bool al[4];
-        if constexpr (KV) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint4 a = lds128(aux_smem(b) + 16u * (32 * hf + i + u));
-            Dt[u] = __uint_as_float(a.x);
-            Lt[u] = __uint_as_float(a.y);
-            qn[u] = __uint_as_float(a.z);
-            nk[u] = row_nk;
-            const int t = col0 + i + u;
-            al[u] = t < p.Tq && grow < p.Tk && (!p.causal || grow <= t);
-          }
-        } else {
-          uint4 a = make_uint4(0u, 0u, 0u, 0u);
-          if (VARIANT == kYat) a = lds128(aux_smem(b) + 4u * (32 * hf + i));
-          const float n4[4] = {__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z),
-                               __uint_as_float(a.w)};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            Dt[u] = row_aux.x;
-            Lt[u] = row_aux.y;
-            qn[u] = row_aux.z;
-            nk[u] = n4[u];
-            const int j = col0 + i + u;
-            al[u] = j < p.Tk && grow < p.Tq && (!p.causal || j <= grow);
-          }
-        }
-        float w[4], c[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          pair_grad<VARIANT, YM>(__uint_as_float(sr[i + u]), __uint_as_float(dr[i + u]), Dt[u],
-                                 Lt[u], qn[u], nk[u], hp, scale, c2, al[u], w[u], c[u], esum, g1,
-                                 g2);
-        if constexpr (DP) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) dsum = fmaf(w[u], __uint_as_float(dr[i + u]), dsum);
-        }
-        wpk[i >> 1] = pack_bf16x2(w[0], w[1]);
-        wpk[(i >> 1) + 1] = pack_bf16x2(w[2], w[3]);
-        cpk[i >> 1] = pack_bf16x2(c[0], c[1]);
-        cpk[(i >> 1) + 1] = pack_bf16x2(c[2], c[3]);
+      const int col0 = row0 + CW * hf;  // global index of this thread's first column
+      // warp-uniform: is every pair of this warp's 32 x CW block allowed?
+      bool full;
+      {
+        const int r_lo = rt * RT + 32 * qd, r_hi = r_lo + 31;
+        if constexpr (KV)
+          full = col0 + CW <= p.Tq && r_hi < p.Tk && (!p.causal || col0 >= r_hi);
+        else
+          full = col0 + CW <= p.Tk && r_hi < p.Tq && (!p.causal || col0 + CW - 1 <= r_lo);
       }
+      uint32_t wpk[CW / 2], cpk[CW / 2];
+      auto chunk = [&](auto full_c) {
+        constexpr bool FULL = decltype(full_c)::value;
+#pragma unroll
+        for (int i = 0; i < CW; i += 2) {
+          float2 X, Y, Z = make_float2(0.f, 0.f);
+          bool al0 = true, al1 = true;
+          if constexpr (KV) {
+            const uint4 u0 = lds128(aux_smem(st) + 16u * (CW * hf + i));
+            const uint4 u1 = lds128(aux_smem(st) + 16u * (CW * hf + i + 1));
+            X = make_float2(__uint_as_float(u0.x), __uint_as_float(u1.x));
+            Y = make_float2(__uint_as_float(u0.y), __uint_as_float(u1.y));
+            if (VARIANT == kYat)
+              Z = __fadd2_rn(make_float2(__uint_as_float(u0.z), __uint_as_float(u1.z)),
+                             make_float2(row_nk, row_nk));
+            if (!FULL) {
+              const int t = col0 + i;
+              al0 = t < p.Tq && grow < p.Tk && (!p.causal || grow <= t);
+              al1 = t + 1 < p.Tq && grow < p.Tk && (!p.causal || grow <= t + 1);
+            }
+          } else {
+            X = make_float2(row_aux.x, row_aux.x);
+            Y = make_float2(row_aux.y, row_aux.y);
+            if (VARIANT == kYat) {
+              const uint2 u = lds64(aux_smem(st) + 4u * (CW * hf + i));
+              Z = __fadd2_rn(make_float2(row_aux.z, row_aux.z),
+                             make_float2(__uint_as_float(u.x), __uint_as_float(u.y)));
+            }
+            if (!FULL) {
+              const int j = col0 + i;
+              al0 = j < p.Tk && grow < p.Tq && (!p.causal || j <= grow);
+              al1 = j + 1 < p.Tk && grow < p.Tq && (!p.causal || j + 1 <= grow);
+            }
+          }
+          const float2 sv = tc::f2(sr[i], sr[i + 1]), dv = tc::f2(dr[i], dr[i + 1]);
+          float2 w, c = make_float2(0.f, 0.f);
+          pair2<VARIANT, YM, FULL, DP>(sv, dv, X, Y, Z, hp, scale, c2, al0, al1, w, c, acc0,
+                                       acc1, acc2);
+          if constexpr (DP) dsum = __ffma2_rn(w, dv, dsum);
+          wpk[i >> 1] = pack_bf16x2(w.x, w.y);
+          cpk[i >> 1] = pack_bf16x2(c.x, c.y);
+        }
+      };
+      if (full)
+        chunk(std::true_type{});
+      else
+        chunk(std::false_type{});
       if constexpr (DP) {
         __syncwarp();
-        if (lane == 0) mbar_arrive(x_empty(b));
+        if (lane == 0) mbar_arrive(x_empty(st));
         continue;
       }
-      if (n >= 2 && !(ok = warp_wait(wc_empty(b), ((n >> 1) & 1) ^ 1, abort, SITE_MAP | 0x20)))
-        break;
-      // row r of the 128-byte-swizzled box: logical 16-byte chunk 4 hf + q at
-      // physical chunk (4 hf + q) ^ (r % 8)
+      // the accumulating MMAs of tile n-1 have read the W / C buffer
+      if (n >= 1 && !(ok = warp_wait(bar_wc_empty, (n - 1) & 1, abort, SITE_MAP | 0x20))) break;
+      // row r of the 128-byte-swizzled box: logical 16-byte chunk 2 hf + q at
+      // physical chunk (2 hf + q) ^ (r % 8)
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const uint32_t off = (uint32_t)r * 128u + (uint32_t)(((4 * hf + q4) ^ (r & 7)) * 16);
+      for (int q4 = 0; q4 < CW / 8; ++q4) {
+        const uint32_t off =
+            (uint32_t)r * 128u + (uint32_t)((((CW / 8) * hf + q4) ^ (r & 7)) * 16);
         if constexpr (KV)
-          sts128(w_smem(b) + off, wpk[4 * q4], wpk[4 * q4 + 1], wpk[4 * q4 + 2], wpk[4 * q4 + 3]);
-        sts128(c_smem(b) + off, cpk[4 * q4], cpk[4 * q4 + 1], cpk[4 * q4 + 2], cpk[4 * q4 + 3]);
+          sts128(w_smem + off, wpk[4 * q4], wpk[4 * q4 + 1], wpk[4 * q4 + 2], wpk[4 * q4 + 3]);
+        sts128(c_smem + off, cpk[4 * q4], cpk[4 * q4 + 1], cpk[4 * q4 + 2], cpk[4 * q4 + 3]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(wc_full(b));
+      mbar_arrive(bar_wc_full);
       if constexpr (HAS_PAR) {
         if (n % per_head == per_head - 1) {  // last tile of this query head
-          float a = g1, e = g2;
+          // Yat: (db, deps) = (acc1, -acc2); s^tau: (deps, dtau) = (acc1, acc2 ln 2)
+          float a = acc1.x + acc1.y, e = acc2.x + acc2.y;
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) {
             a += __shfl_xor_sync(FULL, a, o);
@@ -537,26 +601,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if (lane == 0) {
             atomicAdd(p.dpar + 2 * head, (double)a);
-            atomicAdd(p.dpar + 2 * head + 1, (double)e);
+            atomicAdd(p.dpar + 2 * head + 1, (double)(VARIANT == kYat ? -e : e * LN2));
           }
-          g1 = 0.f;
-          g2 = 0.f;
+          acc1 = make_float2(0.f, 0.f);
+          acc2 = acc1;
         }
       }
     }
     if constexpr (DP) {
       // the two column halves' partial sums, then D_t over the aux array's D
-      xch[hf * RT + r] = dsum;
+      xch[hf * RT + r] = dsum.x + dsum.y;
       named_barrier_sync(1, MAP_WARPS * 32);
-      if (ok && hf == 0 && grow < p.Tq)
-        p.aux_w[((size_t)bh_r * p.Tq_pad + grow) * 4] = xch[r] + xch[RT + r];
+      if (ok && hf == 0 && grow < p.Tq) {
+        float D_t = 0.f;
+#pragma unroll
+        for (int x = 0; x < NQ; ++x) D_t += xch[x * RT + r];
+        p.aux_w[((size_t)bh_r * p.Tq_pad + grow) * 4] = VARIANT == kYat ? -D_t * row_aux.y : -D_t;
+      }
     } else {
     // ---- epilogue: accumulators out of TMEM, Yat's rank-one term, bf16 stores
     if (ok) ok = warp_wait(bar_acc, 0, abort, SITE_MAP | 0x30);
+    float esum = 0.f;  // sum e [d2 > 0] over the row (Yat)
     if (VARIANT == kYat) {
-      xch[hf * RT + r] = esum;
+      xch[hf * RT + r] = acc0.x + acc0.y;
       named_barrier_sync(1, MAP_WARPS * 32);
-      esum = xch[r] + xch[RT + r];
+#pragma unroll
+      for (int x = 0; x < NQ; ++x) esum -= xch[x * RT + r];
     }
     if (ok) {
       tc_fence_after();
@@ -571,20 +641,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                      ((size_t)bh_r * p.Tk + grow) * D
                : reinterpret_cast<__nv_bfloat16 *>(p.dq) + ((size_t)bh_r * p.Tq + grow) * D;
 #pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) {
-          const int col = hf * (D / 2) + 32 * cc;  // this thread's 32 accumulator columns
-          uint32_t ar[32];
-          tmem_ld32(t_lane + TM_A1 + (uint32_t)(acc * D + col), ar);
+        for (int cc = 0; cc < D / (16 * NQ); ++cc) {
+          const int col = hf * (D / NQ) + 16 * cc;  // this thread's next 16 accumulator columns
+          uint32_t ar[16];
+          tmem_ld16(t_lane + TM_A1 + (uint32_t)(acc * D + col), ar);
           tmem_wait_ld();
-          tmem_ld_fence(ar);
-          float v[32];
+          tmem_ld_fence16(ar);
+          float v[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(ar[i]);
+          for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(ar[i]);
           if (rank1) {
             // + 2 esum x_row, x_row = this row of the resident tile (k_j or q_t)
             const float f = 2.f * esum;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q4 = 0; q4 < 2; ++q4) {
               const int chunk = ((col & 63) >> 3) + q4;
               const uint4 x = lds128(r_smem + (uint32_t)(col >> 6) * (RT * 128) +
                                      (uint32_t)r * 128u + (uint32_t)((chunk ^ (r & 7)) * 16));
@@ -600,7 +670,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if (row_ok) {
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
+            for (int q4 = 0; q4 < 2; ++q4)
               stg128(dst + col + 8 * q4, pack_bf16x2(v[8 * q4], v[8 * q4 + 1]),
                      pack_bf16x2(v[8 * q4 + 2], v[8 * q4 + 3]),
                      pack_bf16x2(v[8 * q4 + 4], v[8 * q4 + 5]),
@@ -620,17 +690,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-// Per query row: D = dout . out (softmax; the other maps take D from the
-// row-sum pass), the normaliser (softmax, s^tau: row_mass
-// log2 e, the log2 of Z; Yat: 1 / (row_mass + 1e-9)) and |q|^2 (Yat); zeros
-// for the padding rows up to Tq_pad.  Eight lanes per row.
+// Per query row, the scalars the map warps read (zeros for the padding rows
+// up to Tq_pad): softmax (-D scale, -log2 Z, 0) with D = dout . out; s^tau
+// (0, -log2 Z, 0); Yat (0, 1 / Z, |q|^2 + eps), Z = row_mass + 1e-9.  The
+// row-sum pass fills the first field for Yat (-D / Z) and s^tau (-D).
+// Eight lanes per row.
 template <int VARIANT, int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__restrict__ q,
                                                        const __nv_bfloat16 *__restrict__ out,
                                                        const __nv_bfloat16 *__restrict__ dout,
                                                        const float *__restrict__ row_mass,
-                                                       float4 *__restrict__ aux, int BH, int Tq,
-                                                       int Tq_pad) {
+                                                       const float *__restrict__ eps,
+                                                       float4 *__restrict__ aux, int BH, int h,
+                                                       int Tq, int Tq_pad, float scale) {
   const long long row = ((long long)blockIdx.x * 256 + threadIdx.x) >> 3;
   const int sub = threadIdx.x & 7;
   const bool live = row < (long long)BH * Tq_pad;
@@ -638,18 +710,20 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
   const int t = live ? (int)(row % Tq_pad) : 0;
   const bool valid = live && t < Tq;
   float dsum = 0.f, qsum = 0.f;
-  if (valid) {
+  if (valid && VARIANT != kStau) {
     const size_t base = ((size_t)bh * Tq + t) * D;
 #pragma unroll
     for (int c = sub * 8; c < D; c += 64) {
-      const uint4 o4 = *reinterpret_cast<const uint4 *>(out + base + c);
-      const uint4 d4 = *reinterpret_cast<const uint4 *>(dout + base + c);
-      const uint32_t os[4] = {o4.x, o4.y, o4.z, o4.w}, ds[4] = {d4.x, d4.y, d4.z, d4.w};
+      if constexpr (VARIANT == kSoftmax) {
+        const uint4 o4 = *reinterpret_cast<const uint4 *>(out + base + c);
+        const uint4 d4 = *reinterpret_cast<const uint4 *>(dout + base + c);
+        const uint32_t os[4] = {o4.x, o4.y, o4.z, o4.w}, ds[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        dsum = fmaf(__uint_as_float(os[u] << 16), __uint_as_float(ds[u] << 16), dsum);
-        dsum = fmaf(__uint_as_float(os[u] & 0xffff0000u), __uint_as_float(ds[u] & 0xffff0000u),
-                    dsum);
+        for (int u = 0; u < 4; ++u) {
+          dsum = fmaf(__uint_as_float(os[u] << 16), __uint_as_float(ds[u] << 16), dsum);
+          dsum = fmaf(__uint_as_float(os[u] & 0xffff0000u), __uint_as_float(ds[u] & 0xffff0000u),
+                      dsum);
+        }
       }
       if constexpr (VARIANT == kYat) {
         const uint4 q4 = *reinterpret_cast<const uint4 *>(q + base + c);
@@ -672,9 +746,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     if (valid) {
       const float m = row_mass[(size_t)bh * Tq + t];
-      a.x = dsum;
-      a.y = VARIANT == kYat ? 1.f / (m + 1e-9f) : m * LOG2E;
-      a.z = qsum;
+      a.x = VARIANT == kSoftmax ? -dsum * scale : 0.f;  // the others: the row-sum pass
+      a.y = VARIANT == kYat ? 1.f / (m + 1e-9f) : -m * LOG2E;
+      a.z = VARIANT == kYat ? qsum + eps[bh % h] : 0.f;
     }
     aux[row] = a;
   }
@@ -743,8 +817,8 @@ cudaError_t launch_prep(const BwdParams &p, const void *q, const void *out, cons
   const unsigned blocks = (unsigned)((rows * 8 + 255) / 256);
   bwd_prep_kernel<VARIANT, D><<<blocks, 256, 0, s>>>(
       static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(out),
-      static_cast<const __nv_bfloat16 *>(dout), row_mass, const_cast<float4 *>(p.aux),
-      p.B * p.h, p.Tq, p.Tq_pad);
+      static_cast<const __nv_bfloat16 *>(dout), row_mass, p.eps, const_cast<float4 *>(p.aux),
+      p.B * p.h, p.h, p.Tq, p.Tq_pad, p.scale);
   return cudaGetLastError();
 }
 
