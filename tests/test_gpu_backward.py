@@ -200,3 +200,26 @@ def test_backward_cfg4_gqa_slice():
                           scale=w.scale, **kw)
     gpu = (dq[bi:bi + 1, heads], dk[bi:bi + 1, g:g + 1], dv[bi:bi + 1, g:g + 1], {})
     compare_grads(gpu, ora[:3] + ({},), "cfg4 stau kv head 5")
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_yat_b_zero_ablation_forward_and_backward(causal):
+    """The Yat page's b = 0 ablation (kappa = (q.k)^2 / (|q - k|^2 + eps)):
+    the same kernels with every b_h = 0, forward and backward against the
+    oracle with b = 0."""
+    w = _wl(1, 4, 2, 257, 257 if causal else 400, 128, causal, seed=41)
+    inp = workloads.generate(w)
+    inp = dict(inp, yat_b=np.zeros_like(inp["yat_b"]))
+    dout = workloads.grad_output(w)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    out, mass, mx = attention.forward("yat", q, k, v, b=inp["yat_b"], eps=inp["yat_eps"],
+                                      causal=causal)
+    torch.cuda.synchronize()
+    ora_f = oracle.forward("yat", inp["q"], inp["k"], inp["v"], b=inp["yat_b"], eps=inp["yat_eps"],
+                           causal=causal)
+    pu.compare("yat", tuple(pu.to_np(t) for t in (out, mass, mx)), ora_f,
+               float(inp["v"].abs().max()), inp["q"].dtype, where=f"yat b=0 causal={causal}")
+    gpu = run_gpu_backward("yat", inp, dout, causal=causal, scale=w.scale)
+    ora = oracle.backward("yat", inp["q"], inp["k"], inp["v"], dout, causal=causal,
+                          **_params("yat", inp))
+    compare_grads(gpu, ora, f"yat b=0 causal={causal}")

@@ -569,3 +569,18 @@ def test_backward_invariants():
     assert all(np.all(x == 0) for x in z[:3])
     dq, _, _, _ = oracle.backward("softmax", q[:, :, :1], k[:, :, :1], v[:, :, :1], do[:, :, :1])
     np.testing.assert_array_equal(dq, 0.0)
+
+
+def test_yat_b_zero_is_squared_cosine_over_distance():
+    # b = 0 (the Yat page's ablation): kappa = (q.k)^2 / (|q - k|^2 + eps), so
+    # a key orthogonal to q gets zero weight and flipping a key's sign changes
+    # only the distance term
+    q = _arr([[[[1.0, 0.0]]]])
+    k = _arr([[[[0.0, 2.0], [3.0, 0.0], [-3.0, 0.0]]]])
+    v = _arr([[[[1.0], [2.0], [4.0]]]])
+    out, mass, _, w = oracle.forward("yat", q, k, v, b=0.0, eps=1.0, return_weights=True)
+    k1 = 9.0 / (4.0 + 1.0)    # q.k = 3, |q - k|^2 = 4
+    k2 = 9.0 / (16.0 + 1.0)   # q.k = -3, |q - k|^2 = 16
+    assert w[0, 0, 0, 0] == 0.0
+    assert mass[0, 0, 0] == pytest.approx(k1 + k2, rel=1e-15)
+    assert out[0, 0, 0, 0] == pytest.approx((2.0 * k1 + 4.0 * k2) / (k1 + k2 + 1e-9), rel=1e-14)
