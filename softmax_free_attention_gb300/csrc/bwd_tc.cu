@@ -123,12 +123,12 @@ struct Layout {
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          unsigned site) {
+                                          unsigned site, bool honor_abort = true) {
   if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
-    const int bad = *abort != 0 || (globaltimer_ns() - t0 > WAIT_LIMIT_NS);
+    const int bad = (honor_abort && *abort != 0) || (globaltimer_ns() - t0 > WAIT_LIMIT_NS);
     if (__any_sync(FULL, bad)) {
       if ((threadIdx.x & 31) == 0) {
         atomicCAS(&g_bwd_status, 0u, site | 1u);
@@ -151,6 +151,27 @@ __device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, volat
       return false;
     }
   }
+}
+
+// The MMA warp runs converged (so that its descriptors can live in uniform
+// registers); one elected lane issues each MMA and each commit.
+__device__ __forceinline__ void mma_ss_e(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_e(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          bar)
+      : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -177,33 +198,36 @@ __device__ __forceinline__ void stg128(void *ptr, uint32_t a, uint32_t b, uint32
                : "memory");
 }
 
-// S[128 x 64] = A[128 x D] B[64 x D]^T: A a resident tile (64-column boxes
-// RT*128 bytes apart), B a streamed tile (boxes CT*128 bytes apart).
+// The MMA lane shares its SM sub-partition with four busy map warps, so its
+// instruction count sets how fast it can issue: descriptors are built once
+// and every MMA adds a compile-time offset to them (the start-address field
+// is the low 14 bits of the descriptor, in 16-byte units; shared-memory
+// offsets stay far below its range).
+
+// S[128 x 64] = A[128 x D] B[64 x D]^T from descriptors of a resident tile
+// (64-column boxes RT*128 bytes apart) and a streamed tile (CT*128 apart).
 template <int D>
-__device__ __forceinline__ void issue_scores(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
+__device__ __forceinline__ void issue_scores(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc) {
   constexpr uint32_t IDESC = idesc_bf16_f32(RT, CT, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t a = a_smem + (uint32_t)(kk >> 2) * (RT * 128) + (uint32_t)(kk & 3) * 32;
-    const uint32_t b = b_smem + (uint32_t)(kk >> 2) * (CT * 128) + (uint32_t)(kk & 3) * 32;
-    mma_ss(d_tmem, smem_desc_sw128(a, 16, 1024), smem_desc_sw128(b, 16, 1024), IDESC,
-           kk > 0 ? 1u : 0u);
+    const uint64_t ao = (uint64_t)(((kk >> 2) * (RT * 128) + (kk & 3) * 32) >> 4);
+    const uint64_t bo = (uint64_t)(((kk >> 2) * (CT * 128) + (kk & 3) * 32) >> 4);
+    mma_ss_e(d_tmem, adesc + ao, bdesc + bo, IDESC, kk > 0 ? 1u : 0u);
   }
 }
 
 // Acc[128 x D] (+)= A[128 x 64] B[64 x D]: A the map warps' tile (one 128-byte
-// box per row, K-major), B a streamed tile read N-major (64-column boxes
-// CT*128 bytes apart).
+// box per row, K-major), B a streamed tile read N-major (descriptor with the
+// 64-column boxes CT*128 bytes apart as its leading offset).
 template <int D>
-__device__ __forceinline__ void issue_acc(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
+__device__ __forceinline__ void issue_acc(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc_n,
                                           bool accumulate) {
   constexpr uint32_t IDESC = idesc_bf16_f32(RT, D, true);
 #pragma unroll
-  for (int kk = 0; kk < CT / 16; ++kk) {
-    mma_ss(d_tmem, smem_desc_sw128(a_smem + (uint32_t)kk * 32, 16, 1024),
-           smem_desc_sw128(b_smem + (uint32_t)kk * 2048, CT * 128, 1024), IDESC,
-           (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 0; kk < CT / 16; ++kk)
+    mma_ss_e(d_tmem, adesc + (uint64_t)((kk * 32) >> 4), bdesc_n + (uint64_t)((kk * 2048) >> 4),
+           IDESC, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 struct HeadP {
@@ -437,38 +461,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         thread_wait(x_full(m % NS), (m / NS) & 1, abort, SITE_PRODUCER | 0x30, false);
     }
   } else if (warp == MMA_WARP) {
-    if (lane == 0) {
-      bool ok = thread_wait(bar_r_full, 0, abort, SITE_MMA | 0x10);
+    {
+      bool ok = warp_wait(bar_r_full, 0, abort, SITE_MMA | 0x10);
+      // descriptors: K-major views of the resident tiles, the W / C tiles and
+      // stage 0's streamed tiles; N-major views of stage 0's streamed tiles
+      const uint64_t dR = smem_desc_sw128(r_smem, 16, 1024);
+      const uint64_t dRP = smem_desc_sw128(rp_smem, 16, 1024);
+      const uint64_t dW = smem_desc_sw128(w_smem, 16, 1024);
+      const uint64_t dC = smem_desc_sw128(c_smem, 16, 1024);
+      const uint64_t dX0 = smem_desc_sw128(x_smem(0), 16, 1024);
+      const uint64_t dXP0 = smem_desc_sw128(xp_smem(0), 16, 1024);
+      const uint64_t nX0 = smem_desc_sw128(x_smem(0), CT * 128, 1024);
+      const uint64_t nXP0 = smem_desc_sw128(xp_smem(0), CT * 128, 1024);
+      auto stage_off = [](int st) { return (uint64_t)((st * L::STAGE) >> 4); };
       auto do_acc = [&](int m) -> bool {
         const int st = m % NS;
-        if (!thread_wait(bar_wc_full, m & 1, abort, SITE_MMA | 0x20)) return false;
+        if (!warp_wait(bar_wc_full, m & 1, abort, SITE_MMA | 0x20)) return false;
         tc_fence_after();
         if constexpr (KV) {
-          issue_acc<D>(tmem + TM_A1, w_smem, xp_smem(st), m > 0);      // dV += W^T dout
-          issue_acc<D>(tmem + TM_A1 + D, c_smem, x_smem(st), m > 0);  // dK += C^T Q
+          issue_acc<D>(tmem + TM_A1, dW, nXP0 + stage_off(st), m > 0);     // dV += W^T dout
+          issue_acc<D>(tmem + TM_A1 + D, dC, nX0 + stage_off(st), m > 0);  // dK += C^T Q
         } else {
-          issue_acc<D>(tmem + TM_A1, c_smem, x_smem(st), m > 0);  // dQ += C K
+          issue_acc<D>(tmem + TM_A1, dC, nX0 + stage_off(st), m > 0);  // dQ += C K
         }
-        mma_commit(x_empty(st));
-        mma_commit(bar_wc_empty);
+        mma_commit_e(x_empty(st));
+        mma_commit_e(bar_wc_empty);
         return true;
       };
       for (int n = 0; ok && n < n_tiles; ++n) {
         const int b = n & 1, st = n % NS;
-        if (!(ok = thread_wait(x_full(st), (n / NS) & 1, abort, SITE_MMA | 0x30))) break;
-        if (n >= 2 && !(ok = thread_wait(s_empty(b), ((n >> 1) & 1) ^ 1, abort, SITE_MMA | 0x40)))
+        if (!(ok = warp_wait(x_full(st), (n / NS) & 1, abort, SITE_MMA | 0x30))) break;
+        if (n >= 2 && !(ok = warp_wait(s_empty(b), ((n >> 1) & 1) ^ 1, abort, SITE_MMA | 0x40)))
           break;
         tc_fence_after();
-        issue_scores<D>(tmem + TM_S + 64u * b, r_smem, x_smem(st));
-        issue_scores<D>(tmem + TM_DP + 64u * b, rp_smem, xp_smem(st));
-        mma_commit(s_full(b));
+        issue_scores<D>(tmem + TM_S + 64u * b, dR, dX0 + stage_off(st));
+        issue_scores<D>(tmem + TM_DP + 64u * b, dRP, dXP0 + stage_off(st));
+        mma_commit_e(s_full(b));
         if (!DP && n >= 1) ok = do_acc(n - 1);
       }
       if (!DP && ok && n_tiles > 0) ok = do_acc(n_tiles - 1);
-      if (!DP && ok) mma_commit(bar_acc);
+      if (!DP && ok) mma_commit_e(bar_acc);
       // every MMA this thread issued has completed once `drain` flips
-      mma_commit(bar_drain);
-      thread_wait(bar_drain, 0, abort, SITE_MMA | 0x50, false);
+      mma_commit_e(bar_drain);
+      warp_wait(bar_drain, 0, abort, SITE_MMA | 0x50, false);
     }
   } else {
     // ---- map warps
