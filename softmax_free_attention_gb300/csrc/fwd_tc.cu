@@ -178,40 +178,44 @@ __device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, volat
 
 // S = Q K^T for one 128 x 128 tile from prebuilt descriptors of the Q tile
 // and the K slot: 16-element k steps, 64-column boxes.
-template <int DK>
+// CONV: issued by a converged MMA warp (elected lane), else by one lane.
+template <int DK, bool CONV = false>
 __device__ __forceinline__ void issue_qk_d(uint32_t d_tmem, uint64_t qdesc, uint64_t kdesc) {
   constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, false);
 #pragma unroll
   for (int kk = 0; kk < DK / 16; ++kk) {
     const uint64_t qo = (uint64_t)(((kk >> 2) * (BM * 128) + (kk & 3) * 32) >> 4);
     const uint64_t ko = (uint64_t)(((kk >> 2) * (BN * 128) + (kk & 3) * 32) >> 4);
-    mma_ss(d_tmem, qdesc + qo, kdesc + ko, IDESC, kk > 0 ? 1u : 0u);
+    if constexpr (CONV)
+      mma_ss_e(d_tmem, qdesc + qo, kdesc + ko, IDESC, kk > 0 ? 1u : 0u);
+    else
+      mma_ss(d_tmem, qdesc + qo, kdesc + ko, IDESC, kk > 0 ? 1u : 0u);
   }
 }
 
 // Half of O += P V: PART 0 takes keys [0, 32) and [64, 96) (the first
 // 32-key chunk of each column half, which the map warps finish first), PART 1
 // the other two chunks.
-template <int DV, int PART>
+template <int DV, int PART, bool CONV = false>
 __device__ __forceinline__ void issue_pv_part(uint32_t d_tmem, uint32_t p_tmem, uint64_t vdesc,
                                               bool accumulate) {
   constexpr uint32_t IDESC = idesc_bf16_f32(BM, DV, true);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int kk = (i >> 1) * 4 + PART * 2 + (i & 1);
-    mma_ts(d_tmem, p_tmem + (uint32_t)(kk >> 2) * 64 + (uint32_t)(kk & 3) * 8,
+    (CONV ? mma_ts_e : mma_ts)(d_tmem, p_tmem + (uint32_t)(kk >> 2) * 64 + (uint32_t)(kk & 3) * 8,
            vdesc + (uint64_t)((kk * 2048) >> 4), IDESC, (accumulate || PART == 1 || i > 0) ? 1u : 0u);
   }
 }
 
 // O += P V from a prebuilt descriptor of the V slot.
-template <int DV>
+template <int DV, bool CONV = false>
 __device__ __forceinline__ void issue_pv_d(uint32_t d_tmem, uint32_t p_tmem, uint64_t vdesc,
                                            bool accumulate) {
   constexpr uint32_t IDESC = idesc_bf16_f32(BM, DV, true);
 #pragma unroll
   for (int kk = 0; kk < BN / 16; ++kk) {
-    mma_ts(d_tmem, p_tmem + (uint32_t)(kk >> 2) * 64 + (uint32_t)(kk & 3) * 8,
+    (CONV ? mma_ts_e : mma_ts)(d_tmem, p_tmem + (uint32_t)(kk >> 2) * 64 + (uint32_t)(kk & 3) * 8,
            vdesc + (uint64_t)((kk * 2048) >> 4), IDESC, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
@@ -486,12 +490,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ MMA issue
-    // One lane issues.  Per unit, iteration j: PV0(j-1) S0(j) PV1(j-1) S1(j).
+    // Per unit, iteration j: PV0(j-1) S0(j) PV1(j-1) S1(j).  The softmax
+    // forward runs the warp converged with an elected lane issuing each MMA
+    // and commit (its descriptors then live in uniform registers, which
+    // measured 8% faster); the other maps issue from lane 0 alone, which
+    // measured about 1% faster for them (their split PV adds waits, each
+    // polled by every lane of a converged warp).
     // The next unit's S MMAs follow the last PVs of this one directly; its
     // first PV_x waits until the map warps have read O_x out.  Shared-memory
     // descriptors are built once; a slot's descriptor is the base plus the
     // slot offset in 16-byte units.
-    if (lane == 0) {
+    constexpr bool CONV = VARIANT == kSoftmax && !STATS;
+    auto mwait = [&](uint32_t bar, uint32_t parity, unsigned site, bool honor = true) {
+      return CONV ? warp_wait(bar, parity, abort, site, honor)
+                  : thread_wait(bar, parity, abort, site, honor);
+    };
+    auto mcommit = [&](uint32_t bar) {
+      if constexpr (CONV)
+        mma_commit_e(bar);
+      else
+        mma_commit(bar);
+    };
+    if (CONV || lane == 0) {
       const uint64_t dq0 = smem_desc_sw128(q_smem(0), 16, 1024);
       const uint64_t dq1 = smem_desc_sw128(q_smem(1), 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(slot_smem(0), 16, 1024);
@@ -503,74 +523,76 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int ms = 0;  // running MMA iteration
 #endif
       for (uint32_t uc = 0; ok; ++uc) {
-        if (!thread_wait(unit_full(uc & 1u), (uc >> 1) & 1u, abort, SITE_MMA | 0x70)) break;
+        if (!mwait(unit_full(uc & 1u), (uc >> 1) & 1u, SITE_MMA | 0x70)) break;
         const int u = unit_ring[uc & 1u];
         if (u < 0) break;
         const Unit t = decode_unit(p, u);
-        mbar_arrive(unit_empty(uc & 1u));  // the unit is decoded
-        if (!(ok = thread_wait(bar_q_full, uc & 1u, abort, SITE_MMA | 0x10))) break;
+        if (CONV) __syncwarp();
+        if (!CONV || lane == 0) mbar_arrive(unit_empty(uc & 1u));  // the unit is decoded
+        if (!(ok = mwait(bar_q_full, uc & 1u, SITE_MMA | 0x10))) break;
         for (int j = 0; ok && j <= t.nkv; ++j) {
           const uint32_t vpos = kv_pos + 2u * j - 1u, vs = vpos % L::NS;
           const uint32_t kpos = kv_pos + STEP * j, ks = kpos % L::NS;
           if (HAS_V && j >= 1 &&
-              !(ok = thread_wait(kv_full(vs), (vpos / L::NS) & 1u, abort, SITE_MMA | 0x20)))
+              !(ok = mwait(kv_full(vs), (vpos / L::NS) & 1u, SITE_MMA | 0x20)))
             break;
 #pragma unroll
           for (int x = 0; x < 2; ++x) {
             if (!HAS_V) {  // tau*: S_x(j) may land once the map warps have read S_x(j-1)
               if (j >= 1 && j - 1 < t.n[x]) {
-                if (!(ok = thread_wait(p_full(x), (pph >> x) & 1u, abort, SITE_MMA | 0x30))) break;
+                if (!(ok = mwait(p_full(x), (pph >> x) & 1u, SITE_MMA | 0x30))) break;
                 pph ^= 1u << x;
               }
             } else if (j >= 1 && j - 1 < t.n[x] && SPLIT_PV) {  // O_x += P_x(j-1) V(j-1), in two halves
-              if (!(ok = thread_wait(p_half(x), (pph >> x) & 1u, abort, SITE_MMA | 0x34))) break;
+              if (!(ok = mwait(p_half(x), (pph >> x) & 1u, SITE_MMA | 0x34))) break;
               if (j == 1 &&
-                  !(ok = thread_wait(o_empty(x), ((ou >> x) & 1u) ^ 1u, abort, SITE_MMA | 0x50)))
+                  !(ok = mwait(o_empty(x), ((ou >> x) & 1u) ^ 1u, SITE_MMA | 0x50)))
                 break;
               tc_fence_after();
 #ifdef CATTN_TRACE
               CATTN_TR(4 + 2 * x, ms);
 #endif
-              issue_pv_part<DV, 0>(tmem + TM_O + 128u * x, tmem + TM_S + 128u * x,
+              issue_pv_part<DV, 0, CONV>(tmem + TM_O + 128u * x, tmem + TM_S + 128u * x,
                                    dv0 + vs * SLOT16, j > 1);
-              if (!(ok = thread_wait(p_full(x), (pph >> x) & 1u, abort, SITE_MMA | 0x30))) break;
+              if (!(ok = mwait(p_full(x), (pph >> x) & 1u, SITE_MMA | 0x30))) break;
               pph ^= 1u << x;
               tc_fence_after();
-              issue_pv_part<DV, 1>(tmem + TM_O + 128u * x, tmem + TM_S + 128u * x,
+              issue_pv_part<DV, 1, CONV>(tmem + TM_O + 128u * x, tmem + TM_S + 128u * x,
                                    dv0 + vs * SLOT16, true);
-              if (j == t.n[x]) mma_commit(o_full(x));
+              if (j == t.n[x]) mcommit(o_full(x));
             } else if (j >= 1 && j - 1 < t.n[x]) {  // O_x += P_x(j-1) V(j-1)
-              if (!(ok = thread_wait(p_full(x), (pph >> x) & 1u, abort, SITE_MMA | 0x30))) break;
+              if (!(ok = mwait(p_full(x), (pph >> x) & 1u, SITE_MMA | 0x30))) break;
               pph ^= 1u << x;
               if (j == 1 &&
-                  !(ok = thread_wait(o_empty(x), ((ou >> x) & 1u) ^ 1u, abort, SITE_MMA | 0x50)))
+                  !(ok = mwait(o_empty(x), ((ou >> x) & 1u) ^ 1u, SITE_MMA | 0x50)))
                 break;
               tc_fence_after();
 #ifdef CATTN_TRACE
               CATTN_TR(4 + 2 * x, ms);
 #endif
-              issue_pv_d<DV>(tmem + TM_O + 128u * x, tmem + TM_S + 128u * x, dv0 + vs * SLOT16,
+              issue_pv_d<DV, CONV>(tmem + TM_O + 128u * x, tmem + TM_S + 128u * x, dv0 + vs * SLOT16,
                              j > 1);
-              if (j == t.n[x]) mma_commit(o_full(x));
+              if (j == t.n[x]) mcommit(o_full(x));
             }
             if (x == 0 && j < t.nkv &&
-                !(ok = thread_wait(kv_full(ks), (kpos / L::NS) & 1u, abort, SITE_MMA | 0x40)))
+                !(ok = mwait(kv_full(ks), (kpos / L::NS) & 1u, SITE_MMA | 0x40)))
               break;
             if (j < t.n[x]) {  // S_x = Q_x K(j)^T
               tc_fence_after();
 #ifdef CATTN_TRACE
               CATTN_TR(5 + 2 * x, ms);
 #endif
-              issue_qk_d<DK>(tmem + TM_S + 128u * x, x ? dq1 : dq0, dk0 + ks * SLOT16);
-              mma_commit(s_full(x));
+              issue_qk_d<DK, CONV>(tmem + TM_S + 128u * x, x ? dq1 : dq0, dk0 + ks * SLOT16);
+              mcommit(s_full(x));
             }
           }
           if (!ok) break;
-          if (j == t.nkv - 1) mma_commit(bar_q_empty);  // the unit's last S MMAs
-          if (j < t.nkv) mma_commit(kv_empty(ks));
-          if (HAS_V && j >= 1) mma_commit(kv_empty(vs));
+          if (j == t.nkv - 1) mcommit(bar_q_empty);  // the unit's last S MMAs
+          if (j < t.nkv) mcommit(kv_empty(ks));
+          if (HAS_V && j >= 1) mcommit(kv_empty(vs));
           // every map warp delivered P for tile j-1, so all are done with its key norms
-          if (VARIANT == kYat && j >= 1) mbar_arrive(nk_empty((nk_pos + j - 1) % NKS));
+          if (VARIANT == kYat && j >= 1 && (!CONV || lane == 0))
+            mbar_arrive(nk_empty((nk_pos + j - 1) % NKS));
 #ifdef CATTN_TRACE
           ++ms;
 #endif
@@ -581,8 +603,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       // all MMAs issued by this thread have completed once `drain` flips; this
       // wait ignores the abort flag so TMEM is never released under a live MMA
-      mma_commit(bar_drain);
-      thread_wait(bar_drain, 0, abort, SITE_MMA | 0x60, false);
+      mcommit(bar_drain);
+      mwait(bar_drain, 0, SITE_MMA | 0x60, false);
     }
   } else if (warp < MAP_WARPS) {
     // ------------------------------------------------------------ map warps
