@@ -245,8 +245,8 @@ int cattn_row_stats(int variant, const cattn_problem_t *p, const void *q, const 
  *   dq, dk, dv    bf16, shaped like q, k, v; written, never read
  *   db, deps, dtau  fp32 [h] or NULL: the parameter gradients the map has
  *                 (Yat: db, deps; s^tau: deps, dtau; the others untouched)
- * bf16 only, dk == dv in {64, 128}, yat_m in {0, 1, 2, 3}; anything else is
- * CATTN_ERR_UNSUPPORTED.  A problem with no query rows writes zeros.  The
+ * bf16 only, (dk, dv) in {(64, 64), (128, 128), (128, 64)}, yat_m in
+ * {0, 1, 2, 3}; anything else is CATTN_ERR_UNSUPPORTED.  A problem with no query rows writes zeros.  The
  * kernels' accumulation order is fixed: repeated calls give identical bits
  * for dq, dk and dv (the fp64 parameter sums use atomics).
  * cattn_backward_workspace_bytes: bytes needed (0 if the problem is

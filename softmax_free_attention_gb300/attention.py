@@ -220,7 +220,8 @@ def backward(variant, q, k, v, out, dout, row_mass, *, b=None, eps=None, tau=Non
     """Gradients of sum(dout * out) for the forward that produced ``out`` and
     ``row_mass`` from the same inputs and map.
 
-    bf16 CUDA tensors, dk == dv in {64, 128}.  Returns (dq, dk, dv, dparams):
+    bf16 CUDA tensors, (dk, dv) in {(64, 64), (128, 128), (128, 64)}.  Returns
+    (dq, dk, dv, dparams):
     dq, dk, dv bf16 shaped like q, k, v (GQA: dk, dv summed over the query
     heads sharing a kv head); dparams a dict of fp32 [h] tensors -- Yat:
     'b', 'eps'; s^tau: 'eps', 'tau'; softmax: empty.  Runs asynchronously on
@@ -239,7 +240,8 @@ def backward(variant, q, k, v, out, dout, row_mass, *, b=None, eps=None, tau=Non
     lib = native.load()
     need = int(lib.cattn_backward_workspace_bytes(vid, ctypes.byref(prob)))
     if need == 0:
-        raise ValueError("unsupported problem for the backward (bf16, dk == dv in {64, 128})")
+        raise ValueError("unsupported problem for the backward "
+                         "(bf16, (dk, dv) in {(64, 64), (128, 128), (128, 64)})")
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     bt = _per_head(b, h, dev, "b") if vid == native.YAT else None

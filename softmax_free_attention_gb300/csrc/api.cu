@@ -540,19 +540,21 @@ int cattn_backward(int variant, const cattn_problem_t *p, const void *q, const v
         CATTN_OK)
       return rc;
   }
-  if ((rc = map_cuda(launch_bwd_prep(variant, p->dk, bp, q, out, dout, row_mass, s))) != CATTN_OK)
+  if ((rc = map_cuda(launch_bwd_prep(variant, p->dk, p->dv, bp, q, out, dout, row_mass, s))) !=
+      CATTN_OK)
     return rc;
   BwdMaps m;
-  const int BH = p->B * p->h, BHK = p->B * p->hkv, d = p->dk;
-  if ((rc = encode_bf16_3d(&m.q128, q, d, p->Tq, BH, 128)) != CATTN_OK) return rc;
-  if ((rc = encode_bf16_3d(&m.do128, dout, d, p->Tq, BH, 128)) != CATTN_OK) return rc;
-  if ((rc = encode_bf16_3d(&m.k128, k, d, p->Tk, BHK, 128)) != CATTN_OK) return rc;
-  if ((rc = encode_bf16_3d(&m.v128, v, d, p->Tk, BHK, 128)) != CATTN_OK) return rc;
-  if ((rc = encode_bf16_3d(&m.q64, q, d, p->Tq, BH, 64)) != CATTN_OK) return rc;
-  if ((rc = encode_bf16_3d(&m.do64, dout, d, p->Tq, BH, 64)) != CATTN_OK) return rc;
-  if ((rc = encode_bf16_3d(&m.k64, k, d, p->Tk, BHK, 64)) != CATTN_OK) return rc;
-  if ((rc = encode_bf16_3d(&m.v64, v, d, p->Tk, BHK, 64)) != CATTN_OK) return rc;
-  if ((rc = map_cuda(launch_bwd_tc(variant, d, p->yat_m > 1 ? p->yat_m : 1, bp, m, s))) != CATTN_OK)
+  const int BH = p->B * p->h, BHK = p->B * p->hkv, dk_ = p->dk, dv_ = p->dv;
+  if ((rc = encode_bf16_3d(&m.q128, q, dk_, p->Tq, BH, 128)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&m.do128, dout, dv_, p->Tq, BH, 128)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&m.k128, k, dk_, p->Tk, BHK, 128)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&m.v128, v, dv_, p->Tk, BHK, 128)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&m.q64, q, dk_, p->Tq, BH, 64)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&m.do64, dout, dv_, p->Tq, BH, 64)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&m.k64, k, dk_, p->Tk, BHK, 64)) != CATTN_OK) return rc;
+  if ((rc = encode_bf16_3d(&m.v64, v, dv_, p->Tk, BHK, 64)) != CATTN_OK) return rc;
+  if ((rc = map_cuda(launch_bwd_tc(variant, dk_, dv_, p->yat_m > 1 ? p->yat_m : 1, bp, m, s))) !=
+      CATTN_OK)
     return rc;
   return map_cuda(launch_bwd_param_finalize(variant, bp.dpar, p->h, db, deps, dtau, s));
 }

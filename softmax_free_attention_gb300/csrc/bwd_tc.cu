@@ -45,7 +45,7 @@
 // the accumulating MMAs of tile n run while they map tile n+1.
 //
 // TMEM (512 columns): S[2] at 0 and 64, dP[2] at 128 and 192, the first
-// accumulator (dV, or dQ) at 256, the second (dK) at 256 + D.
+// accumulator (dV, or dQ) at 256, the second (dK) at 256 + DV.
 //
 // Warp roles (576 threads): warps 0-15 map (warp w: TMEM lanes 32 (w % 4)..+31
 // = rows of the resident tile, tile columns [16 (w / 4), +16); four warps per
@@ -90,12 +90,17 @@ constexpr uint32_t TM_A1 = 256;
 
 enum : unsigned { SITE_PRODUCER = 0x1100, SITE_MMA = 0x1200, SITE_MAP = 0x1300 };
 
-template <int D, int SIDE>
+// DK: width of q and k rows; DV: width of v and dout rows.  The resident tile
+// R and the streamed tile X have rows of DK (K and Q, or Q and K), their
+// partners RP and XP rows of DV (V and dout, or dout and V).
+template <int DK, int DV, int SIDE>
 struct Layout {
-  static constexpr int R_TILE = RT * D * 2;
-  static constexpr int X_TILE = CT * D * 2;
+  static constexpr int R_TILE = RT * DK * 2;
+  static constexpr int RP_TILE = RT * DV * 2;
+  static constexpr int X_TILE = CT * DK * 2;
+  static constexpr int XP_TILE = CT * DV * 2;
   static constexpr int AUX = 1024;  // 64 float4 (SIDE_KV) or 64 floats (SIDE_Q)
-  static constexpr int STAGE = 2 * X_TILE + AUX;
+  static constexpr int STAGE = X_TILE + XP_TILE + AUX;
   static constexpr int W_TILE = RT * CT * 2;  // one 128-byte swizzle box per row
   // Stages of the streamed-tile ring: a stage is held from the tile's S MMAs
   // to its accumulating MMAs, so the ring runs two tiles ahead of the map
@@ -104,7 +109,7 @@ struct Layout {
   static constexpr int NS = SIDE == SIDE_KV ? 3 : 4;
   static constexpr int OFF_R = 0;
   static constexpr int OFF_RP = R_TILE;
-  static constexpr int OFF_ST = 2 * R_TILE;
+  static constexpr int OFF_ST = R_TILE + RP_TILE;
   static constexpr int OFF_W = OFF_ST + NS * STAGE;
   static constexpr int OFF_C = OFF_W + (SIDE == SIDE_KV ? W_TILE : 0);
   static constexpr int OFF_XCH = OFF_C + W_TILE;  // [NQ slices][128] floats
@@ -118,7 +123,8 @@ struct Layout {
   // 512 TMEM columns) never shares the SM
   static constexpr int ALLOC = BYTES + 1024 > 120 * 1024 ? BYTES + 1024 : 120 * 1024;
   static_assert(ALLOC <= 227 * 1024, "shared memory budget");
-  static_assert(STAGE % 1024 == 0 && R_TILE % 1024 == 0 && X_TILE % 1024 == 0,
+  static_assert(STAGE % 1024 == 0 && R_TILE % 1024 == 0 && RP_TILE % 1024 == 0 &&
+                    X_TILE % 1024 == 0 && XP_TILE % 1024 == 0,
                 "swizzle atoms stay 1024-B aligned");
 };
 
@@ -302,12 +308,12 @@ __device__ __forceinline__ void pair2(float2 s, float2 dp, float2 X, float2 Y, f
 
 // DP: the row-sum pass (SIDE_Q only): D_t = sum_j w_tj dW_tj from the
 // backward's own weights, written over the aux array's D; no C, no dQ.
-template <int VARIANT, int D, int SIDE, int YM = 1, bool DP = false>
+template <int VARIANT, int DK, int DV, int SIDE, int YM = 1, bool DP = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tm_r,
                const __grid_constant__ CUtensorMap tm_rp, const __grid_constant__ CUtensorMap tm_x,
                const __grid_constant__ CUtensorMap tm_xp) {
-  using L = Layout<D, SIDE>;
+  using L = Layout<DK, DV, SIDE>;
   constexpr bool KV = SIDE == SIDE_KV;
   static_assert(!DP || SIDE == SIDE_Q, "the row-sum pass runs on the query side");
   constexpr bool HAS_PAR = KV && VARIANT != kSoftmax;
@@ -332,7 +338,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t r_smem = sb + L::OFF_R, rp_smem = sb + L::OFF_RP;
   auto x_smem = [&](int st) { return sb + L::OFF_ST + (uint32_t)st * L::STAGE; };
   auto xp_smem = [&](int st) { return x_smem(st) + L::X_TILE; };
-  auto aux_smem = [&](int st) { return x_smem(st) + 2 * L::X_TILE; };
+  auto aux_smem = [&](int st) { return x_smem(st) + L::X_TILE + L::XP_TILE; };
   const uint32_t w_smem = sb + L::OFF_W, c_smem = sb + L::OFF_C;
   float *xch = reinterpret_cast<float *>(smem + L::OFF_XCH);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
@@ -406,12 +412,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == PRODUCER_WARP) {
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar_r_full, 2u * L::R_TILE);
+      mbar_arrive_expect_tx(bar_r_full, (uint32_t)(L::R_TILE + L::RP_TILE));
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
+      for (int c = 0; c < DK / 64; ++c)
         tma_load_3d(r_smem + c * RT * 128, &tm_r, c * 64, rt * RT, bh_r, bar_r_full);
+#pragma unroll
+      for (int c = 0; c < DV / 64; ++c)
         tma_load_3d(rp_smem + c * RT * 128, &tm_rp, c * 64, rt * RT, bh_r, bar_r_full);
-      }
       constexpr uint32_t AUXB = KV ? CT * 16 : (VARIANT == kYat ? CT * 4 : 0);
       int issued = 0;
       for (int n = 0; n < n_tiles; ++n) {
@@ -421,12 +428,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         int bh_x, row0, head;
         stream_tile(n, bh_x, row0, head);
-        mbar_arrive_expect_tx(x_full(st), 2u * L::X_TILE + AUXB);
+        mbar_arrive_expect_tx(x_full(st), (uint32_t)(L::X_TILE + L::XP_TILE) + AUXB);
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
+        for (int c = 0; c < DK / 64; ++c)
           tma_load_3d(x_smem(st) + c * CT * 128, &tm_x, c * 64, row0, bh_x, x_full(st));
+#pragma unroll
+        for (int c = 0; c < DV / 64; ++c)
           tma_load_3d(xp_smem(st) + c * CT * 128, &tm_xp, c * 64, row0, bh_x, x_full(st));
-        }
         if constexpr (KV) {
           bulk_load(aux_smem(st), p.aux + (size_t)bh_x * p.Tq_pad + row0, AUXB, x_full(st));
         } else if constexpr (VARIANT == kYat) {
@@ -458,10 +466,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!warp_wait(bar_wc_full, m & 1, abort, SITE_MMA | 0x20)) return false;
         tc_fence_after();
         if constexpr (KV) {
-          issue_acc<D>(tmem + TM_A1, dW, nXP0 + stage_off(st), m > 0);     // dV += W^T dout
-          issue_acc<D>(tmem + TM_A1 + D, dC, nX0 + stage_off(st), m > 0);  // dK += C^T Q
+          issue_acc<DV>(tmem + TM_A1, dW, nXP0 + stage_off(st), m > 0);      // dV += W^T dout
+          issue_acc<DK>(tmem + TM_A1 + DV, dC, nX0 + stage_off(st), m > 0);  // dK += C^T Q
         } else {
-          issue_acc<D>(tmem + TM_A1, dC, nX0 + stage_off(st), m > 0);  // dQ += C K
+          issue_acc<DK>(tmem + TM_A1, dC, nX0 + stage_off(st), m > 0);  // dQ += C K
         }
         mma_commit_e(x_empty(st));
         mma_commit_e(bar_wc_empty);
@@ -473,8 +481,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (n >= 2 && !(ok = warp_wait(s_empty(b), ((n >> 1) & 1) ^ 1, abort, SITE_MMA | 0x40)))
           break;
         tc_fence_after();
-        issue_scores<D>(tmem + TM_S + 64u * b, dR, dX0 + stage_off(st));
-        issue_scores<D>(tmem + TM_DP + 64u * b, dRP, dXP0 + stage_off(st));
+        issue_scores<DK>(tmem + TM_S + 64u * b, dR, dX0 + stage_off(st));
+        issue_scores<DV>(tmem + TM_DP + 64u * b, dRP, dXP0 + stage_off(st));
         mma_commit_e(s_full(b));
         if (!DP && n >= 1) ok = do_acc(n - 1);
       }
@@ -645,27 +653,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (ok) {
       tc_fence_after();
       const bool row_ok = KV ? grow < p.Tk : grow < p.Tq;
-      constexpr int NACC = KV ? 2 : 1;
+      // one accumulator: NC columns at TMEM column tcol, rows of dst; rank1:
+      // add 2 esum times this row of the resident tile (k_j or q_t, DK wide)
+      auto emit = [&](auto nc_c, uint32_t tcol, __nv_bfloat16 *dst, bool rank1) {
+        constexpr int NC = decltype(nc_c)::value;
 #pragma unroll
-      for (int acc = 0; acc < NACC; ++acc) {
-        // SIDE_KV: acc 0 = dV (no rank-one term), acc 1 = dK; SIDE_Q: dQ
-        const bool rank1 = VARIANT == kYat && (KV ? acc == 1 : true);
-        __nv_bfloat16 *dst =
-            KV ? reinterpret_cast<__nv_bfloat16 *>(acc == 0 ? p.dv : p.dk) +
-                     ((size_t)bh_r * p.Tk + grow) * D
-               : reinterpret_cast<__nv_bfloat16 *>(p.dq) + ((size_t)bh_r * p.Tq + grow) * D;
-#pragma unroll
-        for (int cc = 0; cc < D / (16 * NQ); ++cc) {
-          const int col = hf * (D / NQ) + 16 * cc;  // this thread's next 16 accumulator columns
+        for (int cc = 0; cc < NC / (16 * NQ); ++cc) {
+          const int col = hf * (NC / NQ) + 16 * cc;  // this thread's next 16 columns
           uint32_t ar[16];
-          tmem_ld16(t_lane + TM_A1 + (uint32_t)(acc * D + col), ar);
+          tmem_ld16(t_lane + tcol + (uint32_t)col, ar);
           tmem_wait_ld();
           tmem_ld_fence16(ar);
           float v[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(ar[i]);
           if (rank1) {
-            // + 2 esum x_row, x_row = this row of the resident tile (k_j or q_t)
             const float f = 2.f * esum;
 #pragma unroll
             for (int q4 = 0; q4 < 2; ++q4) {
@@ -691,6 +693,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                      pack_bf16x2(v[8 * q4 + 6], v[8 * q4 + 7]));
           }
         }
+      };
+      if constexpr (KV) {
+        emit(std::integral_constant<int, DV>{}, TM_A1,
+             reinterpret_cast<__nv_bfloat16 *>(p.dv) + ((size_t)bh_r * p.Tk + grow) * DV, false);
+        emit(std::integral_constant<int, DK>{}, TM_A1 + DV,
+             reinterpret_cast<__nv_bfloat16 *>(p.dk) + ((size_t)bh_r * p.Tk + grow) * DK,
+             VARIANT == kYat);
+      } else {
+        emit(std::integral_constant<int, DK>{}, TM_A1,
+             reinterpret_cast<__nv_bfloat16 *>(p.dq) + ((size_t)bh_r * p.Tq + grow) * DK,
+             VARIANT == kYat);
       }
     }
     }  // !DP
@@ -709,7 +722,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // (0, -log2 Z, 0); Yat (0, 1 / Z, |q|^2 + eps), Z = row_mass + 1e-9.  The
 // row-sum pass fills the first field for Yat (-D / Z) and s^tau (-D).
 // Eight lanes per row.
-template <int VARIANT, int D>
+template <int VARIANT, int DK, int DV>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__restrict__ q,
                                                        const __nv_bfloat16 *__restrict__ out,
                                                        const __nv_bfloat16 *__restrict__ dout,
@@ -724,11 +737,11 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
   const int t = live ? (int)(row % Tq_pad) : 0;
   const bool valid = live && t < Tq;
   float dsum = 0.f, qsum = 0.f;
-  if (valid && VARIANT != kStau) {
-    const size_t base = ((size_t)bh * Tq + t) * D;
+  if (valid && VARIANT == kSoftmax) {
+    const size_t base = ((size_t)bh * Tq + t) * DV;
 #pragma unroll
-    for (int c = sub * 8; c < D; c += 64) {
-      if constexpr (VARIANT == kSoftmax) {
+    for (int c = sub * 8; c < DV; c += 64) {
+      {
         const uint4 o4 = *reinterpret_cast<const uint4 *>(out + base + c);
         const uint4 d4 = *reinterpret_cast<const uint4 *>(dout + base + c);
         const uint32_t os[4] = {o4.x, o4.y, o4.z, o4.w}, ds[4] = {d4.x, d4.y, d4.z, d4.w};
@@ -739,7 +752,13 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
                       dsum);
         }
       }
-      if constexpr (VARIANT == kYat) {
+    }
+  }
+  if (valid && VARIANT == kYat) {
+    const size_t base = ((size_t)bh * Tq + t) * DK;
+#pragma unroll
+    for (int c = sub * 8; c < DK; c += 64) {
+      {
         const uint4 q4 = *reinterpret_cast<const uint4 *>(q + base + c);
         const uint32_t qs[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
@@ -782,11 +801,11 @@ __global__ void bwd_param_finalize(const double *dpar, int h, int variant, float
   }
 }
 
-template <int VARIANT, int D, int SIDE, int YM, bool DP = false>
+template <int VARIANT, int DK, int DV, int SIDE, int YM, bool DP = false>
 cudaError_t launch_side(const BwdParams &p, const CUtensorMap &r, const CUtensorMap &rp,
                         const CUtensorMap &x, const CUtensorMap &xp, cudaStream_t s) {
-  using L = Layout<D, SIDE>;
-  auto kern = bwd_kernel<VARIANT, D, SIDE, YM, DP>;
+  using L = Layout<DK, DV, SIDE>;
+  auto kern = bwd_kernel<VARIANT, DK, DV, SIDE, YM, DP>;
   static int configured_for = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -812,62 +831,69 @@ cudaError_t launch_side(const BwdParams &p, const CUtensorMap &r, const CUtensor
 // row's first keys; strongly negative scores) a 2^-9 error in D would be
 // amplified far beyond the bf16 tolerance.  Softmax's gradient is bounded by
 // w <= 1 and keeps dout . out.
-template <int VARIANT, int D, int YM>
+template <int VARIANT, int DK, int DV, int YM>
 cudaError_t launch_all(const BwdParams &p, const BwdMaps &m, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
   if constexpr (VARIANT != kSoftmax) {
-    e = launch_side<VARIANT, D, SIDE_Q, YM, true>(p, m.q128, m.do128, m.k64, m.v64, s);
+    e = launch_side<VARIANT, DK, DV, SIDE_Q, YM, true>(p, m.q128, m.do128, m.k64, m.v64, s);
     if (e != cudaSuccess) return e;
   }
-  e = launch_side<VARIANT, D, SIDE_KV, YM>(p, m.k128, m.v128, m.q64, m.do64, s);
+  e = launch_side<VARIANT, DK, DV, SIDE_KV, YM>(p, m.k128, m.v128, m.q64, m.do64, s);
   if (e != cudaSuccess) return e;
-  return launch_side<VARIANT, D, SIDE_Q, YM>(p, m.q128, m.do128, m.k64, m.v64, s);
+  return launch_side<VARIANT, DK, DV, SIDE_Q, YM>(p, m.q128, m.do128, m.k64, m.v64, s);
 }
 
-template <int VARIANT, int D>
+template <int VARIANT, int DK, int DV>
 cudaError_t launch_prep(const BwdParams &p, const void *q, const void *out, const void *dout,
                         const float *row_mass, cudaStream_t s) {
   const long long rows = (long long)p.B * p.h * p.Tq_pad;
   const unsigned blocks = (unsigned)((rows * 8 + 255) / 256);
-  bwd_prep_kernel<VARIANT, D><<<blocks, 256, 0, s>>>(
+  bwd_prep_kernel<VARIANT, DK, DV><<<blocks, 256, 0, s>>>(
       static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(out),
       static_cast<const __nv_bfloat16 *>(dout), row_mass, p.eps, const_cast<float4 *>(p.aux),
       p.B * p.h, p.h, p.Tq, p.Tq_pad, p.scale);
   return cudaGetLastError();
 }
 
-}  // namespace bwd
-
-bool bwd_tc_supported(int dk, int dv) { return dk == dv && (dk == 64 || dk == 128); }
-
-cudaError_t launch_bwd_prep(int variant, int d, const BwdParams &p, const void *q, const void *out,
-                            const void *dout, const float *row_mass, cudaStream_t s) {
-  using namespace bwd;
-  if (d == 64) {
-    if (variant == kSoftmax) return launch_prep<kSoftmax, 64>(p, q, out, dout, row_mass, s);
-    if (variant == kYat) return launch_prep<kYat, 64>(p, q, out, dout, row_mass, s);
-    return launch_prep<kStau, 64>(p, q, out, dout, row_mass, s);
-  }
-  if (variant == kSoftmax) return launch_prep<kSoftmax, 128>(p, q, out, dout, row_mass, s);
-  if (variant == kYat) return launch_prep<kYat, 128>(p, q, out, dout, row_mass, s);
-  return launch_prep<kStau, 128>(p, q, out, dout, row_mass, s);
+template <int DK, int DV>
+cudaError_t prep_for(int variant, const BwdParams &p, const void *q, const void *out,
+                     const void *dout, const float *row_mass, cudaStream_t s) {
+  if (variant == kSoftmax) return launch_prep<kSoftmax, DK, DV>(p, q, out, dout, row_mass, s);
+  if (variant == kYat) return launch_prep<kYat, DK, DV>(p, q, out, dout, row_mass, s);
+  return launch_prep<kStau, DK, DV>(p, q, out, dout, row_mass, s);
 }
 
-cudaError_t launch_bwd_tc(int variant, int d, int yat_m, const BwdParams &p, const BwdMaps &m,
-                          cudaStream_t s) {
+template <int DK, int DV>
+cudaError_t all_for(int variant, int yat_m, const BwdParams &p, const BwdMaps &m,
+                    cudaStream_t s) {
+  if (variant == kSoftmax) return launch_all<kSoftmax, DK, DV, 1>(p, m, s);
+  if (variant == kStau) return launch_all<kStau, DK, DV, 1>(p, m, s);
+  if (yat_m == 2) return launch_all<kYat, DK, DV, 2>(p, m, s);
+  if (yat_m == 3) return launch_all<kYat, DK, DV, 3>(p, m, s);
+  return launch_all<kYat, DK, DV, 1>(p, m, s);
+}
+
+}  // namespace bwd
+
+bool bwd_tc_supported(int dk, int dv) {
+  return (dk == 64 && dv == 64) || (dk == 128 && dv == 128) || (dk == 128 && dv == 64);
+}
+
+cudaError_t launch_bwd_prep(int variant, int dk, int dv, const BwdParams &p, const void *q,
+                            const void *out, const void *dout, const float *row_mass,
+                            cudaStream_t s) {
   using namespace bwd;
-  if (d == 64) {
-    if (variant == kSoftmax) return launch_all<kSoftmax, 64, 1>(p, m, s);
-    if (variant == kStau) return launch_all<kStau, 64, 1>(p, m, s);
-    if (yat_m == 2) return launch_all<kYat, 64, 2>(p, m, s);
-    if (yat_m == 3) return launch_all<kYat, 64, 3>(p, m, s);
-    return launch_all<kYat, 64, 1>(p, m, s);
-  }
-  if (variant == kSoftmax) return launch_all<kSoftmax, 128, 1>(p, m, s);
-  if (variant == kStau) return launch_all<kStau, 128, 1>(p, m, s);
-  if (yat_m == 2) return launch_all<kYat, 128, 2>(p, m, s);
-  if (yat_m == 3) return launch_all<kYat, 128, 3>(p, m, s);
-  return launch_all<kYat, 128, 1>(p, m, s);
+  if (dk == 64) return prep_for<64, 64>(variant, p, q, out, dout, row_mass, s);
+  if (dv == 64) return prep_for<128, 64>(variant, p, q, out, dout, row_mass, s);
+  return prep_for<128, 128>(variant, p, q, out, dout, row_mass, s);
+}
+
+cudaError_t launch_bwd_tc(int variant, int dk, int dv, int yat_m, const BwdParams &p,
+                          const BwdMaps &m, cudaStream_t s) {
+  using namespace bwd;
+  if (dk == 64) return all_for<64, 64>(variant, yat_m, p, m, s);
+  if (dv == 64) return all_for<128, 64>(variant, yat_m, p, m, s);
+  return all_for<128, 128>(variant, yat_m, p, m, s);
 }
 
 cudaError_t launch_bwd_param_finalize(int variant, const double *dpar, int h, float *db,

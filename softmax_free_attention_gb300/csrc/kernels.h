@@ -95,19 +95,20 @@ struct BwdParams {
   float scale;
   int n_q64, n_q128, n_k64, n_k128;  // tiles of 64 and 128 rows
 };
-// Tensor maps of the backward: q, dout, k, v with 128-row and 64-row boxes.
+// Tensor maps of the backward: q, dout, k, v with 128-row and 64-row boxes
+// (q and k rows dk wide, v and dout rows dv wide).
 struct BwdMaps {
   CUtensorMap q128, do128, k128, v128, q64, do64, k64, v64;
 };
 bool bwd_tc_supported(int dk, int dv);
 // The per-row D, normaliser and |q|^2 (into p.aux) from q, out, dout and
 // the forward's row_mass.
-cudaError_t launch_bwd_prep(int variant, int d, const BwdParams &p, const void *q,
+cudaError_t launch_bwd_prep(int variant, int dk, int dv, const BwdParams &p, const void *q,
                             const void *out, const void *dout, const float *row_mass,
                             cudaStream_t s);
 // The dK/dV pass, then the dQ pass.
-cudaError_t launch_bwd_tc(int variant, int d, int yat_m, const BwdParams &p, const BwdMaps &m,
-                          cudaStream_t s);
+cudaError_t launch_bwd_tc(int variant, int dk, int dv, int yat_m, const BwdParams &p,
+                          const BwdMaps &m, cudaStream_t s);
 // The fp64 per-head parameter sums into the fp32 outputs (any may be NULL).
 cudaError_t launch_bwd_param_finalize(int variant, const double *dpar, int h, float *db,
                                       float *deps, float *dtau, cudaStream_t s);

@@ -100,6 +100,29 @@ def test_backward_matches_oracle(variant, shape):
     compare_grads(gpu, ora, f"{variant} {shape}")
 
 
+DKV_SHAPES = [
+    # B, h, hkv, Tq, Tk, dk, dv, causal: q/k rows wider than v rows
+    (1, 2, 1, 200, 200, 128, 64, True),
+    (2, 2, 2, 129, 129, 128, 64, True),
+    (1, 4, 2, 130, 700, 128, 64, False),
+]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("shape", DKV_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_backward_dk_wider_than_dv(variant, shape):
+    B, h, hkv, Tq, Tk, dk, dv, causal = shape
+    w = workloads.Workload("bwd_dkv", B=B, h=h, hkv=hkv, Tq=Tq, Tk=Tk, dk=dk, dv=dv,
+                           dtype="bf16", causal=causal, yat_param="softplus_uniform",
+                           seed=5 * Tq + Tk)
+    inp = workloads.generate(w)
+    dout = workloads.grad_output(w)
+    gpu = run_gpu_backward(variant, inp, dout, causal=causal, scale=w.scale)
+    ora = oracle.backward(variant, inp["q"], inp["k"], inp["v"], dout, causal=causal,
+                          scale=w.scale, **_params(variant, inp))
+    compare_grads(gpu, ora, f"{variant} {shape}")
+
+
 @pytest.mark.parametrize("m", [2, 3])
 @pytest.mark.parametrize("shape", [(1, 2, 1, 200, 200, 128, True), (1, 2, 2, 130, 300, 64, False)],
                          ids=lambda s: "x".join(map(str, s)))
@@ -147,13 +170,13 @@ def test_backward_deterministic_and_empty():
 
 
 def test_backward_rejects_unsupported():
-    q = torch.zeros(1, 1, 4, 128, dtype=torch.bfloat16, device="cuda")
-    k = torch.zeros(1, 1, 4, 128, dtype=torch.bfloat16, device="cuda")
-    v = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16, device="cuda")
-    out = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros(1, 1, 4, 128, dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(1, 1, 4, 128, dtype=torch.bfloat16, device="cuda")
     mass = torch.zeros(1, 1, 4, device="cuda")
     with pytest.raises(ValueError):
-        attention.backward("softmax", q, k, v, out, out, mass)  # dk != dv
+        attention.backward("softmax", q, k, v, out, out, mass)  # (dk, dv) = (64, 128)
     f = torch.zeros(1, 1, 4, 64, device="cuda")
     with pytest.raises(ValueError):
         attention.backward("softmax", f, f, f, f, f, mass)  # fp32
@@ -223,3 +246,20 @@ def test_yat_b_zero_ablation_forward_and_backward(causal):
     ora = oracle.backward("yat", inp["q"], inp["k"], inp["v"], dout, causal=causal,
                           **_params("yat", inp))
     compare_grads(gpu, ora, f"yat b=0 causal={causal}")
+
+
+def test_backward_cfg5_cross_slice():
+    """Non-causal cross-attention Tq=2048 Tk=32768 dk=128 dv=64 with q, k x8
+    (B=1 h=32), Yat: the whole problem on the GPU, the oracle on two heads."""
+    w = workloads.WORKLOADS["cfg5_cross"]
+    inp = workloads.generate(w)
+    dout = workloads.grad_output(w)
+    dq, dk, dv, gp = run_gpu_backward("yat", inp, dout, causal=False, scale=w.scale)
+    kw = _params("yat", inp)
+    for hd in (0, w.h - 1):
+        sub = {n: x[hd:hd + 1] for n, x in kw.items()}
+        ora = oracle.backward("yat", inp["q"][:, hd:hd + 1], inp["k"][:, hd:hd + 1],
+                              inp["v"][:, hd:hd + 1], dout[:, hd:hd + 1], causal=False, **sub)
+        gpu = (dq[:, hd:hd + 1], dk[:, hd:hd + 1], dv[:, hd:hd + 1],
+               {n: g[hd:hd + 1] for n, g in gp.items()})
+        compare_grads(gpu, ora, f"cfg5 yat head {hd}")
