@@ -443,6 +443,11 @@ BwdWs bwd_ws(int variant, const cattn_problem_t *p) {
   w.nkmax = (size_t)p->h * 2 * sizeof(double);
   size_t off = align256(w.nkmax + sizeof(unsigned int));
   w.aux = off;
+  if (p->dtype == CATTN_F32) {  // the fp32 path: the rows' D and (Yat) Z
+    off += align256((size_t)2 * p->B * p->h * p->Tq * sizeof(float));
+    w.total = off;
+    return w;
+  }
   off += align256((size_t)p->B * p->h * tq_pad(p) * 16);
   if (variant == CATTN_YAT) {
     w.nk = off;
@@ -455,7 +460,9 @@ BwdWs bwd_ws(int variant, const cattn_problem_t *p) {
 int check_bwd_problem(int variant, const cattn_problem_t *p) {
   int rc = check_problem(variant, p);
   if (rc != CATTN_OK) return rc;
-  if (p->dtype != CATTN_BF16 || !bwd_tc_supported(p->dk, p->dv)) return CATTN_ERR_UNSUPPORTED;
+  const bool ok = p->dtype == CATTN_BF16 ? bwd_tc_supported(p->dk, p->dv)
+                                         : fwd_simt_supported(p->dk, p->dv);
+  if (!ok) return CATTN_ERR_UNSUPPORTED;
   return CATTN_OK;
 }
 
@@ -495,8 +502,9 @@ int cattn_backward(int variant, const cattn_problem_t *p, const void *q, const v
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (empty) {
     // no query rows: every gradient is zero
-    const size_t kbytes = (size_t)p->B * p->hkv * p->Tk * p->dk * 2;
-    const size_t vbytes = (size_t)p->B * p->hkv * p->Tk * p->dv * 2;
+    const size_t es = p->dtype == CATTN_F32 ? 4 : 2;
+    const size_t kbytes = (size_t)p->B * p->hkv * p->Tk * p->dk * es;
+    const size_t vbytes = (size_t)p->B * p->hkv * p->Tk * p->dv * es;
     if (!kv_empty && (rc = map_cuda(cudaMemsetAsync(dk, 0, kbytes, s))) != CATTN_OK) return rc;
     if (!kv_empty && (rc = map_cuda(cudaMemsetAsync(dv, 0, vbytes, s))) != CATTN_OK) return rc;
     for (float *g : {db, deps, dtau})
@@ -506,6 +514,35 @@ int cattn_backward(int variant, const cattn_problem_t *p, const void *q, const v
   }
   const BwdWs w = bwd_ws(variant, p);
   char *ws = static_cast<char *>(workspace);
+  if (p->dtype == CATTN_F32) {
+    BwdSimtParams sp;
+    memset(&sp, 0, sizeof(sp));
+    sp.q = static_cast<const float *>(q);
+    sp.k = static_cast<const float *>(k);
+    sp.v = static_cast<const float *>(v);
+    sp.dout = static_cast<const float *>(dout);
+    sp.row_mass = row_mass;
+    sp.b = b;
+    sp.eps = eps;
+    sp.tau = tau;
+    sp.dq = static_cast<float *>(dq);
+    sp.dk = static_cast<float *>(dk);
+    sp.dv = static_cast<float *>(dv);
+    sp.Dbuf = reinterpret_cast<float *>(ws + w.aux);
+    sp.dpar = reinterpret_cast<double *>(ws + w.dpar);
+    sp.B = p->B;
+    sp.h = p->h;
+    sp.hkv = p->hkv;
+    sp.Tq = p->Tq;
+    sp.Tk = p->Tk;
+    sp.causal = p->causal ? 1 : 0;
+    sp.scale = p->scale;
+    if ((rc = map_cuda(cudaMemsetAsync(ws, 0, w.aux, s))) != CATTN_OK) return rc;
+    if ((rc = map_cuda(launch_bwd_simt(variant, p->dk, p->dv, p->yat_m > 1 ? p->yat_m : 1, sp,
+                                       s))) != CATTN_OK)
+      return rc;
+    return map_cuda(launch_bwd_param_finalize(variant, sp.dpar, p->h, db, deps, dtau, s));
+  }
   BwdParams bp;
   memset(&bp, 0, sizeof(bp));
   bp.aux = reinterpret_cast<const float4 *>(ws + w.aux);

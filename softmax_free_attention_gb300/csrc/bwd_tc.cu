@@ -112,8 +112,8 @@ struct Layout {
   static constexpr int OFF_ST = R_TILE + RP_TILE;
   static constexpr int OFF_W = OFF_ST + NS * STAGE;
   static constexpr int OFF_C = OFF_W + (SIDE == SIDE_KV ? W_TILE : 0);
-  static constexpr int OFF_XCH = OFF_C + W_TILE;  // [NQ slices][128] floats
-  static constexpr int OFF_BAR = OFF_XCH + NQ * RT * 4;
+  static constexpr int OFF_XCH = OFF_C + W_TILE;  // [2][NQ slices][128] floats
+  static constexpr int OFF_BAR = OFF_XCH + 2 * NQ * RT * 4;
   // r_full, x_full[NS], x_empty[NS], s_full[2], s_empty[2], wc_full, wc_empty,
   // acc_full, drain
   static constexpr int NBAR = 1 + 2 * NS + 4 + 2 + 2;
@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (VARIANT != kSoftmax) hp.eps = p.eps[head];
       if (VARIANT == kStau) hp.tau = p.tau[head];
     }
-    float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, dsum = acc0;
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, dsum = acc0, wsum = acc0;
     bool ok = true;
     for (int n = 0; n < n_tiles; ++n) {
       const int b = n & 1, st = n % NS;
@@ -584,7 +584,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           float2 w, c = make_float2(0.f, 0.f);
           pair2<VARIANT, YM, FULL, DP>(sv, dv, X, Y, Z, hp, scale, c2, al0, al1, w, c, acc0,
                                        acc1, acc2);
-          if constexpr (DP) dsum = __ffma2_rn(w, dv, dsum);
+          if constexpr (DP) {
+            dsum = __ffma2_rn(w, dv, dsum);
+            if (VARIANT == kYat) wsum = __fadd2_rn(wsum, w);
+          }
           wpk[i >> 1] = pack_bf16x2(w.x, w.y);
           cpk[i >> 1] = pack_bf16x2(c.x, c.y);
         }
@@ -632,13 +635,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     if constexpr (DP) {
       // the two column halves' partial sums, then D_t over the aux array's D
+      // Yat also replaces the forward's 1 / Z by 1 / (sum kappa + 1e-9) of
+      // this pass's own kappas, so that a row's weights, normaliser and D all
+      // come from the same kappa (on a row whose only keys have a nearly
+      // cancelling numerator, a mismatch between the forward's mass and these
+      // kappas reaches the gradient through 2 / (q.k + b))
       xch[hf * RT + r] = dsum.x + dsum.y;
+      xch[(NQ + hf) * RT + r] = wsum.x + wsum.y;
       named_barrier_sync(1, MAP_WARPS * 32);
       if (ok && hf == 0 && grow < p.Tq) {
-        float D_t = 0.f;
+        float D_t = 0.f, W_t = 0.f;
 #pragma unroll
-        for (int x = 0; x < NQ; ++x) D_t += xch[x * RT + r];
-        p.aux_w[((size_t)bh_r * p.Tq_pad + grow) * 4] = VARIANT == kYat ? -D_t * row_aux.y : -D_t;
+        for (int x = 0; x < NQ; ++x) {
+          D_t += xch[x * RT + r];
+          W_t += xch[(NQ + x) * RT + r];
+        }
+        float *a = p.aux_w + ((size_t)bh_r * p.Tq_pad + grow) * 4;
+        if (VARIANT == kYat) {
+          const float zf = 1.f / row_aux.y;          // the forward's M + 1e-9
+          const float inv = 1.f / fmaf(W_t, zf, 1e-9f);  // 1 / (sum kappa + 1e-9)
+          a[0] = -D_t * zf * inv * inv;              // -D / Z, D = sum kappa dW / Z
+          a[1] = inv;
+        } else {
+          a[0] = -D_t;
+        }
       }
     } else {
     // ---- epilogue: accumulators out of TMEM, Yat's rank-one term, bf16 stores

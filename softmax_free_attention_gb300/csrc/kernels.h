@@ -109,6 +109,18 @@ cudaError_t launch_bwd_prep(int variant, int dk, int dv, const BwdParams &p, con
 // The dK/dV pass, then the dQ pass.
 cudaError_t launch_bwd_tc(int variant, int dk, int dv, int yat_m, const BwdParams &p,
                           const BwdMaps &m, cudaStream_t s);
+// fp32 backward on the CUDA cores (the fp32 forward's shapes).
+struct BwdSimtParams {
+  const float *q, *k, *v, *dout, *row_mass, *b, *eps, *tau;
+  float *dq, *dk, *dv;
+  float *Dbuf;   // [2][B*h*Tq] the rows' D and (Yat) Z, written by the dQ pass
+  double *dpar;  // [h][2], zeroed
+  int B, h, hkv, Tq, Tk, causal;
+  float scale;
+};
+cudaError_t launch_bwd_simt(int variant, int dk, int dv, int yat_m, const BwdSimtParams &p,
+                            cudaStream_t s);
+
 // The fp64 per-head parameter sums into the fp32 outputs (any may be NULL).
 cudaError_t launch_bwd_param_finalize(int variant, const double *dpar, int h, float *db,
                                       float *deps, float *dtau, cudaStream_t s);

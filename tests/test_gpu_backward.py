@@ -53,7 +53,7 @@ def run_gpu_backward(variant, inp, dout, *, causal, scale, yat_m=1):
     return res
 
 
-def compare_grads(gpu, ora, where):
+def compare_grads(gpu, ora, where, tol=GRAD_TOL):
     dq, dk, dv, gp = gpu
     odq, odk, odv, op = ora
     for name, g, o in (("dq", dq, odq), ("dk", dk, odk), ("dv", dv, odv)):
@@ -61,13 +61,13 @@ def compare_grads(gpu, ora, where):
         assert np.isfinite(g).all(), f"{where}: non-finite {name}"
         scale = float(np.abs(o).max()) if o.size else 0.0
         err = float(np.abs(g - o).max()) if o.size else 0.0
-        assert err <= GRAD_TOL * scale + 1e-6, f"{where}: {name} max err {err:.3e} vs max {scale:.3e}"
+        assert err <= tol * scale + 1e-6, f"{where}: {name} max err {err:.3e} vs max {scale:.3e}"
     assert sorted(gp) == sorted(op), where
     for name in op:
         g = pu.to_np(gp[name])
         o = op[name]
         err = float(np.abs(g - o).max())
-        lim = GRAD_TOL * float(np.abs(o).max()) + 1e-6
+        lim = tol * float(np.abs(o).max()) + 1e-6
         assert err <= lim, f"{where}: d{name} err {err:.3e} > {lim:.3e} ({g} vs {o})"
 
 
@@ -121,6 +121,31 @@ def test_backward_dk_wider_than_dv(variant, shape):
     ora = oracle.backward(variant, inp["q"], inp["k"], inp["v"], dout, causal=causal,
                           scale=w.scale, **_params(variant, inp))
     compare_grads(gpu, ora, f"{variant} {shape}")
+
+
+F32_SHAPES = [
+    # B, h, hkv, Tq, Tk, dk, dv, causal
+    (1, 4, 4, 256, 256, 32, 32, True),     # the fp32 workload's shape
+    (1, 2, 1, 77, 77, 64, 64, True),
+    (2, 2, 2, 100, 150, 128, 64, False),
+    (1, 1, 1, 65, 65, 128, 128, True),
+]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("shape", F32_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_backward_fp32(variant, shape):
+    """The CUDA-core fp32 backward, held to the fp32 bound 1e-4 of each
+    tensor's largest magnitude."""
+    B, h, hkv, Tq, Tk, dk, dv, causal = shape
+    w = workloads.Workload("bwd32", B=B, h=h, hkv=hkv, Tq=Tq, Tk=Tk, dk=dk, dv=dv, dtype="f32",
+                           causal=causal, yat_param="ln2", seed=Tq + 11)
+    inp = workloads.generate(w)
+    dout = workloads.grad_output(w)
+    gpu = run_gpu_backward(variant, inp, dout, causal=causal, scale=w.scale)
+    ora = oracle.backward(variant, inp["q"], inp["k"], inp["v"], dout, causal=causal,
+                          scale=w.scale, **_params(variant, inp))
+    compare_grads(gpu, ora, f"f32 {variant} {shape}", tol=1e-4)
 
 
 @pytest.mark.parametrize("m", [2, 3])
@@ -177,9 +202,9 @@ def test_backward_rejects_unsupported():
     mass = torch.zeros(1, 1, 4, device="cuda")
     with pytest.raises(ValueError):
         attention.backward("softmax", q, k, v, out, out, mass)  # (dk, dv) = (64, 128)
-    f = torch.zeros(1, 1, 4, 64, device="cuda")
+    f = torch.zeros(1, 1, 4, 48, device="cuda")
     with pytest.raises(ValueError):
-        attention.backward("softmax", f, f, f, f, f, mass)  # fp32
+        attention.backward("softmax", f, f, f, f, f, mass)  # fp32 width 48
 
 
 # ---------------------------------------------------------------- full size
@@ -263,3 +288,28 @@ def test_backward_cfg5_cross_slice():
         gpu = (dq[:, hd:hd + 1], dk[:, hd:hd + 1], dv[:, hd:hd + 1],
                {n: g[hd:hd + 1] for n, g in gp.items()})
         compare_grads(gpu, ora, f"cfg5 yat head {hd}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_backward_yat_cancelling_numerator(dtype):
+    """Edge case: the first (one-key) row of a causal head whose numerator
+    q.k + b nearly cancels, so kappa is tiny and the gradient's factor
+    2 / (q.k + b) is large; the row's weight is kappa / (kappa + 1e-9)."""
+    w = workloads.Workload("bwd_cancel", B=1, h=2, hkv=2, Tq=130, Tk=130, dk=64, dv=64,
+                           dtype=dtype, causal=True, yat_param="ln2", seed=23)
+    inp = workloads.generate(w)
+    q = inp["q"].double()
+    k = inp["k"].double().clone()
+    b = float(inp["yat_b"][0])
+    for target in (0.02, -0.005):  # head 0 and head 1
+        hd = 0 if target > 0 else 1
+        q0, k0 = q[0, hd, 0], k[0, hd, 0]
+        k[0, hd, 0] = k0 - ((q0 @ k0 + b - target) / (q0 @ q0)) * q0
+    inp = dict(inp, k=k.to(inp["k"].dtype))
+    dout = workloads.grad_output(w)
+    gpu = run_gpu_backward("yat", inp, dout, causal=True, scale=w.scale)
+    ora = oracle.backward("yat", inp["q"], inp["k"], inp["v"], dout, causal=True,
+                          **_params("yat", inp))
+    num = float(inp["q"][0, 0, 0].double() @ inp["k"][0, 0, 0].double()) + b
+    compare_grads(gpu, ora, f"yat cancelling numerator {dtype} (q.k + b = {num:.3g})",
+                  tol=GRAD_TOL if dtype == "bf16" else 1e-4)
