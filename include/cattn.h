@@ -224,8 +224,9 @@ int cattn_row_stats(int variant, const cattn_problem_t *p, const void *q, const 
  * same problem whose out and row_mass are passed in.
  *
  * Per query row t the forward's weights are w_tj = f_tj / Z_t; they are
- * recomputed from the scores and row_mass (softmax, s^tau: log Z; Yat: Z
- * before its + 1e-9).  With D_t = dout_t . out_t and dW_tj = dout_t . v_j:
+ * recomputed from the scores and row_mass (softmax, s^tau: log Z; Yat: the
+ * library sums its own kappas for Z).  With D_t = sum_j w_tj dW_tj (= dout_t .
+ * out_t) and dW_tj = dout_t . v_j:
  *   dv_j = sum_t w_tj dout_t
  *   softmax  dS_tj = w_tj (dW_tj - D_t); dq = scale dS k, dk = scale dS^T q
  *   s^tau    dS_tj = w_tj (dW_tj - D_t) tau sigma(s_tj) / phi(s_tj), same
@@ -239,14 +240,15 @@ int cattn_row_stats(int variant, const cattn_problem_t *p, const void *q, const 
  * focal-length knob for attention", core formula).  The sums over query
  * heads sharing a kv head (h > hkv) are taken inside the library.
  *
- *   q, k, v, out  the forward's inputs and output (bf16, layouts as above)
- *   dout          [B, h, Tq, dv] bf16: dL/d out
+ *   q, k, v, out  the forward's inputs and output (layouts as above)
+ *   dout          [B, h, Tq, dv], the element type of q: dL/d out
  *   row_mass      [B, h, Tq] fp32: the forward's row_mass output
- *   dq, dk, dv    bf16, shaped like q, k, v; written, never read
+ *   dq, dk, dv    shaped and typed like q, k, v; written, never read
  *   db, deps, dtau  fp32 [h] or NULL: the parameter gradients the map has
  *                 (Yat: db, deps; s^tau: deps, dtau; the others untouched)
- * bf16 only, (dk, dv) in {(64, 64), (128, 128), (128, 64)}, yat_m in
- * {0, 1, 2, 3}; anything else is CATTN_ERR_UNSUPPORTED.  A problem with no query rows writes zeros.  The
+ * bf16 (tensor cores): (dk, dv) in {(64, 64), (128, 128), (128, 64)}; fp32
+ * (CUDA cores): the fp32 forward's widths; yat_m in {0, 1, 2, 3}; anything
+ * else is CATTN_ERR_UNSUPPORTED.  A problem with no query rows writes zeros.  The
  * kernels' accumulation order is fixed: repeated calls give identical bits
  * for dq, dk and dv (the fp64 parameter sums use atomics).
  * cattn_backward_workspace_bytes: bytes needed (0 if the problem is
