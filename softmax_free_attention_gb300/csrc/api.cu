@@ -46,7 +46,7 @@ struct WsLayout {
 WsLayout ws_layout(int variant, const cattn_problem_t *p) {
   WsLayout w;
   memset(&w, 0, sizeof(w));
-  if (p->dtype != CATTN_BF16) return w;
+  if (p->dtype != CATTN_BF16 || !fwd_tc_supported(p->dk, p->dv)) return w;
   w.sched = tc_schedule(p->B, p->h, p->Tq, p->Tk, p->causal);
   size_t off = 0;
   w.ctrl = off;
@@ -79,9 +79,9 @@ int check_problem(int variant, const cattn_problem_t *p) {
   if (variant != CATTN_YAT && !(p->scale > 0.f && p->scale < 3.0e38f)) return CATTN_ERR_INVALID_ARG;
   if (p->flags & ~CATTN_FLAG_NORMS_READY) return CATTN_ERR_INVALID_ARG;
   if (p->yat_m < 0 || p->yat_m > 3) return CATTN_ERR_INVALID_ARG;
-  const bool shape_ok = p->dtype == CATTN_BF16 ? fwd_tc_supported(p->dk, p->dv)
-                                               : fwd_simt_supported(p->dk, p->dv);
-  if (!shape_ok) return CATTN_ERR_UNSUPPORTED;
+  // every (dk, dv) in {32, 64, 128}^2: the tensor-core kernel for bf16 with
+  // (64, 64), (128, 128), (128, 64), the CUDA-core kernel otherwise
+  if (!fwd_simt_supported(p->dk, p->dv)) return CATTN_ERR_UNSUPPORTED;
   // every index the kernels form stays inside int32 per head and size_t overall
   if ((long long)p->Tq * p->dk > (1ll << 31) || (long long)p->Tk * p->dk > (1ll << 31) ||
       (long long)p->Tk * p->dv > (1ll << 31))
@@ -94,6 +94,11 @@ int check_problem(int variant, const cattn_problem_t *p) {
 }
 
 int map_cuda(cudaError_t e) { return e == cudaSuccess ? CATTN_OK : CATTN_ERR_CUDA; }
+
+// bf16 with widths the tensor-core kernel has tiles for
+bool on_tensor_cores(const cattn_problem_t *p) {
+  return p->dtype == CATTN_BF16 && fwd_tc_supported(p->dk, p->dv);
+}
 
 // The library is built for sm_103a only.
 int check_device() {
@@ -186,7 +191,7 @@ int cattn_key_norms(const cattn_problem_t *p, const void *k, void *workspace,
   int rc = check_problem(CATTN_YAT, p);
   if (rc != CATTN_OK) return rc;
   if (p->dtype != CATTN_BF16) return CATTN_ERR_UNSUPPORTED;
-  if (is_empty(p)) return CATTN_OK;
+  if (is_empty(p) || !on_tensor_cores(p)) return CATTN_OK;  // the CUDA-core path needs no norms
   if (!k || !workspace) return CATTN_ERR_INVALID_ARG;
   if (!aligned16(k) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return CATTN_ERR_UNSUPPORTED;
@@ -238,7 +243,8 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
   fp.n_pairs = (fp.n_qtiles + 1) / 2;  // two query tiles per work unit
   fp.n_kv_tiles = (p->Tk + kTcKeyTile - 1) / kTcKeyTile;
 
-  if (p->dtype == CATTN_F32) return map_cuda(launch_fwd_simt(variant, p->dk, p->dv, fp, s));
+  if (!on_tensor_cores(p))
+    return map_cuda(launch_fwd_simt(variant, p->dtype == CATTN_BF16, p->dk, p->dv, fp, s));
 
   const WsLayout w = ws_layout(variant, p);
   char *ws = static_cast<char *>(workspace);
@@ -283,7 +289,7 @@ size_t tau_ws_bytes(const cattn_problem_t *p) {
 size_t cattn_tau_star_workspace_bytes(const cattn_problem_t *p) {
   if (!p) return 0;
   const cattn_problem_t tp = tau_problem(p);
-  if (check_problem(CATTN_STAU, &tp) != CATTN_OK || tp.dtype != CATTN_BF16) return 0;
+  if (check_problem(CATTN_STAU, &tp) != CATTN_OK || !on_tensor_cores(&tp)) return 0;
   return tau_ws_bytes(&tp);
 }
 
@@ -294,7 +300,7 @@ int cattn_tau_star(const cattn_problem_t *p, const void *q, const void *k, const
   const cattn_problem_t tp = tau_problem(p);
   int rc = check_problem(CATTN_STAU, &tp);
   if (rc != CATTN_OK) return rc;
-  if (tp.dtype != CATTN_BF16) return CATTN_ERR_UNSUPPORTED;
+  if (!on_tensor_cores(&tp)) return CATTN_ERR_UNSUPPORTED;
   if (tp.h == 0) return CATTN_OK;
   if (!eps || !tau_star || !workspace) return CATTN_ERR_INVALID_ARG;
   if (!is_empty(&tp) && (!q || !k)) return CATTN_ERR_INVALID_ARG;
@@ -351,7 +357,7 @@ size_t stats_ws_bytes(int variant, const cattn_problem_t *p) {
 size_t cattn_row_stats_workspace_bytes(int variant, const cattn_problem_t *p) {
   if (!p) return 0;
   const cattn_problem_t tp = tau_problem(p);
-  if (check_problem(variant, &tp) != CATTN_OK || tp.dtype != CATTN_BF16 || tp.yat_m > 1) return 0;
+  if (check_problem(variant, &tp) != CATTN_OK || !on_tensor_cores(&tp) || tp.yat_m > 1) return 0;
   return stats_ws_bytes(variant, &tp);
 }
 
@@ -363,7 +369,7 @@ int cattn_row_stats(int variant, const cattn_problem_t *p, const void *q, const 
   const cattn_problem_t tp = tau_problem(p);
   int rc = check_problem(variant, &tp);
   if (rc != CATTN_OK) return rc;
-  if (tp.dtype != CATTN_BF16 || tp.yat_m > 1) return CATTN_ERR_UNSUPPORTED;
+  if (!on_tensor_cores(&tp) || tp.yat_m > 1) return CATTN_ERR_UNSUPPORTED;
   if (is_empty(&tp)) return CATTN_OK;
   if (!q || !k || !row_mass || !workspace) return CATTN_ERR_INVALID_ARG;
   if (variant == CATTN_YAT && (!b || !eps)) return CATTN_ERR_INVALID_ARG;
@@ -436,6 +442,11 @@ struct BwdWs {
 
 int tq_pad(const cattn_problem_t *p) { return (p->Tq + kTile - 1) / kTile * kTile; }
 
+// bf16 with widths the tensor-core backward has tiles for
+bool bwd_on_tensor_cores(const cattn_problem_t *p) {
+  return p->dtype == CATTN_BF16 && bwd_tc_supported(p->dk, p->dv);
+}
+
 BwdWs bwd_ws(int variant, const cattn_problem_t *p) {
   BwdWs w;
   memset(&w, 0, sizeof(w));
@@ -443,7 +454,7 @@ BwdWs bwd_ws(int variant, const cattn_problem_t *p) {
   w.nkmax = (size_t)p->h * 2 * sizeof(double);
   size_t off = align256(w.nkmax + sizeof(unsigned int));
   w.aux = off;
-  if (p->dtype == CATTN_F32) {  // the fp32 path: the rows' D and (Yat) Z
+  if (!bwd_on_tensor_cores(p)) {  // the CUDA-core path: the rows' D and (Yat) Z
     off += align256((size_t)2 * p->B * p->h * p->Tq * sizeof(float));
     w.total = off;
     return w;
@@ -460,9 +471,7 @@ BwdWs bwd_ws(int variant, const cattn_problem_t *p) {
 int check_bwd_problem(int variant, const cattn_problem_t *p) {
   int rc = check_problem(variant, p);
   if (rc != CATTN_OK) return rc;
-  const bool ok = p->dtype == CATTN_BF16 ? bwd_tc_supported(p->dk, p->dv)
-                                         : fwd_simt_supported(p->dk, p->dv);
-  if (!ok) return CATTN_ERR_UNSUPPORTED;
+  if (!fwd_simt_supported(p->dk, p->dv)) return CATTN_ERR_UNSUPPORTED;
   return CATTN_OK;
 }
 
@@ -514,20 +523,20 @@ int cattn_backward(int variant, const cattn_problem_t *p, const void *q, const v
   }
   const BwdWs w = bwd_ws(variant, p);
   char *ws = static_cast<char *>(workspace);
-  if (p->dtype == CATTN_F32) {
+  if (!bwd_on_tensor_cores(p)) {
     BwdSimtParams sp;
     memset(&sp, 0, sizeof(sp));
-    sp.q = static_cast<const float *>(q);
-    sp.k = static_cast<const float *>(k);
-    sp.v = static_cast<const float *>(v);
-    sp.dout = static_cast<const float *>(dout);
+    sp.q = q;
+    sp.k = k;
+    sp.v = v;
+    sp.dout = dout;
     sp.row_mass = row_mass;
     sp.b = b;
     sp.eps = eps;
     sp.tau = tau;
-    sp.dq = static_cast<float *>(dq);
-    sp.dk = static_cast<float *>(dk);
-    sp.dv = static_cast<float *>(dv);
+    sp.dq = dq;
+    sp.dk = dk;
+    sp.dv = dv;
     sp.Dbuf = reinterpret_cast<float *>(ws + w.aux);
     sp.dpar = reinterpret_cast<double *>(ws + w.dpar);
     sp.B = p->B;
@@ -538,8 +547,8 @@ int cattn_backward(int variant, const cattn_problem_t *p, const void *q, const v
     sp.causal = p->causal ? 1 : 0;
     sp.scale = p->scale;
     if ((rc = map_cuda(cudaMemsetAsync(ws, 0, w.aux, s))) != CATTN_OK) return rc;
-    if ((rc = map_cuda(launch_bwd_simt(variant, p->dk, p->dv, p->yat_m > 1 ? p->yat_m : 1, sp,
-                                       s))) != CATTN_OK)
+    if ((rc = map_cuda(launch_bwd_simt(variant, p->dtype == CATTN_BF16, p->dk, p->dv,
+                                       p->yat_m > 1 ? p->yat_m : 1, sp, s))) != CATTN_OK)
       return rc;
     return map_cuda(launch_bwd_param_finalize(variant, sp.dpar, p->h, db, deps, dtau, s));
   }

@@ -1,8 +1,9 @@
-// bwd_simt.cu -- fp32 attention backward on the CUDA cores.
+// bwd_simt.cu -- attention backward on the CUDA cores.
 //
-// The fp32 path's counterpart of bwd_tc.cu (same gradients, full fp32 FMA
-// arithmetic, the fp32 output tolerance 1e-4 of each tensor's largest
-// magnitude).  Two passes, one warp per row; lane l owns columns l, l+32, ...
+// The CUDA-core counterpart of bwd_tc.cu (same gradients, full fp32 FMA
+// arithmetic): fp32 inputs (held to 1e-4 of each tensor's largest magnitude)
+// and bf16 inputs whose widths have no tensor-core tiles (widened to fp32 on
+// load, gradients rounded to bf16 on store).  Two passes, one warp per row; lane l owns columns l, l+32, ...
 // of the row vectors, and every dot product is a warp reduction:
 //
 //   dQ pass   one warp per query row t: first D_t = sum_j w_tj dW_tj from its
@@ -31,10 +32,17 @@
 // (the chain rule through the maps of "Softmax-Free Attention in JAX/Flax
 // NNX", section "One module, two compatibility functions", and "s^tau: a
 // focal-length knob for attention", core formula).
+#include <cuda_bf16.h>
+
 #include "kernels.h"
 
 namespace cattn {
 namespace bwds {
+
+__device__ __forceinline__ float ldf(const float *p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void stf(float *p, float v) { *p = v; }
+__device__ __forceinline__ void stf(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
 
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int WARPS = 4;  // rows per 128-thread block
@@ -94,8 +102,10 @@ __device__ __forceinline__ Pair pair(float dot, float dw, float d2, float Lt, fl
   return r;
 }
 
-template <int VARIANT, int DK, int DV, int YM>
+template <int VARIANT, int DK, int DV, int YM, typename T>
 __global__ void __launch_bounds__(WARPS * 32) dq_kernel(const BwdSimtParams p) {
+  const T *gq = static_cast<const T *>(p.q), *gk = static_cast<const T *>(p.k);
+  const T *gv = static_cast<const T *>(p.v), *gdo = static_cast<const T *>(p.dout);
   constexpr int KC = DK / 32, VC = DV / 32;
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
@@ -110,18 +120,18 @@ __global__ void __launch_bounds__(WARPS * 32) dq_kernel(const BwdSimtParams p) {
   float Lt = VARIANT == kYat ? 0.f : p.row_mass[row];
   float q[KC], dout[VC];
 #pragma unroll
-  for (int i = 0; i < KC; ++i) q[i] = p.q[row * DK + lane + 32 * i];
+  for (int i = 0; i < KC; ++i) q[i] = ldf(gq + row * DK + lane + 32 * i);
 #pragma unroll
-  for (int i = 0; i < VC; ++i) dout[i] = p.dout[row * DV + lane + 32 * i];
+  for (int i = 0; i < VC; ++i) dout[i] = ldf(gdo + row * DV + lane + 32 * i);
   const int n = p.causal ? min(t + 1, p.Tk) : p.Tk;
-  const float *kb = p.k + (size_t)bhk * p.Tk * DK;
-  const float *vb = p.v + (size_t)bhk * p.Tk * DV;
+  const T *kb = gk + (size_t)bhk * p.Tk * DK;
+  const T *vb = gv + (size_t)bhk * p.Tk * DV;
   auto dots = [&](int j, float &dot, float &dw, float &d2) {
     float a = 0.f, c = 0.f, e = 0.f;
     double a64 = 0.0;
 #pragma unroll
     for (int i = 0; i < KC; ++i) {
-      const float kv = kb[(size_t)j * DK + lane + 32 * i];
+      const float kv = ldf(kb + (size_t)j * DK + lane + 32 * i);
       if (VARIANT == kYat) {
         a64 = fma((double)q[i], (double)kv, a64);
         e = fmaf(q[i] - kv, q[i] - kv, e);
@@ -130,7 +140,7 @@ __global__ void __launch_bounds__(WARPS * 32) dq_kernel(const BwdSimtParams p) {
       }
     }
 #pragma unroll
-    for (int i = 0; i < VC; ++i) c = fmaf(dout[i], vb[(size_t)j * DV + lane + 32 * i], c);
+    for (int i = 0; i < VC; ++i) c = fmaf(dout[i], ldf(vb + (size_t)j * DV + lane + 32 * i), c);
     if (VARIANT == kYat) {
       dot = (float)(warp_sum_d(a64) + (double)b);  // the numerator q.k + b
     } else {
@@ -173,17 +183,19 @@ __global__ void __launch_bounds__(WARPS * 32) dq_kernel(const BwdSimtParams p) {
     const Pair r = pair<VARIANT, YM>(dot, dw, d2, Lt, D, p.scale, b, eps, tau);
 #pragma unroll
     for (int i = 0; i < KC; ++i) {
-      const float kv = kb[(size_t)j * DK + lane + 32 * i];
+      const float kv = ldf(kb + (size_t)j * DK + lane + 32 * i);
       dq[i] = fmaf(r.c, kv, dq[i]);
       if (VARIANT == kYat) dq[i] = fmaf(2.f * r.e, q[i] - kv, dq[i]);
     }
   }
 #pragma unroll
-  for (int i = 0; i < KC; ++i) p.dq[row * DK + lane + 32 * i] = dq[i];
+  for (int i = 0; i < KC; ++i) stf(static_cast<T *>(p.dq) + row * DK + lane + 32 * i, dq[i]);
 }
 
-template <int VARIANT, int DK, int DV, int YM>
+template <int VARIANT, int DK, int DV, int YM, typename T>
 __global__ void __launch_bounds__(WARPS * 32) dkv_kernel(const BwdSimtParams p) {
+  const T *gq = static_cast<const T *>(p.q), *gk = static_cast<const T *>(p.k);
+  const T *gv = static_cast<const T *>(p.v), *gdo = static_cast<const T *>(p.dout);
   constexpr int KC = DK / 32, VC = DV / 32;
   const int lane = threadIdx.x & 31;
   const long long krow = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
@@ -195,12 +207,12 @@ __global__ void __launch_bounds__(WARPS * 32) dkv_kernel(const BwdSimtParams p) 
   float k[KC], v[VC], dk[KC], dv[VC];
 #pragma unroll
   for (int i = 0; i < KC; ++i) {
-    k[i] = p.k[krow * DK + lane + 32 * i];
+    k[i] = ldf(gk + krow * DK + lane + 32 * i);
     dk[i] = 0.f;
   }
 #pragma unroll
   for (int i = 0; i < VC; ++i) {
-    v[i] = p.v[krow * DV + lane + 32 * i];
+    v[i] = ldf(gv + krow * DV + lane + 32 * i);
     dv[i] = 0.f;
   }
   for (int hi = 0; hi < group; ++hi) {
@@ -217,7 +229,7 @@ __global__ void __launch_bounds__(WARPS * 32) dkv_kernel(const BwdSimtParams p) 
       double a64 = 0.0;
 #pragma unroll
       for (int i = 0; i < KC; ++i) {
-        q[i] = p.q[row * DK + lane + 32 * i];
+        q[i] = ldf(gq + row * DK + lane + 32 * i);
         if (VARIANT == kYat) {
           a64 = fma((double)q[i], (double)k[i], a64);
           e = fmaf(q[i] - k[i], q[i] - k[i], e);
@@ -227,7 +239,7 @@ __global__ void __launch_bounds__(WARPS * 32) dkv_kernel(const BwdSimtParams p) 
       }
 #pragma unroll
       for (int i = 0; i < VC; ++i) {
-        dout[i] = p.dout[row * DV + lane + 32 * i];
+        dout[i] = ldf(gdo + row * DV + lane + 32 * i);
         c = fmaf(dout[i], v[i], c);
       }
       const float dot = VARIANT == kYat ? (float)(warp_sum_d(a64) + (double)b) : warp_sum(a);
@@ -252,41 +264,57 @@ __global__ void __launch_bounds__(WARPS * 32) dkv_kernel(const BwdSimtParams p) 
     }
   }
 #pragma unroll
-  for (int i = 0; i < KC; ++i) p.dk[krow * DK + lane + 32 * i] = dk[i];
+  for (int i = 0; i < KC; ++i) stf(static_cast<T *>(p.dk) + krow * DK + lane + 32 * i, dk[i]);
 #pragma unroll
-  for (int i = 0; i < VC; ++i) p.dv[krow * DV + lane + 32 * i] = dv[i];
+  for (int i = 0; i < VC; ++i) stf(static_cast<T *>(p.dv) + krow * DV + lane + 32 * i, dv[i]);
 }
 
-template <int VARIANT, int DK, int DV, int YM>
+template <int VARIANT, int DK, int DV, int YM, typename T>
 cudaError_t launch(const BwdSimtParams &p, cudaStream_t s) {
   const long long qrows = (long long)p.B * p.h * p.Tq;
   const long long krows = (long long)p.B * p.hkv * p.Tk;
   if (qrows > 0)
-    dq_kernel<VARIANT, DK, DV, YM><<<(unsigned)((qrows + WARPS - 1) / WARPS), WARPS * 32, 0, s>>>(p);
+    dq_kernel<VARIANT, DK, DV, YM, T>
+        <<<(unsigned)((qrows + WARPS - 1) / WARPS), WARPS * 32, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || krows <= 0) return e;
-  dkv_kernel<VARIANT, DK, DV, YM><<<(unsigned)((krows + WARPS - 1) / WARPS), WARPS * 32, 0, s>>>(p);
+  dkv_kernel<VARIANT, DK, DV, YM, T>
+      <<<(unsigned)((krows + WARPS - 1) / WARPS), WARPS * 32, 0, s>>>(p);
   return cudaGetLastError();
 }
 
-template <int DK, int DV>
+template <int DK, int DV, typename T>
 cudaError_t launch_for(int variant, int yat_m, const BwdSimtParams &p, cudaStream_t s) {
-  if (variant == kSoftmax) return launch<kSoftmax, DK, DV, 1>(p, s);
-  if (variant == kStau) return launch<kStau, DK, DV, 1>(p, s);
-  if (yat_m == 2) return launch<kYat, DK, DV, 2>(p, s);
-  if (yat_m == 3) return launch<kYat, DK, DV, 3>(p, s);
-  return launch<kYat, DK, DV, 1>(p, s);
+  if (variant == kSoftmax) return launch<kSoftmax, DK, DV, 1, T>(p, s);
+  if (variant == kStau) return launch<kStau, DK, DV, 1, T>(p, s);
+  if (yat_m == 2) return launch<kYat, DK, DV, 2, T>(p, s);
+  if (yat_m == 3) return launch<kYat, DK, DV, 3, T>(p, s);
+  return launch<kYat, DK, DV, 1, T>(p, s);
+}
+
+template <typename T>
+cudaError_t by_shape(int variant, int dk, int dv, int yat_m, const BwdSimtParams &p,
+                     cudaStream_t s) {
+  switch (dk * 1000 + dv) {
+    case 32032: return launch_for<32, 32, T>(variant, yat_m, p, s);
+    case 32064: return launch_for<32, 64, T>(variant, yat_m, p, s);
+    case 32128: return launch_for<32, 128, T>(variant, yat_m, p, s);
+    case 64032: return launch_for<64, 32, T>(variant, yat_m, p, s);
+    case 64064: return launch_for<64, 64, T>(variant, yat_m, p, s);
+    case 64128: return launch_for<64, 128, T>(variant, yat_m, p, s);
+    case 128032: return launch_for<128, 32, T>(variant, yat_m, p, s);
+    case 128064: return launch_for<128, 64, T>(variant, yat_m, p, s);
+    case 128128: return launch_for<128, 128, T>(variant, yat_m, p, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace bwds
 
-cudaError_t launch_bwd_simt(int variant, int dk, int dv, int yat_m, const BwdSimtParams &p,
-                            cudaStream_t s) {
-  using namespace bwds;
-  if (dk == 32) return launch_for<32, 32>(variant, yat_m, p, s);
-  if (dk == 64) return launch_for<64, 64>(variant, yat_m, p, s);
-  if (dv == 64) return launch_for<128, 64>(variant, yat_m, p, s);
-  return launch_for<128, 128>(variant, yat_m, p, s);
+cudaError_t launch_bwd_simt(int variant, bool bf16, int dk, int dv, int yat_m,
+                            const BwdSimtParams &p, cudaStream_t s) {
+  return bf16 ? bwds::by_shape<__nv_bfloat16>(variant, dk, dv, yat_m, p, s)
+              : bwds::by_shape<float>(variant, dk, dv, yat_m, p, s);
 }
 
 }  // namespace cattn

@@ -1,8 +1,11 @@
-// fwd_simt.cu -- fp32 attention forward on the CUDA cores.
+// fwd_simt.cu -- attention forward on the CUDA cores.
 //
 // The fp32 problems are held to an output error of 1e-4 * max|v|; tf32
 // tensor-core operands (10-bit mantissa) cannot reach that, so fp32 inputs
-// take this path in full fp32 FMA arithmetic.  One CTA holds 32 query rows of
+// take this path in full fp32 FMA arithmetic.  bf16 inputs whose head widths
+// the tensor-core kernel has no tiles for (any (dk, dv) in {32, 64, 128}^2
+// other than (64, 64), (128, 128), (128, 64)) take it too, widened to fp32
+// on load and rounded to bf16 on store.  One CTA holds 32 query rows of
 // one (batch, head); 8 warps take 4 rows each.  Keys stream through shared
 // memory 32 at a time; lane l owns key l of the tile for the score and owns
 // value columns l, l+32, ... for the weighted sum.
@@ -14,10 +17,17 @@
 //   s^tau    online softmax of sigma = tau * ln(softplus(s) + eps), which is
 //            phi^tau / sum phi^tau ("s^tau: a focal-length knob for attention",
 //            the equivalence with softmax of tau log phi + C).
+#include <cuda_bf16.h>
+
 #include "kernels.h"
 
 namespace cattn {
 namespace simt {
+
+__device__ __forceinline__ float ldf(const float *p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void stf(float *p, float v) { *p = v; }
+__device__ __forceinline__ void stf(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
 
 constexpr int ROWS = 32;  // query rows per CTA
 constexpr int RPW = 4;    // rows per warp
@@ -44,7 +54,7 @@ struct Smem {
   static constexpr int BYTES = (Q + K + V) * 4;
 };
 
-template <int VARIANT, int DK, int DV>
+template <int VARIANT, int DK, int DV, typename T>
 __global__ void __launch_bounds__(THREADS) fwd_kernel(const FwdParams p) {
   using S = Smem<DK, DV>;
   extern __shared__ float sm[];
@@ -60,13 +70,13 @@ __global__ void __launch_bounds__(THREADS) fwd_kernel(const FwdParams p) {
   const int row0 = blockIdx.x * ROWS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const float *q = reinterpret_cast<const float *>(p.q) + (size_t)bh * p.Tq * DK;
-  const float *k = reinterpret_cast<const float *>(p.k) + (size_t)bh_kv * p.Tk * DK;
-  const float *v = reinterpret_cast<const float *>(p.v) + (size_t)bh_kv * p.Tk * DV;
+  const T *q = reinterpret_cast<const T *>(p.q) + (size_t)bh * p.Tq * DK;
+  const T *k = reinterpret_cast<const T *>(p.k) + (size_t)bh_kv * p.Tk * DK;
+  const T *v = reinterpret_cast<const T *>(p.v) + (size_t)bh_kv * p.Tk * DV;
 
   for (int i = threadIdx.x; i < ROWS * DK; i += THREADS) {
     const int r = i / DK, c = i - r * DK;
-    sq[i] = (row0 + r < p.Tq) ? q[(size_t)(row0 + r) * DK + c] : 0.f;
+    sq[i] = (row0 + r < p.Tq) ? ldf(q + (size_t)(row0 + r) * DK + c) : 0.f;
   }
 
   float b = 0.f, eps = 0.f, tau = 1.f;
@@ -93,11 +103,11 @@ __global__ void __launch_bounds__(THREADS) fwd_kernel(const FwdParams p) {
     __syncthreads();
     for (int i = threadIdx.x; i < KT * DK; i += THREADS) {
       const int r = i / DK, c = i - r * DK;
-      sk[r * (DK + 1) + c] = (kt + r < p.Tk) ? k[(size_t)(kt + r) * DK + c] : 0.f;
+      sk[r * (DK + 1) + c] = (kt + r < p.Tk) ? ldf(k + (size_t)(kt + r) * DK + c) : 0.f;
     }
     for (int i = threadIdx.x; i < KT * DV; i += THREADS) {
       const int r = i / DV;
-      sv[i] = (kt + r < p.Tk) ? v[(size_t)kt * DV + i] : 0.f;
+      sv[i] = (kt + r < p.Tk) ? ldf(v + (size_t)kt * DV + i) : 0.f;
     }
     __syncthreads();
 
@@ -163,9 +173,9 @@ __global__ void __launch_bounds__(THREADS) fwd_kernel(const FwdParams p) {
     const int row = row0 + warp * RPW + rr;
     if (row >= p.Tq) continue;
     const float inv = VARIANT == kYat ? 1.f / (l[rr] + 1e-9f) : 1.f / l[rr];
-    float *orow = reinterpret_cast<float *>(p.out) + ((size_t)bh * p.Tq + row) * DV;
+    T *orow = reinterpret_cast<T *>(p.out) + ((size_t)bh * p.Tq + row) * DV;
 #pragma unroll
-    for (int c = 0; c < VC; ++c) orow[lane + 32 * c] = acc[rr][c] * inv;
+    for (int c = 0; c < VC; ++c) stf(orow + lane + 32 * c, acc[rr][c] * inv);
     if (lane == 0) {
       const size_t ti = (size_t)bh * p.Tq + row;
       if (p.row_mass) p.row_mass[ti] = VARIANT == kYat ? l[rr] : m[rr] + logf(l[rr]);
@@ -174,9 +184,9 @@ __global__ void __launch_bounds__(THREADS) fwd_kernel(const FwdParams p) {
   }
 }
 
-template <int VARIANT, int DK, int DV>
+template <int VARIANT, int DK, int DV, typename T>
 cudaError_t launch(const FwdParams &p, cudaStream_t s) {
-  auto kern = fwd_kernel<VARIANT, DK, DV>;
+  auto kern = fwd_kernel<VARIANT, DK, DV, T>;
   constexpr int bytes = Smem<DK, DV>::BYTES;
   static int configured_for = -1;
   int dev = 0;
@@ -193,26 +203,40 @@ cudaError_t launch(const FwdParams &p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <typename T, int V>
+cudaError_t by_shape(int dk, int dv, const FwdParams &p, cudaStream_t s) {
+  switch (dk * 1000 + dv) {
+    case 32032: return launch<V, 32, 32, T>(p, s);
+    case 32064: return launch<V, 32, 64, T>(p, s);
+    case 32128: return launch<V, 32, 128, T>(p, s);
+    case 64032: return launch<V, 64, 32, T>(p, s);
+    case 64064: return launch<V, 64, 64, T>(p, s);
+    case 64128: return launch<V, 64, 128, T>(p, s);
+    case 128032: return launch<V, 128, 32, T>(p, s);
+    case 128064: return launch<V, 128, 64, T>(p, s);
+    case 128128: return launch<V, 128, 128, T>(p, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename T>
+cudaError_t by_variant(int variant, int dk, int dv, const FwdParams &p, cudaStream_t s) {
+  if (variant == kSoftmax) return by_shape<T, kSoftmax>(dk, dv, p, s);
+  if (variant == kYat) return by_shape<T, kYat>(dk, dv, p, s);
+  return by_shape<T, kStau>(dk, dv, p, s);
+}
+
 }  // namespace simt
 
 bool fwd_simt_supported(int dk, int dv) {
-  return (dk == dv && (dk == 32 || dk == 64 || dk == 128)) || (dk == 128 && dv == 64);
+  auto ok = [](int d) { return d == 32 || d == 64 || d == 128; };
+  return ok(dk) && ok(dv);
 }
 
-cudaError_t launch_fwd_simt(int variant, int dk, int dv, const FwdParams &p, cudaStream_t s) {
-#define CATTN_SIMT_CASE(V, DK_, DV_) \
-  if (variant == V && dk == DK_ && dv == DV_) return simt::launch<V, DK_, DV_>(p, s);
-#define CATTN_SIMT_SHAPES(V)      \
-  CATTN_SIMT_CASE(V, 32, 32)      \
-  CATTN_SIMT_CASE(V, 64, 64)      \
-  CATTN_SIMT_CASE(V, 128, 128)    \
-  CATTN_SIMT_CASE(V, 128, 64)
-  CATTN_SIMT_SHAPES(kSoftmax)
-  CATTN_SIMT_SHAPES(kYat)
-  CATTN_SIMT_SHAPES(kStau)
-#undef CATTN_SIMT_SHAPES
-#undef CATTN_SIMT_CASE
-  return cudaErrorInvalidValue;
+cudaError_t launch_fwd_simt(int variant, bool bf16, int dk, int dv, const FwdParams &p,
+                            cudaStream_t s) {
+  return bf16 ? simt::by_variant<__nv_bfloat16>(variant, dk, dv, p, s)
+              : simt::by_variant<float>(variant, dk, dv, p, s);
 }
 
 }  // namespace cattn

@@ -73,8 +73,10 @@ cudaError_t launch_row_stats_tc(int variant, int dk, const FwdParams &p, const C
 cudaError_t launch_tau_finalize(const double *moments, const float *eps, int h, float *tau,
                                 double *moments_out, cudaStream_t s);
 
-// CUDA-core fp32 forward.
-cudaError_t launch_fwd_simt(int variant, int dk, int dv, const FwdParams &p, cudaStream_t s);
+// CUDA-core forward: fp32 inputs, and bf16 inputs whose widths have no
+// tensor-core tiles; any (dk, dv) in {32, 64, 128}^2.
+cudaError_t launch_fwd_simt(int variant, bool bf16, int dk, int dv, const FwdParams &p,
+                            cudaStream_t s);
 bool fwd_simt_supported(int dk, int dv);
 
 // Squared row norms of a bf16 [BH, T, d] tensor into out[BH, T_pad] (zeros
@@ -109,17 +111,19 @@ cudaError_t launch_bwd_prep(int variant, int dk, int dv, const BwdParams &p, con
 // The dK/dV pass, then the dQ pass.
 cudaError_t launch_bwd_tc(int variant, int dk, int dv, int yat_m, const BwdParams &p,
                           const BwdMaps &m, cudaStream_t s);
-// fp32 backward on the CUDA cores (the fp32 forward's shapes).
+// Backward on the CUDA cores: fp32 inputs, and bf16 inputs whose widths have
+// no tensor-core tiles; any (dk, dv) in {32, 64, 128}^2.
 struct BwdSimtParams {
-  const float *q, *k, *v, *dout, *row_mass, *b, *eps, *tau;
-  float *dq, *dk, *dv;
+  const void *q, *k, *v, *dout;  // fp32 or bf16
+  const float *row_mass, *b, *eps, *tau;
+  void *dq, *dk, *dv;            // the inputs' element type
   float *Dbuf;   // [2][B*h*Tq] the rows' D and (Yat) Z, written by the dQ pass
   double *dpar;  // [h][2], zeroed
   int B, h, hkv, Tq, Tk, causal;
   float scale;
 };
-cudaError_t launch_bwd_simt(int variant, int dk, int dv, int yat_m, const BwdSimtParams &p,
-                            cudaStream_t s);
+cudaError_t launch_bwd_simt(int variant, bool bf16, int dk, int dv, int yat_m,
+                            const BwdSimtParams &p, cudaStream_t s);
 
 // The fp64 per-head parameter sums into the fp32 outputs (any may be NULL).
 cudaError_t launch_bwd_param_finalize(int variant, const double *dpar, int h, float *db,

@@ -195,13 +195,12 @@ def test_backward_deterministic_and_empty():
 
 
 def test_backward_rejects_unsupported():
-    q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16, device="cuda")
-    k = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16, device="cuda")
-    v = torch.zeros(1, 1, 4, 128, dtype=torch.bfloat16, device="cuda")
-    out = torch.zeros(1, 1, 4, 128, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(1, 1, 4, 96, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16, device="cuda")
     mass = torch.zeros(1, 1, 4, device="cuda")
     with pytest.raises(ValueError):
-        attention.backward("softmax", q, k, v, out, out, mass)  # (dk, dv) = (64, 128)
+        attention.backward("softmax", q, q, v, out, out, mass)  # dk = 96
     f = torch.zeros(1, 1, 4, 48, device="cuda")
     with pytest.raises(ValueError):
         attention.backward("softmax", f, f, f, f, f, mass)  # fp32 width 48
@@ -313,3 +312,29 @@ def test_backward_yat_cancelling_numerator(dtype):
     num = float(inp["q"][0, 0, 0].double() @ inp["k"][0, 0, 0].double()) + b
     compare_grads(gpu, ora, f"yat cancelling numerator {dtype} (q.k + b = {num:.3g})",
                   tol=GRAD_TOL if dtype == "bf16" else 1e-4)
+
+
+WIDTH_SHAPES = [  # dtype, B, h, hkv, Tq, Tk, dk, dv, causal
+    ("bf16", 1, 2, 1, 100, 100, 32, 32, True),
+    ("bf16", 1, 2, 2, 70, 140, 64, 128, False),
+    ("bf16", 1, 2, 2, 90, 90, 128, 32, True),
+    ("f32", 1, 2, 2, 80, 80, 64, 32, True),
+    ("f32", 1, 2, 1, 50, 120, 32, 128, False),
+]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("shape", WIDTH_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_backward_cuda_core_widths(variant, shape):
+    """Width pairs without tensor-core tiles: the CUDA-core backward for bf16
+    (gradients rounded to bf16: the bf16 bound) and fp32 (the fp32 bound)."""
+    dtype, B, h, hkv, Tq, Tk, dk, dv, causal = shape
+    w = workloads.Workload("bwd_widths", B=B, h=h, hkv=hkv, Tq=Tq, Tk=Tk, dk=dk, dv=dv,
+                           dtype=dtype, causal=causal, yat_param="softplus_uniform",
+                           seed=Tq + dk + 3 * dv)
+    inp = workloads.generate(w)
+    dout = workloads.grad_output(w)
+    gpu = run_gpu_backward(variant, inp, dout, causal=causal, scale=w.scale)
+    ora = oracle.backward(variant, inp["q"], inp["k"], inp["v"], dout, causal=causal,
+                          scale=w.scale, **_params(variant, inp))
+    compare_grads(gpu, ora, f"{variant} {shape}", tol=GRAD_TOL if dtype == "bf16" else 1e-4)

@@ -366,3 +366,26 @@ def test_row_stats_match_oracle(variant, shape):
     np.testing.assert_allclose(pu.to_np(ent), e_o, atol=2e-3)
     np.testing.assert_allclose(pu.to_np(top), t_o, rtol=2e-3, atol=1e-6)
     assert (np.abs(pu.to_np(small) - s_o) * n <= 2.0 + 1e-9).all()
+
+
+# ---------------------------------------------------------------- every width pair
+
+WIDTH_SHAPES = [  # dtype, B, h, hkv, Tq, Tk, dk, dv, causal: widths without tensor-core tiles
+    ("bf16", 1, 2, 1, 100, 100, 32, 32, True),
+    ("bf16", 1, 2, 2, 70, 140, 64, 128, False),
+    ("bf16", 2, 2, 1, 65, 65, 32, 64, True),
+    ("bf16", 1, 2, 2, 90, 90, 128, 32, True),
+    ("f32", 1, 2, 2, 80, 80, 64, 32, True),
+    ("f32", 1, 2, 1, 50, 120, 32, 128, False),
+]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("shape", WIDTH_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_cuda_core_widths(variant, shape):
+    """(dk, dv) pairs the tensor-core kernel has no tiles for run on the
+    CUDA-core kernel (bf16 widened to fp32), each against the oracle."""
+    dtype, B, h, hkv, Tq, Tk, dk, dv, causal = shape
+    w = _wl("widths", B, h, hkv, Tq, Tk, dk, dv, dtype=dtype, causal=causal, seed=Tq + dk + dv)
+    inp = workloads.generate(w)
+    pu.full_parity(variant, inp, causal=causal, scale=w.scale, where=f"{variant} {shape}")

@@ -70,12 +70,27 @@ def validate(lib, variant, p, q=FAKE, k=FAKE, v=FAKE, b=FAKE, eps=FAKE, tau=FAKE
     (dict(scale=-1.0), native.ERR_INVALID_ARG),
     (dict(flags=2), native.ERR_INVALID_ARG),
     (dict(dk=96, dv=96), native.ERR_UNSUPPORTED),
-    (dict(dk=64, dv=128), native.ERR_UNSUPPORTED),
-    (dict(dk=32, dv=32), native.ERR_UNSUPPORTED),       # bf16 needs 64 or 128
+    (dict(dk=64, dv=256), native.ERR_UNSUPPORTED),
+    (dict(dk=48, dv=32), native.ERR_UNSUPPORTED),       # widths are 32, 64 or 128
 ])
 def test_problem_rejections(lib, kw, code):
     assert validate(lib, native.SOFTMAX, prob(**kw)) == code
     assert lib.cattn_workspace_bytes(native.SOFTMAX, ctypes.byref(prob(**kw))) == 0
+
+
+@pytest.mark.parametrize("dk,dv", [(32, 32), (64, 128), (32, 64), (128, 32)])
+def test_cuda_core_widths_need_no_workspace(lib, dk, dv):
+    # bf16 widths without tensor-core tiles run on the CUDA-core kernel, which
+    # needs no workspace; the tensor-core-only passes over q and k (tau*, row
+    # statistics) take a key width of 64 or 128 whatever dv is
+    p = prob(dk=dk, dv=dv)
+    for variant in (native.SOFTMAX, native.YAT, native.STAU):
+        assert lib.cattn_workspace_bytes(variant, ctypes.byref(p)) == 0
+        assert validate(lib, variant, p) == native.OK
+    tc_keys = dk in (64, 128)
+    assert (lib.cattn_tau_star_workspace_bytes(ctypes.byref(p)) > 0) == tc_keys
+    assert (lib.cattn_row_stats_workspace_bytes(native.YAT, ctypes.byref(p)) > 0) == tc_keys
+    assert lib.cattn_backward_workspace_bytes(native.YAT, ctypes.byref(p)) > 0
 
 
 def test_pointer_rejections(lib):
