@@ -61,8 +61,11 @@ typedef struct CUstream_st *cattn_stream_t;
 /* Score-to-weight maps. */
 enum { CATTN_SOFTMAX = 0, CATTN_YAT = 1, CATTN_STAU = 2 };
 
-/* Element type of q, k, v and out.  bf16 runs on the tensor cores (tcgen05,
- * fp32 accumulation); fp32 runs on the CUDA cores in full fp32. */
+/* Element type of q, k, v and out.  Head widths dk, dv: any of 32, 64, 128.
+ * bf16 with (dk, dv) = (64, 64), (128, 128) or (128, 64) runs on the tensor
+ * cores (tcgen05, fp32 accumulation); fp32, and bf16 with the other width
+ * pairs, run on the CUDA cores in full fp32 (bf16 widened on load, rounded
+ * on store). */
 enum { CATTN_F32 = 0, CATTN_BF16 = 1 };
 
 /* cattn_problem_t.flags */
@@ -246,9 +249,9 @@ int cattn_row_stats(int variant, const cattn_problem_t *p, const void *q, const 
  *   dq, dk, dv    shaped and typed like q, k, v; written, never read
  *   db, deps, dtau  fp32 [h] or NULL: the parameter gradients the map has
  *                 (Yat: db, deps; s^tau: deps, dtau; the others untouched)
- * bf16 (tensor cores): (dk, dv) in {(64, 64), (128, 128), (128, 64)}; fp32
- * (CUDA cores): the fp32 forward's widths; yat_m in {0, 1, 2, 3}; anything
- * else is CATTN_ERR_UNSUPPORTED.  A problem with no query rows writes zeros.  The
+ * Widths as for the forward (the tensor cores for bf16 (64, 64), (128, 128),
+ * (128, 64); the CUDA cores otherwise); yat_m in {0, 1, 2, 3}; anything else
+ * is CATTN_ERR_UNSUPPORTED.  A problem with no query rows writes zeros.  The
  * kernels' accumulation order is fixed: repeated calls give identical bits
  * for dq, dk and dv (the fp64 parameter sums use atomics).
  * cattn_backward_workspace_bytes: bytes needed (0 if the problem is

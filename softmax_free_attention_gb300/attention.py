@@ -220,8 +220,8 @@ def backward(variant, q, k, v, out, dout, row_mass, *, b=None, eps=None, tau=Non
     """Gradients of sum(dout * out) for the forward that produced ``out`` and
     ``row_mass`` from the same inputs and map.
 
-    CUDA tensors: bf16 with (dk, dv) in {(64, 64), (128, 128), (128, 64)}, or
-    fp32 with the fp32 forward's widths.  Returns (dq, dk, dv, dparams):
+    CUDA tensors, bf16 or fp32, widths as for the forward.  Returns
+    (dq, dk, dv, dparams):
     dq, dk, dv shaped and typed like q, k, v (GQA: dk, dv summed over the query
     heads sharing a kv head); dparams a dict of fp32 [h] tensors -- Yat:
     'b', 'eps'; s^tau: 'eps', 'tau'; softmax: empty.  Runs asynchronously on
@@ -240,8 +240,7 @@ def backward(variant, q, k, v, out, dout, row_mass, *, b=None, eps=None, tau=Non
     lib = native.load()
     need = int(lib.cattn_backward_workspace_bytes(vid, ctypes.byref(prob)))
     if need == 0:
-        raise ValueError("unsupported problem for the backward (bf16: (dk, dv) in "
-                         "{(64, 64), (128, 128), (128, 64)}; fp32: the forward's widths)")
+        raise ValueError("unsupported problem for the backward (widths 32, 64 or 128)")
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     bt = _per_head(b, h, dev, "b") if vid == native.YAT else None
