@@ -47,10 +47,11 @@
 // TMEM (512 columns): S[2] at 0 and 64, dP[2] at 128 and 192, the first
 // accumulator (dV, or dQ) at 256, the second (dK) at 256 + DV.
 //
-// Warp roles (576 threads): warps 0-15 map (warp w: TMEM lanes 32 (w % 4)..+31
+// Warp roles (608 threads): warps 0-15 map (warp w: TMEM lanes 32 (w % 4)..+31
 // = rows of the resident tile, tile columns [16 (w / 4), +16); four warps per
 // SM sub-partition hide each other's TMEM and SFU latencies), warp 16 issues
-// the TMA loads, warp 17 allocates TMEM and issues the MMAs from one lane.
+// the TMA loads, warp 17 allocates TMEM and issues the accumulating MMAs,
+// warp 18 issues the S and dP MMAs.
 // Every mbarrier wait is bounded (2 s of %globaltimer); on expiry the kernel
 // records a site code, raises a CTA-wide abort flag and every role leaves its
 // loop, waits for its own copies and MMAs in flight, and TMEM is released.
@@ -70,10 +71,11 @@ namespace bwd {
 
 constexpr int RT = 128;  // rows of the resident tile (TMEM lanes)
 constexpr int CT = 64;   // rows of a streamed tile = columns of S
-constexpr int NUM_THREADS = 576;
+constexpr int NUM_THREADS = 608;
 constexpr int MAP_WARPS = 16;
 constexpr int PRODUCER_WARP = 16;
-constexpr int MMA_WARP = 17;
+constexpr int MMA_WARP = 17;    // the accumulating MMAs (and TMEM allocation)
+constexpr int SCORE_WARP = 18;  // the S and dP MMAs
 constexpr int NQ = MAP_WARPS / 4;  // column slices of a tile: four map warps per TMEM lane quadrant
 constexpr int CW = CT / NQ;        // columns per map warp (16)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
@@ -391,7 +393,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar_wc_full, MAP_WARPS * 32);
     mbar_init(bar_wc_empty, 1);
     mbar_init(bar_acc, 1);
-    mbar_init(bar_drain, 1);
+    mbar_init(bar_drain, 2);  // the commits of both issuing warps
     *abort = 0;
     fence_mbar_init();
   }
@@ -447,34 +449,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int m = issued >= NS ? issued - NS : 0; m < issued; ++m)
         thread_wait(x_full(m % NS), (m / NS) & 1, abort, SITE_PRODUCER | 0x30, false);
     }
-  } else if (warp == MMA_WARP) {
-    {
-      bool ok = warp_wait(bar_r_full, 0, abort, SITE_MMA | 0x10);
-      // descriptors: K-major views of the resident tiles, the W / C tiles and
-      // stage 0's streamed tiles; N-major views of stage 0's streamed tiles
+  } else if (warp == MMA_WARP || warp == SCORE_WARP) {
+    // Two issuing warps, each converged with an elected lane issuing: the
+    // score warp issues S and dP of tile n as soon as its stage has landed
+    // and the map warps have read tile n-2 out of its TMEM buffer; the MMA
+    // warp issues the accumulating MMAs of tile m once the map warps have
+    // written its W and C.  (A single issuer serialised the two streams; the
+    // issuing warps share their SM sub-partitions with busy map warps, so each
+    // MMA takes tens of cycles to issue.)  Neither stream reads what the other
+    // writes except through the mbarriers: S(n) has completed before the map
+    // warps start tile n, so the commit after acc(n) also frees its stage.
+    bool ok = warp_wait(bar_r_full, 0, abort, SITE_MMA | 0x10);
+    auto stage_off = [](int st) { return (uint64_t)((st * L::STAGE) >> 4); };
+    if (warp == SCORE_WARP) {
+      // descriptors: K-major views of the resident tiles and stage 0's streamed tiles
       const uint64_t dR = smem_desc_sw128(r_smem, 16, 1024);
       const uint64_t dRP = smem_desc_sw128(rp_smem, 16, 1024);
-      const uint64_t dW = smem_desc_sw128(w_smem, 16, 1024);
-      const uint64_t dC = smem_desc_sw128(c_smem, 16, 1024);
       const uint64_t dX0 = smem_desc_sw128(x_smem(0), 16, 1024);
       const uint64_t dXP0 = smem_desc_sw128(xp_smem(0), 16, 1024);
-      const uint64_t nX0 = smem_desc_sw128(x_smem(0), CT * 128, 1024);
-      const uint64_t nXP0 = smem_desc_sw128(xp_smem(0), CT * 128, 1024);
-      auto stage_off = [](int st) { return (uint64_t)((st * L::STAGE) >> 4); };
-      auto do_acc = [&](int m) -> bool {
-        const int st = m % NS;
-        if (!warp_wait(bar_wc_full, m & 1, abort, SITE_MMA | 0x20)) return false;
-        tc_fence_after();
-        if constexpr (KV) {
-          issue_acc<DV>(tmem + TM_A1, dW, nXP0 + stage_off(st), m > 0);      // dV += W^T dout
-          issue_acc<DK>(tmem + TM_A1 + DV, dC, nX0 + stage_off(st), m > 0);  // dK += C^T Q
-        } else {
-          issue_acc<DK>(tmem + TM_A1, dC, nX0 + stage_off(st), m > 0);  // dQ += C K
-        }
-        mma_commit_e(x_empty(st));
-        mma_commit_e(bar_wc_empty);
-        return true;
-      };
       for (int n = 0; ok && n < n_tiles; ++n) {
         const int b = n & 1, st = n % NS;
         if (!(ok = warp_wait(x_full(st), (n / NS) & 1, abort, SITE_MMA | 0x30))) break;
@@ -484,14 +476,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         issue_scores<DK>(tmem + TM_S + 64u * b, dR, dX0 + stage_off(st));
         issue_scores<DV>(tmem + TM_DP + 64u * b, dRP, dXP0 + stage_off(st));
         mma_commit_e(s_full(b));
-        if (!DP && n >= 1) ok = do_acc(n - 1);
       }
-      if (!DP && ok && n_tiles > 0) ok = do_acc(n_tiles - 1);
-      if (!DP && ok) mma_commit_e(bar_acc);
-      // every MMA this thread issued has completed once `drain` flips
-      mma_commit_e(bar_drain);
-      warp_wait(bar_drain, 0, abort, SITE_MMA | 0x50, false);
+    } else if constexpr (!DP) {
+      // descriptors: the W / C tiles (K-major) and stage 0's streamed tiles (N-major)
+      const uint64_t dW = smem_desc_sw128(w_smem, 16, 1024);
+      const uint64_t dC = smem_desc_sw128(c_smem, 16, 1024);
+      const uint64_t nX0 = smem_desc_sw128(x_smem(0), CT * 128, 1024);
+      const uint64_t nXP0 = smem_desc_sw128(xp_smem(0), CT * 128, 1024);
+      for (int m = 0; ok && m < n_tiles; ++m) {
+        const int st = m % NS;
+        if (!(ok = warp_wait(bar_wc_full, m & 1, abort, SITE_MMA | 0x20))) break;
+        tc_fence_after();
+        if constexpr (KV) {
+          issue_acc<DV>(tmem + TM_A1, dW, nXP0 + stage_off(st), m > 0);      // dV += W^T dout
+          issue_acc<DK>(tmem + TM_A1 + DV, dC, nX0 + stage_off(st), m > 0);  // dK += C^T Q
+        } else {
+          issue_acc<DK>(tmem + TM_A1, dC, nX0 + stage_off(st), m > 0);  // dQ += C K
+        }
+        mma_commit_e(x_empty(st));
+        mma_commit_e(bar_wc_empty);
+      }
+      if (ok) mma_commit_e(bar_acc);
     }
+    // every MMA either warp issued has completed once `drain` flips
+    mma_commit_e(bar_drain);
+    warp_wait(bar_drain, 0, abort, SITE_MMA | 0x50, false);
   } else {
     // ---- map warps
     const int qd = warp & 3, hf = warp >> 2;  // lane quadrant, column slice
