@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "cattn.h"
+#include "bwd.h"
 #include "kernels.h"
 
 namespace {

@@ -34,6 +34,7 @@
 // focal-length knob for attention", core formula).
 #include <cuda_bf16.h>
 
+#include "bwd.h"
 #include "kernels.h"
 
 namespace cattn {

@@ -59,6 +59,7 @@
 
 #include <type_traits>
 
+#include "bwd.h"
 #include "kernels.h"
 #include "maps.cuh"
 #include "ptx.cuh"
