@@ -84,6 +84,8 @@ BWD_SHAPES = [
     (1, 4, 2, 200, 700, 128, False),
     (1, 1, 1, 1, 129, 64, False),
     (1, 2, 1, 65, 1000, 64, False),
+    (1, 8, 2, 200, 200, 64, True),      # four query heads per kv head
+    (2, 4, 1, 150, 400, 128, False),
 ]
 
 

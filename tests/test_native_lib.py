@@ -203,3 +203,53 @@ def test_workload_table_matches_stated_shapes():
     assert not w["cfg5_cross"].causal
     rows = workloads.sample_rows(w["cfg2_s1"])
     assert rows.min() >= 0 and rows.max() < 32 * 4 * 256
+
+
+def _bwd(lib, variant, p, *, q=FAKE, k=FAKE, v=FAKE, out=FAKE, dout=FAKE, b=FAKE, eps=FAKE,
+         tau=FAKE, mass=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, ws=FAKE, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = lib.cattn_backward_workspace_bytes(variant, ctypes.byref(p))
+    return lib.cattn_backward(variant, ctypes.byref(p), q, k, v, out, dout, b, eps, tau, mass,
+                              dq, dk, dv, None, None, None, ws, ws_bytes, None)
+
+
+def test_backward_workspace_sizes(lib):
+    # tensor cores: [h][2] fp64 parameter sums + key-norm maximum (256-byte
+    # block), the [B*h, ceil(Tq/128)*128] float4 row scalars, and (Yat) the
+    # key norms [B*hkv, ceil(Tk/128)*128] fp32
+    p = prob(B=2, h=4, hkv=2, Tq=200, Tk=200)
+    sm = lib.cattn_backward_workspace_bytes(native.SOFTMAX, ctypes.byref(p))
+    ya = lib.cattn_backward_workspace_bytes(native.YAT, ctypes.byref(p))
+    assert sm == 256 + 2 * 4 * 256 * 16
+    assert ya == sm + 2 * 2 * 256 * 4
+    # CUDA cores (fp32, or bf16 widths without tensor-core tiles): the rows' D and Z
+    for q in (prob(dtype=native.F32, dk=32, dv=32, Tq=100, Tk=100), prob(dk=32, dv=64)):
+        need = 256 + ((2 * q.B * q.h * q.Tq * 4 + 255) // 256) * 256
+        assert lib.cattn_backward_workspace_bytes(native.YAT, ctypes.byref(q)) == need
+    # unsupported widths and bad problems: 0
+    assert lib.cattn_backward_workspace_bytes(native.YAT, ctypes.byref(prob(dk=96, dv=96))) == 0
+    assert lib.cattn_backward_workspace_bytes(native.YAT, ctypes.byref(prob(h=3, hkv=2))) == 0
+    assert lib.cattn_backward_workspace_bytes(9, ctypes.byref(prob())) == 0
+
+
+def test_backward_argument_errors(lib):
+    # every error below is reported before any CUDA call
+    p = prob()
+    assert lib.cattn_backward(native.SOFTMAX, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None,
+                              FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE, 1 << 20,
+                              None) == native.ERR_INVALID_ARG
+    assert _bwd(lib, 9, p, ws_bytes=1 << 20) == native.ERR_INVALID_ARG          # unknown map
+    assert _bwd(lib, native.SOFTMAX, prob(dk=96, dv=96), ws_bytes=1 << 20) == native.ERR_UNSUPPORTED
+    assert _bwd(lib, native.SOFTMAX, prob(h=3, hkv=2), ws_bytes=1 << 20) == native.ERR_SHAPE
+    for name in ("q", "k", "v", "out", "dout", "mass", "dq", "dk", "dv", "ws"):
+        assert _bwd(lib, native.SOFTMAX, p, **{name: None}) == native.ERR_INVALID_ARG, name
+    for name in ("q", "k", "v", "out", "dout", "dq", "dk", "dv"):
+        assert _bwd(lib, native.SOFTMAX, p, **{name: MISALIGNED}) == native.ERR_UNSUPPORTED, name
+    assert _bwd(lib, native.SOFTMAX, p, ws=ctypes.c_void_p((1 << 20) + 16)) == native.ERR_UNSUPPORTED
+    need = lib.cattn_backward_workspace_bytes(native.YAT, ctypes.byref(p))
+    assert _bwd(lib, native.YAT, p, ws_bytes=need - 1) == native.ERR_SHAPE
+    assert _bwd(lib, native.YAT, p, b=None) == native.ERR_INVALID_ARG
+    assert _bwd(lib, native.YAT, p, eps=None) == native.ERR_INVALID_ARG
+    assert _bwd(lib, native.STAU, p, tau=None) == native.ERR_INVALID_ARG
+    assert _bwd(lib, native.STAU, p, eps=None) == native.ERR_INVALID_ARG
+    assert _bwd(lib, native.SOFTMAX, prob(yat_m=4)) == native.ERR_INVALID_ARG
