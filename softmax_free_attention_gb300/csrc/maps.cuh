@@ -127,6 +127,22 @@ __device__ __forceinline__ float log2_phi(float s, float abs_s_log2e, float eps)
   return lg2_approx(fmaxf(s, 0.f) + l1p + eps);
 }
 
+// log2 phi(s) of two scores with the non-SFU arithmetic in f32x2 pairs (the
+// map is bound by instruction issue; the four SFU operations per score stay).
+__device__ __forceinline__ float2 log2_phi2(float2 d, float scale, float c2, float eps) {
+  constexpr float LN2 = 0.6931471805599453f;
+  const float2 s = __fmul2_rn(d, make_float2(scale, scale));
+  const float2 a = __fmul2_rn(make_float2(fabsf(d.x), fabsf(d.y)), make_float2(c2, c2));
+  const float2 e = make_float2(ex2_approx(-a.x), ex2_approx(-a.y));
+  const float2 u = __fadd2_rn(e, make_float2(1.f, 1.f));
+  float2 l1p = __fmul2_rn(make_float2(lg2_approx(u.x), lg2_approx(u.y)), make_float2(LN2, LN2));
+  l1p.x = e.x < 0x1p-12f ? e.x : l1p.x;
+  l1p.y = e.y < 0x1p-12f ? e.y : l1p.y;
+  const float2 phi = __fadd2_rn(make_float2(fmaxf(s.x, 0.f), fmaxf(s.y, 0.f)),
+                                __fadd2_rn(l1p, make_float2(eps, eps)));
+  return make_float2(lg2_approx(phi.x), lg2_approx(phi.y));
+}
+
 // s^tau over one 32-key chunk: p = 2^(tau log2 phi(s) - m).
 template <bool PARTIAL>
 __device__ __forceinline__ void stau_chunk(const uint32_t (&sr)[32], int c, float scale, float c2,
@@ -135,10 +151,9 @@ __device__ __forceinline__ void stau_chunk(const uint32_t (&sr)[32], int c, floa
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {
     const int col = c * 32 + i;
-    const float d0 = __uint_as_float(sr[i]), d1 = __uint_as_float(sr[i + 1]);
-    const float g0 = log2_phi(d0 * scale, fabsf(d0) * c2, eps);
-    const float g1 = log2_phi(d1 * scale, fabsf(d1) * c2, eps);
-    float2 pr = make_float2(ex2_approx(fmaf(tau, g0, neg_m)), ex2_approx(fmaf(tau, g1, neg_m)));
+    const float2 g = log2_phi2(f2(sr[i], sr[i + 1]), scale, c2, eps);
+    const float2 x = __ffma2_rn(make_float2(tau, tau), g, make_float2(neg_m, neg_m));
+    float2 pr = make_float2(ex2_approx(x.x), ex2_approx(x.y));
     if (PARTIAL) {
       pr.x = col < limit ? pr.x : 0.f;
       pr.y = col + 1 < limit ? pr.y : 0.f;
