@@ -32,7 +32,7 @@
 //            head that shares the kv head, stream through a two-stage ring
 //            with the per-row D, normaliser and |q|^2.  Per tile:
 //              S^T = K Q^T and dP^T = V dout^T     tcgen05, into TMEM
-//              W^T and C^T                          eight warps, into shared memory
+//              W^T and C^T                          the map warps, into TMEM and smem
 //              dV += W^T dout and dK += C^T Q       tcgen05, accumulators in TMEM
 //   SIDE_Q   one CTA per 128-query tile of one (batch, head): Q and dout stay,
 //            64-key tiles of K and V (and the squared key norms) stream.
@@ -45,7 +45,9 @@
 // the accumulating MMAs of tile n run while they map tile n+1.
 //
 // TMEM (512 columns): S[2] at 0 and 64, dP[2] at 128 and 192, the first
-// accumulator (dV, or dQ) at 256, the second (dK) at 256 + DV.
+// accumulator (dV, or dQ) at 256, the second (dK) at 256 + DV.  In the dK/dV
+// pass the map warps write W^T (bf16) over the dP columns they have read, and
+// the dV MMAs take it from there; C^T goes through shared memory.
 //
 // Warp roles (608 threads): warps 0-15 map (warp w: TMEM lanes 32 (w % 4)..+31
 // = rows of the resident tile, tile columns [16 (w / 4), +16); four warps per
@@ -79,6 +81,7 @@ constexpr int MMA_WARP = 17;    // the accumulating MMAs (and TMEM allocation)
 constexpr int SCORE_WARP = 18;  // the S and dP MMAs
 constexpr int NQ = MAP_WARPS / 4;  // column slices of a tile: four map warps per TMEM lane quadrant
 constexpr int CW = CT / NQ;        // columns per map warp (16)
+static_assert(CW == 16, "a map warp's W^T slice is one K step of the dV MMAs");
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr unsigned FULL = 0xffffffffu;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -105,16 +108,17 @@ struct Layout {
   static constexpr int AUX = 1024;  // 64 float4 (SIDE_KV) or 64 floats (SIDE_Q)
   static constexpr int STAGE = X_TILE + XP_TILE + AUX;
   static constexpr int W_TILE = RT * CT * 2;  // one 128-byte swizzle box per row
-  // Stages of the streamed-tile ring: a stage is held from the tile's S MMAs
-  // to its accumulating MMAs, so the ring runs two tiles ahead of the map
-  // warps.  One W / C buffer: the map warps of tile n+1 finish long after the
-  // accumulating MMAs of tile n have read it.
-  static constexpr int NS = SIDE == SIDE_KV ? 3 : 4;
+  // Four stages in the streamed-tile ring: a stage is held from the tile's S
+  // MMAs to its accumulating MMAs and a load takes about two thousand cycles,
+  // so the ring runs three tiles ahead of the map warps.  One C buffer in
+  // shared memory (the map warps of tile n+1 finish long after the MMAs of
+  // tile n have read it); W^T goes to TMEM over the dP columns the map warps
+  // have read, which is what leaves room for the fourth stage.
+  static constexpr int NS = 4;
   static constexpr int OFF_R = 0;
   static constexpr int OFF_RP = R_TILE;
   static constexpr int OFF_ST = R_TILE + RP_TILE;
-  static constexpr int OFF_W = OFF_ST + NS * STAGE;
-  static constexpr int OFF_C = OFF_W + (SIDE == SIDE_KV ? W_TILE : 0);
+  static constexpr int OFF_C = OFF_ST + NS * STAGE;
   static constexpr int OFF_XCH = OFF_C + W_TILE;  // [2][NQ slices][128] floats
   static constexpr int OFF_BAR = OFF_XCH + 2 * NQ * RT * 4;
   // r_full, x_full[NS], x_empty[NS], s_full[2], s_empty[2], wc_full, wc_empty,
@@ -216,6 +220,19 @@ __device__ __forceinline__ void issue_acc(uint32_t d_tmem, uint64_t adesc, uint6
   for (int kk = 0; kk < CT / 16; ++kk)
     mma_ss_e(d_tmem, adesc + (uint64_t)((kk * 32) >> 4), bdesc_n + (uint64_t)((kk * 2048) >> 4),
            IDESC, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// Acc[128 x D] (+)= A[128 x 64] B[64 x D] with A in TMEM (bf16 pairs; K
+// step kk, indices 16 kk .. 16 kk + 15, at columns 16 kk .. 16 kk + 7 from
+// a_tmem) and B a streamed tile read N-major.
+template <int D>
+__device__ __forceinline__ void issue_acc_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc_n,
+                                             bool accumulate) {
+  constexpr uint32_t IDESC = idesc_bf16_f32(RT, D, true);
+#pragma unroll
+  for (int kk = 0; kk < CT / 16; ++kk)
+    mma_ts_e(d_tmem, a_tmem + (uint32_t)kk * 16u, bdesc_n + (uint64_t)((kk * 2048) >> 4), IDESC,
+             (accumulate || kk > 0) ? 1u : 0u);
 }
 
 struct HeadP {
@@ -342,7 +359,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto x_smem = [&](int st) { return sb + L::OFF_ST + (uint32_t)st * L::STAGE; };
   auto xp_smem = [&](int st) { return x_smem(st) + L::X_TILE; };
   auto aux_smem = [&](int st) { return x_smem(st) + L::X_TILE + L::XP_TILE; };
-  const uint32_t w_smem = sb + L::OFF_W, c_smem = sb + L::OFF_C;
+  const uint32_t c_smem = sb + L::OFF_C;
   float *xch = reinterpret_cast<float *>(smem + L::OFF_XCH);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
   volatile int *abort = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
@@ -389,7 +406,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(s_full(b), 1);
-      mbar_init(s_empty(b), MAP_WARPS * 32);
+      // SIDE_KV: the commit after the tile's dV MMAs, which read W^T out of
+      // the dP columns; else every map thread once it has read S and dP
+      mbar_init(s_empty(b), KV ? 1 : MAP_WARPS * 32);
     }
     mbar_init(bar_wc_full, MAP_WARPS * 32);
     mbar_init(bar_wc_empty, 1);
@@ -479,8 +498,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mma_commit_e(s_full(b));
       }
     } else if constexpr (!DP) {
-      // descriptors: the W / C tiles (K-major) and stage 0's streamed tiles (N-major)
-      const uint64_t dW = smem_desc_sw128(w_smem, 16, 1024);
+      // descriptors: the C tile (K-major) and stage 0's streamed tiles (N-major)
       const uint64_t dC = smem_desc_sw128(c_smem, 16, 1024);
       const uint64_t nX0 = smem_desc_sw128(x_smem(0), CT * 128, 1024);
       const uint64_t nXP0 = smem_desc_sw128(xp_smem(0), CT * 128, 1024);
@@ -489,13 +507,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!(ok = warp_wait(bar_wc_full, m & 1, abort, SITE_MMA | 0x20))) break;
         tc_fence_after();
         if constexpr (KV) {
-          issue_acc<DV>(tmem + TM_A1, dW, nXP0 + stage_off(st), m > 0);      // dV += W^T dout
-          issue_acc<DK>(tmem + TM_A1 + DV, dC, nX0 + stage_off(st), m > 0);  // dK += C^T Q
+          // dV += W^T dout (W^T from TMEM), dK += C^T Q
+          issue_acc_ts<DV>(tmem + TM_A1, tmem + TM_DP + 64u * (m & 1), nXP0 + stage_off(st),
+                           m > 0);
+          issue_acc<DK>(tmem + TM_A1 + DV, dC, nX0 + stage_off(st), m > 0);
         } else {
           issue_acc<DK>(tmem + TM_A1, dC, nX0 + stage_off(st), m > 0);  // dQ += C K
         }
         mma_commit_e(x_empty(st));
         mma_commit_e(bar_wc_empty);
+        if constexpr (KV) mma_commit_e(s_empty(m & 1));  // S / dP / W^T buffer free
       }
       if (ok) mma_commit_e(bar_acc);
     }
@@ -544,7 +565,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tmem_ld_fence16(sr);
       tmem_ld_fence16(dr);
       tc_fence_before();
-      mbar_arrive(s_empty(b));
+      if constexpr (!KV) mbar_arrive(s_empty(b));
 
       const int col0 = row0 + CW * hf;  // global index of this thread's first column
       // warp-uniform: is every pair of this warp's 32 x CW block allowed?
@@ -611,7 +632,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) mbar_arrive(x_empty(st));
         continue;
       }
-      // the accumulating MMAs of tile n-1 have read the W / C buffer
+      // W^T of this thread's 16 queries (K step hf of the dV MMAs), as bf16
+      // pairs, over the first 8 of the 16 dP columns this warp itself read
+      if constexpr (KV) tmem_st8(t_lane + TM_DP + 64u * b + 16u * hf, wpk);
+      // the accumulating MMAs of tile n-1 have read the C buffer
       if (n >= 1 && !(ok = warp_wait(bar_wc_empty, (n - 1) & 1, abort, SITE_MAP | 0x20))) break;
       // row r of the 128-byte-swizzled box: logical 16-byte chunk 2 hf + q at
       // physical chunk (2 hf + q) ^ (r % 8)
@@ -619,10 +643,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int q4 = 0; q4 < CW / 8; ++q4) {
         const uint32_t off =
             (uint32_t)r * 128u + (uint32_t)((((CW / 8) * hf + q4) ^ (r & 7)) * 16);
-        if constexpr (KV)
-          sts128(w_smem + off, wpk[4 * q4], wpk[4 * q4 + 1], wpk[4 * q4 + 2], wpk[4 * q4 + 3]);
         sts128(c_smem + off, cpk[4 * q4], cpk[4 * q4 + 1], cpk[4 * q4 + 2], cpk[4 * q4 + 3]);
       }
+      if constexpr (KV) tmem_wait_st();
+      tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(bar_wc_full);
       if constexpr (HAS_PAR) {
