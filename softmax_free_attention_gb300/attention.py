@@ -96,12 +96,17 @@ def forward(variant, q, k, v, *, b=None, eps=None, tau=None, causal=False, scale
 
     Returns (out [B,h,Tq,dv], row_mass [B,h,Tq] or None, row_max [B,h,Tq] or None).
     CUDA tensors: runs asynchronously on the current stream.  CPU tensors: copied
-    to the current CUDA device, computed there, and copied back (synchronous).
+    to the current CUDA device, computed there, and copied back into pinned host
+    tensors (or into the host tensors passed as out / row_mass / row_max),
+    pipelined over HOST_CHUNKS chunks of the batch (synchronous; one library
+    call per chunk, so Yat's key-norm bound and the key split are those of the
+    chunk).
     """
     vid = variant_id(variant)
     if q.device.type == "cpu":
         return _forward_from_host(vid, q, k, v, b=b, eps=eps, tau=tau, causal=causal,
-                                  scale=scale, telemetry=telemetry, yat_m=yat_m)
+                                  scale=scale, telemetry=telemetry, yat_m=yat_m, out=out,
+                                  row_mass=row_mass, row_max=row_max)
     if q.device.type != "cuda":
         raise ValueError("tensors must live on a CUDA device or on the host")
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -136,15 +141,74 @@ def forward(variant, q, k, v, *, b=None, eps=None, tau=None, causal=False, scale
     return out, row_mass, row_max
 
 
-def _forward_from_host(vid, q, k, v, *, b, eps, tau, causal, scale, telemetry, yat_m):
+HOST_CHUNKS = 8  # batch chunks of the host-buffer forward (copy / compute overlap)
+
+
+def _forward_from_host(vid, q, k, v, *, b, eps, tau, causal, scale, telemetry, yat_m,
+                       out=None, row_mass=None, row_max=None, chunks=None):
+    """The forward of host tensors, pipelined over chunks of the batch: chunk
+    i+1 is copied in on one stream while chunk i is computed on the current
+    stream and chunk i-1 is copied out on a third, into the host outputs
+    (the caller's, else new pinned tensors).  Batch entries are independent
+    problems, so each chunk is one library call on its slice.  Returns once
+    the outputs are on the host.  Pinned buffers let the copies overlap the
+    computation; pageable ones still give the right result, with the copies
+    serialised."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        if t.device.type != "cpu":
+            raise ValueError("q, k, v must all be on the host or all on one CUDA device")
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    make_problem(q, k, v, causal=causal, scale=scale, yat_m=yat_m)  # validates the shapes
     dev = torch.device("cuda", torch.cuda.current_device())
-    qd = q.to(dev, non_blocking=True)
-    kd = k.to(dev, non_blocking=True)
-    vd = v.to(dev, non_blocking=True)
-    o, m, x = forward(vid, qd, kd, vd, b=b, eps=eps, tau=tau, causal=causal, scale=scale,
-                      telemetry=telemetry, yat_m=yat_m)
-    res = (o.to("cpu"), None if m is None else m.to("cpu"), None if x is None else x.to("cpu"))
-    return res
+    B, h, Tq, _ = q.shape
+    dv = v.shape[-1]
+    n = max(1, min(B, HOST_CHUNKS if chunks is None else int(chunks)))
+    edges = [B * i // n for i in range(n + 1)]
+    def host_out(t, shape, dtype, name):
+        if t is None:
+            return torch.empty(shape, dtype=dtype, pin_memory=True)
+        if t.device.type != "cpu" or tuple(t.shape) != shape or t.dtype != dtype or \
+                not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor of shape {shape}, {dtype}")
+        return t
+
+    out = host_out(out, (B, h, Tq, dv), q.dtype, "out")
+    mass = host_out(row_mass, (B, h, Tq), torch.float32, "row_mass") if telemetry else None
+    mx = host_out(row_max, (B, h, Tq), torch.float32, "row_max") if telemetry else None
+    qd, kd, vd = (torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (q, k, v))
+    od = torch.empty(out.shape, dtype=out.dtype, device=dev)
+    massd = torch.empty(mass.shape, dtype=torch.float32, device=dev) if telemetry else None
+    mxd = torch.empty(mx.shape, dtype=torch.float32, device=dev) if telemetry else None
+    bt = _per_head(b, h, dev, "b") if vid == native.YAT else None
+    et = _per_head(eps, h, dev, "eps") if vid in (native.YAT, native.STAU) else None
+    tt = _per_head(tau, h, dev, "tau") if vid == native.STAU else None
+    compute = torch.cuda.current_stream(dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    s_in.wait_stream(compute)  # the device buffers come from the current stream's pool
+    for i in range(n):
+        a, z = edges[i], edges[i + 1]
+        if a == z:
+            continue
+        loaded = torch.cuda.Event()
+        with torch.cuda.stream(s_in):
+            for src, dst in ((q, qd), (k, kd), (v, vd)):
+                dst[a:z].copy_(src[a:z], non_blocking=True)
+            loaded.record(s_in)
+        compute.wait_event(loaded)
+        forward(vid, qd[a:z], kd[a:z], vd[a:z], b=bt, eps=et, tau=tt, causal=causal, scale=scale,
+                out=od[a:z], row_mass=None if massd is None else massd[a:z],
+                row_max=None if mxd is None else mxd[a:z], telemetry=telemetry, yat_m=yat_m)
+        computed = torch.cuda.Event()
+        computed.record(compute)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(computed)
+            out[a:z].copy_(od[a:z], non_blocking=True)
+            if telemetry:
+                mass[a:z].copy_(massd[a:z], non_blocking=True)
+                mx[a:z].copy_(mxd[a:z], non_blocking=True)
+    s_out.synchronize()
+    return out, mass, mx
 
 
 def tau_star(q, k, eps, *, causal=False, scale=None, return_moments=False, workspace=None):

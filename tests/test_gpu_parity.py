@@ -196,6 +196,44 @@ def test_host_tensors_round_trip():
     assert torch.equal(host[0], dev[0].cpu()) and torch.equal(host[1], dev[1].cpu())
 
 
+@pytest.mark.parametrize("variant,causal,hkv", [("yat", True, 4), ("stau", False, 2),
+                                                 ("softmax", False, 4)])
+def test_host_tensors_pipelined_chunks(variant, causal, hkv):
+    """The host-buffer forward runs one library call per batch chunk, with the
+    copies on their own streams; each chunk must equal the same call made on
+    device tensors, bit for bit, outputs and telemetry alike."""
+    w = _wl("host_chunks", 6, 4, hkv, 200, 200 if causal else 330, 64, 64, causal=causal,
+            qk=2.0, seed=11)
+    inp = workloads.generate(w)
+    kw = {"yat": dict(b=inp["yat_b"], eps=inp["yat_eps"]), "softmax": {},
+          "stau": dict(eps=inp["stau_eps"], tau=inp["tau"])}[variant]
+    pinned = {n: inp[n].pin_memory() for n in ("q", "k", "v")}
+    host = attention.forward(variant, pinned["q"], pinned["k"], pinned["v"], causal=causal,
+                             scale=w.scale, **kw)
+    assert all(t.device.type == "cpu" for t in host)
+    n = min(w.B, attention.HOST_CHUNKS)
+    edges = [w.B * i // n for i in range(n + 1)]
+    for a, z in zip(edges[:-1], edges[1:]):
+        dev = attention.forward(variant, *(inp[x][a:z].contiguous().cuda() for x in ("q", "k", "v")),
+                                causal=causal, scale=w.scale, **kw)
+        torch.cuda.synchronize()
+        for got, want in zip(host, dev):
+            assert torch.equal(got[a:z], want.cpu())
+    # the caller's own (pageable) host outputs get the same values
+    mine = (torch.empty_like(host[0]), torch.empty_like(host[1]), torch.empty_like(host[2]))
+    attention.forward(variant, pinned["q"], pinned["k"], pinned["v"], causal=causal,
+                      scale=w.scale, out=mine[0], row_mass=mine[1], row_max=mine[2], **kw)
+    assert all(torch.equal(a, b) for a, b in zip(mine, host))
+    # one chunk gives the same answer within the tolerance (Yat's fast-path
+    # bound and the key split depend on the whole call)
+    one = attention._forward_from_host(attention.variant_id(variant), pinned["q"], pinned["k"],
+                                       pinned["v"], b=kw.get("b"), eps=kw.get("eps"),
+                                       tau=kw.get("tau"), causal=causal, scale=w.scale,
+                                       telemetry=True, yat_m=1, chunks=1)
+    vmax = float(inp["v"].abs().max())
+    assert float((one[0].float() - host[0].float()).abs().max()) <= 2e-2 * vmax
+
+
 def test_empty_problems():
     q = torch.zeros(0, 2, 16, 64, dtype=torch.bfloat16, device="cuda")
     k = torch.zeros(0, 2, 16, 64, dtype=torch.bfloat16, device="cuda")
