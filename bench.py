@@ -443,8 +443,8 @@ def main():
         e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, world, dev)
         e2e = {"value": job_tflops(flops, 1, e2e_s, world), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
-               "pipeline": f"{min(w.B, attention.HOST_CHUNKS)} batch chunks; copies in, "
-                           "kernels and copies out on three streams"}
+               "pipeline": f"cattn_forward_host: {min(w.B, attention.HOST_CHUNKS)} batch "
+                           "chunks; copies in, kernels and copies out on three streams"}
 
     # ---- CPU baseline: the oracle on the host cores, bounded sample
     cpu = None

@@ -178,6 +178,51 @@ int cattn_forward_noalloc(int variant, const cattn_problem_t *p, const void *q, 
                           void *out, float *row_mass, float *row_max_score,
                           cattn_stream_t stream);
 
+/* The forward of q, k, v held in HOST memory, with the outputs written back
+ * to host memory: the computation of cattn_forward (the same maps, pages and
+ * sections as above) plus the data movement, pipelined over `chunks` chunks
+ * of the batch.  Batch entries are independent problems, so chunk c (batch
+ * entries [B*c/n, B*(c+1)/n), n = min(chunks, B, 64)) is one cattn_forward
+ * call on its slice, and its results equal those of that call bit for bit.
+ * Chunk c+1 is copied in on `copy_in` while chunk c runs on `compute` and
+ * chunk c-1 is copied out on `copy_out`.
+ *
+ * q_host, k_host, v_host: host [B,h,Tq,dk], [B,hkv,Tk,dk], [B,hkv,Tk,dv];
+ * out_host [B,h,Tq,dv]; row_mass_host, row_max_host: host fp32 [B,h,Tq] or
+ * NULL.  Page-locked host memory lets the copies overlap the computation;
+ * pageable memory gives the same results with the copies serialised by the
+ * CUDA runtime.  b, eps, tau: DEVICE fp32 [h], as for cattn_forward.
+ * q_dev, k_dev, v_dev, out_dev: device staging buffers of the full shapes
+ * above (16-byte aligned); row_mass_dev / row_max_dev: device fp32 [B,h,Tq],
+ * NULL exactly when the host telemetry pointer is NULL.  workspace: at least
+ * cattn_forward_host_workspace_bytes() bytes (the workspace of the largest
+ * chunk; the chunks share it).  The caller owns every buffer; nothing is
+ * allocated per call.
+ *
+ * Asynchronous: the call returns once everything is enqueued; the host
+ * outputs are complete when `copy_out` (or `compute`, which is made to wait
+ * for the last copy out) has drained, and no host input may change before
+ * `copy_in` has.  Work the caller enqueued earlier on `compute` finishes
+ * before the copies touch the staging buffers.  The three streams may be the
+ * same stream (then nothing overlaps).  The first call on a device creates
+ * the library's pool of 130 CUDA events for that device, kept until exit;
+ * make it before any stream capture.  Calls from several host threads are
+ * enqueued one at a time.
+ *
+ * Errors: as cattn_forward, checked for every chunk size before anything is
+ * enqueued; CATTN_ERR_INVALID_ARG also for chunks < 1, a NULL host pointer,
+ * mismatched telemetry pointers, or CATTN_FLAG_NORMS_READY (the key norms
+ * are computed per chunk).  A CUDA error while enqueuing returns
+ * CATTN_ERR_CUDA with the chunks before it already enqueued. */
+size_t cattn_forward_host_workspace_bytes(int variant, const cattn_problem_t *p, int chunks);
+int cattn_forward_host(int variant, const cattn_problem_t *p, const void *q_host,
+                       const void *k_host, const void *v_host, const float *b, const float *eps,
+                       const float *tau, void *out_host, float *row_mass_host,
+                       float *row_max_host, void *q_dev, void *k_dev, void *v_dev, void *out_dev,
+                       float *row_mass_dev, float *row_max_dev, void *workspace,
+                       size_t workspace_bytes, int chunks, cattn_stream_t compute,
+                       cattn_stream_t copy_in, cattn_stream_t copy_out);
+
 /* tau* of the s^tau map, per query head, from one pass over the softmax
  * scores ("s^tau: a focal-length knob for attention", the closed-form
  * paragraph): tau*_i = Cov(s, ln phi(s)) / Var(ln phi(s)) over the scores

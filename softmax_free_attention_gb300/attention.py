@@ -146,25 +146,21 @@ HOST_CHUNKS = 8  # batch chunks of the host-buffer forward (copy / compute overl
 
 def _forward_from_host(vid, q, k, v, *, b, eps, tau, causal, scale, telemetry, yat_m,
                        out=None, row_mass=None, row_max=None, chunks=None):
-    """The forward of host tensors, pipelined over chunks of the batch: chunk
-    i+1 is copied in on one stream while chunk i is computed on the current
-    stream and chunk i-1 is copied out on a third, into the host outputs
-    (the caller's, else new pinned tensors).  Batch entries are independent
-    problems, so each chunk is one library call on its slice.  Returns once
-    the outputs are on the host.  Pinned buffers let the copies overlap the
-    computation; pageable ones still give the right result, with the copies
-    serialised."""
+    """Host tensors in, host tensors out, through cattn_forward_host: the
+    library pipelines the copies in, the forward and the copies out over
+    chunks of the batch on three streams (the current stream computes).  The
+    outputs go to the caller's host tensors, else to new pinned ones.
+    Returns once they are on the host."""
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         if t.device.type != "cpu":
             raise ValueError("q, k, v must all be on the host or all on one CUDA device")
         if not t.is_contiguous():
             raise ValueError(f"{n} must be contiguous")
-    make_problem(q, k, v, causal=causal, scale=scale, yat_m=yat_m)  # validates the shapes
+    prob = make_problem(q, k, v, causal=causal, scale=scale, yat_m=yat_m)
     dev = torch.device("cuda", torch.cuda.current_device())
     B, h, Tq, _ = q.shape
     dv = v.shape[-1]
-    n = max(1, min(B, HOST_CHUNKS if chunks is None else int(chunks)))
-    edges = [B * i // n for i in range(n + 1)]
+
     def host_out(t, shape, dtype, name):
         if t is None:
             return torch.empty(shape, dtype=dtype, pin_memory=True)
@@ -183,31 +179,19 @@ def _forward_from_host(vid, q, k, v, *, b, eps, tau, causal, scale, telemetry, y
     bt = _per_head(b, h, dev, "b") if vid == native.YAT else None
     et = _per_head(eps, h, dev, "eps") if vid in (native.YAT, native.STAU) else None
     tt = _per_head(tau, h, dev, "tau") if vid == native.STAU else None
+    n = HOST_CHUNKS if chunks is None else int(chunks)
+    lib = native.load()
+    need = int(lib.cattn_forward_host_workspace_bytes(vid, ctypes.byref(prob), n))
+    ws = torch.empty(need, dtype=torch.uint8, device=dev) if need else None
     compute = torch.cuda.current_stream(dev)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    s_in.wait_stream(compute)  # the device buffers come from the current stream's pool
-    for i in range(n):
-        a, z = edges[i], edges[i + 1]
-        if a == z:
-            continue
-        loaded = torch.cuda.Event()
-        with torch.cuda.stream(s_in):
-            for src, dst in ((q, qd), (k, kd), (v, vd)):
-                dst[a:z].copy_(src[a:z], non_blocking=True)
-            loaded.record(s_in)
-        compute.wait_event(loaded)
-        forward(vid, qd[a:z], kd[a:z], vd[a:z], b=bt, eps=et, tau=tt, causal=causal, scale=scale,
-                out=od[a:z], row_mass=None if massd is None else massd[a:z],
-                row_max=None if mxd is None else mxd[a:z], telemetry=telemetry, yat_m=yat_m)
-        computed = torch.cuda.Event()
-        computed.record(compute)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(computed)
-            out[a:z].copy_(od[a:z], non_blocking=True)
-            if telemetry:
-                mass[a:z].copy_(massd[a:z], non_blocking=True)
-                mx[a:z].copy_(mxd[a:z], non_blocking=True)
-    s_out.synchronize()
+    status = lib.cattn_forward_host(
+        vid, ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v), _ptr(bt), _ptr(et), _ptr(tt),
+        _ptr(out), _ptr(mass), _ptr(mx), _ptr(qd), _ptr(kd), _ptr(vd), _ptr(od), _ptr(massd),
+        _ptr(mxd), _ptr(ws), need, n, ctypes.c_void_p(compute.cuda_stream),
+        ctypes.c_void_p(s_in.cuda_stream), ctypes.c_void_p(s_out.cuda_stream))
+    native.check(status, "cattn_forward_host")
+    compute.synchronize()  # it waits for the last copy out
     return out, mass, mx
 
 

@@ -27,6 +27,7 @@ ERR_SCRATCH_LIMIT = 6
 # every symbol include/cattn.h declares
 EXPORTS = ("cattn_version", "cattn_error_string", "cattn_workspace_bytes", "cattn_validate",
            "cattn_key_norms", "cattn_forward", "cattn_forward_noalloc",
+           "cattn_forward_host_workspace_bytes", "cattn_forward_host",
            "cattn_tau_star_workspace_bytes", "cattn_tau_star", "cattn_row_stats_workspace_bytes",
            "cattn_row_stats", "cattn_backward_workspace_bytes", "cattn_backward",
            "cattn_check_status")
@@ -77,6 +78,10 @@ def load():
     lib.cattn_forward.restype = i
     lib.cattn_forward_noalloc.argtypes = [i, pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.cattn_forward_noalloc.restype = i
+    lib.cattn_forward_host_workspace_bytes.argtypes = [i, pp, i]
+    lib.cattn_forward_host_workspace_bytes.restype = sz
+    lib.cattn_forward_host.argtypes = [i, pp] + [vp] * 16 + [sz, i, vp, vp, vp]
+    lib.cattn_forward_host.restype = i
     lib.cattn_tau_star_workspace_bytes.argtypes = [pp]
     lib.cattn_tau_star_workspace_bytes.restype = sz
     lib.cattn_tau_star.argtypes = [pp, vp, vp, vp, vp, vp, vp, sz, vp]

@@ -196,14 +196,17 @@ def test_host_tensors_round_trip():
     assert torch.equal(host[0], dev[0].cpu()) and torch.equal(host[1], dev[1].cpu())
 
 
-@pytest.mark.parametrize("variant,causal,hkv", [("yat", True, 4), ("stau", False, 2),
-                                                 ("softmax", False, 4)])
-def test_host_tensors_pipelined_chunks(variant, causal, hkv):
-    """The host-buffer forward runs one library call per batch chunk, with the
-    copies on their own streams; each chunk must equal the same call made on
-    device tensors, bit for bit, outputs and telemetry alike."""
-    w = _wl("host_chunks", 6, 4, hkv, 200, 200 if causal else 330, 64, 64, causal=causal,
-            qk=2.0, seed=11)
+@pytest.mark.parametrize("variant,causal,hkv,dtype", [("yat", True, 4, "bf16"),
+                                                       ("stau", False, 2, "bf16"),
+                                                       ("softmax", False, 4, "bf16"),
+                                                       ("yat", True, 2, "f32")])
+def test_host_tensors_pipelined_chunks(variant, causal, hkv, dtype):
+    """The host-buffer forward (cattn_forward_host) runs one forward per batch
+    chunk, with the copies on their own streams; each chunk must equal the
+    same call made on device tensors, bit for bit, outputs and telemetry
+    alike."""
+    w = _wl("host_chunks", 6, 4, hkv, 200, 200 if causal else 330, 64, 64, dtype=dtype,
+            causal=causal, qk=2.0, seed=11)
     inp = workloads.generate(w)
     kw = {"yat": dict(b=inp["yat_b"], eps=inp["yat_eps"]), "softmax": {},
           "stau": dict(eps=inp["stau_eps"], tau=inp["tau"])}[variant]
@@ -232,6 +235,35 @@ def test_host_tensors_pipelined_chunks(variant, causal, hkv):
                                        telemetry=True, yat_m=1, chunks=1)
     vmax = float(inp["v"].abs().max())
     assert float((one[0].float() - host[0].float()).abs().max()) <= 2e-2 * vmax
+
+
+def test_host_entry_on_one_stream_and_empty():
+    """cattn_forward_host with one stream for all three roles (nothing
+    overlaps) gives the same bits; an empty batch is a no-op."""
+    import ctypes
+    from softmax_free_attention_gb300 import native
+    # causal: never split over keys, so the chunking cannot change a bit
+    w = _wl("host_one_stream", 5, 2, 2, 130, 130, 128, 64, causal=True, seed=12)
+    inp = workloads.generate(w)
+    q, k, v = (inp[n].contiguous() for n in ("q", "k", "v"))
+    ref = attention.forward("softmax", q, k, v, causal=True, scale=w.scale)
+    prob = attention.make_problem(q, k, v, causal=True, scale=w.scale)
+    lib = native.load()
+    need = int(lib.cattn_forward_host_workspace_bytes(native.SOFTMAX, ctypes.byref(prob), 3))
+    dev = [torch.empty(t.shape, dtype=t.dtype, device="cuda") for t in (q, k, v, ref[0])]
+    tel = [torch.empty(ref[1].shape, device="cuda") for _ in range(2)]
+    out = [torch.empty_like(ref[0]), torch.empty_like(ref[1]), torch.empty_like(ref[2])]
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    p = lambda t: ctypes.c_void_p(t.data_ptr())
+    st = lib.cattn_forward_host(native.SOFTMAX, ctypes.byref(prob), p(q), p(k), p(v), None, None,
+                                None, p(out[0]), p(out[1]), p(out[2]), *(p(t) for t in dev),
+                                p(tel[0]), p(tel[1]), p(ws), need, 3, s, s, s)
+    assert st == native.OK
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(out, ref))
+    e = attention.forward("softmax", q[:0], k[:0], v[:0], causal=True)
+    assert e[0].shape == (0, 2, 130, 64)
 
 
 def test_empty_problems():

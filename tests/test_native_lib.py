@@ -253,3 +253,44 @@ def test_backward_argument_errors(lib):
     assert _bwd(lib, native.STAU, p, tau=None) == native.ERR_INVALID_ARG
     assert _bwd(lib, native.STAU, p, eps=None) == native.ERR_INVALID_ARG
     assert _bwd(lib, native.SOFTMAX, prob(yat_m=4)) == native.ERR_INVALID_ARG
+
+
+def test_host_forward_workspace_and_argument_checks(lib):
+    """cattn_forward_host sizes its workspace for the largest chunk and
+    rejects bad arguments on the host, before any CUDA call."""
+    ws = lambda v, p: lib.cattn_workspace_bytes(v, ctypes.byref(p))
+    hws = lambda v, p, n: lib.cattn_forward_host_workspace_bytes(v, ctypes.byref(p), n)
+    p = prob(B=16, h=4, hkv=2, Tq=300, Tk=300, dk=64, dv=64)
+    assert hws(native.YAT, p, 8) == ws(native.YAT, prob(B=2, h=4, hkv=2, Tq=300, Tk=300, dk=64,
+                                                        dv=64))
+    assert hws(native.YAT, p, 1) == ws(native.YAT, p)
+    # 16 entries in 3 chunks: sizes 5 and 6; the larger one's workspace
+    assert hws(native.YAT, p, 3) == ws(native.YAT, prob(B=6, h=4, hkv=2, Tq=300, Tk=300, dk=64,
+                                                        dv=64))
+    # more chunks than batch entries: one entry per chunk
+    assert hws(native.SOFTMAX, p, 100) == ws(native.SOFTMAX, prob(B=1, h=4, hkv=2, Tq=300,
+                                                                  Tk=300, dk=64, dv=64))
+    # split problems need more room per entry when there are fewer units:
+    # the size is the larger of the two chunk sizes' workspaces
+    ps = prob(B=3, h=2, hkv=2, Tq=200, Tk=2100, causal=0)
+    assert hws(native.SOFTMAX, ps, 2) == max(ws(native.SOFTMAX, prob(B=1, h=2, hkv=2, Tq=200,
+                                                                     Tk=2100, causal=0)),
+                                             ws(native.SOFTMAX, prob(B=2, h=2, hkv=2, Tq=200,
+                                                                     Tk=2100, causal=0)))
+    assert hws(native.SOFTMAX, p, 0) == 0 and hws(native.SOFTMAX, prob(B=0), 4) == 0
+
+    need = hws(native.YAT, p, 4)
+
+    def call(prob_=p, chunks=4, qh=FAKE, mass_h=None, mass_d=None, ws_ptr=FAKE, ws_bytes=need):
+        return lib.cattn_forward_host(native.YAT, ctypes.byref(prob_), qh, FAKE, FAKE, FAKE,
+                                      FAKE, None, FAKE, mass_h, None, FAKE, FAKE, FAKE, FAKE,
+                                      mass_d, None, ws_ptr, ws_bytes, chunks, None, None, None)
+    assert call(chunks=0) == native.ERR_INVALID_ARG
+    assert call(qh=None) == native.ERR_INVALID_ARG
+    assert call(mass_h=FAKE) == native.ERR_INVALID_ARG          # host telemetry, no device one
+    assert call(mass_d=FAKE) == native.ERR_INVALID_ARG
+    assert call(prob_=prob(B=16, h=4, hkv=2, Tq=300, Tk=300, dk=64, dv=64,
+                           flags=native.FLAG_NORMS_READY)) == native.ERR_INVALID_ARG
+    assert call(ws_bytes=need - 1) == native.ERR_SHAPE           # the chunk's workspace
+    assert call(prob_=prob(B=16, h=3, hkv=2)) == native.ERR_SHAPE
+    assert call(prob_=prob(B=0, h=4, hkv=2)) == native.OK        # empty: nothing enqueued
