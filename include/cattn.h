@@ -36,8 +36,9 @@
  *   out [B, h,   Tq, dv]      (same element type as q, k, v)
  *   b, eps, tau: fp32 [h], one value per query head.
  * All data pointers are DEVICE pointers on the current CUDA device and must
- * be 16-byte aligned (cattn_forward_host also takes host buffers, named so).  The caller owns every buffer; the library never
- * allocates, frees or keeps a reference to them after the call returns.
+ * be 16-byte aligned (cattn_forward_host also takes host buffers, named so).
+ * The caller owns every buffer; the library never allocates, frees or keeps
+ * a reference to them after the call returns.
  *
  * Execution.  Every call is asynchronous on `stream` (NULL = legacy default
  * stream) and never synchronises, except cattn_check_status.  Argument
