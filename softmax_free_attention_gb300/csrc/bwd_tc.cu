@@ -264,9 +264,9 @@ __device__ __forceinline__ void pair2(float2 s, float2 dp, float2 X, float2 Y, f
   } else if constexpr (VARIANT == kStau) {
     const float2 sc = __fmul2_rn(s, make_float2(scale, scale));
     const float e0 = ex2_approx(-fabsf(s.x) * c2), e1 = ex2_approx(-fabsf(s.y) * c2);
-    const float l0 = e0 < 0x1p-12f ? e0 : lg2_approx(1.f + e0) * LN2;
-    const float l1 = e1 < 0x1p-12f ? e1 : lg2_approx(1.f + e1) * LN2;
-    const float2 phi = make_float2(fmaxf(sc.x, 0.f) + l0 + hp.eps, fmaxf(sc.y, 0.f) + l1 + hp.eps);
+    // log1p as the forward computes it, so the weights match its normaliser
+    const float2 l = tc::log1p_unit2(make_float2(e0, e1));
+    const float2 phi = make_float2(fmaxf(sc.x, 0.f) + l.x + hp.eps, fmaxf(sc.y, 0.f) + l.y + hp.eps);
     const float2 lp = make_float2(lg2_approx(phi.x), lg2_approx(phi.y));
     const float2 x = __ffma2_rn(make_float2(hp.tau, hp.tau), lp, Y);
     w = make_float2(ex2_approx(x.x), ex2_approx(x.y));

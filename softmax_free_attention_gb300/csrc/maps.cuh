@@ -9,7 +9,8 @@
 //   softmax  2^(scale log2(e) q.k - m)
 //   s^tau    2^(tau log2(softplus(scale q.k) + eps) - m)  ("s^tau: a focal-length
 //            knob for attention": phi^tau with phi = softplus(s) + eps, taken in
-//            the log domain so that phi^tau cannot overflow)
+//            the log domain so that phi^tau cannot overflow; softplus's log1p
+//            by a polynomial, log1p_unit)
 #pragma once
 
 #include <stdint.h>
@@ -119,25 +120,43 @@ __device__ __forceinline__ void softmax_chunk(const uint32_t (&sr)[32], int c, f
   }
 }
 
-// log2(softplus(s) + eps), softplus(s) = max(s, 0) + ln(1 + 2^(-|s| log2 e)).
+// log1p(e) for e in [0, 1] as e P(e), P the degree-5 Chebyshev interpolant
+// of log1p(x)/x on [0, 1] (interpolation at the Chebyshev points, converted
+// to powers of x): relative error below 1e-5 over the whole interval, tiny e
+// included, on the FMA pipe.  Every tensor-core path that forms phi(s) (the
+// s^tau forward map, its running max, the row statistics, tau* and the
+// backward) uses it, so that a backward's weights match the forward's
+// normaliser.
+constexpr float kL1p0 = 0.999990582f, kL1p1 = -0.499314666f, kL1p2 = 0.324849576f,
+                kL1p3 = -0.209079534f, kL1p4 = 0.10013973f, kL1p5 = -0.023443656f;
+__device__ __forceinline__ float log1p_unit(float e) {
+  float p = fmaf(kL1p5, e, kL1p4);
+  p = fmaf(p, e, kL1p3);
+  p = fmaf(p, e, kL1p2);
+  p = fmaf(p, e, kL1p1);
+  p = fmaf(p, e, kL1p0);
+  return e * p;
+}
+__device__ __forceinline__ float2 log1p_unit2(float2 e) {
+  float2 p = __ffma2_rn(make_float2(kL1p5, kL1p5), e, make_float2(kL1p4, kL1p4));
+  p = __ffma2_rn(p, e, make_float2(kL1p3, kL1p3));
+  p = __ffma2_rn(p, e, make_float2(kL1p2, kL1p2));
+  p = __ffma2_rn(p, e, make_float2(kL1p1, kL1p1));
+  p = __ffma2_rn(p, e, make_float2(kL1p0, kL1p0));
+  return __fmul2_rn(e, p);
+}
+
+// log2(softplus(s) + eps), softplus(s) = max(s, 0) + log1p(2^(-|s| log2 e)).
 __device__ __forceinline__ float log2_phi(float s, float abs_s_log2e, float eps) {
-  constexpr float LN2 = 0.6931471805599453f;
-  const float e = ex2_approx(-abs_s_log2e);
-  const float l1p = e < 0x1p-12f ? e : lg2_approx(1.f + e) * LN2;
-  return lg2_approx(fmaxf(s, 0.f) + l1p + eps);
+  return lg2_approx(fmaxf(s, 0.f) + log1p_unit(ex2_approx(-abs_s_log2e)) + eps);
 }
 
 // log2 phi(s) of two scores with the non-SFU arithmetic in f32x2 pairs (the
-// map is bound by instruction issue; the four SFU operations per score stay).
+// map is bound by instruction issue): two SFU operations per score.
 __device__ __forceinline__ float2 log2_phi2(float2 d, float scale, float c2, float eps) {
-  constexpr float LN2 = 0.6931471805599453f;
   const float2 s = __fmul2_rn(d, make_float2(scale, scale));
   const float2 a = __fmul2_rn(make_float2(fabsf(d.x), fabsf(d.y)), make_float2(c2, c2));
-  const float2 e = make_float2(ex2_approx(-a.x), ex2_approx(-a.y));
-  const float2 u = __fadd2_rn(e, make_float2(1.f, 1.f));
-  float2 l1p = __fmul2_rn(make_float2(lg2_approx(u.x), lg2_approx(u.y)), make_float2(LN2, LN2));
-  l1p.x = e.x < 0x1p-12f ? e.x : l1p.x;
-  l1p.y = e.y < 0x1p-12f ? e.y : l1p.y;
+  const float2 l1p = log1p_unit2(make_float2(ex2_approx(-a.x), ex2_approx(-a.y)));
   const float2 phi = __fadd2_rn(make_float2(fmaxf(s.x, 0.f), fmaxf(s.y, 0.f)),
                                 __fadd2_rn(l1p, make_float2(eps, eps)));
   return make_float2(lg2_approx(phi.x), lg2_approx(phi.y));
