@@ -126,7 +126,9 @@ __device__ __forceinline__ void softmax_chunk(const uint32_t (&sr)[32], int c, f
 // included, on the FMA pipe.  Every tensor-core path that forms phi(s) (the
 // s^tau forward map, its running max, the row statistics, tau* and the
 // backward) uses it, so that a backward's weights match the forward's
-// normaliser.
+// normaliser.  The coefficients are numpy's
+// Chebyshev.interpolate(lambda x: log1p(x) / x, 5, domain=[0, 1]) converted
+// to the power basis and rounded to fp32.
 constexpr float kL1p0 = 0.999990582f, kL1p1 = -0.499314666f, kL1p2 = 0.324849576f,
                 kL1p3 = -0.209079534f, kL1p4 = 0.10013973f, kL1p5 = -0.023443656f;
 __device__ __forceinline__ float log1p_unit(float e) {
