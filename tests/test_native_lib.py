@@ -294,3 +294,30 @@ def test_host_forward_workspace_and_argument_checks(lib):
     assert call(ws_bytes=need - 1) == native.ERR_SHAPE           # the chunk's workspace
     assert call(prob_=prob(B=16, h=3, hkv=2)) == native.ERR_SHAPE
     assert call(prob_=prob(B=0, h=4, hkv=2)) == native.OK        # empty: nothing enqueued
+
+
+def test_log1p_polynomial_coefficients():
+    """The s^tau map's log1p(e) = e P(e) on [0, 1] (csrc/maps.cuh): the
+    coefficients as written, evaluated in fp32 Horner form like the kernels,
+    stay within the stated 1e-5 relative error against numpy's log1p, tiny
+    arguments included, and are the degree-5 Chebyshev interpolant they are
+    said to be."""
+    import numpy as np
+    from numpy.polynomial import chebyshev, polynomial
+    with open(os.path.join(ROOT, "softmax_free_attention_gb300", "csrc", "maps.cuh")) as f:
+        text = f.read()
+    coef = {int(i): float(c) for i, c in re.findall(r"kL1p(\d) = (-?[0-9.]+)f", text)}
+    assert sorted(coef) == list(range(6))
+    c32 = [np.float32(coef[i]) for i in range(6)]
+    x = np.concatenate([np.geomspace(1e-30, 1e-3, 2000), np.linspace(1e-3, 1.0, 200001)])
+    x = x.astype(np.float32)
+    p = np.full_like(x, c32[5])
+    for c in c32[4::-1]:
+        p = (p * x + c).astype(np.float32)
+    approx = (x * p).astype(np.float64)
+    exact = np.log1p(x.astype(np.float64))
+    assert (np.abs(approx - exact) / exact).max() < 1e-5
+    # interpolation at the Chebyshev points, which exclude the end points
+    ref = chebyshev.Chebyshev.interpolate(lambda t: np.log1p(t) / t, 5, domain=[0, 1])
+    want = ref.convert(kind=polynomial.Polynomial).coef
+    assert np.allclose(np.float32(want), c32, rtol=0, atol=2e-7)
