@@ -264,9 +264,8 @@ __device__ __forceinline__ void pair2(float2 s, float2 dp, float2 X, float2 Y, f
   } else if constexpr (VARIANT == kStau) {
     const float2 sc = __fmul2_rn(s, make_float2(scale, scale));
     const float e0 = ex2_approx(-fabsf(s.x) * c2), e1 = ex2_approx(-fabsf(s.y) * c2);
-    // log1p as the forward computes it, so the weights match its normaliser
-    const float2 l = tc::log1p_unit2(make_float2(e0, e1));
-    const float2 phi = make_float2(fmaxf(sc.x, 0.f) + l.x + hp.eps, fmaxf(sc.y, 0.f) + l.y + hp.eps);
+    // phi as the forward computes it, so the weights match its normaliser
+    const float2 phi = tc::phi2(sc, make_float2(e0, e1), hp.eps);
     const float2 lp = make_float2(lg2_approx(phi.x), lg2_approx(phi.y));
     const float2 x = __ffma2_rn(make_float2(hp.tau, hp.tau), lp, Y);
     w = make_float2(ex2_approx(x.x), ex2_approx(x.y));

@@ -10,7 +10,7 @@
 //   s^tau    2^(tau log2(softplus(scale q.k) + eps) - m)  ("s^tau: a focal-length
 //            knob for attention": phi^tau with phi = softplus(s) + eps, taken in
 //            the log domain so that phi^tau cannot overflow; softplus's log1p
-//            by a polynomial, log1p_unit)
+//            by a polynomial, phi2)
 #pragma once
 
 #include <stdint.h>
@@ -125,32 +125,37 @@ __device__ __forceinline__ void softmax_chunk(const uint32_t (&sr)[32], int c, f
 // to powers of x): relative error below 1e-5 over the whole interval, tiny e
 // included, on the FMA pipe.  Every tensor-core path that forms phi(s) (the
 // s^tau forward map, its running max, the row statistics, tau* and the
-// backward) uses it, so that a backward's weights match the forward's
-// normaliser.  The coefficients are numpy's
+// backward) does it through phi1 / phi2 below, so that a backward's weights
+// match the forward's normaliser.  The coefficients are numpy's
 // Chebyshev.interpolate(lambda x: log1p(x) / x, 5, domain=[0, 1]) converted
 // to the power basis and rounded to fp32.
 constexpr float kL1p0 = 0.999990582f, kL1p1 = -0.499314666f, kL1p2 = 0.324849576f,
                 kL1p3 = -0.209079534f, kL1p4 = 0.10013973f, kL1p5 = -0.023443656f;
-__device__ __forceinline__ float log1p_unit(float e) {
+// phi = softplus(s) + eps = max(s, 0) + log1p(e) + eps, e = 2^(-|s| log2 e),
+// with max(s, 0) formed as (s + |s|) / 2 (exact in fp32) and eps folded into
+// the polynomial's last multiply: three operations after P(e).
+__device__ __forceinline__ float phi1(float s, float e, float eps) {
   float p = fmaf(kL1p5, e, kL1p4);
   p = fmaf(p, e, kL1p3);
   p = fmaf(p, e, kL1p2);
   p = fmaf(p, e, kL1p1);
   p = fmaf(p, e, kL1p0);
-  return e * p;
+  return fmaf(0.5f, s + fabsf(s), fmaf(e, p, eps));
 }
-__device__ __forceinline__ float2 log1p_unit2(float2 e) {
+__device__ __forceinline__ float2 phi2(float2 s, float2 e, float eps) {
   float2 p = __ffma2_rn(make_float2(kL1p5, kL1p5), e, make_float2(kL1p4, kL1p4));
   p = __ffma2_rn(p, e, make_float2(kL1p3, kL1p3));
   p = __ffma2_rn(p, e, make_float2(kL1p2, kL1p2));
   p = __ffma2_rn(p, e, make_float2(kL1p1, kL1p1));
   p = __ffma2_rn(p, e, make_float2(kL1p0, kL1p0));
-  return __fmul2_rn(e, p);
+  const float2 l = __ffma2_rn(e, p, make_float2(eps, eps));
+  const float2 u = __fadd2_rn(s, make_float2(fabsf(s.x), fabsf(s.y)));
+  return __ffma2_rn(make_float2(0.5f, 0.5f), u, l);
 }
 
-// log2(softplus(s) + eps), softplus(s) = max(s, 0) + log1p(2^(-|s| log2 e)).
+// log2(softplus(s) + eps).
 __device__ __forceinline__ float log2_phi(float s, float abs_s_log2e, float eps) {
-  return lg2_approx(fmaxf(s, 0.f) + log1p_unit(ex2_approx(-abs_s_log2e)) + eps);
+  return lg2_approx(phi1(s, ex2_approx(-abs_s_log2e), eps));
 }
 
 // log2 phi(s) of two scores with the non-SFU arithmetic in f32x2 pairs (the
@@ -158,9 +163,7 @@ __device__ __forceinline__ float log2_phi(float s, float abs_s_log2e, float eps)
 __device__ __forceinline__ float2 log2_phi2(float2 d, float scale, float c2, float eps) {
   const float2 s = __fmul2_rn(d, make_float2(scale, scale));
   const float2 a = __fmul2_rn(make_float2(fabsf(d.x), fabsf(d.y)), make_float2(c2, c2));
-  const float2 l1p = log1p_unit2(make_float2(ex2_approx(-a.x), ex2_approx(-a.y)));
-  const float2 phi = __fadd2_rn(make_float2(fmaxf(s.x, 0.f), fmaxf(s.y, 0.f)),
-                                __fadd2_rn(l1p, make_float2(eps, eps)));
+  const float2 phi = phi2(s, make_float2(ex2_approx(-a.x), ex2_approx(-a.y)), eps);
   return make_float2(lg2_approx(phi.x), lg2_approx(phi.y));
 }
 
