@@ -196,23 +196,33 @@ template <bool PARTIAL>
 __device__ __forceinline__ void tau_chunk(const uint32_t (&sr)[32], int c, float scale, float c2,
                                           float eps, float g0, int limit, float (&st)[5]) {
   constexpr float LN2 = 0.6931471805599453f;
+  // two keys at a time in f32x2 pairs; the sums of each half kept apart
+  float2 sum_s = make_float2(0.f, 0.f), sum_g = sum_s, sum_sg = sum_s, sum_gg = sum_s;
+  float n = 0.f;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float d = __uint_as_float(sr[i]);
-    float s = d * scale;
-    float g = fmaf(log2_phi(s, fabsf(d) * c2, eps), LN2, -g0);
-    float w = 1.f;
-    if (PARTIAL && c * 32 + i >= limit) {
-      s = 0.f;
-      g = 0.f;
-      w = 0.f;
+  for (int i = 0; i < 32; i += 2) {
+    const float2 d = f2(sr[i], sr[i + 1]);
+    float2 s = __fmul2_rn(d, make_float2(scale, scale));
+    const float2 a = __fmul2_rn(make_float2(fabsf(d.x), fabsf(d.y)), make_float2(c2, c2));
+    const float2 phi = phi2(s, make_float2(ex2_approx(-a.x), ex2_approx(-a.y)), eps);
+    float2 g = __ffma2_rn(make_float2(lg2_approx(phi.x), lg2_approx(phi.y)), make_float2(LN2, LN2),
+                          make_float2(-g0, -g0));
+    if (PARTIAL) {
+      const bool ok0 = c * 32 + i < limit, ok1 = c * 32 + i + 1 < limit;
+      s = make_float2(ok0 ? s.x : 0.f, ok1 ? s.y : 0.f);
+      g = make_float2(ok0 ? g.x : 0.f, ok1 ? g.y : 0.f);
+      n += (ok0 ? 1.f : 0.f) + (ok1 ? 1.f : 0.f);
     }
-    st[0] += w;
-    st[1] += s;
-    st[2] += g;
-    st[3] = fmaf(s, g, st[3]);
-    st[4] = fmaf(g, g, st[4]);
+    sum_s = __fadd2_rn(sum_s, s);
+    sum_g = __fadd2_rn(sum_g, g);
+    sum_sg = __ffma2_rn(s, g, sum_sg);
+    sum_gg = __ffma2_rn(g, g, sum_gg);
   }
+  st[0] += PARTIAL ? n : 32.f;
+  st[1] += sum_s.x + sum_s.y;
+  st[2] += sum_g.x + sum_g.y;
+  st[3] += sum_sg.x + sum_sg.y;
+  st[4] += sum_gg.x + sum_gg.y;
 }
 
 // Row statistics of the map over one thread's keys (normalised entropy: "The
