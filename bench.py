@@ -230,6 +230,32 @@ def cpu_oracle_sample(w, inputs, target_seconds, seed=0, cap_rows=None):
     return f / t / 1e12, t, rows_per_pair * 8, threads
 
 
+def sdpa_context(q, k, v, w, flops, steps):
+    """Time torch.nn.functional.scaled_dot_product_attention (softmax, the
+    backend torch picks) on the benchmark's inputs, for context beside the
+    library's softmax map.  Any failure is reported, not raised."""
+    import torch
+    import torch.nn.functional as F
+    try:
+        if w.hkv != w.h:
+            return {"unavailable": "grouped kv heads"}
+        f = lambda: F.scaled_dot_product_attention(q, k, v, is_causal=w.causal, scale=w.scale)
+        for _ in range(3):
+            f()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            f()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / steps
+        return {"kernel_ms": ms, "tflops": flops / (ms * 1e-3) / 1e12,
+                "what": "torch scaled_dot_product_attention, softmax, same inputs (context only)"}
+    except Exception as e:  # context only: the benchmark line does not depend on it
+        return {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+
+
 def reference_arm(args):
     """The fp64 oracle on the host cores, as the reference arm."""
     rank = int(os.environ.get("RANK", "0"))
@@ -453,6 +479,11 @@ def main():
         cpu = {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"{rows} random query rows from 8 (batch, head) pairs of {w.name}, "
                          f"Yat map, fp64 ({secs:.1f} s)"}
+
+    # ---- context only, last: torch's own scaled_dot_product_attention
+    # (softmax) on the same device inputs; not part of the step, never the
+    # headline, and run after every figure the line depends on
+    per_variant["sdpa_context"] = sdpa_context(q, k, v, w, flops, args.steps)
 
     achieved = fwd_tflops
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",

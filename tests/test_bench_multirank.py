@@ -56,3 +56,20 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
         batch, steps, warmup, gpus = None, 1, 1, 2
 
     assert bench.reference_arm(Args()) == 0
+
+
+def test_sdpa_context_never_raises():
+    """The torch SDPA context figure is optional: without a GPU (or for
+    grouped kv heads) it reports why instead of failing the benchmark line."""
+    import torch
+    from softmax_free_attention_gb300 import workloads
+    w = workloads.Workload("ctx", B=1, h=2, hkv=2, Tq=16, Tk=16, dk=32, dv=32, dtype="bf16",
+                           causal=True, qk_factor=1.0, yat_param="ln2", seed=0)
+    q = torch.zeros(1, 2, 16, 32, dtype=torch.bfloat16)
+    res = bench.sdpa_context(q, q, q, w, w.flops(), 2)
+    if not torch.cuda.is_available():
+        assert "unavailable" in res
+    wg = workloads.Workload("ctx_gqa", B=1, h=2, hkv=1, Tq=16, Tk=16, dk=32, dv=32, dtype="bf16",
+                            causal=True, qk_factor=1.0, yat_param="ln2", seed=0)
+    assert bench.sdpa_context(q, q[:, :1], q[:, :1], wg, wg.flops(), 2) == {
+        "unavailable": "grouped kv heads"}
