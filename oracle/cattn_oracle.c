@@ -30,7 +30,7 @@
  *     the core-formula paragraph: a_i = phi(s_i)^tau / sum_j phi(s_j)^tau,
  *     phi(s) = softplus(s) + eps, one tau per head.
  *
- * Readings where the pages leave a step open (each also listed in the design doc):
+ * Readings where the pages leave a step open:
  *   - Yat scores are the raw q.k (no 1/sqrt(d) scale); softmax and s^tau use
  *     s = scale * q.k with the caller's scale.
  *   - The squared distance |q-k|^2 is summed directly over the components
