@@ -73,7 +73,15 @@ enum { CATTN_F32 = 0, CATTN_BF16 = 1 };
 enum {
   /* Yat only: the workspace already holds the squared row norms of this k,
    * written by cattn_key_norms for the same problem; skip them. */
-  CATTN_FLAG_NORMS_READY = 1
+  CATTN_FLAG_NORMS_READY = 1,
+  /* Testing only: the tensor-core forward (bf16 inputs) starts with a wait on
+   * a barrier that nothing completes.  The bounded wait gives up after 20 ms,
+   * every role of the kernel leaves its loop (copies already started are
+   * waited for, tensor memory is released), the outputs are left undefined,
+   * and the next cattn_check_status returns CATTN_ERR_TIMEOUT.  It exercises
+   * the kernel's timeout path without a fault; other entry points and the
+   * CUDA-core path ignore it. */
+  CATTN_FLAG_TEST_STALL = 2
 };
 
 /* Status codes. */

@@ -26,11 +26,14 @@ int tk_pad(const cattn_problem_t *p) { return (p->Tk + kTile - 1) / kTile * kTil
 bool is_empty(const cattn_problem_t *p) { return p->B == 0 || p->h == 0 || p->Tq == 0; }
 
 // Workspace layout of the bf16 (tensor-core) path, each part 256-byte aligned:
-//   ctrl       256 B: the persistent schedule's unit ticket (zeroed by each
-//              forward), then (Yat) the largest key norm as fp32 bits
+//   ctrl       256 B: the persistent schedule's unit ticket and (Yat) the
+//              count of rows listed for the near-key pass (both zeroed by
+//              each forward), then (Yat) the largest key norm as fp32 bits
 //              (zeroed and written by the key-norm prologue)
 //   nk         Yat only: squared k row norms [B*hkv, Tk_pad], fp32 (the
 //              query norms are taken in-kernel from the Q tiles)
+//   near       Yat only: the rows listed for the near-key pass, (batch*head,
+//              row) uint32 pairs, room for every row once per key split
 //   part_o     key splits only: unnormalised partial outputs
 //              [n_splits, B*h, Tq, dv] fp32
 //   part_stat  key splits only: per-row [n_splits, B*h, Tq, 4] fp32
@@ -40,9 +43,13 @@ size_t ws_nk_bytes(const cattn_problem_t *p) {
 }
 
 struct WsLayout {
-  size_t ctrl, nk, part_o, part_stat, total;
+  size_t ctrl, nk, near, part_o, part_stat, total;
+  size_t near_cap;
   TcSchedule sched;
 };
+
+// the control block's words
+constexpr int kCtrlTicket = 0, kCtrlNearCount = 1, kCtrlNkMax = 2;
 
 WsLayout ws_layout(int variant, const cattn_problem_t *p) {
   WsLayout w;
@@ -55,6 +62,9 @@ WsLayout ws_layout(int variant, const cattn_problem_t *p) {
   if (variant == CATTN_YAT) {
     w.nk = off;
     off += ws_nk_bytes(p);
+    w.near = off;
+    w.near_cap = (size_t)w.sched.n_splits * p->B * p->h * p->Tq;
+    off += align256(w.near_cap * 8);
   }
   if (w.sched.n_splits > 1) {
     const size_t rows = (size_t)w.sched.n_splits * p->B * p->h * p->Tq;
@@ -78,7 +88,7 @@ int check_problem(int variant, const cattn_problem_t *p) {
   if (p->h % p->hkv != 0) return CATTN_ERR_SHAPE;
   if (p->causal && p->Tq != p->Tk) return CATTN_ERR_SHAPE;
   if (variant != CATTN_YAT && !(p->scale > 0.f && p->scale < 3.0e38f)) return CATTN_ERR_INVALID_ARG;
-  if (p->flags & ~CATTN_FLAG_NORMS_READY) return CATTN_ERR_INVALID_ARG;
+  if (p->flags & ~(CATTN_FLAG_NORMS_READY | CATTN_FLAG_TEST_STALL)) return CATTN_ERR_INVALID_ARG;
   if (p->yat_m < 0 || p->yat_m > 3) return CATTN_ERR_INVALID_ARG;
   // every (dk, dv) in {32, 64, 128}^2: the tensor-core kernel for bf16 with
   // (64, 64), (128, 128), (128, 64), the CUDA-core kernel otherwise
@@ -202,7 +212,8 @@ int cattn_key_norms(const cattn_problem_t *p, const void *k, void *workspace,
   if (rc != CATTN_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float *nk = reinterpret_cast<float *>(static_cast<char *>(workspace) + w.nk);
-  unsigned int *nk_max = reinterpret_cast<unsigned int *>(static_cast<char *>(workspace) + w.ctrl) + 1;
+  unsigned int *nk_max =
+      reinterpret_cast<unsigned int *>(static_cast<char *>(workspace) + w.ctrl) + kCtrlNkMax;
   if ((rc = map_cuda(cudaMemsetAsync(nk_max, 0, sizeof(unsigned int), s))) != CATTN_OK) return rc;
   return map_cuda(
       launch_row_sqnorm_bf16(k, nk, p->B * p->hkv, p->Tk, tk_pad(p), p->dk, nk_max, s));
@@ -243,6 +254,7 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
   fp.n_qtiles = (p->Tq + kTcQueryTile - 1) / kTcQueryTile;
   fp.n_pairs = (fp.n_qtiles + 1) / 2;  // two query tiles per work unit
   fp.n_kv_tiles = (p->Tk + kTcKeyTile - 1) / kTcKeyTile;
+  fp.test_stall = (p->flags & CATTN_FLAG_TEST_STALL) ? 1 : 0;
 
   if (!on_tensor_cores(p))
     return map_cuda(launch_fwd_simt(variant, p->dtype == CATTN_BF16, p->dk, p->dv, fp, s));
@@ -253,14 +265,17 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
   fp.kv_per_split = w.sched.kv_per_split;
   fp.head_group = w.sched.head_group;
   fp.n_units = (int)w.sched.n_units;
-  fp.tile_counter = reinterpret_cast<unsigned int *>(ws + w.ctrl);
+  fp.tile_counter = reinterpret_cast<unsigned int *>(ws + w.ctrl) + kCtrlTicket;
   if (w.sched.n_splits > 1) {
     fp.part_o = reinterpret_cast<float *>(ws + w.part_o);
     fp.part_stat = reinterpret_cast<float *>(ws + w.part_stat);
   }
   if (variant == CATTN_YAT) {
     fp.nk = reinterpret_cast<const float *>(ws + w.nk);
-    fp.nk_max = reinterpret_cast<const unsigned int *>(ws + w.ctrl) + 1;
+    fp.nk_max = reinterpret_cast<const unsigned int *>(ws + w.ctrl) + kCtrlNkMax;
+    fp.near_count = reinterpret_cast<unsigned int *>(ws + w.ctrl) + kCtrlNearCount;
+    fp.near_rows = reinterpret_cast<uint2 *>(ws + w.near);
+    fp.near_cap = (unsigned int)(w.near_cap < 0xffffffffu ? w.near_cap : 0xffffffffu);
     if (!(p->flags & CATTN_FLAG_NORMS_READY)) {
       rc = cattn_key_norms(p, k, workspace, workspace_bytes, stream);
       if (rc != CATTN_OK) return rc;
@@ -270,7 +285,8 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
   if ((rc = encode_bf16_3d(&tq, q, p->dk, p->Tq, p->B * p->h, kTcQueryTile)) != CATTN_OK) return rc;
   if ((rc = encode_bf16_3d(&tk, k, p->dk, p->Tk, p->B * p->hkv, kTcKeyTile)) != CATTN_OK) return rc;
   if ((rc = encode_bf16_3d(&tv, v, p->dv, p->Tk, p->B * p->hkv, kTcKeyTile)) != CATTN_OK) return rc;
-  if ((rc = map_cuda(cudaMemsetAsync(fp.tile_counter, 0, sizeof(unsigned int), s))) != CATTN_OK)
+  // the ticket and the near-key count start at zero
+  if ((rc = map_cuda(cudaMemsetAsync(ws + w.ctrl, 0, 2 * sizeof(unsigned int), s))) != CATTN_OK)
     return rc;
   return map_cuda(launch_fwd_tc(variant, p->dk, p->dv, fp, tq, tk, tv, s));
 }

@@ -96,6 +96,8 @@ constexpr int PRODUCER_WARP = 16;
 constexpr int MMA_WARP = 17;
 constexpr int NKS = 4;  // stages of the key-norm ring
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+// the limit of the test-only wait that nothing completes (FwdParams::test_stall)
+constexpr uint64_t STALL_LIMIT_NS = 20000000ull;
 constexpr unsigned FULL = 0xffffffffu;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
@@ -131,8 +133,8 @@ struct Layout {
   static constexpr int OFF_BAR = OFF_XCHG + XCHG_FLOATS * 4;
   // q_full, q_empty, kv_full[NS], kv_empty[NS], nk_full[NKS], nk_empty[NKS],
   // s_full[2], p_full[2], o_full[2], o_empty[2], unit_full[2], unit_empty[2], drain,
-  // p_half[2]
-  static constexpr int NBAR = 2 + 2 * NS + 2 * NKS + 15;
+  // p_half[2], never (nothing arrives on it: the test-only stall)
+  static constexpr int NBAR = 2 + 2 * NS + 2 * NKS + 16;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // TMEM base address, abort flag, unit ring[2]
   static constexpr int BYTES = OFF_MISC + 16;
@@ -144,12 +146,13 @@ struct Layout {
 // Warp-collective bounded wait.  Every lane polls (so every lane acquires the
 // phase), the exit decision is warp-uniform.  Returns false on timeout/abort.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          unsigned site, bool honor_abort = true) {
+                                          unsigned site, bool honor_abort = true,
+                                          uint64_t limit_ns = WAIT_LIMIT_NS) {
   if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
-    const int bad = (honor_abort && *abort != 0) || (globaltimer_ns() - t0 > WAIT_LIMIT_NS);
+    const int bad = (honor_abort && *abort != 0) || (globaltimer_ns() - t0 > limit_ns);
     if (__any_sync(FULL, bad)) {
       if ((threadIdx.x & 31) == 0) {
         atomicCAS(&g_status, 0u, site | 1u);
@@ -163,12 +166,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // Single-thread bounded wait (the MMA issuer runs on one lane).  Returns
 // false on timeout or abort.
 __device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                            unsigned site, bool honor_abort = true) {
+                                            unsigned site, bool honor_abort = true,
+                                            uint64_t limit_ns = WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((honor_abort && *abort != 0) || (globaltimer_ns() - t0 > WAIT_LIMIT_NS)) {
+    if ((honor_abort && *abort != 0) || (globaltimer_ns() - t0 > limit_ns)) {
       atomicCAS(&g_status, 0u, site | 1u);
       *abort = 1;
       return false;
@@ -364,6 +368,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto unit_empty = [&](uint32_t s) { return bar0 + 8u * (B2 + 10 + s); };
   const uint32_t bar_drain = bar0 + 8u * (B2 + 12);
   auto p_half = [&](int x) { return bar0 + 8u * (B2 + 13 + x); };
+  const uint32_t bar_never = bar0 + 8u * (B2 + 15);
   auto q_smem = [&](int x) { return sb + L::OFF_Q + (uint32_t)x * L::Q_TILE; };
   auto slot_smem = [&](uint32_t s) { return sb + L::OFF_RING + s * L::SLOT; };
   const float *nk_ring = reinterpret_cast<const float *>(smem + L::OFF_NK);
@@ -394,6 +399,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(unit_empty(x), 1 + MAP_WARPS);  // the MMA lane and every map warp
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_never, 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -433,6 +439,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       int u = blockIdx.x;
       uint32_t kv_pos = 0, nk_pos = 0;
+      // copies started: Q pairs, K/V ring positions, key-norm ring positions
+      uint32_t q_armed = 0, kv_issued = 0, nk_issued = 0;
       for (uint32_t uc = 0;; ++uc) {
         const uint32_t us = uc & 1u;
         if (!thread_wait(unit_empty(us), ((uc >> 1) & 1u) ^ 1u, abort, SITE_PRODUCER | 0x40)) break;
@@ -449,6 +457,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (t.n[1] > 0)
             tma_load_3d(q_smem(1) + c * BM * 128, &tm_q, c * 64, t.q0 + BM, t.bh, bar_q_full);
         }
+        ++q_armed;
         bool ok = true;
         for (int j = 0; j < t.nkv; ++j) {
           const int jt = t.kv_begin + j;  // key tile
@@ -461,6 +470,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int c = 0; c < DK / 64; ++c)
               tma_load_3d(slot_smem(s) + c * BN * 128, &tm_k, c * 64, jt * BN, t.bh_kv, kv_full(s));
+            kv_issued = pos + 1;
           }
           if (VARIANT == kYat) {  // squared key norms of the tile
             const uint32_t pos = nk_pos + j, s = pos % NKS;
@@ -470,6 +480,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_arrive_expect_tx(nk_full(s), BN * 4);
             bulk_load(sb + L::OFF_NK + s * BN * 4,
                       p.nk + (size_t)t.bh_kv * p.Tk_pad + (size_t)jt * BN, BN * 4, nk_full(s));
+            nk_issued = pos + 1;
           }
           if (HAS_V) {  // V
             const uint32_t pos = kv_pos + 2u * j + 1u, s = pos % L::NS;
@@ -480,12 +491,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int c = 0; c < DV / 64; ++c)
               tma_load_3d(slot_smem(s) + c * BN * 128, &tm_v, c * 64, jt * BN, t.bh_kv, kv_full(s));
+            kv_issued = pos + 1;
           }
         }
         if (!ok) break;
         kv_pos += STEP * t.nkv;
         nk_pos += t.nkv;
         u = (int)atomicAdd(p.tile_counter, 1u) + (int)gridDim.x;
+      }
+      {
+        // every copy this lane started lands in shared memory before the CTA
+        // can exit: long since consumed when the schedule ran to its end,
+        // possibly still in flight after an abort (each the latest use of its
+        // barrier; bounded waits that ignore the abort flag)
+        if (q_armed > 0)
+          thread_wait(bar_q_full, (q_armed - 1u) & 1u, abort, SITE_PRODUCER | 0x60, false);
+        for (uint32_t pos = kv_issued > (uint32_t)L::NS ? kv_issued - L::NS : 0u; pos < kv_issued; ++pos)
+          thread_wait(kv_full(pos % L::NS), (pos / L::NS) & 1u, abort, SITE_PRODUCER | 0x60, false);
+        for (uint32_t pos = nk_issued > (uint32_t)NKS ? nk_issued - NKS : 0u; pos < nk_issued; ++pos)
+          thread_wait(nk_full(pos % NKS), (pos / NKS) & 1u, abort, SITE_PRODUCER | 0x60, false);
       }
     }
   } else if (warp == MMA_WARP) {
@@ -523,6 +547,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int ms = 0;  // running MMA iteration
 #endif
       for (uint32_t uc = 0; ok; ++uc) {
+        if (uc == 0 && p.test_stall) {
+          // test-only: a wait on a barrier that nothing arrives on runs out
+          // after a short limit, and every role takes the abort path
+          ok = CONV ? warp_wait(bar_never, 0u, abort, SITE_MMA | 0x80, true, STALL_LIMIT_NS)
+                    : thread_wait(bar_never, 0u, abort, SITE_MMA | 0x80, true, STALL_LIMIT_NS);
+          if (!ok) break;
+        }
         if (!mwait(unit_full(uc & 1u), (uc >> 1) & 1u, SITE_MMA | 0x70)) break;
         const int u = unit_ring[uc & 1u];
         if (u < 0) break;
@@ -637,12 +668,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float m_used = -INFINITY;               // softmax / s^tau: running max, log2 units
       float yb = 0.f, yeps = 0.f, qe = 0.f, tau = 1.f, seps = 0.f;
       bool fast = false;  // Yat: the fast map path is exact up to rounding for this unit
+      // Yat row statistics: this row's guard against a cancelled distance and
+      // where its query row and the unit's first key sit in memory
+      float st_thr = INFINITY;
+      const uint4 *st_q4 = nullptr, *st_k4 = nullptr;
       {
         const Unit t = decode_unit(p, u);
         nk_tiles = x ? t.n[1] : t.n[0];
         nkv = t.nkv;
         const int row = t.q0 + x * BM + r;
         lim_base = (p.causal ? min(row + 1, p.Tk) : p.Tk) - t.kv_begin * BN;
+        if (VARIANT == kYat && STATS) {
+          if (row < p.Tq)
+            st_q4 = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.q) +
+                                                    ((size_t)t.bh * p.Tq + row) * DK);
+          st_k4 = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(p.k) +
+                                                  ((size_t)t.bh_kv * p.Tk + (size_t)t.kv_begin * BN) * DK);
+        }
         // tau* counts scores of real rows only (the forward just drops the
         // outputs of rows past Tq)
         if (VARIANT == kTau && row >= p.Tq) lim_base = 0;
@@ -708,6 +750,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // the bounds under which the map's fast path is exact up to rounding
           const float span = qe + __uint_as_float(*p.nk_max);
           fast = yeps >= 0x1p-60f && __all_sync(FULL, span <= 0x1p61f && span * 0x1p-16f <= yeps);
+          if (STATS && st_q4) st_thr = yat_near_threshold(s2.x + s2.y, yb, YM);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_q_empty);
@@ -783,10 +826,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                                      : make_float2(n4.x, n4.y),
                                                              make_float2(yb, yb), make_float2(qe, qe),
                                                              yeps);
-                w0 = kk.x * nz_scale;
-                w1 = kk.y * nz_scale;
-                l0 = lg2_approx(kk.x) * LN2 - nz_log;
-                l1 = lg2_approx(kk.y) * LN2 - nz_log;
+                float k0 = kk.x, k1 = kk.y;
+                // the guard against a cancelled distance, key by key (allowed
+                // keys only: the others may lie past the end of k)
+                const uint4 *kt4 = st_k4 + (size_t)j * BN * (DK / 8);
+                if (col < limit && k0 > st_thr)
+                  k0 = yat_direct_call<DK, YM>(st_q4, kt4 + (size_t)col * (DK / 8), yb, yeps);
+                if (col + 1 < limit && k1 > st_thr)
+                  k1 = yat_direct_call<DK, YM>(st_q4, kt4 + (size_t)(col + 1) * (DK / 8), yb, yeps);
+                w0 = k0 * nz_scale;
+                w1 = k1 * nz_scale;
+                l0 = lg2_approx(k0) * LN2 - nz_log;
+                l1 = lg2_approx(k1) * LN2 - nz_log;
               } else {
                 const float d0 = __uint_as_float(sr1[i]), d1 = __uint_as_float(sr1[i + 1]);
                 float x0, x1;  // log2 of the weights
@@ -1047,6 +1098,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if (row_ok && half == 0) {
             const size_t ti = (size_t)t.bh * p.Tq + row;
+            if (VARIANT == kYat && all_top > yat_near_threshold(qe - yeps, yb, YM)) {
+              // a key may sit close enough to q for the assembled distance to
+              // have cancelled: the near-key pass recomputes this row
+              const unsigned slot = atomicAdd(p.near_count, 1u);
+              if (slot < p.near_cap) p.near_rows[slot] = make_uint2((unsigned)t.bh, (unsigned)row);
+            }
             if (p.row_mass)
               p.row_mass[ti] = VARIANT == kYat ? total : (m_used + log2f(total)) * LN2;
             if (p.row_max) p.row_max[ti] = VARIANT == kYat ? all_top : all_top * p.scale;
@@ -1067,8 +1124,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        o[8 * i + 4], o[8 * i + 5], o[8 * i + 6], o[8 * i + 7]);
             }
           }
-          if (row_ok && half == 0)
+          if (row_ok && half == 0) {
             reinterpret_cast<float4 *>(p.part_stat)[ti] = make_float4(total, m_used, all_top, 0.f);
+            if (VARIANT == kYat && all_top > yat_near_threshold(qe - yeps, yb, YM)) {
+              const unsigned slot = atomicAdd(p.near_count, 1u);
+              if (slot < p.near_cap) p.near_rows[slot] = make_uint2((unsigned)t.bh, (unsigned)row);
+            }
+          }
         }
         // O_x has been read: the next unit's first PV_x may overwrite it
         tc_fence_before();
@@ -1131,6 +1193,102 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Fw
   }
 }
 
+// The near-key pass of the Yat forward.  A row whose computed max kappa
+// passed yat_near_threshold may hold a key so close to its query that the
+// assembled distance |q|^2 + |k|^2 - 2 q.k cancelled; the fused kernel listed
+// it (near_rows), and here one CTA per listed row recomputes the whole row by
+// the plain definition: kappa_j = (q.k_j + b)^{2M} / (max(|q - k_j|^2, 0) +
+// eps) with the dot product and the distance summed over the components in
+// fp32 (eight warps take every eighth key; a warp's lanes split the
+// components, then each lane accumulates its dv/32 columns of kappa v), and
+// writes out = sum kappa v / (sum kappa + 1e-9), the row mass and max kappa
+// over what the fused kernel (and, with key splits, the combine) stored.  A
+// row listed twice (once per key split) is recomputed twice, with the same
+// result.  With no row listed every CTA returns at once.
+template <int DK, int DV, int YM>
+__global__ void __launch_bounds__(256) near_fix_kernel(const __grid_constant__ FwdParams p) {
+  constexpr int QE = DK / 32;  // q and k components per lane
+  constexpr int VE = DV / 32;  // v columns per lane
+  __shared__ float s_mass[8], s_top[8];
+  __shared__ float s_o[8][DV];
+  const unsigned n = min(*p.near_count, p.near_cap);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q);
+  const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(p.k);
+  const __nv_bfloat16 *vg = static_cast<const __nv_bfloat16 *>(p.v);
+  for (unsigned e = blockIdx.x; e < n; e += gridDim.x) {
+    const uint2 id = p.near_rows[e];
+    const int bh = (int)id.x, row = (int)id.y;
+    const int head = bh % p.h, batch = bh / p.h;
+    const size_t bh_kv = (size_t)batch * p.hkv + head / (p.h / p.hkv);
+    const float b = p.b[head], eps = p.eps[head];
+    float qf[QE];
+#pragma unroll
+    for (int i = 0; i < QE; ++i)
+      qf[i] = __bfloat162float(qg[((size_t)bh * p.Tq + row) * DK + lane * QE + i]);
+    const int lim = p.causal ? min(row + 1, p.Tk) : p.Tk;
+    float mass = 0.f, top = 0.f, o[VE];
+#pragma unroll
+    for (int c = 0; c < VE; ++c) o[c] = 0.f;
+    for (int j = warp; j < lim; j += 8) {
+      const __nv_bfloat16 *kr = kg + (bh_kv * p.Tk + j) * DK + lane * QE;
+      float dot = 0.f, d2 = 0.f;
+#pragma unroll
+      for (int i = 0; i < QE; ++i) {
+        const float kf = __bfloat162float(kr[i]);
+        dot = fmaf(qf[i], kf, dot);
+        const float df = qf[i] - kf;
+        d2 = fmaf(df, df, d2);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        dot += __shfl_xor_sync(FULL, dot, off);
+        d2 += __shfl_xor_sync(FULL, d2, off);
+      }
+      const float tt = dot + b;
+      float num = tt * tt;
+      if constexpr (YM == 2) num = num * num;
+      if constexpr (YM == 3) num = num * num * num;
+      const float kap = num / (fmaxf(d2, 0.f) + eps);
+      mass += kap;
+      top = fmaxf(top, kap);
+      const __nv_bfloat16 *vr = vg + (bh_kv * p.Tk + j) * DV + lane * VE;
+#pragma unroll
+      for (int c = 0; c < VE; ++c) o[c] = fmaf(kap, __bfloat162float(vr[c]), o[c]);
+    }
+    if (lane == 0) {
+      s_mass[warp] = mass;
+      s_top[warp] = top;
+    }
+#pragma unroll
+    for (int c = 0; c < VE; ++c) s_o[warp][lane * VE + c] = o[c];
+    __syncthreads();
+    if (warp == 0) {
+      float m_all = 0.f, t_all = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        m_all += s_mass[w];
+        t_all = fmaxf(t_all, s_top[w]);
+      }
+      const float inv = 1.f / (m_all + 1e-9f);
+      const size_t ti = (size_t)bh * p.Tq + row;
+      __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.out) + ti * DV + lane * VE;
+#pragma unroll
+      for (int c = 0; c < VE; ++c) {
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) acc += s_o[w][lane * VE + c];
+        orow[c] = __float2bfloat16_rn(acc * inv);
+      }
+      if (lane == 0) {
+        if (p.row_mass) p.row_mass[ti] = m_all;
+        if (p.row_max) p.row_max[ti] = t_all;
+      }
+    }
+    __syncthreads();
+  }
+}
+
 // tau* = (sum s g - sum s sum g / n) / (sum g^2 - (sum g)^2 / n), one thread
 // per head, in fp64 (the shift g0 cancels).
 __global__ void tau_finalize_kernel(const double *moments, const float *eps, int h, float *tau,
@@ -1171,10 +1329,17 @@ cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap 
   if constexpr (VARIANT == kTau || STATS) {
     return e;
   } else {
-    if (e != cudaSuccess || p.n_splits == 1) return e;
-    const long long rows = (long long)p.B * p.h * p.Tq;
-    combine_kernel<VARIANT, DV><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p);
-    return cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (p.n_splits > 1) {
+      const long long rows = (long long)p.B * p.h * p.Tq;
+      combine_kernel<VARIANT, DV><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if constexpr (VARIANT == kYat) {
+      near_fix_kernel<DK, DV, YM><<<sm_count, 256, 0, s>>>(p);
+      e = cudaGetLastError();
+    }
+    return e;
   }
 }
 

@@ -45,6 +45,16 @@ struct FwdParams {
   // outputs (any may be NULL)
   const float *norm_in;
   float *st_entropy, *st_small, *st_top10;
+  // Yat: rows whose max kappa passed the near-key guard, listed by the fused
+  // kernel for the near-key pass: (batch * h + head, row) pairs, their count
+  // (zeroed before launch) and the list's capacity
+  unsigned int *near_count;
+  uint2 *near_rows;
+  unsigned int near_cap;
+  // test only (CATTN_FLAG_TEST_STALL): the tensor-core forward's MMA warp
+  // first waits on a barrier that nothing completes, so that the bounded wait
+  // runs out and the kernel takes its abort path
+  int test_stall;
 };
 
 // Split count and grouping of the persistent tensor-core schedule; a pure

@@ -48,6 +48,58 @@ __device__ __forceinline__ float2 yat_pair(float2 d, float2 nk, float2 b2, float
   return __fmul2_rn(num, make_float2(rcp_approx(fmaxf(den.x, yeps)), rcp_approx(fmaxf(den.y, yeps))));
 }
 
+// kappa of one (query row, key) pair straight from the stored bf16 rows, the
+// dot product and |q - k|^2 each summed over the components in fp32 (no norm
+// expansion, so nothing cancels), for the few keys whose assembled distance
+// may have lost its digits (see yat_near_threshold).
+template <int DK, int M>
+__device__ __forceinline__ float yat_direct(const uint4 *q4, const uint4 *k4, float b, float eps) {
+  float2 dot = make_float2(0.f, 0.f), d2 = dot;
+#pragma unroll 2
+  for (int i = 0; i < DK / 8; ++i) {
+    const uint4 a = __ldg(q4 + i), c = __ldg(k4 + i);
+    const uint32_t qa[4] = {a.x, a.y, a.z, a.w}, ka[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float2 qf = make_float2(__uint_as_float(qa[w] << 16), __uint_as_float(qa[w] & 0xffff0000u));
+      const float2 kf = make_float2(__uint_as_float(ka[w] << 16), __uint_as_float(ka[w] & 0xffff0000u));
+      dot = __ffma2_rn(qf, kf, dot);
+      const float2 df = make_float2(qf.x - kf.x, qf.y - kf.y);
+      d2 = __ffma2_rn(df, df, d2);
+    }
+  }
+  const float t = (dot.x + dot.y) + b;
+  float num = t * t;
+  if constexpr (M == 2) num = num * num;
+  if constexpr (M == 3) num = num * num * num;
+  return num / (fmaxf(d2.x + d2.y, 0.f) + eps);
+}
+
+// yat_direct as a called function, for call sites that take it key by key
+// (the row statistics pass) and should not each carry a copy of the loop.
+template <int DK, int M>
+__device__ __noinline__ float yat_direct_call(const uint4 *q4, const uint4 *k4, float b, float eps) {
+  return yat_direct<DK, M>(q4, k4, b, eps);
+}
+
+// Guard of the assembled distance for one query row.  |q|^2 + |k|^2 - 2 q.k
+// is three fp32 sums of at most 128 terms, together off by at most
+// E = 2^-16 (|q|^2 + |k|^2) from the true squared distance; that is below
+// 2^-12 of den = d^2 + eps unless den < (|q|^2 + |k|^2) / 16.  Such a key has
+// 0.695 |q| < |k| < 1.44 |q| and q.k > (15/32)(|q|^2 + |k|^2), so its computed
+// kappa exceeds thr = (b + (15/32)|q|^2)^(2M) / (0.2 |q|^2) (b >= 0).  Keys of
+// random direction sit far below thr (kappa of order |q|^2 / (2 d)).  A row
+// whose computed max kappa passes thr is recomputed by the plain definition
+// (the forward's near-key pass, near_fix_kernel; the row statistics pass key
+// by key).  nq = 0 gives +inf (no key can be at risk).
+__device__ __forceinline__ float yat_near_threshold(float nq, float b, int M) {
+  const float a = fmaf(0.46875f, nq, b);
+  float num = a * a;
+  if (M == 2) num = num * num;
+  if (M == 3) num = num * num * num;
+  return a > 0.f ? num / (0.2f * nq) : 0.f;
+}
+
 // Masks, accumulates and packs one pair: masked keys (col >= limit) get
 // kappa = 0; mass (two chains) and top take kappa; returns P = bf16(kappa).
 template <bool PARTIAL>

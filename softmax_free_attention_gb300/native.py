@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(HERE, "libcattn.so")
 SOFTMAX, YAT, STAU = 0, 1, 2
 F32, BF16 = 0, 1
 FLAG_NORMS_READY = 1
+FLAG_TEST_STALL = 2  # testing only: the forward kernel waits on a barrier nothing completes
 
 OK = 0
 ERR_INVALID_ARG = 1

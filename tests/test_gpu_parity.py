@@ -308,6 +308,74 @@ def test_yat_fast_and_exact_map_paths(eps, qk, where):
     pu.full_parity("yat", inp, causal=True, scale=w.scale, where=where)
 
 
+# ---------------------------------------------------------------- Yat with q close to k
+
+# (name, d, q/k factor, eps): the char-level norms x16 at d = 64 and the
+# cross-attention norms x8 at d = 128; eps = 1 takes the map's fast path at
+# these norms, eps = 0.05 its clamped path
+NEAR_CASES = [
+    ("s16_d64_fast", 64, 16.0, 1.0),
+    ("s16_d64_exact", 64, 16.0, 0.05),
+    ("x8_d128_fast", 128, 8.0, 1.0),
+    ("x8_d128_exact", 128, 8.0, 0.05),
+]
+
+
+def _closed_form_self(q, b, eps):
+    """kappa(q, q) = (|q|^2 + b)^2 / eps per row ("The Kernel Between the
+    Roles", section "Two of our beliefs, measured"), in fp64 from the stored
+    bf16 values: [B, h, T]."""
+    qq = q.to(torch.float64)
+    n = (qq * qq).sum(-1)
+    return ((n + torch.as_tensor(b, dtype=torch.float64)[None, :, None]) ** 2
+            / torch.as_tensor(eps, dtype=torch.float64)[None, :, None]).numpy()
+
+
+@pytest.mark.parametrize("case", NEAR_CASES, ids=lambda c: c[0])
+def test_yat_keys_equal_to_queries(case):
+    """k = q (tied, causal): every row's own key sits at distance zero, where
+    |q|^2 + |k|^2 - 2 q.k cancels completely.  out, the row mass and max
+    kappa must match the oracle, and max kappa must equal the closed form
+    (|q|^2 + b)^2 / eps of the diagonal."""
+    name, d, s, eps = case
+    w = _wl("tied", 2, 2, 2, 300, 300, d, d, causal=True, qk=s, seed=31)
+    inp = workloads.generate(w)
+    inp["k"] = inp["q"].clone()
+    inp["yat_b"] = np.array([0.3, 2.0], dtype=np.float32)
+    inp["yat_eps"] = np.full(2, eps, dtype=np.float32)
+    pu.full_parity("yat", inp, causal=True, scale=w.scale, two_step=True, where=f"tied {name}")
+    _, _, mx = pu.run_gpu("yat", inp, causal=True, scale=w.scale)
+    ref = _closed_form_self(inp["q"], inp["yat_b"], inp["yat_eps"])
+    rel = np.abs(pu.to_np(mx) - ref) / ref
+    assert rel.max() <= pu.TEL_TOL, f"tied {name}: max kappa vs closed form {rel.max():.3e}"
+
+
+@pytest.mark.parametrize("case", NEAR_CASES, ids=lambda c: c[0])
+def test_yat_some_keys_copied_from_queries(case):
+    """Random keys with a few rows replaced by query rows (exact copies and
+    copies with one element nudged by one bf16 step), non-causal with a
+    ragged key tail, and causal: the near-coincident keys must not lose the
+    row mass or max kappa to the cancellation of the assembled distance."""
+    name, d, s, eps = case
+    for causal, Tk in ((False, 700), (True, 300)):
+        w = _wl("copied", 1, 2, 2, 300, Tk, d, d, causal=causal, qk=s, seed=57)
+        inp = workloads.generate(w)
+        k = inp["k"].clone()
+        q = inp["q"]
+        pairs = [(5, 3), (100, 140), (299, 299), (128, 130)] if causal else \
+                [(5, 3), (100, 400), (299, 699), (128, 130), (17, 255)]
+        for n_pair, (t, j) in enumerate(pairs):
+            k[0, :, j] = q[0, :, t]
+            if n_pair % 2:
+                # one element moved by a bf16 step or two: a tiny, nonzero distance
+                k[0, :, j, 7] = (k[0, :, j, 7].float() * (1.0 + 2.0 ** -7)).to(torch.bfloat16)
+        inp["k"] = k
+        inp["yat_b"] = np.array([0.3, 2.0], dtype=np.float32)
+        inp["yat_eps"] = np.full(2, eps, dtype=np.float32)
+        pu.full_parity("yat", inp, causal=causal, scale=w.scale, two_step=True,
+                       where=f"copied {name} causal={causal}")
+
+
 # ---------------------------------------------------------------- tau*
 
 TAU_SHAPES = [  # B, h, hkv, T_q, T_k, d, causal

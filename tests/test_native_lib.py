@@ -68,7 +68,7 @@ def validate(lib, variant, p, q=FAKE, k=FAKE, v=FAKE, b=FAKE, eps=FAKE, tau=FAKE
     (dict(dtype=7), native.ERR_INVALID_ARG),
     (dict(scale=0.0), native.ERR_INVALID_ARG),
     (dict(scale=-1.0), native.ERR_INVALID_ARG),
-    (dict(flags=2), native.ERR_INVALID_ARG),
+    (dict(flags=4), native.ERR_INVALID_ARG),            # no such flag
     (dict(dk=96, dv=96), native.ERR_UNSUPPORTED),
     (dict(dk=64, dv=256), native.ERR_UNSUPPORTED),
     (dict(dk=48, dv=32), native.ERR_UNSUPPORTED),       # widths are 32, 64 or 128
@@ -121,11 +121,13 @@ def test_pointer_rejections(lib):
 
 
 def test_workspace_layout(lib):
-    # 256-byte ticket, then (Yat) nk [B*hkv, ceil(Tk/128)*128] fp32, rounded
+    # 256-byte control block, then (Yat) nk [B*hkv, ceil(Tk/128)*128] fp32 and
+    # the near-key list (one 8-byte entry per row and key split), each rounded
     # to 256 B
     p = prob(B=2, h=4, hkv=2, Tq=300, Tk=300, dk=64, dv=64)
     nk = (2 * 2 * 384 * 4 + 255) // 256 * 256
-    assert lib.cattn_workspace_bytes(native.YAT, ctypes.byref(p)) == 256 + nk
+    near = (2 * 4 * 300 * 8 + 255) // 256 * 256
+    assert lib.cattn_workspace_bytes(native.YAT, ctypes.byref(p)) == 256 + nk + near
     assert lib.cattn_workspace_bytes(native.SOFTMAX, ctypes.byref(p)) == 256
     assert lib.cattn_workspace_bytes(native.STAU, ctypes.byref(p)) == 256
     p32 = prob(dtype=native.F32, dk=32, dv=32)
@@ -138,6 +140,15 @@ def test_workspace_layout(lib):
     # causal problems are never split
     pc = prob(B=1, h=2, hkv=2, Tq=2100, Tk=2100)
     assert lib.cattn_workspace_bytes(native.SOFTMAX, ctypes.byref(pc)) == 256
+
+
+def test_test_stall_flag_is_accepted(lib):
+    # the timeout-path test flag (alone or with the norms flag) passes the checks
+    for f in (native.FLAG_TEST_STALL, native.FLAG_TEST_STALL | native.FLAG_NORMS_READY):
+        p = prob(flags=f)
+        need = lib.cattn_workspace_bytes(native.YAT, ctypes.byref(p))
+        assert need > 0
+        assert validate(lib, native.YAT, p, ws=FAKE, ws_bytes=need) == native.OK
 
 
 def test_yat_power_range(lib):
