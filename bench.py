@@ -36,6 +36,11 @@ if ROOT not in sys.path:
 METRIC = "attention fwd TFLOP/s and % of GB300 bf16 tensor peak per variant, 1 GPU"
 WORKLOAD = "cfg3"
 FALLBACK_TFLOPS = 1900.0
+# NVIDIA's nominal dense bf16 figure for one GB300 (no sparsity): every
+# tensor-core fraction is also reported against it, beside the measured
+# cuBLAS peak that the roofline uses
+DATASHEET_TFLOPS = 2250.0
+FALLBACK_HBM_GBS = 6800.0
 
 
 def parse_args():
@@ -46,6 +51,8 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload table (every config, every map)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override B (small cases for profiler captures; not a bench line)")
     return ap.parse_args()
@@ -77,6 +84,51 @@ def measured_peaks():
         return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0.0)), "measured"
     except Exception:
         return FALLBACK_TFLOPS, 1700.0, "fallback"
+
+
+def measured_hbm_gbs():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def host_cpu():
+    """Model name and clock of the host cores (lscpu, else /proc/cpuinfo and
+    sysfs); missing fields are None."""
+    model, vendor, mhz = None, None, None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            key, _, val = ln.partition(":")
+            key, val = key.strip(), val.strip()
+            if key == "Model name" and not model:
+                model = val
+            elif key == "Vendor ID" and not vendor:
+                vendor = val
+            elif key == "CPU max MHz" and val:
+                mhz = float(val)
+    except Exception:
+        pass
+    if model and vendor and vendor not in model:
+        model = f"{vendor} {model}"
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for ln in f:
+                    if ln.lower().startswith("model name"):
+                        model = ln.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    if mhz is None:
+        try:
+            with open("/sys/devices/system/cpu/cpu0/cpufreq/cpuinfo_max_freq") as f:
+                mhz = int(f.read().strip()) / 1000.0
+        except Exception:
+            pass
+    return model, mhz
 
 
 KERNEL_SOURCES = ("fwd_tc.cu", "maps.cuh", "ptx.cuh", "kernels.h")
@@ -230,6 +282,101 @@ def cpu_oracle_sample(w, inputs, target_seconds, seed=0, cap_rows=None):
     return f / t / 1e12, t, rows_per_pair * 8, threads
 
 
+def oracle_full_runs(variants=("yat", "softmax")):
+    """The fp64 oracle over every row of the two small workloads (the fp32
+    char-level shapes and the bf16 char-level GPT shapes): wall time and
+    TFLOP/s by the metric's FLOP count."""
+    import oracle
+    from softmax_free_attention_gb300 import workloads
+    res = {}
+    for name in ("cfg1_f32", "cfg2_s1"):
+        w = workloads.WORKLOADS[name]
+        inp = workloads.generate(w)
+        for variant in variants:
+            kw = {"yat": dict(b=inp["yat_b"], eps=inp["yat_eps"]), "softmax": {},
+                  "stau": dict(eps=inp["stau_eps"], tau=inp["tau"])}[variant]
+            t0 = time.perf_counter()
+            oracle.forward(variant, inp["q"], inp["k"], inp["v"], causal=w.causal, scale=w.scale,
+                           nthreads=os.cpu_count() or 1, **kw)
+            dt = time.perf_counter() - t0
+            res[f"{name}/{variant}"] = {"s": dt, "tflops": w.flops() / dt / 1e12}
+    return res
+
+
+def per_config_table(dev, peak_burst, hbm_gbs, reps=20):
+    """Every workload and map through cattn_forward on device-resident inputs:
+    the whole call (Yat with its key-norm prologue) captured once in a CUDA
+    graph and replayed, CUDA events over `reps` replays, so that the time is
+    the device's and not the Python binding's.  The bound is the larger of
+    the tensor time (metric FLOP / measured bf16 peak) and the HBM time
+    (q, k, v read once, out and telemetry written once / measured copy
+    bandwidth); frac = bound / measured time.  fp32 runs on the CUDA cores,
+    where the tensor bound does not apply: reported against the HBM time."""
+    import torch
+
+    from softmax_free_attention_gb300 import attention, workloads
+    table = {}
+    for name, w in workloads.WORKLOADS.items():
+        inp = workloads.generate(w)
+        q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+        par = {"yat": dict(b=torch.as_tensor(inp["yat_b"], device=dev),
+                           eps=torch.as_tensor(inp["yat_eps"], device=dev)),
+               "softmax": {},
+               "stau": dict(eps=torch.as_tensor(inp["stau_eps"], device=dev),
+                            tau=torch.as_tensor(inp["tau"], device=dev))}
+        out = torch.empty((w.B, w.h, w.Tq, w.dv), dtype=q.dtype, device=dev)
+        mass = torch.empty((w.B, w.h, w.Tq), dtype=torch.float32, device=dev)
+        mx = torch.empty_like(mass)
+        esz = q.element_size()
+        hbm_bytes = ((q.numel() + k.numel() + v.numel() + out.numel()) * esz
+                     + 2 * mass.numel() * 4)
+        hbm_us = hbm_bytes / (hbm_gbs * 1e9) * 1e6
+        tensor_us = w.flops() / (peak_burst * 1e12) * 1e6 if w.dtype == "bf16" else 0.0
+        row = {}
+        for variant in ("yat", "softmax", "stau"):
+            prob = attention.make_problem(q, k, v, causal=w.causal, scale=w.scale)
+            need = attention.workspace_bytes(variant, prob)
+            ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+            f = lambda: attention.forward(variant, q, k, v, causal=w.causal, scale=w.scale,
+                                          out=out, row_mass=mass, row_max=mx, workspace=ws,
+                                          **par[variant])
+            try:
+                s = torch.cuda.Stream(dev)
+                s.wait_stream(torch.cuda.current_stream(dev))
+                with torch.cuda.stream(s):
+                    for _ in range(3):
+                        f()
+                torch.cuda.current_stream(dev).wait_stream(s)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    f()
+                for _ in range(3):
+                    g.replay()
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                for _ in range(reps):
+                    g.replay()
+                b.record()
+                torch.cuda.synchronize()
+                us = a.elapsed_time(b) * 1e3 / reps
+                bound_us = max(hbm_us, tensor_us)
+                row[variant] = {"us": us, "tflops": w.flops() / (us * 1e-6) / 1e12,
+                                "bound": "tensor" if tensor_us >= hbm_us else "hbm",
+                                "bound_us": bound_us, "frac": bound_us / us}
+                del g
+            except Exception as e:  # reported, never fatal for the line
+                row[variant] = {"unavailable": f"{type(e).__name__}: {e}"[:160]}
+        assert attention.check_status() == 0
+        table[name] = {"shape": f"B={w.B} h={w.h} hkv={w.hkv} Tq={w.Tq} Tk={w.Tk} dk={w.dk} "
+                                f"dv={w.dv} {w.dtype} {'causal' if w.causal else 'non-causal'}",
+                       "hbm_us": hbm_us, "tensor_us": tensor_us, **row}
+        del q, k, v, out, mass, mx, inp
+        torch.cuda.empty_cache()
+    return table
+
+
 def sdpa_context(q, k, v, w, flops, steps):
     """Time torch.nn.functional.scaled_dot_product_attention (softmax, the
     backend torch picks) on the benchmark's inputs, for context beside the
@@ -373,10 +520,14 @@ def main():
     # ---- per-variant forward timing on the same inputs
     per_variant = {}
     fwd_tflops = flops / (fwd_ms * 1e-3) / 1e12
-    per_variant["yat"] = {"tflops": flops / (ms_per_step * 1e-3) / 1e12,
+    step_tflops = flops / (ms_per_step * 1e-3) / 1e12
+    per_variant["yat"] = {"tflops": step_tflops,
                           "kernel_tflops": fwd_tflops, "kernel_ms": fwd_ms,
                           "norm_prologue_ms": norms_ms,
-                          "frac_of_peak": fwd_tflops / peak_burst}
+                          "frac_of_peak": fwd_tflops / peak_burst,
+                          "frac_of_datasheet_peak": fwd_tflops / DATASHEET_TFLOPS,
+                          "step_frac_of_peak": step_tflops / peak_burst,
+                          "step_frac_of_datasheet_peak": step_tflops / DATASHEET_TFLOPS}
     for variant in ("softmax", "stau"):
         for _ in range(3):
             variant_step(variant)
@@ -389,9 +540,12 @@ def main():
         torch.cuda.synchronize()
         ms = a.elapsed_time(b) / args.steps
         tf = flops / (ms * 1e-3) / 1e12
-        per_variant[variant] = {"tflops": tf, "kernel_ms": ms, "frac_of_peak": tf / peak_burst}
+        per_variant[variant] = {"tflops": tf, "kernel_ms": ms, "frac_of_peak": tf / peak_burst,
+                                "frac_of_datasheet_peak": tf / DATASHEET_TFLOPS}
     assert attention.check_status() == 0
     per_variant["yat_over_softmax"] = per_variant["yat"]["tflops"] / per_variant["softmax"]["tflops"]
+    per_variant["yat_kernel_over_softmax"] = (per_variant["yat"]["kernel_tflops"]
+                                              / per_variant["softmax"]["tflops"])
 
     # ---- tau* of the s^tau map from the same scores: one S = QK^T pass plus
     # per-score ln phi statistics (SFU-bound), not part of the step above
@@ -476,9 +630,18 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         val, secs, rows, threads = cpu_oracle_sample(w, inputs_host, 12.0)
+        model, mhz = host_cpu()
         cpu = {"value": val, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                "sample": f"{rows} random query rows from 8 (batch, head) pairs of {w.name}, "
-                         f"Yat map, fp64 ({secs:.1f} s)"}
+                         f"Yat map, fp64 ({secs:.1f} s)",
+               "cpu_model": model, "cpu_max_mhz": mhz if mhz else "not exposed by the host",
+               "full_runs": oracle_full_runs()}
+
+    # ---- every workload and map, device-resident, graph-replayed calls
+    hbm_gbs, hbm_kind = measured_hbm_gbs()
+    configs = None
+    if not args.no_configs and args.batch is None:
+        configs = per_config_table(dev, peak_burst, hbm_gbs)
 
     # ---- context only, last: torch's own scaled_dot_product_attention
     # (softmax) on the same device inputs; not part of the step, never the
@@ -489,13 +652,16 @@ def main():
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
                 "frac": achieved / peak_burst, "traffic": recorded_traffic(),
                 "peak_kind": f"{peak_kind} bf16 burst (cuBLAS)",
+                "frac_of_datasheet_peak": achieved / DATASHEET_TFLOPS,
+                "datasheet_peak": DATASHEET_TFLOPS,
                 "kernel": "cattn::tc::fwd_kernel<Yat,128,128>"}
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "config": config_block(w), "per_variant": per_variant,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "clocks": clocks.summary(), "gpu_launches": 2 * args.steps,
+            "per_config": configs, "hbm_peak_gbs": {"value": hbm_gbs, "kind": hbm_kind},
+            "clocks": clocks.summary(), "gpu_launches": 3 * args.steps,
             "peak_sustained_tflops": peak_sust}
     if rank == 0:
         print(json.dumps(line))

@@ -2,9 +2,11 @@
 memory on the call path (for example a plug-in whose host engine plans all
 device memory at start-up and forbids later allocations).
 
-The GPU test calls the entry point through the C ABI twice in a row, on two
-different problems, and checks each result against cattn_forward run with an
-ordinary caller-supplied workspace.  This file is collected last on purpose.
+The GPU test calls the entry point through the C ABI on several problems in a
+row (causal ones, then non-causal ones whose keys are split, so that their
+partial outputs share the array), and checks each result against
+cattn_forward run with an ordinary caller-supplied workspace.  This file is
+collected last on purpose.
 """
 import ctypes
 
@@ -45,9 +47,9 @@ def test_noalloc_rejects_oversized_problem_on_the_host(lib):
     assert rc == native.ERR_INVALID_ARG
 
 
-def _problem_inputs(name, B, h, hkv, T, d, seed):
-    w = workloads.Workload(name, B=B, h=h, hkv=hkv, Tq=T, Tk=T, dk=d, dv=d, dtype="bf16",
-                           causal=True, qk_factor=2.0, yat_param="softplus_uniform", seed=seed)
+def _problem_inputs(name, B, h, hkv, Tq, Tk, d, causal, seed):
+    w = workloads.Workload(name, B=B, h=h, hkv=hkv, Tq=Tq, Tk=Tk, dk=d, dv=d, dtype="bf16",
+                           causal=causal, qk_factor=2.0, yat_param="softplus_uniform", seed=seed)
     return w, workloads.generate(w, device="cuda")
 
 
@@ -56,16 +58,22 @@ def test_noalloc_matches_forward_on_two_calls_in_a_row(lib):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    # two different problems: the second call finds the first one's norms in
-    # the shared scratch and must not be affected by them
-    for (B, h, hkv, T, d, seed) in [(2, 4, 2, 640, 128, 11), (1, 2, 2, 300, 64, 12)]:
-        w, inp = _problem_inputs("noalloc", B, h, hkv, T, d, seed)
+    # different problems back to back: each call finds the previous one's
+    # norms (and, for the last, key-split partials) in the shared scratch and
+    # must not be affected by them; the last is non-causal with few query
+    # rows, so its keys are split in two and the partials of both splits sit
+    # in the shared array before the combine
+    for (B, h, hkv, Tq, Tk, d, causal, seed) in [(2, 4, 2, 640, 640, 128, True, 11),
+                                                 (1, 2, 2, 300, 300, 64, True, 12),
+                                                 (1, 2, 2, 128, 2048, 64, False, 13),
+                                                 (1, 2, 2, 128, 2048, 64, False, 14)]:
+        w, inp = _problem_inputs("noalloc", B, h, hkv, Tq, Tk, d, causal, seed)
         q, k, v = inp["q"], inp["k"], inp["v"]
         b = torch.as_tensor(inp["yat_b"], device="cuda")
         eps = torch.as_tensor(inp["yat_eps"], device="cuda")
-        ref_out, ref_mass, ref_max = attention.forward("yat", q, k, v, b=b, eps=eps, causal=True,
+        ref_out, ref_mass, ref_max = attention.forward("yat", q, k, v, b=b, eps=eps, causal=causal,
                                                        scale=w.scale)
-        prob = attention.make_problem(q, k, v, causal=True, scale=w.scale)
+        prob = attention.make_problem(q, k, v, causal=causal, scale=w.scale)
         out = torch.empty_like(ref_out)
         mass = torch.empty_like(ref_mass)
         mx = torch.empty_like(ref_max)
@@ -86,6 +94,6 @@ def test_noalloc_matches_forward_on_two_calls_in_a_row(lib):
     rc = lib.cattn_forward_noalloc(native.SOFTMAX, ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v),
                                    None, None, None, _ptr(out), None, None, stream)
     assert rc == native.OK
-    ref = attention.forward("softmax", q, k, v, causal=True, scale=w.scale, telemetry=False)[0]
+    ref = attention.forward("softmax", q, k, v, causal=causal, scale=w.scale, telemetry=False)[0]
     torch.cuda.synchronize()
     assert (out.float() - ref.float()).abs().max().item() <= OUT_TOL * float(v.abs().max())
