@@ -64,9 +64,11 @@ enum { CATTN_SOFTMAX = 0, CATTN_YAT = 1, CATTN_STAU = 2 };
 
 /* Element type of q, k, v and out.  Head widths dk, dv: any of 32, 64, 128.
  * bf16 with (dk, dv) = (64, 64), (128, 128) or (128, 64) runs on the tensor
- * cores (tcgen05, fp32 accumulation); fp32, and bf16 with the other width
- * pairs, run on the CUDA cores in full fp32 (bf16 widened on load, rounded
- * on store). */
+ * cores (tcgen05 kind::f16, fp32 accumulation); bf16 with the other width
+ * pairs runs on the CUDA cores in fp32 (widened on load, rounded on store).
+ * fp32 runs on the tensor cores as tcgen05 kind::tf32 in three passes (each
+ * operand split into tf32 hi and lo parts: hi*hi + hi*lo + lo*hi), which
+ * carries products to about 2^-20 of their size. */
 enum { CATTN_F32 = 0, CATTN_BF16 = 1 };
 
 /* cattn_problem_t.flags */
@@ -104,8 +106,8 @@ typedef struct {
   int hkv;    /* key/value heads, h % hkv == 0; query head i reads kv head i / (h/hkv) */
   int Tq;     /* query rows per head (>= 0; 0 is a no-op) */
   int Tk;     /* key rows per head (>= 1) */
-  int dk;     /* query/key width and        bf16: (dk, dv) in {(64,64), (128,128), (128,64)} */
-  int dv;     /* value width; supported:    fp32: (dk, dv) in {(32,32), (64,64), (128,128), (128,64)} */
+  int dk;     /* query/key width: 32, 64 or 128 */
+  int dv;     /* value width: 32, 64 or 128 (any pair; see the element types above) */
   int dtype;  /* CATTN_F32 or CATTN_BF16 */
   int causal; /* nonzero: key j is allowed for query row t only when j <= t; needs Tq == Tk */
   float scale; /* softmax and s^tau multiply q.k by this (> 0, e.g. 1/sqrt(dk)); Yat ignores it */
@@ -121,15 +123,19 @@ int cattn_version(void);
 const char *cattn_error_string(int status);
 
 /* Bytes of device workspace cattn_forward / cattn_key_norms need for this
- * problem and variant (0 if none), 256-byte aligned.  The fp32 path needs
- * none.  The bf16 path needs 256 bytes for its work-unit ticket, plus, for
+ * problem and variant (0 if none), 256-byte aligned.  The bf16 tensor-core
+ * path needs a 256-byte control block (its work-unit ticket and, for
+ * CATTN_YAT, the count of rows listed for the near-key pass), plus, for
  * CATTN_YAT, the fp32 squared norms of every key row (padded to a multiple of
- * 128 rows per head), plus, for
- * non-causal problems with few (batch, head, 256-row) units, the fp32 partial
- * outputs and per-row statistics of a fixed split of the keys (at most 64
- * splits, chosen from the shape alone).  The contents need not be
- * initialised.  Returns 0 for an invalid problem as well; cattn_validate says
- * why. */
+ * 128 rows per head) and the near-key list (8 bytes per row and key split),
+ * plus, for non-causal problems with few (batch, head, 256-row) units, the
+ * fp32 partial outputs and per-row statistics of a fixed split of the keys (at
+ * most 64 splits, chosen from the shape alone).  The fp32 path needs the
+ * control block, the tf32 hi / lo parts of q, k and of v transposed (keys
+ * padded to a multiple of 128): twice the inputs' size, plus, for CATTN_YAT,
+ * the key norms and the near-key list.  bf16 widths without tensor-core tiles
+ * need none.  The contents need not be initialised.  Returns 0 for an invalid
+ * problem as well; cattn_validate says why. */
 size_t cattn_workspace_bytes(int variant, const cattn_problem_t *p);
 
 /* Host-side argument checks only: never touches the GPU, never dereferences

@@ -19,8 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcattn.so")
-SOURCES = ["fwd_tc.cu", "bwd_tc.cu", "fwd_simt.cu", "bwd_simt.cu", "norms.cu", "api.cu", "noalloc.cu",
-           "host.cu"]
+SOURCES = ["fwd_tc.cu", "fwd_tf32.cu", "bwd_tc.cu", "fwd_simt.cu", "bwd_simt.cu", "norms.cu",
+           "api.cu", "noalloc.cu", "host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -37,7 +37,9 @@ bool is_empty(const cattn_problem_t *p) { return p->B == 0 || p->h == 0 || p->Tq
 //   part_o     key splits only: unnormalised partial outputs
 //              [n_splits, B*h, Tq, dv] fp32
 //   part_stat  key splits only: per-row [n_splits, B*h, Tq, 4] fp32
-// The fp32 (CUDA-core) path needs none.
+// The fp32 path (kind::tf32 on the tensor cores, three passes) has its own
+// layout (ws_tf32).  bf16 with widths the tensor-core kernel has no tiles for
+// (the CUDA-core kernel) needs none.
 size_t ws_nk_bytes(const cattn_problem_t *p) {
   return align256((size_t)p->B * p->hkv * tk_pad(p) * sizeof(float));
 }
@@ -50,6 +52,45 @@ struct WsLayout {
 
 // the control block's words
 constexpr int kCtrlTicket = 0, kCtrlNearCount = 1, kCtrlNkMax = 2;
+
+// Workspace of the fp32 path, each part 256-byte aligned: the control block
+// (the near-key count), the hi / lo parts of q and k in their own layouts and
+// of v transposed [B*hkv, dv, Tk_pad], then (Yat) |k|^2 [B*hkv, Tk_pad] and
+// the near-key list.
+struct WsTf32 {
+  size_t ctrl, qh, ql, kh, kl, vth, vtl, nk, near, total;
+  size_t near_cap;
+};
+
+WsTf32 ws_tf32(int variant, const cattn_problem_t *p) {
+  WsTf32 w;
+  memset(&w, 0, sizeof(w));
+  const size_t nq = (size_t)p->B * p->h * p->Tq * p->dk * 4;
+  const size_t nk = (size_t)p->B * p->hkv * p->Tk * p->dk * 4;
+  const size_t nvt = (size_t)p->B * p->hkv * p->dv * tk_pad(p) * 4;
+  size_t off = 256;
+  w.qh = off;
+  off += align256(nq);
+  w.ql = off;
+  off += align256(nq);
+  w.kh = off;
+  off += align256(nk);
+  w.kl = off;
+  off += align256(nk);
+  w.vth = off;
+  off += align256(nvt);
+  w.vtl = off;
+  off += align256(nvt);
+  if (variant == CATTN_YAT) {
+    w.nk = off;
+    off += ws_nk_bytes(p);
+    w.near = off;
+    w.near_cap = (size_t)p->B * p->h * p->Tq;
+    off += align256(w.near_cap * 8);
+  }
+  w.total = off;
+  return w;
+}
 
 WsLayout ws_layout(int variant, const cattn_problem_t *p) {
   WsLayout w;
@@ -75,6 +116,10 @@ WsLayout ws_layout(int variant, const cattn_problem_t *p) {
   }
   w.total = off;
   return w;
+}
+
+size_t forward_ws_bytes(int variant, const cattn_problem_t *p) {
+  return p->dtype == CATTN_F32 ? ws_tf32(variant, p).total : ws_layout(variant, p).total;
 }
 
 int check_problem(int variant, const cattn_problem_t *p) {
@@ -137,6 +182,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
+// fp32 [outer, rows, inner] as a 3-D tensor map with boxes of 32 x box_rows x 1
+// (128-byte rows) and 128-byte swizzle.  Reads past the extents are zeros.
+int encode_f32_3d(CUtensorMap *map, const void *base, int inner, int rows, int outer,
+                  int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return CATTN_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)outer};
+  cuuint64_t strides[2] = {(cuuint64_t)inner * 4, (cuuint64_t)rows * inner * 4};
+  cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CATTN_OK : CATTN_ERR_CUDA;
+}
+
 // bf16 [BH, T, d] as a 3-D tensor map with 64 x box_rows x 1 boxes and 128-byte
 // swizzle (the shared-memory layout the tcgen05 descriptors describe).  Rows
 // past T read as zeros.
@@ -174,7 +235,7 @@ const char *cattn_error_string(int status) {
 
 size_t cattn_workspace_bytes(int variant, const cattn_problem_t *p) {
   if (check_problem(variant, p) != CATTN_OK) return 0;
-  return ws_layout(variant, p).total;
+  return forward_ws_bytes(variant, p);
 }
 
 int cattn_validate(int variant, const cattn_problem_t *p, const void *q, const void *k,
@@ -188,7 +249,7 @@ int cattn_validate(int variant, const cattn_problem_t *p, const void *q, const v
   if (variant == CATTN_STAU && (!eps || !tau)) return CATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return CATTN_ERR_UNSUPPORTED;
-  const size_t need = ws_layout(variant, p).total;
+  const size_t need = forward_ws_bytes(variant, p);
   if (need > 0) {
     if (!workspace) return CATTN_ERR_INVALID_ARG;
     if (workspace_bytes < need) return CATTN_ERR_SHAPE;
@@ -256,6 +317,41 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
   fp.n_kv_tiles = (p->Tk + kTcKeyTile - 1) / kTcKeyTile;
   fp.test_stall = (p->flags & CATTN_FLAG_TEST_STALL) ? 1 : 0;
 
+  if (p->dtype == CATTN_F32) {
+    // fp32: split q, k, v into tf32 hi / lo parts, then the three-pass
+    // tensor-core forward, then (Yat) the near-key pass
+    const WsTf32 w = ws_tf32(variant, p);
+    char *ws = static_cast<char *>(workspace);
+    Tf32Split sp;
+    sp.qh = reinterpret_cast<float *>(ws + w.qh);
+    sp.ql = reinterpret_cast<float *>(ws + w.ql);
+    sp.kh = reinterpret_cast<float *>(ws + w.kh);
+    sp.kl = reinterpret_cast<float *>(ws + w.kl);
+    sp.vth = reinterpret_cast<float *>(ws + w.vth);
+    sp.vtl = reinterpret_cast<float *>(ws + w.vtl);
+    sp.nk = variant == CATTN_YAT ? reinterpret_cast<float *>(ws + w.nk) : nullptr;
+    fp.nk = sp.nk;
+    if (variant == CATTN_YAT) {
+      fp.near_count = reinterpret_cast<unsigned int *>(ws + w.ctrl) + kCtrlNearCount;
+      fp.near_rows = reinterpret_cast<uint2 *>(ws + w.near);
+      fp.near_cap = (unsigned int)(w.near_cap < 0xffffffffu ? w.near_cap : 0xffffffffu);
+    }
+    Tf32Maps m;
+    const int BH = p->B * p->h, BHK = p->B * p->hkv;
+    if ((rc = encode_f32_3d(&m.qh, sp.qh, p->dk, p->Tq, BH, 128)) != CATTN_OK) return rc;
+    if ((rc = encode_f32_3d(&m.ql, sp.ql, p->dk, p->Tq, BH, 128)) != CATTN_OK) return rc;
+    if ((rc = encode_f32_3d(&m.kh, sp.kh, p->dk, p->Tk, BHK, 32)) != CATTN_OK) return rc;
+    if ((rc = encode_f32_3d(&m.kl, sp.kl, p->dk, p->Tk, BHK, 32)) != CATTN_OK) return rc;
+    if ((rc = encode_f32_3d(&m.vh, sp.vth, fp.Tk_pad, p->dv, BHK, p->dv)) != CATTN_OK) return rc;
+    if ((rc = encode_f32_3d(&m.vl, sp.vtl, fp.Tk_pad, p->dv, BHK, p->dv)) != CATTN_OK) return rc;
+    if ((rc = map_cuda(cudaMemsetAsync(ws + w.ctrl, 0, 2 * sizeof(unsigned int), s))) != CATTN_OK)
+      return rc;
+    if ((rc = map_cuda(launch_split_tf32(fp, sp, variant, p->dk, p->dv, s))) != CATTN_OK) return rc;
+    if ((rc = map_cuda(launch_fwd_tf32(variant, p->dk, p->dv, fp, m, s))) != CATTN_OK) return rc;
+    if (variant == CATTN_YAT)
+      return map_cuda(launch_near_fix_f32(p->dk, p->dv, fp.yat_m, fp, s));
+    return CATTN_OK;
+  }
   if (!on_tensor_cores(p))
     return map_cuda(launch_fwd_simt(variant, p->dtype == CATTN_BF16, p->dk, p->dv, fp, s));
 
@@ -625,10 +721,11 @@ int cattn_backward(int variant, const cattn_problem_t *p, const void *q, const v
 int cattn_check_status(cattn_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return CATTN_ERR_CUDA;
-  unsigned int status = 0, bstatus = 0;
+  unsigned int status = 0, bstatus = 0, tstatus = 0;
   if (read_and_clear_status(&status) != cudaSuccess) return CATTN_ERR_CUDA;
   if (read_and_clear_bwd_status(&bstatus) != cudaSuccess) return CATTN_ERR_CUDA;
-  return (status | bstatus) ? CATTN_ERR_TIMEOUT : CATTN_OK;
+  if (read_and_clear_tf32_status(&tstatus) != cudaSuccess) return CATTN_ERR_CUDA;
+  return (status | bstatus | tstatus) ? CATTN_ERR_TIMEOUT : CATTN_OK;
 }
 
 }  // extern "C"

@@ -1,11 +1,10 @@
 // fwd_simt.cu -- attention forward on the CUDA cores.
 //
-// The fp32 problems are held to an output error of 1e-4 * max|v|; tf32
-// tensor-core operands (10-bit mantissa) cannot reach that, so fp32 inputs
-// take this path in full fp32 FMA arithmetic.  bf16 inputs whose head widths
-// the tensor-core kernel has no tiles for (any (dk, dv) in {32, 64, 128}^2
-// other than (64, 64), (128, 128), (128, 64)) take it too, widened to fp32
-// on load and rounded to bf16 on store.  One CTA holds 32 query rows of
+// bf16 inputs whose head widths the tensor-core kernel has no tiles for (any
+// (dk, dv) in {32, 64, 128}^2 other than (64, 64), (128, 128), (128, 64))
+// take this path, widened to fp32 on load and rounded to bf16 on store.
+// (fp32 inputs run on the tensor cores as three-pass tf32, fwd_tf32.cu; the
+// kernel here is instantiated for fp32 as well.)  One CTA holds 32 query rows of
 // one (batch, head); 8 warps take 4 rows each.  Keys stream through shared
 // memory 32 at a time; lane l owns key l of the tile for the score and owns
 // value columns l, l+32, ... for the weighted sum.

@@ -1205,7 +1205,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Fw
 // over what the fused kernel (and, with key splits, the combine) stored.  A
 // row listed twice (once per key split) is recomputed twice, with the same
 // result.  With no row listed every CTA returns at once.
-template <int DK, int DV, int YM>
+__device__ __forceinline__ float elem_f(const float *p) { return *p; }
+__device__ __forceinline__ float elem_f(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void elem_st(float *p, float v) { *p = v; }
+__device__ __forceinline__ void elem_st(__nv_bfloat16 *p, float v) { *p = __float2bfloat16_rn(v); }
+
+template <int DK, int DV, int YM, typename T>
 __global__ void __launch_bounds__(256) near_fix_kernel(const __grid_constant__ FwdParams p) {
   constexpr int QE = DK / 32;  // q and k components per lane
   constexpr int VE = DV / 32;  // v columns per lane
@@ -1213,9 +1218,9 @@ __global__ void __launch_bounds__(256) near_fix_kernel(const __grid_constant__ F
   __shared__ float s_o[8][DV];
   const unsigned n = min(*p.near_count, p.near_cap);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q);
-  const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(p.k);
-  const __nv_bfloat16 *vg = static_cast<const __nv_bfloat16 *>(p.v);
+  const T *qg = static_cast<const T *>(p.q);
+  const T *kg = static_cast<const T *>(p.k);
+  const T *vg = static_cast<const T *>(p.v);
   for (unsigned e = blockIdx.x; e < n; e += gridDim.x) {
     const uint2 id = p.near_rows[e];
     const int bh = (int)id.x, row = (int)id.y;
@@ -1225,17 +1230,17 @@ __global__ void __launch_bounds__(256) near_fix_kernel(const __grid_constant__ F
     float qf[QE];
 #pragma unroll
     for (int i = 0; i < QE; ++i)
-      qf[i] = __bfloat162float(qg[((size_t)bh * p.Tq + row) * DK + lane * QE + i]);
+      qf[i] = elem_f(qg + ((size_t)bh * p.Tq + row) * DK + lane * QE + i);
     const int lim = p.causal ? min(row + 1, p.Tk) : p.Tk;
     float mass = 0.f, top = 0.f, o[VE];
 #pragma unroll
     for (int c = 0; c < VE; ++c) o[c] = 0.f;
     for (int j = warp; j < lim; j += 8) {
-      const __nv_bfloat16 *kr = kg + (bh_kv * p.Tk + j) * DK + lane * QE;
+      const T *kr = kg + (bh_kv * p.Tk + j) * DK + lane * QE;
       float dot = 0.f, d2 = 0.f;
 #pragma unroll
       for (int i = 0; i < QE; ++i) {
-        const float kf = __bfloat162float(kr[i]);
+        const float kf = elem_f(kr + i);
         dot = fmaf(qf[i], kf, dot);
         const float df = qf[i] - kf;
         d2 = fmaf(df, df, d2);
@@ -1252,9 +1257,9 @@ __global__ void __launch_bounds__(256) near_fix_kernel(const __grid_constant__ F
       const float kap = num / (fmaxf(d2, 0.f) + eps);
       mass += kap;
       top = fmaxf(top, kap);
-      const __nv_bfloat16 *vr = vg + (bh_kv * p.Tk + j) * DV + lane * VE;
+      const T *vr = vg + (bh_kv * p.Tk + j) * DV + lane * VE;
 #pragma unroll
-      for (int c = 0; c < VE; ++c) o[c] = fmaf(kap, __bfloat162float(vr[c]), o[c]);
+      for (int c = 0; c < VE; ++c) o[c] = fmaf(kap, elem_f(vr + c), o[c]);
     }
     if (lane == 0) {
       s_mass[warp] = mass;
@@ -1272,13 +1277,13 @@ __global__ void __launch_bounds__(256) near_fix_kernel(const __grid_constant__ F
       }
       const float inv = 1.f / (m_all + 1e-9f);
       const size_t ti = (size_t)bh * p.Tq + row;
-      __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.out) + ti * DV + lane * VE;
+      T *orow = static_cast<T *>(p.out) + ti * DV + lane * VE;
 #pragma unroll
       for (int c = 0; c < VE; ++c) {
         float acc = 0.f;
 #pragma unroll
         for (int w = 0; w < 8; ++w) acc += s_o[w][lane * VE + c];
-        orow[c] = __float2bfloat16_rn(acc * inv);
+        elem_st(orow + c, acc * inv);
       }
       if (lane == 0) {
         if (p.row_mass) p.row_mass[ti] = m_all;
@@ -1336,7 +1341,7 @@ cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap 
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if constexpr (VARIANT == kYat) {
-      near_fix_kernel<DK, DV, YM><<<sm_count, 256, 0, s>>>(p);
+      near_fix_kernel<DK, DV, YM, __nv_bfloat16><<<sm_count, 256, 0, s>>>(p);
       e = cudaGetLastError();
     }
     return e;
@@ -1408,6 +1413,34 @@ cudaError_t launch_row_stats_tc(int variant, int dk, const FwdParams &p, const C
   CATTN_TC_STATS(kStau, 64)
   CATTN_TC_STATS(kStau, 128)
 #undef CATTN_TC_STATS
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_near_fix_f32(int dk, int dv, int ym, const FwdParams &p, cudaStream_t s) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+#define CATTN_NEAR_F32(DK_, DV_)                                                        \
+  if (dk == DK_ && dv == DV_) {                                                         \
+    if (ym == 2)                                                                        \
+      tc::near_fix_kernel<DK_, DV_, 2, float><<<sms, 256, 0, s>>>(p);                   \
+    else if (ym == 3)                                                                   \
+      tc::near_fix_kernel<DK_, DV_, 3, float><<<sms, 256, 0, s>>>(p);                   \
+    else                                                                                \
+      tc::near_fix_kernel<DK_, DV_, 1, float><<<sms, 256, 0, s>>>(p);                   \
+    return cudaGetLastError();                                                          \
+  }
+  CATTN_NEAR_F32(32, 32)
+  CATTN_NEAR_F32(32, 64)
+  CATTN_NEAR_F32(32, 128)
+  CATTN_NEAR_F32(64, 32)
+  CATTN_NEAR_F32(64, 64)
+  CATTN_NEAR_F32(64, 128)
+  CATTN_NEAR_F32(128, 32)
+  CATTN_NEAR_F32(128, 64)
+  CATTN_NEAR_F32(128, 128)
+#undef CATTN_NEAR_F32
   return cudaErrorInvalidValue;
 }
 

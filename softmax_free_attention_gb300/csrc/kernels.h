@@ -89,6 +89,26 @@ cudaError_t launch_fwd_simt(int variant, bool bf16, int dk, int dv, const FwdPar
                             cudaStream_t s);
 bool fwd_simt_supported(int dk, int dv);
 
+// fp32 inputs on the tensor cores (kind::tf32 in three passes).  The split
+// pass writes the hi / lo parts of q and k (their own layouts), of v
+// transposed to [B*hkv, dv, Tk_pad] (keys contiguous, zero past Tk) and, for
+// Yat, |k|^2 [B*hkv, Tk_pad]; the forward reads them through these maps
+// (32-element boxes, 128-byte swizzle): q, k boxes of 128 and 32 rows, v^T
+// boxes of 32 keys by dv rows.
+struct Tf32Split {
+  float *qh, *ql, *kh, *kl, *vth, *vtl, *nk;
+};
+struct Tf32Maps {
+  CUtensorMap qh, ql, kh, kl, vh, vl;
+};
+cudaError_t launch_split_tf32(const FwdParams &p, const Tf32Split &w, int variant, int dk, int dv,
+                              cudaStream_t s);
+cudaError_t launch_fwd_tf32(int variant, int dk, int dv, const FwdParams &p, const Tf32Maps &m,
+                            cudaStream_t s);
+cudaError_t read_and_clear_tf32_status(unsigned int *value);
+// The near-key pass for fp32 inputs (the bf16 forward launches its own).
+cudaError_t launch_near_fix_f32(int dk, int dv, int ym, const FwdParams &p, cudaStream_t s);
+
 // Squared row norms of a bf16 [BH, T, d] tensor into out[BH, T_pad] (zeros
 // for padded rows); their maximum is folded into *max_bits (fp32 bits, which
 // must hold 0 or an earlier maximum) with atomicMax.

@@ -130,8 +130,17 @@ def test_workspace_layout(lib):
     assert lib.cattn_workspace_bytes(native.YAT, ctypes.byref(p)) == 256 + nk + near
     assert lib.cattn_workspace_bytes(native.SOFTMAX, ctypes.byref(p)) == 256
     assert lib.cattn_workspace_bytes(native.STAU, ctypes.byref(p)) == 256
+    # fp32 (three-pass tf32 on the tensor cores): the control block, hi / lo
+    # of q and k, hi / lo of v transposed with its keys padded to a multiple of
+    # 128, then (Yat) |k|^2 and the near-key list; each part rounded to 256 B
     p32 = prob(dtype=native.F32, dk=32, dv=32)
-    assert lib.cattn_workspace_bytes(native.YAT, ctypes.byref(p32)) == 0
+    r256 = lambda x: (x + 255) // 256 * 256
+    qk = r256(1 * 4 * 256 * 32 * 4)
+    vt = r256(1 * 4 * 32 * 256 * 4)
+    base32 = 256 + 4 * qk + 2 * vt
+    assert lib.cattn_workspace_bytes(native.SOFTMAX, ctypes.byref(p32)) == base32
+    assert lib.cattn_workspace_bytes(native.YAT, ctypes.byref(p32)) == \
+        base32 + r256(1 * 4 * 256 * 4) + r256(1 * 4 * 256 * 8)
     # non-causal with two 256-row units and 17 key tiles: two key splits of 9
     # and 8 tiles, each leaving fp32 partials [2, B*h, Tq, dv] and [2, B*h, Tq, 4]
     ps = prob(B=1, h=2, hkv=2, Tq=200, Tk=2100, causal=0)
