@@ -344,8 +344,7 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
     if ((rc = encode_f32_3d(&m.kl, sp.kl, p->dk, p->Tk, BHK, 32)) != CATTN_OK) return rc;
     if ((rc = encode_f32_3d(&m.vh, sp.vth, fp.Tk_pad, p->dv, BHK, p->dv)) != CATTN_OK) return rc;
     if ((rc = encode_f32_3d(&m.vl, sp.vtl, fp.Tk_pad, p->dv, BHK, p->dv)) != CATTN_OK) return rc;
-    if ((rc = map_cuda(cudaMemsetAsync(ws + w.ctrl, 0, 2 * sizeof(unsigned int), s))) != CATTN_OK)
-      return rc;
+    // (the split pass also zeroes the near-key count)
     if ((rc = map_cuda(launch_split_tf32(fp, sp, variant, p->dk, p->dv, s))) != CATTN_OK) return rc;
     if ((rc = map_cuda(launch_fwd_tf32(variant, p->dk, p->dv, fp, m, s))) != CATTN_OK) return rc;
     if (variant == CATTN_YAT)
@@ -372,17 +371,23 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
     fp.near_count = reinterpret_cast<unsigned int *>(ws + w.ctrl) + kCtrlNearCount;
     fp.near_rows = reinterpret_cast<uint2 *>(ws + w.near);
     fp.near_cap = (unsigned int)(w.near_cap < 0xffffffffu ? w.near_cap : 0xffffffffu);
-    if (!(p->flags & CATTN_FLAG_NORMS_READY)) {
-      rc = cattn_key_norms(p, k, workspace, workspace_bytes, stream);
-      if (rc != CATTN_OK) return rc;
-    }
   }
   CUtensorMap tq, tk, tv;
   if ((rc = encode_bf16_3d(&tq, q, p->dk, p->Tq, p->B * p->h, kTcQueryTile)) != CATTN_OK) return rc;
   if ((rc = encode_bf16_3d(&tk, k, p->dk, p->Tk, p->B * p->hkv, kTcKeyTile)) != CATTN_OK) return rc;
   if ((rc = encode_bf16_3d(&tv, v, p->dv, p->Tk, p->B * p->hkv, kTcKeyTile)) != CATTN_OK) return rc;
-  // the ticket and the near-key count start at zero
-  if ((rc = map_cuda(cudaMemsetAsync(ws + w.ctrl, 0, 2 * sizeof(unsigned int), s))) != CATTN_OK)
+  // the ticket and the near-key count start at zero, and so does the largest
+  // key norm when this call takes the norms itself (one memset for all three)
+  const bool own_norms = variant == CATTN_YAT && !(p->flags & CATTN_FLAG_NORMS_READY);
+  if ((rc = map_cuda(cudaMemsetAsync(ws + w.ctrl, 0, (own_norms ? 3 : 2) * sizeof(unsigned int),
+                                     s))) != CATTN_OK)
+    return rc;
+  if (own_norms &&
+      (rc = map_cuda(launch_row_sqnorm_bf16(k, reinterpret_cast<float *>(ws + w.nk), p->B * p->hkv,
+                                            p->Tk, tk_pad(p), p->dk,
+                                            reinterpret_cast<unsigned int *>(ws + w.ctrl) +
+                                                kCtrlNkMax,
+                                            s))) != CATTN_OK)
     return rc;
   return map_cuda(launch_fwd_tc(variant, p->dk, p->dv, fp, tq, tk, tv, s));
 }

@@ -449,55 +449,74 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // ---------------------------------------------------------------- split pass
 
-// hi / lo of q or k, element by element (same layout as the input).
-__global__ void split_kernel(const float *__restrict__ x, float *__restrict__ hi,
-                             float *__restrict__ lo, size_t n) {
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const float v = x[i], h = tf32_hi(v);
-    hi[i] = h;
-    lo[i] = v - h;
-  }
-}
+// One launch prepares every operand of the fp32 forward.  Blocks [0, nb_e)
+// split q then k element by element (hi, lo in the input's layout); blocks
+// [nb_e, nb_e + nb_v) each transpose one 32 keys x 32 columns tile of v into
+// v^T hi / lo [BHkv, dv, Tk_pad] (keys contiguous, zero past Tk) through
+// shared memory; the remaining blocks (Yat) take |k|^2 of 256 key rows each
+// (fp64 accumulation, rounded once; zero for padded rows).  Block 0 also
+// zeroes the near-key count the forward appends to.
+struct PrepArgs {
+  const float *q, *k, *v;
+  Tf32Split w;
+  unsigned int *near_count;
+  size_t nq, nk;          // elements of q and of k
+  int nb_e, nb_v;         // blocks of the element split and of the transpose
+  int tiles_k, tiles_c;   // transpose tiles per (bh_kv) along keys and columns
+  int BHkv, Tk, Tk_pad, dk, dv;
+};
 
-// v [BHkv, Tk, dv] -> hi / lo of its transpose [BHkv, dv, Tk_pad] (keys
-// contiguous, zero past Tk), through a 32 x 32 tile of shared memory.
-__global__ void split_transpose_kernel(const float *__restrict__ v, float *__restrict__ vth,
-                                       float *__restrict__ vtl, int Tk, int Tk_pad, int dv) {
+__global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ PrepArgs a) {
   __shared__ float tile[32][33];
-  const int bhkv = blockIdx.z;
-  const int k0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
-  const float *vb = v + (size_t)bhkv * Tk * dv;
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const int key = k0 + i, col = c0 + threadIdx.x;
-    tile[i][threadIdx.x] = (key < Tk && col < dv) ? vb[(size_t)key * dv + col] : 0.f;
-  }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const int col = c0 + i, key = k0 + threadIdx.x;
-    if (col < dv && key < Tk_pad) {
-      const float val = tile[threadIdx.x][i], h = tf32_hi(val);
-      const size_t o = ((size_t)bhkv * dv + col) * Tk_pad + key;
-      vth[o] = h;
-      vtl[o] = val - h;
+  const int blk = blockIdx.x;
+  if (blk == 0 && threadIdx.x == 0 && a.near_count) *a.near_count = 0u;
+  if (blk < a.nb_e) {
+    const size_t n = a.nq + a.nk;
+    for (size_t i = (size_t)blk * 256 + threadIdx.x; i < n; i += (size_t)a.nb_e * 256) {
+      const bool isq = i < a.nq;
+      const size_t j = isq ? i : i - a.nq;
+      const float x = isq ? a.q[j] : a.k[j], h = tf32_hi(x);
+      (isq ? a.w.qh : a.w.kh)[j] = h;
+      (isq ? a.w.ql : a.w.kl)[j] = x - h;
     }
-  }
-}
-
-// |k|^2 of each fp32 key row, accumulated in fp64 and rounded once.
-__global__ void key_sqnorm_kernel(const float *__restrict__ k, float *__restrict__ nk, int rows,
-                                  int T, int T_pad, int d) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= rows * T_pad) return;
-  const int bhkv = i / T_pad, t = i - bhkv * T_pad;
-  if (t >= T) {
-    nk[i] = 0.f;
     return;
   }
-  const float *kr = k + ((size_t)bhkv * T + t) * d;
+  if (blk < a.nb_e + a.nb_v) {
+    int t = blk - a.nb_e;
+    const int tk = t % a.tiles_k;
+    t /= a.tiles_k;
+    const int tc = t % a.tiles_c;
+    const int bhkv = t / a.tiles_c;
+    const int k0 = tk * 32, c0 = tc * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+    const float *vb = a.v + (size_t)bhkv * a.Tk * a.dv;
+    for (int i = ty; i < 32; i += 8) {
+      const int key = k0 + i, col = c0 + tx;
+      tile[i][tx] = (key < a.Tk && col < a.dv) ? vb[(size_t)key * a.dv + col] : 0.f;
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+      const int col = c0 + i, key = k0 + tx;
+      if (col < a.dv && key < a.Tk_pad) {
+        const float val = tile[tx][i], h = tf32_hi(val);
+        const size_t o = ((size_t)bhkv * a.dv + col) * a.Tk_pad + key;
+        a.w.vth[o] = h;
+        a.w.vtl[o] = val - h;
+      }
+    }
+    return;
+  }
+  const int i = (blk - a.nb_e - a.nb_v) * 256 + threadIdx.x;
+  if (i >= a.BHkv * a.Tk_pad) return;
+  const int bhkv = i / a.Tk_pad, t = i - bhkv * a.Tk_pad;
+  if (t >= a.Tk) {
+    a.w.nk[i] = 0.f;
+    return;
+  }
+  const float *kr = a.k + ((size_t)bhkv * a.Tk + t) * a.dk;
   double s = 0.0;
-  for (int c = 0; c < d; ++c) s = fma((double)kr[c], (double)kr[c], s);
-  nk[i] = (float)s;
+  for (int c = 0; c < a.dk; ++c) s = fma((double)kr[c], (double)kr[c], s);
+  a.w.nk[i] = (float)s;
 }
 
 template <int VARIANT, int DK, int DV, int YM>
@@ -538,25 +557,29 @@ cudaError_t by_shape(int dk, int dv, const FwdParams &p, const Tf32Maps &m, cuda
 
 cudaError_t launch_split_tf32(const FwdParams &p, const Tf32Split &w, int variant, int dk,
                               int dv, cudaStream_t s) {
-  const size_t nq = (size_t)p.B * p.h * p.Tq * dk, nkk = (size_t)p.B * p.hkv * p.Tk * dk;
-  const unsigned gq = (unsigned)((nq + 255) / 256 < 4096 ? (nq + 255) / 256 : 4096);
-  const unsigned gk = (unsigned)((nkk + 255) / 256 < 4096 ? (nkk + 255) / 256 : 4096);
-  if (nq > 0) tf32::split_kernel<<<gq, 256, 0, s>>>(static_cast<const float *>(p.q), w.qh, w.ql, nq);
-  if (nkk > 0)
-    tf32::split_kernel<<<gk, 256, 0, s>>>(static_cast<const float *>(p.k), w.kh, w.kl, nkk);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int BHkv = p.B * p.hkv;
-  if (BHkv > 0) {
-    dim3 g((unsigned)((p.Tk_pad + 31) / 32), (unsigned)((dv + 31) / 32), (unsigned)BHkv);
-    tf32::split_transpose_kernel<<<g, dim3(32, 8), 0, s>>>(static_cast<const float *>(p.v), w.vth,
-                                                            w.vtl, p.Tk, p.Tk_pad, dv);
-    if (variant == kYat) {
-      const int n = BHkv * p.Tk_pad;
-      tf32::key_sqnorm_kernel<<<(n + 255) / 256, 256, 0, s>>>(static_cast<const float *>(p.k), w.nk,
-                                                               BHkv, p.Tk, p.Tk_pad, dk);
-    }
-  }
+  tf32::PrepArgs a;
+  a.q = static_cast<const float *>(p.q);
+  a.k = static_cast<const float *>(p.k);
+  a.v = static_cast<const float *>(p.v);
+  a.w = w;
+  a.near_count = variant == kYat ? p.near_count : nullptr;
+  a.nq = (size_t)p.B * p.h * p.Tq * dk;
+  a.nk = (size_t)p.B * p.hkv * p.Tk * dk;
+  const size_t ne = a.nq + a.nk;
+  a.nb_e = (int)((ne + 255) / 256 < 2048 ? (ne + 255) / 256 : 2048);
+  if (a.nb_e < 1) a.nb_e = 1;
+  a.BHkv = p.B * p.hkv;
+  a.Tk = p.Tk;
+  a.Tk_pad = p.Tk_pad;
+  a.dk = dk;
+  a.dv = dv;
+  a.tiles_k = (p.Tk_pad + 31) / 32;
+  a.tiles_c = (dv + 31) / 32;
+  a.nb_v = a.BHkv * a.tiles_k * a.tiles_c;
+  const int nb_n = variant == kYat ? (a.BHkv * p.Tk_pad + 255) / 256 : 0;
+  const long long blocks = (long long)a.nb_e + a.nb_v + nb_n;
+  if (blocks <= 0) return cudaSuccess;
+  tf32::prep_kernel<<<(unsigned)blocks, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

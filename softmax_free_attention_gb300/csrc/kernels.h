@@ -101,6 +101,7 @@ struct Tf32Split {
 struct Tf32Maps {
   CUtensorMap qh, ql, kh, kl, vh, vl;
 };
+// (one launch; it also zeroes p.near_count for Yat)
 cudaError_t launch_split_tf32(const FwdParams &p, const Tf32Split &w, int variant, int dk, int dv,
                               cudaStream_t s);
 cudaError_t launch_fwd_tf32(int variant, int dk, int dv, const FwdParams &p, const Tf32Maps &m,
