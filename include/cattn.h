@@ -166,6 +166,25 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
                   float *row_mass, float *row_max_score, void *workspace,
                   size_t workspace_bytes, cattn_stream_t stream);
 
+/* The forward of cattn_forward, plus each row's normalised entropy of the
+ * map's weights written into row_entropy (device fp32 [B, h, Tq], required):
+ * -sum_j w_j ln w_j / ln n over the row's n allowed keys, 0 when n = 1 ("The
+ * Kernel Between the Roles", section "The run": zero for a row on one key,
+ * one for a row spread evenly; Yat weights kappa / (M + 1e-9), as the row
+ * statistics pass).  Accumulated in the same pass as the output: each row
+ * keeps sum_j f_j log2 f_j of its weights' numerators f (Yat kappa; softmax
+ * and s^tau the exponentials on their running max, moved onto a new max
+ * exactly as the normaliser is) and writes ln Z - ln 2 (sum f log2 f) / Z
+ * (Yat: (M ln Z' - ln 2 sum f log2 f) / Z', Z' = M + 1e-9).  bf16 inputs on
+ * the tensor cores with yat_m = 1 only (else CATTN_ERR_UNSUPPORTED); other
+ * arguments, the workspace and the errors are those of cattn_forward.  The
+ * fraction of weights below 1e-6 and the top-10 mass still need
+ * cattn_row_stats. */
+int cattn_forward_entropy(int variant, const cattn_problem_t *p, const void *q, const void *k,
+                          const void *v, const float *b, const float *eps, const float *tau,
+                          void *out, float *row_mass, float *row_max_score, float *row_entropy,
+                          void *workspace, size_t workspace_bytes, cattn_stream_t stream);
+
 /* The same forward for callers that cannot allocate device memory (a plug-in
  * whose host engine plans all device memory at start-up and forbids later
  * allocations, or a latency-critical loop that cannot afford cudaMalloc's

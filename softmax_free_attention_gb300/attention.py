@@ -141,6 +141,37 @@ def forward(variant, q, k, v, *, b=None, eps=None, tau=None, causal=False, scale
     return out, row_mass, row_max
 
 
+def forward_entropy(variant, q, k, v, *, b=None, eps=None, tau=None, causal=False, scale=None,
+                    workspace=None, norms_ready=False):
+    """forward() on CUDA bf16 tensors, plus each row's normalised entropy of the
+    map's weights accumulated in the same pass (cattn_forward_entropy).
+
+    Returns (out, row_mass, row_max, row_entropy), the last [B, h, Tq] fp32.
+    """
+    vid = variant_id(variant)
+    prob = make_problem(q, k, v, causal=causal, scale=scale, norms_ready=norms_ready)
+    dev = q.device
+    B, h, Tq, _ = q.shape
+    out = torch.empty((B, h, Tq, v.shape[-1]), dtype=q.dtype, device=dev)
+    row_mass = torch.empty((B, h, Tq), dtype=torch.float32, device=dev)
+    row_max = torch.empty_like(row_mass)
+    row_ent = torch.empty_like(row_mass)
+    bt = _per_head(b, h, dev, "b") if vid == native.YAT else None
+    et = _per_head(eps, h, dev, "eps") if vid in (native.YAT, native.STAU) else None
+    tt = _per_head(tau, h, dev, "tau") if vid == native.STAU else None
+    lib = native.load()
+    need = int(lib.cattn_workspace_bytes(vid, ctypes.byref(prob)))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    status = lib.cattn_forward_entropy(vid, ctypes.byref(prob), _ptr(q), _ptr(k), _ptr(v),
+                                       _ptr(bt), _ptr(et), _ptr(tt), _ptr(out), _ptr(row_mass),
+                                       _ptr(row_max), _ptr(row_ent), _ptr(workspace), ws_bytes,
+                                       _stream_handle(dev))
+    native.check(status, "cattn_forward_entropy")
+    return out, row_mass, row_max, row_ent
+
+
 HOST_CHUNKS = 8  # batch chunks of the host-buffer forward (copy / compute overlap)
 
 

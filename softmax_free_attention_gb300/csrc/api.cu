@@ -280,10 +280,16 @@ int cattn_key_norms(const cattn_problem_t *p, const void *k, void *workspace,
       launch_row_sqnorm_bf16(k, nk, p->B * p->hkv, p->Tk, tk_pad(p), p->dk, nk_max, s));
 }
 
-int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const void *k,
-                  const void *v, const float *b, const float *eps, const float *tau, void *out,
-                  float *row_mass, float *row_max_score, void *workspace,
-                  size_t workspace_bytes, cattn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The forward of cattn_forward and cattn_forward_entropy (row_entropy NULL
+// for the former).
+int forward_impl(int variant, const cattn_problem_t *p, const void *q, const void *k,
+                 const void *v, const float *b, const float *eps, const float *tau, void *out,
+                 float *row_mass, float *row_max_score, float *row_entropy, void *workspace,
+                 size_t workspace_bytes, cattn_stream_t stream) {
   int rc = cattn_validate(variant, p, q, k, v, b, eps, tau, out, workspace, workspace_bytes);
   if (rc != CATTN_OK) return rc;
   if (is_empty(p)) return CATTN_OK;
@@ -300,6 +306,7 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
   fp.out_align32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0;
   fp.row_mass = row_mass;
   fp.row_max = row_max_score;
+  fp.row_entropy = row_entropy;
   fp.b = b;
   fp.eps = eps;
   fp.tau = tau;
@@ -390,6 +397,31 @@ int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const vo
                                             s))) != CATTN_OK)
     return rc;
   return map_cuda(launch_fwd_tc(variant, p->dk, p->dv, fp, tq, tk, tv, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+int cattn_forward(int variant, const cattn_problem_t *p, const void *q, const void *k,
+                  const void *v, const float *b, const float *eps, const float *tau, void *out,
+                  float *row_mass, float *row_max_score, void *workspace,
+                  size_t workspace_bytes, cattn_stream_t stream) {
+  return forward_impl(variant, p, q, k, v, b, eps, tau, out, row_mass, row_max_score, nullptr,
+                      workspace, workspace_bytes, stream);
+}
+
+int cattn_forward_entropy(int variant, const cattn_problem_t *p, const void *q, const void *k,
+                          const void *v, const float *b, const float *eps, const float *tau,
+                          void *out, float *row_mass, float *row_max_score, float *row_entropy,
+                          void *workspace, size_t workspace_bytes, cattn_stream_t stream) {
+  int rc = check_problem(variant, p);
+  if (rc != CATTN_OK) return rc;
+  if (!on_tensor_cores(p) || p->yat_m > 1) return CATTN_ERR_UNSUPPORTED;
+  if (is_empty(p)) return CATTN_OK;
+  if (!row_entropy) return CATTN_ERR_INVALID_ARG;
+  return forward_impl(variant, p, q, k, v, b, eps, tau, out, row_mass, row_max_score, row_entropy,
+                      workspace, workspace_bytes, stream);
 }
 
 // The tau* pass reads no V: its problem is checked as an s^tau problem whose

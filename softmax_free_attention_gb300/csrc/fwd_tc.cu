@@ -331,7 +331,10 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams &p, int u) {
 
 // YM: Yat numerator exponent 2 YM (1 for the other maps).  STATS: the row
 // statistics pass (no V, no PV, no O; the weights' statistics per row).
-template <int VARIANT, int DK, int DV, int YM = 1, bool STATS = false>
+// ENT: the forward also accumulates each row's sum f log2 f of its weights'
+// numerators f (Yat kappa; softmax, s^tau 2^(x - m) on the running max m) and
+// writes the row's normalised entropy.
+template <int VARIANT, int DK, int DV, int YM = 1, bool STATS = false, bool ENT = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
@@ -664,6 +667,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // this row relative to the unit's first key tile
       int nk_tiles, lim_base, nkv;
       float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // Yat: mass; else l
+      float2 ent[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // ENT: sum f log2 f
       float top[2] = {-INFINITY, -INFINITY};  // Yat: max kappa; else max raw dot
       float m_used = -INFINITY;               // softmax / s^tau: running max, log2 units
       float yb = 0.f, yeps = 0.f, qe = 0.f, tau = 1.f, seps = 0.f;
@@ -883,14 +887,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tmem_ld_fence(sr);
               if (fast) {
                 if (kind == 2)
-                  yat_chunk<true, true, YM>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+                  yat_chunk<true, true, YM, ENT>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk,
+                                                ent);
                 else
-                  yat_chunk<false, true, YM>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+                  yat_chunk<false, true, YM, ENT>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk,
+                                                ent);
               } else {
                 if (kind == 2)
-                  yat_chunk<true, false, YM>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+                  yat_chunk<true, false, YM, ENT>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk,
+                                                ent);
                 else
-                  yat_chunk<false, false, YM>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk);
+                  yat_chunk<false, false, YM, ENT>(sr, half * 2 + c, nk4, yb, qe, yeps, limit, acc, top, hk,
+                                                ent);
               }
             }
             tmem_st16(t_s + 16 * c, hk);
@@ -928,6 +936,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (__any_sync(FULL, m_new > m_used + RESCALE_THRESHOLD)) {
             const float mn = fmaxf(m_used, m_new);
             corr = ex2_approx(m_used - mn);
+            if (ENT && m_used > -INFINITY) {
+              // sum p (x - m) onto the new max: each p scales by corr and each
+              // exponent drops by mn - m_used
+              const float dm = m_used - mn;
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                ent[hh].x = corr * fmaf(dm, acc[hh].x, ent[hh].x);
+                ent[hh].y = corr * fmaf(dm, acc[hh].y, ent[hh].y);
+              }
+            }
             acc[0].x *= corr;
             acc[0].y *= corr;
             acc[1].x *= corr;
@@ -948,16 +966,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t hk[16];
             if (VARIANT == kSoftmax) {
               if (partial)
-                softmax_chunk<true>(sr[c], half * 2 + c, c2, -m_used, limit, acc, hk);
+                softmax_chunk<true, ENT>(sr[c], half * 2 + c, c2, -m_used, limit, acc, hk, ent);
               else
-                softmax_chunk<false>(sr[c], half * 2 + c, c2, -m_used, limit, acc, hk);
+                softmax_chunk<false, ENT>(sr[c], half * 2 + c, c2, -m_used, limit, acc, hk, ent);
             } else {
               if (partial)
-                stau_chunk<true>(sr[c], half * 2 + c, p.scale, c2, tau, seps, -m_used, limit, acc,
-                                 hk);
+                stau_chunk<true, ENT>(sr[c], half * 2 + c, p.scale, c2, tau, seps, -m_used, limit,
+                                      acc, hk, ent);
               else
-                stau_chunk<false>(sr[c], half * 2 + c, p.scale, c2, tau, seps, -m_used, limit, acc,
-                                  hk);
+                stau_chunk<false, ENT>(sr[c], half * 2 + c, p.scale, c2, tau, seps, -m_used, limit,
+                                       acc, hk, ent);
             }
             if (SPLIT_PV && c == 0) {
               // O holds every tile before j (S_x(j) landed after PV_x(j-1)):
@@ -1050,11 +1068,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float part = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
         const float ptop = fmaxf(top[0], top[1]);
         float *fb = xchg + (8 + (uint32_t)x * 4) * BM;  // [2 values][2 halves][BM]
+        float *eb = xchg + (16 + (uint32_t)x * 2) * BM;  // ENT: [2 halves][BM]
         fb[(0 * 2 + half) * BM + r] = part;
         fb[(1 * 2 + half) * BM + r] = ptop;
+        const float pent = ENT ? (ent[0].x + ent[0].y) + (ent[1].x + ent[1].y) : 0.f;
+        if (ENT) eb[half * BM + r] = pent;
         named_barrier_sync(named_bar, 64);
         const float total = part + fb[(0 * 2 + (half ^ 1)) * BM + r];
         const float all_top = fmaxf(ptop, fb[(1 * 2 + (half ^ 1)) * BM + r]);
+        const float all_ent = ENT ? pent + eb[(half ^ 1) * BM + r] : 0.f;
         // the partner reads fb before either warp writes it for the next unit
         named_barrier_sync(named_bar, 64);
         // everything that does not need O before the wait, while the last PV runs
@@ -1098,6 +1120,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if (row_ok && half == 0) {
             const size_t ti = (size_t)t.bh * p.Tq + row;
+            if (ENT) {
+              // normalised entropy of the row's weights f / Z from Z and
+              // sum f log2 f: -sum w ln w = ln Z - ln 2 (sum f log2 f) / Z
+              // (Yat: w = kappa / Z', Z' = M + 1e-9, so the first term is
+              // M ln Z' / Z')
+              const int n = p.causal ? min(row + 1, p.Tk) : p.Tk;
+              float hrow;
+              if (VARIANT == kYat) {
+                const float z = total + 1e-9f;
+                hrow = (total * logf(z) - LN2 * all_ent) / z;
+              } else {
+                hrow = logf(total) - LN2 * all_ent / total;
+              }
+              p.row_entropy[ti] = n > 1 ? hrow / logf((float)n) : 0.f;
+            }
             if (VARIANT == kYat && all_top > yat_near_threshold(qe - yeps, yb, YM)) {
               // a key may sit close enough to q for the assembled distance to
               // have cancelled: the near-key pass recomputes this row
@@ -1125,7 +1162,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           if (row_ok && half == 0) {
-            reinterpret_cast<float4 *>(p.part_stat)[ti] = make_float4(total, m_used, all_top, 0.f);
+            reinterpret_cast<float4 *>(p.part_stat)[ti] = make_float4(total, m_used, all_top, all_ent);
             if (VARIANT == kYat && all_top > yat_near_threshold(qe - yeps, yb, YM)) {
               const unsigned slot = atomicAdd(p.near_count, 1u);
               if (slot < p.near_cap) p.near_rows[slot] = make_uint2((unsigned)t.bh, (unsigned)row);
@@ -1167,7 +1204,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Fw
     m_all = fmaxf(m_all, st.y);
     top = fmaxf(top, st.z);
   }
-  float total = 0.f;
+  float total = 0.f, ent = 0.f;  // ent: sum f log2 f on m_all (ENT)
   constexpr int PER_LANE = DV / 32;  // 2 or 4 columns per lane
   float o[PER_LANE];
 #pragma unroll
@@ -1176,6 +1213,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Fw
     const float4 st = stat[(long long)s * rows + rrow];
     const float w = VARIANT == kYat ? 1.f : (st.y == -INFINITY ? 0.f : exp2f(st.y - m_all));
     total += w * st.x;
+    if (p.row_entropy && w > 0.f)
+      ent += VARIANT == kYat ? st.w : w * fmaf(st.y - m_all, st.x, st.w);
     const float *src = p.part_o + ((long long)s * rows + rrow) * DV + lane * PER_LANE;
 #pragma unroll
     for (int i = 0; i < PER_LANE; ++i) o[i] += w * src[i];
@@ -1190,6 +1229,16 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Fw
   if (lane == 0) {
     if (p.row_mass) p.row_mass[rrow] = VARIANT == kYat ? total : (m_all + log2f(total)) * LN2;
     if (p.row_max) p.row_max[rrow] = VARIANT == kYat ? top : top * p.scale;
+    if (p.row_entropy) {  // key splits are non-causal: every row has Tk keys
+      float hrow;
+      if (VARIANT == kYat) {
+        const float z = total + 1e-9f;
+        hrow = (total * logf(z) - LN2 * ent) / z;
+      } else {
+        hrow = logf(total) - LN2 * ent / total;
+      }
+      p.row_entropy[rrow] = p.Tk > 1 ? hrow / logf((float)p.Tk) : 0.f;
+    }
   }
 }
 
@@ -1214,7 +1263,7 @@ template <int DK, int DV, int YM, typename T>
 __global__ void __launch_bounds__(256) near_fix_kernel(const __grid_constant__ FwdParams p) {
   constexpr int QE = DK / 32;  // q and k components per lane
   constexpr int VE = DV / 32;  // v columns per lane
-  __shared__ float s_mass[8], s_top[8];
+  __shared__ float s_mass[8], s_top[8], s_slog[8];
   __shared__ float s_o[8][DV];
   const unsigned n = min(*p.near_count, p.near_cap);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1232,7 +1281,7 @@ __global__ void __launch_bounds__(256) near_fix_kernel(const __grid_constant__ F
     for (int i = 0; i < QE; ++i)
       qf[i] = elem_f(qg + ((size_t)bh * p.Tq + row) * DK + lane * QE + i);
     const int lim = p.causal ? min(row + 1, p.Tk) : p.Tk;
-    float mass = 0.f, top = 0.f, o[VE];
+    float mass = 0.f, top = 0.f, slog = 0.f, o[VE];  // slog: sum kappa ln kappa
 #pragma unroll
     for (int c = 0; c < VE; ++c) o[c] = 0.f;
     for (int j = warp; j < lim; j += 8) {
@@ -1257,6 +1306,7 @@ __global__ void __launch_bounds__(256) near_fix_kernel(const __grid_constant__ F
       const float kap = num / (fmaxf(d2, 0.f) + eps);
       mass += kap;
       top = fmaxf(top, kap);
+      if (kap > 0.f) slog = fmaf(kap, logf(kap), slog);
       const T *vr = vg + (bh_kv * p.Tk + j) * DV + lane * VE;
 #pragma unroll
       for (int c = 0; c < VE; ++c) o[c] = fmaf(kap, elem_f(vr + c), o[c]);
@@ -1264,16 +1314,18 @@ __global__ void __launch_bounds__(256) near_fix_kernel(const __grid_constant__ F
     if (lane == 0) {
       s_mass[warp] = mass;
       s_top[warp] = top;
+      s_slog[warp] = slog;
     }
 #pragma unroll
     for (int c = 0; c < VE; ++c) s_o[warp][lane * VE + c] = o[c];
     __syncthreads();
     if (warp == 0) {
-      float m_all = 0.f, t_all = 0.f;
+      float m_all = 0.f, t_all = 0.f, l_all = 0.f;
 #pragma unroll
       for (int w = 0; w < 8; ++w) {
         m_all += s_mass[w];
         t_all = fmaxf(t_all, s_top[w]);
+        l_all += s_slog[w];
       }
       const float inv = 1.f / (m_all + 1e-9f);
       const size_t ti = (size_t)bh * p.Tq + row;
@@ -1288,6 +1340,11 @@ __global__ void __launch_bounds__(256) near_fix_kernel(const __grid_constant__ F
       if (lane == 0) {
         if (p.row_mass) p.row_mass[ti] = m_all;
         if (p.row_max) p.row_max[ti] = t_all;
+        if (p.row_entropy) {  // -sum w ln w with w = kappa / (M + 1e-9)
+          const float z = m_all + 1e-9f;
+          const float hrow = (m_all * logf(z) - l_all) / z;
+          p.row_entropy[ti] = lim > 1 ? hrow / logf((float)lim) : 0.f;
+        }
       }
     }
     __syncthreads();
@@ -1310,11 +1367,11 @@ __global__ void tau_finalize_kernel(const double *moments, const float *eps, int
   }
 }
 
-template <int VARIANT, int DK, int DV, int YM = 1, bool STATS = false>
+template <int VARIANT, int DK, int DV, int YM = 1, bool STATS = false, bool ENT = false>
 cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                    const CUtensorMap &tv, cudaStream_t s) {
   using L = Layout<DK, DV>;
-  auto kern = fwd_kernel<VARIANT, DK, DV, YM, STATS>;
+  auto kern = fwd_kernel<VARIANT, DK, DV, YM, STATS, ENT>;
   static int configured_for = -1;
   static int sm_count = 0;
   int dev = 0;
@@ -1375,8 +1432,10 @@ bool fwd_tc_supported(int dk, int dv) {
 
 cudaError_t launch_fwd_tc(int variant, int dk, int dv, const FwdParams &p, const CUtensorMap &tq,
                           const CUtensorMap &tk, const CUtensorMap &tv, cudaStream_t s) {
-#define CATTN_TC_CASE(V, DK_, DV_) \
-  if (variant == V && dk == DK_ && dv == DV_) return tc::launch<V, DK_, DV_>(p, tq, tk, tv, s);
+#define CATTN_TC_CASE(V, DK_, DV_)                                                   \
+  if (variant == V && dk == DK_ && dv == DV_)                                        \
+    return p.row_entropy ? tc::launch<V, DK_, DV_, 1, false, true>(p, tq, tk, tv, s) \
+                         : tc::launch<V, DK_, DV_>(p, tq, tk, tv, s);
 #define CATTN_TC_YAT_M(DK_, DV_, M_)                            \
   if (variant == kYat && p.yat_m == M_ && dk == DK_ && dv == DV_) \
     return tc::launch<kYat, DK_, DV_, M_>(p, tq, tk, tv, s);
@@ -1396,9 +1455,9 @@ cudaError_t launch_fwd_tc(int variant, int dk, int dv, const FwdParams &p, const
   CATTN_TC_CASE(kStau, 64, 64)
   CATTN_TC_CASE(kStau, 128, 128)
   CATTN_TC_CASE(kStau, 128, 64)
-  CATTN_TC_CASE(kTau, 64, 64)
-  CATTN_TC_CASE(kTau, 128, 128)
 #undef CATTN_TC_CASE
+  if (variant == kTau && dk == 64 && dv == 64) return tc::launch<kTau, 64, 64>(p, tq, tk, tv, s);
+  if (variant == kTau && dk == 128 && dv == 128) return tc::launch<kTau, 128, 128>(p, tq, tk, tv, s);
   return cudaErrorInvalidValue;
 }
 

@@ -21,6 +21,7 @@ struct FwdParams {
   void *out;                    // [B, h, Tq, dv]
   int out_align32;              // out is 32-byte aligned (whole-sector stores)
   float *row_mass, *row_max;    // [B, h, Tq] or NULL
+  float *row_entropy;           // [B, h, Tq] normalised entropy of the map, or NULL (bf16, yat_m 1)
   const float *b, *eps, *tau;   // [h]
   int yat_m;                    // Yat numerator exponent 2 yat_m (1, 2 or 3)
   const float *nk;              // [B*hkv, Tk_pad]  squared k row norms (Yat, bf16), zero padded

@@ -102,24 +102,31 @@ __device__ __forceinline__ float yat_near_threshold(float nq, float b, int M) {
 
 // Masks, accumulates and packs one pair: masked keys (col >= limit) get
 // kappa = 0; mass (two chains) and top take kappa; returns P = bf16(kappa).
-template <bool PARTIAL>
-__device__ __forceinline__ uint32_t yat_fold(float2 k, int col, int limit, float2 &mass, float &top) {
+// ENT: ent also takes kappa log2 kappa (0 for kappa = 0), the row's
+// sum f log2 f for its entropy.
+template <bool PARTIAL, bool ENT = false>
+__device__ __forceinline__ uint32_t yat_fold(float2 k, int col, int limit, float2 &mass, float &top,
+                                             float2 &ent) {
   if (PARTIAL) {
     k.x = col < limit ? k.x : 0.f;
     k.y = col + 1 < limit ? k.y : 0.f;
   }
   mass = __fadd2_rn(mass, k);
   top = max3(top, k.x, k.y);
+  if (ENT) {
+    const float2 lk = make_float2(k.x > 0.f ? lg2_approx(k.x) : 0.f, k.y > 0.f ? lg2_approx(k.y) : 0.f);
+    ent = __ffma2_rn(k, lk, ent);
+  }
   return pack_bf16x2(k.x, k.y);
 }
 
 // Yat map over one 32-key chunk (columns 32c .. 32c+31 of the tile) of one row.  sr: raw
 // dots; nk4: squared key norms of the tile (groups of four).
-template <bool PARTIAL, bool FAST, int M = 1>
+template <bool PARTIAL, bool FAST, int M = 1, bool ENT = false>
 __device__ __forceinline__ void yat_chunk(const uint32_t (&sr)[32], int c, const float4 *nk4,
                                           float yb, float qe, float yeps, int limit,
                                           float2 (&mass)[2], float (&top)[2],
-                                          uint32_t (&pk)[16]) {
+                                          uint32_t (&pk)[16], float2 (&ent)[2]) {
   const float2 b2 = make_float2(yb, yb), qe2 = make_float2(qe, qe);
 #pragma unroll
   for (int i = 0; i < 32; i += 4) {
@@ -130,7 +137,7 @@ __device__ __forceinline__ void yat_chunk(const uint32_t (&sr)[32], int c, const
       const float2 k = yat_pair<FAST, M>(f2(sr[ii], sr[ii + 1]),
                                       h ? make_float2(n4.z, n4.w) : make_float2(n4.x, n4.y), b2, qe2,
                                       yeps);
-      pk[ii >> 1] = yat_fold<PARTIAL>(k, c * 32 + ii, limit, mass[h], top[h]);
+      pk[ii >> 1] = yat_fold<PARTIAL, ENT>(k, c * 32 + ii, limit, mass[h], top[h], ent[h]);
     }
   }
 }
@@ -153,10 +160,11 @@ __device__ __forceinline__ float chunk_max(const uint32_t (&sr)[32], int c, int 
 }
 
 // softmax over one 32-key chunk: p = 2^(dot * c2 - m), c2 = scale * log2(e).
-template <bool PARTIAL>
+// ENT: ent also takes p (dot c2 - m), the row's sum p log2 p (relative to m).
+template <bool PARTIAL, bool ENT = false>
 __device__ __forceinline__ void softmax_chunk(const uint32_t (&sr)[32], int c, float c2,
                                               float neg_m, int limit, float2 (&l)[2],
-                                              uint32_t (&pk)[16]) {
+                                              uint32_t (&pk)[16], float2 (&ent)[2]) {
   const float2 c22 = make_float2(c2, c2), nm2 = make_float2(neg_m, neg_m);
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {
@@ -168,6 +176,7 @@ __device__ __forceinline__ void softmax_chunk(const uint32_t (&sr)[32], int c, f
       pr.y = col + 1 < limit ? pr.y : 0.f;
     }
     l[(i >> 1) & 1] = __fadd2_rn(l[(i >> 1) & 1], pr);
+    if (ENT) ent[(i >> 1) & 1] = __ffma2_rn(pr, x, ent[(i >> 1) & 1]);
     pk[i >> 1] = pack_bf16x2(pr.x, pr.y);
   }
 }
@@ -220,10 +229,10 @@ __device__ __forceinline__ float2 log2_phi2(float2 d, float scale, float c2, flo
 }
 
 // s^tau over one 32-key chunk: p = 2^(tau log2 phi(s) - m).
-template <bool PARTIAL>
+template <bool PARTIAL, bool ENT = false>
 __device__ __forceinline__ void stau_chunk(const uint32_t (&sr)[32], int c, float scale, float c2,
                                            float tau, float eps, float neg_m, int limit,
-                                           float2 (&l)[2], uint32_t (&pk)[16]) {
+                                           float2 (&l)[2], uint32_t (&pk)[16], float2 (&ent)[2]) {
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {
     const int col = c * 32 + i;
@@ -235,6 +244,7 @@ __device__ __forceinline__ void stau_chunk(const uint32_t (&sr)[32], int c, floa
       pr.y = col + 1 < limit ? pr.y : 0.f;
     }
     l[(i >> 1) & 1] = __fadd2_rn(l[(i >> 1) & 1], pr);
+    if (ENT) ent[(i >> 1) & 1] = __ffma2_rn(pr, x, ent[(i >> 1) & 1]);
     pk[i >> 1] = pack_bf16x2(pr.x, pr.y);
   }
 }

@@ -27,7 +27,7 @@ ERR_SCRATCH_LIMIT = 6
 
 # every symbol include/cattn.h declares
 EXPORTS = ("cattn_version", "cattn_error_string", "cattn_workspace_bytes", "cattn_validate",
-           "cattn_key_norms", "cattn_forward", "cattn_forward_noalloc",
+           "cattn_key_norms", "cattn_forward", "cattn_forward_entropy", "cattn_forward_noalloc",
            "cattn_forward_host_workspace_bytes", "cattn_forward_host",
            "cattn_tau_star_workspace_bytes", "cattn_tau_star", "cattn_row_stats_workspace_bytes",
            "cattn_row_stats", "cattn_backward_workspace_bytes", "cattn_backward",
@@ -77,6 +77,8 @@ def load():
     lib.cattn_key_norms.restype = i
     lib.cattn_forward.argtypes = [i, pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.cattn_forward.restype = i
+    lib.cattn_forward_entropy.argtypes = [i, pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.cattn_forward_entropy.restype = i
     lib.cattn_forward_noalloc.argtypes = [i, pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.cattn_forward_noalloc.restype = i
     lib.cattn_forward_host_workspace_bytes.argtypes = [i, pp, i]

@@ -506,6 +506,54 @@ def test_row_stats_match_oracle(variant, shape):
     assert (np.abs(pu.to_np(small) - s_o) * n <= 2.0 + 1e-9).all()
 
 
+ENT_SHAPES = [  # B, h, hkv, T_q, T_k, d, causal
+    (2, 4, 2, 300, 300, 128, True),
+    (1, 2, 1, 130, 130, 64, True),
+    (1, 2, 2, 200, 2100, 128, False),   # two key splits: the entropy sums merge in the combine
+]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("shape", ENT_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_forward_entropy_matches_oracle(variant, shape):
+    """The forward's online entropy (sum f log2 f kept beside the normaliser,
+    moved onto each new running max) against the oracle's per-row normalised
+    entropy, at the row statistics pass's 2e-3 absolute; out and telemetry of
+    the same call against the oracle as usual."""
+    import oracle
+    B, h, hkv, Tq, Tk, d, causal = shape
+    w = _wl("ent", B, h, hkv, Tq, Tk, d, d, causal=causal, qk=2.0, seed=Tq + 9)
+    inp = workloads.generate(w)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    kw = pu.params_for(variant, inp)
+    out, mass, mx, ent = attention.forward_entropy(variant, q, k, v, causal=causal, scale=w.scale,
+                                                   **kw)
+    torch.cuda.synchronize()
+    assert attention.check_status() == 0
+    e_o, _, _ = oracle.row_stats(variant, inp["q"], inp["k"], inp["v"], causal=causal,
+                                 scale=w.scale, **kw)
+    np.testing.assert_allclose(pu.to_np(ent), e_o, atol=2e-3)
+    ora = pu.run_oracle(variant, inp, causal=causal, scale=w.scale)
+    pu.compare(variant, (pu.to_np(out), pu.to_np(mass), pu.to_np(mx)), ora,
+               float(inp["v"].abs().max()), q.dtype, where=f"entropy forward {variant} {shape}")
+
+
+def test_forward_entropy_on_near_keys():
+    """Rows recomputed by the Yat near-key pass carry their entropy too."""
+    import oracle
+    w = _wl("ent_tied", 1, 2, 2, 300, 300, 64, 64, causal=True, qk=16.0, seed=31)
+    inp = workloads.generate(w)
+    inp["k"] = inp["q"].clone()
+    inp["yat_b"] = np.array([0.3, 2.0], dtype=np.float32)
+    inp["yat_eps"] = np.full(2, 0.05, dtype=np.float32)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    kw = pu.params_for("yat", inp)
+    _, _, _, ent = attention.forward_entropy("yat", q, k, v, causal=True, **kw)
+    torch.cuda.synchronize()
+    e_o, _, _ = oracle.row_stats("yat", inp["q"], inp["k"], inp["v"], causal=True, **kw)
+    np.testing.assert_allclose(pu.to_np(ent), e_o, atol=2e-3)
+
+
 # ---------------------------------------------------------------- every width pair
 
 WIDTH_SHAPES = [  # dtype, B, h, hkv, Tq, Tk, dk, dv, causal: widths without tensor-core tiles
