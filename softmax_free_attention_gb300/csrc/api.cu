@@ -182,36 +182,73 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// fp32 [outer, rows, inner] as a 3-D tensor map with boxes of 32 x box_rows x 1
-// (128-byte rows) and 128-byte swizzle.  Reads past the extents are zeros.
-int encode_f32_3d(CUtensorMap *map, const void *base, int inner, int rows, int outer,
-                  int box_rows) {
+// A 3-D tiled tensor map [outer, rows, inner] of 2- or 4-byte elements with
+// boxes of (128 bytes of inner) x box_rows x 1 and 128-byte swizzle (the
+// shared-memory layout the tcgen05 descriptors describe); reads past the
+// extents are zeros.  Encoded maps are kept in a small cache keyed by (base
+// address, element size, extents, box rows): a map holds nothing but those
+// values, so an entry stays valid for any buffer later found at the same
+// address with the same shape, and repeated calls on the same tensors skip
+// the driver's encode.
+struct MapKey {
+  uintptr_t base;
+  int esize, inner, rows, outer, box_rows;
+  bool operator==(const MapKey &o) const {
+    return base == o.base && esize == o.esize && inner == o.inner && rows == o.rows &&
+           outer == o.outer && box_rows == o.box_rows;
+  }
+};
+constexpr int kMapCache = 64;
+struct MapCache {
+  std::mutex mu;
+  MapKey key[kMapCache];
+  CUtensorMap map[kMapCache];
+  int used = 0, next = 0;
+};
+MapCache &map_cache() {
+  static MapCache c;
+  return c;
+}
+
+int encode_3d(CUtensorMap *map, const void *base, int esize, int inner, int rows, int outer,
+              int box_rows) {
+  const MapKey k{reinterpret_cast<uintptr_t>(base), esize, inner, rows, outer, box_rows};
+  MapCache &c = map_cache();
+  {
+    std::lock_guard<std::mutex> lock(c.mu);
+    for (int i = 0; i < c.used; ++i)
+      if (c.key[i] == k) {
+        *map = c.map[i];
+        return CATTN_OK;
+      }
+  }
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return CATTN_ERR_CUDA;
   cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)outer};
-  cuuint64_t strides[2] = {(cuuint64_t)inner * 4, (cuuint64_t)rows * inner * 4};
-  cuuint32_t box[3] = {32, (cuuint32_t)box_rows, 1};
+  cuuint64_t strides[2] = {(cuuint64_t)inner * esize, (cuuint64_t)rows * inner * esize};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / esize), (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(map, esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                  3, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? CATTN_OK : CATTN_ERR_CUDA;
+  if (r != CUDA_SUCCESS) return CATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(c.mu);
+  const int slot = c.used < kMapCache ? c.used++ : (c.next++ % kMapCache);
+  c.key[slot] = k;
+  c.map[slot] = *map;
+  return CATTN_OK;
 }
 
-// bf16 [BH, T, d] as a 3-D tensor map with 64 x box_rows x 1 boxes and 128-byte
-// swizzle (the shared-memory layout the tcgen05 descriptors describe).  Rows
-// past T read as zeros.
+// fp32 [outer, rows, inner] with boxes of 32 x box_rows x 1 (128-byte rows).
+int encode_f32_3d(CUtensorMap *map, const void *base, int inner, int rows, int outer,
+                  int box_rows) {
+  return encode_3d(map, base, 4, inner, rows, outer, box_rows);
+}
+
+// bf16 [BH, T, d] with boxes of 64 x box_rows x 1.  Rows past T read as zeros.
 int encode_bf16_3d(CUtensorMap *map, const void *base, int d, int T, int BH, int box_rows) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (!fn) return CATTN_ERR_CUDA;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)T, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)T * d * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? CATTN_OK : CATTN_ERR_CUDA;
+  return encode_3d(map, base, 2, d, T, BH, box_rows);
 }
 
 }  // namespace
@@ -384,9 +421,14 @@ int forward_impl(int variant, const cattn_problem_t *p, const void *q, const voi
   if ((rc = encode_bf16_3d(&tk, k, p->dk, p->Tk, p->B * p->hkv, kTcKeyTile)) != CATTN_OK) return rc;
   if ((rc = encode_bf16_3d(&tv, v, p->dv, p->Tk, p->B * p->hkv, kTcKeyTile)) != CATTN_OK) return rc;
   // the ticket and the near-key count start at zero, and so does the largest
-  // key norm when this call takes the norms itself (one memset for all three)
+  // key norm when this call takes the norms itself (one memset for all
+  // three); softmax and s^tau with no more units than CTAs read none of them
   const bool own_norms = variant == CATTN_YAT && !(p->flags & CATTN_FLAG_NORMS_READY);
-  if ((rc = map_cuda(cudaMemsetAsync(ws + w.ctrl, 0, (own_norms ? 3 : 2) * sizeof(unsigned int),
+  const int grid = tc_grid_size(w.sched.n_units);
+  if (grid < 0) return CATTN_ERR_CUDA;
+  const bool ticket = w.sched.n_units > grid;
+  if ((variant == CATTN_YAT || ticket) &&
+      (rc = map_cuda(cudaMemsetAsync(ws + w.ctrl, 0, (own_norms ? 3 : 2) * sizeof(unsigned int),
                                      s))) != CATTN_OK)
     return rc;
   if (own_norms &&

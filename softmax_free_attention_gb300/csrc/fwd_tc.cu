@@ -500,7 +500,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
         kv_pos += STEP * t.nkv;
         nk_pos += t.nkv;
-        u = (int)atomicAdd(p.tile_counter, 1u) + (int)gridDim.x;
+        // with no more units than CTAs every unit was handed out at launch
+        // and the ticket is never read (nor needs zeroing)
+        u = p.n_units <= (int)gridDim.x ? p.n_units
+                                        : (int)atomicAdd(p.tile_counter, 1u) + (int)gridDim.x;
       }
       {
         // every copy this lane started lands in shared memory before the CTA
@@ -1424,6 +1427,19 @@ TcSchedule tc_schedule(int B, int h, int Tq, int Tk, int causal) {
   s.n_splits = s.n_kv_tiles > 0 ? (s.n_kv_tiles + s.kv_per_split - 1) / s.kv_per_split : 1;
   s.n_units = pairs * s.n_splits;
   return s;
+}
+
+int tc_grid_size(long long n_units) {
+  constexpr int kMaxDev = 64;
+  static int sms[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return -1;
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    sms[dev] = n;
+  }
+  return n_units < sms[dev] ? (int)n_units : sms[dev];
 }
 
 bool fwd_tc_supported(int dk, int dv) {

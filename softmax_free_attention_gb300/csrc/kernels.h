@@ -72,6 +72,9 @@ TcSchedule tc_schedule(int B, int h, int Tq, int Tk, int causal);
 cudaError_t launch_fwd_tc(int variant, int dk, int dv, const FwdParams &p, const CUtensorMap &tq,
                           const CUtensorMap &tk, const CUtensorMap &tv, cudaStream_t s);
 bool fwd_tc_supported(int dk, int dv);
+// CTAs the persistent forward launches for n_units units (one per SM at
+// most), -1 if the device cannot be queried.
+int tc_grid_size(long long n_units);
 
 // The row statistics pass: the map's S and weights again (no V), per-row
 // normalised entropy, fraction below 1e-6 and top-10 mass.  dk 64 or 128.
