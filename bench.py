@@ -567,6 +567,32 @@ def main():
     per_variant["tau_star"] = {"kernel_ms": tau_ms, "qk_tflops": qk_flops / (tau_ms * 1e-3) / 1e12,
                                "scores_per_s": qk_flops / (2 * w.dk) / (tau_ms * 1e-3)}
 
+    # ---- the map's row statistics on the same inputs: the second pass
+    # (cattn_row_stats: entropy, fraction below 1e-6, top-10 mass) and the
+    # forward with the entropy accumulated online (cattn_forward_entropy)
+    for variant in ("yat", "softmax", "stau"):
+        kw = {"yat": dict(b=yb, eps=ye), "softmax": {}, "stau": dict(eps=se, tau=tau)}[variant]
+        _, m_s, _ = attention.forward(variant, q, k, v, causal=w.causal, scale=w.scale, **kw)
+        need = attention.workspace_bytes(variant, prob)
+        ws_v = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+        f_stats = lambda: attention.row_stats(variant, q, k, m_s, causal=w.causal, scale=w.scale,
+                                              **kw)
+        f_ent = lambda: attention.forward_entropy(variant, q, k, v, causal=w.causal, scale=w.scale,
+                                                  workspace=ws_v, **kw)
+        for name, f in (("row_stats_ms", f_stats), ("forward_entropy_ms", f_ent)):
+            for _ in range(3):
+                f()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(max(3, args.steps // 2)):
+                f()
+            b.record()
+            torch.cuda.synchronize()
+            per_variant[variant][name] = a.elapsed_time(b) / max(3, args.steps // 2)
+        del m_s, ws_v
+    assert attention.check_status() == 0
+
     # ---- backward of each map on the same inputs (not part of the step above):
     # the row-sum pass (Yat, s^tau), the dK/dV pass and the dQ pass; FLOPs
     # counted as 2.5 forward passes (the five products S, dP, dV, dK, dQ)
