@@ -60,6 +60,8 @@
 // leave their loops so that TMEM is still released.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "kernels.h"
 #include "maps.cuh"
 #include "ptx.cuh"
@@ -707,23 +709,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       // tau*: this thread's partial sums of 1, s, g, s g, g^2 over the unit
       float st[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
-      // row statistics: this thread's share of the row, and the row's
-      // normaliser from the forward (Yat: 1 / (M + 1e-9) and ln(M + 1e-9);
-      // softmax / s^tau: the log-sum-exp in log2 units)
+      // row statistics: this thread's share of the row, the row's normaliser
+      // from the forward (Yat: 1 / Z' and ln Z', Z' = M + 1e-9; softmax /
+      // s^tau: the log-sum-exp in log2 units) and the threshold of the count
+      // below 1e-6 in the accumulated domain (Yat 1e-6 Z', else log2 1e-6)
       RowStats rs;
-      float nz_scale = 0.f, nz_log = 0.f;
+      float nz_scale = 0.f, nz_log = 0.f, small_thr = 0.f;
       if constexpr (STATS) {
-        rs.n = rs.hsum = rs.small = 0.f;
+        rs.hs = rs.sk = make_float2(0.f, 0.f);
+        rs.small = 0.f;
 #pragma unroll
-        for (int i = 0; i < 10; ++i) rs.top[i] = 0.f;
+        for (int i = 0; i < 10; ++i) rs.top[i] = VARIANT == kYat ? 0.f : -INFINITY;
         const Unit t = decode_unit(p, u);
         const int row = t.q0 + x * BM + r;
         const float z = row < p.Tq ? p.norm_in[(size_t)t.bh * p.Tq + row] : 0.f;
         if (VARIANT == kYat) {
           nz_scale = 1.f / (z + 1e-9f);
           nz_log = logf(z + 1e-9f);
+          small_thr = 1e-6f * (z + 1e-9f);
         } else {
           nz_log = z * LOG2E;
+          small_thr = -19.931568569324174f;  // log2(1e-6)
         }
         if (row >= p.Tq) lim_base = 0;  // rows past Tq have no keys
       }
@@ -802,68 +808,71 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           continue;
         }
         if constexpr (STATS) {
-          // the row statistics: the map's weights w of the allowed keys, one
-          // 32-key chunk at a time
+          // the row statistics over the allowed keys, one 32-key chunk at a
+          // time; tiles with no masked key take the unmasked path
           const float4 *nk4 = nullptr;
           if (VARIANT == kYat) {
             const uint32_t npos = nk_pos + j, ns = npos % NKS;
             if (!(ok = warp_wait(nk_full(ns), (npos / NKS) & 1u, abort, SITE_EPI | 0x20))) break;
             nk4 = reinterpret_cast<const float4 *>(nk_ring + ns * BN);
           }
+          auto stats_tile = [&](auto partial_tag) {
+            constexpr bool PARTIAL = decltype(partial_tag)::value;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int cc = half * 2 + c;
-            uint32_t sr1[32];
-            tmem_ld32(t_s + 32 * c, sr1);
-            tmem_wait_ld();
-            tmem_ld_fence(sr1);
+            for (int c = 0; c < 2; ++c) {
+              const int cc = half * 2 + c;
+              uint32_t sr1[32];
+              tmem_ld32(t_s + 32 * c, sr1);
+              tmem_wait_ld();
+              tmem_ld_fence(sr1);
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const int col = cc * 32 + i;
-              float w0, w1, l0, l1;
-              if (VARIANT == kYat) {
-                const float4 n4 = nk4[(cc * 32 + i) >> 2];
-                const float2 kk = fast ? yat_pair<true, YM>(f2(sr1[i], sr1[i + 1]),
-                                                            (i & 2) ? make_float2(n4.z, n4.w)
-                                                                    : make_float2(n4.x, n4.y),
-                                                            make_float2(yb, yb), make_float2(qe, qe),
-                                                            yeps)
-                                       : yat_pair<false, YM>(f2(sr1[i], sr1[i + 1]),
-                                                             (i & 2) ? make_float2(n4.z, n4.w)
-                                                                     : make_float2(n4.x, n4.y),
-                                                             make_float2(yb, yb), make_float2(qe, qe),
-                                                             yeps);
-                float k0 = kk.x, k1 = kk.y;
-                // the guard against a cancelled distance, key by key (allowed
-                // keys only: the others may lie past the end of k)
-                const uint4 *kt4 = st_k4 + (size_t)j * BN * (DK / 8);
-                if (col < limit && k0 > st_thr)
-                  k0 = yat_direct_call<DK, YM>(st_q4, kt4 + (size_t)col * (DK / 8), yb, yeps);
-                if (col + 1 < limit && k1 > st_thr)
-                  k1 = yat_direct_call<DK, YM>(st_q4, kt4 + (size_t)(col + 1) * (DK / 8), yb, yeps);
-                w0 = k0 * nz_scale;
-                w1 = k1 * nz_scale;
-                l0 = lg2_approx(k0) * LN2 - nz_log;
-                l1 = lg2_approx(k1) * LN2 - nz_log;
-              } else {
-                const float d0 = __uint_as_float(sr1[i]), d1 = __uint_as_float(sr1[i + 1]);
-                float x0, x1;  // log2 of the weights
-                if (VARIANT == kSoftmax) {
-                  x0 = fmaf(d0, c2, -nz_log);
-                  x1 = fmaf(d1, c2, -nz_log);
+              for (int i = 0; i < 32; i += 2) {
+                const int col = cc * 32 + i;
+                const bool al0 = !PARTIAL || col < limit, al1 = !PARTIAL || col + 1 < limit;
+                if (VARIANT == kYat) {
+                  const float4 n4 = nk4[(cc * 32 + i) >> 2];
+                  const float2 nk2 = (i & 2) ? make_float2(n4.z, n4.w) : make_float2(n4.x, n4.y);
+                  const float2 kk =
+                      fast ? yat_pair<true, YM>(f2(sr1[i], sr1[i + 1]), nk2, make_float2(yb, yb),
+                                                make_float2(qe, qe), yeps)
+                           : yat_pair<false, YM>(f2(sr1[i], sr1[i + 1]), nk2, make_float2(yb, yb),
+                                                 make_float2(qe, qe), yeps);
+                  float k0 = kk.x, k1 = kk.y;
+                  // the guard against a cancelled distance, key by key (allowed
+                  // keys only: the others may lie past the end of k)
+                  const uint4 *kt4 = st_k4 + (size_t)j * BN * (DK / 8);
+                  if (al0 && k0 > st_thr)
+                    k0 = yat_direct_call<DK, YM>(st_q4, kt4 + (size_t)col * (DK / 8), yb, yeps);
+                  if (al1 && k1 > st_thr)
+                    k1 = yat_direct_call<DK, YM>(st_q4, kt4 + (size_t)(col + 1) * (DK / 8), yb, yeps);
+                  if (PARTIAL) {
+                    k0 = al0 ? k0 : 0.f;
+                    k1 = al1 ? k1 : 0.f;
+                  }
+                  stats_pair_yat<PARTIAL>(rs, make_float2(k0, k1), small_thr, al0, al1);
                 } else {
-                  x0 = fmaf(tau, log2_phi(d0 * p.scale, fabsf(d0) * c2, seps), -nz_log);
-                  x1 = fmaf(tau, log2_phi(d1 * p.scale, fabsf(d1) * c2, seps), -nz_log);
+                  const float d0 = __uint_as_float(sr1[i]), d1 = __uint_as_float(sr1[i + 1]);
+                  float x0, x1;  // log2 of the weights
+                  if (VARIANT == kSoftmax) {
+                    x0 = fmaf(d0, c2, -nz_log);
+                    x1 = fmaf(d1, c2, -nz_log);
+                  } else {
+                    x0 = fmaf(tau, log2_phi(d0 * p.scale, fabsf(d0) * c2, seps), -nz_log);
+                    x1 = fmaf(tau, log2_phi(d1 * p.scale, fabsf(d1) * c2, seps), -nz_log);
+                  }
+                  if (PARTIAL) {
+                    x0 = al0 ? x0 : -1e30f;
+                    x1 = al1 ? x1 : -1e30f;
+                  }
+                  stats_pair_log<PARTIAL>(rs, make_float2(x0, x1), small_thr, al0, al1);
                 }
-                w0 = ex2_approx(x0);
-                w1 = ex2_approx(x1);
-                l0 = x0 * LN2;
-                l1 = x1 * LN2;
               }
-              stats_add(rs, w0, l0, col < limit);
-              stats_add(rs, w1, l1, col + 1 < limit);
             }
-          }
+          };
+          if (partial)
+            stats_tile(std::true_type{});
+          else
+            stats_tile(std::false_type{});
           // S (and, for Yat, the tile's key norms) read: S(j+1) may land
           tc_fence_before();
           mbar_arrive(p_full(x));
@@ -1012,16 +1021,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // half 0 through shared memory, half 0 writes the row's statistics
           float *sx = xchg + (uint32_t)x * BM;  // [13 values][2 tiles][BM]
           if (half == 1) {
-            sx[(0 * 2) * BM + r] = rs.n;
-            sx[(1 * 2) * BM + r] = rs.hsum;
+            sx[(0 * 2) * BM + r] = rs.hs.x + rs.hs.y;
+            sx[(1 * 2) * BM + r] = rs.sk.x + rs.sk.y;
             sx[(2 * 2) * BM + r] = rs.small;
 #pragma unroll
             for (int i = 0; i < 10; ++i) sx[((3 + i) * 2) * BM + r] = rs.top[i];
           }
           named_barrier_sync(named_bar, 64);
           if (half == 0) {
-            rs.n += sx[(0 * 2) * BM + r];
-            rs.hsum += sx[(1 * 2) * BM + r];
+            const float hs = (rs.hs.x + rs.hs.y) + sx[(0 * 2) * BM + r];
+            const float sk = (rs.sk.x + rs.sk.y) + sx[(1 * 2) * BM + r];
             rs.small += sx[(2 * 2) * BM + r];
 #pragma unroll
             for (int i = 0; i < 10; ++i) {
@@ -1037,11 +1046,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int row = t.q0 + x * BM + r;
             if (row < p.Tq) {
               const size_t ti = (size_t)t.bh * p.Tq + row;
+              // the row's allowed keys
+              const float n = (float)(p.causal ? min(row + 1, p.Tk) : p.Tk);
               float top10 = 0.f;
 #pragma unroll
-              for (int i = 0; i < 10; ++i) top10 += rs.top[i];
-              if (p.st_entropy) p.st_entropy[ti] = rs.n > 1.f ? -rs.hsum / logf(rs.n) : 0.f;
-              if (p.st_small) p.st_small[ti] = rs.small / rs.n;
+              for (int i = 0; i < 10; ++i) top10 += VARIANT == kYat ? rs.top[i] : ex2_approx(rs.top[i]);
+              // sum w ln w over the row
+              const float hsum = VARIANT == kYat ? nz_scale * (LN2 * hs - nz_log * sk) : LN2 * hs;
+              if (VARIANT == kYat) top10 *= nz_scale;
+              if (p.st_entropy) p.st_entropy[ti] = n > 1.f ? -hsum / logf(n) : 0.f;
+              if (p.st_small) p.st_small[ti] = rs.small / n;
               if (p.st_top10) p.st_top10[ti] = top10;
             }
           }

@@ -289,32 +289,56 @@ __device__ __forceinline__ void tau_chunk(const uint32_t (&sr)[32], int c, float
 
 // Row statistics of the map over one thread's keys (normalised entropy: "The
 // Kernel Between the Roles", section "The run"; sparsity below 1e-6 and top-10
-// concentration: the s^tau page's fine-tuning comparison): the number of
-// allowed keys, sum w ln w, the count of weights below 1e-6, and the ten
-// largest weights in descending order.
+// concentration: the s^tau page's fine-tuning comparison), kept on the map's
+// unnormalised values so that the row's normaliser is applied once at the
+// end.  Yat takes kappa: hs = sum kappa log2 kappa and sk = sum kappa, so that
+// sum w ln w = (ln 2 hs - ln Z' sk) / Z' with w = kappa / Z'; softmax and s^tau
+// take x = log2 w: hs = sum 2^x x, so that sum w ln w = ln 2 hs.  small counts
+// the allowed keys under the row's threshold (Yat 1e-6 Z', else log2 1e-6);
+// top holds the ten largest kappa (or x), in descending order.
 struct RowStats {
-  float n, hsum, small;
+  float2 hs, sk;
+  float small;
   float top[10];
 };
 
-// Adds one key's weight w (ln w = lnw) if it is allowed.  The top-10 insert is
-// a bubble through the sorted list, taken only when some lane of the warp has
-// a weight above its tenth largest.
-__device__ __forceinline__ void stats_add(RowStats &st, float w, float lnw, bool allowed) {
-  if (allowed) {
-    st.n += 1.f;
-    st.hsum += w > 0.f ? w * lnw : 0.f;
-    st.small += w < 1e-6f ? 1.f : 0.f;
-  }
-  float v = allowed ? w : 0.f;
-  if (__any_sync(0xffffffffu, v > st.top[9])) {
+// The top-10 insert is a bubble through the sorted list, taken only when some
+// lane of the warp has a value above its tenth largest.
+__device__ __forceinline__ void top10_insert(float (&top)[10], float v) {
+  if (__any_sync(0xffffffffu, v > top[9])) {
 #pragma unroll
     for (int i = 0; i < 10; ++i) {
-      const float hi = fmaxf(st.top[i], v);
-      v = fminf(st.top[i], v);
-      st.top[i] = hi;
+      const float hi = fmaxf(top[i], v);
+      v = fminf(top[i], v);
+      top[i] = hi;
     }
   }
+}
+
+// Two keys of the Yat map: kappa (0 for keys that are not allowed; al0 / al1
+// tell them apart for the count when PARTIAL).
+template <bool PARTIAL>
+__device__ __forceinline__ void stats_pair_yat(RowStats &st, float2 k, float thr, bool al0, bool al1) {
+  // kappa log2 kappa is 0 for kappa = 0 (the clamp keeps the log finite)
+  const float2 lk = make_float2(lg2_approx(fmaxf(k.x, 1e-30f)), lg2_approx(fmaxf(k.y, 1e-30f)));
+  st.hs = __ffma2_rn(k, lk, st.hs);
+  st.sk = __fadd2_rn(st.sk, k);
+  st.small += ((!PARTIAL || al0) && k.x < thr) ? 1.f : 0.f;
+  st.small += ((!PARTIAL || al1) && k.y < thr) ? 1.f : 0.f;
+  top10_insert(st.top, k.x);
+  top10_insert(st.top, k.y);
+}
+
+// Two keys of softmax or s^tau: x = log2 of the weight (a large negative
+// finite value for keys that are not allowed, so that 2^x x is 0).
+template <bool PARTIAL>
+__device__ __forceinline__ void stats_pair_log(RowStats &st, float2 x, float thr, bool al0, bool al1) {
+  const float2 w = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+  st.hs = __ffma2_rn(w, x, st.hs);
+  st.small += ((!PARTIAL || al0) && x.x < thr) ? 1.f : 0.f;
+  st.small += ((!PARTIAL || al1) && x.y < thr) ? 1.f : 0.f;
+  top10_insert(st.top, x.x);
+  top10_insert(st.top, x.y);
 }
 
 }  // namespace tc
