@@ -5,11 +5,30 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <atomic>
+#include <chrono>
 #include <mutex>
 
 #include "cattn.h"
 #include "bwd.h"
 #include "kernels.h"
+
+namespace cattn {
+
+// Generations of the key-norm maximum: distinct over the process's calls
+// (a word whose generation differs from the call's is replaced, whatever its
+// value), never 0, and seeded with the seconds since the epoch so that a
+// workspace another process used is unlikely to hold the current one.
+unsigned int next_norm_generation() {
+  static std::atomic<unsigned int> g{(unsigned int)std::chrono::duration_cast<std::chrono::seconds>(
+                                         std::chrono::system_clock::now().time_since_epoch())
+                                         .count()};
+  unsigned int v = g.fetch_add(1u) + 1u;
+  while (v == 0u) v = g.fetch_add(1u) + 1u;
+  return v;
+}
+
+}  // namespace cattn
 
 namespace {
 
@@ -50,7 +69,8 @@ struct WsLayout {
   TcSchedule sched;
 };
 
-// the control block's words
+// the control block's words: the unit ticket, the near-key count, and (a
+// 64-bit word at byte 8) the largest key norm with its generation
 constexpr int kCtrlTicket = 0, kCtrlNearCount = 1, kCtrlNkMax = 2;
 
 // Workspace of the fp32 path, each part 256-byte aligned: the control block
@@ -310,11 +330,10 @@ int cattn_key_norms(const cattn_problem_t *p, const void *k, void *workspace,
   if (rc != CATTN_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   float *nk = reinterpret_cast<float *>(static_cast<char *>(workspace) + w.nk);
-  unsigned int *nk_max =
-      reinterpret_cast<unsigned int *>(static_cast<char *>(workspace) + w.ctrl) + kCtrlNkMax;
-  if ((rc = map_cuda(cudaMemsetAsync(nk_max, 0, sizeof(unsigned int), s))) != CATTN_OK) return rc;
-  return map_cuda(
-      launch_row_sqnorm_bf16(k, nk, p->B * p->hkv, p->Tk, tk_pad(p), p->dk, nk_max, s));
+  unsigned long long *nk_max = reinterpret_cast<unsigned long long *>(
+      reinterpret_cast<unsigned int *>(static_cast<char *>(workspace) + w.ctrl) + kCtrlNkMax);
+  return map_cuda(launch_row_sqnorm_bf16(k, nk, p->B * p->hkv, p->Tk, tk_pad(p), p->dk, nk_max,
+                                         next_norm_generation(), nullptr, 0, s));
 }
 
 }  // extern "C"
@@ -409,9 +428,14 @@ int forward_impl(int variant, const cattn_problem_t *p, const void *q, const voi
     fp.part_o = reinterpret_cast<float *>(ws + w.part_o);
     fp.part_stat = reinterpret_cast<float *>(ws + w.part_stat);
   }
+  // the forward takes the key norms itself unless the caller marked them ready
+  const bool own_norms = variant == CATTN_YAT && !(p->flags & CATTN_FLAG_NORMS_READY);
+  unsigned int *ctrl = reinterpret_cast<unsigned int *>(ws + w.ctrl);
+  const unsigned int gen = own_norms ? next_norm_generation() : 0u;
   if (variant == CATTN_YAT) {
     fp.nk = reinterpret_cast<const float *>(ws + w.nk);
-    fp.nk_max = reinterpret_cast<const unsigned int *>(ws + w.ctrl) + kCtrlNkMax;
+    fp.nk_max = reinterpret_cast<const unsigned long long *>(ctrl + kCtrlNkMax);
+    fp.nk_gen = gen;
     fp.near_count = reinterpret_cast<unsigned int *>(ws + w.ctrl) + kCtrlNearCount;
     fp.near_rows = reinterpret_cast<uint2 *>(ws + w.near);
     fp.near_cap = (unsigned int)(w.near_cap < 0xffffffffu ? w.near_cap : 0xffffffffu);
@@ -420,24 +444,23 @@ int forward_impl(int variant, const cattn_problem_t *p, const void *q, const voi
   if ((rc = encode_bf16_3d(&tq, q, p->dk, p->Tq, p->B * p->h, kTcQueryTile)) != CATTN_OK) return rc;
   if ((rc = encode_bf16_3d(&tk, k, p->dk, p->Tk, p->B * p->hkv, kTcKeyTile)) != CATTN_OK) return rc;
   if ((rc = encode_bf16_3d(&tv, v, p->dv, p->Tk, p->B * p->hkv, kTcKeyTile)) != CATTN_OK) return rc;
-  // the ticket and the near-key count start at zero, and so does the largest
-  // key norm when this call takes the norms itself (one memset for all
-  // three); softmax and s^tau with no more units than CTAs read none of them
-  const bool own_norms = variant == CATTN_YAT && !(p->flags & CATTN_FLAG_NORMS_READY);
+  // the unit ticket and the near-key count start at zero: the key-norm
+  // kernel zeroes them when this call takes the norms (its maximum carries
+  // this call's generation and needs no zeroing), a memset otherwise;
+  // softmax and s^tau with no more units than CTAs read neither
   const int grid = tc_grid_size(w.sched.n_units);
   if (grid < 0) return CATTN_ERR_CUDA;
   const bool ticket = w.sched.n_units > grid;
-  if ((variant == CATTN_YAT || ticket) &&
-      (rc = map_cuda(cudaMemsetAsync(ws + w.ctrl, 0, (own_norms ? 3 : 2) * sizeof(unsigned int),
-                                     s))) != CATTN_OK)
+  if (own_norms) {
+    if ((rc = map_cuda(launch_row_sqnorm_bf16(
+             k, reinterpret_cast<float *>(ws + w.nk), p->B * p->hkv, p->Tk, tk_pad(p), p->dk,
+             reinterpret_cast<unsigned long long *>(ctrl + kCtrlNkMax), gen, ctrl, 2, s))) !=
+        CATTN_OK)
+      return rc;
+  } else if ((variant == CATTN_YAT || ticket) &&
+             (rc = map_cuda(cudaMemsetAsync(ctrl, 0, 2 * sizeof(unsigned int), s))) != CATTN_OK) {
     return rc;
-  if (own_norms &&
-      (rc = map_cuda(launch_row_sqnorm_bf16(k, reinterpret_cast<float *>(ws + w.nk), p->B * p->hkv,
-                                            p->Tk, tk_pad(p), p->dk,
-                                            reinterpret_cast<unsigned int *>(ws + w.ctrl) +
-                                                kCtrlNkMax,
-                                            s))) != CATTN_OK)
-    return rc;
+  }
   return map_cuda(launch_fwd_tc(variant, p->dk, p->dv, fp, tq, tk, tv, s));
 }
 
@@ -601,21 +624,24 @@ int cattn_row_stats(int variant, const cattn_problem_t *p, const void *q, const 
   fp.st_entropy = entropy;
   fp.st_small = frac_small;
   fp.st_top10 = top10;
-  if (variant == CATTN_YAT) {
-    fp.nk = reinterpret_cast<const float *>(ws + 256);
-    fp.nk_max = reinterpret_cast<const unsigned int *>(ws) + 1;
-    // the key norms and their maximum into this workspace
-    unsigned int *nk_max = reinterpret_cast<unsigned int *>(ws) + 1;
-    if ((rc = map_cuda(cudaMemsetAsync(nk_max, 0, sizeof(unsigned int), s))) != CATTN_OK) return rc;
-    if ((rc = map_cuda(launch_row_sqnorm_bf16(k, reinterpret_cast<float *>(ws + 256), tp.B * tp.hkv,
-                                              tp.Tk, tk_pad(&tp), tp.dk, nk_max, s))) != CATTN_OK)
-      return rc;
-  }
   CUtensorMap tq, tk;
   if ((rc = encode_bf16_3d(&tq, q, tp.dk, tp.Tq, tp.B * tp.h, kTcQueryTile)) != CATTN_OK) return rc;
   if ((rc = encode_bf16_3d(&tk, k, tp.dk, tp.Tk, tp.B * tp.hkv, kTcKeyTile)) != CATTN_OK) return rc;
-  if ((rc = map_cuda(cudaMemsetAsync(fp.tile_counter, 0, sizeof(unsigned int), s))) != CATTN_OK)
+  if (variant == CATTN_YAT) {
+    // the key norms and their maximum (64-bit word at byte 8, this call's
+    // generation) into this workspace; the norm kernel zeroes the ticket
+    fp.nk = reinterpret_cast<const float *>(ws + 256);
+    unsigned long long *nk_max = reinterpret_cast<unsigned long long *>(ws + 8);
+    fp.nk_max = nk_max;
+    fp.nk_gen = next_norm_generation();
+    if ((rc = map_cuda(launch_row_sqnorm_bf16(k, reinterpret_cast<float *>(ws + 256), tp.B * tp.hkv,
+                                              tp.Tk, tk_pad(&tp), tp.dk, nk_max, fp.nk_gen,
+                                              fp.tile_counter, 1, s))) != CATTN_OK)
+      return rc;
+  } else if ((rc = map_cuda(cudaMemsetAsync(fp.tile_counter, 0, sizeof(unsigned int), s))) !=
+             CATTN_OK) {
     return rc;
+  }
   return map_cuda(launch_row_stats_tc(variant, tp.dk, fp, tq, tk, s));
 }
 
@@ -644,7 +670,7 @@ BwdWs bwd_ws(int variant, const cattn_problem_t *p) {
   memset(&w, 0, sizeof(w));
   w.dpar = 0;
   w.nkmax = (size_t)p->h * 2 * sizeof(double);
-  size_t off = align256(w.nkmax + sizeof(unsigned int));
+  size_t off = align256(w.nkmax + sizeof(unsigned long long));
   w.aux = off;
   if (!bwd_on_tensor_cores(p)) {  // the CUDA-core path: the rows' D and (Yat) Z
     off += align256((size_t)2 * p->B * p->h * p->Tq * sizeof(float));
@@ -772,10 +798,10 @@ int cattn_backward(int variant, const cattn_problem_t *p, const void *q, const v
   if ((rc = map_cuda(cudaMemsetAsync(ws, 0, w.aux, s))) != CATTN_OK) return rc;
   if (variant == CATTN_YAT) {
     bp.nk = reinterpret_cast<const float *>(ws + w.nk);
-    unsigned int *nk_max = reinterpret_cast<unsigned int *>(ws + w.nkmax);
+    unsigned long long *nk_max = reinterpret_cast<unsigned long long *>(ws + w.nkmax);
     if ((rc = map_cuda(launch_row_sqnorm_bf16(k, reinterpret_cast<float *>(ws + w.nk),
-                                              p->B * p->hkv, p->Tk, tk_pad(p), p->dk, nk_max, s))) !=
-        CATTN_OK)
+                                              p->B * p->hkv, p->Tk, tk_pad(p), p->dk, nk_max,
+                                              next_norm_generation(), nullptr, 0, s))) != CATTN_OK)
       return rc;
   }
   if ((rc = map_cuda(launch_bwd_prep(variant, p->dk, p->dv, bp, q, out, dout, row_mass, s))) !=

@@ -761,7 +761,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           qe = (s2.x + s2.y) + yeps;
           // the bounds under which the map's fast path is exact up to rounding
-          const float span = qe + __uint_as_float(*p.nk_max);
+          // (a maximum of another generation of norms bounds nothing: the
+          // exact path then)
+          const unsigned long long nkw = *p.nk_max;
+          const float nkm = p.nk_gen == 0u || (unsigned)(nkw >> 32) == p.nk_gen
+                                ? __uint_as_float((unsigned)nkw)
+                                : INFINITY;
+          const float span = qe + nkm;
           fast = yeps >= 0x1p-60f && __all_sync(FULL, span <= 0x1p61f && span * 0x1p-16f <= yeps);
           if (STATS && st_q4) st_thr = yat_near_threshold(s2.x + s2.y, yb, YM);
         }
@@ -1203,6 +1209,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // the key-split combine or the near-key pass may start launching (they
+  // wait for this grid's completion before they read anything)
+  griddep_launch_dependents();
 }
 
 // Key-split combine: one warp per query row merges the n_splits partials.
@@ -1210,6 +1219,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // bring each partial onto the largest running max first.
 template <int VARIANT, int DV>
 __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ FwdParams p) {
+  griddep_wait();  // the fused kernel's partials
   const long long rows = (long long)p.B * p.h * p.Tq;
   const long long rrow = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (rrow >= rows) return;
@@ -1282,6 +1292,7 @@ __global__ void __launch_bounds__(256) near_fix_kernel(const __grid_constant__ F
   constexpr int VE = DV / 32;  // v columns per lane
   __shared__ float s_mass[8], s_top[8], s_slog[8];
   __shared__ float s_o[8][DV];
+  griddep_wait();  // the fused kernel's list, outputs and telemetry
   const unsigned n = min(*p.near_count, p.near_cap);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const T *qg = static_cast<const T *>(p.q);
@@ -1384,6 +1395,25 @@ __global__ void tau_finalize_kernel(const double *moments, const float *eps, int
   }
 }
 
+// Launch of a kernel that follows the fused kernel on the stream: with the
+// programmatic serialisation attribute it may begin launching while the
+// fused kernel's last CTAs finish; it waits (griddepcontrol.wait) before it
+// reads their results.
+template <typename Kern>
+cudaError_t launch_dependent(Kern kern, unsigned grid, cudaStream_t s, const FwdParams &p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 template <int VARIANT, int DK, int DV, int YM = 1, bool STATS = false, bool ENT = false>
 cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                    const CUtensorMap &tv, cudaStream_t s) {
@@ -1403,6 +1433,8 @@ cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap 
   }
   if (p.n_units <= 0) return cudaSuccess;
   const int grid = p.n_units < sm_count ? p.n_units : sm_count;  // one CTA per SM
+  // (an ordinary launch: as a programmatic dependent of the key-norm kernel
+  // it measured 3% slower on a causal B=16, 16-head, 4096-token problem)
   kern<<<grid, NUM_THREADS, L::ALLOC, s>>>(p, tq, tk, tv);
   e = cudaGetLastError();
   if constexpr (VARIANT == kTau || STATS) {
@@ -1411,13 +1443,12 @@ cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap 
     if (e != cudaSuccess) return e;
     if (p.n_splits > 1) {
       const long long rows = (long long)p.B * p.h * p.Tq;
-      combine_kernel<VARIANT, DV><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(p);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      if ((e = launch_dependent(combine_kernel<VARIANT, DV>, (unsigned)((rows + 7) / 8), s, p)) !=
+          cudaSuccess)
+        return e;
     }
-    if constexpr (VARIANT == kYat) {
-      near_fix_kernel<DK, DV, YM, __nv_bfloat16><<<sm_count, 256, 0, s>>>(p);
-      e = cudaGetLastError();
-    }
+    if constexpr (VARIANT == kYat)
+      e = launch_dependent(near_fix_kernel<DK, DV, YM, __nv_bfloat16>, (unsigned)sm_count, s, p);
     return e;
   }
 }

@@ -25,7 +25,11 @@ struct FwdParams {
   const float *b, *eps, *tau;   // [h]
   int yat_m;                    // Yat numerator exponent 2 yat_m (1, 2 or 3)
   const float *nk;              // [B*hkv, Tk_pad]  squared k row norms (Yat, bf16), zero padded
-  const unsigned int *nk_max;   // the largest of them, fp32 bits (Yat, bf16)
+  // the largest of them as (generation << 32) | fp32 bits, and the
+  // generation of this call's norms (0: take the word as it is, the caller
+  // computed the norms)
+  const unsigned long long *nk_max;
+  unsigned int nk_gen;
   int B, h, hkv, Tq, Tk, Tk_pad;
   int causal;
   float scale;
@@ -115,10 +119,18 @@ cudaError_t read_and_clear_tf32_status(unsigned int *value);
 cudaError_t launch_near_fix_f32(int dk, int dv, int ym, const FwdParams &p, cudaStream_t s);
 
 // Squared row norms of a bf16 [BH, T, d] tensor into out[BH, T_pad] (zeros
-// for padded rows); their maximum is folded into *max_bits (fp32 bits, which
-// must hold 0 or an earlier maximum) with atomicMax.
+// for padded rows).  Their maximum is folded into *max64 as (gen << 32) |
+// fp32 bits by compare-and-swap: a word of another generation (an earlier
+// call's, or the workspace's old contents) is replaced and within gen the
+// value only grows, so the word needs no zeroing.  Block 0
+// also zeroes n_zero words at zero_words (the control words of the kernel
+// that follows).
 cudaError_t launch_row_sqnorm_bf16(const void *x, float *out, int BH, int T, int T_pad, int d,
-                                   unsigned int *max_bits, cudaStream_t s);
+                                   unsigned long long *max64, unsigned int gen,
+                                   unsigned int *zero_words, int n_zero, cudaStream_t s);
+// A generation for launch_row_sqnorm_bf16: strictly increasing over the
+// process's calls, never 0.
+unsigned int next_norm_generation();
 
 // Device status word set by the forward kernels whose bounded waits gave up.
 cudaError_t read_and_clear_status(unsigned int *value);

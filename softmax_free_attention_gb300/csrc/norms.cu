@@ -23,7 +23,11 @@ template <int G>  // threads per row = d / 8
 __global__ void __launch_bounds__(kThreads) row_sqnorm_kernel(const uint4 *__restrict__ x,
                                                               float *__restrict__ out, int T,
                                                               int T_pad, long long n_out,
-                                                              unsigned int *__restrict__ max_bits) {
+                                                              unsigned long long *__restrict__ max64,
+                                                              unsigned int gen,
+                                                              unsigned int *__restrict__ zero_words,
+                                                              int n_zero) {
+  if (blockIdx.x == 0 && threadIdx.x < n_zero) zero_words[threadIdx.x] = 0u;
   // One pass of a block covers SPAN consecutive output slots; T_pad is a
   // multiple of 128 >= SPAN, so a span never crosses from one head to the next.
   constexpr int RPB = kThreads / G;
@@ -59,7 +63,7 @@ __global__ void __launch_bounds__(kThreads) row_sqnorm_kernel(const uint4 *__res
       running_max = fmaxf(running_max, acc);
     }
   }
-  // one atomic per CTA; non-negative floats order like their bit patterns
+  // one update per CTA; non-negative floats order like their bit patterns
   __shared__ float warp_max[kThreads / 32];
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1)
@@ -70,14 +74,23 @@ __global__ void __launch_bounds__(kThreads) row_sqnorm_kernel(const uint4 *__res
     float m = warp_max[0];
 #pragma unroll
     for (int w = 1; w < kThreads / 32; ++w) m = fmaxf(m, warp_max[w]);
-    atomicMax(max_bits, __float_as_uint(m));
+    // a word of another generation (an earlier call's maximum, or whatever
+    // the workspace held) is replaced; within this generation it only grows
+    const unsigned long long mine = ((unsigned long long)gen << 32) | __float_as_uint(m);
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(max64);
+    while (!((unsigned)(old >> 32) == gen && old >= mine)) {
+      const unsigned long long seen = atomicCAS(max64, old, mine);
+      if (seen == old) break;
+      old = seen;
+    }
   }
 }
 
 }  // namespace
 
 cudaError_t launch_row_sqnorm_bf16(const void *x, float *out, int BH, int T, int T_pad, int d,
-                                   unsigned int *max_bits, cudaStream_t s) {
+                                   unsigned long long *max64, unsigned int gen,
+                                   unsigned int *zero_words, int n_zero, cudaStream_t s) {
   const long long n_out = (long long)BH * T_pad;
   if (n_out == 0) return cudaSuccess;
   const int G = d / 8;
@@ -92,9 +105,11 @@ cudaError_t launch_row_sqnorm_bf16(const void *x, float *out, int BH, int T, int
   if (blocks > 8LL * sms) blocks = 8LL * sms;
   const uint4 *xv = reinterpret_cast<const uint4 *>(x);
   if (G == 16)
-    row_sqnorm_kernel<16><<<(unsigned)blocks, kThreads, 0, s>>>(xv, out, T, T_pad, n_out, max_bits);
+    row_sqnorm_kernel<16><<<(unsigned)blocks, kThreads, 0, s>>>(xv, out, T, T_pad, n_out, max64, gen,
+                                                                 zero_words, n_zero);
   else
-    row_sqnorm_kernel<8><<<(unsigned)blocks, kThreads, 0, s>>>(xv, out, T, T_pad, n_out, max_bits);
+    row_sqnorm_kernel<8><<<(unsigned)blocks, kThreads, 0, s>>>(xv, out, T, T_pad, n_out, max64, gen,
+                                                                zero_words, n_zero);
   return cudaGetLastError();
 }
 
