@@ -451,7 +451,15 @@ int forward_impl(int variant, const cattn_problem_t *p, const void *q, const voi
   const int grid = tc_grid_size(w.sched.n_units);
   if (grid < 0) return CATTN_ERR_CUDA;
   const bool ticket = w.sched.n_units > grid;
-  if (own_norms) {
+  // a Yat problem whose units all run in one wave (no key split, keys <= 2048,
+  // exponent 1, no entropy) is one launch: the fused kernel takes the key
+  // norms of its unit and recomputes its near-key rows itself, and reads no
+  // control word
+  fp.inline_norms = own_norms && !ticket && w.sched.n_splits == 1 && fp.n_kv_tiles <= 16 &&
+                    fp.yat_m == 1 && row_entropy == nullptr;
+  if (fp.inline_norms) {
+    // nothing before the kernel
+  } else if (own_norms) {
     if ((rc = map_cuda(launch_row_sqnorm_bf16(
              k, reinterpret_cast<float *>(ws + w.nk), p->B * p->hkv, p->Tk, tk_pad(p), p->dk,
              reinterpret_cast<unsigned long long *>(ctrl + kCtrlNkMax), gen, ctrl, 2, s))) !=

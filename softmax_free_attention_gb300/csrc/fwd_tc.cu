@@ -97,6 +97,8 @@ constexpr int MAP_WARPS = 16;
 constexpr int PRODUCER_WARP = 16;
 constexpr int MMA_WARP = 17;
 constexpr int NKS = 4;  // stages of the key-norm ring
+// the one-launch Yat forward (INORM): key tiles a unit may have (Tk <= 2048)
+constexpr int INORM_MAX_TILES = 16;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 // the limit of the test-only wait that nothing completes (FwdParams::test_stall)
 constexpr uint64_t STALL_LIMIT_NS = 20000000ull;
@@ -132,11 +134,19 @@ struct Layout {
   static constexpr int OFF_XCHG = OFF_NK + NKS * BN * 4;
   // (the row statistics pass uses [13 values][2 tiles][BM] of it)
   static constexpr int XCHG_FLOATS = 26 * BM;
-  static constexpr int OFF_BAR = OFF_XCHG + XCHG_FLOATS * 4;
+  // one-launch Yat forward: the unit's key norms and their largest (fp32
+  // bits), the unit's rows listed for the near-key recompute and their count
+  static constexpr int OFF_NKU = OFF_XCHG + XCHG_FLOATS * 4;
+  static constexpr int OFF_NKU_MAX = OFF_NKU + INORM_MAX_TILES * BN * 4;
+  static constexpr int OFF_NEAR = OFF_NKU_MAX + 16;
+  static constexpr int OFF_NEAR_N = OFF_NEAR + 2 * BM * 4;
+  static constexpr int OFF_BAR = OFF_NEAR_N + 16;
   // q_full, q_empty, kv_full[NS], kv_empty[NS], nk_full[NKS], nk_empty[NKS],
   // s_full[2], p_full[2], o_full[2], o_empty[2], unit_full[2], unit_empty[2], drain,
-  // p_half[2], never (nothing arrives on it: the test-only stall)
-  static constexpr int NBAR = 2 + 2 * NS + 2 * NKS + 16;
+  // p_half[2], never (nothing arrives on it: the test-only stall), and for the
+  // one-launch Yat forward nku_ready (the unit's key norms written) and
+  // rows_done (every row of the unit written)
+  static constexpr int NBAR = 2 + 2 * NS + 2 * NKS + 18;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // TMEM base address, abort flag, unit ring[2]
   static constexpr int BYTES = OFF_MISC + 16;
@@ -336,11 +346,76 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams &p, int u) {
 // ENT: the forward also accumulates each row's sum f log2 f of its weights'
 // numerators f (Yat kappa; softmax, s^tau 2^(x - m) on the running max m) and
 // writes the row's normalised entropy.
-template <int VARIANT, int DK, int DV, int YM = 1, bool STATS = false, bool ENT = false>
+// One row of the Yat map by its plain definition, by one warp (the lanes
+// share the components of q and k and the columns of v; the keys in order):
+// the output row, its mass and max kappa (the near-key recompute of the
+// one-launch path; the separate near-key pass spreads a row over 8 warps).
+template <int DK, int DV, int YM>
+__device__ __noinline__ void near_row_warp(const FwdParams &p, int bh, int row, int lane) {
+  constexpr int QE = DK / 32, VE = DV / 32;
+  if (row >= p.Tq) return;
+  const int head = bh % p.h, batch = bh / p.h;
+  const size_t bh_kv = (size_t)batch * p.hkv + head / (p.h / p.hkv);
+  const float b = p.b[head], eps = p.eps[head];
+  const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.q);
+  const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(p.k);
+  const __nv_bfloat16 *vg = static_cast<const __nv_bfloat16 *>(p.v);
+  float qf[QE];
+#pragma unroll
+  for (int i = 0; i < QE; ++i)
+    qf[i] = __bfloat162float(qg[((size_t)bh * p.Tq + row) * DK + lane * QE + i]);
+  const int lim = p.causal ? min(row + 1, p.Tk) : p.Tk;
+  float mass = 0.f, top = 0.f, o[VE];
+#pragma unroll
+  for (int c = 0; c < VE; ++c) o[c] = 0.f;
+  for (int j = 0; j < lim; ++j) {
+    const __nv_bfloat16 *kr = kg + (bh_kv * p.Tk + j) * DK + lane * QE;
+    float dot = 0.f, d2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < QE; ++i) {
+      const float kf = __bfloat162float(kr[i]);
+      dot = fmaf(qf[i], kf, dot);
+      const float df = qf[i] - kf;
+      d2 = fmaf(df, df, d2);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      dot += __shfl_xor_sync(FULL, dot, off);
+      d2 += __shfl_xor_sync(FULL, d2, off);
+    }
+    const float tt = dot + b;
+    float num = tt * tt;
+    if constexpr (YM == 2) num = num * num;
+    if constexpr (YM == 3) num = num * num * num;
+    const float kap = num / (fmaxf(d2, 0.f) + eps);
+    mass += kap;
+    top = fmaxf(top, kap);
+    const __nv_bfloat16 *vr = vg + (bh_kv * p.Tk + j) * DV + lane * VE;
+#pragma unroll
+    for (int c = 0; c < VE; ++c) o[c] = fmaf(kap, __bfloat162float(vr[c]), o[c]);
+  }
+  const float inv = 1.f / (mass + 1e-9f);
+  const size_t ti = (size_t)bh * p.Tq + row;
+  __nv_bfloat16 *orow = static_cast<__nv_bfloat16 *>(p.out) + ti * DV + lane * VE;
+#pragma unroll
+  for (int c = 0; c < VE; ++c) orow[c] = __float2bfloat16_rn(o[c] * inv);
+  if (lane == 0) {
+    if (p.row_mass) p.row_mass[ti] = mass;
+    if (p.row_max) p.row_max[ti] = top;
+  }
+}
+
+// INORM: the one-launch Yat forward for problems whose units all run in one
+// wave (one unit per CTA, keys <= 2048, no key splits): the map warps take
+// the unit's key norms themselves at its start, and recompute the rows they
+// flag for the near-key guard at its end, so no other launch is needed.
+template <int VARIANT, int DK, int DV, int YM = 1, bool STATS = false, bool ENT = false,
+          bool INORM = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fwd_kernel(const __grid_constant__ FwdParams p, const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v) {
   using L = Layout<DK, DV>;
+  static_assert(!INORM || (VARIANT == kYat && !STATS && !ENT), "one-launch path: Yat forward only");
   // Yat and s^tau split each PV in two: half of it runs while the map warps
   // work on the second half of P (softmax, whose map is the shortest, keeps
   // one PV and its rescale after the map)
@@ -374,6 +449,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t bar_drain = bar0 + 8u * (B2 + 12);
   auto p_half = [&](int x) { return bar0 + 8u * (B2 + 13 + x); };
   const uint32_t bar_never = bar0 + 8u * (B2 + 15);
+  const uint32_t bar_nku_ready = bar0 + 8u * (B2 + 16);
+  const uint32_t bar_rows_done = bar0 + 8u * (B2 + 17);
+  float *nku = reinterpret_cast<float *>(smem + L::OFF_NKU);
+  unsigned int *nku_max = reinterpret_cast<unsigned int *>(smem + L::OFF_NKU_MAX);
+  unsigned int *near_list = reinterpret_cast<unsigned int *>(smem + L::OFF_NEAR);
+  unsigned int *near_n = reinterpret_cast<unsigned int *>(smem + L::OFF_NEAR_N);
   auto q_smem = [&](int x) { return sb + L::OFF_Q + (uint32_t)x * L::Q_TILE; };
   auto slot_smem = [&](uint32_t s) { return sb + L::OFF_RING + s * L::SLOT; };
   const float *nk_ring = reinterpret_cast<const float *>(smem + L::OFF_NK);
@@ -405,6 +486,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     mbar_init(bar_drain, 1);
     mbar_init(bar_never, 1);
+    mbar_init(bar_nku_ready, MAP_WARPS);  // lane 0 of every map warp
+    mbar_init(bar_rows_done, MAP_WARPS);
+    *nku_max = 0u;
+    *near_n = 0u;
     *abort = 0;
     fence_mbar_init();
   }
@@ -477,7 +562,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tma_load_3d(slot_smem(s) + c * BN * 128, &tm_k, c * 64, jt * BN, t.bh_kv, kv_full(s));
             kv_issued = pos + 1;
           }
-          if (VARIANT == kYat) {  // squared key norms of the tile
+          if (VARIANT == kYat && !INORM) {  // squared key norms of the tile
             const uint32_t pos = nk_pos + j, s = pos % NKS;
             if (!(ok = thread_wait(nk_empty(s), ((pos / NKS) & 1u) ^ 1u, abort,
                                    SITE_PRODUCER | 0x20)))
@@ -630,7 +715,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (j < t.nkv) mcommit(kv_empty(ks));
           if (HAS_V && j >= 1) mcommit(kv_empty(vs));
           // every map warp delivered P for tile j-1, so all are done with its key norms
-          if (VARIANT == kYat && j >= 1 && (!CONV || lane == 0))
+          if (VARIANT == kYat && !INORM && j >= 1 && (!CONV || lane == 0))
             mbar_arrive(nk_empty((nk_pos + j - 1) % NKS));
 #ifdef CATTN_TRACE
           ++ms;
@@ -733,6 +818,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (row >= p.Tq) lim_base = 0;  // rows past Tq have no keys
       }
+      if constexpr (INORM) {
+        // the unit's key norms (keys 0 .. nkv BN, zero past Tk) and their
+        // largest, by all sixteen map warps (thread m takes keys m, m + 512,
+        // ...) while the first tiles load; the unit is the CTA's only one
+        const Unit t = decode_unit(p, u);
+        const __nv_bfloat16 *kh = static_cast<const __nv_bfloat16 *>(p.k) + (size_t)t.bh_kv * p.Tk * DK;
+        float lmax = 0.f;
+        for (int key = warp * 32 + lane; key < nkv * BN; key += MAP_WARPS * 32) {
+          float2 s2 = make_float2(0.f, 0.f);
+          if (key < p.Tk) {
+            const uint4 *row4 = reinterpret_cast<const uint4 *>(kh + (size_t)key * DK);
+#pragma unroll
+            for (int c0 = 0; c0 < DK / 8; c0 += 8) {
+              uint4 kv4[8];
+#pragma unroll
+              for (int c = 0; c < 8; ++c) kv4[c] = __ldg(row4 + c0 + c);
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const uint32_t w4[4] = {kv4[c].x, kv4[c].y, kv4[c].z, kv4[c].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float2 f = make_float2(__uint_as_float(w4[e] << 16),
+                                               __uint_as_float(w4[e] & 0xffff0000u));
+                  s2 = __ffma2_rn(f, f, s2);
+                }
+              }
+            }
+          }
+          const float nrm = s2.x + s2.y;
+          nku[key] = nrm;
+          lmax = fmaxf(lmax, nrm);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(FULL, lmax, o));
+        // (non-negative floats order like their bit patterns)
+        if (lane == 0) atomicMax(nku_max, __float_as_uint(lmax));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_nku_ready);
+        if (!(ok = warp_wait(bar_nku_ready, 0u, abort, SITE_EPI | 0x50))) break;
+      }
       const float g0 = VARIANT == kTau ? logf(0.6931472f + seps) : 0.f;
       if (VARIANT == kYat) {
         // |q|^2 of this thread's row, in fp32 from the bf16 Q tile in shared
@@ -763,10 +888,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // the bounds under which the map's fast path is exact up to rounding
           // (a maximum of another generation of norms bounds nothing: the
           // exact path then)
-          const unsigned long long nkw = *p.nk_max;
-          const float nkm = p.nk_gen == 0u || (unsigned)(nkw >> 32) == p.nk_gen
-                                ? __uint_as_float((unsigned)nkw)
-                                : INFINITY;
+          float nkm;
+          if constexpr (INORM) {
+            nkm = __uint_as_float(*nku_max);  // this unit's keys
+          } else {
+            const unsigned long long nkw = *p.nk_max;
+            nkm = p.nk_gen == 0u || (unsigned)(nkw >> 32) == p.nk_gen ? __uint_as_float((unsigned)nkw)
+                                                                     : INFINITY;
+          }
           const float span = qe + nkm;
           fast = yeps >= 0x1p-60f && __all_sync(FULL, span <= 0x1p61f && span * 0x1p-16f <= yeps);
           if (STATS && st_q4) st_thr = yat_near_threshold(s2.x + s2.y, yb, YM);
@@ -887,9 +1016,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool rescale = false;
         float corr = 1.f;
         if (VARIANT == kYat) {
-          const uint32_t npos = nk_pos + j, ns = npos % NKS;
-          if (!(ok = warp_wait(nk_full(ns), (npos / NKS) & 1u, abort, SITE_EPI | 0x20))) break;
-          const float4 *nk4 = reinterpret_cast<const float4 *>(nk_ring + ns * BN);
+          const float4 *nk4;
+          if constexpr (INORM) {
+            nk4 = reinterpret_cast<const float4 *>(nku + j * BN);
+          } else {
+            const uint32_t npos = nk_pos + j, ns = npos % NKS;
+            if (!(ok = warp_wait(nk_full(ns), (npos / NKS) & 1u, abort, SITE_EPI | 0x20))) break;
+            nk4 = reinterpret_cast<const float4 *>(nk_ring + ns * BN);
+          }
           // chunk by chunk: P chunk c lands on S columns this warp has read
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
@@ -1160,9 +1294,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (VARIANT == kYat && all_top > yat_near_threshold(qe - yeps, yb, YM)) {
               // a key may sit close enough to q for the assembled distance to
-              // have cancelled: the near-key pass recomputes this row
-              const unsigned slot = atomicAdd(p.near_count, 1u);
-              if (slot < p.near_cap) p.near_rows[slot] = make_uint2((unsigned)t.bh, (unsigned)row);
+              // have cancelled: the near-key pass recomputes this row (the
+              // one-launch path: this CTA, after its unit)
+              if constexpr (INORM) {
+                near_list[atomicAdd(near_n, 1u)] = (unsigned)(x * BM + r);
+              } else {
+                const unsigned slot = atomicAdd(p.near_count, 1u);
+                if (slot < p.near_cap) p.near_rows[slot] = make_uint2((unsigned)t.bh, (unsigned)row);
+              }
             }
             if (p.row_mass)
               p.row_mass[ti] = VARIANT == kYat ? total : (m_used + log2f(total)) * LN2;
@@ -1200,6 +1339,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       nk_pos += nkv;
       release_unit(uc);
+    }
+    if constexpr (INORM) {
+      // every row of the CTA's unit written: the rows listed for the
+      // near-key guard are recomputed by the plain definition, one per warp
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_rows_done);
+      if (ok && warp_wait(bar_rows_done, 0u, abort, SITE_EPI | 0x58)) {
+        const Unit t = decode_unit(p, (int)blockIdx.x);
+        const unsigned n = *near_n;
+        for (unsigned e = (unsigned)warp; e < n; e += MAP_WARPS)
+          near_row_warp<DK, DV, YM>(p, t.bh, t.q0 + (int)near_list[e], lane);
+      }
     }
   }
 
@@ -1414,11 +1565,12 @@ cudaError_t launch_dependent(Kern kern, unsigned grid, cudaStream_t s, const Fwd
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int VARIANT, int DK, int DV, int YM = 1, bool STATS = false, bool ENT = false>
+template <int VARIANT, int DK, int DV, int YM = 1, bool STATS = false, bool ENT = false,
+          bool INORM = false>
 cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                    const CUtensorMap &tv, cudaStream_t s) {
   using L = Layout<DK, DV>;
-  auto kern = fwd_kernel<VARIANT, DK, DV, YM, STATS, ENT>;
+  auto kern = fwd_kernel<VARIANT, DK, DV, YM, STATS, ENT, INORM>;
   static int configured_for = -1;
   static int sm_count = 0;
   int dev = 0;
@@ -1447,7 +1599,7 @@ cudaError_t launch(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap 
           cudaSuccess)
         return e;
     }
-    if constexpr (VARIANT == kYat)
+    if constexpr (VARIANT == kYat && !INORM)  // (the one-launch path recomputes its rows itself)
       e = launch_dependent(near_fix_kernel<DK, DV, YM, __nv_bfloat16>, (unsigned)sm_count, s, p);
     return e;
   }
@@ -1497,6 +1649,14 @@ cudaError_t launch_fwd_tc(int variant, int dk, int dv, const FwdParams &p, const
   if (variant == V && dk == DK_ && dv == DV_)                                        \
     return p.row_entropy ? tc::launch<V, DK_, DV_, 1, false, true>(p, tq, tk, tv, s) \
                          : tc::launch<V, DK_, DV_>(p, tq, tk, tv, s);
+#define CATTN_TC_INORM(DK_, DV_)                                                      \
+  if (variant == kYat && p.inline_norms && p.yat_m == 1 && !p.row_entropy && dk == DK_ && \
+      dv == DV_)                                                                      \
+    return tc::launch<kYat, DK_, DV_, 1, false, false, true>(p, tq, tk, tv, s);
+  CATTN_TC_INORM(64, 64)
+  CATTN_TC_INORM(128, 128)
+  CATTN_TC_INORM(128, 64)
+#undef CATTN_TC_INORM
 #define CATTN_TC_YAT_M(DK_, DV_, M_)                            \
   if (variant == kYat && p.yat_m == M_ && dk == DK_ && dv == DV_) \
     return tc::launch<kYat, DK_, DV_, M_>(p, tq, tk, tv, s);

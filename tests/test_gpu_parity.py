@@ -292,6 +292,34 @@ def test_constant_values_give_constant_output():
 
 # ---------------------------------------------------------------- both Yat map paths
 
+def test_yat_workspace_contents_do_not_matter():
+    """The forward needs no zeroed workspace: the key-norm kernel zeroes the
+    control words it reads and keeps the largest key norm in a word tagged
+    with the call's generation, replacing a word of any other generation.  A
+    workspace full of 0xFF bytes, or one whose maximum word carries a
+    generation no call has drawn yet, must give the same bits as a zeroed
+    one (with eps large enough that the map takes its fast path, which a
+    stale maximum would switch off)."""
+    w = _wl("ws", 2, 4, 2, 333, 333, 128, 128, causal=True, qk=1.0, seed=21)
+    inp = workloads.generate(w, device="cuda")
+    b = torch.full((4,), 0.5, device="cuda")
+    eps = torch.full((4,), 0.5, device="cuda")
+    prob = attention.make_problem(inp["q"], inp["k"], inp["v"], causal=True, scale=w.scale)
+    need = attention.workspace_bytes("yat", prob)
+    zero = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    full = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    future = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    # bytes 8-15: the largest key norm (0.0) under generation 0xFFFFFFF0
+    future[8:16] = torch.tensor([0, 0, 0, 0, 0xF0, 0xFF, 0xFF, 0xFF], dtype=torch.uint8)
+    outs = [attention.forward("yat", inp["q"], inp["k"], inp["v"], b=b, eps=eps, causal=True,
+                              workspace=ws) for ws in (zero, full, future, zero)]
+    torch.cuda.synchronize()
+    assert attention.check_status() == 0
+    for o in outs[1:]:
+        for x, y in zip(outs[0], o):
+            assert torch.equal(x, y)
+
+
 @pytest.mark.parametrize("eps,qk,where", [
     (0.5, 1.0, "fast path: eps well above the rounding of |q|^2 + |k|^2"),
     (1e-3, 4.0, "exact path: eps below (|q|^2 + max |k|^2) 2^-16"),
