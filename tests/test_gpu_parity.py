@@ -299,11 +299,12 @@ def test_yat_workspace_contents_do_not_matter():
     workspace full of 0xFF bytes, or one whose maximum word carries a
     generation no call has drawn yet, must give the same bits as a zeroed
     one (with eps large enough that the map takes its fast path, which a
-    stale maximum would switch off)."""
-    w = _wl("ws", 2, 4, 2, 333, 333, 128, 128, causal=True, qk=1.0, seed=21)
+    stale maximum would switch off).  2100 keys: more than the one-launch
+    path takes, so the key-norm kernel and its maximum word are used."""
+    w = _wl("ws", 1, 2, 2, 2100, 2100, 128, 128, causal=True, qk=1.0, seed=21)
     inp = workloads.generate(w, device="cuda")
-    b = torch.full((4,), 0.5, device="cuda")
-    eps = torch.full((4,), 0.5, device="cuda")
+    b = torch.full((2,), 0.5, device="cuda")
+    eps = torch.full((2,), 0.5, device="cuda")
     prob = attention.make_problem(inp["q"], inp["k"], inp["v"], causal=True, scale=w.scale)
     need = attention.workspace_bytes("yat", prob)
     zero = torch.zeros(need, dtype=torch.uint8, device="cuda")
@@ -371,7 +372,10 @@ def test_yat_keys_equal_to_queries(case):
     inp["k"] = inp["q"].clone()
     inp["yat_b"] = np.array([0.3, 2.0], dtype=np.float32)
     inp["yat_eps"] = np.full(2, eps, dtype=np.float32)
+    # the key-norm kernel with the separate near-key pass, and the one call
+    # whose units all run in one wave (its rows recomputed inside the kernel)
     pu.full_parity("yat", inp, causal=True, scale=w.scale, two_step=True, where=f"tied {name}")
+    pu.full_parity("yat", inp, causal=True, scale=w.scale, where=f"tied {name} one launch")
     _, _, mx = pu.run_gpu("yat", inp, causal=True, scale=w.scale)
     ref = _closed_form_self(inp["q"], inp["yat_b"], inp["yat_eps"])
     rel = np.abs(pu.to_np(mx) - ref) / ref
@@ -402,6 +406,8 @@ def test_yat_some_keys_copied_from_queries(case):
         inp["yat_eps"] = np.full(2, eps, dtype=np.float32)
         pu.full_parity("yat", inp, causal=causal, scale=w.scale, two_step=True,
                        where=f"copied {name} causal={causal}")
+        pu.full_parity("yat", inp, causal=causal, scale=w.scale,
+                       where=f"copied {name} causal={causal} one call")
 
 
 # ---------------------------------------------------------------- tau*
