@@ -125,7 +125,8 @@ const char *cattn_error_string(int status);
 /* Bytes of device workspace cattn_forward / cattn_key_norms need for this
  * problem and variant (0 if none), 256-byte aligned.  The bf16 tensor-core
  * path needs a 256-byte control block (its work-unit ticket and, for
- * CATTN_YAT, the count of rows listed for the near-key pass), plus, for
+ * CATTN_YAT, the count of rows listed for the near-key pass and the largest
+ * key norm), plus, for
  * CATTN_YAT, the fp32 squared norms of every key row (padded to a multiple of
  * 128 rows per head) and the near-key list (8 bytes per row and key split),
  * plus, for non-causal problems with few (batch, head, 256-row) units, the
@@ -152,7 +153,10 @@ int cattn_validate(int variant, const cattn_problem_t *p, const void *q, const v
  * "One module, two compatibility functions"); the forward kernel takes |q|^2
  * itself from the query tiles it holds, |k|^2 from here because every key
  * tile serves many query tiles.  bf16 problems only.  cattn_forward(CATTN_YAT,
- * ...) runs this itself unless CATTN_FLAG_NORMS_READY is set. */
+ * ...) runs this itself unless CATTN_FLAG_NORMS_READY is set, except for a
+ * problem whose work units all run in one wave (no key split, Tk <= 2048,
+ * yat_m 1), where the forward kernel takes each unit's key norms itself and
+ * makes no other launch. */
 int cattn_key_norms(const cattn_problem_t *p, const void *k, void *workspace,
                     size_t workspace_bytes, cattn_stream_t stream);
 

@@ -47,8 +47,11 @@ bool is_empty(const cattn_problem_t *p) { return p->B == 0 || p->h == 0 || p->Tq
 // Workspace layout of the bf16 (tensor-core) path, each part 256-byte aligned:
 //   ctrl       256 B: the persistent schedule's unit ticket and (Yat) the
 //              count of rows listed for the near-key pass (both zeroed by
-//              each forward), then (Yat) the largest key norm as fp32 bits
-//              (zeroed and written by the key-norm prologue)
+//              each forward: by the key-norm kernel when the forward takes
+//              the norms, else by a memset; the one-launch Yat forward reads
+//              neither), then at byte 8 (Yat) the largest key norm as a
+//              64-bit (generation << 32 | fp32 bits) word, which needs no
+//              zeroing (launch_row_sqnorm_bf16)
 //   nk         Yat only: squared k row norms [B*hkv, Tk_pad], fp32 (the
 //              query norms are taken in-kernel from the Q tiles)
 //   near       Yat only: the rows listed for the near-key pass, (batch*head,
@@ -658,8 +661,8 @@ int cattn_row_stats(int variant, const cattn_problem_t *p, const void *q, const 
 namespace {
 
 // Backward workspace, each part 256-byte aligned:
-//   dpar   [h][2] fp64 per-head parameter gradient sums, then (Yat) the largest
-//          key norm as fp32 bits (both zeroed by each call)
+//   dpar   [h][2] fp64 per-head parameter gradient sums (zeroed by each call),
+//          then (Yat) the largest key norm as a 64-bit generation-tagged word
 //   aux    [B*h, Tq_pad] float4: D, normaliser, |q|^2 per query row
 //   nk     Yat only: squared k row norms [B*hkv, Tk_pad]
 struct BwdWs {

@@ -42,7 +42,7 @@ struct FwdParams {
   int kv_per_split;  // key tiles per split
   int head_group;    // (batch, head) pairs whose units are scheduled together
   int n_units;       // B * h * n_pairs * n_splits
-  unsigned int *tile_counter;  // next unit to hand out (zeroed before launch)
+  unsigned int *tile_counter;  // next unit to hand out (zero at launch; unread when the units fit in one wave)
   float *part_o;     // [n_splits, B*h, Tq, dv] unnormalised partial outputs (n_splits > 1)
   float *part_stat;  // [n_splits, B*h, Tq, 4]: mass or l, running max (log2), top score
   double *moments;   // kTau: [h][6] sums n, s, g, s g, g^2 (g = ln phi(s) - g0), zeroed
