@@ -97,7 +97,8 @@ constexpr int MAP_WARPS = 16;
 constexpr int PRODUCER_WARP = 16;
 constexpr int MMA_WARP = 17;
 constexpr int NKS = 4;  // stages of the key-norm ring
-// the one-launch Yat forward (INORM): key tiles a unit may have (Tk <= 2048)
+// the one-launch Yat forward (INORM): key tiles a unit may have (Tk <= 2048;
+// the recompute of a flagged row there takes one warp over the row's keys)
 constexpr int INORM_MAX_TILES = 16;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 // the limit of the test-only wait that nothing completes (FwdParams::test_stall)
@@ -134,19 +135,18 @@ struct Layout {
   static constexpr int OFF_XCHG = OFF_NK + NKS * BN * 4;
   // (the row statistics pass uses [13 values][2 tiles][BM] of it)
   static constexpr int XCHG_FLOATS = 26 * BM;
-  // one-launch Yat forward: the unit's key norms and their largest (fp32
-  // bits), the unit's rows listed for the near-key recompute and their count
+  // one-launch Yat forward: each map warp's key norms of the current tile
+  // (BN floats per warp, its 64 keys filled), the unit's rows listed for the
+  // near-key recompute and their count
   static constexpr int OFF_NKU = OFF_XCHG + XCHG_FLOATS * 4;
-  static constexpr int OFF_NKU_MAX = OFF_NKU + INORM_MAX_TILES * BN * 4;
-  static constexpr int OFF_NEAR = OFF_NKU_MAX + 16;
+  static constexpr int OFF_NEAR = OFF_NKU + MAP_WARPS * BN * 4;
   static constexpr int OFF_NEAR_N = OFF_NEAR + 2 * BM * 4;
   static constexpr int OFF_BAR = OFF_NEAR_N + 16;
   // q_full, q_empty, kv_full[NS], kv_empty[NS], nk_full[NKS], nk_empty[NKS],
   // s_full[2], p_full[2], o_full[2], o_empty[2], unit_full[2], unit_empty[2], drain,
   // p_half[2], never (nothing arrives on it: the test-only stall), and for the
-  // one-launch Yat forward nku_ready (the unit's key norms written) and
-  // rows_done (every row of the unit written)
-  static constexpr int NBAR = 2 + 2 * NS + 2 * NKS + 18;
+  // one-launch Yat forward rows_done (every row of the unit written)
+  static constexpr int NBAR = 2 + 2 * NS + 2 * NKS + 17;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // TMEM base address, abort flag, unit ring[2]
   static constexpr int BYTES = OFF_MISC + 16;
@@ -346,6 +346,43 @@ __device__ __forceinline__ Unit decode_unit(const FwdParams &p, int u) {
 // ENT: the forward also accumulates each row's sum f log2 f of its weights'
 // numerators f (Yat kappa; softmax, s^tau 2^(x - m) on the running max m) and
 // writes the row's normalised entropy.
+// Squared norms of keys 64 half + lane and 64 half + 32 + lane of a K tile
+// in shared memory (rows of DK bf16 in 64-column boxes BN rows apart, each
+// 128-byte box row swizzled in 16-byte units; the sum does not depend on
+// where a unit sits, and the order of a row's units is rotated by lane so
+// that a warp's loads fall in distinct banks): written to nkw at those key
+// offsets; returns the largest over the warp's 64 keys (zero rows past Tk
+// give zero).
+template <int DK>
+__device__ __forceinline__ float inorm_tile_norms(uint32_t slot, int half, int lane, float *nkw) {
+  float mx = 0.f;
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {
+    const int key = 64 * half + 32 * h2 + lane;
+    float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < DK / 64; ++c) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint4 v = lds128(slot + (uint32_t)(c * (BN * 128) + key * 128) +
+                               ((uint32_t)((k + lane) & 7) << 4));
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = make_float2(__uint_as_float(w4[e] << 16), __uint_as_float(w4[e] & 0xffff0000u));
+          s2 = __ffma2_rn(f, f, s2);
+        }
+      }
+    }
+    const float nrm = s2.x + s2.y;
+    nkw[key] = nrm;
+    mx = fmaxf(mx, nrm);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
+  return mx;
+}
+
 // One row of the Yat map by its plain definition, by one warp (the lanes
 // share the components of q and k and the columns of v; the keys in order):
 // the output row, its mass and max kappa (the near-key recompute of the
@@ -449,10 +486,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t bar_drain = bar0 + 8u * (B2 + 12);
   auto p_half = [&](int x) { return bar0 + 8u * (B2 + 13 + x); };
   const uint32_t bar_never = bar0 + 8u * (B2 + 15);
-  const uint32_t bar_nku_ready = bar0 + 8u * (B2 + 16);
-  const uint32_t bar_rows_done = bar0 + 8u * (B2 + 17);
+  const uint32_t bar_rows_done = bar0 + 8u * (B2 + 16);
   float *nku = reinterpret_cast<float *>(smem + L::OFF_NKU);
-  unsigned int *nku_max = reinterpret_cast<unsigned int *>(smem + L::OFF_NKU_MAX);
   unsigned int *near_list = reinterpret_cast<unsigned int *>(smem + L::OFF_NEAR);
   unsigned int *near_n = reinterpret_cast<unsigned int *>(smem + L::OFF_NEAR_N);
   auto q_smem = [&](int x) { return sb + L::OFF_Q + (uint32_t)x * L::Q_TILE; };
@@ -469,7 +504,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bar_q_empty, VARIANT == kYat ? 1 + MAP_WARPS : 1);
     for (int s = 0; s < L::NS; ++s) {
       mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+      // one-launch Yat: a K slot (the even positions) is also released by
+      // every map warp once it has taken its keys' norms out of it
+      mbar_init(kv_empty(s), INORM && (s % 2) == 0 ? 1 + MAP_WARPS : 1);
     }
     for (int s = 0; s < NKS; ++s) {
       mbar_init(nk_full(s), 1);
@@ -486,9 +523,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     mbar_init(bar_drain, 1);
     mbar_init(bar_never, 1);
-    mbar_init(bar_nku_ready, MAP_WARPS);  // lane 0 of every map warp
-    mbar_init(bar_rows_done, MAP_WARPS);
-    *nku_max = 0u;
+    mbar_init(bar_rows_done, MAP_WARPS);  // lane 0 of every map warp
     *near_n = 0u;
     *abort = 0;
     fence_mbar_init();
@@ -818,46 +853,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (row >= p.Tq) lim_base = 0;  // rows past Tq have no keys
       }
-      if constexpr (INORM) {
-        // the unit's key norms (keys 0 .. nkv BN, zero past Tk) and their
-        // largest, by all sixteen map warps (thread m takes keys m, m + 512,
-        // ...) while the first tiles load; the unit is the CTA's only one
-        const Unit t = decode_unit(p, u);
-        const __nv_bfloat16 *kh = static_cast<const __nv_bfloat16 *>(p.k) + (size_t)t.bh_kv * p.Tk * DK;
-        float lmax = 0.f;
-        for (int key = warp * 32 + lane; key < nkv * BN; key += MAP_WARPS * 32) {
-          float2 s2 = make_float2(0.f, 0.f);
-          if (key < p.Tk) {
-            const uint4 *row4 = reinterpret_cast<const uint4 *>(kh + (size_t)key * DK);
-#pragma unroll
-            for (int c0 = 0; c0 < DK / 8; c0 += 8) {
-              uint4 kv4[8];
-#pragma unroll
-              for (int c = 0; c < 8; ++c) kv4[c] = __ldg(row4 + c0 + c);
-#pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                const uint32_t w4[4] = {kv4[c].x, kv4[c].y, kv4[c].z, kv4[c].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const float2 f = make_float2(__uint_as_float(w4[e] << 16),
-                                               __uint_as_float(w4[e] & 0xffff0000u));
-                  s2 = __ffma2_rn(f, f, s2);
-                }
-              }
-            }
-          }
-          const float nrm = s2.x + s2.y;
-          nku[key] = nrm;
-          lmax = fmaxf(lmax, nrm);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(FULL, lmax, o));
-        // (non-negative floats order like their bit patterns)
-        if (lane == 0) atomicMax(nku_max, __float_as_uint(lmax));
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_nku_ready);
-        if (!(ok = warp_wait(bar_nku_ready, 0u, abort, SITE_EPI | 0x50))) break;
-      }
       const float g0 = VARIANT == kTau ? logf(0.6931472f + seps) : 0.f;
       if (VARIANT == kYat) {
         // |q|^2 of this thread's row, in fp32 from the bf16 Q tile in shared
@@ -888,23 +883,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // the bounds under which the map's fast path is exact up to rounding
           // (a maximum of another generation of norms bounds nothing: the
           // exact path then)
-          float nkm;
-          if constexpr (INORM) {
-            nkm = __uint_as_float(*nku_max);  // this unit's keys
-          } else {
+          if constexpr (!INORM) {  // (the one-launch path bounds each key tile itself)
             const unsigned long long nkw = *p.nk_max;
-            nkm = p.nk_gen == 0u || (unsigned)(nkw >> 32) == p.nk_gen ? __uint_as_float((unsigned)nkw)
-                                                                     : INFINITY;
+            const float nkm = p.nk_gen == 0u || (unsigned)(nkw >> 32) == p.nk_gen
+                                  ? __uint_as_float((unsigned)nkw)
+                                  : INFINITY;
+            const float span = qe + nkm;
+            fast = yeps >= 0x1p-60f && __all_sync(FULL, span <= 0x1p61f && span * 0x1p-16f <= yeps);
           }
-          const float span = qe + nkm;
-          fast = yeps >= 0x1p-60f && __all_sync(FULL, span <= 0x1p61f && span * 0x1p-16f <= yeps);
           if (STATS && st_q4) st_thr = yat_near_threshold(s2.x + s2.y, yb, YM);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_q_empty);
       }
 
+      // one-launch Yat: this warp's norms of key tile j, taken from the K slot
+      // (ring position 2j of the CTA's only unit) while the S MMAs run; then
+      // the slot may be refilled.  A tile this warp does not map is only
+      // released (every map warp releases every K slot of the unit).
+      auto inorm_tile = [&](int j, bool take) -> bool {
+        if constexpr (INORM) {
+          const uint32_t kpos = 2u * (uint32_t)j, ks = kpos % L::NS;
+          if (!warp_wait(kv_full(ks), (kpos / L::NS) & 1u, abort, SITE_EPI | 0x50)) return false;
+          if (take) {
+            const float mx = inorm_tile_norms<DK>(slot_smem(ks), half, lane, nku + warp * BN);
+            fast = yat_fast_ok(mx, qe, yeps);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(kv_empty(ks));
+        }
+        return true;
+      };
       for (int j = 0; j < nk_tiles; ++j, ph ^= 1u) {
+        if constexpr (INORM) {
+          if (!(ok = inorm_tile(j, true))) break;
+        }
         if (!(ok = warp_wait(s_full(x), ph & 1u, abort, SITE_EPI | 0x10))) break;
         tc_fence_after();
 #ifdef CATTN_TRACE
@@ -1018,7 +1031,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (VARIANT == kYat) {
           const float4 *nk4;
           if constexpr (INORM) {
-            nk4 = reinterpret_cast<const float4 *>(nku + j * BN);
+            nk4 = reinterpret_cast<const float4 *>(nku + warp * BN);
           } else {
             const uint32_t npos = nk_pos + j, ns = npos % NKS;
             if (!(ok = warp_wait(nk_full(ns), (npos / NKS) & 1u, abort, SITE_EPI | 0x20))) break;
@@ -1153,6 +1166,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++tr_step;
 #endif
         mbar_arrive(p_full(x));
+      }
+      if constexpr (INORM) {  // the unit's K slots this warp does not map
+        for (int j = nk_tiles; ok && j < nkv; ++j) ok = inorm_tile(j, false);
       }
 
       if constexpr (STATS) {

@@ -75,6 +75,17 @@ __device__ __forceinline__ float yat_direct(const uint4 *q4, const uint4 *k4, fl
   return num / (fmaxf(d2.x + d2.y, 0.f) + eps);
 }
 
+// Whether yat_pair<true> (one reciprocal per key pair, no clamp) is exact up
+// to rounding for every row of the warp against keys whose squared norms are
+// at most nk_max (qe = |q|^2 + eps of the lane's row): the assembled distance
+// is then off by at most 2^-16 (qe + nk_max) <= eps from the true one, so
+// den >= eps / 2 > 0, and den0 * den1 <= (qe + nk_max)^2 stays finite.
+// Warp-uniform.
+__device__ __forceinline__ bool yat_fast_ok(float nk_max, float qe, float yeps) {
+  const float span = qe + nk_max;
+  return yeps >= 0x1p-60f && __all_sync(0xffffffffu, span <= 0x1p61f && span * 0x1p-16f <= yeps);
+}
+
 // yat_direct as a called function, for call sites that take it key by key
 // (the row statistics pass) and should not each carry a copy of the loop.
 template <int DK, int M>
