@@ -312,8 +312,9 @@ def per_config_table(dev, peak_burst, hbm_gbs, reps=20):
     the device's and not the Python binding's.  The bound is the larger of
     the tensor time (metric FLOP / measured bf16 peak) and the HBM time
     (q, k, v read once, out and telemetry written once / measured copy
-    bandwidth); frac = bound / measured time.  fp32 runs on the CUDA cores,
-    where the tensor bound does not apply: reported against the HBM time."""
+    bandwidth); frac = bound / measured time.  fp32 runs as three tf32 passes
+    on the tensor cores, where the bf16 tensor bound does not apply: reported
+    against the HBM time."""
     import torch
 
     from softmax_free_attention_gb300 import attention, workloads
