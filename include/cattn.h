@@ -154,9 +154,9 @@ int cattn_validate(int variant, const cattn_problem_t *p, const void *q, const v
  * itself from the query tiles it holds, |k|^2 from here because every key
  * tile serves many query tiles.  bf16 problems only.  cattn_forward(CATTN_YAT,
  * ...) runs this itself unless CATTN_FLAG_NORMS_READY is set, except for a
- * problem whose work units all run in one wave (no key split, Tk <= 2048,
- * yat_m 1), where the forward kernel takes each unit's key norms itself and
- * makes no other launch. */
+ * problem whose work units all run in one wave with short rows (no key split,
+ * Tk <= 512 at dk 64 or 256 at dk 128, yat_m 1), where the forward kernel
+ * takes the key norms itself and makes no other launch. */
 int cattn_key_norms(const cattn_problem_t *p, const void *k, void *workspace,
                     size_t workspace_bytes, cattn_stream_t stream);
 

@@ -454,12 +454,15 @@ int forward_impl(int variant, const cattn_problem_t *p, const void *q, const voi
   const int grid = tc_grid_size(w.sched.n_units);
   if (grid < 0) return CATTN_ERR_CUDA;
   const bool ticket = w.sched.n_units > grid;
-  // a Yat problem whose units all run in one wave (no key split, keys <= 2048,
-  // exponent 1, no entropy) is one launch: the fused kernel takes the key
-  // norms of its unit and recomputes its near-key rows itself, and reads no
-  // control word
-  fp.inline_norms = own_norms && !ticket && w.sched.n_splits == 1 && fp.n_kv_tiles <= 16 &&
-                    fp.yat_m == 1 && row_entropy == nullptr;
+  // a Yat problem whose units all run in one wave with short rows (no key
+  // split, key tiles x dk <= 256: up to 512 keys at dk 64, 256 at dk 128;
+  // exponent 1, no entropy) is one launch: the fused kernel takes each key
+  // tile's norms from shared memory and recomputes its near-key rows itself,
+  // and reads no control word.  (The map warps' norm work grows with the
+  // tiles and dk: at 1024 keys and dk 128 the one launch measured 28% slower
+  // than the key-norm kernel and the fused kernel.)
+  fp.inline_norms = own_norms && !ticket && w.sched.n_splits == 1 &&
+                    fp.n_kv_tiles * p->dk <= 256 && fp.yat_m == 1 && row_entropy == nullptr;
   if (fp.inline_norms) {
     // nothing before the kernel
   } else if (own_norms) {

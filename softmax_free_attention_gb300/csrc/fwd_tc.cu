@@ -97,9 +97,6 @@ constexpr int MAP_WARPS = 16;
 constexpr int PRODUCER_WARP = 16;
 constexpr int MMA_WARP = 17;
 constexpr int NKS = 4;  // stages of the key-norm ring
-// the one-launch Yat forward (INORM): key tiles a unit may have (Tk <= 2048;
-// the recompute of a flagged row there takes one warp over the row's keys)
-constexpr int INORM_MAX_TILES = 16;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 // the limit of the test-only wait that nothing completes (FwdParams::test_stall)
 constexpr uint64_t STALL_LIMIT_NS = 20000000ull;
@@ -443,9 +440,10 @@ __device__ __noinline__ void near_row_warp(const FwdParams &p, int bh, int row, 
 }
 
 // INORM: the one-launch Yat forward for problems whose units all run in one
-// wave (one unit per CTA, keys <= 2048, no key splits): the map warps take
-// the unit's key norms themselves at its start, and recompute the rows they
-// flag for the near-key guard at its end, so no other launch is needed.
+// wave with short rows (one unit per CTA, no key splits, key tiles x dk <=
+// 256): the map warps take each key tile's norms from the K tile in shared
+// memory, and recompute the rows they flag for the near-key guard at the
+// unit's end, so no other launch is needed.
 template <int VARIANT, int DK, int DV, int YM = 1, bool STATS = false, bool ENT = false,
           bool INORM = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)

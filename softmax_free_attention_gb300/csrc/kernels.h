@@ -57,9 +57,9 @@ struct FwdParams {
   uint2 *near_rows;
   unsigned int near_cap;
   // Yat (bf16, yat_m 1, no entropy): every unit runs in one wave with no key
-  // split and Tk <= 2048, so the fused kernel takes each unit's key norms and
-  // recomputes its flagged rows itself; nk, nk_max and the near-key list are
-  // not used and no other launch is made
+  // split and at most 256 / dk key tiles, so the fused kernel takes each key
+  // tile's norms and recomputes its flagged rows itself; nk, nk_max and the
+  // near-key list are not used and no other launch is made
   int inline_norms;
   // test only (CATTN_FLAG_TEST_STALL): the tensor-core forward's MMA warp
   // first waits on a barrier that nothing completes, so that the bounded wait
