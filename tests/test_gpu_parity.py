@@ -82,6 +82,10 @@ SHAPES = [
     (1, 2, 2, 200, 2100, 128, 128, False),   # 2 splits of 9 and 8 key tiles
     (1, 1, 1, 130, 4100, 128, 64, False),    # 4 splits, the last one ragged
     (2, 2, 1, 64, 2048, 64, 64, False),      # 2 splits, GQA
+    # causal with few query pairs and long rows: one wave, the heaviest unit
+    # (the last pair) 17 key tiles, the last one ragged; GQA with 8 key tiles
+    (1, 2, 2, 2100, 2100, 128, 128, True),
+    (2, 2, 1, 1024, 1024, 64, 64, True),
 ]
 
 
@@ -544,6 +548,7 @@ ENT_SHAPES = [  # B, h, hkv, T_q, T_k, d, causal
     (2, 4, 2, 300, 300, 128, True),
     (1, 2, 1, 130, 130, 64, True),
     (1, 2, 2, 200, 2100, 128, False),   # two key splits: the entropy sums merge in the combine
+    (1, 2, 2, 1100, 1100, 64, True),    # causal, long ragged rows
 ]
 
 
