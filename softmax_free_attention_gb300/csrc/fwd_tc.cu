@@ -971,11 +971,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tmem_ld32(t_s + 32 * c, sr1);
               tmem_wait_ld();
               tmem_ld_fence(sr1);
+              if (VARIANT == kYat) {
+                // kappa of the chunk's keys in place of their dots, then the
+                // guard against a cancelled distance: the (rare) allowed keys
+                // whose kappa passed the row's bound are recomputed by the
+                // plain definition, outside the accumulation loop below
 #pragma unroll
-              for (int i = 0; i < 32; i += 2) {
-                const int col = cc * 32 + i;
-                const bool al0 = !PARTIAL || col < limit, al1 = !PARTIAL || col + 1 < limit;
-                if (VARIANT == kYat) {
+                for (int i = 0; i < 32; i += 2) {
                   const float4 n4 = nk4[(cc * 32 + i) >> 2];
                   const float2 nk2 = (i & 2) ? make_float2(n4.z, n4.w) : make_float2(n4.x, n4.y);
                   const float2 kk =
@@ -983,14 +985,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                 make_float2(qe, qe), yeps)
                            : yat_pair<false, YM>(f2(sr1[i], sr1[i + 1]), nk2, make_float2(yb, yb),
                                                  make_float2(qe, qe), yeps);
-                  float k0 = kk.x, k1 = kk.y;
-                  // the guard against a cancelled distance, key by key (allowed
-                  // keys only: the others may lie past the end of k)
-                  const uint4 *kt4 = st_k4 + (size_t)j * BN * (DK / 8);
-                  if (al0 && k0 > st_thr)
-                    k0 = yat_direct_call<DK, YM>(st_q4, kt4 + (size_t)col * (DK / 8), yb, yeps);
-                  if (al1 && k1 > st_thr)
-                    k1 = yat_direct_call<DK, YM>(st_q4, kt4 + (size_t)(col + 1) * (DK / 8), yb, yeps);
+                  sr1[i] = __float_as_uint(kk.x);
+                  sr1[i + 1] = __float_as_uint(kk.y);
+                }
+                unsigned flag = 0u;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  flag |= ((!PARTIAL || cc * 32 + i < limit) && __uint_as_float(sr1[i]) > st_thr) ? 1u << i
+                                                                                                 : 0u;
+                // (allowed keys only: the others may lie past the end of k;
+                // one call site, the result put in place by a select chain so
+                // that the chunk stays in registers)
+                const uint4 *kt4 = st_k4 + ((size_t)j * BN + (size_t)cc * 32) * (DK / 8);
+                while (flag != 0u) {
+                  const int i = __ffs(flag) - 1;
+                  flag &= flag - 1u;
+                  const uint32_t v = __float_as_uint(
+                      yat_direct_call<DK, YM>(st_q4, kt4 + (size_t)i * (DK / 8), yb, yeps));
+#pragma unroll
+                  for (int t = 0; t < 32; ++t) sr1[t] = t == i ? v : sr1[t];
+                }
+              }
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const int col = cc * 32 + i;
+                const bool al0 = !PARTIAL || col < limit, al1 = !PARTIAL || col + 1 < limit;
+                if (VARIANT == kYat) {
+                  // (kappa of the chunk, over the raw dots: see below)
+                  float k0 = __uint_as_float(sr1[i]), k1 = __uint_as_float(sr1[i + 1]);
                   if (PARTIAL) {
                     k0 = al0 ? k0 : 0.f;
                     k1 = al1 ? k1 : 0.f;

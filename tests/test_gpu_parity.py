@@ -341,6 +341,36 @@ def test_yat_fast_and_exact_map_paths(eps, qk, where):
     pu.full_parity("yat", inp, causal=True, scale=w.scale, where=where)
 
 
+@pytest.mark.parametrize("b,qk,where", [
+    (1.0, 0.01, "b far above |q|^2 + eps: every row recomputed by the plain definition"),
+    (1.0, 0.06, "b a few times |q|^2: the scores carry b, no row flagged"),
+    (-3.0, 0.3, "negative b"),
+    (40.0, 1.0, "b a third of |q|^2"),
+])
+def test_yat_bias_against_the_norms(b, qk, where):
+    """b from far above |q|^2 + eps to a third of |q|^2, and negative, with a
+    small eps: the numerator (q.k + b)^2 and the assembled distance must
+    match the oracle whichever term dominates."""
+    w = _wl("bias", 1, 2, 2, 300, 300, 128, 128, causal=True, qk=qk, seed=31)
+    inp = workloads.generate(w)
+    inp["yat_b"] = np.full(2, b, dtype=np.float32)
+    inp["yat_eps"] = np.full(2, 1e-3, dtype=np.float32)
+    pu.full_parity("yat", inp, causal=True, scale=w.scale, where=where)
+
+
+def test_yat_zero_query_rows():
+    """Query rows of zeros have kappa = b^2 / (|k|^2 + eps) exactly, eps far
+    below b (both Yat paths: the one-launch form at 256 keys, the key-norm
+    kernel path at 1100)."""
+    for T in (256, 1100):
+        w = _wl("zrows", 1, 2, 2, T, T, 128, 128, causal=True, seed=32)
+        inp = workloads.generate(w)
+        inp["q"][:, :, ::5, :] = 0
+        inp["yat_b"] = np.full(2, 0.75, dtype=np.float32)
+        inp["yat_eps"] = np.full(2, 1e-4, dtype=np.float32)
+        pu.full_parity("yat", inp, causal=True, scale=w.scale, where=f"zero rows T={T}")
+
+
 # ---------------------------------------------------------------- Yat with q close to k
 
 # (name, d, q/k factor, eps): the char-level norms x16 at d = 64 and the
