@@ -128,7 +128,7 @@ struct Layout {
   static constexpr int OFF_RING = OFF_Q + 2 * Q_TILE;
   static constexpr int OFF_NK = OFF_RING + NS * SLOT;
   // row-max exchange of the two column halves: per tile [2 uses][2 tiles][2 halves][BM],
-  // final [2 tiles][2 values][2 halves][BM]
+  // final [2 tiles][2 values][2 halves][BM], the entropy sums [2 tiles][2 halves][BM]
   static constexpr int OFF_XCHG = OFF_NK + NKS * BN * 4;
   // (the row statistics pass uses [13 values][2 tiles][BM] of it)
   static constexpr int XCHG_FLOATS = 26 * BM;
@@ -1277,6 +1277,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row = t.q0 + x * BM + r;
         const bool row_ok = row < p.Tq;
         const float inv = VARIANT == kYat ? 1.f / (total + 1e-9f) : 1.f / total;
+        // Yat: a key may sit close enough to q for the assembled distance to
+        // have cancelled; the near-key pass then recomputes this row (the
+        // one-launch path: this CTA, after its unit).  Taken here, ahead of
+        // the wait and without a division: on the unit boundary the guard
+        // measured about 1% of the kernel as an IEEE division after the wait.
+        const bool near_row =
+            VARIANT == kYat && row_ok && half == 0 && yat_near_flag(all_top, qe - yeps, yb, YM);
         if (!(ok = warp_wait(o_full(x), (ph >> 1) & 1u, abort, SITE_EPI | 0x30))) break;
         tc_fence_after();
         if (p.n_splits == 1) {
@@ -1328,10 +1335,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
               p.row_entropy[ti] = n > 1 ? hrow / logf((float)n) : 0.f;
             }
-            if (VARIANT == kYat && all_top > yat_near_threshold(qe - yeps, yb, YM)) {
-              // a key may sit close enough to q for the assembled distance to
-              // have cancelled: the near-key pass recomputes this row (the
-              // one-launch path: this CTA, after its unit)
+            if (near_row) {
               if constexpr (INORM) {
                 near_list[atomicAdd(near_n, 1u)] = (unsigned)(x * BM + r);
               } else {
@@ -1361,7 +1365,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           if (row_ok && half == 0) {
             reinterpret_cast<float4 *>(p.part_stat)[ti] = make_float4(total, m_used, all_top, all_ent);
-            if (VARIANT == kYat && all_top > yat_near_threshold(qe - yeps, yb, YM)) {
+            if (near_row) {
               const unsigned slot = atomicAdd(p.near_count, 1u);
               if (slot < p.near_cap) p.near_rows[slot] = make_uint2((unsigned)t.bh, (unsigned)row);
             }

@@ -111,6 +111,16 @@ __device__ __forceinline__ float yat_near_threshold(float nq, float b, int M) {
   return a > 0.f ? num / (0.2f * nq) : 0.f;
 }
 
+// top > yat_near_threshold(nq, b, M) without the division (the forward's
+// finalise takes it once per row on the way to releasing O).
+__device__ __forceinline__ bool yat_near_flag(float top, float nq, float b, int M) {
+  const float a = fmaf(0.46875f, nq, b);
+  float num = a * a;
+  if (M == 2) num = num * num;
+  if (M == 3) num = num * num * num;
+  return a > 0.f ? top * (0.2f * nq) > num : top > 0.f;
+}
+
 // Masks, accumulates and packs one pair: masked keys (col >= limit) get
 // kappa = 0; mass (two chains) and top take kappa; returns P = bf16(kappa).
 // ENT: ent also takes kappa log2 kappa (0 for kappa = 0), the row's
