@@ -135,7 +135,9 @@ __device__ __forceinline__ uint32_t yat_fold(float2 k, int col, int limit, float
   mass = __fadd2_rn(mass, k);
   top = max3(top, k.x, k.y);
   if (ENT) {
-    const float2 lk = make_float2(k.x > 0.f ? lg2_approx(k.x) : 0.f, k.y > 0.f ? lg2_approx(k.y) : 0.f);
+    // (the clamp keeps the flush-to-zero log finite, so that kappa = 0 adds
+    // 0 without a select)
+    const float2 lk = make_float2(lg2_approx(fmaxf(k.x, 1e-30f)), lg2_approx(fmaxf(k.y, 1e-30f)));
     ent = __ffma2_rn(k, lk, ent);
   }
   return pack_bf16x2(k.x, k.y);
