@@ -666,7 +666,8 @@ namespace {
 // Backward workspace, each part 256-byte aligned:
 //   dpar   [h][2] fp64 per-head parameter gradient sums (zeroed by each call),
 //          then (Yat) the largest key norm as a 64-bit generation-tagged word
-//   aux    [B*h, Tq_pad] float4: D, normaliser, |q|^2 per query row
+//   aux    three planes [B*h, Tq_pad] of floats: D, normaliser, |q|^2 per
+//          query row (room for four)
 //   nk     Yat only: squared k row norms [B*hkv, Tk_pad]
 struct BwdWs {
   size_t dpar, nkmax, aux, nk, total;
@@ -786,8 +787,9 @@ int cattn_backward(int variant, const cattn_problem_t *p, const void *q, const v
   }
   BwdParams bp;
   memset(&bp, 0, sizeof(bp));
-  bp.aux = reinterpret_cast<const float4 *>(ws + w.aux);
+  bp.aux = reinterpret_cast<const float *>(ws + w.aux);
   bp.aux_w = reinterpret_cast<float *>(ws + w.aux);
+  bp.aux_plane = (size_t)p->B * p->h * tq_pad(p);
   bp.b = b;
   bp.eps = eps;
   bp.tau = tau;

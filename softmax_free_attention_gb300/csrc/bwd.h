@@ -8,8 +8,13 @@ namespace cattn {
 
 // Everything the backward kernels read besides the tensor maps.
 struct BwdParams {
-  const float4 *aux;           // [B*h, Tq_pad]: D = dout . out, normaliser, |q|^2, 0
-  float *aux_w;                // the same array as floats (the Yat row-sum pass writes D)
+  // per query row, three planes of [B*h, Tq_pad] floats aux_plane apart:
+  // D = dout . out (as -D or -D / Z), the normaliser, |q|^2 + eps (Yat), so
+  // that a pass streaming query rows reads each quantity of two adjacent
+  // rows as one pair
+  const float *aux;
+  float *aux_w;                // the same planes, written (the row-sum pass rewrites D and 1 / Z)
+  size_t aux_plane;
   const float *nk;             // [B*hkv, Tk_pad] squared k row norms (Yat), zero padded
   const float *b, *eps, *tau;  // [h]
   void *dq, *dk, *dv;          // bf16, shaped like q, k, v

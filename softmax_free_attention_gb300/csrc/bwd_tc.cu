@@ -105,7 +105,7 @@ struct Layout {
   static constexpr int RP_TILE = RT * DV * 2;
   static constexpr int X_TILE = CT * DK * 2;
   static constexpr int XP_TILE = CT * DV * 2;
-  static constexpr int AUX = 1024;  // 64 float4 (SIDE_KV) or 64 floats (SIDE_Q)
+  static constexpr int AUX = 1024;  // up to three 64-float planes (SIDE_KV) or 64 floats (SIDE_Q)
   static constexpr int STAGE = X_TILE + XP_TILE + AUX;
   static constexpr int W_TILE = RT * CT * 2;  // one 128-byte swizzle box per row
   // Four stages in the streamed-tile ring: a stage is held from the tile's S
@@ -440,7 +440,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
       for (int c = 0; c < DV / 64; ++c)
         tma_load_3d(rp_smem + c * RT * 128, &tm_rp, c * 64, rt * RT, bh_r, bar_r_full);
-      constexpr uint32_t AUXB = KV ? CT * 16 : (VARIANT == kYat ? CT * 4 : 0);
+      // the streamed rows' aux: (dK/dV pass) -D, 1 / Z and, for Yat, |q|^2 +
+      // eps, one plane after another; (dQ pass, Yat) the key norms
+      constexpr uint32_t AUX_PLANES = KV ? (VARIANT == kYat ? 3u : 2u) : (VARIANT == kYat ? 1u : 0u);
+      constexpr uint32_t AUXB = AUX_PLANES * CT * 4;
       int issued = 0;
       for (int n = 0; n < n_tiles; ++n) {
         const int st = n % NS;
@@ -457,7 +460,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int c = 0; c < DV / 64; ++c)
           tma_load_3d(xp_smem(st) + c * CT * 128, &tm_xp, c * 64, row0, bh_x, x_full(st));
         if constexpr (KV) {
-          bulk_load(aux_smem(st), p.aux + (size_t)bh_x * p.Tq_pad + row0, AUXB, x_full(st));
+#pragma unroll
+          for (uint32_t k = 0; k < AUX_PLANES; ++k)
+            bulk_load(aux_smem(st) + k * CT * 4u, p.aux + k * p.aux_plane + (size_t)bh_x * p.Tq_pad + row0,
+                      CT * 4u, x_full(st));
         } else if constexpr (VARIANT == kYat) {
           bulk_load(aux_smem(st), p.nk + (size_t)bh_x * p.Tk_pad + row0, AUXB, x_full(st));
         }
@@ -536,7 +542,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if constexpr (KV) {
       if (VARIANT == kYat) row_nk = p.nk[(size_t)bh_r * p.Tk_pad + grow];
     } else {
-      row_aux = reinterpret_cast<const float4 *>(p.aux)[(size_t)bh_r * p.Tq_pad + grow];
+      const size_t ri = (size_t)bh_r * p.Tq_pad + grow;
+      row_aux = make_float4(p.aux[ri], p.aux[p.aux_plane + ri], p.aux[2 * p.aux_plane + ri], 0.f);
       const int head = bh_r % p.h;
       if (VARIANT == kYat) hp.b = p.b[head];
       if (VARIANT != kSoftmax) hp.eps = p.eps[head];
@@ -584,13 +591,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           float2 X, Y, Z = make_float2(0.f, 0.f);
           bool al0 = true, al1 = true;
           if constexpr (KV) {
-            const uint4 u0 = lds128(aux_smem(st) + 16u * (CW * hf + i));
-            const uint4 u1 = lds128(aux_smem(st) + 16u * (CW * hf + i + 1));
-            X = make_float2(__uint_as_float(u0.x), __uint_as_float(u1.x));
-            Y = make_float2(__uint_as_float(u0.y), __uint_as_float(u1.y));
-            if (VARIANT == kYat)
-              Z = __fadd2_rn(make_float2(__uint_as_float(u0.z), __uint_as_float(u1.z)),
+            // the two columns' -D, 1 / Z (and |q|^2 + eps) as pairs, one plane each
+            const uint32_t ao = aux_smem(st) + 4u * (CW * hf + i);
+            const uint2 ux = lds64(ao), uy = lds64(ao + CT * 4u);
+            X = make_float2(__uint_as_float(ux.x), __uint_as_float(ux.y));
+            Y = make_float2(__uint_as_float(uy.x), __uint_as_float(uy.y));
+            if (VARIANT == kYat) {
+              const uint2 uz = lds64(ao + 2u * CT * 4u);
+              Z = __fadd2_rn(make_float2(__uint_as_float(uz.x), __uint_as_float(uz.y)),
                              make_float2(row_nk, row_nk));
+            }
             if (!FULL) {
               const int t = col0 + i;
               al0 = t < p.Tq && grow < p.Tk && (!p.causal || grow <= t);
@@ -683,12 +693,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           D_t += xch[x * RT + r];
           W_t += xch[(NQ + x) * RT + r];
         }
-        float *a = p.aux_w + ((size_t)bh_r * p.Tq_pad + grow) * 4;
+        float *a = p.aux_w + (size_t)bh_r * p.Tq_pad + grow;
         if (VARIANT == kYat) {
           const float zf = 1.f / row_aux.y;          // the forward's M + 1e-9
           const float inv = 1.f / fmaf(W_t, zf, 1e-9f);  // 1 / (sum kappa + 1e-9)
           a[0] = -D_t * zf * inv * inv;              // -D / Z, D = sum kappa dW / Z
-          a[1] = inv;
+          a[p.aux_plane] = inv;
         } else {
           a[0] = -D_t;
         }
@@ -781,8 +791,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
                                                        const __nv_bfloat16 *__restrict__ dout,
                                                        const float *__restrict__ row_mass,
                                                        const float *__restrict__ eps,
-                                                       float4 *__restrict__ aux, int BH, int h,
-                                                       int Tq, int Tq_pad, float scale) {
+                                                       float *__restrict__ aux, size_t plane,
+                                                       int BH, int h, int Tq, int Tq_pad,
+                                                       float scale) {
   const long long row = ((long long)blockIdx.x * 256 + threadIdx.x) >> 3;
   const int sub = threadIdx.x & 7;
   const bool live = row < (long long)BH * Tq_pad;
@@ -836,7 +847,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16 *__re
       a.y = VARIANT == kYat ? 1.f / (m + 1e-9f) : -m * LOG2E;
       a.z = VARIANT == kYat ? qsum + eps[bh % h] : 0.f;
     }
-    aux[row] = a;
+    aux[row] = a.x;
+    aux[plane + row] = a.y;
+    aux[2 * plane + row] = a.z;
   }
 }
 
@@ -903,7 +916,7 @@ cudaError_t launch_prep(const BwdParams &p, const void *q, const void *out, cons
   const unsigned blocks = (unsigned)((rows * 8 + 255) / 256);
   bwd_prep_kernel<VARIANT, DK, DV><<<blocks, 256, 0, s>>>(
       static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(out),
-      static_cast<const __nv_bfloat16 *>(dout), row_mass, p.eps, const_cast<float4 *>(p.aux),
+      static_cast<const __nv_bfloat16 *>(dout), row_mass, p.eps, p.aux_w, p.aux_plane,
       p.B * p.h, p.h, p.Tq, p.Tq_pad, p.scale);
   return cudaGetLastError();
 }
