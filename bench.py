@@ -146,19 +146,24 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per full-size launch of the fused Yat kernel, from the
-    committed ncu summary, if it was captured on the current kernel sources;
-    otherwise None.  The summary holds `source_hash:`, the per-launch DRAM
-    bytes of the captured (smaller) case and the factor that scales it to the
-    benchmark workload."""
+def recorded_traffic(batch=None):
+    """DRAM bytes per launch of the fused Yat kernel on the benchmark workload
+    (at `batch` if given: every tensor scales with it), from the committed
+    ncu summary, if it was captured on the current kernel sources; otherwise
+    None.  The summary holds `source_hash:`, the per-launch DRAM bytes of the
+    captured (smaller) case and the factor that scales it to the benchmark
+    workload."""
     try:
         with open(TRAFFIC_SUMMARY) as f:
             text = f.read()
         fields = dict(re.findall(r"^- (\w+): `([^`]+)`", text, flags=re.M))
         if fields.get("source_hash") != kernel_source_hash():
             return None
-        return float(fields["dram_bytes_per_launch"]) * float(fields["scale_to_workload"])
+        full = float(fields["dram_bytes_per_launch"]) * float(fields["scale_to_workload"])
+        if batch:
+            from softmax_free_attention_gb300 import workloads
+            full *= batch / workloads.WORKLOADS[WORKLOAD].B
+        return full
     except Exception:
         return None
 
@@ -688,7 +693,7 @@ def main():
 
     achieved = fwd_tflops
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_burst, "unit": "TFLOP/s",
-                "frac": achieved / peak_burst, "traffic": recorded_traffic(),
+                "frac": achieved / peak_burst, "traffic": recorded_traffic(w.B),
                 "peak_kind": f"{peak_kind} bf16 burst (cuBLAS)",
                 "frac_of_datasheet_peak": achieved / DATASHEET_TFLOPS,
                 "datasheet_peak": DATASHEET_TFLOPS,
