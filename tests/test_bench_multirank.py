@@ -73,3 +73,20 @@ def test_sdpa_context_never_raises():
                             causal=True, qk_factor=1.0, yat_param="ln2", seed=0)
     assert bench.sdpa_context(q, q[:, :1], q[:, :1], wg, wg.flops(), 2) == {
         "unavailable": "grouped kv heads"}
+
+
+def test_recorded_traffic_follows_the_sources_and_the_batch():
+    """The roofline's DRAM traffic comes from the committed ncu summary only
+    while its source hash matches the kernel sources, and scales with the
+    batch (every tensor of the workload does)."""
+    full = bench.recorded_traffic()
+    if full is None:
+        pytest.skip("the committed summary was captured on other kernel sources")
+    from softmax_free_attention_gb300 import workloads
+    B = workloads.WORKLOADS[bench.WORKLOAD].B
+    assert bench.recorded_traffic(B) == full
+    assert abs(bench.recorded_traffic(B // 4) - full / 4) <= 1e-6 * full
+    # algorithmic bytes of the full launch: q, k, v read and out written once
+    w = workloads.WORKLOADS[bench.WORKLOAD]
+    algo = 2 * (w.B * w.h * w.Tq * (w.dk + w.dv) + w.B * w.hkv * w.Tk * (w.dk + w.dv))
+    assert 0.8 * algo < full < 1.2 * algo
