@@ -274,10 +274,13 @@ __device__ __forceinline__ void pair2(float2 s, float2 dp, float2 X, float2 Y, f
       w.y = al1 ? w.y : 0.f;
     }
     if constexpr (!WONLY) {
-      const float r0 = rcp_approx(1.f + e0), r1 = rcp_approx(1.f + e1);
-      const float2 sig = make_float2(sc.x >= 0.f ? r0 : e0 * r0, sc.y >= 0.f ? r1 : e1 * r1);
-      const float2 trphi =
-          __fmul2_rn(make_float2(hp.tau, hp.tau), make_float2(rcp_approx(phi.x), rcp_approx(phi.y)));
+      // 1 / (1 + e) and 1 / phi from one reciprocal of their product
+      const float2 ope = __fadd2_rn(make_float2(e0, e1), make_float2(1.f, 1.f));
+      const float2 pq = __fmul2_rn(ope, phi);
+      const float2 rq = make_float2(rcp_approx(pq.x), rcp_approx(pq.y));
+      const float2 r01 = __fmul2_rn(phi, rq);
+      const float2 sig = make_float2(sc.x >= 0.f ? r01.x : e0 * r01.x, sc.y >= 0.f ? r01.y : e1 * r01.y);
+      const float2 trphi = __fmul2_rn(make_float2(hp.tau, hp.tau), __fmul2_rn(ope, rq));
       const float2 base = __fmul2_rn(w, __fadd2_rn(dp, X));  // w (dW - D)
       const float2 bt = __fmul2_rn(base, trphi);
       c = __fmul2_rn(__fmul2_rn(bt, sig), make_float2(scale, scale));
